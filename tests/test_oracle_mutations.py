@@ -1,0 +1,141 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case plants one mistake in the oracle (on the CPU, through monkeypatch)
+and checks that at least one pin in ``test_oracle_pins`` then fails.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+import oracle.forge_oracle as F
+from tests import test_oracle_pins as P
+
+
+def _patch(monkeypatch, name, fn):
+    monkeypatch.setattr(F, name, fn)
+    monkeypatch.setattr(O, name, fn)
+
+
+def _adamw_variant(kind):
+    def f(G, W, m, v, hyper, t):
+        lr, b1, b2, eps, wd = hyper.as_f64()
+        m1 = b1 * m + (1 - b1) * G
+        v1 = b2 * v + (1 - b2) * G * G
+        bc1, bc2 = 1 - b1 ** t, 1 - b2 ** t
+        if kind == "no_bias_correction":
+            bc1 = bc2 = 1.0
+        if kind == "eps_inside_sqrt":
+            W1 = (1 - lr * wd) * W - lr * (m1 / bc1) / np.sqrt(v1 / bc2 + eps)
+        elif kind == "coupled_decay":
+            m1 = b1 * m + (1 - b1) * (G + wd * W)
+            v1 = b2 * v + (1 - b2) * (G + wd * W) ** 2
+            W1 = W - lr * (m1 / bc1) / (np.sqrt(v1 / bc2) + eps)
+        elif kind == "decay_after_update":
+            W1 = (1 - lr * wd) * (W - lr * (m1 / bc1) / (np.sqrt(v1 / bc2) + eps))
+        elif kind == "wrong_sign":
+            W1 = (1 - lr * wd) * W + lr * (m1 / bc1) / (np.sqrt(v1 / bc2) + eps)
+        elif kind == "swapped_betas":
+            m1 = b2 * m + (1 - b2) * G
+            v1 = b1 * v + (1 - b1) * G * G
+            W1 = (1 - lr * wd) * W - lr * (m1 / bc1) / (np.sqrt(v1 / bc2) + eps)
+        else:
+            W1 = (1 - lr * wd) * W - lr * (m1 / bc1) / (np.sqrt(v1 / bc2) + eps)
+        return W1, m1, v1
+    return f
+
+
+ADAMW_PINS = [
+    lambda: P.test_adamw_matches_torch_optim_adamw_f64(10),
+    P.test_step1_moves_each_weight_by_lr_times_sign,
+    P.test_step1_with_eps_is_close_to_sign_step,
+    P.test_no_tokens_decays_moments,
+]
+
+
+def _fails_one(pins):
+    for pin in pins:
+        try:
+            pin()
+        except AssertionError:
+            return True
+    return False
+
+
+@pytest.mark.parametrize("kind", ["no_bias_correction", "eps_inside_sqrt",
+                                  "coupled_decay", "decay_after_update",
+                                  "wrong_sign", "swapped_betas"])
+def test_adamw_mistakes_are_caught(monkeypatch, kind):
+    _patch(monkeypatch, "adamw_f64", _adamw_variant(kind))
+    assert _fails_one(ADAMW_PINS)
+
+
+def test_unmutated_adamw_variant_passes(monkeypatch):
+    _patch(monkeypatch, "adamw_f64", _adamw_variant("none"))
+    assert not _fails_one(ADAMW_PINS)
+
+
+@pytest.mark.parametrize("kind", ["transposed", "x_first", "dropped_token"])
+def test_wgrad_mistakes_are_caught(monkeypatch, kind):
+    def wg(x_bits, dy_bits, rows=None):
+        X, dY = F.bf16_to_f64(x_bits), F.bf16_to_f64(dy_bits)
+        if rows is not None:
+            dY = dY[:, rows]
+        if kind == "transposed":
+            return (dY.T @ X).T.copy() if X.shape[1] != dY.shape[1] else (dY.T @ X).T
+        if kind == "x_first":
+            return X.T @ dY
+        return dY[1:].T @ X[1:]
+    _patch(monkeypatch, "wgrad", wg)
+    pins = [lambda: P.test_wgrad_exact_rational_bruteforce(7, 3, 5),
+            P.test_wgrad_one_hot_closed_form]
+    assert _fails_one(pins)
+
+
+@pytest.mark.parametrize("kind", ["truncate", "half_away", "via_float32"])
+def test_bf16_rounding_mistakes_are_caught(monkeypatch, kind):
+    good = F.f64_to_bf16
+
+    def bad(x):
+        x = np.asarray(x, dtype=np.float64)
+        if kind == "via_float32":     # double rounding
+            f = x.astype(np.float32)
+            return good(f.astype(np.float64))
+        a = np.abs(x)
+        _, e = np.frexp(a)
+        q = np.where(e - 1 >= -126, e - 8, -133).astype(np.int32)
+        s = np.ldexp(a, -q)
+        r = np.floor(s) if kind == "truncate" else np.floor(s + 0.5)
+        return good(np.copysign(np.ldexp(r, q), x))
+    _patch(monkeypatch, "f64_to_bf16", bad)
+    pins = [P.test_bf16_midpoints_round_to_even, P.test_bf16_overflow_and_subnormals]
+    assert _fails_one(pins)
+
+
+@pytest.mark.parametrize("kind", ["columns", "qmax_128", "no_floor", "block_64"])
+def test_int8_mistakes_are_caught(monkeypatch, kind):
+    def quant(x, floor_one):
+        x = np.asarray(x, dtype=np.float64)
+        rows, cols = x.shape
+        blk = 64 if kind == "block_64" else 128
+        if kind == "columns":
+            a = np.repeat(np.max(np.abs(x), axis=0, keepdims=True), rows, axis=0)
+            a = a.reshape(rows, cols // 128, 128).max(axis=2)
+        else:
+            a = np.max(np.abs(x.reshape(rows, cols // blk, blk)), axis=2)
+            if blk == 64:
+                a = a.reshape(rows, cols // 128, 2).max(axis=2) * 0 + a[:, ::2]
+        qmax = 128.0 if kind == "qmax_128" else 127.0
+        s = a / qmax
+        sb = np.repeat(s, 128, axis=1)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            q = np.where(sb > 0, np.rint(x / np.where(sb > 0, sb, 1)), 0)
+        q = np.clip(q, -127, 127)
+        if floor_one and kind != "no_floor":
+            q = np.where(sb > 0, np.maximum(q, 1), q)
+        return q.astype(np.int8), s.astype(np.float32)
+    _patch(monkeypatch, "quantize_int8_blocks", quant)
+    pins = [P.test_int8_exactly_representable_block_round_trips,
+            P.test_int8_error_within_half_a_step,
+            P.test_int8_blocks_are_128_wide_along_rows,
+            P.test_int8_second_moment_floor]
+    assert _fails_one(pins)

@@ -1,0 +1,172 @@
+/*
+ * libforge: the fused weight-gradient + AdamW step of a linear layer on a
+ * GB300 (sm_103a).  C ABI.
+ *
+ * Source of the operation: "FORGE: Fused On-Register Gradient Elimination for
+ * Memory-Efficient LLM Training" (arXiv 2606.22932).
+ *   - section 2.1, Eq. 3: the weight gradient of Y = X W^T is G = dY^T X;
+ *   - section 2.2, Eq. 4: G is accumulated per weight tile over chunks of the
+ *     token axis, in fp32;
+ *   - section 2.2, Algorithm 1: AdamW is applied to each accumulator tile and
+ *     only W, m and v return to memory; G is never stored;
+ *   - section 1, Eq. 1 and Appendix B "INT8 states": moments stored as fp32,
+ *     bf16 or blockwise-absmax int8.
+ *
+ * Layout.  Every matrix is dense, row-major, with no padding between rows:
+ *   X  [bt,    d_in ]  bf16   activations of the layer's forward pass
+ *   dY [bt,    d_out]  bf16   gradient of the loss with respect to Y
+ *   W  [d_out, d_in ]  bf16   weight, updated in place
+ *   dW [d_out, d_in ]  fp32 or bf16 (forge_wgrad output, forge_adamw input)
+ *   m, v [d_out, d_in] moments in the chosen format, updated in place
+ *   int8 scales [d_out, d_in/128] fp32, one per row and 128-column block.
+ *
+ * Ownership.  The caller owns every buffer (device memory).  The library
+ * allocates no device memory in any call; it keeps a small host-side cache of
+ * TMA descriptors keyed by pointer and shape.
+ *
+ * Errors.  Argument errors are returned synchronously, before anything is
+ * enqueued.  Launch failures return FORGE_ERR_LAUNCH.  Kernels never trap:
+ * every wait inside a kernel is bounded, and when a bound runs out the kernel
+ * records FORGE_ERR_DEVICE_TIMEOUT in a per-library device word and returns;
+ * forge_device_error() reads and clears it (FORGE_ERR_DEVICE_CONFIG is reported
+ * the same way).
+ *
+ * Ordering precondition (documented, not checked).  W is overwritten in
+ * place, so the layer's input gradient dX = dY W must already have been
+ * computed, or enqueued earlier on the same stream, before forge_wgrad_adamw
+ * or forge_adamw runs (section 2.2 and Appendix A, Remark 2).  A weight read
+ * by more than one backward path (tied weights) must not use the fused call.
+ */
+#ifndef FORGE_H_
+#define FORGE_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FORGE_OK = 0,
+  FORGE_ERR_NULL = 1,           /* a required pointer is NULL                         */
+  FORGE_ERR_ALIGN = 2,          /* a pointer is not 16-byte aligned                   */
+  FORGE_ERR_SHAPE = 3,          /* bt < 0, d_in/d_out <= 0 or not a multiple of 8,
+                                   int8 moments with d_in % 128 != 0, or a size over
+                                   the 32-bit index range of the kernels             */
+  FORGE_ERR_FORMAT = 4,         /* unknown moment format or dtype                     */
+  FORGE_ERR_HYPER = 5,          /* step < 1, beta outside [0,1), lr/eps/wd < 0 or NaN */
+  FORGE_ERR_ALIAS = 6,          /* an input overlaps an output                        */
+  FORGE_ERR_ARCH = 7,           /* current device is not sm_103 (no fallback exists)  */
+  FORGE_ERR_LAUNCH = 8,         /* a kernel launch or TMA descriptor encode failed    */
+  FORGE_ERR_DEVICE_TIMEOUT = 9, /* a bounded wait inside a kernel ran out             */
+  FORGE_ERR_CUDA = 10,          /* a CUDA runtime call failed                         */
+  FORGE_ERR_DEVICE_CONFIG = 11  /* a kernel found its shared-memory window unusable
+                                   (not 1 KB aligned) and did no work               */
+} forge_status;
+
+typedef enum {
+  FORGE_MOM_FP32 = 0,       /* k = 8 bytes of state per parameter                   */
+  FORGE_MOM_BF16 = 1,       /* k = 4, round to nearest even                          */
+  FORGE_MOM_INT8_B128 = 2   /* k = 2 (+ scales): per row and 128-column block an
+                               absmax scale s = a/127 and codes round(x/s) in
+                               [-127,127]; the second moment is stored as
+                               r = sqrt(v) with codes in [1,127] when a > 0       */
+} forge_moment_fmt;
+
+typedef enum { FORGE_DT_FP32 = 0, FORGE_DT_BF16 = 1 } forge_dtype;
+
+/* One moment tensor.  data: fp32, bf16 or int8 [d_out, d_in].  scale: fp32
+ * [d_out, d_in/128] for FORGE_MOM_INT8_B128, ignored (may be NULL) otherwise. */
+typedef struct {
+  void* data;
+  float* scale;
+} forge_moment;
+
+/* A cudaStream_t passed as an opaque pointer; NULL is the legacy default stream. */
+typedef void* forge_stream;
+
+/*
+ * forge_wgrad_adamw: one fused step for one linear layer (Algorithm 1).
+ *   G = dY^T X (fp32 accumulation over all bt tokens inside the GPU's tensor
+ *   memory, never written to global memory), then per element
+ *     m' = beta1 m + (1 - beta1) G
+ *     v' = beta2 v + (1 - beta2) G^2
+ *     W' = (1 - lr wd) W - (lr / (1 - beta1^step)) m' / (sqrt(v' / (1 - beta2^step)) + eps)
+ *   and W', m', v' are stored (W' bf16 round-to-nearest-even).  The weight update
+ *   reads the unrounded m', v' of this step.
+ * Arguments: X, dY device pointers (read only); W, m, v device pointers (read
+ *   and written); bt >= 0 tokens (bt = 0 means G = 0); d_in, d_out > 0 and
+ *   multiples of 8; step >= 1 is the 1-based count of this step.
+ *   Pointers 16-byte aligned.  X and dY must not overlap W, m, v or scales.
+ * Asynchronous on `stream`.
+ */
+forge_status forge_wgrad_adamw(const void* X, const void* dY, void* W,
+                               forge_moment m, forge_moment v,
+                               int64_t bt, int64_t d_in, int64_t d_out,
+                               float lr, float beta1, float beta2, float eps,
+                               float weight_decay, int64_t step,
+                               forge_moment_fmt fmt, forge_stream stream);
+
+/*
+ * forge_wgrad: the unfused gradient, dW = dY^T X stored to global memory
+ * (the "store-G control" of the FORGE page's Appendix D).  It runs the same
+ * tensor-core main loop as forge_wgrad_adamw, so with dw_dtype = FORGE_DT_FP32
+ * it produces bit for bit the accumulator the fused call consumes.
+ * dw_dtype FORGE_DT_BF16 rounds dW to bf16 (the standard bf16 pipeline).
+ * dW must not overlap X or dY.  bt = 0 writes zeros.  Asynchronous on `stream`.
+ */
+forge_status forge_wgrad(const void* X, const void* dY, void* dW, forge_dtype dw_dtype,
+                         int64_t bt, int64_t d_in, int64_t d_out, forge_stream stream);
+
+/*
+ * forge_adamw: the unfused optimizer step on a stored gradient dW (fp32 or
+ * bf16), with exactly the per-element arithmetic of forge_wgrad_adamw.
+ * forge_wgrad(FP32) followed by forge_adamw gives the same bits as
+ * forge_wgrad_adamw (Appendix A, "Floating-point characterization").
+ * dW may be NULL, which means a zero gradient.  dW must not overlap W, m, v.
+ */
+forge_status forge_adamw(const void* dW, forge_dtype dw_dtype, void* W,
+                         forge_moment m, forge_moment v,
+                         int64_t d_in, int64_t d_out,
+                         float lr, float beta1, float beta2, float eps,
+                         float weight_decay, int64_t step,
+                         forge_moment_fmt fmt, forge_stream stream);
+
+/* Synchronises `stream`, then returns and clears the device error word of the
+ * current device: FORGE_OK, FORGE_ERR_DEVICE_TIMEOUT if a kernel gave up on a
+ * bounded wait since the last call, or FORGE_ERR_DEVICE_CONFIG.  FORGE_ERR_CUDA
+ * if the sync failed. */
+forge_status forge_device_error(forge_stream stream);
+
+/* A static, human-readable name for a status code. */
+const char* forge_status_string(forge_status status);
+
+/* The tile configuration the fused kernel would use for a shape, written as
+ * text into buf (at most len bytes, always NUL-terminated).  Returns the
+ * number of bytes needed, or -1 for an invalid shape or format. */
+int forge_describe_config(int64_t bt, int64_t d_in, int64_t d_out,
+                          forge_moment_fmt fmt, char* buf, int len);
+
+/* Diagnostics for FORGE_ERR_DEVICE_TIMEOUT: where the first timed-out wait
+ * since the last call happened, as site*100000 + block*100 (site 1 operand
+ * slot free, 2 accumulator free, 3 operands landed, 4 state slot free,
+ * 5 accumulator ready, 6 state landed, 7 output slot free, 8-10 teardown
+ * drains), or 0 if none; -1 if the device cannot be queried.  Reading clears
+ * it.  Call after forge_device_error() has synchronised. */
+int forge_debug_timeout_site(void);
+
+/* Bounded-wait limit for the kernels' internal waits, in nanoseconds
+ * (default 2e9).  Applies to launches made after the call. */
+void forge_set_wait_limit_ns(uint64_t ns);
+
+/* Testing aid for the timeout path: when enabled, the next fused or forge_wgrad
+ * launch skips its first operand-load arrival, so its waits run out, the kernel
+ * records FORGE_ERR_DEVICE_TIMEOUT and returns with its outputs unspecified.
+ * The flag clears itself after that one launch. */
+void forge_debug_drop_first_arrival(int enable);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FORGE_H_ */

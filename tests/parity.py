@@ -1,0 +1,132 @@
+"""Comparison helpers for the GPU-vs-oracle parity tests.
+
+Tolerances (stated bar, with the GEMM's own rounding accounted for):
+
+* tau: the GPU forms each G_pq in fp32 as ceil(BT/16) tensor-core
+  accumulations of 16 exact bf16 products; the oracle forms it in fp64.  Their
+  difference is bounded by ``tau = (ceil(BT/16) + 8) * 2**-21 * S_pq`` with
+  ``S_pq = sum_t |dY_tp X_tq|`` (a few fp32 units of roundoff per
+  accumulation, truncation included).
+* W (bf16): the GPU result must lie within 1 ulp of the range of oracle
+  results over G in [G - tau, G + tau]; among entries whose oracle result does
+  not move within that range, at least 99.99% must be within 1 ulp of the
+  oracle and none more than 2 ulp.
+* fp32 moments: ``|d| <= 1e-5 |ref| + (propagated tau)``.
+* bf16 moments: within 1 ulp of the oracle range over G +- tau.
+* int8 moments: codes within 1 level of the oracle range over G +- tau,
+  scales within 1e-5 relative plus the propagated tau.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+
+import oracle as O
+
+
+def bf16_ordered(bits) -> np.ndarray:
+    """Monotone integer image of bf16 bit patterns (+0 and -0 both map to 0)."""
+    b = np.asarray(bits).astype(np.int64) & 0xFFFF
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def bf16_ulp_diff(a_bits, b_bits) -> np.ndarray:
+    return np.abs(bf16_ordered(a_bits) - bf16_ordered(b_bits))
+
+
+def tau_bound(S: np.ndarray, bt: int) -> np.ndarray:
+    return (math.ceil(bt / 16) + 8) * 2.0 ** -21 * S
+
+
+@dataclass
+class Report:
+    n: int
+    frac_within_1: float
+    max_ulp: int
+    sensitive: int
+    violations: int
+
+    def __str__(self):
+        return (f"n={self.n} within1={100 * self.frac_within_1:.4f}% max={self.max_ulp} "
+                f"sensitive={self.sensitive} violations={self.violations}")
+
+
+def _oracle_range(G, tau, W, m, v, hyper, t):
+    """Oracle fp64 results at G - tau, G, G + tau."""
+    outs = [O.adamw_f64(G + d, W, m, v, hyper, t) for d in (-tau, 0.0 * tau, tau)]
+    return outs   # list of (W', m', v')
+
+
+def check_step(gpu_w_bits, gpu_m, gpu_v, ref_inputs, hyper, t, fmt, bt, label=""):
+    """Compare one GPU step with the oracle.
+
+    ref_inputs: dict with G, S (fp64 [R, Din]), W_bits, m (Moment), v (Moment):
+    the state and gradient the step started from, for the compared rows.
+    gpu_m / gpu_v: Moment objects holding the GPU's stored moments (same rows).
+    Raises AssertionError with a report when a bound is broken."""
+    G, S = ref_inputs["G"], ref_inputs["S"]
+    tau = tau_bound(S, bt)
+    W = O.bf16_to_f64(ref_inputs["W_bits"])
+    m0 = O.decode_moment(ref_inputs["m"], False)
+    v0 = O.decode_moment(ref_inputs["v"], True)
+    lo, mid, hi = _oracle_range(G, tau, W, m0, v0, hyper, t)
+    reports = {}
+
+    # ---- W (bf16)
+    wb = [bf16_ordered(O.f64_to_bf16(x[0])) for x in (lo, mid, hi)]
+    wlo, whi = np.minimum.reduce(wb), np.maximum.reduce(wb)
+    g = bf16_ordered(gpu_w_bits)
+    viol = (g < wlo - 1) | (g > whi + 1)
+    sensitive = whi > wlo
+    d = np.abs(g - wb[1])
+    ns = ~sensitive
+    rep = Report(int(g.size), float(np.mean(d[ns] <= 1)) if ns.any() else 1.0,
+                 int(d[ns].max()) if ns.any() else 0, int(sensitive.sum()), int(viol.sum()))
+    reports["W"] = rep
+    assert rep.violations == 0, f"{label} W: {rep}"
+    assert rep.frac_within_1 >= 0.9999 and rep.max_ulp <= 2, f"{label} W: {rep}"
+
+    # ---- moments
+    if fmt == O.FMT_FP32:
+        for which, idx, beta_term in (("m", 1, None), ("v", 2, None)):
+            ref = mid[idx]
+            got = (gpu_m if which == "m" else gpu_v).data.astype(np.float64)
+            spread = np.maximum(np.abs(lo[idx] - ref), np.abs(hi[idx] - ref))
+            allow = 1e-5 * np.abs(ref) + spread + 1e-38
+            err = np.abs(got - ref)
+            nv = int(np.sum(err > allow))
+            reports[which] = f"max rel {float(np.max(err / np.maximum(np.abs(ref), 1e-30))):.2e} violations={nv}"
+            assert nv == 0, f"{label} {which}: {reports[which]}"
+    elif fmt == O.FMT_BF16:
+        for which, idx in (("m", 1), ("v", 2)):
+            rb = [bf16_ordered(O.f64_to_bf16(x[idx])) for x in (lo, mid, hi)]
+            rlo, rhi = np.minimum.reduce(rb), np.maximum.reduce(rb)
+            got = bf16_ordered((gpu_m if which == "m" else gpu_v).data)
+            nv = int(np.sum((got < rlo - 1) | (got > rhi + 1)))
+            reports[which] = f"max ulp {int(np.max(np.abs(got - rb[1])))} violations={nv}"
+            assert nv == 0, f"{label} {which}: {reports[which]}"
+    else:
+        for which, idx in (("m", 1), ("v", 2)):
+            second = which == "v"
+            encs = [O.encode_moment(O.FMT_INT8, x[idx], second) for x in (lo, mid, hi)]
+            mom = gpu_m if which == "m" else gpu_v
+            # scales: within 1e-5 relative of the oracle's range
+            sc = np.stack([e.scale.astype(np.float64) for e in encs])
+            slo, shi = sc.min(axis=0), sc.max(axis=0)
+            gs = mom.scale.astype(np.float64)
+            s_bad = (gs < slo * (1 - 1e-5)) | (gs > shi * (1 + 1e-5))
+            # codes: within one level of the codes the oracle range gives
+            cs = np.stack([e.data.astype(np.int64) for e in encs])
+            clo, chi = cs.min(axis=0), cs.max(axis=0)
+            gc = mom.data.astype(np.int64)
+            c_bad = (gc < clo - 1) | (gc > chi + 1)
+            if second:
+                blk_nz = np.repeat(gs > 0, O.INT8_BLOCK, axis=1)
+                c_bad |= blk_nz & (gc < 1)
+            reports[which] = (f"scale violations={int(s_bad.sum())} code violations={int(c_bad.sum())}"
+                              f" max code diff={int(np.max(np.abs(gc - cs[1])))}")
+            assert not s_bad.any() and not c_bad.any(), f"{label} {which}: {reports[which]}"
+    return reports

@@ -1,0 +1,210 @@
+// The unfused optimizer step: AdamW on a stored gradient dW (fp32 or bf16, or
+// none for a zero gradient), with the per-element arithmetic of the fused
+// kernel's epilogue (forge_math.cuh).  This is the second kernel of the
+// two-kernel path the FORGE page compares against ("cuBLAS + FORGE optimizer
+// kernel", Appendix E; "store-G control" plus update, Appendix D).
+//
+// An HBM-streaming kernel: grid-stride over 16-byte vectors, loads and stores
+// marked streaming (each byte is touched once).
+#include <cuda_bf16.h>
+
+#include "forge_internal.h"
+
+namespace forge {
+
+// dW formats: 0 fp32, 1 bf16, 2 no gradient (zero).
+template <int DW>
+__device__ __forceinline__ void load_grad8(const void* dW, int64_t i8, float (&g)[8]) {
+  if constexpr (DW == 0) {
+    const float4* p = reinterpret_cast<const float4*>(dW) + 2 * i8;
+    const float4 a = __ldcs(p), b = __ldcs(p + 1);
+    g[0] = a.x; g[1] = a.y; g[2] = a.z; g[3] = a.w;
+    g[4] = b.x; g[5] = b.y; g[6] = b.z; g[7] = b.w;
+  } else if constexpr (DW == 1) {
+    const uint4 a = __ldcs(reinterpret_cast<const uint4*>(dW) + i8);
+    const uint32_t u[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) { g[2 * k] = bf16_lo(u[k]); g[2 * k + 1] = bf16_hi(u[k]); }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) g[k] = 0.0f;
+  }
+}
+
+// fp32 or bf16 moments: one thread per 8 consecutive elements.
+template <int FMT, int DW>
+__global__ void __launch_bounds__(256) adamw_vec8_kernel(const void* __restrict__ dW,
+                                                         uint16_t* __restrict__ W,
+                                                         void* __restrict__ m,
+                                                         void* __restrict__ v, int64_t n8,
+                                                         const AdamWConsts h) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += stride) {
+    float g[8], w[8], mm[8], vv[8];
+    load_grad8<DW>(dW, i, g);
+    uint4* wp = reinterpret_cast<uint4*>(W) + i;
+    const uint4 wq = __ldcs(wp);
+    const uint32_t wu[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) { w[2 * k] = bf16_lo(wu[k]); w[2 * k + 1] = bf16_hi(wu[k]); }
+    if constexpr (FMT == kFmtF32) {
+      float4* mp = reinterpret_cast<float4*>(m) + 2 * i;
+      float4* vp = reinterpret_cast<float4*>(v) + 2 * i;
+      const float4 m0 = __ldcs(mp), m1 = __ldcs(mp + 1), v0 = __ldcs(vp), v1 = __ldcs(vp + 1);
+      mm[0] = m0.x; mm[1] = m0.y; mm[2] = m0.z; mm[3] = m0.w;
+      mm[4] = m1.x; mm[5] = m1.y; mm[6] = m1.z; mm[7] = m1.w;
+      vv[0] = v0.x; vv[1] = v0.y; vv[2] = v0.z; vv[3] = v0.w;
+      vv[4] = v1.x; vv[5] = v1.y; vv[6] = v1.z; vv[7] = v1.w;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float r;
+        adamw_elem(g[k], w[k], mm[k], vv[k], r, h);
+      }
+      __stcs(mp, make_float4(mm[0], mm[1], mm[2], mm[3]));
+      __stcs(mp + 1, make_float4(mm[4], mm[5], mm[6], mm[7]));
+      __stcs(vp, make_float4(vv[0], vv[1], vv[2], vv[3]));
+      __stcs(vp + 1, make_float4(vv[4], vv[5], vv[6], vv[7]));
+    } else {
+      uint4* mp = reinterpret_cast<uint4*>(m) + i;
+      uint4* vp = reinterpret_cast<uint4*>(v) + i;
+      const uint4 mq = __ldcs(mp), vq = __ldcs(vp);
+      const uint32_t mu[4] = {mq.x, mq.y, mq.z, mq.w};
+      const uint32_t vu[4] = {vq.x, vq.y, vq.z, vq.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        mm[2 * k] = bf16_lo(mu[k]); mm[2 * k + 1] = bf16_hi(mu[k]);
+        vv[2 * k] = bf16_lo(vu[k]); vv[2 * k + 1] = bf16_hi(vu[k]);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float r;
+        adamw_elem(g[k], w[k], mm[k], vv[k], r, h);
+      }
+      __stcs(mp, make_uint4(pack_bf16x2(mm[0], mm[1]), pack_bf16x2(mm[2], mm[3]),
+                            pack_bf16x2(mm[4], mm[5]), pack_bf16x2(mm[6], mm[7])));
+      __stcs(vp, make_uint4(pack_bf16x2(vv[0], vv[1]), pack_bf16x2(vv[2], vv[3]),
+                            pack_bf16x2(vv[4], vv[5]), pack_bf16x2(vv[6], vv[7])));
+    }
+    __stcs(wp, make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]),
+                          pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7])));
+  }
+}
+
+// int8 moments: one warp per 128-column block of one row; lane l owns
+// columns 4l..4l+3.  The block absmax is a warp max.
+template <int DW>
+__global__ void __launch_bounds__(256) adamw_int8_kernel(const void* __restrict__ dW,
+                                                         uint16_t* __restrict__ W,
+                                                         int8_t* __restrict__ mq,
+                                                         int8_t* __restrict__ vq,
+                                                         float* __restrict__ m_scale,
+                                                         float* __restrict__ v_scale,
+                                                         int64_t nblocks, const AdamWConsts h) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t b = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       b < nblocks; b += warps) {
+    const int64_t e0 = b * 128 + 4 * lane;   // first element of this lane
+    float g[4], w[4], mm[4], vv[4], rr[4];
+    if constexpr (DW == 0) {
+      const float4 a = __ldcs(reinterpret_cast<const float4*>(dW) + e0 / 4);
+      g[0] = a.x; g[1] = a.y; g[2] = a.z; g[3] = a.w;
+    } else if constexpr (DW == 1) {
+      const uint2 a = __ldcs(reinterpret_cast<const uint2*>(dW) + e0 / 4);
+      g[0] = bf16_lo(a.x); g[1] = bf16_hi(a.x); g[2] = bf16_lo(a.y); g[3] = bf16_hi(a.y);
+    } else {
+      g[0] = g[1] = g[2] = g[3] = 0.0f;
+    }
+    uint2* wp = reinterpret_cast<uint2*>(W) + e0 / 4;
+    const uint2 wv = __ldcs(wp);
+    w[0] = bf16_lo(wv.x); w[1] = bf16_hi(wv.x); w[2] = bf16_lo(wv.y); w[3] = bf16_hi(wv.y);
+    uint32_t* mp = reinterpret_cast<uint32_t*>(mq) + e0 / 4;
+    uint32_t* vp = reinterpret_cast<uint32_t*>(vq) + e0 / 4;
+    const uint32_t mc = __ldcs(mp), vc = __ldcs(vp);
+    const float sm = m_scale[b], sv = v_scale[b];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      mm[k] = dequant_m(static_cast<int8_t>((mc >> (8 * k)) & 0xFFu), sm);
+      vv[k] = dequant_v(static_cast<int8_t>((vc >> (8 * k)) & 0xFFu), sv);
+    }
+    float amax_m = 0.0f, amax_r = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      adamw_elem(g[k], w[k], mm[k], vv[k], rr[k], h);
+      amax_m = fmaxf(amax_m, fabsf(mm[k]));
+      amax_r = fmaxf(amax_r, rr[k]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      amax_m = fmaxf(amax_m, __shfl_xor_sync(0xffffffffu, amax_m, o));
+      amax_r = fmaxf(amax_r, __shfl_xor_sync(0xffffffffu, amax_r, o));
+    }
+    const float inv_m = int8_inv_step(amax_m), inv_r = int8_inv_step(amax_r);
+    const bool r_nz = amax_r > 0.0f;
+    uint32_t mo = 0, vo = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      mo |= (static_cast<uint32_t>(quant_m_code(mm[k], inv_m)) & 0xFFu) << (8 * k);
+      vo |= (static_cast<uint32_t>(quant_r_code(rr[k], inv_r, r_nz)) & 0xFFu) << (8 * k);
+    }
+    __stcs(mp, mo);
+    __stcs(vp, vo);
+    __stcs(wp, make_uint2(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3])));
+    if (lane == 0) {
+      m_scale[b] = int8_scale(amax_m);
+      v_scale[b] = int8_scale(amax_r);
+    }
+  }
+}
+
+template <int FMT, int DW>
+static cudaError_t launch_vec8(const void* dW, void* W, void* m, void* v, int64_t n, int grid,
+                               const AdamWConsts& h, cudaStream_t stream) {
+  adamw_vec8_kernel<FMT, DW><<<grid, 256, 0, stream>>>(dW, static_cast<uint16_t*>(W), m, v, n / 8,
+                                                      h);
+  return cudaGetLastError();
+}
+
+template <int DW>
+static cudaError_t launch_i8(const void* dW, void* W, void* m, void* v, float* ms, float* vs,
+                             int64_t n, int grid, const AdamWConsts& h, cudaStream_t stream) {
+  adamw_int8_kernel<DW><<<grid, 256, 0, stream>>>(dW, static_cast<uint16_t*>(W),
+                                                 static_cast<int8_t*>(m), static_cast<int8_t*>(v),
+                                                 ms, vs, n / 128, h);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_adamw(const void* dW, int dw_fmt, void* W, void* m, void* v, float* m_scale,
+                         float* v_scale, int64_t d_in, int64_t d_out, int fmt,
+                         const AdamWConsts& h, int num_sms, cudaStream_t stream) {
+  const int64_t n = d_in * d_out;
+  const int dw = dW == nullptr ? 2 : dw_fmt;
+  if (fmt == kFmtI8) {
+    const int64_t nb = n / 128;
+    const int64_t want = (nb + 7) / 8;
+    const int grid = static_cast<int>(want < 8LL * num_sms ? (want > 0 ? want : 1) : 8LL * num_sms);
+    switch (dw) {
+      case 0: return launch_i8<0>(dW, W, m, v, m_scale, v_scale, n, grid, h, stream);
+      case 1: return launch_i8<1>(dW, W, m, v, m_scale, v_scale, n, grid, h, stream);
+      default: return launch_i8<2>(dW, W, m, v, m_scale, v_scale, n, grid, h, stream);
+    }
+  }
+  const int64_t n8 = n / 8;
+  const int64_t want = (n8 + 255) / 256;
+  const int grid = static_cast<int>(want < 8LL * num_sms ? (want > 0 ? want : 1) : 8LL * num_sms);
+  if (fmt == kFmtF32) {
+    switch (dw) {
+      case 0: return launch_vec8<kFmtF32, 0>(dW, W, m, v, n, grid, h, stream);
+      case 1: return launch_vec8<kFmtF32, 1>(dW, W, m, v, n, grid, h, stream);
+      default: return launch_vec8<kFmtF32, 2>(dW, W, m, v, n, grid, h, stream);
+    }
+  }
+  switch (dw) {
+    case 0: return launch_vec8<kFmtBF16, 0>(dW, W, m, v, n, grid, h, stream);
+    case 1: return launch_vec8<kFmtBF16, 1>(dW, W, m, v, n, grid, h, stream);
+    default: return launch_vec8<kFmtBF16, 2>(dW, W, m, v, n, grid, h, stream);
+  }
+}
+
+}  // namespace forge

@@ -1,0 +1,493 @@
+// The C ABI of libforge: argument validation, TMA descriptor encoding (cached),
+// tile configuration, launches and the device error word.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/forge.h"
+#include "forge_internal.h"
+
+namespace forge {
+
+cudaError_t launch_gemm_fused_f32(const GemmConfig&, const GemmMaps&, const GemmParams&,
+                                  cudaStream_t);
+cudaError_t launch_gemm_fused_bf16(const GemmConfig&, const GemmMaps&, const GemmParams&,
+                                   cudaStream_t);
+cudaError_t launch_gemm_fused_i8(const GemmConfig&, const GemmMaps&, const GemmParams&,
+                                 cudaStream_t);
+cudaError_t launch_gemm_store_f32(const GemmConfig&, const GemmMaps&, const GemmParams&,
+                                  cudaStream_t);
+cudaError_t launch_gemm_store_bf16(const GemmConfig&, const GemmMaps&, const GemmParams&,
+                                   cudaStream_t);
+
+cudaError_t launch_gemm(int mode, int fmt, const GemmConfig& cfg, const GemmMaps& maps,
+                        const GemmParams& p, cudaStream_t stream) {
+  if (mode == kModeFused) {
+    switch (fmt) {
+      case kFmtF32: return launch_gemm_fused_f32(cfg, maps, p, stream);
+      case kFmtBF16: return launch_gemm_fused_bf16(cfg, maps, p, stream);
+      case kFmtI8: return launch_gemm_fused_i8(cfg, maps, p, stream);
+    }
+  } else {
+    switch (fmt) {
+      case kFmtF32: return launch_gemm_store_f32(cfg, maps, p, stream);
+      case kFmtBF16: return launch_gemm_store_bf16(cfg, maps, p, stream);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+// One error word per device; a kernel that gives up on a bounded wait writes
+// FORGE_ERR_DEVICE_TIMEOUT here.
+__device__ int g_forge_device_error;
+// Where the first timeout since the last read happened (diagnostics).
+__device__ int g_forge_device_error_site;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int cc_major = 0, cc_minor = 0, num_sms = 0;
+  int* err_word = nullptr;
+  int* site_word = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+uint64_t g_wait_limit_ns = 2000000000ull;
+int g_drop_first_arrival = 0;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Cache of encoded descriptors keyed by everything that goes into them.
+struct MapKey {
+  const void* ptr;
+  int dtype;
+  uint64_t inner, outer, stride;
+  uint32_t box_inner, box_outer;
+  int swizzle;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && dtype == o.dtype && inner == o.inner && outer == o.outer &&
+           stride == o.stride && box_inner == o.box_inner && box_outer == o.box_outer &&
+           swizzle == o.swizzle;
+  }
+};
+constexpr int kCacheSize = 256;
+struct MapEntry {
+  bool used = false;
+  MapKey key;
+  CUtensorMap map;
+};
+MapEntry g_cache[kCacheSize];
+int g_cache_next = 0;
+
+forge_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FORGE_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FORGE_ERR_CUDA;
+    if (d.cc_major != 10 || d.cc_minor != 3) return FORGE_ERR_ARCH;
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_forge_device_error) != cudaSuccess) return FORGE_ERR_CUDA;
+    d.err_word = static_cast<int*>(addr);
+    if (cudaGetSymbolAddress(&addr, g_forge_device_error_site) != cudaSuccess) return FORGE_ERR_CUDA;
+    d.site_word = static_cast<int*>(addr);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return FORGE_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    d.ready = true;
+  }
+  *out = &d;
+  return FORGE_OK;
+}
+
+// Encode (or fetch from the cache) a 2-D row-major tensor map.
+bool get_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dt, uint64_t inner,
+             uint64_t outer, uint64_t stride_bytes, uint32_t box_inner, uint32_t box_outer,
+             CUtensorMapSwizzle sw) {
+  MapKey key{ptr, static_cast<int>(dt), inner, outer, stride_bytes, box_inner, box_outer,
+             static_cast<int>(sw)};
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (int i = 0; i < kCacheSize; ++i) {
+    if (g_cache[i].used && g_cache[i].key == key) {
+      *out = g_cache[i].map;
+      return true;
+    }
+  }
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUtensorMap m;
+  std::memset(&m, 0, sizeof(m));
+  CUresult r = g_encode(&m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  MapEntry& e = g_cache[g_cache_next];
+  g_cache_next = (g_cache_next + 1) % kCacheSize;
+  e.used = true;
+  e.key = key;
+  e.map = m;
+  *out = m;
+  return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+int mom_elem_bytes(forge_moment_fmt f) {
+  return f == FORGE_MOM_FP32 ? 4 : (f == FORGE_MOM_BF16 ? 2 : 1);
+}
+
+forge_status check_shape(int64_t bt, int64_t d_in, int64_t d_out) {
+  const int64_t lim = (1LL << 31) - 1;
+  if (bt < 0 || d_in <= 0 || d_out <= 0) return FORGE_ERR_SHAPE;
+  if (bt > lim || d_in > lim || d_out > lim) return FORGE_ERR_SHAPE;
+  if (d_in % 8 != 0 || d_out % 8 != 0) return FORGE_ERR_SHAPE;
+  return FORGE_OK;
+}
+
+forge_status check_hyper(float lr, float b1, float b2, float eps, float wd, int64_t step) {
+  if (step < 1) return FORGE_ERR_HYPER;
+  if (!(b1 >= 0.0f && b1 < 1.0f) || !(b2 >= 0.0f && b2 < 1.0f)) return FORGE_ERR_HYPER;
+  if (!(lr >= 0.0f) || !(eps >= 0.0f) || !(wd >= 0.0f)) return FORGE_ERR_HYPER;
+  if (!std::isfinite(lr) || !std::isfinite(eps) || !std::isfinite(wd)) return FORGE_ERR_HYPER;
+  return FORGE_OK;
+}
+
+// Validation shared by the fused call and forge_adamw (state side).
+forge_status check_state(void* W, const forge_moment& m, const forge_moment& v, int64_t d_in,
+                         int64_t d_out, forge_moment_fmt fmt) {
+  if (fmt != FORGE_MOM_FP32 && fmt != FORGE_MOM_BF16 && fmt != FORGE_MOM_INT8_B128)
+    return FORGE_ERR_FORMAT;
+  if (!W || !m.data || !v.data) return FORGE_ERR_NULL;
+  if (fmt == FORGE_MOM_INT8_B128) {
+    if (!m.scale || !v.scale) return FORGE_ERR_NULL;
+    if (d_in % 128 != 0) return FORGE_ERR_SHAPE;
+    if (!aligned16(m.scale) || !aligned16(v.scale)) return FORGE_ERR_ALIGN;
+  }
+  if (!aligned16(W) || !aligned16(m.data) || !aligned16(v.data)) return FORGE_ERR_ALIGN;
+  const uint64_t n = static_cast<uint64_t>(d_in) * static_cast<uint64_t>(d_out);
+  const uint64_t nm = n * mom_elem_bytes(fmt);
+  const uint64_t ns = (fmt == FORGE_MOM_INT8_B128) ? n / 128 * 4 : 0;
+  // the three (five) state tensors must be distinct
+  if (overlaps(W, 2 * n, m.data, nm) || overlaps(W, 2 * n, v.data, nm) ||
+      overlaps(m.data, nm, v.data, nm))
+    return FORGE_ERR_ALIAS;
+  if (ns && (overlaps(m.scale, ns, v.scale, ns) || overlaps(m.scale, ns, W, 2 * n) ||
+             overlaps(v.scale, ns, W, 2 * n) || overlaps(m.scale, ns, m.data, nm) ||
+             overlaps(m.scale, ns, v.data, nm) || overlaps(v.scale, ns, m.data, nm) ||
+             overlaps(v.scale, ns, v.data, nm)))
+    return FORGE_ERR_ALIAS;
+  return FORGE_OK;
+}
+
+bool input_overlaps_state(const void* in, uint64_t nin, void* W, const forge_moment& m,
+                          const forge_moment& v, int64_t d_in, int64_t d_out,
+                          forge_moment_fmt fmt) {
+  const uint64_t n = static_cast<uint64_t>(d_in) * static_cast<uint64_t>(d_out);
+  const uint64_t nm = n * mom_elem_bytes(fmt);
+  const uint64_t ns = (fmt == FORGE_MOM_INT8_B128) ? n / 128 * 4 : 0;
+  return overlaps(in, nin, W, 2 * n) || overlaps(in, nin, m.data, nm) ||
+         overlaps(in, nin, v.data, nm) || (ns && overlaps(in, nin, m.scale, ns)) ||
+         (ns && overlaps(in, nin, v.scale, ns));
+}
+
+AdamWConsts make_consts(float lr, float b1, float b2, float eps, float wd, int64_t step) {
+  const double db1 = b1, db2 = b2, dlr = lr, dwd = wd;
+  const double bc1 = 1.0 - std::pow(db1, static_cast<double>(step));
+  const double bc2 = 1.0 - std::pow(db2, static_cast<double>(step));
+  AdamWConsts h;
+  h.beta1 = b1;
+  h.beta2 = b2;
+  h.omb1 = static_cast<float>(1.0 - db1);
+  h.omb2 = static_cast<float>(1.0 - db2);
+  h.eps = eps;
+  h.decay = static_cast<float>(1.0 - dlr * dwd);
+  h.neg_step_size = static_cast<float>(-dlr / bc1);
+  h.inv_sqrt_bc2 = static_cast<float>(1.0 / std::sqrt(bc2));
+  return h;
+}
+
+GemmConfig choose_config(int64_t bt, int64_t d_in, int64_t d_out, int num_sms) {
+  (void)bt;
+  GemmConfig c;
+  c.bn = 128;
+  c.group_m = 8;
+  const int64_t tiles = ((d_out + kBM - 1) / kBM) * ((d_in + c.bn - 1) / c.bn);
+  c.grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+  return c;
+}
+
+GemmParams base_params(int64_t bt, int64_t d_in, int64_t d_out, const GemmConfig& cfg,
+                       const DeviceInfo& d) {
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.bt = static_cast<int32_t>(bt);
+  p.d_in = static_cast<int32_t>(d_in);
+  p.d_out = static_cast<int32_t>(d_out);
+  p.tiles_m = static_cast<int32_t>((d_out + kBM - 1) / kBM);
+  p.tiles_n = static_cast<int32_t>((d_in + cfg.bn - 1) / cfg.bn);
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.num_k = static_cast<int32_t>((bt + kBK - 1) / kBK);
+  p.group_m = cfg.group_m;
+  p.err = d.err_word;
+  p.err_site = d.site_word;
+  p.timeout_ns = g_wait_limit_ns;
+  return p;
+}
+
+// Operand descriptors: dY [bt, d_out] and X [bt, d_in], boxes of 64 columns x
+// kBK tokens with the 128-byte swizzle.
+bool operand_maps(GemmMaps& maps, const void* X, const void* dY, int64_t bt, int64_t d_in,
+                  int64_t d_out) {
+  return get_map(&maps.dy, dY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_out, bt, d_out * 2, 64, kBK,
+                 CU_TENSOR_MAP_SWIZZLE_128B) &&
+         get_map(&maps.x, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_in, bt, d_in * 2, 64, kBK,
+                 CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+int take_drop_flag() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  const int f = g_drop_first_arrival;
+  g_drop_first_arrival = 0;
+  return f;
+}
+
+}  // namespace
+}  // namespace forge
+
+using namespace forge;
+
+extern "C" {
+
+forge_status forge_wgrad_adamw(const void* X, const void* dY, void* W, forge_moment m,
+                               forge_moment v, int64_t bt, int64_t d_in, int64_t d_out, float lr,
+                               float beta1, float beta2, float eps, float weight_decay,
+                               int64_t step, forge_moment_fmt fmt, forge_stream stream) {
+  forge_status s = check_shape(bt, d_in, d_out);
+  if (s != FORGE_OK) return s;
+  if (bt > 0 && (!X || !dY)) return FORGE_ERR_NULL;
+  s = check_state(W, m, v, d_in, d_out, fmt);
+  if (s != FORGE_OK) return s;
+  if (bt > 0 && (!aligned16(X) || !aligned16(dY))) return FORGE_ERR_ALIGN;
+  s = check_hyper(lr, beta1, beta2, eps, weight_decay, step);
+  if (s != FORGE_OK) return s;
+  if (bt > 0 &&
+      (input_overlaps_state(X, 2ull * bt * d_in, W, m, v, d_in, d_out, fmt) ||
+       input_overlaps_state(dY, 2ull * bt * d_out, W, m, v, d_in, d_out, fmt)))
+    return FORGE_ERR_ALIAS;
+  DeviceInfo* d = nullptr;
+  s = device_info(&d);
+  if (s != FORGE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const AdamWConsts h = make_consts(lr, beta1, beta2, eps, weight_decay, step);
+  const int ifmt = static_cast<int>(fmt);
+  if (bt == 0) {   // G = 0: the moments decay and W takes decay and the m-driven update
+    return launch_adamw(nullptr, 0, W, m.data, v.data, m.scale, v.scale, d_in, d_out, ifmt, h,
+                        d->num_sms, st) == cudaSuccess
+               ? FORGE_OK
+               : FORGE_ERR_LAUNCH;
+  }
+  const GemmConfig cfg = choose_config(bt, d_in, d_out, d->num_sms);
+  GemmMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  bool ok = operand_maps(maps, X, dY, bt, d_in, d_out);
+  if (fmt == FORGE_MOM_INT8_B128) {
+    ok = ok &&
+         get_map(&maps.w, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_in, d_out, d_in * 2, 64, kBM,
+                 CU_TENSOR_MAP_SWIZZLE_128B) &&
+         get_map(&maps.m, m.data, CU_TENSOR_MAP_DATA_TYPE_UINT8, d_in, d_out, d_in, 128, kBM,
+                 CU_TENSOR_MAP_SWIZZLE_128B) &&
+         get_map(&maps.v, v.data, CU_TENSOR_MAP_DATA_TYPE_UINT8, d_in, d_out, d_in, 128, kBM,
+                 CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    const bool f32 = fmt == FORGE_MOM_FP32;
+    const CUtensorMapDataType mdt =
+        f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapSwizzle msw = f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const int eb = f32 ? 4 : 2;
+    ok = ok &&
+         get_map(&maps.w, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_in, d_out, d_in * 2, 32, kBM,
+                 CU_TENSOR_MAP_SWIZZLE_64B) &&
+         get_map(&maps.m, m.data, mdt, d_in, d_out, d_in * eb, 32, kBM, msw) &&
+         get_map(&maps.v, v.data, mdt, d_in, d_out, d_in * eb, 32, kBM, msw);
+  }
+  if (!ok) return FORGE_ERR_LAUNCH;
+  GemmParams p = base_params(bt, d_in, d_out, cfg, *d);
+  p.h = h;
+  p.m_scale = m.scale;
+  p.v_scale = v.scale;
+  p.drop_first_arrival = take_drop_flag();
+  return launch_gemm(kModeFused, ifmt, cfg, maps, p, st) == cudaSuccess ? FORGE_OK
+                                                                         : FORGE_ERR_LAUNCH;
+}
+
+forge_status forge_wgrad(const void* X, const void* dY, void* dW, forge_dtype dw_dtype,
+                         int64_t bt, int64_t d_in, int64_t d_out, forge_stream stream) {
+  forge_status s = check_shape(bt, d_in, d_out);
+  if (s != FORGE_OK) return s;
+  if (dw_dtype != FORGE_DT_FP32 && dw_dtype != FORGE_DT_BF16) return FORGE_ERR_FORMAT;
+  if (!dW || (bt > 0 && (!X || !dY))) return FORGE_ERR_NULL;
+  if (!aligned16(dW) || (bt > 0 && (!aligned16(X) || !aligned16(dY)))) return FORGE_ERR_ALIGN;
+  const uint64_t nbytes =
+      static_cast<uint64_t>(d_in) * d_out * (dw_dtype == FORGE_DT_FP32 ? 4 : 2);
+  if (bt > 0 && (overlaps(dW, nbytes, X, 2ull * bt * d_in) ||
+                 overlaps(dW, nbytes, dY, 2ull * bt * d_out)))
+    return FORGE_ERR_ALIAS;
+  DeviceInfo* d = nullptr;
+  s = device_info(&d);
+  if (s != FORGE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (bt == 0) return cudaMemsetAsync(dW, 0, nbytes, st) == cudaSuccess ? FORGE_OK : FORGE_ERR_CUDA;
+  const GemmConfig cfg = choose_config(bt, d_in, d_out, d->num_sms);
+  GemmMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  bool ok = operand_maps(maps, X, dY, bt, d_in, d_out);
+  if (dw_dtype == FORGE_DT_FP32)
+    ok = ok && get_map(&maps.w, dW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d_in, d_out, d_in * 4, 32, kBM,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+  else
+    ok = ok && get_map(&maps.w, dW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_in, d_out, d_in * 2, 32,
+                       kBM, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (!ok) return FORGE_ERR_LAUNCH;
+  GemmParams p = base_params(bt, d_in, d_out, cfg, *d);
+  p.drop_first_arrival = take_drop_flag();
+  const int ifmt = dw_dtype == FORGE_DT_FP32 ? kFmtF32 : kFmtBF16;
+  return launch_gemm(kModeStoreG, ifmt, cfg, maps, p, st) == cudaSuccess ? FORGE_OK
+                                                                          : FORGE_ERR_LAUNCH;
+}
+
+forge_status forge_adamw(const void* dW, forge_dtype dw_dtype, void* W, forge_moment m,
+                         forge_moment v, int64_t d_in, int64_t d_out, float lr, float beta1,
+                         float beta2, float eps, float weight_decay, int64_t step,
+                         forge_moment_fmt fmt, forge_stream stream) {
+  forge_status s = check_shape(0, d_in, d_out);
+  if (s != FORGE_OK) return s;
+  if (dw_dtype != FORGE_DT_FP32 && dw_dtype != FORGE_DT_BF16) return FORGE_ERR_FORMAT;
+  s = check_state(W, m, v, d_in, d_out, fmt);
+  if (s != FORGE_OK) return s;
+  if (dW && !aligned16(dW)) return FORGE_ERR_ALIGN;
+  s = check_hyper(lr, beta1, beta2, eps, weight_decay, step);
+  if (s != FORGE_OK) return s;
+  const uint64_t nbytes =
+      static_cast<uint64_t>(d_in) * d_out * (dw_dtype == FORGE_DT_FP32 ? 4 : 2);
+  if (dW && input_overlaps_state(dW, nbytes, W, m, v, d_in, d_out, fmt)) return FORGE_ERR_ALIAS;
+  DeviceInfo* d = nullptr;
+  s = device_info(&d);
+  if (s != FORGE_OK) return s;
+  const AdamWConsts h = make_consts(lr, beta1, beta2, eps, weight_decay, step);
+  return launch_adamw(dW, dw_dtype == FORGE_DT_FP32 ? 0 : 1, W, m.data, v.data, m.scale, v.scale,
+                      d_in, d_out, static_cast<int>(fmt), h, d->num_sms,
+                      static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FORGE_OK
+             : FORGE_ERR_LAUNCH;
+}
+
+forge_status forge_device_error(forge_stream stream) {
+  DeviceInfo* d = nullptr;
+  forge_status s = device_info(&d);
+  if (s != FORGE_OK) return s;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FORGE_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, d->err_word, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FORGE_ERR_CUDA;
+  if (word != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(d->err_word, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return FORGE_ERR_CUDA;
+    return static_cast<forge_status>(word);
+  }
+  return FORGE_OK;
+}
+
+const char* forge_status_string(forge_status status) {
+  switch (status) {
+    case FORGE_OK: return "FORGE_OK";
+    case FORGE_ERR_NULL: return "FORGE_ERR_NULL: a required pointer is NULL";
+    case FORGE_ERR_ALIGN: return "FORGE_ERR_ALIGN: a pointer is not 16-byte aligned";
+    case FORGE_ERR_SHAPE: return "FORGE_ERR_SHAPE: unsupported shape";
+    case FORGE_ERR_FORMAT: return "FORGE_ERR_FORMAT: unknown moment format or dtype";
+    case FORGE_ERR_HYPER: return "FORGE_ERR_HYPER: hyperparameter out of range";
+    case FORGE_ERR_ALIAS: return "FORGE_ERR_ALIAS: an input overlaps an output";
+    case FORGE_ERR_ARCH: return "FORGE_ERR_ARCH: the current device is not sm_103";
+    case FORGE_ERR_LAUNCH: return "FORGE_ERR_LAUNCH: kernel launch or descriptor encode failed";
+    case FORGE_ERR_DEVICE_TIMEOUT:
+      return "FORGE_ERR_DEVICE_TIMEOUT: a bounded wait inside a kernel ran out";
+    case FORGE_ERR_CUDA: return "FORGE_ERR_CUDA: a CUDA runtime call failed";
+    case FORGE_ERR_DEVICE_CONFIG:
+      return "FORGE_ERR_DEVICE_CONFIG: a kernel found its shared-memory window unusable";
+  }
+  return "FORGE: unknown status";
+}
+
+int forge_describe_config(int64_t bt, int64_t d_in, int64_t d_out, forge_moment_fmt fmt, char* buf,
+                          int len) {
+  if (check_shape(bt, d_in, d_out) != FORGE_OK) return -1;
+  if (fmt != FORGE_MOM_FP32 && fmt != FORGE_MOM_BF16 && fmt != FORGE_MOM_INT8_B128) return -1;
+  int sms = 152;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+      sms = n;
+  }
+  const GemmConfig c = choose_config(bt, d_in, d_out, sms);
+  const int fm = static_cast<int>(fmt);
+  const int sw = slice_cols(kModeFused, fm);
+  const int need = std::snprintf(buf, buf ? len : 0,
+                                 "tile=%dx%d bk=%d slice=%d grid=%d group_m=%d threads=%d", kBM,
+                                 c.bn, kBK, sw, c.grid, c.group_m, kNumThreads);
+  return need + 1;
+}
+
+int forge_debug_timeout_site(void) {
+  DeviceInfo* d = nullptr;
+  if (device_info(&d) != FORGE_OK) return -1;
+  int word = 0;
+  if (cudaMemcpy(&word, d->site_word, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return -1;
+  const int zero = 0;
+  if (cudaMemcpy(d->site_word, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return -1;
+  return word;
+}
+
+void forge_set_wait_limit_ns(uint64_t ns) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_wait_limit_ns = ns;
+}
+
+void forge_debug_drop_first_arrival(int enable) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_drop_first_arrival = enable ? 1 : 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,657 @@
+// The tensor-core weight-gradient kernel, in two modes:
+//   kModeFused : G = dY^T X per 128 x BN weight tile, then AdamW on the tile
+//                straight from the tensor-memory accumulator; only W, m, v
+//                (and int8 scales) are written back.  This is the FORGE step
+//                ("FORGE: Fused On-Register Gradient Elimination", section 2.2,
+//                Eq. 4 and Algorithm 1), with the accumulator in TMEM.
+//   kModeStoreG: the same main loop, storing G (fp32 or bf16): the unfused
+//                gradient ("store-G control", Appendix D).
+//
+// One persistent CTA per SM walks tiles t = blockIdx.x, blockIdx.x + gridDim.x,
+// ...  Warp roles (384 threads):
+//   warp 0      TMA producer: dY and X chunks of kBK tokens into a STAGES ring
+//   warp 1      TMEM owner and MMA issuer: tcgen05.mma 128 x BN x 16, bf16 in,
+//               fp32 accumulate, into one of two TMEM accumulators (the next
+//               tile's main loop overlaps this tile's epilogue)
+//   warp 2      state loader (fused mode): W/m/v slices of the tile, TMA into
+//               an NS-slot ring, issued ahead of the epilogue
+//   warps 4-11  epilogue: TMEM -> registers, AdamW in fp32, results written in
+//               place into the slot, then TMA-stored by one thread
+//
+// Operands: A = dY^T (M = weight rows) and B = X (N = weight columns) are both
+// contiguous along M/N, so both are fed to the MMA MN-major, straight from the
+// TMA boxes [kBK tokens][64 elements] with the 128-byte swizzle.
+//
+// Every wait is bounded (GemmParams::timeout_ns).  When a bound runs out the
+// CTA raises a shared abort flag, records FORGE_ERR_DEVICE_TIMEOUT in the
+// device error word, lets its in-flight copies and MMAs land, frees its
+// tensor memory and returns.  Nothing traps.
+#pragma once
+
+#include "forge_internal.h"
+#include "forge_ptx.cuh"
+
+namespace forge {
+
+constexpr int kSmemLimit = 232448;   // max dynamic shared memory per CTA (227 KB)
+
+template <int MODE, int FMT, int BN>
+struct GemmTraits {
+  static constexpr int SW = slice_cols(MODE, FMT);     // columns per epilogue slice
+  static constexpr int SLICES = BN / SW;
+  static constexpr int HALF = SW / 2;                  // columns per epilogue thread per slice
+  static constexpr int A_BYTES = kBM * kBK * 2;
+  static constexpr int B_BYTES = BN * kBK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int W_ELEM = (MODE == kModeStoreG && FMT == kFmtF32) ? 4 : 2;
+  static constexpr int MOM_ELEM =
+      (MODE == kModeStoreG) ? 0 : (FMT == kFmtF32 ? 4 : (FMT == kFmtBF16 ? 2 : 1));
+  static constexpr int W_BYTES = kBM * SW * W_ELEM;
+  static constexpr int M_BYTES = kBM * SW * MOM_ELEM;
+  static constexpr int SLOT_BYTES = W_BYTES + 2 * M_BYTES;
+  // Pipeline depths: ring stages for operands, slots for state.
+  static constexpr int STAGES =
+      (BN == 128) ? ((MODE == kModeFused && FMT != kFmtBF16) ? 3 : 4)
+                  : ((MODE == kModeFused) ? (FMT == kFmtI8 ? 2 : 3) : 4);
+  static constexpr int XCH_BYTES = (MODE == kModeFused && FMT == kFmtI8) ? 2 * 2 * kBM * 4 : 0;
+  static constexpr int FIXED_BYTES = 8 * (2 * STAGES + 4 + 2 * 4 + 1) + 16 + XCH_BYTES;
+  static constexpr int NS_FIT = (kSmemLimit - FIXED_BYTES - STAGES * STAGE_BYTES) / SLOT_BYTES;
+  static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;
+  static_assert(NS >= 2, "shared memory does not fit two state slots");
+  static constexpr int TMEM_COLS = 2 * BN;
+  // shared-memory carve (offsets from the 1024-aligned base)
+  static constexpr int OFF_SLOTS = STAGES * STAGE_BYTES;
+  static constexpr int OFF_BARS = OFF_SLOTS + NS * SLOT_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * NS + 1;
+  static constexpr int OFF_TMEM = OFF_BARS + 8 * NUM_BARS;
+  static constexpr int OFF_ABORT = OFF_TMEM + 4;
+  static constexpr int OFF_XCH = (OFF_ABORT + 4 + 15) & ~15;
+  static constexpr int SMEM_USED = OFF_XCH + XCH_BYTES;
+  // Ask for 1 KB of slack to align the base; where that would pass the limit
+  // the kernel checks at run time that its window is aligned well enough.
+  static constexpr int SMEM_ALLOC = (SMEM_USED + 1024 < kSmemLimit) ? SMEM_USED + 1024 : kSmemLimit;
+  static_assert(SMEM_USED <= kSmemLimit, "shared memory budget exceeded");
+  static_assert(BN % SW == 0 && BN % 64 == 0, "tile width");
+  static_assert(TMEM_COLS <= 512, "tensor memory has 512 columns");
+};
+
+struct WaitCtx {
+  volatile uint32_t* abort_flag;
+  int* err;
+  int* site;          // where the first timeout happened (diagnostics)
+  uint64_t timeout_ns;
+};
+
+// Wait sites, recorded as site*100000 + blockIdx.x*100 + index on a timeout.
+enum WaitSite : int {
+  kSiteProducerEmpty = 1, kSiteMmaTmemEmpty = 2, kSiteMmaFull = 3, kSiteLoaderEmpty = 4,
+  kSiteEpiTmemFull = 5, kSiteEpiSlotFull = 6, kSiteEpiSlotFree = 7, kSiteDrainOperands = 8,
+  kSiteDrainState = 9, kSiteDrainMma = 10
+};
+
+// Wait until the phase of `bar` with `parity` completes.  Gives up (returns
+// false) when the CTA's abort flag is raised, if `honor_abort`, or when the
+// time limit runs out, in which case it raises the abort flag and records the
+// timeout in the device error word.
+static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                                 int site, bool honor_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (honor_abort && *w.abort_flag) return false;
+    if (globaltimer_ns() - t0 > w.timeout_ns) {
+      *w.abort_flag = 1u;
+      atomicCAS(w.err, 0, kErrDeviceTimeout);
+      atomicCAS(w.site, 0, site * 100000 + static_cast<int>(blockIdx.x) * 100);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& tm, int& tn) {
+  const int per_group = p.group_m * p.tiles_n;
+  const int g = t / per_group;
+  const int first_m = g * p.group_m;
+  const int gsize = min(p.tiles_m - first_m, p.group_m);
+  const int r = t - g * per_group;
+  tm = first_m + r % gsize;
+  tn = r / gsize;
+}
+
+// ---------------------------------------------------------------------------
+// Epilogue slice bodies.  Each epilogue thread owns one tile row (`row`, the
+// TMEM lane) and HALF consecutive columns of the slice.
+// ---------------------------------------------------------------------------
+
+// fp32 or bf16 moments; SW = 32, HALF = 16.
+template <int FMT>
+__device__ __forceinline__ void epi_slice_fused_16(uint32_t taddr, bool zero_grad, uint8_t* slot,
+                                                   uint32_t row, int h, const AdamWConsts& hc) {
+  using T = GemmTraits<kModeFused, FMT, 128>;
+  uint32_t graw[16];
+  tmem_ld_x16(taddr, graw);
+  tmem_ld_wait();
+  float g[16], w[16], m[16], v[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) g[i] = zero_grad ? 0.0f : __uint_as_float(graw[i]);
+
+  uint8_t* wbox = slot;                 // [128][32] bf16: 64-byte rows
+  uint8_t* mbox = slot + T::W_BYTES;
+  uint8_t* vbox = mbox + T::M_BYTES;
+  uint4 wq[2];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) wq[c] = *reinterpret_cast<const uint4*>(wbox + sw64_off(row, 2 * h + c));
+  const uint32_t* wu = reinterpret_cast<const uint32_t*>(wq);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    w[2 * i] = bf16_lo(wu[i]);
+    w[2 * i + 1] = bf16_hi(wu[i]);
+  }
+  if constexpr (FMT == kFmtF32) {        // [128][32] fp32: 128-byte rows
+    float4 mq[4], vq[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      mq[c] = *reinterpret_cast<const float4*>(mbox + sw128_off(row, 4 * h + c));
+      vq[c] = *reinterpret_cast<const float4*>(vbox + sw128_off(row, 4 * h + c));
+    }
+    const float* mf = reinterpret_cast<const float*>(mq);
+    const float* vf = reinterpret_cast<const float*>(vq);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) { m[i] = mf[i]; v[i] = vf[i]; }
+  } else {                               // [128][32] bf16: 64-byte rows
+    uint4 mq[2], vq[2];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      mq[c] = *reinterpret_cast<const uint4*>(mbox + sw64_off(row, 2 * h + c));
+      vq[c] = *reinterpret_cast<const uint4*>(vbox + sw64_off(row, 2 * h + c));
+    }
+    const uint32_t* mu = reinterpret_cast<const uint32_t*>(mq);
+    const uint32_t* vu = reinterpret_cast<const uint32_t*>(vq);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      m[2 * i] = bf16_lo(mu[i]); m[2 * i + 1] = bf16_hi(mu[i]);
+      v[2 * i] = bf16_lo(vu[i]); v[2 * i + 1] = bf16_hi(vu[i]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float r;
+    adamw_elem(g[i], w[i], m[i], v[i], r, hc);
+  }
+  uint32_t wo[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) wo[i] = pack_bf16x2(w[2 * i], w[2 * i + 1]);
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+    *reinterpret_cast<uint4*>(wbox + sw64_off(row, 2 * h + c)) =
+        make_uint4(wo[4 * c], wo[4 * c + 1], wo[4 * c + 2], wo[4 * c + 3]);
+  if constexpr (FMT == kFmtF32) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      *reinterpret_cast<float4*>(mbox + sw128_off(row, 4 * h + c)) =
+          make_float4(m[4 * c], m[4 * c + 1], m[4 * c + 2], m[4 * c + 3]);
+      *reinterpret_cast<float4*>(vbox + sw128_off(row, 4 * h + c)) =
+          make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+    }
+  } else {
+    uint32_t mo[8], vo[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      mo[i] = pack_bf16x2(m[2 * i], m[2 * i + 1]);
+      vo[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    }
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      *reinterpret_cast<uint4*>(mbox + sw64_off(row, 2 * h + c)) =
+          make_uint4(mo[4 * c], mo[4 * c + 1], mo[4 * c + 2], mo[4 * c + 3]);
+      *reinterpret_cast<uint4*>(vbox + sw64_off(row, 2 * h + c)) =
+          make_uint4(vo[4 * c], vo[4 * c + 1], vo[4 * c + 2], vo[4 * c + 3]);
+    }
+  }
+}
+
+// Decode 32 int8 codes (two 16-byte chunks) to floats.
+__device__ __forceinline__ void load_codes32(const uint8_t* box, uint32_t row, int chunk0,
+                                             int (&q)[32]) {
+  const uint4 a = *reinterpret_cast<const uint4*>(box + sw128_off(row, chunk0));
+  const uint4 b = *reinterpret_cast<const uint4*>(box + sw128_off(row, chunk0 + 1));
+  const uint32_t words[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      q[4 * i + k] = static_cast<int>(static_cast<int8_t>((words[i] >> (8 * k)) & 0xFFu));
+  }
+}
+__device__ __forceinline__ void store_codes32(uint8_t* box, uint32_t row, int chunk0,
+                                              const int (&q)[32]) {
+  uint32_t words[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t wv = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) wv |= (static_cast<uint32_t>(q[4 * i + k]) & 0xFFu) << (8 * k);
+    words[i] = wv;
+  }
+  *reinterpret_cast<uint4*>(box + sw128_off(row, chunk0)) =
+      make_uint4(words[0], words[1], words[2], words[3]);
+  *reinterpret_cast<uint4*>(box + sw128_off(row, chunk0 + 1)) =
+      make_uint4(words[4], words[5], words[6], words[7]);
+}
+
+// int8 moments; SW = 128 (one quantisation block), HALF = 64.  Two passes
+// over the thread's 64 columns: the first updates W and finds the block
+// absmax of m' and r' = sqrt(v') (combined with the partner thread holding
+// the other 64 columns of the row), the second recomputes m', r' and writes
+// their codes.  The exchange barrier is executed by every epilogue thread.
+__device__ __forceinline__ void epi_slice_fused_i8(uint32_t taddr, bool zero_grad, bool active,
+                                                   uint8_t* slot, float* xch, uint32_t row,
+                                                   int h, const float* m_scale_row,
+                                                   const float* v_scale_row, float* m_scale_out,
+                                                   float* v_scale_out,
+                                                   const AdamWConsts& hc) {
+  using T = GemmTraits<kModeFused, kFmtI8, 128>;
+  uint8_t* wbox = slot + h * (kBM * 64 * 2);   // box h: [128][64] bf16, 128-byte rows
+  uint8_t* mbox = slot + T::W_BYTES;           // [128][128] int8
+  uint8_t* vbox = mbox + T::M_BYTES;
+  float sm_old = 0.0f, sv_old = 0.0f;
+  if (active) {
+    sm_old = *m_scale_row;
+    sv_old = *v_scale_row;
+  }
+  float amax_m = 0.0f, amax_r = 0.0f;
+#pragma unroll 1
+  for (int c = 0; c < 2; ++c) {
+    uint32_t graw[32];
+    tmem_ld_x32(taddr + 32 * c, graw);
+    tmem_ld_wait();
+    int qm[32], qv[32];
+    load_codes32(mbox, row, 4 * h + 2 * c, qm);
+    load_codes32(vbox, row, 4 * h + 2 * c, qv);
+    uint4 wq[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) wq[k] = *reinterpret_cast<const uint4*>(wbox + sw128_off(row, 4 * c + k));
+    const uint32_t* wu = reinterpret_cast<const uint32_t*>(wq);
+    uint32_t wo[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float w0 = bf16_lo(wu[i]), w1 = bf16_hi(wu[i]);
+      float g0 = zero_grad ? 0.0f : __uint_as_float(graw[2 * i]);
+      float g1 = zero_grad ? 0.0f : __uint_as_float(graw[2 * i + 1]);
+      float m0 = dequant_m(qm[2 * i], sm_old), m1 = dequant_m(qm[2 * i + 1], sm_old);
+      float v0 = dequant_v(qv[2 * i], sv_old), v1 = dequant_v(qv[2 * i + 1], sv_old);
+      float r0, r1;
+      adamw_elem(g0, w0, m0, v0, r0, hc);
+      adamw_elem(g1, w1, m1, v1, r1, hc);
+      amax_m = fmaxf(amax_m, fmaxf(fabsf(m0), fabsf(m1)));
+      amax_r = fmaxf(amax_r, fmaxf(r0, r1));
+      wo[i] = pack_bf16x2(w0, w1);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      *reinterpret_cast<uint4*>(wbox + sw128_off(row, 4 * c + k)) =
+          make_uint4(wo[4 * k], wo[4 * k + 1], wo[4 * k + 2], wo[4 * k + 3]);
+  }
+  // combine the row's two halves
+  xch[(h * 2 + 0) * kBM + row] = amax_m;
+  xch[(h * 2 + 1) * kBM + row] = amax_r;
+  named_bar_sync(2, kEpiThreads);
+  amax_m = fmaxf(amax_m, xch[((1 - h) * 2 + 0) * kBM + row]);
+  amax_r = fmaxf(amax_r, xch[((1 - h) * 2 + 1) * kBM + row]);
+  const float inv_m = int8_inv_step(amax_m), inv_r = int8_inv_step(amax_r);
+  const bool r_nz = amax_r > 0.0f;
+#pragma unroll 1
+  for (int c = 0; c < 2; ++c) {
+    uint32_t graw[32];
+    tmem_ld_x32(taddr + 32 * c, graw);
+    tmem_ld_wait();
+    int qm[32], qv[32];
+    load_codes32(mbox, row, 4 * h + 2 * c, qm);
+    load_codes32(vbox, row, 4 * h + 2 * c, qv);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      float g = zero_grad ? 0.0f : __uint_as_float(graw[i]);
+      float w = 0.0f, m = dequant_m(qm[i], sm_old), v = dequant_v(qv[i], sv_old), r;
+      adamw_elem(g, w, m, v, r, hc);
+      qm[i] = quant_m_code(m, inv_m);
+      qv[i] = quant_r_code(r, inv_r, r_nz);
+    }
+    store_codes32(mbox, row, 4 * h + 2 * c, qm);
+    store_codes32(vbox, row, 4 * h + 2 * c, qv);
+  }
+  if (active && h == 0) {
+    *m_scale_out = int8_scale(amax_m);
+    *v_scale_out = int8_scale(amax_r);
+  }
+}
+
+// Store-G: write the fp32 accumulator as fp32 or bf16.  SW = 32, HALF = 16.
+template <int FMT>
+__device__ __forceinline__ void epi_slice_store(uint32_t taddr, bool zero_grad, uint8_t* slot,
+                                                uint32_t row, int h) {
+  uint32_t graw[16];
+  tmem_ld_x16(taddr, graw);
+  tmem_ld_wait();
+  float g[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) g[i] = zero_grad ? 0.0f : __uint_as_float(graw[i]);
+  if constexpr (FMT == kFmtF32) {        // [128][32] fp32: 128-byte rows
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      *reinterpret_cast<float4*>(slot + sw128_off(row, 4 * h + c)) =
+          make_float4(g[4 * c], g[4 * c + 1], g[4 * c + 2], g[4 * c + 3]);
+  } else {                               // [128][32] bf16: 64-byte rows
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = pack_bf16x2(g[2 * i], g[2 * i + 1]);
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+      *reinterpret_cast<uint4*>(slot + sw64_off(row, 2 * h + c)) =
+          make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+template <int MODE, int FMT, int BN>
+__global__ void __launch_bounds__(kNumThreads, 1)
+    forge_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+  using T = GemmTraits<MODE, FMT, BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  {
+    uint32_t dyn;
+    asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    if (base - raw + T::SMEM_USED > dyn) {   // uniform across the CTA: nothing started yet
+      if (threadIdx.x == 0) atomicCAS(p.err, 0, kErrDeviceConfig);
+      return;
+    }
+  }
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const uint32_t bars = base + T::OFF_BARS;
+  auto bar_full = [&](int s) { return bars + 8u * s; };
+  auto bar_empty = [&](int s) { return bars + 8u * (T::STAGES + s); };
+  auto bar_tfull = [&](int b) { return bars + 8u * (2 * T::STAGES + b); };
+  auto bar_tempty = [&](int b) { return bars + 8u * (2 * T::STAGES + 2 + b); };
+  auto bar_sfull = [&](int j) { return bars + 8u * (2 * T::STAGES + 4 + j); };
+  auto bar_sempty = [&](int j) { return bars + 8u * (2 * T::STAGES + 4 + T::NS + j); };
+  const uint32_t bar_drain = bars + 8u * (2 * T::STAGES + 4 + 2 * T::NS);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + T::OFF_ABORT);
+  const WaitCtx wc{abort_flag, p.err, p.err_site, p.timeout_ns};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < T::STAGES; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_tfull(b), 1);
+      mbar_init(bar_tempty(b), kEpiThreads);
+    }
+    for (int j = 0; j < T::NS; ++j) {
+      mbar_init(bar_sfull(j), 1);
+      mbar_init(bar_sempty(j), 1);
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0u;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&maps.dy);
+    tma_prefetch_desc(&maps.x);
+    tma_prefetch_desc(&maps.w);
+    if (MODE == kModeFused) {
+      tma_prefetch_desc(&maps.m);
+      tma_prefetch_desc(&maps.v);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(base + T::OFF_TMEM, T::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(gbase + T::OFF_TMEM);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_last();
+      uint32_t cnt = 0;
+      int32_t last_armed[T::STAGES];
+#pragma unroll
+      for (int s = 0; s < T::STAGES; ++s) last_armed[s] = -1;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        int tm, tn;
+        tile_coords(t, p, tm, tn);
+        for (int k = 0; k < p.num_k; ++k, ++cnt) {
+          const int s = cnt % T::STAGES;
+          const uint32_t ph = (cnt / T::STAGES) & 1u;
+          if (!wait_bounded(bar_empty(s), ph ^ 1u, wc, kSiteProducerEmpty)) { ok = false; break; }
+          if (p.drop_first_arrival && cnt == 0) continue;   // testing aid
+          const uint32_t dst = base + s * T::STAGE_BYTES;
+          mbar_arrive_expect_tx(bar_full(s), T::STAGE_BYTES);
+          tma_load_2d(dst, &maps.dy, tm * kBM, k * kBK, bar_full(s), pol);
+          tma_load_2d(dst + 64 * kBK * 2, &maps.dy, tm * kBM + 64, k * kBK, bar_full(s), pol);
+#pragma unroll
+          for (int hb = 0; hb < BN / 64; ++hb)
+            tma_load_2d(dst + T::A_BYTES + hb * 64 * kBK * 2, &maps.x, tn * BN + hb * 64, k * kBK,
+                        bar_full(s), pol);
+          last_armed[s] = static_cast<int32_t>(cnt);
+        }
+      }
+      // let every armed load land before the CTA can exit
+      for (int s = 0; s < T::STAGES; ++s)
+        if (last_armed[s] >= 0)
+          wait_bounded(bar_full(s), (static_cast<uint32_t>(last_armed[s]) / T::STAGES) & 1u, wc,
+                       kSiteDrainOperands, false);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc_bf16_mn(kBM, BN);
+      constexpr uint32_t kLBO = kBK * 128;   // next 64-element group along M/N
+      constexpr uint32_t kSBO = 1024;        // next 8-token group
+      uint32_t cnt = 0;
+      bool ok = true;
+      int it = 0;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++it) {
+        const int buf = it & 1;
+        const uint32_t use = (it >> 1) & 1;
+        if (!wait_bounded(bar_tempty(buf), use ^ 1u, wc, kSiteMmaTmemEmpty)) { ok = false; break; }
+        tc_fence_after_sync();
+        const uint32_t d = tmem_base + buf * BN;
+        for (int k = 0; k < p.num_k; ++k, ++cnt) {
+          const int s = cnt % T::STAGES;
+          const uint32_t ph = (cnt / T::STAGES) & 1u;
+          if (!wait_bounded(bar_full(s), ph, wc, kSiteMmaFull)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint32_t a0 = base + s * T::STAGE_BYTES;
+          const uint32_t b0 = a0 + T::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t ad = make_sdesc_mn_sw128(a0 + kk * 2048, kLBO, kSBO);
+            const uint64_t bd = make_sdesc_mn_sw128(b0 + kk * 2048, kLBO, kSBO);
+            umma_bf16(d, ad, bd, idesc, (k | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(bar_empty(s));
+        }
+        if (!ok) break;
+        if (p.num_k > 0)
+          umma_commit(bar_tfull(buf));
+        else
+          mbar_arrive(bar_tfull(buf));
+      }
+      // every MMA issued must complete before the tensor memory is freed
+      umma_commit(bar_drain);
+      wait_bounded(bar_drain, 0u, wc, kSiteDrainMma, false);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ state loader
+    if (MODE == kModeFused && lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      uint32_t cnt = 0;
+      int32_t last_armed[T::NS];
+#pragma unroll
+      for (int j = 0; j < T::NS; ++j) last_armed[j] = -1;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        int tm, tn;
+        tile_coords(t, p, tm, tn);
+        for (int s = 0; s < T::SLICES; ++s, ++cnt) {
+          const int j = cnt % T::NS;
+          const uint32_t ph = (cnt / T::NS) & 1u;
+          if (!wait_bounded(bar_sempty(j), ph ^ 1u, wc, kSiteLoaderEmpty)) { ok = false; break; }
+          const int x0 = tn * BN + s * T::SW;
+          const int y0 = tm * kBM;
+          last_armed[j] = static_cast<int32_t>(cnt);   // latest phase started on slot j
+          if (x0 >= p.d_in) {        // slice entirely past the last column
+            mbar_arrive(bar_sfull(j));
+            continue;
+          }
+          const uint32_t slot = base + T::OFF_SLOTS + j * T::SLOT_BYTES;
+          mbar_arrive_expect_tx(bar_sfull(j), T::SLOT_BYTES);
+          if constexpr (FMT == kFmtI8) {
+            tma_load_2d(slot, &maps.w, x0, y0, bar_sfull(j), pol);
+            tma_load_2d(slot + kBM * 64 * 2, &maps.w, x0 + 64, y0, bar_sfull(j), pol);
+          } else {
+            tma_load_2d(slot, &maps.w, x0, y0, bar_sfull(j), pol);
+          }
+          tma_load_2d(slot + T::W_BYTES, &maps.m, x0, y0, bar_sfull(j), pol);
+          tma_load_2d(slot + T::W_BYTES + T::M_BYTES, &maps.v, x0, y0, bar_sfull(j), pol);
+        }
+      }
+      // let the loads of each slot's latest phase land before the CTA can exit
+      for (int j = 0; j < T::NS; ++j)
+        if (last_armed[j] >= 0)
+          wait_bounded(bar_sfull(j), (static_cast<uint32_t>(last_armed[j]) / T::NS) & 1u, wc,
+                       kSiteDrainState, false);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                  // TMEM lane quadrant this warp may read
+    const int h = (warp - 4) >> 2;           // column half of each slice
+    const uint32_t row = q * 32 + lane;      // tile row = TMEM lane
+    const bool store_thread = (threadIdx.x == 128);
+    const bool zero_grad = (p.num_k == 0);
+    float* xch = reinterpret_cast<float*>(gbase + T::OFF_XCH);
+    const int scale_cols = p.d_in / 128;
+    uint32_t scnt = 0;
+    int it = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+      int tm, tn;
+      tile_coords(t, p, tm, tn);
+      const int buf = it & 1;
+      const uint32_t use = (it >> 1) & 1;
+      bool good = wait_bounded(bar_tfull(buf), use, wc, kSiteEpiTmemFull);
+      tc_fence_after_sync();
+      bool any_bad = false;
+      for (int s = 0; s < T::SLICES; ++s, ++scnt) {
+        const int j = scnt % T::NS;
+        const uint32_t ph = (scnt / T::NS) & 1u;
+        if (MODE == kModeFused)
+          good = good && wait_bounded(bar_sfull(j), ph, wc, kSiteEpiSlotFull);
+        else
+          good = good && wait_bounded(bar_sempty(j), ph ^ 1u, wc, kSiteEpiSlotFree);
+        // tcgen05.ld is warp-collective: the whole warp takes the same branch
+        good = __all_sync(0xffffffffu, good);
+        const int x0 = tn * BN + s * T::SW;
+        const int y0 = tm * kBM;
+        const bool active = x0 < p.d_in;
+        uint8_t* slot = gbase + T::OFF_SLOTS + j * T::SLOT_BYTES;
+        const uint32_t taddr =
+            tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + s * T::SW + h * T::HALF;
+        if constexpr (MODE == kModeFused && FMT == kFmtI8) {
+          const bool row_ok = active && (y0 + static_cast<int>(row)) < p.d_out;
+          const size_t sidx = static_cast<size_t>(y0 + row) * scale_cols + (x0 >> 7);
+          epi_slice_fused_i8(taddr, zero_grad, good && row_ok, slot, xch, row, h,
+                             p.m_scale + (row_ok ? sidx : 0), p.v_scale + (row_ok ? sidx : 0),
+                             p.m_scale + (row_ok ? sidx : 0), p.v_scale + (row_ok ? sidx : 0),
+                             p.h);
+        } else if (good && active) {
+          if constexpr (MODE == kModeFused)
+            epi_slice_fused_16<FMT>(taddr, zero_grad, slot, row, h, p.h);
+          else
+            epi_slice_store<FMT>(taddr, zero_grad, slot, row, h);
+        }
+        if (s == T::SLICES - 1) {
+          tc_fence_before_sync();
+          mbar_arrive(bar_tempty(buf));
+        }
+        fence_proxy_async_smem();
+        any_bad = named_bar_or(1, kEpiThreads, !good);
+        if (any_bad) break;
+        if (store_thread) {
+          if (active) {
+            const uint32_t sl = smem_u32(slot);
+            if constexpr (MODE == kModeFused && FMT == kFmtI8) {
+              tma_store_2d(&maps.w, x0, y0, sl);
+              tma_store_2d(&maps.w, x0 + 64, y0, sl + kBM * 64 * 2);
+            } else {
+              tma_store_2d(&maps.w, x0, y0, sl);
+            }
+            if constexpr (MODE == kModeFused) {
+              tma_store_2d(&maps.m, x0, y0, sl + T::W_BYTES);
+              tma_store_2d(&maps.v, x0, y0, sl + T::W_BYTES + T::M_BYTES);
+            }
+          }
+          bulk_commit_group();
+          bulk_wait_group_read<1>();
+          if (scnt > 0) mbar_arrive(bar_sempty((scnt - 1) % T::NS));
+        }
+      }
+      if (any_bad) break;
+    }
+    if (store_thread) bulk_wait_group<0>();
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, T::TMEM_COLS);
+  }
+}
+
+template <int MODE, int FMT, int BN>
+cudaError_t launch_gemm_t(const GemmConfig& cfg, const GemmMaps& maps, const GemmParams& p,
+                          cudaStream_t stream) {
+  using T = GemmTraits<MODE, FMT, BN>;
+  auto kern = forge_gemm_kernel<MODE, FMT, BN>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       T::SMEM_ALLOC);
+  if (e != cudaSuccess) return e;
+  kern<<<cfg.grid, kNumThreads, T::SMEM_ALLOC, stream>>>(maps, p);
+  return cudaGetLastError();
+}
+
+template <int MODE, int FMT>
+cudaError_t launch_gemm_fmt(const GemmConfig& cfg, const GemmMaps& maps, const GemmParams& p,
+                            cudaStream_t stream) {
+  switch (cfg.bn) {
+    case 128: return launch_gemm_t<MODE, FMT, 128>(cfg, maps, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int MODE, int FMT>
+size_t gemm_smem_bytes_fmt(int bn) {
+  switch (bn) {
+    case 128: return GemmTraits<MODE, FMT, 128>::SMEM_ALLOC;
+    default: return 0;
+  }
+}
+
+}  // namespace forge

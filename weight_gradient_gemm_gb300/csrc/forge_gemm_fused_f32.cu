@@ -1,0 +1,14 @@
+// Instantiates the tensor-core weight-gradient kernel for one mode and format
+// (one translation unit each, so they compile in parallel).
+#include "forge_gemm.cuh"
+
+namespace forge {
+
+cudaError_t launch_gemm_fused_f32(const GemmConfig& cfg, const GemmMaps& maps,
+                                const GemmParams& p, cudaStream_t stream) {
+  return launch_gemm_fmt<kModeFused, kFmtF32>(cfg, maps, p, stream);
+}
+
+size_t gemm_smem_bytes_fused_f32(int bn) { return gemm_smem_bytes_fmt<kModeFused, kFmtF32>(bn); }
+
+}  // namespace forge

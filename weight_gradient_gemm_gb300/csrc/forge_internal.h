@@ -1,0 +1,66 @@
+// Internal declarations shared by the host API and the kernel translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "forge_math.cuh"
+
+namespace forge {
+
+// Device error word values (match forge_status).
+constexpr int kErrDeviceTimeout = 9;
+constexpr int kErrDeviceConfig = 11;
+
+// Tile geometry of the tensor-core kernels.
+constexpr int kBM = 128;     // weight rows per tile (MMA M)
+constexpr int kBK = 64;      // tokens per pipeline stage
+constexpr int kNumThreads = 384;   // 4 role warps + 8 epilogue warps
+constexpr int kEpiThreads = 256;
+
+enum Mode : int { kModeFused = 0, kModeStoreG = 1 };
+// Epilogue formats: fused moment formats 0..2 (fp32, bf16, int8); store-G dW
+// formats 0..1 (fp32, bf16).
+enum Fmt : int { kFmtF32 = 0, kFmtBF16 = 1, kFmtI8 = 2 };
+
+struct GemmParams {
+  int32_t bt, d_in, d_out;
+  int32_t tiles_m, tiles_n, num_tiles, num_k;
+  int32_t group_m;            // tile-order swizzle: rows of tiles per group
+  AdamWConsts h;
+  float* m_scale;             // int8 scales [d_out, d_in/128]
+  float* v_scale;
+  int* err;                   // device error word
+  int* err_site;              // device word: where a wait first timed out
+  uint64_t timeout_ns;
+  int32_t drop_first_arrival;  // testing aid, see forge_debug_drop_first_arrival
+};
+
+struct GemmMaps {
+  CUtensorMap dy, x;      // operands
+  CUtensorMap w, m, v;    // fused: state; store-G: w is dW
+};
+
+// Launch configuration chosen on the host.
+struct GemmConfig {
+  int bn;        // tile width (MMA N)
+  int grid;      // persistent CTAs
+  int group_m;
+};
+
+// Box widths (columns per epilogue slice) by mode/format, used both to
+// encode the TMA descriptors and inside the kernels.
+__host__ __device__ constexpr int slice_cols(int mode, int fmt) {
+  return (mode == kModeFused && fmt == kFmtI8) ? 128 : 32;
+}
+
+// Launchers (one per instantiated kernel family); return a CUDA error.
+cudaError_t launch_gemm(int mode, int fmt, const GemmConfig& cfg, const GemmMaps& maps,
+                        const GemmParams& p, cudaStream_t stream);
+
+cudaError_t launch_adamw(const void* dW, int dw_fmt, void* W, void* m, void* v, float* m_scale,
+                         float* v_scale, int64_t d_in, int64_t d_out, int fmt,
+                         const AdamWConsts& h, int num_sms, cudaStream_t stream);
+
+}  // namespace forge

@@ -1,0 +1,79 @@
+// Per-element optimizer arithmetic shared by the fused kernel's epilogue and
+// the unfused AdamW kernel.  Both call exactly these functions, so for the
+// same fp32 gradient they produce the same bits (the FORGE page, Appendix A,
+// "Floating-point characterization").  Every operation is an explicit
+// round-to-nearest intrinsic, so the compiler cannot contract or reorder it
+// differently in the two call sites.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+
+namespace forge {
+
+// AdamW constants for one step (Algorithm 1), prepared on the host in fp64
+// and rounded once to fp32.
+struct AdamWConsts {
+  float beta1, beta2;
+  float omb1, omb2;        // 1 - beta1, 1 - beta2
+  float eps;
+  float decay;             // 1 - lr * wd
+  float neg_step_size;     // -lr / (1 - beta1^t)
+  float inv_sqrt_bc2;      // 1 / sqrt(1 - beta2^t)
+};
+
+// One AdamW element.  In: g (fp32 gradient), w, m, v.  Out: w', m', v' and
+// r' = sqrt(v').  The weight update reads the unrounded m' and v'.
+//   m' = beta1 m + (1-beta1) g
+//   v' = beta2 v + (1-beta2) g^2
+//   w' = (1 - lr wd) w - (lr/bc1) m' / (sqrt(v') / sqrt(bc2) + eps)
+__device__ __forceinline__ void adamw_elem(float g, float& w, float& m, float& v, float& r,
+                                           const AdamWConsts& c) {
+  const float m1 = __fmaf_rn(c.beta1, m, __fmul_rn(c.omb1, g));
+  const float v1 = __fmaf_rn(c.beta2, v, __fmul_rn(c.omb2, __fmul_rn(g, g)));
+  const float r1 = __fsqrt_rn(v1);
+  const float denom = __fmaf_rn(r1, c.inv_sqrt_bc2, c.eps);
+  const float upd = __fdiv_rn(m1, denom);
+  w = __fmaf_rn(c.neg_step_size, upd, __fmul_rn(w, c.decay));
+  m = m1;
+  v = v1;
+  r = r1;
+}
+
+// bf16 <-> fp32 (round to nearest even on the way down).
+__device__ __forceinline__ float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t packed) {
+  return __uint_as_float(packed & 0xFFFF0000u);
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Blockwise absmax int8 (128 columns of one row per block).
+//   scale s = a / 127; code = round(x / s) computed as round(x * (127 / a)),
+//   ties to even, clamped to [-127, 127].  The second moment is stored as
+//   r = sqrt(v) with codes of at least 1 in a block whose absmax is non-zero.
+__device__ __forceinline__ float int8_scale(float absmax) { return __fdiv_rn(absmax, 127.0f); }
+__device__ __forceinline__ float int8_inv_step(float absmax) {
+  return absmax > 0.0f ? __fdiv_rn(127.0f, absmax) : 0.0f;
+}
+__device__ __forceinline__ int quant_m_code(float x, float inv) {
+  int q = __float2int_rn(__fmul_rn(x, inv));
+  return max(-127, min(127, q));
+}
+__device__ __forceinline__ int quant_r_code(float r, float inv, bool nonzero_block) {
+  int q = __float2int_rn(__fmul_rn(r, inv));
+  q = min(127, q);
+  return nonzero_block ? max(1, q) : 0;
+}
+// Decoded int8 values: m = code * s_m; v = (code * s_r)^2.
+__device__ __forceinline__ float dequant_m(int code, float s) {
+  return __fmul_rn(static_cast<float>(code), s);
+}
+__device__ __forceinline__ float dequant_v(int code, float s) {
+  const float r = __fmul_rn(static_cast<float>(code), s);
+  return __fmul_rn(r, r);
+}
+
+}  // namespace forge

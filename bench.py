@@ -1,0 +1,508 @@
+#!/usr/bin/env python
+"""Benchmark of the fused weight-gradient + AdamW step (libforge) on GB300.
+
+One step = one fused forge_wgrad_adamw call on each of the seven projections
+of a Llama-3.1-8B decoder layer (q, k, v, o, gate, up, down) at a fixed token
+count, inputs resident in HBM.  Prints one JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle arm
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(independent replicas: the path has no cross-rank exchange), the timed region
+is bracketed by barriers, and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from weight_gradient_gemm_gb300.inputs import (LLAMA31_8B_SHAPES, bf16_bits,  # noqa: E402
+                                               make_step_inputs)
+
+METRIC = "fused wgrad+AdamW TFLOP/s and % roofline, Llama-3.1-8B linears, 1 GB300"
+HYPER = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+FMT_NAMES = {0: "fp32", 1: "bf16", 2: "int8_block128"}
+STATE_BYTES = {0: 20.0, 1: 12.0, 2: 8.0 + 16.0 / 128.0}   # W r/w + m, v r/w (+ scales)
+L2_BYTES = 126 * 2 ** 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+WORKLOADS = {
+    # name: (config index of the recipe, BT, moment format, dY std, spike fraction)
+    "llama31_8b_layer_bt512_fp32": (1, 512, 0, 1e-3, 0.0),
+    "llama31_8b_layer_bt512_bf16": (2, 512, 1, 1e-3, 0.01),
+    "llama31_8b_layer_bt2048_bf16": (2, 2048, 1, 1e-3, 0.01),
+    "llama31_8b_layer_bt8192_bf16": (2, 8192, 1, 1e-3, 0.01),
+    "llama31_8b_layer_bt4096_int8": (3, 4096, 2, 1e-3, 0.0),
+}
+DEFAULT_WORKLOAD = "llama31_8b_layer_bt512_fp32"
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest() -> str:
+    """Hash of the kernel sources; a stored ncu traffic figure is used only
+    while it matches."""
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "weight_gradient_gemm_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(workload: str):
+    """ncu DRAM bytes per launch of the fused kernel for this workload, from
+    profiles/, if the profile was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"forge_gemm_fused_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+    if fields.get("source_sha256") != source_digest():
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.perf_counter(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        note = None
+        if not inside:   # timed window shorter than the sampling period
+            mid = 0.5 * (t0 + t1)
+            inside = [min(self.samples, key=lambda s: abs(s[0] - mid))[1]]
+            note = "nearest sample (window shorter than 100 ms)"
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        smax = [num(p[2]) for p in inside if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for p in inside for n, v in zip(names, p[5:9]) if v.lower() == "active"})
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+               "samples": len(inside)}
+        if note:
+            out["note"] = note
+        return out
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+class Layer:
+    """Device buffers of one decoder layer's seven projections."""
+
+    def __init__(self, cfg, bt, fmt, dy_std, spike, dev, with_host=True, only=None):
+        from weight_gradient_gemm_gb300 import forge as F
+        self.items = []
+        for i, (name, d_out, d_in) in enumerate(LLAMA31_8B_SHAPES):
+            if only and name not in only:
+                continue
+            s = make_step_inputs(cfg, i, 0, bt, d_in, d_out, x_std=1.0, dy_std=dy_std,
+                                 with_w=True, spike_frac=spike)
+            x_host = s.x.pin_memory() if with_host else None
+            dy_host = s.dy.pin_memory() if with_host else None
+            m, v, ms, vs = F.alloc_moments(d_out, d_in, fmt, dev)
+            self.items.append(dict(
+                name=name, d_in=d_in, d_out=d_out, x=s.x.to(dev), dy=s.dy.to(dev),
+                w=s.w.to(dev), m=m, v=v, ms=ms, vs=vs, x_host=x_host, dy_host=dy_host))
+        self.bt = bt
+        self.fmt = fmt
+
+    def flops(self):
+        return sum(2.0 * self.bt * it["d_in"] * it["d_out"] for it in self.items)
+
+    def params(self):
+        return sum(it["d_in"] * it["d_out"] for it in self.items)
+
+    def alg_bytes(self):
+        return sum(it["d_in"] * it["d_out"] * STATE_BYTES[self.fmt]
+                   + 2.0 * self.bt * (it["d_in"] + it["d_out"]) for it in self.items)
+
+    def h2d_bytes(self):
+        return sum(2 * self.bt * (it["d_in"] + it["d_out"]) for it in self.items)
+
+
+def fused_step(F, layer, step, events=None, stream=None):
+    for i, it in enumerate(layer.items):
+        if events is not None:
+            events[i][0].record(stream)
+        F.wgrad_adamw(it["x"], it["dy"], it["w"], it["m"], it["v"], step=step,
+                      m_scale=it["ms"], v_scale=it["vs"], **HYPER)
+        if events is not None:
+            events[i][1].record(stream)
+
+
+def run_gpu(args, rank, world, dev):
+    from weight_gradient_gemm_gb300 import forge as F
+    F.lib()
+    cfg, bt, fmt, dy_std, spike = WORKLOADS[args.workload]
+    layer = Layer(cfg, bt, fmt, dy_std, spike, dev,
+                  only=args.only.split(",") if args.only else None)
+    stream = torch.cuda.current_stream()
+    dist = world > 1
+
+    def barrier():
+        if dist:
+            torch.distributed.barrier()
+
+    # moments warmed by 10 prior steps (same seeded inputs), then W warm-up steps
+    step = 0
+    for _ in range(10):
+        step += 1
+        fused_step(F, layer, step)
+    for _ in range(args.warmup):
+        step += 1
+        fused_step(F, layer, step)
+    assert F.device_error() == 0
+
+    # ---- timed region: K steps, kernels timed one by one on the launch stream
+    n = len(layer.items)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    time.sleep(0.25 if sampler else 0.0)
+    barrier()
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    t_start.record(stream)
+    for k in range(args.steps):
+        step += 1
+        fused_step(F, layer, step, ev[k], stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.perf_counter()
+    barrier()
+    status = F.device_error()
+    if status != 0:
+        raise RuntimeError(F.status_string(status))
+    elapsed_ms = t_start.elapsed_time(t_end)
+    kern_ms = sum(a.elapsed_time(b) for row in ev for (a, b) in row)
+    if sampler:
+        sampler.stop()
+    if dist:
+        t = torch.tensor([elapsed_ms, kern_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms, kern_ms = float(t[0]), float(t[1])
+
+    # ---- unfused comparison arm: forge_wgrad (bf16 dW) + forge_adamw
+    unf_steps = max(3, min(args.steps, 50))
+    dw = torch.empty(max(it["d_in"] * it["d_out"] for it in layer.items), dtype=torch.bfloat16,
+                     device=dev)
+    for _ in range(2):
+        step += 1
+        unfused_step(F, layer, step, dw)
+    barrier()
+    torch.cuda.synchronize()
+    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    u0.record(stream)
+    for _ in range(unf_steps):
+        step += 1
+        unfused_step(F, layer, step, dw)
+    u1.record(stream)
+    torch.cuda.synchronize()
+    unf_ms = u0.elapsed_time(u1) / unf_steps
+    assert F.device_error() == 0
+
+    # ---- end to end through the public API with host buffers: every step
+    # copies X and dY from pinned host memory, runs the seven fused calls and
+    # reads back the library's status word (4 bytes) for the step
+    e2e_steps = max(3, min(args.steps, 100))
+    barrier()
+    torch.cuda.synchronize()
+    e0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        step += 1
+        for it in layer.items:
+            it["x"].copy_(it["x_host"], non_blocking=True)
+            it["dy"].copy_(it["dy_host"], non_blocking=True)
+        fused_step(F, layer, step)
+        st = F.device_error()    # synchronises, reads the 4-byte device status
+        if st != 0:
+            raise RuntimeError(F.status_string(st))
+    e1 = time.perf_counter()
+    e2e_ms = (e1 - e0) * 1e3 / e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms, unf_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms, unf_ms = float(t[0]), float(t[1])
+
+    return dict(layer=layer, elapsed_ms=elapsed_ms, kern_ms=kern_ms, unf_ms=unf_ms,
+                e2e_ms=e2e_ms, clocks=sampler.summary(w0, w1) if sampler else None,
+                config=F.describe_config(bt, 4096, 4096, fmt))
+
+
+def unfused_step(F, layer, step, dw):
+    for it in layer.items:
+        g = dw[:it["d_in"] * it["d_out"]].view(it["d_out"], it["d_in"])
+        F.wgrad(it["x"], it["dy"], g)
+        F.adamw(g, it["w"], it["m"], it["v"], step=step, m_scale=it["ms"], v_scale=it["vs"],
+                **HYPER)
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (reported baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(workload: str, rows: int):
+    """Inputs for one oracle step on the first `rows` weight rows of each of
+    the seven projections."""
+    import oracle as O
+    cfg, bt, fmt, dy_std, spike = WORKLOADS[workload]
+    out = []
+    for i, (name, d_out, d_in) in enumerate(LLAMA31_8B_SHAPES):
+        s = make_step_inputs(cfg, i, 0, bt, d_in, d_out, dy_std=dy_std, with_w=True,
+                             spike_frac=spike)
+        r = min(rows, d_out)
+        out.append(dict(x=bf16_bits(s.x), dy=bf16_bits(s.dy)[:, :r].copy(),
+                        w=bf16_bits(s.w)[:r].copy(), m=O.zero_moment(fmt, r, d_in),
+                        v=O.zero_moment(fmt, r, d_in), r=r, d_in=d_in))
+    return out, bt
+
+
+def oracle_step(sample, t):
+    import oracle as O
+    h = O.Hyper(lr=HYPER["lr"], beta1=HYPER["beta1"], beta2=HYPER["beta2"], eps=HYPER["eps"],
+                wd=HYPER["weight_decay"])
+    for s in sample:
+        O.step(s["x"], s["dy"], s["w"], s["m"], s["v"], h, t)
+
+
+def oracle_threads() -> int:
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def time_oracle(workload: str, target_s: float):
+    """Oracle TFLOP/s on a row sample sized for about target_s seconds."""
+    sample, bt = oracle_sample(workload, 8)
+    t0 = time.perf_counter()
+    oracle_step(sample, 1)
+    per_row = (time.perf_counter() - t0) / 8
+    rows = max(1, min(4096, int(target_s / max(per_row, 1e-6))))
+    sample, bt = oracle_sample(workload, rows)
+    t0 = time.perf_counter()
+    oracle_step(sample, 1)
+    dt = time.perf_counter() - t0
+    flops = sum(2.0 * bt * s["r"] * s["d_in"] for s in sample)
+    return flops / dt / 1e12, dt, rows, bt
+
+
+def cpu_baseline_block(workload):
+    value, dt, rows, bt = time_oracle(workload, 12.0)
+    return {"value": value, "unit": "TFLOP/s", "cores": oracle_threads(), "kind": "oracle",
+            "sample": (f"one fp64 oracle step (numpy: BLAS matmul for G, then AdamW and rounding)"
+                       f" on the first {rows} rows of each of the 7 projections at BT={bt}, "
+                       f"{dt:.1f} s")}
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, on a bounded sample
+    of the same workload each step."""
+    cfg, bt, fmt, dy_std, spike = WORKLOADS[args.workload]
+    budget_s = 120.0
+    per_step = budget_s / max(1, args.steps + args.warmup)
+    sample, _ = oracle_sample(args.workload, 4)
+    t0 = time.perf_counter()
+    oracle_step(sample, 1)
+    per_row = (time.perf_counter() - t0) / 4
+    rows = max(1, min(4096, int(per_step / max(per_row, 1e-6))))
+    sample, bt = oracle_sample(args.workload, rows)
+    for t in range(args.warmup):
+        oracle_step(sample, t + 1)
+    t0 = time.perf_counter()
+    for t in range(args.steps):
+        oracle_step(sample, args.warmup + t + 1)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    flops = sum(2.0 * bt * s["r"] * s["d_in"] for s in sample)
+    value = flops / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "bt": bt, "moments": FMT_NAMES[fmt],
+                   "sample_rows_per_projection": rows},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle_threads(),
+                         "kind": "oracle",
+                         "sample": f"first {rows} rows of each of the 7 projections per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="forge", choices=["forge", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default="",
+                    help="comma-separated projections (q,k,v,o,gate,up,down) for small profiling "
+                         "runs; the JSON line then describes that subset")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        return
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        torch.distributed.barrier()
+    res = run_gpu(args, rank, world, dev)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return
+
+    layer = res["layer"]
+    cfg, bt, fmt, dy_std, spike = WORKLOADS[args.workload]
+    peaks, peak_kind = measured_peaks()
+    ms = res["elapsed_ms"] / args.steps
+    flops = layer.flops()
+    value = world * flops / (ms * 1e-3) / 1e12
+    launches = args.steps * len(layer.items)
+    kern_s_per_launch = res["kern_ms"] * 1e-3 / launches
+    alg_bytes_launch = layer.alg_bytes() / len(layer.items)
+    alg_flops_launch = flops / len(layer.items)
+    t_hbm = layer.alg_bytes() / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        achieved = alg_bytes_launch / kern_s_per_launch / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": stored_traffic(args.workload),
+                "peak_kind": f"{peak_kind} (copy bandwidth)"}
+    else:
+        achieved = alg_flops_launch / kern_s_per_launch / 1e12
+        peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": stored_traffic(args.workload),
+                "peak_kind": f"{peak_kind} (cuBLAS bf16, sustained)"}
+    roofline_time = max(t_hbm, t_tc)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "bt": bt, "moments": FMT_NAMES[fmt],
+                   "projections": [it["name"] for it in layer.items],
+                   "params_per_step": layer.params(),
+                   "l2": f"inputs larger than L2: {layer.alg_bytes() / 1e9:.2f} GB streamed per "
+                         f"step vs {L2_BYTES / 2 ** 20:.0f} MiB L2",
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "kernel": res["config"]},
+        "roofline": roof,
+        "roofline_step": {"roofline_ms": roofline_time * 1e3,
+                          "frac_of_roofline": roofline_time * 1e3 / ms,
+                          "params_per_s": layer.params() / (ms * 1e-3) * world,
+                          "hbm_gbs": layer.alg_bytes() / (ms * 1e-3) / 1e9},
+        "unfused": {"ms_per_step": res["unf_ms"],
+                    "value": world * flops / (res["unf_ms"] * 1e-3) / 1e12,
+                    "fused_speedup": res["unf_ms"] / ms,
+                    "path": "forge_wgrad (bf16 dW) + forge_adamw"},
+        "e2e": {"value": world * flops / (res["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": res["e2e_ms"], "h2d_bytes_per_step": layer.h2d_bytes(),
+                "d2h_bytes_per_step": 4},
+        "gpu_launches": launches,
+        "clocks": res["clocks"],
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline_block(args.workload)
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -4,9 +4,10 @@ Tolerances (stated bar, with the GEMM's own rounding accounted for):
 
 * tau: the GPU forms each G_pq in fp32 as ceil(BT/16) tensor-core
   accumulations of 16 exact bf16 products; the oracle forms it in fp64.  Their
-  difference is bounded by ``tau = (ceil(BT/16) + 8) * 2**-21 * S_pq`` with
-  ``S_pq = sum_t |dY_tp X_tq|`` (a few fp32 units of roundoff per
-  accumulation, truncation included).
+  difference is bounded by ``tau = (ceil(BT/16) + 8) * 2**-23 * S_pq`` with
+  ``S_pq = sum_t |dY_tp X_tq|``: at most one fp32 unit of roundoff (2^-23
+  relative, truncation included) per accumulation, plus margin for the
+  summation inside one MMA.
 * W (bf16): the GPU result must lie within 1 ulp of the range of oracle
   results over G in [G - tau, G + tau]; among entries whose oracle result does
   not move within that range, at least 99.99% must be within 1 ulp of the
@@ -38,7 +39,7 @@ def bf16_ulp_diff(a_bits, b_bits) -> np.ndarray:
 
 
 def tau_bound(S: np.ndarray, bt: int) -> np.ndarray:
-    return (math.ceil(bt / 16) + 8) * 2.0 ** -21 * S
+    return (math.ceil(bt / 16) + 8) * 2.0 ** -23 * S
 
 
 @dataclass

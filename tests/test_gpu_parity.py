@@ -27,6 +27,17 @@ def _gpu():
     require_gpu()
 
 
+@pytest.fixture(params=[("stream", "128"), ("mma", "128"), ("stream", "256"), ("mma", "256")],
+                ids=lambda p: f"{p[0]}-bn{p[1]}")
+def profile(request, monkeypatch):
+    """Every pipeline profile and tile width of the tensor-core kernel (the
+    library picks them by token count; FORGE_PROFILE and FORGE_BN force them;
+    int8 moments always use 128-wide tiles)."""
+    monkeypatch.setenv("FORGE_PROFILE", request.param[0])
+    monkeypatch.setenv("FORGE_BN", request.param[1])
+    return request.param
+
+
 def _trajectory(fmt, bt, d_in, d_out, steps, cfg, x_std=1.0, dy_std=0.01, spike=0.0,
                 hyper=TINY, rows=None):
     """Run `steps` steps; at each step the GPU starts from the oracle's state
@@ -63,7 +74,7 @@ def test_tiny_config_three_steps(fmt):
     (O.FMT_BF16, 65, 256, 264),
     (O.FMT_INT8, 1000, 256, 256),
 ])
-def test_ragged_shapes(fmt, bt, d_in, d_out):
+def test_ragged_shapes(fmt, bt, d_in, d_out, profile):
     _trajectory(fmt, bt, d_in, d_out, 2, cfg=7, dy_std=1e-3, spike=0.02)
 
 
@@ -82,7 +93,7 @@ def test_no_tokens_is_decay_without_special_case(fmt):
 
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("shape", [(200, 384, 392), (512, 4096, 1024)])
-def test_fused_equals_unfused_bitwise(fmt, shape):
+def test_fused_equals_unfused_bitwise(fmt, shape, profile):
     bt, d_in, d_out = shape
     if fmt == O.FMT_INT8 and d_in % 128:
         pytest.skip("int8 needs 128 | d_in")
@@ -100,7 +111,7 @@ def test_fused_equals_unfused_bitwise(fmt, shape):
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("shape", [(64, 256, 128), (200, 264, 392), (4096, 512, 256)])
-def test_wgrad_against_oracle(dtype, shape):
+def test_wgrad_against_oracle(dtype, shape, profile):
     bt, d_in, d_out = shape
     s = make_step_inputs(10, 0, 1, bt, d_in, d_out, dy_std=1e-3)
     dW = torch.full((d_out, d_in), float("nan"), dtype=dtype, device=DEV)

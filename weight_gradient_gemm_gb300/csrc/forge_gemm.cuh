@@ -35,7 +35,8 @@ namespace forge {
 
 constexpr int kSmemLimit = 232448;   // max dynamic shared memory per CTA (227 KB)
 
-template <int MODE, int FMT, int BN>
+
+template <int MODE, int FMT, int BN, int PROF>
 struct GemmTraits {
   static constexpr int SW = slice_cols(MODE, FMT);     // columns per epilogue slice
   static constexpr int SLICES = BN / SW;
@@ -49,27 +50,34 @@ struct GemmTraits {
   static constexpr int W_BYTES = kBM * SW * W_ELEM;
   static constexpr int M_BYTES = kBM * SW * MOM_ELEM;
   static constexpr int SLOT_BYTES = W_BYTES + 2 * M_BYTES;
-  // Pipeline depths: ring stages for operands, slots for state.
-  static constexpr int STAGES =
-      (BN == 128) ? ((MODE == kModeFused && FMT != kFmtBF16) ? 3 : 4)
-                  : ((MODE == kModeFused) ? (FMT == kFmtI8 ? 2 : 3) : 4);
-  static constexpr int XCH_BYTES = (MODE == kModeFused && FMT == kFmtI8) ? 2 * 2 * kBM * 4 : 0;
-  static constexpr int FIXED_BYTES = 8 * (2 * STAGES + 4 + 2 * 4 + 1) + 16 + XCH_BYTES;
-  static constexpr int NS_FIT = (kSmemLimit - FIXED_BYTES - STAGES * STAGE_BYTES) / SLOT_BYTES;
-  static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;
+  static constexpr bool I8 = (MODE == kModeFused && FMT == kFmtI8);
+  // int8 row-halves exchange: [2 buffers][2 halves][2 kinds][128 rows] floats
+  static constexpr int XCH_BYTES = I8 ? 2 * 2 * 2 * kBM * 4 : 0;
+  static constexpr int MAX_BARS = 2 * 6 + 4 + 3 * 6 + 2;
+  static constexpr int BUDGET = kSmemLimit - (8 * MAX_BARS + 16 + XCH_BYTES);
+  static constexpr int NS_CAP = 6;
+  static constexpr int stages_mma() {
+    int st = 6;
+    while (st > 2 && (BUDGET - st * STAGE_BYTES) / SLOT_BYTES < 2) --st;
+    return st;
+  }
+  static constexpr int STAGES = (PROF == kProfStream) ? 2 : stages_mma();
+  static constexpr int NS_FIT = (BUDGET - STAGES * STAGE_BYTES) / SLOT_BYTES;
+  static constexpr int NS = NS_FIT > NS_CAP ? NS_CAP : NS_FIT;
   static_assert(NS >= 2, "shared memory does not fit two state slots");
   static constexpr int TMEM_COLS = 2 * BN;
   // shared-memory carve (offsets from the 1024-aligned base)
   static constexpr int OFF_SLOTS = STAGES * STAGE_BYTES;
   static constexpr int OFF_BARS = OFF_SLOTS + NS * SLOT_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * NS + 1;
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + 3 * NS + 2;
   static constexpr int OFF_TMEM = OFF_BARS + 8 * NUM_BARS;
   static constexpr int OFF_ABORT = OFF_TMEM + 4;
   static constexpr int OFF_XCH = (OFF_ABORT + 4 + 15) & ~15;
   static constexpr int SMEM_USED = OFF_XCH + XCH_BYTES;
   // Ask for 1 KB of slack to align the base; where that would pass the limit
   // the kernel checks at run time that its window is aligned well enough.
-  static constexpr int SMEM_ALLOC = (SMEM_USED + 1024 < kSmemLimit) ? SMEM_USED + 1024 : kSmemLimit;
+  static constexpr int SMEM_ALLOC =
+      (SMEM_USED + 1024 < kSmemLimit) ? SMEM_USED + 1024 : kSmemLimit;
   static_assert(SMEM_USED <= kSmemLimit, "shared memory budget exceeded");
   static_assert(BN % SW == 0 && BN % 64 == 0, "tile width");
   static_assert(TMEM_COLS <= 512, "tensor memory has 512 columns");
@@ -86,7 +94,7 @@ struct WaitCtx {
 enum WaitSite : int {
   kSiteProducerEmpty = 1, kSiteMmaTmemEmpty = 2, kSiteMmaFull = 3, kSiteLoaderEmpty = 4,
   kSiteEpiTmemFull = 5, kSiteEpiSlotFull = 6, kSiteEpiSlotFree = 7, kSiteDrainOperands = 8,
-  kSiteDrainState = 9, kSiteDrainMma = 10
+  kSiteDrainState = 9, kSiteDrainMma = 10, kSiteStoreSlotDone = 11, kSiteEpiExchange = 12
 };
 
 // Wait until the phase of `bar` with `parity` completes.  Gives up (returns
@@ -130,7 +138,7 @@ __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& tm,
 template <int FMT>
 __device__ __forceinline__ void epi_slice_fused_16(uint32_t taddr, bool zero_grad, uint8_t* slot,
                                                    uint32_t row, int h, const AdamWConsts& hc) {
-  using T = GemmTraits<kModeFused, FMT, 128>;
+  using T = GemmTraits<kModeFused, FMT, 128, kProfStream>;
   uint32_t graw[16];
   tmem_ld_x16(taddr, graw);
   tmem_ld_wait();
@@ -244,23 +252,26 @@ __device__ __forceinline__ void store_codes32(uint8_t* box, uint32_t row, int ch
 
 // int8 moments; SW = 128 (one quantisation block), HALF = 64.  Two passes
 // over the thread's 64 columns: the first updates W and finds the block
-// absmax of m' and r' = sqrt(v') (combined with the partner thread holding
-// the other 64 columns of the row), the second recomputes m', r' and writes
-// their codes.  The exchange barrier is executed by every epilogue thread.
-__device__ __forceinline__ void epi_slice_fused_i8(uint32_t taddr, bool zero_grad, bool active,
-                                                   uint8_t* slot, float* xch, uint32_t row,
-                                                   int h, const float* m_scale_row,
-                                                   const float* v_scale_row, float* m_scale_out,
-                                                   float* v_scale_out,
-                                                   const AdamWConsts& hc) {
-  using T = GemmTraits<kModeFused, kFmtI8, 128>;
+// absmax of m' and r' = sqrt(v') (combined with the partner thread, in the
+// other epilogue warp of the same TMEM lane quadrant, that holds the other 64
+// columns of the row), the second recomputes m', r' and writes their codes.
+// The two halves meet at an mbarrier (bounded wait); `xch` is this slice's
+// buffer of a double buffer, so a fast thread can write the next slice's
+// partials while a slow one still reads these.  Returns false (warp-uniform)
+// if the exchange timed out.
+__device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, bool zero_grad, bool active,
+                                                   uint8_t* slot, float* xch, uint32_t bar_xch,
+                                                   uint32_t xphase, const WaitCtx& wc,
+                                                   uint32_t row, int h, float* m_scale_rc,
+                                                   float* v_scale_rc, const AdamWConsts& hc) {
+  using T = GemmTraits<kModeFused, kFmtI8, 128, kProfStream>;
   uint8_t* wbox = slot + h * (kBM * 64 * 2);   // box h: [128][64] bf16, 128-byte rows
   uint8_t* mbox = slot + T::W_BYTES;           // [128][128] int8
   uint8_t* vbox = mbox + T::M_BYTES;
   float sm_old = 0.0f, sv_old = 0.0f;
   if (active) {
-    sm_old = *m_scale_row;
-    sv_old = *v_scale_row;
+    sm_old = *m_scale_rc;
+    sv_old = *v_scale_rc;
   }
   float amax_m = 0.0f, amax_r = 0.0f;
 #pragma unroll 1
@@ -273,7 +284,8 @@ __device__ __forceinline__ void epi_slice_fused_i8(uint32_t taddr, bool zero_gra
     load_codes32(vbox, row, 4 * h + 2 * c, qv);
     uint4 wq[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) wq[k] = *reinterpret_cast<const uint4*>(wbox + sw128_off(row, 4 * c + k));
+    for (int k = 0; k < 4; ++k)
+      wq[k] = *reinterpret_cast<const uint4*>(wbox + sw128_off(row, 4 * c + k));
     const uint32_t* wu = reinterpret_cast<const uint32_t*>(wq);
     uint32_t wo[16];
 #pragma unroll
@@ -298,7 +310,10 @@ __device__ __forceinline__ void epi_slice_fused_i8(uint32_t taddr, bool zero_gra
   // combine the row's two halves
   xch[(h * 2 + 0) * kBM + row] = amax_m;
   xch[(h * 2 + 1) * kBM + row] = amax_r;
-  named_bar_sync(2, kEpiThreads);
+  mbar_arrive(bar_xch);
+  bool ok = wait_bounded(bar_xch, xphase, wc, kSiteEpiExchange);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok) return false;
   amax_m = fmaxf(amax_m, xch[((1 - h) * 2 + 0) * kBM + row]);
   amax_r = fmaxf(amax_r, xch[((1 - h) * 2 + 1) * kBM + row]);
   const float inv_m = int8_inv_step(amax_m), inv_r = int8_inv_step(amax_r);
@@ -323,9 +338,10 @@ __device__ __forceinline__ void epi_slice_fused_i8(uint32_t taddr, bool zero_gra
     store_codes32(vbox, row, 4 * h + 2 * c, qv);
   }
   if (active && h == 0) {
-    *m_scale_out = int8_scale(amax_m);
-    *v_scale_out = int8_scale(amax_r);
+    *m_scale_rc = int8_scale(amax_m);
+    *v_scale_rc = int8_scale(amax_r);
   }
+  return true;
 }
 
 // Store-G: write the fp32 accumulator as fp32 or bf16.  SW = 32, HALF = 16.
@@ -357,10 +373,10 @@ __device__ __forceinline__ void epi_slice_store(uint32_t taddr, bool zero_grad, 
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <int MODE, int FMT, int BN>
+template <int MODE, int FMT, int BN, int PROF>
 __global__ void __launch_bounds__(kNumThreads, 1)
     forge_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
-  using T = GemmTraits<MODE, FMT, BN>;
+  using T = GemmTraits<MODE, FMT, BN, PROF>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -384,7 +400,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   auto bar_tempty = [&](int b) { return bars + 8u * (2 * T::STAGES + 2 + b); };
   auto bar_sfull = [&](int j) { return bars + 8u * (2 * T::STAGES + 4 + j); };
   auto bar_sempty = [&](int j) { return bars + 8u * (2 * T::STAGES + 4 + T::NS + j); };
-  const uint32_t bar_drain = bars + 8u * (2 * T::STAGES + 4 + 2 * T::NS);
+  auto bar_sdone = [&](int j) { return bars + 8u * (2 * T::STAGES + 4 + 2 * T::NS + j); };
+  const uint32_t bar_drain = bars + 8u * (2 * T::STAGES + 4 + 3 * T::NS);
+  const uint32_t bar_xch = bar_drain + 8u;
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + T::OFF_ABORT);
   const WaitCtx wc{abort_flag, p.err, p.err_site, p.timeout_ns};
 
@@ -400,8 +418,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     for (int j = 0; j < T::NS; ++j) {
       mbar_init(bar_sfull(j), 1);
       mbar_init(bar_sempty(j), 1);
+      mbar_init(bar_sdone(j), kEpiThreads);
     }
     mbar_init(bar_drain, 1);
+    mbar_init(bar_xch, kEpiThreads);
     *abort_flag = 0u;
     fence_mbarrier_init();
   }
@@ -457,6 +477,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           wait_bounded(bar_full(s), (static_cast<uint32_t>(last_armed[s]) / T::STAGES) & 1u, wc,
                        kSiteDrainOperands, false);
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -497,6 +518,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       umma_commit(bar_drain);
       wait_bounded(bar_drain, 0u, wc, kSiteDrainMma, false);
     }
+    __syncwarp();
   } else if (warp == 2) {
     // ------------------------------------------------------------ state loader
     if (MODE == kModeFused && lane == 0) {
@@ -538,48 +560,87 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           wait_bounded(bar_sfull(j), (static_cast<uint32_t>(last_armed[j]) / T::NS) & 1u, wc,
                        kSiteDrainState, false);
     }
-  } else if (warp >= 4) {
+    __syncwarp();
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ store warp
+    // TMA-stores each finished slice and frees its slot as soon as the store
+    // has read it, off the epilogue's critical path.
+    if (lane == 0) {
+      uint32_t cnt = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        int tm, tn;
+        tile_coords(t, p, tm, tn);
+        for (int s = 0; s < T::SLICES; ++s, ++cnt) {
+          const int j = cnt % T::NS;
+          const uint32_t ph = (cnt / T::NS) & 1u;
+          if (!wait_bounded(bar_sdone(j), ph, wc, kSiteStoreSlotDone)) { ok = false; break; }
+          const int x0 = tn * BN + s * T::SW;
+          const int y0 = tm * kBM;
+          if (x0 < p.d_in) {
+            const uint32_t sl = base + T::OFF_SLOTS + j * T::SLOT_BYTES;
+            if constexpr (T::I8) {
+              tma_store_2d(&maps.w, x0, y0, sl);
+              tma_store_2d(&maps.w, x0 + 64, y0, sl + kBM * 64 * 2);
+            } else {
+              tma_store_2d(&maps.w, x0, y0, sl);
+            }
+            if constexpr (MODE == kModeFused) {
+              tma_store_2d(&maps.m, x0, y0, sl + T::W_BYTES);
+              tma_store_2d(&maps.v, x0, y0, sl + T::W_BYTES + T::M_BYTES);
+            }
+            bulk_commit_group();
+            bulk_wait_group_read<0>();
+          }
+          mbar_arrive(bar_sempty(j));
+        }
+      }
+      bulk_wait_group<0>();
+    }
+    __syncwarp();
+  } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                  // TMEM lane quadrant this warp may read
     const int h = (warp - 4) >> 2;           // column half of each slice
     const uint32_t row = q * 32 + lane;      // tile row = TMEM lane
-    const bool store_thread = (threadIdx.x == 128);
     const bool zero_grad = (p.num_k == 0);
     float* xch = reinterpret_cast<float*>(gbase + T::OFF_XCH);
     const int scale_cols = p.d_in / 128;
-    uint32_t scnt = 0;
+    uint32_t scnt = 0, xcnt = 0;
     int it = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++it) {
       int tm, tn;
       tile_coords(t, p, tm, tn);
       const int buf = it & 1;
       const uint32_t use = (it >> 1) & 1;
       bool good = wait_bounded(bar_tfull(buf), use, wc, kSiteEpiTmemFull);
+      // tcgen05.ld is warp-collective: the whole warp takes the same branch
+      if (!__all_sync(0xffffffffu, good)) { ok = false; break; }
       tc_fence_after_sync();
-      bool any_bad = false;
       for (int s = 0; s < T::SLICES; ++s, ++scnt) {
         const int j = scnt % T::NS;
         const uint32_t ph = (scnt / T::NS) & 1u;
         if (MODE == kModeFused)
-          good = good && wait_bounded(bar_sfull(j), ph, wc, kSiteEpiSlotFull);
+          good = wait_bounded(bar_sfull(j), ph, wc, kSiteEpiSlotFull);
         else
-          good = good && wait_bounded(bar_sempty(j), ph ^ 1u, wc, kSiteEpiSlotFree);
-        // tcgen05.ld is warp-collective: the whole warp takes the same branch
-        good = __all_sync(0xffffffffu, good);
+          good = wait_bounded(bar_sempty(j), ph ^ 1u, wc, kSiteEpiSlotFree);
+        if (!__all_sync(0xffffffffu, good)) { ok = false; break; }
         const int x0 = tn * BN + s * T::SW;
         const int y0 = tm * kBM;
         const bool active = x0 < p.d_in;
         uint8_t* slot = gbase + T::OFF_SLOTS + j * T::SLOT_BYTES;
         const uint32_t taddr =
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + s * T::SW + h * T::HALF;
-        if constexpr (MODE == kModeFused && FMT == kFmtI8) {
+        if constexpr (T::I8) {
           const bool row_ok = active && (y0 + static_cast<int>(row)) < p.d_out;
-          const size_t sidx = static_cast<size_t>(y0 + row) * scale_cols + (x0 >> 7);
-          epi_slice_fused_i8(taddr, zero_grad, good && row_ok, slot, xch, row, h,
-                             p.m_scale + (row_ok ? sidx : 0), p.v_scale + (row_ok ? sidx : 0),
-                             p.m_scale + (row_ok ? sidx : 0), p.v_scale + (row_ok ? sidx : 0),
-                             p.h);
-        } else if (good && active) {
+          const size_t sidx = row_ok ? static_cast<size_t>(y0 + row) * scale_cols + (x0 >> 7) : 0;
+          const bool xok = epi_slice_fused_i8(
+              taddr, zero_grad, row_ok, slot, xch + (xcnt & 1u) * (2 * 2 * kBM), bar_xch,
+              xcnt & 1u, wc, row, h, p.m_scale + sidx, p.v_scale + sidx, p.h);
+          ++xcnt;
+          if (!xok) { ok = false; break; }
+        } else if (active) {
           if constexpr (MODE == kModeFused)
             epi_slice_fused_16<FMT>(taddr, zero_grad, slot, row, h, p.h);
           else
@@ -590,30 +651,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           mbar_arrive(bar_tempty(buf));
         }
         fence_proxy_async_smem();
-        any_bad = named_bar_or(1, kEpiThreads, !good);
-        if (any_bad) break;
-        if (store_thread) {
-          if (active) {
-            const uint32_t sl = smem_u32(slot);
-            if constexpr (MODE == kModeFused && FMT == kFmtI8) {
-              tma_store_2d(&maps.w, x0, y0, sl);
-              tma_store_2d(&maps.w, x0 + 64, y0, sl + kBM * 64 * 2);
-            } else {
-              tma_store_2d(&maps.w, x0, y0, sl);
-            }
-            if constexpr (MODE == kModeFused) {
-              tma_store_2d(&maps.m, x0, y0, sl + T::W_BYTES);
-              tma_store_2d(&maps.v, x0, y0, sl + T::W_BYTES + T::M_BYTES);
-            }
-          }
-          bulk_commit_group();
-          bulk_wait_group_read<1>();
-          if (scnt > 0) mbar_arrive(bar_sempty((scnt - 1) % T::NS));
-        }
+        mbar_arrive(bar_sdone(j));
       }
-      if (any_bad) break;
     }
-    if (store_thread) bulk_wait_group<0>();
   }
 
   // ---------------------------------------------------------------- teardown
@@ -625,14 +665,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   }
 }
 
-template <int MODE, int FMT, int BN>
+template <int MODE, int FMT, int BN, int PROF>
 cudaError_t launch_gemm_t(const GemmConfig& cfg, const GemmMaps& maps, const GemmParams& p,
                           cudaStream_t stream) {
-  using T = GemmTraits<MODE, FMT, BN>;
-  auto kern = forge_gemm_kernel<MODE, FMT, BN>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       T::SMEM_ALLOC);
-  if (e != cudaSuccess) return e;
+  using T = GemmTraits<MODE, FMT, BN, PROF>;
+  auto kern = forge_gemm_kernel<MODE, FMT, BN, PROF>;
+  static int attr_done[64] = {0};   // per device: the attribute is set once
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         T::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = 1;
+  }
   kern<<<cfg.grid, kNumThreads, T::SMEM_ALLOC, stream>>>(maps, p);
   return cudaGetLastError();
 }
@@ -640,18 +686,20 @@ cudaError_t launch_gemm_t(const GemmConfig& cfg, const GemmMaps& maps, const Gem
 template <int MODE, int FMT>
 cudaError_t launch_gemm_fmt(const GemmConfig& cfg, const GemmMaps& maps, const GemmParams& p,
                             cudaStream_t stream) {
-  switch (cfg.bn) {
-    case 128: return launch_gemm_t<MODE, FMT, 128>(cfg, maps, p, stream);
-    default: return cudaErrorInvalidValue;
+  if (cfg.bn == 128 && cfg.prof == kProfStream)
+    return launch_gemm_t<MODE, FMT, 128, kProfStream>(cfg, maps, p, stream);
+  if (cfg.bn == 128 && cfg.prof == kProfMma)
+    return launch_gemm_t<MODE, FMT, 128, kProfMma>(cfg, maps, p, stream);
+  // 128 x 256 tiles: the whole 512-column tensor memory holds two accumulators.
+  // Not built for int8 moments, whose 64 KB state slots do not fit twice next
+  // to the wider operand stages.
+  if constexpr (!(MODE == kModeFused && FMT == kFmtI8)) {
+    if (cfg.bn == 256 && cfg.prof == kProfStream)
+      return launch_gemm_t<MODE, FMT, 256, kProfStream>(cfg, maps, p, stream);
+    if (cfg.bn == 256 && cfg.prof == kProfMma)
+      return launch_gemm_t<MODE, FMT, 256, kProfMma>(cfg, maps, p, stream);
   }
-}
-
-template <int MODE, int FMT>
-size_t gemm_smem_bytes_fmt(int bn) {
-  switch (bn) {
-    case 128: return GemmTraits<MODE, FMT, 128>::SMEM_ALLOC;
-    default: return 0;
-  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace forge

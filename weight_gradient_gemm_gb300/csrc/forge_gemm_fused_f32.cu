@@ -9,6 +9,5 @@ cudaError_t launch_gemm_fused_f32(const GemmConfig& cfg, const GemmMaps& maps,
   return launch_gemm_fmt<kModeFused, kFmtF32>(cfg, maps, p, stream);
 }
 
-size_t gemm_smem_bytes_fused_f32(int bn) { return gemm_smem_bytes_fmt<kModeFused, kFmtF32>(bn); }
 
 }  // namespace forge

@@ -9,6 +9,5 @@ cudaError_t launch_gemm_store_bf16(const GemmConfig& cfg, const GemmMaps& maps,
   return launch_gemm_fmt<kModeStoreG, kFmtBF16>(cfg, maps, p, stream);
 }
 
-size_t gemm_smem_bytes_store_bf16(int bn) { return gemm_smem_bytes_fmt<kModeStoreG, kFmtBF16>(bn); }
 
 }  // namespace forge

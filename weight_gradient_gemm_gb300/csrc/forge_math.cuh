@@ -22,6 +22,22 @@ struct AdamWConsts {
   float inv_sqrt_bc2;      // 1 / sqrt(1 - beta2^t)
 };
 
+// Square root and reciprocal on the special-function unit (PTX sqrt.approx /
+// rcp.approx: relative error about 2^-23).  The update they feed is added to
+// a weight rounded to bf16 (2^-8 relative), so their error is far below what
+// the stored result can show; the moments themselves use only exact-rounded
+// multiply-adds.
+__device__ __forceinline__ float sqrt_approx(float x) {
+  float y;
+  asm("sqrt.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // One AdamW element.  In: g (fp32 gradient), w, m, v.  Out: w', m', v' and
 // r' = sqrt(v').  The weight update reads the unrounded m' and v'.
 //   m' = beta1 m + (1-beta1) g
@@ -31,9 +47,9 @@ __device__ __forceinline__ void adamw_elem(float g, float& w, float& m, float& v
                                            const AdamWConsts& c) {
   const float m1 = __fmaf_rn(c.beta1, m, __fmul_rn(c.omb1, g));
   const float v1 = __fmaf_rn(c.beta2, v, __fmul_rn(c.omb2, __fmul_rn(g, g)));
-  const float r1 = __fsqrt_rn(v1);
+  const float r1 = sqrt_approx(v1);
   const float denom = __fmaf_rn(r1, c.inv_sqrt_bc2, c.eps);
-  const float upd = __fdiv_rn(m1, denom);
+  const float upd = __fmul_rn(m1, rcp_approx(denom));
   w = __fmaf_rn(c.neg_step_size, upd, __fmul_rn(w, c.decay));
   m = m1;
   v = v1;

@@ -27,14 +27,16 @@ def _gpu():
     require_gpu()
 
 
-@pytest.fixture(params=[("stream", "128"), ("mma", "128"), ("stream", "256"), ("mma", "256")],
-                ids=lambda p: f"{p[0]}-bn{p[1]}")
+@pytest.fixture(params=[("stream", "128", "1"), ("mma", "128", "1"), ("stream", "256", "1"),
+                        ("mma", "256", "1"), ("stream", "256", "2"), ("mma", "256", "2")],
+                ids=lambda p: f"{p[0]}-bn{p[1]}-cta{p[2]}")
 def profile(request, monkeypatch):
-    """Every pipeline profile and tile width of the tensor-core kernel (the
-    library picks them by token count; FORGE_PROFILE and FORGE_BN force them;
-    int8 moments always use 128-wide tiles)."""
+    """Every pipeline profile, tile width and CTA grouping of the tensor-core
+    kernel (the library picks them by token count; FORGE_PROFILE, FORGE_BN and
+    FORGE_CG force them; 1-CTA int8 moments always use 128-wide tiles)."""
     monkeypatch.setenv("FORGE_PROFILE", request.param[0])
     monkeypatch.setenv("FORGE_BN", request.param[1])
+    monkeypatch.setenv("FORGE_CG", request.param[2])
     return request.param
 
 

@@ -240,24 +240,32 @@ AdamWConsts make_consts(float lr, float b1, float b2, float eps, float wd, int64
 // Tile configuration.  Below about a thousand tokens the step is bound by
 // streaming W, m, v through HBM and the stream profile (deep state pipeline)
 // wins; above it the main loop dominates and the mma profile (deep operand
-// pipeline) with 128 x 256 tiles wins: the wider tile reads 25% fewer operand
-// bytes from shared memory per FLOP.  FORGE_PROFILE=stream|mma and
-// FORGE_BN=128|256 override the choice.
+// pipeline) on 256 x 256 tiles computed by a CTA pair (tcgen05 cta_group::2)
+// wins: each SM then reads only its half of the B operand from shared memory.
+// FORGE_PROFILE=stream|mma, FORGE_CG=1|2 and FORGE_BN=128|256 override it.
 GemmConfig choose_config(int64_t bt, int64_t d_in, int64_t d_out, int fmt, int num_sms) {
   GemmConfig c;
   c.group_m = 8;
   c.prof = bt <= 1024 ? kProfStream : kProfMma;
-  c.bn = (c.prof == kProfMma && fmt != kFmtI8) ? 256 : 128;
+  c.cg = (c.prof == kProfMma) ? 2 : 1;
+  c.bn = (c.cg == 2) ? 256 : 128;
   if (const char* e = std::getenv("FORGE_PROFILE")) {
     if (std::strcmp(e, "stream") == 0) c.prof = kProfStream;
     if (std::strcmp(e, "mma") == 0) c.prof = kProfMma;
   }
+  if (const char* e = std::getenv("FORGE_CG")) {
+    if (std::strcmp(e, "1") == 0) c.cg = 1;
+    if (std::strcmp(e, "2") == 0) c.cg = 2;
+  }
   if (const char* e = std::getenv("FORGE_BN")) {
     if (std::strcmp(e, "128") == 0) c.bn = 128;
-    if (std::strcmp(e, "256") == 0 && fmt != kFmtI8) c.bn = 256;
+    if (std::strcmp(e, "256") == 0) c.bn = 256;
   }
-  const int64_t tiles = ((d_out + kBM - 1) / kBM) * ((d_in + c.bn - 1) / c.bn);
-  c.grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+  if (c.cg == 2) c.bn = 256;                    // pairs always use 256 x 256 tiles
+  if (c.cg == 1 && fmt == kFmtI8) c.bn = 128;   // 1-CTA int8 only with 128-wide tiles
+  const int64_t tiles = ((d_out + kBM * c.cg - 1) / (kBM * c.cg)) * ((d_in + c.bn - 1) / c.bn);
+  const int64_t units = num_sms / c.cg;
+  c.grid = static_cast<int>(c.cg * (tiles < units ? tiles : units));
   return c;
 }
 
@@ -268,7 +276,7 @@ GemmParams base_params(int64_t bt, int64_t d_in, int64_t d_out, const GemmConfig
   p.bt = static_cast<int32_t>(bt);
   p.d_in = static_cast<int32_t>(d_in);
   p.d_out = static_cast<int32_t>(d_out);
-  p.tiles_m = static_cast<int32_t>((d_out + kBM - 1) / kBM);
+  p.tiles_m = static_cast<int32_t>((d_out + kBM * cfg.cg - 1) / (kBM * cfg.cg));
   p.tiles_n = static_cast<int32_t>((d_in + cfg.bn - 1) / cfg.bn);
   p.num_tiles = p.tiles_m * p.tiles_n;
   p.num_k = static_cast<int32_t>((bt + kBK - 1) / kBK);
@@ -478,9 +486,9 @@ int forge_describe_config(int64_t bt, int64_t d_in, int64_t d_out, forge_moment_
   const GemmConfig c = choose_config(bt, d_in, d_out, fm, sms);
   const int sw = slice_cols(kModeFused, fm);
   const int need = std::snprintf(buf, buf ? len : 0,
-                                 "tile=%dx%d bk=%d slice=%d grid=%d group_m=%d threads=%d "
+                                 "tile=%dx%d ctas=%d bk=%d slice=%d grid=%d group_m=%d threads=%d "
                                  "profile=%s",
-                                 kBM, c.bn, kBK, sw, c.grid, c.group_m, kNumThreads,
+                                 kBM * c.cg, c.bn, c.cg, kBK, sw, c.grid, c.group_m, kNumThreads,
                                  c.prof == kProfStream ? "stream" : "mma");
   return need + 1;
 }

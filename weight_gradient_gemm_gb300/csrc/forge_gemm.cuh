@@ -36,13 +36,18 @@ namespace forge {
 constexpr int kSmemLimit = 232448;   // max dynamic shared memory per CTA (227 KB)
 
 
-template <int MODE, int FMT, int BN, int PROF>
+// BN is the accumulator width per CTA (the MMA N).  With CG = 2 a pair of
+// CTAs computes a 256 x BN tile with one tcgen05.mma.cta_group::2: each CTA
+// loads its 128 rows of A and BN/2 columns of B and holds 128 x BN of D.
+template <int MODE, int FMT, int BN, int PROF, int CG = 1>
 struct GemmTraits {
   static constexpr int SW = slice_cols(MODE, FMT);     // columns per epilogue slice
   static constexpr int SLICES = BN / SW;
   static constexpr int HALF = SW / 2;                  // columns per epilogue thread per slice
+  static constexpr int TM = kBM * CG;                  // weight rows per tile
+  static constexpr int BNL = BN / CG;                  // B columns loaded per CTA
   static constexpr int A_BYTES = kBM * kBK * 2;
-  static constexpr int B_BYTES = BN * kBK * 2;
+  static constexpr int B_BYTES = BNL * kBK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int W_ELEM = (MODE == kModeStoreG && FMT == kFmtF32) ? 4 : 2;
   static constexpr int MOM_ELEM =
@@ -79,7 +84,8 @@ struct GemmTraits {
   static constexpr int SMEM_ALLOC =
       (SMEM_USED + 1024 < kSmemLimit) ? SMEM_USED + 1024 : kSmemLimit;
   static_assert(SMEM_USED <= kSmemLimit, "shared memory budget exceeded");
-  static_assert(BN % SW == 0 && BN % 64 == 0, "tile width");
+  static_assert(BN % SW == 0 && BNL % 64 == 0, "tile width");
+  static_assert(CG == 1 || (CG == 2 && BN == 256), "CTA pairs use 256 x 256 tiles");
   static_assert(TMEM_COLS <= 512, "tensor memory has 512 columns");
 };
 
@@ -373,10 +379,11 @@ __device__ __forceinline__ void epi_slice_store(uint32_t taddr, bool zero_grad, 
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <int MODE, int FMT, int BN, int PROF>
+template <int MODE, int FMT, int BN, int PROF, int CG>
 __global__ void __launch_bounds__(kNumThreads, 1)
     forge_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
-  using T = GemmTraits<MODE, FMT, BN, PROF>;
+  using T = GemmTraits<MODE, FMT, BN, PROF, CG>;
+  constexpr bool kPair = (CG == 2);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -392,6 +399,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // A CTA pair walks the tiles as one unit; rank 0 issues the pair's MMAs.
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const bool leader = (rank == 0);
+  const int unit0 = kPair ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int units = kPair ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
 
   const uint32_t bars = base + T::OFF_BARS;
   auto bar_full = [&](int s) { return bars + 8u * s; };
@@ -413,7 +425,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_tfull(b), 1);
-      mbar_init(bar_tempty(b), kEpiThreads);
+      mbar_init(bar_tempty(b), CG * (kEpiThreads / 32));   // one arrival per epilogue warp
     }
     for (int j = 0; j < T::NS; ++j) {
       mbar_init(bar_sfull(j), 1);
@@ -434,9 +446,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       tma_prefetch_desc(&maps.v);
     }
   }
+  // the peer's barriers must be initialised before any cross-CTA arrival
+  if constexpr (kPair) cluster_sync_all(); else __syncthreads();
   if (warp == 1) {
-    tmem_alloc(base + T::OFF_TMEM, T::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(base + T::OFF_TMEM, T::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(base + T::OFF_TMEM, T::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -452,7 +471,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll
       for (int s = 0; s < T::STAGES; ++s) last_armed[s] = -1;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      for (int t = unit0; ok && t < p.num_tiles; t += units) {
         int tm, tn;
         tile_coords(t, p, tm, tn);
         for (int k = 0; k < p.num_k; ++k, ++cnt) {
@@ -461,14 +480,28 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           if (!wait_bounded(bar_empty(s), ph ^ 1u, wc, kSiteProducerEmpty)) { ok = false; break; }
           if (p.drop_first_arrival && cnt == 0) continue;   // testing aid
           const uint32_t dst = base + s * T::STAGE_BYTES;
-          mbar_arrive_expect_tx(bar_full(s), T::STAGE_BYTES);
-          tma_load_2d(dst, &maps.dy, tm * kBM, k * kBK, bar_full(s), pol);
-          tma_load_2d(dst + 64 * kBK * 2, &maps.dy, tm * kBM + 64, k * kBK, bar_full(s), pol);
+          const int ya = tm * T::TM + static_cast<int>(rank) * kBM;      // this CTA's A rows
+          const int xb = tn * BN + static_cast<int>(rank) * T::BNL;      // this CTA's B columns
+          if constexpr (kPair) {
+            // both CTAs' loads complete on the leader's barrier, which expects both
+            const uint32_t fb = mapa_shared(bar_full(s), 0);
+            if (leader) mbar_arrive_expect_tx(bar_full(s), 2 * T::STAGE_BYTES);
+            tma_load_2d_pair(dst, &maps.dy, ya, k * kBK, fb, pol);
+            tma_load_2d_pair(dst + 64 * kBK * 2, &maps.dy, ya + 64, k * kBK, fb, pol);
 #pragma unroll
-          for (int hb = 0; hb < BN / 64; ++hb)
-            tma_load_2d(dst + T::A_BYTES + hb * 64 * kBK * 2, &maps.x, tn * BN + hb * 64, k * kBK,
-                        bar_full(s), pol);
-          last_armed[s] = static_cast<int32_t>(cnt);
+            for (int hb = 0; hb < T::BNL / 64; ++hb)
+              tma_load_2d_pair(dst + T::A_BYTES + hb * 64 * kBK * 2, &maps.x, xb + hb * 64,
+                               k * kBK, fb, pol);
+          } else {
+            mbar_arrive_expect_tx(bar_full(s), T::STAGE_BYTES);
+            tma_load_2d(dst, &maps.dy, ya, k * kBK, bar_full(s), pol);
+            tma_load_2d(dst + 64 * kBK * 2, &maps.dy, ya + 64, k * kBK, bar_full(s), pol);
+#pragma unroll
+            for (int hb = 0; hb < T::BNL / 64; ++hb)
+              tma_load_2d(dst + T::A_BYTES + hb * 64 * kBK * 2, &maps.x, xb + hb * 64, k * kBK,
+                          bar_full(s), pol);
+          }
+          if (leader) last_armed[s] = static_cast<int32_t>(cnt);
         }
       }
       // let every armed load land before the CTA can exit
@@ -480,14 +513,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc_bf16_mn(kBM, BN);
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = make_idesc_bf16_mn(T::TM, BN);
       constexpr uint32_t kLBO = kBK * 128;   // next 64-element group along M/N
       constexpr uint32_t kSBO = 1024;        // next 8-token group
       uint32_t cnt = 0;
       bool ok = true;
       int it = 0;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++it) {
+      for (int t = unit0; ok && t < p.num_tiles; t += units, ++it) {
         const int buf = it & 1;
         const uint32_t use = (it >> 1) & 1;
         if (!wait_bounded(bar_tempty(buf), use ^ 1u, wc, kSiteMmaTmemEmpty)) { ok = false; break; }
@@ -504,18 +537,26 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t ad = make_sdesc_mn_sw128(a0 + kk * 2048, kLBO, kSBO);
             const uint64_t bd = make_sdesc_mn_sw128(b0 + kk * 2048, kLBO, kSBO);
-            umma_bf16(d, ad, bd, idesc, (k | kk) != 0 ? 1u : 0u);
+            if constexpr (kPair)
+              umma_bf16_pair(d, ad, bd, idesc, (k | kk) != 0 ? 1u : 0u);
+            else
+              umma_bf16(d, ad, bd, idesc, (k | kk) != 0 ? 1u : 0u);
           }
-          umma_commit(bar_empty(s));
+          // frees stage s in both CTAs once these MMAs have read it
+          if constexpr (kPair) umma_commit_pair_mc(bar_empty(s), 0x3); else umma_commit(bar_empty(s));
         }
         if (!ok) break;
-        if (p.num_k > 0)
-          umma_commit(bar_tfull(buf));
-        else
-          mbar_arrive(bar_tfull(buf));
+        if constexpr (kPair) {
+          umma_commit_pair_mc(bar_tfull(buf), 0x3);
+        } else {
+          if (p.num_k > 0)
+            umma_commit(bar_tfull(buf));
+          else
+            mbar_arrive(bar_tfull(buf));
+        }
       }
       // every MMA issued must complete before the tensor memory is freed
-      umma_commit(bar_drain);
+      if constexpr (kPair) umma_commit_pair_mc(bar_drain, 0x1); else umma_commit(bar_drain);
       wait_bounded(bar_drain, 0u, wc, kSiteDrainMma, false);
     }
     __syncwarp();
@@ -528,7 +569,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll
       for (int j = 0; j < T::NS; ++j) last_armed[j] = -1;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      for (int t = unit0; ok && t < p.num_tiles; t += units) {
         int tm, tn;
         tile_coords(t, p, tm, tn);
         for (int s = 0; s < T::SLICES; ++s, ++cnt) {
@@ -536,9 +577,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           const uint32_t ph = (cnt / T::NS) & 1u;
           if (!wait_bounded(bar_sempty(j), ph ^ 1u, wc, kSiteLoaderEmpty)) { ok = false; break; }
           const int x0 = tn * BN + s * T::SW;
-          const int y0 = tm * kBM;
+          const int y0 = tm * T::TM + static_cast<int>(rank) * kBM;
           last_armed[j] = static_cast<int32_t>(cnt);   // latest phase started on slot j
-          if (x0 >= p.d_in) {        // slice entirely past the last column
+          if (x0 >= p.d_in || y0 >= p.d_out) {   // slice entirely outside the weight
             mbar_arrive(bar_sfull(j));
             continue;
           }
@@ -568,7 +609,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     if (lane == 0) {
       uint32_t cnt = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      for (int t = unit0; ok && t < p.num_tiles; t += units) {
         int tm, tn;
         tile_coords(t, p, tm, tn);
         for (int s = 0; s < T::SLICES; ++s, ++cnt) {
@@ -576,8 +617,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           const uint32_t ph = (cnt / T::NS) & 1u;
           if (!wait_bounded(bar_sdone(j), ph, wc, kSiteStoreSlotDone)) { ok = false; break; }
           const int x0 = tn * BN + s * T::SW;
-          const int y0 = tm * kBM;
-          if (x0 < p.d_in) {
+          const int y0 = tm * T::TM + static_cast<int>(rank) * kBM;
+          if (x0 < p.d_in && y0 < p.d_out) {
             const uint32_t sl = base + T::OFF_SLOTS + j * T::SLOT_BYTES;
             if constexpr (T::I8) {
               tma_store_2d(&maps.w, x0, y0, sl);
@@ -609,7 +650,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     uint32_t scnt = 0, xcnt = 0;
     int it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++it) {
+    for (int t = unit0; ok && t < p.num_tiles; t += units, ++it) {
       int tm, tn;
       tile_coords(t, p, tm, tn);
       const int buf = it & 1;
@@ -627,8 +668,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           good = wait_bounded(bar_sempty(j), ph ^ 1u, wc, kSiteEpiSlotFree);
         if (!__all_sync(0xffffffffu, good)) { ok = false; break; }
         const int x0 = tn * BN + s * T::SW;
-        const int y0 = tm * kBM;
-        const bool active = x0 < p.d_in;
+        const int y0 = tm * T::TM + static_cast<int>(rank) * kBM;
+        const bool active = x0 < p.d_in && y0 < p.d_out;
         uint8_t* slot = gbase + T::OFF_SLOTS + j * T::SLOT_BYTES;
         const uint32_t taddr =
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + s * T::SW + h * T::HALF;
@@ -646,9 +687,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           else
             epi_slice_store<FMT>(taddr, zero_grad, slot, row, h);
         }
-        if (s == T::SLICES - 1) {
+        if (s == T::SLICES - 1) {   // this warp has read the whole accumulator
           tc_fence_before_sync();
-          mbar_arrive(bar_tempty(buf));
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (kPair) mbar_arrive_cluster(mapa_shared(bar_tempty(buf), 0));
+            else mbar_arrive(bar_tempty(buf));
+          }
         }
         fence_proxy_async_smem();
         mbar_arrive(bar_sdone(j));
@@ -658,47 +703,92 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
   // ---------------------------------------------------------------- teardown
   tc_fence_before_sync();
-  __syncthreads();
+  if constexpr (kPair) {
+    // after a timeout, give copies still in flight into this CTA's shared
+    // memory time to land (their completions go to the leader's barriers)
+    if (*abort_flag) {
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 200000ull) {
+      }
+    }
+    // neither CTA leaves while its peer may still read its shared memory or
+    // arrive on its barriers
+    cluster_sync_all();
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, T::TMEM_COLS);
+    if constexpr (kPair) tmem_dealloc_pair(tmem_base, T::TMEM_COLS);
+    else tmem_dealloc(tmem_base, T::TMEM_COLS);
   }
 }
 
-template <int MODE, int FMT, int BN, int PROF>
+template <int MODE, int FMT, int BN, int PROF, int CG>
 cudaError_t launch_gemm_t(const GemmConfig& cfg, const GemmMaps& maps, const GemmParams& p,
                           cudaStream_t stream) {
-  using T = GemmTraits<MODE, FMT, BN, PROF>;
-  auto kern = forge_gemm_kernel<MODE, FMT, BN, PROF>;
-  static int attr_done[64] = {0};   // per device: the attribute is set once
+  using T = GemmTraits<MODE, FMT, BN, PROF, CG>;
+  auto kern = forge_gemm_kernel<MODE, FMT, BN, PROF, CG>;
+  static int attr_done[64] = {0};     // per device: attributes set, pair count known
+  static int max_pairs[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+  const bool cached = dev >= 0 && dev < 64 && attr_done[dev];
+  if (!cached) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          T::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_done[dev] = 1;
   }
-  kern<<<cfg.grid, kNumThreads, T::SMEM_ALLOC, stream>>>(maps, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t lc = {};
+  lc.blockDim = dim3(kNumThreads, 1, 1);
+  lc.dynamicSmemBytes = T::SMEM_ALLOC;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  int grid = cfg.grid;
+  if constexpr (CG == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    int pairs = cached ? max_pairs[dev] : 0;
+    if (!cached) {
+      lc.gridDim = dim3(2 * 76, 1, 1);
+      cudaError_t e = cudaOccupancyMaxActiveClusters(&pairs, kern, &lc);
+      if (e != cudaSuccess || pairs <= 0) return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
+      if (dev >= 0 && dev < 64) max_pairs[dev] = pairs;
+    }
+    grid = 2 * (cfg.grid / 2 < pairs ? cfg.grid / 2 : pairs);
+  } else {
+    lc.attrs = nullptr;
+    lc.numAttrs = 0;
+  }
+  if (!cached && dev >= 0 && dev < 64) attr_done[dev] = 1;
+  lc.gridDim = dim3(grid, 1, 1);
+  return cudaLaunchKernelEx(&lc, kern, maps, p);
 }
 
 template <int MODE, int FMT>
 cudaError_t launch_gemm_fmt(const GemmConfig& cfg, const GemmMaps& maps, const GemmParams& p,
                             cudaStream_t stream) {
-  if (cfg.bn == 128 && cfg.prof == kProfStream)
-    return launch_gemm_t<MODE, FMT, 128, kProfStream>(cfg, maps, p, stream);
-  if (cfg.bn == 128 && cfg.prof == kProfMma)
-    return launch_gemm_t<MODE, FMT, 128, kProfMma>(cfg, maps, p, stream);
-  // 128 x 256 tiles: the whole 512-column tensor memory holds two accumulators.
+  if (cfg.cg == 1 && cfg.bn == 128 && cfg.prof == kProfStream)
+    return launch_gemm_t<MODE, FMT, 128, kProfStream, 1>(cfg, maps, p, stream);
+  if (cfg.cg == 1 && cfg.bn == 128 && cfg.prof == kProfMma)
+    return launch_gemm_t<MODE, FMT, 128, kProfMma, 1>(cfg, maps, p, stream);
+  // 256-wide accumulators use all 512 tensor-memory columns (two buffers).
   // Not built for int8 moments, whose 64 KB state slots do not fit twice next
-  // to the wider operand stages.
+  // to the wider 1-CTA operand stages.
   if constexpr (!(MODE == kModeFused && FMT == kFmtI8)) {
-    if (cfg.bn == 256 && cfg.prof == kProfStream)
-      return launch_gemm_t<MODE, FMT, 256, kProfStream>(cfg, maps, p, stream);
-    if (cfg.bn == 256 && cfg.prof == kProfMma)
-      return launch_gemm_t<MODE, FMT, 256, kProfMma>(cfg, maps, p, stream);
+    if (cfg.cg == 1 && cfg.bn == 256 && cfg.prof == kProfStream)
+      return launch_gemm_t<MODE, FMT, 256, kProfStream, 1>(cfg, maps, p, stream);
+    if (cfg.cg == 1 && cfg.bn == 256 && cfg.prof == kProfMma)
+      return launch_gemm_t<MODE, FMT, 256, kProfMma, 1>(cfg, maps, p, stream);
   }
+  if (cfg.cg == 2 && cfg.bn == 256 && cfg.prof == kProfStream)
+    return launch_gemm_t<MODE, FMT, 256, kProfStream, 2>(cfg, maps, p, stream);
+  if (cfg.cg == 2 && cfg.bn == 256 && cfg.prof == kProfMma)
+    return launch_gemm_t<MODE, FMT, 256, kProfMma, 2>(cfg, maps, p, stream);
   return cudaErrorInvalidValue;
 }
 

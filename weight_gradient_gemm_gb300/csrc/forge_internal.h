@@ -49,9 +49,10 @@ struct GemmMaps {
 
 // Launch configuration chosen on the host.
 struct GemmConfig {
-  int bn;        // tile width (MMA N)
+  int cg;        // CTAs per tile: 1, or 2 for a CTA pair (cta_group::2, 256-row tiles)
+  int bn;        // accumulator width per CTA (MMA N)
   int prof;      // pipeline profile: 0 stream (HBM-bound), 1 mma (tensor-bound)
-  int grid;      // persistent CTAs
+  int grid;      // persistent CTAs (even for CTA pairs)
   int group_m;
 };
 

@@ -51,6 +51,19 @@ WORKLOADS = {
     "llama31_8b_layer_bt4096_int8": (3, 4096, 2, 1e-3, 0.0),
 }
 DEFAULT_WORKLOAD = "llama31_8b_layer_bt512_fp32"
+_RECIPE = {"fp32": (1, 0, 1e-3, 0.0), "bf16": (2, 1, 1e-3, 0.01), "int8": (3, 2, 1e-3, 0.0)}
+
+
+def workload_spec(name: str):
+    """(recipe config, BT, moment format, dY std, spike fraction) of a named
+    workload; besides the table, any llama31_8b_layer_bt<BT>_<fp32|bf16|int8>."""
+    if name in WORKLOADS:
+        return WORKLOADS[name]
+    parts = name.split("_")
+    if len(parts) == 5 and name.startswith("llama31_8b_layer_bt") and parts[4] in _RECIPE:
+        cfg, fmt, dy_std, spike = _RECIPE[parts[4]]
+        return (cfg, int(parts[3][2:]), fmt, dy_std, spike)
+    raise SystemExit(f"unknown workload {name}")
 
 
 # ---------------------------------------------------------------------------
@@ -208,7 +221,7 @@ def fused_step(F, layer, step, events=None, stream=None):
 def run_gpu(args, rank, world, dev):
     from weight_gradient_gemm_gb300 import forge as F
     F.lib()
-    cfg, bt, fmt, dy_std, spike = WORKLOADS[args.workload]
+    cfg, bt, fmt, dy_std, spike = workload_spec(args.workload)
     layer = Layer(cfg, bt, fmt, dy_std, spike, dev,
                   only=args.only.split(",") if args.only else None)
     stream = torch.cuda.current_stream()
@@ -251,6 +264,8 @@ def run_gpu(args, rank, world, dev):
         raise RuntimeError(F.status_string(status))
     elapsed_ms = t_start.elapsed_time(t_end)
     kern_ms = sum(a.elapsed_time(b) for row in ev for (a, b) in row)
+    per_proj_ms = [sum(row[i][0].elapsed_time(row[i][1]) for row in ev) / args.steps
+                   for i in range(n)]
     if sampler:
         sampler.stop()
     if dist:
@@ -301,6 +316,7 @@ def run_gpu(args, rank, world, dev):
         e2e_ms, unf_ms = float(t[0]), float(t[1])
 
     return dict(layer=layer, elapsed_ms=elapsed_ms, kern_ms=kern_ms, unf_ms=unf_ms,
+                per_proj_ms=per_proj_ms,
                 e2e_ms=e2e_ms, clocks=sampler.summary(w0, w1) if sampler else None,
                 config=F.describe_config(bt, 4096, 4096, fmt))
 
@@ -321,7 +337,7 @@ def oracle_sample(workload: str, rows: int):
     """Inputs for one oracle step on the first `rows` weight rows of each of
     the seven projections."""
     import oracle as O
-    cfg, bt, fmt, dy_std, spike = WORKLOADS[workload]
+    cfg, bt, fmt, dy_std, spike = workload_spec(workload)
     out = []
     for i, (name, d_out, d_in) in enumerate(LLAMA31_8B_SHAPES):
         s = make_step_inputs(cfg, i, 0, bt, d_in, d_out, dy_std=dy_std, with_w=True,
@@ -374,7 +390,7 @@ def cpu_baseline_block(workload):
 def run_reference(args):
     """The reference arm: the CPU oracle, as it stands, on a bounded sample
     of the same workload each step."""
-    cfg, bt, fmt, dy_std, spike = WORKLOADS[args.workload]
+    cfg, bt, fmt, dy_std, spike = workload_spec(args.workload)
     budget_s = 120.0
     per_step = budget_s / max(1, args.steps + args.warmup)
     sample, _ = oracle_sample(args.workload, 4)
@@ -415,7 +431,8 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="forge", choices=["forge", "reference"])
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    help="one of %s, or llama31_8b_layer_bt<BT>_<fp32|bf16|int8>" % sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="",
                     help="comma-separated projections (q,k,v,o,gate,up,down) for small profiling "
@@ -449,7 +466,7 @@ def main():
         return
 
     layer = res["layer"]
-    cfg, bt, fmt, dy_std, spike = WORKLOADS[args.workload]
+    cfg, bt, fmt, dy_std, spike = workload_spec(args.workload)
     peaks, peak_kind = measured_peaks()
     ms = res["elapsed_ms"] / args.steps
     flops = layer.flops()
@@ -496,6 +513,13 @@ def main():
         "e2e": {"value": world * flops / (res["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": res["e2e_ms"], "h2d_bytes_per_step": layer.h2d_bytes(),
                 "d2h_bytes_per_step": 4},
+        "per_projection": [
+            {"name": it["name"], "shape": [it["d_out"], it["d_in"]],
+             "us": round(t * 1e3, 2),
+             "gbs": round((it["d_in"] * it["d_out"] * STATE_BYTES[fmt]
+                           + 2.0 * bt * (it["d_in"] + it["d_out"])) / (t * 1e-3) / 1e9, 1),
+             "tflops": round(2.0 * bt * it["d_in"] * it["d_out"] / (t * 1e-3) / 1e12, 1)}
+            for it, t in zip(layer.items, res["per_proj_ms"])],
         "gpu_launches": launches,
         "clocks": res["clocks"],
     }

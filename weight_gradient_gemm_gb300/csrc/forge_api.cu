@@ -237,21 +237,31 @@ AdamWConsts make_consts(float lr, float b1, float b2, float eps, float wd, int64
   return h;
 }
 
-// Tile configuration.  Below about a thousand tokens the step is bound by
-// streaming W, m, v through HBM and the stream profile (deep state pipeline)
-// wins; above it the main loop dominates and the mma profile (deep operand
-// pipeline) on 256 x 256 tiles computed by a CTA pair (tcgen05 cta_group::2)
-// wins: each SM then reads only its half of the B operand from shared memory.
-// FORGE_PROFILE=stream|mma, FORGE_CG=1|2 and FORGE_BN=128|256 override it.
+// Tile configuration, from measured sweeps over the Llama-3.1-8B projections
+// on GB300.  At a few hundred tokens the step streams W, m, v through HBM:
+// 128 x 128 tiles on one CTA with a deep state pipeline (fp32 and int8
+// moments) or equal stage and slot depths (bf16 moments).  From about a
+// thousand tokens the main loop matters and 256 x 256 tiles on a CTA pair
+// (tcgen05 cta_group::2) win, since each SM then reads only half of the B
+// operand from shared memory: balanced depths up to a few thousand tokens,
+// then the deepest operand pipeline.  FORGE_PROFILE=stream|balanced|mma,
+// FORGE_CG=1|2 and FORGE_BN=128|256 override the choice.
 GemmConfig choose_config(int64_t bt, int64_t d_in, int64_t d_out, int fmt, int num_sms) {
   GemmConfig c;
   c.group_m = 8;
-  c.prof = bt <= 1024 ? kProfStream : kProfMma;
-  c.cg = (c.prof == kProfMma) ? 2 : 1;
+  if (bt <= 768) {
+    c.cg = 1;
+    c.prof = (fmt == kFmtBF16) ? kProfBalanced : kProfStream;
+  } else {
+    c.cg = 2;
+    const int64_t balanced_upto = (fmt == kFmtBF16) ? 3072 : (fmt == kFmtF32 ? 1536 : 0);
+    c.prof = bt <= balanced_upto ? kProfBalanced : kProfMma;
+  }
   c.bn = (c.cg == 2) ? 256 : 128;
   if (const char* e = std::getenv("FORGE_PROFILE")) {
     if (std::strcmp(e, "stream") == 0) c.prof = kProfStream;
     if (std::strcmp(e, "mma") == 0) c.prof = kProfMma;
+    if (std::strcmp(e, "balanced") == 0) c.prof = kProfBalanced;
   }
   if (const char* e = std::getenv("FORGE_CG")) {
     if (std::strcmp(e, "1") == 0) c.cg = 1;
@@ -489,7 +499,9 @@ int forge_describe_config(int64_t bt, int64_t d_in, int64_t d_out, forge_moment_
                                  "tile=%dx%d ctas=%d bk=%d slice=%d grid=%d group_m=%d threads=%d "
                                  "profile=%s",
                                  kBM * c.cg, c.bn, c.cg, kBK, sw, c.grid, c.group_m, kNumThreads,
-                                 c.prof == kProfStream ? "stream" : "mma");
+                                 c.prof == kProfStream ? "stream"
+                                 : c.prof == kProfMma  ? "mma"
+                                                       : "balanced");
   return need + 1;
 }
 

@@ -56,9 +56,9 @@ struct GemmTraits {
   static constexpr int M_BYTES = kBM * SW * MOM_ELEM;
   static constexpr int SLOT_BYTES = W_BYTES + 2 * M_BYTES;
   static constexpr bool I8 = (MODE == kModeFused && FMT == kFmtI8);
-  // int8 row-halves exchange: [2 buffers][2 halves][2 kinds][128 rows] floats
-  static constexpr int XCH_BYTES = I8 ? 2 * 2 * 2 * kBM * 4 : 0;
-  static constexpr int MAX_BARS = 2 * 6 + 4 + 3 * 6 + 2;
+  // int8 row-halves exchange: [2 halves][2 kinds][128 rows] floats
+  static constexpr int XCH_BYTES = I8 ? 2 * 2 * kBM * 4 : 0;
+  static constexpr int MAX_BARS = 2 * 6 + 4 + 3 * 6 + 3;
   static constexpr int BUDGET = kSmemLimit - (8 * MAX_BARS + 16 + XCH_BYTES);
   static constexpr int NS_CAP = 6;
   static constexpr int stages_mma() {
@@ -66,7 +66,13 @@ struct GemmTraits {
     while (st > 2 && (BUDGET - st * STAGE_BYTES) / SLOT_BYTES < 2) --st;
     return st;
   }
-  static constexpr int STAGES = (PROF == kProfStream) ? 2 : stages_mma();
+  static constexpr int stages_balanced() {
+    int st = 6;
+    while (st > 2 && (BUDGET - st * STAGE_BYTES) / SLOT_BYTES < st) --st;
+    return st;
+  }
+  static constexpr int STAGES =
+      (PROF == kProfStream) ? 2 : (PROF == kProfMma ? stages_mma() : stages_balanced());
   static constexpr int NS_FIT = (BUDGET - STAGES * STAGE_BYTES) / SLOT_BYTES;
   static constexpr int NS = NS_FIT > NS_CAP ? NS_CAP : NS_FIT;
   static_assert(NS >= 2, "shared memory does not fit two state slots");
@@ -74,7 +80,7 @@ struct GemmTraits {
   // shared-memory carve (offsets from the 1024-aligned base)
   static constexpr int OFF_SLOTS = STAGES * STAGE_BYTES;
   static constexpr int OFF_BARS = OFF_SLOTS + NS * SLOT_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 4 + 3 * NS + 2;
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + 3 * NS + 3;
   static constexpr int OFF_TMEM = OFF_BARS + 8 * NUM_BARS;
   static constexpr int OFF_ABORT = OFF_TMEM + 4;
   static constexpr int OFF_XCH = (OFF_ABORT + 4 + 15) & ~15;
@@ -261,13 +267,14 @@ __device__ __forceinline__ void store_codes32(uint8_t* box, uint32_t row, int ch
 // absmax of m' and r' = sqrt(v') (combined with the partner thread, in the
 // other epilogue warp of the same TMEM lane quadrant, that holds the other 64
 // columns of the row), the second recomputes m', r' and writes their codes.
-// The two halves meet at an mbarrier (bounded wait); `xch` is this slice's
-// buffer of a double buffer, so a fast thread can write the next slice's
-// partials while a slow one still reads these.  Returns false (warp-uniform)
-// if the exchange timed out.
+// The two halves meet at an mbarrier (bounded wait).  `xch` is one buffer:
+// before writing it a thread waits until every thread has read the previous
+// block's values (bar_xch_read), so a fast thread cannot overwrite them.
+// Returns false (warp-uniform) if a wait timed out.
 __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, bool zero_grad, bool active,
                                                    uint8_t* slot, float* xch, uint32_t bar_xch,
-                                                   uint32_t xphase, const WaitCtx& wc,
+                                                   uint32_t bar_xch_read, uint32_t xphase,
+                                                   const WaitCtx& wc,
                                                    uint32_t row, int h, float* m_scale_rc,
                                                    float* v_scale_rc, const AdamWConsts& hc) {
   using T = GemmTraits<kModeFused, kFmtI8, 128, kProfStream>;
@@ -314,14 +321,16 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, bool zero_gra
           make_uint4(wo[4 * k], wo[4 * k + 1], wo[4 * k + 2], wo[4 * k + 3]);
   }
   // combine the row's two halves
+  bool ok = wait_bounded(bar_xch_read, xphase ^ 1u, wc, kSiteEpiExchange);
+  if (!__all_sync(0xffffffffu, ok)) return false;
   xch[(h * 2 + 0) * kBM + row] = amax_m;
   xch[(h * 2 + 1) * kBM + row] = amax_r;
   mbar_arrive(bar_xch);
-  bool ok = wait_bounded(bar_xch, xphase, wc, kSiteEpiExchange);
-  ok = __all_sync(0xffffffffu, ok);
-  if (!ok) return false;
+  ok = wait_bounded(bar_xch, xphase, wc, kSiteEpiExchange);
+  if (!__all_sync(0xffffffffu, ok)) return false;
   amax_m = fmaxf(amax_m, xch[((1 - h) * 2 + 0) * kBM + row]);
   amax_r = fmaxf(amax_r, xch[((1 - h) * 2 + 1) * kBM + row]);
+  mbar_arrive(bar_xch_read);
   const float inv_m = int8_inv_step(amax_m), inv_r = int8_inv_step(amax_r);
   const bool r_nz = amax_r > 0.0f;
 #pragma unroll 1
@@ -415,6 +424,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   auto bar_sdone = [&](int j) { return bars + 8u * (2 * T::STAGES + 4 + 2 * T::NS + j); };
   const uint32_t bar_drain = bars + 8u * (2 * T::STAGES + 4 + 3 * T::NS);
   const uint32_t bar_xch = bar_drain + 8u;
+  const uint32_t bar_xch_read = bar_drain + 16u;
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + T::OFF_ABORT);
   const WaitCtx wc{abort_flag, p.err, p.err_site, p.timeout_ns};
 
@@ -434,6 +444,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
     mbar_init(bar_drain, 1);
     mbar_init(bar_xch, kEpiThreads);
+    mbar_init(bar_xch_read, kEpiThreads);
     *abort_flag = 0u;
     fence_mbarrier_init();
   }
@@ -676,9 +687,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if constexpr (T::I8) {
           const bool row_ok = active && (y0 + static_cast<int>(row)) < p.d_out;
           const size_t sidx = row_ok ? static_cast<size_t>(y0 + row) * scale_cols + (x0 >> 7) : 0;
-          const bool xok = epi_slice_fused_i8(
-              taddr, zero_grad, row_ok, slot, xch + (xcnt & 1u) * (2 * 2 * kBM), bar_xch,
-              xcnt & 1u, wc, row, h, p.m_scale + sidx, p.v_scale + sidx, p.h);
+          const bool xok = epi_slice_fused_i8(taddr, zero_grad, row_ok, slot, xch, bar_xch,
+                                              bar_xch_read, xcnt & 1u, wc, row, h,
+                                              p.m_scale + sidx, p.v_scale + sidx, p.h);
           ++xcnt;
           if (!xok) { ok = false; break; }
         } else if (active) {
@@ -769,26 +780,31 @@ cudaError_t launch_gemm_t(const GemmConfig& cfg, const GemmMaps& maps, const Gem
   return cudaLaunchKernelEx(&lc, kern, maps, p);
 }
 
+template <int MODE, int FMT, int PROF>
+cudaError_t launch_gemm_prof(const GemmConfig& cfg, const GemmMaps& maps, const GemmParams& p,
+                             cudaStream_t stream) {
+  if (cfg.cg == 1 && cfg.bn == 128)
+    return launch_gemm_t<MODE, FMT, 128, PROF, 1>(cfg, maps, p, stream);
+  // 256-wide accumulators use all 512 tensor-memory columns (two buffers).
+  // Not built for 1-CTA int8 moments, whose 64 KB state slots do not fit
+  // twice next to the wider 1-CTA operand stages.
+  if constexpr (!(MODE == kModeFused && FMT == kFmtI8)) {
+    if (cfg.cg == 1 && cfg.bn == 256)
+      return launch_gemm_t<MODE, FMT, 256, PROF, 1>(cfg, maps, p, stream);
+  }
+  if (cfg.cg == 2 && cfg.bn == 256)
+    return launch_gemm_t<MODE, FMT, 256, PROF, 2>(cfg, maps, p, stream);
+  return cudaErrorInvalidValue;
+}
+
 template <int MODE, int FMT>
 cudaError_t launch_gemm_fmt(const GemmConfig& cfg, const GemmMaps& maps, const GemmParams& p,
                             cudaStream_t stream) {
-  if (cfg.cg == 1 && cfg.bn == 128 && cfg.prof == kProfStream)
-    return launch_gemm_t<MODE, FMT, 128, kProfStream, 1>(cfg, maps, p, stream);
-  if (cfg.cg == 1 && cfg.bn == 128 && cfg.prof == kProfMma)
-    return launch_gemm_t<MODE, FMT, 128, kProfMma, 1>(cfg, maps, p, stream);
-  // 256-wide accumulators use all 512 tensor-memory columns (two buffers).
-  // Not built for int8 moments, whose 64 KB state slots do not fit twice next
-  // to the wider 1-CTA operand stages.
-  if constexpr (!(MODE == kModeFused && FMT == kFmtI8)) {
-    if (cfg.cg == 1 && cfg.bn == 256 && cfg.prof == kProfStream)
-      return launch_gemm_t<MODE, FMT, 256, kProfStream, 1>(cfg, maps, p, stream);
-    if (cfg.cg == 1 && cfg.bn == 256 && cfg.prof == kProfMma)
-      return launch_gemm_t<MODE, FMT, 256, kProfMma, 1>(cfg, maps, p, stream);
+  switch (cfg.prof) {
+    case kProfStream: return launch_gemm_prof<MODE, FMT, kProfStream>(cfg, maps, p, stream);
+    case kProfMma: return launch_gemm_prof<MODE, FMT, kProfMma>(cfg, maps, p, stream);
+    case kProfBalanced: return launch_gemm_prof<MODE, FMT, kProfBalanced>(cfg, maps, p, stream);
   }
-  if (cfg.cg == 2 && cfg.bn == 256 && cfg.prof == kProfStream)
-    return launch_gemm_t<MODE, FMT, 256, kProfStream, 2>(cfg, maps, p, stream);
-  if (cfg.cg == 2 && cfg.bn == 256 && cfg.prof == kProfMma)
-    return launch_gemm_t<MODE, FMT, 256, kProfMma, 2>(cfg, maps, p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -20,11 +20,13 @@ constexpr int kNumThreads = 384;   // 4 role warps + 8 epilogue warps
 constexpr int kEpiThreads = 256;
 
 enum Mode : int { kModeFused = 0, kModeStoreG = 1 };
-// Pipeline profiles: kProfStream (small token counts, HBM-bound epilogue) keeps
-// two operand stages and gives the rest of shared memory to state slots;
-// kProfMma (large token counts, tensor-bound main loop) keeps as many operand
-// stages as fit next to two state slots.
-enum Prof : int { kProfStream = 0, kProfMma = 1 };
+// Pipeline profiles, i.e. how shared memory is split between operand stages
+// and state slots: kProfStream (small token counts, HBM-bound epilogue) keeps
+// two operand stages and gives the rest to state slots; kProfMma (large token
+// counts, tensor-bound main loop) keeps as many operand stages as fit next to
+// two state slots; kProfBalanced keeps as many stages as slots, for the range
+// where the main loop and the epilogue take about the same time.
+enum Prof : int { kProfStream = 0, kProfMma = 1, kProfBalanced = 2 };
 // Epilogue formats: fused moment formats 0..2 (fp32, bf16, int8); store-G dW
 // formats 0..1 (fp32, bf16).
 enum Fmt : int { kFmtF32 = 0, kFmtBF16 = 1, kFmtI8 = 2 };

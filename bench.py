@@ -364,13 +364,23 @@ def oracle_threads() -> int:
     return os.cpu_count() or 1
 
 
+def _oracle_rows_for(workload: str, target_s: float) -> int:
+    """Rows per projection for an oracle step of about target_s seconds: a
+    two-point fit (fixed cost of decoding X plus a cost per weight row)."""
+    times = {}
+    for r in (16, 64):
+        sample, _ = oracle_sample(workload, r)
+        t0 = time.perf_counter()
+        oracle_step(sample, 1)
+        times[r] = time.perf_counter() - t0
+    per_row = max((times[64] - times[16]) / 48.0, 1e-7)
+    fixed = max(times[16] - 16 * per_row, 0.0)
+    return max(1, min(14336, int((target_s - fixed) / per_row)))
+
+
 def time_oracle(workload: str, target_s: float):
     """Oracle TFLOP/s on a row sample sized for about target_s seconds."""
-    sample, bt = oracle_sample(workload, 8)
-    t0 = time.perf_counter()
-    oracle_step(sample, 1)
-    per_row = (time.perf_counter() - t0) / 8
-    rows = max(1, min(4096, int(target_s / max(per_row, 1e-6))))
+    rows = _oracle_rows_for(workload, target_s)
     sample, bt = oracle_sample(workload, rows)
     t0 = time.perf_counter()
     oracle_step(sample, 1)
@@ -380,7 +390,7 @@ def time_oracle(workload: str, target_s: float):
 
 
 def cpu_baseline_block(workload):
-    value, dt, rows, bt = time_oracle(workload, 12.0)
+    value, dt, rows, bt = time_oracle(workload, 10.0)
     return {"value": value, "unit": "TFLOP/s", "cores": oracle_threads(), "kind": "oracle",
             "sample": (f"one fp64 oracle step (numpy: BLAS matmul for G, then AdamW and rounding)"
                        f" on the first {rows} rows of each of the 7 projections at BT={bt}, "
@@ -393,11 +403,7 @@ def run_reference(args):
     cfg, bt, fmt, dy_std, spike = workload_spec(args.workload)
     budget_s = 120.0
     per_step = budget_s / max(1, args.steps + args.warmup)
-    sample, _ = oracle_sample(args.workload, 4)
-    t0 = time.perf_counter()
-    oracle_step(sample, 1)
-    per_row = (time.perf_counter() - t0) / 4
-    rows = max(1, min(4096, int(per_step / max(per_row, 1e-6))))
+    rows = _oracle_rows_for(args.workload, 0.6 * per_step)   # the fit runs slightly short
     sample, bt = oracle_sample(args.workload, rows)
     for t in range(args.warmup):
         oracle_step(sample, t + 1)

@@ -107,6 +107,35 @@ forge_status forge_wgrad_adamw(const void* X, const void* dY, void* W,
                                float weight_decay, int64_t step,
                                forge_moment_fmt fmt, forge_stream stream);
 
+/* Most layers one grouped call can step. */
+#define FORGE_MAX_GROUP 8
+
+/* One linear layer of a grouped call; the fields have the meaning of the
+ * same-named arguments of forge_wgrad_adamw. */
+typedef struct {
+  const void* X;        /* [bt, d_in]  bf16, read only (may be shared by layers) */
+  const void* dY;       /* [bt, d_out] bf16, read only                           */
+  void* W;              /* [d_out, d_in] bf16, updated in place                  */
+  forge_moment m, v;    /* moments (and int8 scales), updated in place           */
+  int64_t d_in, d_out;
+} forge_linear;
+
+/*
+ * forge_wgrad_adamw_grouped: forge_wgrad_adamw on n (1..FORGE_MAX_GROUP)
+ * independent linear layers with the same token count bt, hyperparameters,
+ * step and moment format, in ONE kernel launch whose persistent CTAs walk a
+ * single tile queue over all layers (largest first).  Results are those of n
+ * separate forge_wgrad_adamw calls, bit for bit.  Inputs may be shared between
+ * layers (e.g. the q, k, v projections read the same X); no layer's W, m, v or
+ * scales may overlap any layer's inputs or outputs (FORGE_ERR_ALIAS).
+ * FORGE_ERR_NULL if `layers` is NULL, FORGE_ERR_SHAPE if n is out of range;
+ * otherwise the errors of forge_wgrad_adamw.  Asynchronous on `stream`.
+ */
+forge_status forge_wgrad_adamw_grouped(const forge_linear* layers, int n, int64_t bt,
+                                       float lr, float beta1, float beta2, float eps,
+                                       float weight_decay, int64_t step,
+                                       forge_moment_fmt fmt, forge_stream stream);
+
 /*
  * forge_wgrad: the unfused gradient, dW = dY^T X stored to global memory
  * (the "store-G control" of the FORGE page's Appendix D).  It runs the same

@@ -95,3 +95,29 @@ def test_wgrad_and_adamw_argument_errors(L):
     assert L.forge_adamw(C, 0, C, m, v, 256, 128, 1e-3, 0.9, 0.999, 1e-8, 0.01, 1, 0, None) == 6
     assert L.forge_adamw(A, 3, C, m, v, 256, 128, 1e-3, 0.9, 0.999, 1e-8, 0.01, 1, 0, None) == 4
     assert L.forge_adamw(A, 0, C, m, v, 256, 128, 1e-3, 0.9, 0.999, 1e-8, 0.01, 0, 0, None) == 5
+
+
+def grouped(L, layers, bt=64, step=1, fmt=0):
+    arr = (F.ForgeLinear * max(1, len(layers)))(*layers)
+    return L.forge_wgrad_adamw_grouped(arr, len(layers), bt, 1e-3, 0.9, 0.999, 1e-8, 0.01, step,
+                                       fmt, None)
+
+
+def lin(X, dY, W, m, v, d_in=256, d_out=128, ms=None, vs=None):
+    return F.ForgeLinear(X, dY, W, F.ForgeMoment(m, ms), F.ForgeMoment(v, vs), d_in, d_out)
+
+
+G = 1 << 40
+
+
+def test_grouped_argument_errors(L):
+    assert L.forge_wgrad_adamw_grouped(None, 1, 64, 1e-3, 0.9, 0.999, 1e-8, 0.01, 1, 0, None) == 1
+    a = lin(A, B, C, D, D + G)
+    b = lin(A, B, C + 2 * G, D + 3 * G, D + 4 * G)     # shares X and dY with a: allowed
+    assert grouped(L, []) == 3                          # n = 0
+    assert grouped(L, [a] * 9) == 3                     # n > FORGE_MAX_GROUP
+    assert grouped(L, [a, lin(A, B, C, D + 5 * G, D + 6 * G)]) == 6   # two layers share W
+    assert grouped(L, [a, lin(C, B, C + 2 * G, D + 3 * G, D + 4 * G)]) == 6  # X of one is W of other
+    assert grouped(L, [a, lin(A, B, C + 2 * G, D + 3 * G, D + 4 * G, d_in=260)]) == 3
+    assert grouped(L, [a, b], step=0) == 5
+    assert grouped(L, [a, b]) in (0, 7, 10)            # valid: stops at the device query here

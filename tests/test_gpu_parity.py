@@ -234,3 +234,58 @@ def test_bounded_wait_reports_timeout_and_recovers():
     m0, v0 = O.zero_moment(0, d_out, d_in), O.zero_moment(0, d_out, d_in)
     gw, gm, gv = gpu_fused(s.x, s.dy, w, m0, v0, TINY, 1)
     check_step(gw, gm, gv, ref_inputs(s.x, s.dy, w, m0, v0), TINY, 1, 0, bt, label="after")
+
+
+def _group_case(fmt, shapes, bt, share_x, seed):
+    """Host state for several layers; layers with the same d_in share X when
+    share_x (as q, k, v do)."""
+    layers = []
+    xs = {}
+    rng = np.random.default_rng(seed)
+    for i, (d_out, d_in) in enumerate(shapes):
+        s = make_step_inputs(20 + seed, i, 1, bt, d_in, d_out, dy_std=1e-3, with_w=True,
+                             spike_frac=0.01)
+        x = xs.setdefault(d_in, s.x) if share_x else s.x
+        m = O.encode_moment(fmt, rng.normal(0, 1e-4, (d_out, d_in)), False)
+        v = O.encode_moment(fmt, rng.uniform(1e-10, 1e-8, (d_out, d_in)), True)
+        layers.append(dict(x=x, dy=s.dy, w=bf16_bits(s.w), m=m, v=v))
+    return layers
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("bt", [200, 2048])
+def test_grouped_equals_separate_calls_bitwise(fmt, bt):
+    shapes = [(392, 256), (1024, 512), (136, 256), (256, 384), (512, 512)]
+    layers = _group_case(fmt, shapes, bt, share_x=True, seed=1)
+    sep = [gpu_fused(l["x"], l["dy"], l["w"], l["m"], l["v"], TINY, 3) for l in layers]
+    dev = []
+    xdev = {}
+    for l in layers:
+        W, md, vd, ms, vs = dev_state(l["w"], l["m"], l["v"])
+        X = xdev.setdefault(id(l["x"]), l["x"].to(DEV))
+        dev.append(dict(X=X, dY=l["dy"].to(DEV), W=W, m=md, v=vd, m_scale=ms, v_scale=vs))
+    F.wgrad_adamw_grouped(dev, step=3, **hyper_kwargs(TINY))
+    assert F.device_error() == 0
+    from .gpu_util import mom_from_dev
+    for a, d in zip(sep, dev):
+        assert np.array_equal(a[0], bf16_bits(d["W"].cpu()))
+        assert same_moment(a[1], mom_from_dev(fmt, d["m"], d["m_scale"]))
+        assert same_moment(a[2], mom_from_dev(fmt, d["v"], d["v_scale"]))
+
+
+def test_grouped_against_oracle_all_profiles(profile):
+    fmt = O.FMT_FP32
+    shapes = [(264, 136), (128, 256), (392, 264)]
+    bt = 130
+    layers = _group_case(fmt, shapes, bt, share_x=False, seed=2)
+    dev = []
+    for l in layers:
+        W, md, vd, ms, vs = dev_state(l["w"], l["m"], l["v"])
+        dev.append(dict(X=l["x"].to(DEV), dY=l["dy"].to(DEV), W=W, m=md, v=vd))
+    F.wgrad_adamw_grouped(dev, step=5, **hyper_kwargs(TINY))
+    assert F.device_error() == 0
+    from .gpu_util import mom_from_dev
+    for l, d in zip(layers, dev):
+        ref = ref_inputs(l["x"], l["dy"], l["w"], l["m"], l["v"])
+        check_step(bf16_bits(d["W"].cpu()), mom_from_dev(fmt, d["m"], None),
+                   mom_from_dev(fmt, d["v"], None), ref, TINY, 5, fmt, bt, label="grouped")

@@ -14,29 +14,24 @@
 
 namespace forge {
 
-cudaError_t launch_gemm_fused_f32(const GemmConfig&, const GemmMaps&, const GemmParams&,
-                                  cudaStream_t);
-cudaError_t launch_gemm_fused_bf16(const GemmConfig&, const GemmMaps&, const GemmParams&,
-                                   cudaStream_t);
-cudaError_t launch_gemm_fused_i8(const GemmConfig&, const GemmMaps&, const GemmParams&,
-                                 cudaStream_t);
-cudaError_t launch_gemm_store_f32(const GemmConfig&, const GemmMaps&, const GemmParams&,
-                                  cudaStream_t);
-cudaError_t launch_gemm_store_bf16(const GemmConfig&, const GemmMaps&, const GemmParams&,
-                                   cudaStream_t);
+cudaError_t launch_gemm_fused_f32(const GemmConfig&, const GemmArgs&, cudaStream_t);
+cudaError_t launch_gemm_fused_bf16(const GemmConfig&, const GemmArgs&, cudaStream_t);
+cudaError_t launch_gemm_fused_i8(const GemmConfig&, const GemmArgs&, cudaStream_t);
+cudaError_t launch_gemm_store_f32(const GemmConfig&, const GemmArgs&, cudaStream_t);
+cudaError_t launch_gemm_store_bf16(const GemmConfig&, const GemmArgs&, cudaStream_t);
 
-cudaError_t launch_gemm(int mode, int fmt, const GemmConfig& cfg, const GemmMaps& maps,
-                        const GemmParams& p, cudaStream_t stream) {
+cudaError_t launch_gemm(int mode, int fmt, const GemmConfig& cfg, const GemmArgs& args,
+                        cudaStream_t stream) {
   if (mode == kModeFused) {
     switch (fmt) {
-      case kFmtF32: return launch_gemm_fused_f32(cfg, maps, p, stream);
-      case kFmtBF16: return launch_gemm_fused_bf16(cfg, maps, p, stream);
-      case kFmtI8: return launch_gemm_fused_i8(cfg, maps, p, stream);
+      case kFmtF32: return launch_gemm_fused_f32(cfg, args, stream);
+      case kFmtBF16: return launch_gemm_fused_bf16(cfg, args, stream);
+      case kFmtI8: return launch_gemm_fused_i8(cfg, args, stream);
     }
   } else {
     switch (fmt) {
-      case kFmtF32: return launch_gemm_store_f32(cfg, maps, p, stream);
-      case kFmtBF16: return launch_gemm_store_bf16(cfg, maps, p, stream);
+      case kFmtF32: return launch_gemm_store_f32(cfg, args, stream);
+      case kFmtBF16: return launch_gemm_store_bf16(cfg, args, stream);
     }
   }
   return cudaErrorInvalidValue;
@@ -246,7 +241,7 @@ AdamWConsts make_consts(float lr, float b1, float b2, float eps, float wd, int64
 // operand from shared memory: balanced depths up to a few thousand tokens,
 // then the deepest operand pipeline.  FORGE_PROFILE=stream|balanced|mma,
 // FORGE_CG=1|2 and FORGE_BN=128|256 override the choice.
-GemmConfig choose_config(int64_t bt, int64_t d_in, int64_t d_out, int fmt, int num_sms) {
+GemmConfig choose_config(int64_t bt, int fmt) {
   GemmConfig c;
   c.group_m = 8;
   if (bt <= 768) {
@@ -273,28 +268,45 @@ GemmConfig choose_config(int64_t bt, int64_t d_in, int64_t d_out, int fmt, int n
   }
   if (c.cg == 2) c.bn = 256;                    // pairs always use 256 x 256 tiles
   if (c.cg == 1 && fmt == kFmtI8) c.bn = 128;   // 1-CTA int8 only with 128-wide tiles
-  const int64_t tiles = ((d_out + kBM * c.cg - 1) / (kBM * c.cg)) * ((d_in + c.bn - 1) / c.bn);
-  const int64_t units = num_sms / c.cg;
-  c.grid = static_cast<int>(c.cg * (tiles < units ? tiles : units));
+  c.grid = 0;
   return c;
 }
 
-GemmParams base_params(int64_t bt, int64_t d_in, int64_t d_out, const GemmConfig& cfg,
-                       const DeviceInfo& d) {
+int64_t tiles_of(const GemmConfig& c, int64_t d_in, int64_t d_out) {
+  return ((d_out + kBM * c.cg - 1) / (kBM * c.cg)) * ((d_in + c.bn - 1) / c.bn);
+}
+
+// Persistent grid: one CTA (or CTA pair) per SM (pair of SMs), at most one per tile.
+void set_grid(GemmConfig& c, int64_t tiles, int num_sms) {
+  const int64_t units = num_sms / c.cg;
+  c.grid = static_cast<int>(c.cg * (tiles < units ? tiles : units));
+}
+
+GemmParams base_params(int64_t bt, const GemmConfig& cfg, const DeviceInfo& d) {
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
   p.bt = static_cast<int32_t>(bt);
-  p.d_in = static_cast<int32_t>(d_in);
-  p.d_out = static_cast<int32_t>(d_out);
-  p.tiles_m = static_cast<int32_t>((d_out + kBM * cfg.cg - 1) / (kBM * cfg.cg));
-  p.tiles_n = static_cast<int32_t>((d_in + cfg.bn - 1) / cfg.bn);
-  p.num_tiles = p.tiles_m * p.tiles_n;
   p.num_k = static_cast<int32_t>((bt + kBK - 1) / kBK);
   p.group_m = cfg.group_m;
   p.err = d.err_word;
   p.err_site = d.site_word;
   p.timeout_ns = g_wait_limit_ns;
   return p;
+}
+
+// Appends one linear layer to a launch's tile queue.
+void add_problem(GemmParams& p, const GemmConfig& cfg, int64_t d_in, int64_t d_out,
+                 float* m_scale, float* v_scale) {
+  GemmProblem& q = p.prob[p.nprob];
+  q.d_in = static_cast<int32_t>(d_in);
+  q.d_out = static_cast<int32_t>(d_out);
+  q.tiles_m = static_cast<int32_t>((d_out + kBM * cfg.cg - 1) / (kBM * cfg.cg));
+  q.tiles_n = static_cast<int32_t>((d_in + cfg.bn - 1) / cfg.bn);
+  q.tile_start = p.num_tiles;
+  q.m_scale = m_scale;
+  q.v_scale = v_scale;
+  p.num_tiles += q.tiles_m * q.tiles_n;
+  p.nprob += 1;
 }
 
 // Operand descriptors: dY [bt, d_out] and X [bt, d_in], boxes of 64 columns x
@@ -305,6 +317,63 @@ bool operand_maps(GemmMaps& maps, const void* X, const void* dY, int64_t bt, int
                  CU_TENSOR_MAP_SWIZZLE_128B) &&
          get_map(&maps.x, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_in, bt, d_in * 2, 64, kBK,
                  CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// State descriptors of one layer for the fused kernel: W (bf16) and the two
+// moments, boxes of one epilogue slice (32 columns, or 128 for int8) x 128 rows.
+bool state_maps(GemmMaps& maps, void* W, const forge_moment& m, const forge_moment& v,
+                int64_t d_in, int64_t d_out, forge_moment_fmt fmt) {
+  if (fmt == FORGE_MOM_INT8_B128) {
+    return get_map(&maps.w, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_in, d_out, d_in * 2, 64, kBM,
+                   CU_TENSOR_MAP_SWIZZLE_128B) &&
+           get_map(&maps.m, m.data, CU_TENSOR_MAP_DATA_TYPE_UINT8, d_in, d_out, d_in, 128, kBM,
+                   CU_TENSOR_MAP_SWIZZLE_128B) &&
+           get_map(&maps.v, v.data, CU_TENSOR_MAP_DATA_TYPE_UINT8, d_in, d_out, d_in, 128, kBM,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  const bool f32 = fmt == FORGE_MOM_FP32;
+  const CUtensorMapDataType mdt =
+      f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle msw = f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const int eb = f32 ? 4 : 2;
+  return get_map(&maps.w, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_in, d_out, d_in * 2, 32, kBM,
+                 CU_TENSOR_MAP_SWIZZLE_64B) &&
+         get_map(&maps.m, m.data, mdt, d_in, d_out, d_in * eb, 32, kBM, msw) &&
+         get_map(&maps.v, v.data, mdt, d_in, d_out, d_in * eb, 32, kBM, msw);
+}
+
+uint64_t state_bytes_of(const forge_linear& L, forge_moment_fmt fmt) {
+  const uint64_t n = static_cast<uint64_t>(L.d_in) * static_cast<uint64_t>(L.d_out);
+  return n * (2 + 2 * mom_elem_bytes(fmt));
+}
+
+// Checks one layer of a fused launch (everything but cross-layer aliasing).
+forge_status check_linear(const forge_linear& L, int64_t bt, forge_moment_fmt fmt) {
+  forge_status s = check_shape(bt, L.d_in, L.d_out);
+  if (s != FORGE_OK) return s;
+  if (bt > 0 && (!L.X || !L.dY)) return FORGE_ERR_NULL;
+  s = check_state(L.W, L.m, L.v, L.d_in, L.d_out, fmt);
+  if (s != FORGE_OK) return s;
+  if (bt > 0 && (!aligned16(L.X) || !aligned16(L.dY))) return FORGE_ERR_ALIGN;
+  return FORGE_OK;
+}
+
+// The outputs (W, m, v, scales) of layer b overlap an input or an output of layer a.
+bool layers_clash(const forge_linear& a, const forge_linear& b, int64_t bt, forge_moment_fmt fmt,
+                  bool same) {
+  if (bt > 0 && (input_overlaps_state(a.X, 2ull * bt * a.d_in, b.W, b.m, b.v, b.d_in, b.d_out, fmt) ||
+                 input_overlaps_state(a.dY, 2ull * bt * a.d_out, b.W, b.m, b.v, b.d_in, b.d_out,
+                                      fmt)))
+    return true;
+  if (same) return false;
+  const uint64_t n = static_cast<uint64_t>(a.d_in) * static_cast<uint64_t>(a.d_out);
+  const uint64_t nm = n * mom_elem_bytes(fmt);
+  const uint64_t ns = (fmt == FORGE_MOM_INT8_B128) ? n / 128 * 4 : 0;
+  return input_overlaps_state(a.W, 2 * n, b.W, b.m, b.v, b.d_in, b.d_out, fmt) ||
+         input_overlaps_state(a.m.data, nm, b.W, b.m, b.v, b.d_in, b.d_out, fmt) ||
+         input_overlaps_state(a.v.data, nm, b.W, b.m, b.v, b.d_in, b.d_out, fmt) ||
+         (ns && input_overlaps_state(a.m.scale, ns, b.W, b.m, b.v, b.d_in, b.d_out, fmt)) ||
+         (ns && input_overlaps_state(a.v.scale, ns, b.W, b.m, b.v, b.d_in, b.d_out, fmt));
 }
 
 int take_drop_flag() {
@@ -321,22 +390,20 @@ using namespace forge;
 
 extern "C" {
 
-forge_status forge_wgrad_adamw(const void* X, const void* dY, void* W, forge_moment m,
-                               forge_moment v, int64_t bt, int64_t d_in, int64_t d_out, float lr,
-                               float beta1, float beta2, float eps, float weight_decay,
-                               int64_t step, forge_moment_fmt fmt, forge_stream stream) {
-  forge_status s = check_shape(bt, d_in, d_out);
+forge_status forge_wgrad_adamw_grouped(const forge_linear* layers, int n, int64_t bt, float lr,
+                                       float beta1, float beta2, float eps, float weight_decay,
+                                       int64_t step, forge_moment_fmt fmt, forge_stream stream) {
+  if (!layers) return FORGE_ERR_NULL;
+  if (n < 1 || n > FORGE_MAX_GROUP) return FORGE_ERR_SHAPE;
+  for (int i = 0; i < n; ++i) {
+    forge_status s = check_linear(layers[i], bt, fmt);
+    if (s != FORGE_OK) return s;
+  }
+  forge_status s = check_hyper(lr, beta1, beta2, eps, weight_decay, step);
   if (s != FORGE_OK) return s;
-  if (bt > 0 && (!X || !dY)) return FORGE_ERR_NULL;
-  s = check_state(W, m, v, d_in, d_out, fmt);
-  if (s != FORGE_OK) return s;
-  if (bt > 0 && (!aligned16(X) || !aligned16(dY))) return FORGE_ERR_ALIGN;
-  s = check_hyper(lr, beta1, beta2, eps, weight_decay, step);
-  if (s != FORGE_OK) return s;
-  if (bt > 0 &&
-      (input_overlaps_state(X, 2ull * bt * d_in, W, m, v, d_in, d_out, fmt) ||
-       input_overlaps_state(dY, 2ull * bt * d_out, W, m, v, d_in, d_out, fmt)))
-    return FORGE_ERR_ALIAS;
+  for (int i = 0; i < n; ++i)
+    for (int j = 0; j < n; ++j)
+      if (layers_clash(layers[i], layers[j], bt, fmt, i == j)) return FORGE_ERR_ALIAS;
   DeviceInfo* d = nullptr;
   s = device_info(&d);
   if (s != FORGE_OK) return s;
@@ -344,43 +411,57 @@ forge_status forge_wgrad_adamw(const void* X, const void* dY, void* W, forge_mom
   const AdamWConsts h = make_consts(lr, beta1, beta2, eps, weight_decay, step);
   const int ifmt = static_cast<int>(fmt);
   if (bt == 0) {   // G = 0: the moments decay and W takes decay and the m-driven update
-    return launch_adamw(nullptr, 0, W, m.data, v.data, m.scale, v.scale, d_in, d_out, ifmt, h,
-                        d->num_sms, st) == cudaSuccess
-               ? FORGE_OK
-               : FORGE_ERR_LAUNCH;
+    for (int i = 0; i < n; ++i) {
+      const forge_linear& L = layers[i];
+      if (launch_adamw(nullptr, 0, L.W, L.m.data, L.v.data, L.m.scale, L.v.scale, L.d_in,
+                       L.d_out, ifmt, h, d->num_sms, st) != cudaSuccess)
+        return FORGE_ERR_LAUNCH;
+    }
+    return FORGE_OK;
   }
-  const GemmConfig cfg = choose_config(bt, d_in, d_out, ifmt, d->num_sms);
-  GemmMaps maps;
-  std::memset(&maps, 0, sizeof(maps));
-  bool ok = operand_maps(maps, X, dY, bt, d_in, d_out);
-  if (fmt == FORGE_MOM_INT8_B128) {
-    ok = ok &&
-         get_map(&maps.w, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_in, d_out, d_in * 2, 64, kBM,
-                 CU_TENSOR_MAP_SWIZZLE_128B) &&
-         get_map(&maps.m, m.data, CU_TENSOR_MAP_DATA_TYPE_UINT8, d_in, d_out, d_in, 128, kBM,
-                 CU_TENSOR_MAP_SWIZZLE_128B) &&
-         get_map(&maps.v, v.data, CU_TENSOR_MAP_DATA_TYPE_UINT8, d_in, d_out, d_in, 128, kBM,
-                 CU_TENSOR_MAP_SWIZZLE_128B);
-  } else {
-    const bool f32 = fmt == FORGE_MOM_FP32;
-    const CUtensorMapDataType mdt =
-        f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    const CUtensorMapSwizzle msw = f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    const int eb = f32 ? 4 : 2;
-    ok = ok &&
-         get_map(&maps.w, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_in, d_out, d_in * 2, 32, kBM,
-                 CU_TENSOR_MAP_SWIZZLE_64B) &&
-         get_map(&maps.m, m.data, mdt, d_in, d_out, d_in * eb, 32, kBM, msw) &&
-         get_map(&maps.v, v.data, mdt, d_in, d_out, d_in * eb, 32, kBM, msw);
+  GemmConfig cfg = choose_config(bt, ifmt);
+  // largest layers first, so the small ones fill the last wave
+  int order[FORGE_MAX_GROUP];
+  for (int i = 0; i < n; ++i) order[i] = i;
+  for (int i = 1; i < n; ++i)
+    for (int j = i; j > 0 && state_bytes_of(layers[order[j]], fmt) >
+                                 state_bytes_of(layers[order[j - 1]], fmt); --j) {
+      const int t = order[j];
+      order[j] = order[j - 1];
+      order[j - 1] = t;
+    }
+  GemmArgs args;
+  std::memset(&args, 0, sizeof(args));
+  args.p = base_params(bt, cfg, *d);
+  args.p.h = h;
+  for (int k = 0; k < n; ++k) {
+    const forge_linear& L = layers[order[k]];
+    GemmMaps& maps = args.maps[k];
+    if (!operand_maps(maps, L.X, L.dY, bt, L.d_in, L.d_out) ||
+        !state_maps(maps, L.W, L.m, L.v, L.d_in, L.d_out, fmt))
+      return FORGE_ERR_LAUNCH;
+    add_problem(args.p, cfg, L.d_in, L.d_out, L.m.scale, L.v.scale);
   }
-  if (!ok) return FORGE_ERR_LAUNCH;
-  GemmParams p = base_params(bt, d_in, d_out, cfg, *d);
-  p.h = h;
-  p.m_scale = m.scale;
-  p.v_scale = v.scale;
-  p.drop_first_arrival = take_drop_flag();
-  return launch_gemm(kModeFused, ifmt, cfg, maps, p, st) == cudaSuccess ? FORGE_OK
-                                                                         : FORGE_ERR_LAUNCH;
+  set_grid(cfg, args.p.num_tiles, d->num_sms);
+  args.p.drop_first_arrival = take_drop_flag();
+  return launch_gemm(kModeFused, ifmt, cfg, args, st) == cudaSuccess ? FORGE_OK
+                                                                      : FORGE_ERR_LAUNCH;
+}
+
+forge_status forge_wgrad_adamw(const void* X, const void* dY, void* W, forge_moment m,
+                               forge_moment v, int64_t bt, int64_t d_in, int64_t d_out, float lr,
+                               float beta1, float beta2, float eps, float weight_decay,
+                               int64_t step, forge_moment_fmt fmt, forge_stream stream) {
+  forge_linear L;
+  L.X = X;
+  L.dY = dY;
+  L.W = W;
+  L.m = m;
+  L.v = v;
+  L.d_in = d_in;
+  L.d_out = d_out;
+  return forge_wgrad_adamw_grouped(&L, 1, bt, lr, beta1, beta2, eps, weight_decay, step, fmt,
+                                   stream);
 }
 
 forge_status forge_wgrad(const void* X, const void* dY, void* dW, forge_dtype dw_dtype,
@@ -401,9 +482,10 @@ forge_status forge_wgrad(const void* X, const void* dY, void* dW, forge_dtype dw
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (bt == 0) return cudaMemsetAsync(dW, 0, nbytes, st) == cudaSuccess ? FORGE_OK : FORGE_ERR_CUDA;
   const int ifmt = dw_dtype == FORGE_DT_FP32 ? kFmtF32 : kFmtBF16;
-  const GemmConfig cfg = choose_config(bt, d_in, d_out, ifmt, d->num_sms);
-  GemmMaps maps;
-  std::memset(&maps, 0, sizeof(maps));
+  GemmConfig cfg = choose_config(bt, ifmt);
+  GemmArgs args;
+  std::memset(&args, 0, sizeof(args));
+  GemmMaps& maps = args.maps[0];
   bool ok = operand_maps(maps, X, dY, bt, d_in, d_out);
   if (dw_dtype == FORGE_DT_FP32)
     ok = ok && get_map(&maps.w, dW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d_in, d_out, d_in * 4, 32, kBM,
@@ -412,10 +494,12 @@ forge_status forge_wgrad(const void* X, const void* dY, void* dW, forge_dtype dw
     ok = ok && get_map(&maps.w, dW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_in, d_out, d_in * 2, 32,
                        kBM, CU_TENSOR_MAP_SWIZZLE_64B);
   if (!ok) return FORGE_ERR_LAUNCH;
-  GemmParams p = base_params(bt, d_in, d_out, cfg, *d);
-  p.drop_first_arrival = take_drop_flag();
-  return launch_gemm(kModeStoreG, ifmt, cfg, maps, p, st) == cudaSuccess ? FORGE_OK
-                                                                          : FORGE_ERR_LAUNCH;
+  args.p = base_params(bt, cfg, *d);
+  add_problem(args.p, cfg, d_in, d_out, nullptr, nullptr);
+  set_grid(cfg, args.p.num_tiles, d->num_sms);
+  args.p.drop_first_arrival = take_drop_flag();
+  return launch_gemm(kModeStoreG, ifmt, cfg, args, st) == cudaSuccess ? FORGE_OK
+                                                                       : FORGE_ERR_LAUNCH;
 }
 
 forge_status forge_adamw(const void* dW, forge_dtype dw_dtype, void* W, forge_moment m,
@@ -493,7 +577,8 @@ int forge_describe_config(int64_t bt, int64_t d_in, int64_t d_out, forge_moment_
       sms = n;
   }
   const int fm = static_cast<int>(fmt);
-  const GemmConfig c = choose_config(bt, d_in, d_out, fm, sms);
+  GemmConfig c = choose_config(bt, fm);
+  set_grid(c, tiles_of(c, d_in, d_out), sms);
   const int sw = slice_cols(kModeFused, fm);
   const int need = std::snprintf(buf, buf ? len : 0,
                                  "tile=%dx%d ctas=%d bk=%d slice=%d grid=%d group_m=%d threads=%d "

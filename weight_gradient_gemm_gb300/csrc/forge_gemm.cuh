@@ -131,14 +131,25 @@ static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, 
   }
 }
 
-__device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& tm, int& tn) {
-  const int per_group = p.group_m * p.tiles_n;
-  const int g = t / per_group;
+// Global tile index -> (layer, tile row, tile column).  Layers are laid out
+// one after another in the queue; inside a layer, groups of group_m tile rows
+// are walked column by column so that concurrent tiles share operand panels
+// in L2.
+__device__ __forceinline__ int tile_coords(int t, const GemmParams& p, int& tm, int& tn) {
+  int pi = 0;
+#pragma unroll
+  for (int i = 1; i < kMaxGroup; ++i)
+    if (i < p.nprob && t >= p.prob[i].tile_start) pi = i;
+  const GemmProblem& q = p.prob[pi];
+  const int lt = t - q.tile_start;
+  const int per_group = p.group_m * q.tiles_n;
+  const int g = lt / per_group;
   const int first_m = g * p.group_m;
-  const int gsize = min(p.tiles_m - first_m, p.group_m);
-  const int r = t - g * per_group;
+  const int gsize = min(q.tiles_m - first_m, p.group_m);
+  const int r = lt - g * per_group;
   tm = first_m + r % gsize;
   tn = r / gsize;
+  return pi;
 }
 
 // ---------------------------------------------------------------------------
@@ -390,7 +401,8 @@ __device__ __forceinline__ void epi_slice_store(uint32_t taddr, bool zero_grad, 
 // ---------------------------------------------------------------------------
 template <int MODE, int FMT, int BN, int PROF, int CG>
 __global__ void __launch_bounds__(kNumThreads, 1)
-    forge_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+    forge_gemm_kernel(const __grid_constant__ GemmArgs a) {
+  const GemmParams& p = a.p;
   using T = GemmTraits<MODE, FMT, BN, PROF, CG>;
   constexpr bool kPair = (CG == 2);
   extern __shared__ uint8_t smem_raw[];
@@ -449,12 +461,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     fence_mbarrier_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&maps.dy);
-    tma_prefetch_desc(&maps.x);
-    tma_prefetch_desc(&maps.w);
-    if (MODE == kModeFused) {
-      tma_prefetch_desc(&maps.m);
-      tma_prefetch_desc(&maps.v);
+    for (int i = 0; i < p.nprob; ++i) {
+      tma_prefetch_desc(&a.maps[i].dy);
+      tma_prefetch_desc(&a.maps[i].x);
+      tma_prefetch_desc(&a.maps[i].w);
+      if (MODE == kModeFused) {
+        tma_prefetch_desc(&a.maps[i].m);
+        tma_prefetch_desc(&a.maps[i].v);
+      }
     }
   }
   // the peer's barriers must be initialised before any cross-CTA arrival
@@ -484,7 +498,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       bool ok = true;
       for (int t = unit0; ok && t < p.num_tiles; t += units) {
         int tm, tn;
-        tile_coords(t, p, tm, tn);
+        const int pi = tile_coords(t, p, tm, tn);
+        const GemmMaps& maps = a.maps[pi];
+        const GemmProblem& pr = p.prob[pi];
+        (void)pr;
         for (int k = 0; k < p.num_k; ++k, ++cnt) {
           const int s = cnt % T::STAGES;
           const uint32_t ph = (cnt / T::STAGES) & 1u;
@@ -582,7 +599,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       bool ok = true;
       for (int t = unit0; ok && t < p.num_tiles; t += units) {
         int tm, tn;
-        tile_coords(t, p, tm, tn);
+        const int pi = tile_coords(t, p, tm, tn);
+        const GemmMaps& maps = a.maps[pi];
+        const GemmProblem& pr = p.prob[pi];
+        (void)pr;
         for (int s = 0; s < T::SLICES; ++s, ++cnt) {
           const int j = cnt % T::NS;
           const uint32_t ph = (cnt / T::NS) & 1u;
@@ -590,7 +610,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           const int x0 = tn * BN + s * T::SW;
           const int y0 = tm * T::TM + static_cast<int>(rank) * kBM;
           last_armed[j] = static_cast<int32_t>(cnt);   // latest phase started on slot j
-          if (x0 >= p.d_in || y0 >= p.d_out) {   // slice entirely outside the weight
+          if (x0 >= pr.d_in || y0 >= pr.d_out) {   // slice entirely outside the weight
             mbar_arrive(bar_sfull(j));
             continue;
           }
@@ -622,14 +642,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       bool ok = true;
       for (int t = unit0; ok && t < p.num_tiles; t += units) {
         int tm, tn;
-        tile_coords(t, p, tm, tn);
+        const int pi = tile_coords(t, p, tm, tn);
+        const GemmMaps& maps = a.maps[pi];
+        const GemmProblem& pr = p.prob[pi];
+        (void)pr;
         for (int s = 0; s < T::SLICES; ++s, ++cnt) {
           const int j = cnt % T::NS;
           const uint32_t ph = (cnt / T::NS) & 1u;
           if (!wait_bounded(bar_sdone(j), ph, wc, kSiteStoreSlotDone)) { ok = false; break; }
           const int x0 = tn * BN + s * T::SW;
           const int y0 = tm * T::TM + static_cast<int>(rank) * kBM;
-          if (x0 < p.d_in && y0 < p.d_out) {
+          if (x0 < pr.d_in && y0 < pr.d_out) {
             const uint32_t sl = base + T::OFF_SLOTS + j * T::SLOT_BYTES;
             if constexpr (T::I8) {
               tma_store_2d(&maps.w, x0, y0, sl);
@@ -657,13 +680,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const uint32_t row = q * 32 + lane;      // tile row = TMEM lane
     const bool zero_grad = (p.num_k == 0);
     float* xch = reinterpret_cast<float*>(gbase + T::OFF_XCH);
-    const int scale_cols = p.d_in / 128;
     uint32_t scnt = 0, xcnt = 0;
     int it = 0;
     bool ok = true;
     for (int t = unit0; ok && t < p.num_tiles; t += units, ++it) {
       int tm, tn;
-      tile_coords(t, p, tm, tn);
+      const int pi = tile_coords(t, p, tm, tn);
+      const GemmProblem& pr = p.prob[pi];
+      const int scale_cols = pr.d_in / 128;
       const int buf = it & 1;
       const uint32_t use = (it >> 1) & 1;
       bool good = wait_bounded(bar_tfull(buf), use, wc, kSiteEpiTmemFull);
@@ -680,16 +704,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if (!__all_sync(0xffffffffu, good)) { ok = false; break; }
         const int x0 = tn * BN + s * T::SW;
         const int y0 = tm * T::TM + static_cast<int>(rank) * kBM;
-        const bool active = x0 < p.d_in && y0 < p.d_out;
+        const bool active = x0 < pr.d_in && y0 < pr.d_out;
         uint8_t* slot = gbase + T::OFF_SLOTS + j * T::SLOT_BYTES;
         const uint32_t taddr =
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + s * T::SW + h * T::HALF;
         if constexpr (T::I8) {
-          const bool row_ok = active && (y0 + static_cast<int>(row)) < p.d_out;
+          const bool row_ok = active && (y0 + static_cast<int>(row)) < pr.d_out;
           const size_t sidx = row_ok ? static_cast<size_t>(y0 + row) * scale_cols + (x0 >> 7) : 0;
           const bool xok = epi_slice_fused_i8(taddr, zero_grad, row_ok, slot, xch, bar_xch,
                                               bar_xch_read, xcnt & 1u, wc, row, h,
-                                              p.m_scale + sidx, p.v_scale + sidx, p.h);
+                                              pr.m_scale + sidx, pr.v_scale + sidx, p.h);
           ++xcnt;
           if (!xok) { ok = false; break; }
         } else if (active) {
@@ -736,8 +760,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 }
 
 template <int MODE, int FMT, int BN, int PROF, int CG>
-cudaError_t launch_gemm_t(const GemmConfig& cfg, const GemmMaps& maps, const GemmParams& p,
-                          cudaStream_t stream) {
+cudaError_t launch_gemm_t(const GemmConfig& cfg, const GemmArgs& args, cudaStream_t stream) {
   using T = GemmTraits<MODE, FMT, BN, PROF, CG>;
   auto kern = forge_gemm_kernel<MODE, FMT, BN, PROF, CG>;
   static int attr_done[64] = {0};     // per device: attributes set, pair count known
@@ -777,33 +800,31 @@ cudaError_t launch_gemm_t(const GemmConfig& cfg, const GemmMaps& maps, const Gem
   }
   if (!cached && dev >= 0 && dev < 64) attr_done[dev] = 1;
   lc.gridDim = dim3(grid, 1, 1);
-  return cudaLaunchKernelEx(&lc, kern, maps, p);
+  return cudaLaunchKernelEx(&lc, kern, args);
 }
 
 template <int MODE, int FMT, int PROF>
-cudaError_t launch_gemm_prof(const GemmConfig& cfg, const GemmMaps& maps, const GemmParams& p,
-                             cudaStream_t stream) {
+cudaError_t launch_gemm_prof(const GemmConfig& cfg, const GemmArgs& args, cudaStream_t stream) {
   if (cfg.cg == 1 && cfg.bn == 128)
-    return launch_gemm_t<MODE, FMT, 128, PROF, 1>(cfg, maps, p, stream);
+    return launch_gemm_t<MODE, FMT, 128, PROF, 1>(cfg, args, stream);
   // 256-wide accumulators use all 512 tensor-memory columns (two buffers).
   // Not built for 1-CTA int8 moments, whose 64 KB state slots do not fit
   // twice next to the wider 1-CTA operand stages.
   if constexpr (!(MODE == kModeFused && FMT == kFmtI8)) {
     if (cfg.cg == 1 && cfg.bn == 256)
-      return launch_gemm_t<MODE, FMT, 256, PROF, 1>(cfg, maps, p, stream);
+      return launch_gemm_t<MODE, FMT, 256, PROF, 1>(cfg, args, stream);
   }
   if (cfg.cg == 2 && cfg.bn == 256)
-    return launch_gemm_t<MODE, FMT, 256, PROF, 2>(cfg, maps, p, stream);
+    return launch_gemm_t<MODE, FMT, 256, PROF, 2>(cfg, args, stream);
   return cudaErrorInvalidValue;
 }
 
 template <int MODE, int FMT>
-cudaError_t launch_gemm_fmt(const GemmConfig& cfg, const GemmMaps& maps, const GemmParams& p,
-                            cudaStream_t stream) {
+cudaError_t launch_gemm_fmt(const GemmConfig& cfg, const GemmArgs& args, cudaStream_t stream) {
   switch (cfg.prof) {
-    case kProfStream: return launch_gemm_prof<MODE, FMT, kProfStream>(cfg, maps, p, stream);
-    case kProfMma: return launch_gemm_prof<MODE, FMT, kProfMma>(cfg, maps, p, stream);
-    case kProfBalanced: return launch_gemm_prof<MODE, FMT, kProfBalanced>(cfg, maps, p, stream);
+    case kProfStream: return launch_gemm_prof<MODE, FMT, kProfStream>(cfg, args, stream);
+    case kProfMma: return launch_gemm_prof<MODE, FMT, kProfMma>(cfg, args, stream);
+    case kProfBalanced: return launch_gemm_prof<MODE, FMT, kProfBalanced>(cfg, args, stream);
   }
   return cudaErrorInvalidValue;
 }

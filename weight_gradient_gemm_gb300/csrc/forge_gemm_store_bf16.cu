@@ -4,9 +4,9 @@
 
 namespace forge {
 
-cudaError_t launch_gemm_store_bf16(const GemmConfig& cfg, const GemmMaps& maps,
-                                const GemmParams& p, cudaStream_t stream) {
-  return launch_gemm_fmt<kModeStoreG, kFmtBF16>(cfg, maps, p, stream);
+cudaError_t launch_gemm_store_bf16(const GemmConfig& cfg, const GemmArgs& args,
+                                cudaStream_t stream) {
+  return launch_gemm_fmt<kModeStoreG, kFmtBF16>(cfg, args, stream);
 }
 
 

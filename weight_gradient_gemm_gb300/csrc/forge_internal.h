@@ -31,13 +31,25 @@ enum Prof : int { kProfStream = 0, kProfMma = 1, kProfBalanced = 2 };
 // formats 0..1 (fp32, bf16).
 enum Fmt : int { kFmtF32 = 0, kFmtBF16 = 1, kFmtI8 = 2 };
 
-struct GemmParams {
-  int32_t bt, d_in, d_out;
-  int32_t tiles_m, tiles_n, num_tiles, num_k;
-  int32_t group_m;            // tile-order swizzle: rows of tiles per group
-  AdamWConsts h;
+// Most linear layers one launch can step (a grouped launch walks one tile
+// queue across all of them).
+constexpr int kMaxGroup = 8;
+
+// One linear layer of a launch.
+struct GemmProblem {
+  int32_t d_in, d_out;
+  int32_t tiles_m, tiles_n;
+  int32_t tile_start;         // first index of this layer's tiles in the launch's queue
   float* m_scale;             // int8 scales [d_out, d_in/128]
   float* v_scale;
+};
+
+struct GemmParams {
+  int32_t bt, num_k;          // shared token count of every layer in the launch
+  int32_t nprob, num_tiles;   // layers, and tiles over all of them
+  int32_t group_m;            // tile-order swizzle: rows of tiles per group
+  AdamWConsts h;
+  GemmProblem prob[kMaxGroup];
   int* err;                   // device error word
   int* err_site;              // device word: where a wait first timed out
   uint64_t timeout_ns;
@@ -47,6 +59,12 @@ struct GemmParams {
 struct GemmMaps {
   CUtensorMap dy, x;      // operands
   CUtensorMap w, m, v;    // fused: state; store-G: w is dW
+};
+
+// Everything a launch reads from its parameter space (about 5.5 KB).
+struct GemmArgs {
+  GemmMaps maps[kMaxGroup];
+  GemmParams p;
 };
 
 // Launch configuration chosen on the host.
@@ -65,8 +83,8 @@ __host__ __device__ constexpr int slice_cols(int mode, int fmt) {
 }
 
 // Launchers (one per instantiated kernel family); return a CUDA error.
-cudaError_t launch_gemm(int mode, int fmt, const GemmConfig& cfg, const GemmMaps& maps,
-                        const GemmParams& p, cudaStream_t stream);
+cudaError_t launch_gemm(int mode, int fmt, const GemmConfig& cfg, const GemmArgs& args,
+                        cudaStream_t stream);
 
 cudaError_t launch_adamw(const void* dW, int dw_fmt, void* W, void* m, void* v, float* m_scale,
                          float* v_scale, int64_t d_in, int64_t d_out, int fmt,

@@ -39,6 +39,14 @@ class ForgeMoment(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("scale", ctypes.c_void_p)]
 
 
+class ForgeLinear(ctypes.Structure):
+    _fields_ = [("X", ctypes.c_void_p), ("dY", ctypes.c_void_p), ("W", ctypes.c_void_p),
+                ("m", ForgeMoment), ("v", ForgeMoment), ("d_in", ctypes.c_int64),
+                ("d_out", ctypes.c_int64)]
+
+
+MAX_GROUP = 8
+
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
 
@@ -57,6 +65,9 @@ def lib() -> ctypes.CDLL:
             L.forge_wgrad_adamw.argtypes = [vp, vp, vp, ForgeMoment, ForgeMoment, i64, i64, i64,
                                             f32, f32, f32, f32, f32, i64, st, vp]
             L.forge_wgrad_adamw.restype = st
+            L.forge_wgrad_adamw_grouped.argtypes = [ctypes.POINTER(ForgeLinear), st, i64,
+                                                    f32, f32, f32, f32, f32, i64, st, vp]
+            L.forge_wgrad_adamw_grouped.restype = st
             L.forge_wgrad.argtypes = [vp, vp, vp, st, i64, i64, i64, vp]
             L.forge_wgrad.restype = st
             L.forge_adamw.argtypes = [vp, st, vp, ForgeMoment, ForgeMoment, i64, i64,
@@ -146,6 +157,35 @@ def wgrad_adamw(X: torch.Tensor, dY: torch.Tensor, W: torch.Tensor, m: torch.Ten
         _ptr(X), _ptr(dY), _ptr(W), _moment(m, m_scale), _moment(v, v_scale), bt, d_in, d_out,
         lr, beta1, beta2, eps, weight_decay, step, fmt, _stream(stream))
     _check(st, "forge_wgrad_adamw")
+
+
+def wgrad_adamw_grouped(layers, *, lr: float, beta1: float, beta2: float, eps: float,
+                        weight_decay: float, step: int, stream=None) -> None:
+    """The fused step on several linear layers (same token count, moment
+    format and hyperparameters) in one launch.  `layers` is a sequence of
+    dicts with keys X, dY, W, m, v and, for int8 moments, m_scale, v_scale."""
+    n = len(layers)
+    arr = (ForgeLinear * max(n, 1))()
+    fmt = None
+    bt = None
+    for i, ly in enumerate(layers):
+        for k in ("X", "dY", "W", "m", "v"):
+            _dense(ly[k], k)
+        f = moment_format(ly["m"])
+        if fmt is not None and f != fmt:
+            raise ValueError("all layers of a group need the same moment format")
+        fmt = f
+        b = ly["X"].shape[0]
+        if bt is not None and b != bt:
+            raise ValueError("all layers of a group need the same token count")
+        bt = b
+        arr[i] = ForgeLinear(_ptr(ly["X"]), _ptr(ly["dY"]), _ptr(ly["W"]),
+                             _moment(ly["m"], ly.get("m_scale")),
+                             _moment(ly["v"], ly.get("v_scale")),
+                             ly["X"].shape[1], ly["dY"].shape[1])
+    st = lib().forge_wgrad_adamw_grouped(arr, n, bt or 0, lr, beta1, beta2, eps, weight_decay,
+                                         step, fmt if fmt is not None else 0, _stream(stream))
+    _check(st, "forge_wgrad_adamw_grouped")
 
 
 def wgrad(X: torch.Tensor, dY: torch.Tensor, dW: torch.Tensor, stream=None) -> None:

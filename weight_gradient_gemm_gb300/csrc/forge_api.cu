@@ -249,7 +249,7 @@ GemmConfig choose_config(int64_t bt, int fmt) {
     c.prof = (fmt == kFmtBF16) ? kProfBalanced : kProfStream;
   } else {
     c.cg = 2;
-    const int64_t balanced_upto = (fmt == kFmtBF16) ? 3072 : (fmt == kFmtF32 ? 1536 : 0);
+    const int64_t balanced_upto = (fmt == kFmtBF16) ? 3072 : 1536;
     c.prof = bt <= balanced_upto ? kProfBalanced : kProfMma;
   }
   c.bn = (c.cg == 2) ? 256 : 128;
@@ -322,13 +322,14 @@ bool operand_maps(GemmMaps& maps, const void* X, const void* dY, int64_t bt, int
 // State descriptors of one layer for the fused kernel: W (bf16) and the two
 // moments, boxes of one epilogue slice (32 columns, or 128 for int8) x 128 rows.
 bool state_maps(GemmMaps& maps, void* W, const forge_moment& m, const forge_moment& v,
-                int64_t d_in, int64_t d_out, forge_moment_fmt fmt) {
+                int64_t d_in, int64_t d_out, forge_moment_fmt fmt, int prof) {
   if (fmt == FORGE_MOM_INT8_B128) {
-    return get_map(&maps.w, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_in, d_out, d_in * 2, 64, kBM,
+    const uint32_t rows = static_cast<uint32_t>(slot_rows(kModeFused, kFmtI8, prof));
+    return get_map(&maps.w, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_in, d_out, d_in * 2, 64, rows,
                    CU_TENSOR_MAP_SWIZZLE_128B) &&
-           get_map(&maps.m, m.data, CU_TENSOR_MAP_DATA_TYPE_UINT8, d_in, d_out, d_in, 128, kBM,
+           get_map(&maps.m, m.data, CU_TENSOR_MAP_DATA_TYPE_UINT8, d_in, d_out, d_in, 128, rows,
                    CU_TENSOR_MAP_SWIZZLE_128B) &&
-           get_map(&maps.v, v.data, CU_TENSOR_MAP_DATA_TYPE_UINT8, d_in, d_out, d_in, 128, kBM,
+           get_map(&maps.v, v.data, CU_TENSOR_MAP_DATA_TYPE_UINT8, d_in, d_out, d_in, 128, rows,
                    CU_TENSOR_MAP_SWIZZLE_128B);
   }
   const bool f32 = fmt == FORGE_MOM_FP32;
@@ -438,7 +439,7 @@ forge_status forge_wgrad_adamw_grouped(const forge_linear* layers, int n, int64_
     const forge_linear& L = layers[order[k]];
     GemmMaps& maps = args.maps[k];
     if (!operand_maps(maps, L.X, L.dY, bt, L.d_in, L.d_out) ||
-        !state_maps(maps, L.W, L.m, L.v, L.d_in, L.d_out, fmt))
+        !state_maps(maps, L.W, L.m, L.v, L.d_in, L.d_out, fmt, cfg.prof))
       return FORGE_ERR_LAUNCH;
     add_problem(args.p, cfg, L.d_in, L.d_out, L.m.scale, L.v.scale);
   }

@@ -42,7 +42,10 @@ constexpr int kSmemLimit = 232448;   // max dynamic shared memory per CTA (227 K
 template <int MODE, int FMT, int BN, int PROF, int CG = 1>
 struct GemmTraits {
   static constexpr int SW = slice_cols(MODE, FMT);     // columns per epilogue slice
-  static constexpr int SLICES = BN / SW;
+  static constexpr int RPS = slot_rows(MODE, FMT, PROF);   // rows per state slot
+  static constexpr int PARTS = kBM / RPS;              // slots per 128-row column slice
+  // slots per tile, ordered (column slice, part) with the part varying fastest
+  static constexpr int SLICES = PARTS * (BN / SW);
   static constexpr int HALF = SW / 2;                  // columns per epilogue thread per slice
   static constexpr int TM = kBM * CG;                  // weight rows per tile
   static constexpr int BNL = BN / CG;                  // B columns loaded per CTA
@@ -52,13 +55,13 @@ struct GemmTraits {
   static constexpr int W_ELEM = (MODE == kModeStoreG && FMT == kFmtF32) ? 4 : 2;
   static constexpr int MOM_ELEM =
       (MODE == kModeStoreG) ? 0 : (FMT == kFmtF32 ? 4 : (FMT == kFmtBF16 ? 2 : 1));
-  static constexpr int W_BYTES = kBM * SW * W_ELEM;
-  static constexpr int M_BYTES = kBM * SW * MOM_ELEM;
+  static constexpr int W_BYTES = RPS * SW * W_ELEM;
+  static constexpr int M_BYTES = RPS * SW * MOM_ELEM;
   static constexpr int SLOT_BYTES = W_BYTES + 2 * M_BYTES;
   static constexpr bool I8 = (MODE == kModeFused && FMT == kFmtI8);
   // int8 row-halves exchange: [2 halves][2 kinds][128 rows] floats
   static constexpr int XCH_BYTES = I8 ? 2 * 2 * kBM * 4 : 0;
-  static constexpr int MAX_BARS = 2 * 6 + 4 + 3 * 6 + 3;
+  static constexpr int MAX_BARS = 2 * 6 + 4 + 3 * 6 + 5;
   static constexpr int BUDGET = kSmemLimit - (8 * MAX_BARS + 16 + XCH_BYTES);
   static constexpr int NS_CAP = 6;
   static constexpr int stages_mma() {
@@ -80,7 +83,7 @@ struct GemmTraits {
   // shared-memory carve (offsets from the 1024-aligned base)
   static constexpr int OFF_SLOTS = STAGES * STAGE_BYTES;
   static constexpr int OFF_BARS = OFF_SLOTS + NS * SLOT_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 4 + 3 * NS + 3;
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + 3 * NS + 5;
   static constexpr int OFF_TMEM = OFF_BARS + 8 * NUM_BARS;
   static constexpr int OFF_ABORT = OFF_TMEM + 4;
   static constexpr int OFF_XCH = (OFF_ABORT + 4 + 15) & ~15;
@@ -93,6 +96,8 @@ struct GemmTraits {
   static_assert(BN % SW == 0 && BNL % 64 == 0, "tile width");
   static_assert(CG == 1 || (CG == 2 && BN == 256), "CTA pairs use 256 x 256 tiles");
   static_assert(TMEM_COLS <= 512, "tensor memory has 512 columns");
+  // with half-tile slots each half of the epilogue owns every other slot
+  static_assert(PARTS == 1 || (NS % PARTS == 0 && SLICES % PARTS == 0), "slot ownership");
 };
 
 struct WaitCtx {
@@ -282,16 +287,19 @@ __device__ __forceinline__ void store_codes32(uint8_t* box, uint32_t row, int ch
 // before writing it a thread waits until every thread has read the previous
 // block's values (bar_xch_read), so a fast thread cannot overwrite them.
 // Returns false (warp-uniform) if a wait timed out.
+// `row` is the thread's row inside the RPS-row slot, `trow` its TMEM lane.
+template <int RPS>
 __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, bool zero_grad, bool active,
                                                    uint8_t* slot, float* xch, uint32_t bar_xch,
                                                    uint32_t bar_xch_read, uint32_t xphase,
-                                                   const WaitCtx& wc,
-                                                   uint32_t row, int h, float* m_scale_rc,
+                                                   const WaitCtx& wc, uint32_t row, uint32_t trow,
+                                                   int h, float* m_scale_rc,
                                                    float* v_scale_rc, const AdamWConsts& hc) {
-  using T = GemmTraits<kModeFused, kFmtI8, 128, kProfStream>;
-  uint8_t* wbox = slot + h * (kBM * 64 * 2);   // box h: [128][64] bf16, 128-byte rows
-  uint8_t* mbox = slot + T::W_BYTES;           // [128][128] int8
-  uint8_t* vbox = mbox + T::M_BYTES;
+  constexpr int kWBytes = RPS * 128 * 2;
+  constexpr int kMBytes = RPS * 128;
+  uint8_t* wbox = slot + h * (RPS * 64 * 2);   // box h: [RPS][64] bf16, 128-byte rows
+  uint8_t* mbox = slot + kWBytes;              // [RPS][128] int8
+  uint8_t* vbox = mbox + kMBytes;
   float sm_old = 0.0f, sv_old = 0.0f;
   if (active) {
     sm_old = *m_scale_rc;
@@ -334,13 +342,13 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, bool zero_gra
   // combine the row's two halves
   bool ok = wait_bounded(bar_xch_read, xphase ^ 1u, wc, kSiteEpiExchange);
   if (!__all_sync(0xffffffffu, ok)) return false;
-  xch[(h * 2 + 0) * kBM + row] = amax_m;
-  xch[(h * 2 + 1) * kBM + row] = amax_r;
+  xch[(h * 2 + 0) * kBM + trow] = amax_m;
+  xch[(h * 2 + 1) * kBM + trow] = amax_r;
   mbar_arrive(bar_xch);
   ok = wait_bounded(bar_xch, xphase, wc, kSiteEpiExchange);
   if (!__all_sync(0xffffffffu, ok)) return false;
-  amax_m = fmaxf(amax_m, xch[((1 - h) * 2 + 0) * kBM + row]);
-  amax_r = fmaxf(amax_r, xch[((1 - h) * 2 + 1) * kBM + row]);
+  amax_m = fmaxf(amax_m, xch[((1 - h) * 2 + 0) * kBM + trow]);
+  amax_r = fmaxf(amax_r, xch[((1 - h) * 2 + 1) * kBM + trow]);
   mbar_arrive(bar_xch_read);
   const float inv_m = int8_inv_step(amax_m), inv_r = int8_inv_step(amax_r);
   const bool r_nz = amax_r > 0.0f;
@@ -435,8 +443,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   auto bar_sempty = [&](int j) { return bars + 8u * (2 * T::STAGES + 4 + T::NS + j); };
   auto bar_sdone = [&](int j) { return bars + 8u * (2 * T::STAGES + 4 + 2 * T::NS + j); };
   const uint32_t bar_drain = bars + 8u * (2 * T::STAGES + 4 + 3 * T::NS);
-  const uint32_t bar_xch = bar_drain + 8u;
-  const uint32_t bar_xch_read = bar_drain + 16u;
+  // int8 row-half exchange barriers, one pair per slot part: [xch0, xch1, read0, read1]
+  const uint32_t bar_xch0 = bar_drain + 8u;
+  const uint32_t bar_xch_read0 = bar_drain + 24u;
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + T::OFF_ABORT);
   const WaitCtx wc{abort_flag, p.err, p.err_site, p.timeout_ns};
 
@@ -452,11 +461,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     for (int j = 0; j < T::NS; ++j) {
       mbar_init(bar_sfull(j), 1);
       mbar_init(bar_sempty(j), 1);
-      mbar_init(bar_sdone(j), kEpiThreads);
+      mbar_init(bar_sdone(j), kEpiThreads / T::PARTS);
     }
     mbar_init(bar_drain, 1);
-    mbar_init(bar_xch, kEpiThreads);
-    mbar_init(bar_xch_read, kEpiThreads);
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(bar_xch0 + 8u * g, kEpiThreads / T::PARTS);
+      mbar_init(bar_xch_read0 + 8u * g, kEpiThreads / T::PARTS);
+    }
     *abort_flag = 0u;
     fence_mbarrier_init();
   }
@@ -607,8 +618,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           const int j = cnt % T::NS;
           const uint32_t ph = (cnt / T::NS) & 1u;
           if (!wait_bounded(bar_sempty(j), ph ^ 1u, wc, kSiteLoaderEmpty)) { ok = false; break; }
-          const int x0 = tn * BN + s * T::SW;
-          const int y0 = tm * T::TM + static_cast<int>(rank) * kBM;
+          const int x0 = tn * BN + (s / T::PARTS) * T::SW;
+          const int y0 = tm * T::TM + static_cast<int>(rank) * kBM + (s % T::PARTS) * T::RPS;
           last_armed[j] = static_cast<int32_t>(cnt);   // latest phase started on slot j
           if (x0 >= pr.d_in || y0 >= pr.d_out) {   // slice entirely outside the weight
             mbar_arrive(bar_sfull(j));
@@ -618,7 +629,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           mbar_arrive_expect_tx(bar_sfull(j), T::SLOT_BYTES);
           if constexpr (FMT == kFmtI8) {
             tma_load_2d(slot, &maps.w, x0, y0, bar_sfull(j), pol);
-            tma_load_2d(slot + kBM * 64 * 2, &maps.w, x0 + 64, y0, bar_sfull(j), pol);
+            tma_load_2d(slot + T::RPS * 64 * 2, &maps.w, x0 + 64, y0, bar_sfull(j), pol);
           } else {
             tma_load_2d(slot, &maps.w, x0, y0, bar_sfull(j), pol);
           }
@@ -650,13 +661,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           const int j = cnt % T::NS;
           const uint32_t ph = (cnt / T::NS) & 1u;
           if (!wait_bounded(bar_sdone(j), ph, wc, kSiteStoreSlotDone)) { ok = false; break; }
-          const int x0 = tn * BN + s * T::SW;
-          const int y0 = tm * T::TM + static_cast<int>(rank) * kBM;
+          const int x0 = tn * BN + (s / T::PARTS) * T::SW;
+          const int y0 = tm * T::TM + static_cast<int>(rank) * kBM + (s % T::PARTS) * T::RPS;
           if (x0 < pr.d_in && y0 < pr.d_out) {
             const uint32_t sl = base + T::OFF_SLOTS + j * T::SLOT_BYTES;
             if constexpr (T::I8) {
               tma_store_2d(&maps.w, x0, y0, sl);
-              tma_store_2d(&maps.w, x0 + 64, y0, sl + kBM * 64 * 2);
+              tma_store_2d(&maps.w, x0 + 64, y0, sl + T::RPS * 64 * 2);
             } else {
               tma_store_2d(&maps.w, x0, y0, sl);
             }
@@ -678,6 +689,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const int q = warp & 3;                  // TMEM lane quadrant this warp may read
     const int h = (warp - 4) >> 2;           // column half of each slice
     const uint32_t row = q * 32 + lane;      // tile row = TMEM lane
+    // with half-tile slots, quadrants 0-1 take part 0 (even slots) and 2-3 part 1
+    const int part = (T::PARTS == 1) ? 0 : (q >> 1);
+    const uint32_t srow = (T::PARTS == 1) ? row : static_cast<uint32_t>((q & 1) * 32 + lane);
+    const uint32_t bar_xch = bar_xch0 + 8u * part;
+    const uint32_t bar_xch_read = bar_xch_read0 + 8u * part;
     const bool zero_grad = (p.num_k == 0);
     float* xch = reinterpret_cast<float*>(gbase + T::OFF_XCH);
     uint32_t scnt = 0, xcnt = 0;
@@ -695,6 +711,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       if (!__all_sync(0xffffffffu, good)) { ok = false; break; }
       tc_fence_after_sync();
       for (int s = 0; s < T::SLICES; ++s, ++scnt) {
+        if (T::PARTS > 1 && (s % T::PARTS) != part) continue;   // the other half's slot
         const int j = scnt % T::NS;
         const uint32_t ph = (scnt / T::NS) & 1u;
         if (MODE == kModeFused)
@@ -702,18 +719,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         else
           good = wait_bounded(bar_sempty(j), ph ^ 1u, wc, kSiteEpiSlotFree);
         if (!__all_sync(0xffffffffu, good)) { ok = false; break; }
-        const int x0 = tn * BN + s * T::SW;
-        const int y0 = tm * T::TM + static_cast<int>(rank) * kBM;
+        const int cb = s / T::PARTS;             // column slice
+        const int x0 = tn * BN + cb * T::SW;
+        const int y0 = tm * T::TM + static_cast<int>(rank) * kBM + part * T::RPS;
         const bool active = x0 < pr.d_in && y0 < pr.d_out;
         uint8_t* slot = gbase + T::OFF_SLOTS + j * T::SLOT_BYTES;
-        const uint32_t taddr =
-            tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + s * T::SW + h * T::HALF;
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN +
+                               cb * T::SW + h * T::HALF;
         if constexpr (T::I8) {
-          const bool row_ok = active && (y0 + static_cast<int>(row)) < pr.d_out;
-          const size_t sidx = row_ok ? static_cast<size_t>(y0 + row) * scale_cols + (x0 >> 7) : 0;
-          const bool xok = epi_slice_fused_i8(taddr, zero_grad, row_ok, slot, xch, bar_xch,
-                                              bar_xch_read, xcnt & 1u, wc, row, h,
-                                              pr.m_scale + sidx, pr.v_scale + sidx, p.h);
+          const bool row_ok = active && (y0 + static_cast<int>(srow)) < pr.d_out;
+          const size_t sidx = row_ok ? static_cast<size_t>(y0 + srow) * scale_cols + (x0 >> 7) : 0;
+          const bool xok = epi_slice_fused_i8<T::RPS>(
+              taddr, zero_grad, row_ok, slot, xch, bar_xch, bar_xch_read, xcnt & 1u, wc, srow,
+              row, h, pr.m_scale + sidx, pr.v_scale + sidx, p.h);
           ++xcnt;
           if (!xok) { ok = false; break; }
         } else if (active) {
@@ -722,7 +740,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           else
             epi_slice_store<FMT>(taddr, zero_grad, slot, row, h);
         }
-        if (s == T::SLICES - 1) {   // this warp has read the whole accumulator
+        if (s == T::SLICES - T::PARTS + part) {   // this warp has read the whole accumulator
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) {

@@ -82,6 +82,14 @@ __host__ __device__ constexpr int slice_cols(int mode, int fmt) {
   return (mode == kModeFused && fmt == kFmtI8) ? 128 : 32;
 }
 
+// Rows of one state slot.  A whole 128-row tile, except for int8 moments in
+// the profiles with deep operand pipelines: there a slot holds half a tile (64
+// rows, 32 KB instead of 64 KB), processed by the four epilogue warps of its
+// two TMEM lane quadrants, which leaves shared memory for two more stages.
+__host__ __device__ constexpr int slot_rows(int mode, int fmt, int prof) {
+  return (mode == kModeFused && fmt == kFmtI8 && prof != kProfStream) ? 64 : 128;
+}
+
 // Launchers (one per instantiated kernel family); return a CUDA error.
 cudaError_t launch_gemm(int mode, int fmt, const GemmConfig& cfg, const GemmArgs& args,
                         cudaStream_t stream);

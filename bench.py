@@ -353,6 +353,167 @@ def unfused_step(F, layer, step, dw):
 
 
 # ---------------------------------------------------------------------------
+# the full linear stack (32 layers x 7 projections)
+# ---------------------------------------------------------------------------
+
+STACK_LAYERS = 32
+
+
+class Stack:
+    """All 224 projections of Llama-3.1-8B, generated on the device (seeded
+    normal values of the same recipe; activations of this size are not drawn
+    on the host).  As in the model, q, k, v read one X per layer and gate, up
+    read one X per layer; o and down have their own."""
+
+    def __init__(self, bt, fmt, dy_std, dev, seed=5000):
+        from weight_gradient_gemm_gb300 import forge as F
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+
+        def normal(shape, std):
+            return (torch.randn(shape, generator=g, device=dev, dtype=torch.float32) * std
+                    ).to(torch.bfloat16)
+
+        self.bt, self.fmt = bt, fmt
+        self.layers = []
+        for _ in range(STACK_LAYERS):
+            xs = {"attn": normal((bt, 4096), 1.0), "o": normal((bt, 4096), 1.0),
+                  "mlp": normal((bt, 4096), 1.0), "down": normal((bt, 14336), 1.0)}
+            which = {"q": "attn", "k": "attn", "v": "attn", "o": "o", "gate": "mlp",
+                     "up": "mlp", "down": "down"}
+            items = []
+            for name, d_out, d_in in LLAMA31_8B_SHAPES:
+                m, v, ms, vs = F.alloc_moments(d_out, d_in, fmt, dev)
+                items.append(dict(name=name, d_in=d_in, d_out=d_out, X=xs[which[name]],
+                                  dY=normal((bt, d_out), dy_std), W=normal((d_out, d_in), 0.02),
+                                  m=m, v=v, m_scale=ms, v_scale=vs))
+            self.layers.append(items)
+
+    def linears(self):
+        return [it for layer in self.layers for it in layer]
+
+    def flops(self):
+        return sum(2.0 * self.bt * it["d_in"] * it["d_out"] for it in self.linears())
+
+    def params(self):
+        return sum(it["d_in"] * it["d_out"] for it in self.linears())
+
+    def alg_bytes(self):
+        # state once per linear; each distinct X once; each dY once
+        state = sum(it["d_in"] * it["d_out"] * STATE_BYTES[self.fmt] for it in self.linears())
+        xs = {id(it["X"]): it["X"].numel() * 2 for it in self.linears()}
+        dys = sum(it["dY"].numel() * 2 for it in self.linears())
+        return state + sum(xs.values()) + dys
+
+
+def stack_step(F, stack, step, events=None, stream=None):
+    """One optimizer step over the whole stack in backward order (layer 31
+    first); each layer's seven projections are one grouped launch."""
+    for i, layer in enumerate(reversed(stack.layers)):
+        if events is not None:
+            events[i][0].record(stream)
+        F.wgrad_adamw_grouped(layer, step=step, **HYPER)
+        if events is not None:
+            events[i][1].record(stream)
+
+
+def stack_unfused_step(F, stack, step, dw):
+    for layer in reversed(stack.layers):
+        for it in reversed(layer):        # down, up, gate, o, v, k, q
+            g = dw[:it["d_in"] * it["d_out"]].view(it["d_out"], it["d_in"])
+            F.wgrad(it["X"], it["dY"], g)
+            F.adamw(g, it["W"], it["m"], it["v"], step=step, m_scale=it["m_scale"],
+                    v_scale=it["v_scale"], **HYPER)
+
+
+def run_stack(args, dev):
+    """The full-stack workload: fused step vs the library's unfused path."""
+    from weight_gradient_gemm_gb300 import forge as F
+    F.lib()
+    parts = args.workload.split("_")
+    bt = int(parts[3][2:])
+    fmt = {"fp32": 0, "bf16": 1, "int8": 2}[parts[4]]
+    stack = Stack(bt, fmt, 1e-3, dev)
+    stream = torch.cuda.current_stream()
+    step = 0
+    for _ in range(args.warmup):
+        step += 1
+        stack_step(F, stack, step)
+    assert F.device_error() == 0
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(STACK_LAYERS)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev.index)
+    time.sleep(0.25)
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    t0.record(stream)
+    for k in range(args.steps):
+        step += 1
+        stack_step(F, stack, step, ev[k], stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.perf_counter()
+    sampler.stop()
+    st = F.device_error()
+    if st != 0:
+        raise RuntimeError(F.status_string(st))
+    ms = t0.elapsed_time(t1) / args.steps
+    kern_ms = sum(a.elapsed_time(b) for row in ev for (a, b) in row) / args.steps
+    # the unfused path: forge_wgrad (bf16 dW) + forge_adamw per linear
+    dw = torch.empty(max(it["d_in"] * it["d_out"] for it in stack.linears()),
+                     dtype=torch.bfloat16, device=dev)
+    step += 1
+    stack_unfused_step(F, stack, step, dw)
+    torch.cuda.synchronize()
+    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    unf_steps = max(2, min(args.steps, 5))
+    u0.record(stream)
+    for _ in range(unf_steps):
+        step += 1
+        stack_unfused_step(F, stack, step, dw)
+    u1.record(stream)
+    torch.cuda.synchronize()
+    assert F.device_error() == 0
+    unf_ms = u0.elapsed_time(u1) / unf_steps
+
+    peaks, peak_kind = measured_peaks()
+    flops, byts = stack.flops(), stack.alg_bytes()
+    t_hbm = byts / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops_sustained"] * 1e12)
+    kern_s_per_launch = kern_ms * 1e-3 / STACK_LAYERS
+    if t_hbm >= t_tc:
+        ach = byts / STACK_LAYERS / kern_s_per_launch / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "traffic": None,
+                "peak_kind": f"{peak_kind} (copy bandwidth)"}
+    else:
+        ach = flops / STACK_LAYERS / kern_s_per_launch / 1e12
+        pk = peaks["bf16_tflops_sustained"]
+        roof = {"bound": "tensor", "achieved": ach, "peak": pk, "unit": "TFLOP/s",
+                "frac": ach / pk, "traffic": None,
+                "peak_kind": f"{peak_kind} (cuBLAS bf16, sustained)"}
+    line = {
+        "metric": METRIC, "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded normal, generated on the device)",
+        "config": {"workload": args.workload, "bt": bt, "moments": FMT_NAMES[fmt],
+                   "linears": 7 * STACK_LAYERS, "params_per_step": stack.params(),
+                   "order": "backward: layer 31 to 0, one grouped launch per layer",
+                   "l2": f"inputs larger than L2: {byts / 1e9:.1f} GB per step"},
+        "roofline": roof,
+        "roofline_step": {"roofline_ms": max(t_hbm, t_tc) * 1e3,
+                          "frac_of_roofline": max(t_hbm, t_tc) * 1e3 / ms},
+        "unfused": {"ms_per_step": unf_ms, "fused_speedup": unf_ms / ms,
+                    "path": "forge_wgrad (bf16 dW) + forge_adamw, 448 launches per step"},
+        "gpu_launches": STACK_LAYERS * args.steps,
+        "clocks": sampler.summary(w0, w1),
+    }
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------------------
 # the CPU oracle (reported baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
@@ -461,7 +622,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="forge", choices=["forge", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    help="one of %s, or llama31_8b_layer_bt<BT>_<fp32|bf16|int8>" % sorted(WORKLOADS))
+                    help="one of %s, llama31_8b_layer_bt<BT>_<fp32|bf16|int8>, or the full "
+                         "224-linear stack llama31_8b_stack_bt<BT>_<fp32|bf16|int8>" % sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="",
                     help="comma-separated projections (q,k,v,o,gate,up,down) for small profiling "
@@ -488,6 +650,11 @@ def main():
         __graft_entry__.build()
     if world > 1:
         torch.distributed.barrier()
+    if args.workload.startswith("llama31_8b_stack_"):
+        if world > 1:
+            raise SystemExit("the stack workload runs on one GPU")
+        run_stack(args, dev)
+        return
     res = run_gpu(args, rank, world, dev)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -5,6 +5,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -65,7 +66,8 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
-// Cache of encoded descriptors keyed by everything that goes into them.
+// Cache of encoded descriptors keyed by everything that goes into them (a
+// whole model's linears fit; it is cleared if it ever grows past kCacheMax).
 struct MapKey {
   const void* ptr;
   int dtype;
@@ -78,14 +80,18 @@ struct MapKey {
            swizzle == o.swizzle;
   }
 };
-constexpr int kCacheSize = 256;
-struct MapEntry {
-  bool used = false;
-  MapKey key;
-  CUtensorMap map;
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    uint64_t h = reinterpret_cast<uintptr_t>(k.ptr) * 0x9E3779B97F4A7C15ull;
+    for (uint64_t v : {static_cast<uint64_t>(k.dtype), k.inner, k.outer, k.stride,
+                       static_cast<uint64_t>(k.box_inner) << 32 | k.box_outer,
+                       static_cast<uint64_t>(k.swizzle)})
+      h = (h ^ v) * 0x100000001B3ull;
+    return static_cast<size_t>(h);
+  }
 };
-MapEntry g_cache[kCacheSize];
-int g_cache_next = 0;
+constexpr size_t kCacheMax = 8192;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_cache;
 
 forge_status device_info(DeviceInfo** out) {
   int dev = 0;
@@ -125,11 +131,10 @@ bool get_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dt, uint64_t
   MapKey key{ptr, static_cast<int>(dt), inner, outer, stride_bytes, box_inner, box_outer,
              static_cast<int>(sw)};
   std::lock_guard<std::mutex> lk(g_mu);
-  for (int i = 0; i < kCacheSize; ++i) {
-    if (g_cache[i].used && g_cache[i].key == key) {
-      *out = g_cache[i].map;
-      return true;
-    }
+  auto it = g_cache.find(key);
+  if (it != g_cache.end()) {
+    *out = it->second;
+    return true;
   }
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {stride_bytes};
@@ -141,11 +146,8 @@ bool get_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dt, uint64_t
                         CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
-  MapEntry& e = g_cache[g_cache_next];
-  g_cache_next = (g_cache_next + 1) % kCacheSize;
-  e.used = true;
-  e.key = key;
-  e.map = m;
+  if (g_cache.size() >= kCacheMax) g_cache.clear();
+  g_cache.emplace(key, m);
   *out = m;
   return true;
 }

@@ -646,9 +646,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     __syncwarp();
   } else if (warp == 3) {
     // ------------------------------------------------------------ store warp
-    // TMA-stores each finished slice and frees its slot as soon as the store
-    // has read it, off the epilogue's critical path.
-    if (lane == 0) {
+    // Lane j TMA-stores the slices that land in state slot j and frees the
+    // slot as soon as its store has read it, off the epilogue's critical
+    // path; the lanes wait on their own bulk groups, so one slow store does
+    // not hold back the release of the other slots.
+    if (lane < T::NS) {
       uint32_t cnt = 0;
       bool ok = true;
       for (int t = unit0; ok && t < p.num_tiles; t += units) {
@@ -656,9 +658,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const int pi = tile_coords(t, p, tm, tn);
         const GemmMaps& maps = a.maps[pi];
         const GemmProblem& pr = p.prob[pi];
-        (void)pr;
         for (int s = 0; s < T::SLICES; ++s, ++cnt) {
           const int j = cnt % T::NS;
+          if (j != lane) continue;
           const uint32_t ph = (cnt / T::NS) & 1u;
           if (!wait_bounded(bar_sdone(j), ph, wc, kSiteStoreSlotDone)) { ok = false; break; }
           const int x0 = tn * BN + (s / T::PARTS) * T::SW;

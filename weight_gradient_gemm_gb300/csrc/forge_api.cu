@@ -240,8 +240,8 @@ AdamWConsts make_consts(float lr, float b1, float b2, float eps, float wd, int64
 // moments) or equal stage and slot depths (bf16 moments).  From about a
 // thousand tokens the main loop matters and 256 x 256 tiles on a CTA pair
 // (tcgen05 cta_group::2) win, since each SM then reads only half of the B
-// operand from shared memory: balanced depths up to a few thousand tokens,
-// then the deepest operand pipeline.  FORGE_PROFILE=stream|balanced|mma,
+// operand from shared memory: balanced depths up to 1536 tokens, then the
+// deepest operand pipeline.  FORGE_PROFILE=stream|balanced|mma,
 // FORGE_CG=1|2 and FORGE_BN=128|256 override the choice.
 GemmConfig choose_config(int64_t bt, int fmt) {
   GemmConfig c;
@@ -251,8 +251,7 @@ GemmConfig choose_config(int64_t bt, int fmt) {
     c.prof = (fmt == kFmtBF16) ? kProfBalanced : kProfStream;
   } else {
     c.cg = 2;
-    const int64_t balanced_upto = (fmt == kFmtBF16) ? 3072 : 1536;
-    c.prof = bt <= balanced_upto ? kProfBalanced : kProfMma;
+    c.prof = bt <= 1536 ? kProfBalanced : kProfMma;
   }
   c.bn = (c.cg == 2) ? 256 : 128;
   if (const char* e = std::getenv("FORGE_PROFILE")) {

@@ -602,7 +602,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   } else if (warp == 2) {
     // ------------------------------------------------------------ state loader
     if (MODE == kModeFused && lane == 0) {
-      const uint64_t pol = l2_policy_evict_first();
+      // Normal priority, not evict-first: a 32-column slice covers only half
+      // of a 128-byte line of W (and of bf16 m, v), and the slice after it
+      // reads the other half a moment later.  Marked evict-first, the line
+      // is often gone by then and DRAM serves it twice (measured: 24 % more
+      // DRAM reads at BT = 512 with fp32 moments, 69 % with bf16 moments);
+      // at normal priority the reads equal the state's size.
+      const uint64_t pol = l2_policy_evict_normal();
       uint32_t cnt = 0;
       int32_t last_armed[T::NS];
 #pragma unroll

@@ -287,7 +287,8 @@ GemmParams base_params(int64_t bt, const GemmConfig& cfg, const DeviceInfo& d) {
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
   p.bt = static_cast<int32_t>(bt);
-  p.num_k = static_cast<int32_t>((bt + kBK - 1) / kBK);
+  const int bk = bk_of(cfg.cg);
+  p.num_k = static_cast<int32_t>((bt + bk - 1) / bk);
   p.group_m = cfg.group_m;
   p.err = d.err_word;
   p.err_site = d.site_word;
@@ -311,12 +312,12 @@ void add_problem(GemmParams& p, const GemmConfig& cfg, int64_t d_in, int64_t d_o
 }
 
 // Operand descriptors: dY [bt, d_out] and X [bt, d_in], boxes of 64 columns x
-// kBK tokens with the 128-byte swizzle.
+// bk tokens with the 128-byte swizzle.
 bool operand_maps(GemmMaps& maps, const void* X, const void* dY, int64_t bt, int64_t d_in,
-                  int64_t d_out) {
-  return get_map(&maps.dy, dY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_out, bt, d_out * 2, 64, kBK,
+                  int64_t d_out, int bk) {
+  return get_map(&maps.dy, dY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_out, bt, d_out * 2, 64, bk,
                  CU_TENSOR_MAP_SWIZZLE_128B) &&
-         get_map(&maps.x, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_in, bt, d_in * 2, 64, kBK,
+         get_map(&maps.x, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_in, bt, d_in * 2, 64, bk,
                  CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
@@ -439,7 +440,7 @@ forge_status forge_wgrad_adamw_grouped(const forge_linear* layers, int n, int64_
   for (int k = 0; k < n; ++k) {
     const forge_linear& L = layers[order[k]];
     GemmMaps& maps = args.maps[k];
-    if (!operand_maps(maps, L.X, L.dY, bt, L.d_in, L.d_out) ||
+    if (!operand_maps(maps, L.X, L.dY, bt, L.d_in, L.d_out, bk_of(cfg.cg)) ||
         !state_maps(maps, L.W, L.m, L.v, L.d_in, L.d_out, fmt, cfg.prof))
       return FORGE_ERR_LAUNCH;
     add_problem(args.p, cfg, L.d_in, L.d_out, L.m.scale, L.v.scale);
@@ -488,7 +489,7 @@ forge_status forge_wgrad(const void* X, const void* dY, void* dW, forge_dtype dw
   GemmArgs args;
   std::memset(&args, 0, sizeof(args));
   GemmMaps& maps = args.maps[0];
-  bool ok = operand_maps(maps, X, dY, bt, d_in, d_out);
+  bool ok = operand_maps(maps, X, dY, bt, d_in, d_out, bk_of(cfg.cg));
   if (dw_dtype == FORGE_DT_FP32)
     ok = ok && get_map(&maps.w, dW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d_in, d_out, d_in * 4, 32, kBM,
                        CU_TENSOR_MAP_SWIZZLE_128B);
@@ -585,7 +586,7 @@ int forge_describe_config(int64_t bt, int64_t d_in, int64_t d_out, forge_moment_
   const int need = std::snprintf(buf, buf ? len : 0,
                                  "tile=%dx%d ctas=%d bk=%d slice=%d grid=%d group_m=%d threads=%d "
                                  "profile=%s",
-                                 kBM * c.cg, c.bn, c.cg, kBK, sw, c.grid, c.group_m, kNumThreads,
+                                 kBM * c.cg, c.bn, c.cg, bk_of(c.cg), sw, c.grid, c.group_m, kNumThreads,
                                  c.prof == kProfStream ? "stream"
                                  : c.prof == kProfMma  ? "mma"
                                                        : "balanced");

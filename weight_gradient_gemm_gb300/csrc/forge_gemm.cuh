@@ -9,7 +9,7 @@
 //
 // One persistent CTA per SM walks tiles t = blockIdx.x, blockIdx.x + gridDim.x,
 // ...  Warp roles (384 threads):
-//   warp 0      TMA producer: dY and X chunks of kBK tokens into a STAGES ring
+//   warp 0      TMA producer: dY and X chunks of BK tokens into a STAGES ring
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma 128 x BN x 16, bf16 in,
 //               fp32 accumulate, into one of two TMEM accumulators (the next
 //               tile's main loop overlaps this tile's epilogue)
@@ -20,7 +20,7 @@
 //
 // Operands: A = dY^T (M = weight rows) and B = X (N = weight columns) are both
 // contiguous along M/N, so both are fed to the MMA MN-major, straight from the
-// TMA boxes [kBK tokens][64 elements] with the 128-byte swizzle.
+// TMA boxes [BK tokens][64 elements] with the 128-byte swizzle.
 //
 // Every wait is bounded (GemmParams::timeout_ns).  When a bound runs out the
 // CTA raises a shared abort flag, records FORGE_ERR_DEVICE_TIMEOUT in the
@@ -49,8 +49,9 @@ struct GemmTraits {
   static constexpr int HALF = SW / 2;                  // columns per epilogue thread per slice
   static constexpr int TM = kBM * CG;                  // weight rows per tile
   static constexpr int BNL = BN / CG;                  // B columns loaded per CTA
-  static constexpr int A_BYTES = kBM * kBK * 2;
-  static constexpr int B_BYTES = BNL * kBK * 2;
+  static constexpr int BK = bk_of(CG);                 // tokens per operand stage
+  static constexpr int A_BYTES = kBM * BK * 2;
+  static constexpr int B_BYTES = BNL * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int W_ELEM = (MODE == kModeStoreG && FMT == kFmtF32) ? 4 : 2;
   static constexpr int MOM_ELEM =
@@ -64,20 +65,24 @@ struct GemmTraits {
   static constexpr int MAX_BARS = 2 * 6 + 4 + 3 * 6 + 5;
   static constexpr int BUDGET = kSmemLimit - (8 * MAX_BARS + 16 + XCH_BYTES);
   static constexpr int NS_CAP = 6;
+  // state slots that fit next to `st` operand stages, a multiple of PARTS
+  static constexpr int slots_beside(int st) {
+    const int n = (BUDGET - st * STAGE_BYTES) / SLOT_BYTES;
+    return ((n > NS_CAP ? NS_CAP : n) / PARTS) * PARTS;
+  }
   static constexpr int stages_mma() {
     int st = 6;
-    while (st > 2 && (BUDGET - st * STAGE_BYTES) / SLOT_BYTES < 2) --st;
+    while (st > 2 && slots_beside(st) < 2) --st;
     return st;
   }
   static constexpr int stages_balanced() {
     int st = 6;
-    while (st > 2 && (BUDGET - st * STAGE_BYTES) / SLOT_BYTES < st) --st;
+    while (st > 2 && slots_beside(st) < st) --st;
     return st;
   }
   static constexpr int STAGES =
       (PROF == kProfStream) ? 2 : (PROF == kProfMma ? stages_mma() : stages_balanced());
-  static constexpr int NS_FIT = (BUDGET - STAGES * STAGE_BYTES) / SLOT_BYTES;
-  static constexpr int NS = NS_FIT > NS_CAP ? NS_CAP : NS_FIT;
+  static constexpr int NS = slots_beside(STAGES);
   static_assert(NS >= 2, "shared memory does not fit two state slots");
   static constexpr int TMEM_COLS = 2 * BN;
   // shared-memory carve (offsets from the 1024-aligned base)
@@ -118,9 +123,14 @@ enum WaitSite : int {
 // false) when the CTA's abort flag is raised, if `honor_abort`, or when the
 // time limit runs out, in which case it raises the abort flag and records the
 // timeout in the device error word.
-static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtx& w,
-                                                 int site, bool honor_abort = true) {
-  if (mbar_try_wait(bar, parity)) return true;
+//
+// The first test is inlined; only a wait that has to spin calls the bounded
+// loop.  The MMA issuer passes through one wait per pipeline stage, and a
+// call there (frame set-up, argument moves) sits between two stages' MMAs
+// long enough for the tensor core to run dry: with the call the plain GEMM
+// main loop ran 11 % slower.
+static __device__ __noinline__ bool wait_spin(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                              int site, bool honor_abort) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
@@ -134,6 +144,11 @@ static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, 
       return false;
     }
   }
+}
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                             int site, bool honor_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_spin(bar, parity, w, site, honor_abort);
 }
 
 // Global tile index -> (layer, tile row, tile column).  Layers are laid out
@@ -525,19 +540,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             // both CTAs' loads complete on the leader's barrier, which expects both
             const uint32_t fb = mapa_shared(bar_full(s), 0);
             if (leader) mbar_arrive_expect_tx(bar_full(s), 2 * T::STAGE_BYTES);
-            tma_load_2d_pair(dst, &maps.dy, ya, k * kBK, fb, pol);
-            tma_load_2d_pair(dst + 64 * kBK * 2, &maps.dy, ya + 64, k * kBK, fb, pol);
+            tma_load_2d_pair(dst, &maps.dy, ya, k * T::BK, fb, pol);
+            tma_load_2d_pair(dst + 64 * T::BK * 2, &maps.dy, ya + 64, k * T::BK, fb, pol);
 #pragma unroll
             for (int hb = 0; hb < T::BNL / 64; ++hb)
-              tma_load_2d_pair(dst + T::A_BYTES + hb * 64 * kBK * 2, &maps.x, xb + hb * 64,
-                               k * kBK, fb, pol);
+              tma_load_2d_pair(dst + T::A_BYTES + hb * 64 * T::BK * 2, &maps.x, xb + hb * 64,
+                               k * T::BK, fb, pol);
           } else {
             mbar_arrive_expect_tx(bar_full(s), T::STAGE_BYTES);
-            tma_load_2d(dst, &maps.dy, ya, k * kBK, bar_full(s), pol);
-            tma_load_2d(dst + 64 * kBK * 2, &maps.dy, ya + 64, k * kBK, bar_full(s), pol);
+            tma_load_2d(dst, &maps.dy, ya, k * T::BK, bar_full(s), pol);
+            tma_load_2d(dst + 64 * T::BK * 2, &maps.dy, ya + 64, k * T::BK, bar_full(s), pol);
 #pragma unroll
             for (int hb = 0; hb < T::BNL / 64; ++hb)
-              tma_load_2d(dst + T::A_BYTES + hb * 64 * kBK * 2, &maps.x, xb + hb * 64, k * kBK,
+              tma_load_2d(dst + T::A_BYTES + hb * 64 * T::BK * 2, &maps.x, xb + hb * 64, k * T::BK,
                           bar_full(s), pol);
           }
           if (leader) last_armed[s] = static_cast<int32_t>(cnt);
@@ -554,7 +569,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
       constexpr uint32_t idesc = make_idesc_bf16_mn(T::TM, BN);
-      constexpr uint32_t kLBO = kBK * 128;   // next 64-element group along M/N
+      constexpr uint32_t kLBO = T::BK * 128;   // next 64-element group along M/N
       constexpr uint32_t kSBO = 1024;        // next 8-token group
       uint32_t cnt = 0;
       bool ok = true;
@@ -573,7 +588,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           const uint32_t a0 = base + s * T::STAGE_BYTES;
           const uint32_t b0 = a0 + T::A_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
+          for (int kk = 0; kk < T::BK / 16; ++kk) {
             const uint64_t ad = make_sdesc_mn_sw128(a0 + kk * 2048, kLBO, kSBO);
             const uint64_t bd = make_sdesc_mn_sw128(b0 + kk * 2048, kLBO, kSBO);
             if constexpr (kPair)

@@ -15,7 +15,8 @@ constexpr int kErrDeviceConfig = 11;
 
 // Tile geometry of the tensor-core kernels.
 constexpr int kBM = 128;     // weight rows per tile (MMA M)
-constexpr int kBK = 64;      // tokens per pipeline stage
+constexpr int kBK = 64;      // tokens per pipeline stage on one CTA
+constexpr int kBKPair = 64;  // tokens per pipeline stage on a CTA pair
 constexpr int kNumThreads = 384;   // 4 role warps + 8 epilogue warps
 constexpr int kEpiThreads = 256;
 
@@ -75,6 +76,10 @@ struct GemmConfig {
   int grid;      // persistent CTAs (even for CTA pairs)
   int group_m;
 };
+
+// Tokens per operand pipeline stage (the TMA box height of dY and X), used
+// both to encode the operand descriptors and inside the kernels.
+__host__ __device__ constexpr int bk_of(int cg) { return cg == 2 ? kBKPair : kBK; }
 
 // Box widths (columns per epilogue slice) by mode/format, used both to
 // encode the TMA descriptors and inside the kernels.

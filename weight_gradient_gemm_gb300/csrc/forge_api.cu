@@ -242,10 +242,9 @@ AdamWConsts make_consts(float lr, float b1, float b2, float eps, float wd, int64
 // (tcgen05 cta_group::2) win, since each SM then reads only half of the B
 // operand from shared memory: balanced depths up to 1536 tokens, then the
 // deepest operand pipeline.  FORGE_PROFILE=stream|balanced|mma,
-// FORGE_CG=1|2 and FORGE_BN=128|256 override the choice.
+// FORGE_CG=1|2, FORGE_BN=128|256 and FORGE_GROUP_M=1..64 override the choice.
 GemmConfig choose_config(int64_t bt, int fmt) {
   GemmConfig c;
-  c.group_m = 8;
   if (bt <= 768) {
     c.cg = 1;
     c.prof = (fmt == kFmtBF16) ? kProfBalanced : kProfStream;
@@ -269,6 +268,13 @@ GemmConfig choose_config(int64_t bt, int fmt) {
   }
   if (c.cg == 2) c.bn = 256;                    // pairs always use 256 x 256 tiles
   if (c.cg == 1 && fmt == kFmtI8) c.bn = 128;   // 1-CTA int8 only with 128-wide tiles
+  // Tile rows per raster group (the kernel's tile_coords): 4 for 128 x 128
+  // tiles, 1 (plain row-major order) for pairs, from the same sweeps.
+  c.group_m = (c.cg == 1) ? 4 : 1;
+  if (const char* e = std::getenv("FORGE_GROUP_M")) {
+    const int g = std::atoi(e);
+    if (g >= 1 && g <= 64) c.group_m = g;
+  }
   c.grid = 0;
   return c;
 }

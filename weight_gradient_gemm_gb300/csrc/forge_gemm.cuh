@@ -84,7 +84,10 @@ struct GemmTraits {
       (PROF == kProfStream) ? 2 : (PROF == kProfMma ? stages_mma() : stages_balanced());
   static constexpr int NS = slots_beside(STAGES);
   static_assert(NS >= 2, "shared memory does not fit two state slots");
-  static constexpr int TMEM_COLS = 2 * BN;
+  // int8 with 128-wide accumulators: the spare 256 tensor-memory columns hold
+  // the epilogue's m', r' between its two passes
+  static constexpr bool STASH = I8 && BN == 128;
+  static constexpr int TMEM_COLS = STASH ? 512 : 2 * BN;
   // shared-memory carve (offsets from the 1024-aligned base)
   static constexpr int OFF_SLOTS = STAGES * STAGE_BYTES;
   static constexpr int OFF_BARS = OFF_SLOTS + NS * SLOT_BYTES;
@@ -303,23 +306,25 @@ __device__ __forceinline__ void store_codes32(uint8_t* box, uint32_t row, int ch
 // block's values (bar_xch_read), so a fast thread cannot overwrite them.
 // Returns false (warp-uniform) if a wait timed out.
 // `row` is the thread's row inside the RPS-row slot, `trow` its TMEM lane.
-template <int RPS>
-__device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, bool zero_grad, bool active,
-                                                   uint8_t* slot, float* xch, uint32_t bar_xch,
-                                                   uint32_t bar_xch_read, uint32_t xphase,
-                                                   const WaitCtx& wc, uint32_t row, uint32_t trow,
-                                                   int h, float* m_scale_rc,
-                                                   float* v_scale_rc, const AdamWConsts& hc) {
+// STASH: the first pass parks m' and r' (fp32) in 128 spare tensor-memory
+// columns at `saddr` (this thread's lane) and the second pass reads them back
+// instead of dequantising and updating the moments a second time; possible
+// when the accumulators leave 256 of the 512 columns free (128-wide tiles).
+// sm_old, sv_old: the block's current scales (0 for rows outside the weight).
+template <int RPS, bool STASH>
+__device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, uint32_t saddr, bool zero_grad,
+                                                   bool active, uint8_t* slot, float* xch,
+                                                   uint32_t bar_xch, uint32_t bar_xch_read,
+                                                   uint32_t xphase, const WaitCtx& wc,
+                                                   uint32_t row, uint32_t trow, int h,
+                                                   float sm_old, float sv_old,
+                                                   float* m_scale_rc, float* v_scale_rc,
+                                                   const AdamWConsts& hc) {
   constexpr int kWBytes = RPS * 128 * 2;
   constexpr int kMBytes = RPS * 128;
   uint8_t* wbox = slot + h * (RPS * 64 * 2);   // box h: [RPS][64] bf16, 128-byte rows
   uint8_t* mbox = slot + kWBytes;              // [RPS][128] int8
   uint8_t* vbox = mbox + kMBytes;
-  float sm_old = 0.0f, sv_old = 0.0f;
-  if (active) {
-    sm_old = *m_scale_rc;
-    sv_old = *v_scale_rc;
-  }
   float amax_m = 0.0f, amax_r = 0.0f;
 #pragma unroll 1
   for (int c = 0; c < 2; ++c) {
@@ -348,12 +353,23 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, bool zero_gra
       amax_m = fmaxf(amax_m, fmaxf(fabsf(m0), fabsf(m1)));
       amax_r = fmaxf(amax_r, fmaxf(r0, r1));
       wo[i] = pack_bf16x2(w0, w1);
+      if constexpr (STASH) {   // the old codes are consumed: reuse their registers
+        qm[2 * i] = __float_as_int(m0);
+        qm[2 * i + 1] = __float_as_int(m1);
+        qv[2 * i] = __float_as_int(r0);
+        qv[2 * i + 1] = __float_as_int(r1);
+      }
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k)
       *reinterpret_cast<uint4*>(wbox + sw128_off(row, 4 * c + k)) =
           make_uint4(wo[4 * k], wo[4 * k + 1], wo[4 * k + 2], wo[4 * k + 3]);
+    if constexpr (STASH) {
+      tmem_st_x32(saddr + 64 * c, reinterpret_cast<const uint32_t(&)[32]>(qm));
+      tmem_st_x32(saddr + 64 * c + 32, reinterpret_cast<const uint32_t(&)[32]>(qv));
+    }
   }
+  if constexpr (STASH) tmem_st_wait();
   // combine the row's two halves
   bool ok = wait_bounded(bar_xch_read, xphase ^ 1u, wc, kSiteEpiExchange);
   if (!__all_sync(0xffffffffu, ok)) return false;
@@ -369,19 +385,31 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, bool zero_gra
   const bool r_nz = amax_r > 0.0f;
 #pragma unroll 1
   for (int c = 0; c < 2; ++c) {
-    uint32_t graw[32];
-    tmem_ld_x32(taddr + 32 * c, graw);
-    tmem_ld_wait();
     int qm[32], qv[32];
-    load_codes32(mbox, row, 4 * h + 2 * c, qm);
-    load_codes32(vbox, row, 4 * h + 2 * c, qv);
+    if constexpr (STASH) {
+      uint32_t ms[32], rs[32];
+      tmem_ld_x32(saddr + 64 * c, ms);
+      tmem_ld_x32(saddr + 64 * c + 32, rs);
+      tmem_ld_wait();
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      float g = zero_grad ? 0.0f : __uint_as_float(graw[i]);
-      float w = 0.0f, m = dequant_m(qm[i], sm_old), v = dequant_v(qv[i], sv_old), r;
-      adamw_elem(g, w, m, v, r, hc);
-      qm[i] = quant_m_code(m, inv_m);
-      qv[i] = quant_r_code(r, inv_r, r_nz);
+      for (int i = 0; i < 32; ++i) {
+        qm[i] = quant_m_code(__uint_as_float(ms[i]), inv_m);
+        qv[i] = quant_r_code(__uint_as_float(rs[i]), inv_r, r_nz);
+      }
+    } else {
+      uint32_t graw[32];
+      tmem_ld_x32(taddr + 32 * c, graw);
+      tmem_ld_wait();
+      load_codes32(mbox, row, 4 * h + 2 * c, qm);
+      load_codes32(vbox, row, 4 * h + 2 * c, qv);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float g = zero_grad ? 0.0f : __uint_as_float(graw[i]);
+        float w = 0.0f, m = dequant_m(qm[i], sm_old), v = dequant_v(qv[i], sv_old), r;
+        adamw_elem(g, w, m, v, r, hc);
+        qm[i] = quant_m_code(m, inv_m);
+        qv[i] = quant_r_code(r, inv_r, r_nz);
+      }
     }
     store_codes32(mbox, row, 4 * h + 2 * c, qm);
     store_codes32(vbox, row, 4 * h + 2 * c, qv);
@@ -718,6 +746,31 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const uint32_t bar_xch_read = bar_xch_read0 + 8u * part;
     const bool zero_grad = (p.num_k == 0);
     float* xch = reinterpret_cast<float*>(gbase + T::OFF_XCH);
+    // int8: the old block scales of this thread's row are read one tile ahead,
+    // so their global-memory latency is not paid at the start of each slice
+    constexpr int NCB = BN / T::SW;   // 1 or 2 for int8 (slices are selected, not indexed)
+    static_assert(!T::I8 || NCB <= 2, "int8 tiles hold at most two 128-column blocks");
+    float sc_m[NCB], sc_v[NCB], nx_m[NCB], nx_v[NCB];
+    auto load_scales = [&](int tt, float (&om)[NCB], float (&ov)[NCB]) {
+#pragma unroll
+      for (int cb = 0; cb < NCB; ++cb) om[cb] = ov[cb] = 0.0f;
+      if (tt >= p.num_tiles) return;
+      int tm2, tn2;
+      const GemmProblem& q2 = p.prob[tile_coords(tt, p, tm2, tn2)];
+      const int y = tm2 * T::TM + static_cast<int>(rank) * kBM + part * T::RPS +
+                    static_cast<int>(srow);
+      if (y >= q2.d_out) return;
+#pragma unroll
+      for (int cb = 0; cb < NCB; ++cb) {
+        const int x = tn2 * BN + cb * T::SW;
+        if (x < q2.d_in) {
+          const size_t idx = static_cast<size_t>(y) * (q2.d_in / 128) + (x >> 7);
+          om[cb] = q2.m_scale[idx];
+          ov[cb] = q2.v_scale[idx];
+        }
+      }
+    };
+    if constexpr (T::I8) load_scales(unit0, nx_m, nx_v);
     uint32_t scnt = 0, xcnt = 0;
     int it = 0;
     bool ok = true;
@@ -726,6 +779,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const int pi = tile_coords(t, p, tm, tn);
       const GemmProblem& pr = p.prob[pi];
       const int scale_cols = pr.d_in / 128;
+      if constexpr (T::I8) {
+#pragma unroll
+        for (int cb = 0; cb < NCB; ++cb) {
+          sc_m[cb] = nx_m[cb];
+          sc_v[cb] = nx_v[cb];
+        }
+        load_scales(t + units, nx_m, nx_v);
+      }
       const int buf = it & 1;
       const uint32_t use = (it >> 1) & 1;
       bool good = wait_bounded(bar_tfull(buf), use, wc, kSiteEpiTmemFull);
@@ -751,9 +812,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if constexpr (T::I8) {
           const bool row_ok = active && (y0 + static_cast<int>(srow)) < pr.d_out;
           const size_t sidx = row_ok ? static_cast<size_t>(y0 + srow) * scale_cols + (x0 >> 7) : 0;
-          const bool xok = epi_slice_fused_i8<T::RPS>(
-              taddr, zero_grad, row_ok, slot, xch, bar_xch, bar_xch_read, xcnt & 1u, wc, srow,
-              row, h, pr.m_scale + sidx, pr.v_scale + sidx, p.h);
+          const uint32_t saddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + 2 * BN +
+                                 static_cast<uint32_t>(h) * 128u;
+          const bool xok = epi_slice_fused_i8<T::RPS, T::STASH>(
+              taddr, saddr, zero_grad, row_ok, slot, xch, bar_xch, bar_xch_read, xcnt & 1u, wc,
+              srow, row, h, cb == 0 ? sc_m[0] : sc_m[NCB - 1], cb == 0 ? sc_v[0] : sc_v[NCB - 1],
+              pr.m_scale + sidx, pr.v_scale + sidx, p.h);
           ++xcnt;
           if (!xok) { ok = false; break; }
         } else if (active) {

@@ -83,7 +83,7 @@ __device__ __forceinline__ int quant_r_code(float r, float inv, bool nonzero_blo
   q = min(127, q);
   return nonzero_block ? max(1, q) : 0;
 }
-// Decoded int8 values: m = code * s_m; v = (code * s_r)^2.
+// Decoded int8 values: m = code * s; v = (code * s)^2.
 __device__ __forceinline__ float dequant_m(int code, float s) {
   return __fmul_rn(static_cast<float>(code), s);
 }

@@ -29,7 +29,8 @@ def _gpu():
 
 @pytest.fixture(params=[("stream", "128", "1"), ("mma", "128", "1"), ("balanced", "128", "1"),
                         ("stream", "256", "1"), ("mma", "256", "1"), ("stream", "256", "2"),
-                        ("balanced", "256", "2"), ("mma", "256", "2")],
+                        ("balanced", "256", "2"), ("mma", "256", "2"), ("deep", "128", "1"),
+                        ("deep", "256", "2")],
                 ids=lambda p: f"{p[0]}-bn{p[1]}-cta{p[2]}")
 def profile(request, monkeypatch):
     """Every pipeline profile, tile width and CTA grouping of the tensor-core

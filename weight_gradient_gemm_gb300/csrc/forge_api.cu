@@ -240,8 +240,9 @@ AdamWConsts make_consts(float lr, float b1, float b2, float eps, float wd, int64
 // moments) or equal stage and slot depths (bf16 moments).  From about a
 // thousand tokens the main loop matters and 256 x 256 tiles on a CTA pair
 // (tcgen05 cta_group::2) win, since each SM then reads only half of the B
-// operand from shared memory: balanced depths up to 1536 tokens, then the
-// deepest operand pipeline.  FORGE_PROFILE=stream|balanced|mma,
+// operand from shared memory: balanced depths up to 1536 tokens, then as many
+// operand stages as fit next to two state slots, and above 3072 tokens next
+// to two half-tile slots.  FORGE_PROFILE=stream|balanced|mma|deep,
 // FORGE_CG=1|2, FORGE_BN=128|256 and FORGE_GROUP_M=1..64 override the choice.
 GemmConfig choose_config(int64_t bt, int fmt) {
   GemmConfig c;
@@ -250,13 +251,14 @@ GemmConfig choose_config(int64_t bt, int fmt) {
     c.prof = (fmt == kFmtBF16) ? kProfBalanced : kProfStream;
   } else {
     c.cg = 2;
-    c.prof = bt <= 1536 ? kProfBalanced : kProfMma;
+    c.prof = bt <= 1536 ? kProfBalanced : (bt <= 3072 ? kProfMma : kProfDeep);
   }
   c.bn = (c.cg == 2) ? 256 : 128;
   if (const char* e = std::getenv("FORGE_PROFILE")) {
     if (std::strcmp(e, "stream") == 0) c.prof = kProfStream;
     if (std::strcmp(e, "mma") == 0) c.prof = kProfMma;
     if (std::strcmp(e, "balanced") == 0) c.prof = kProfBalanced;
+    if (std::strcmp(e, "deep") == 0) c.prof = kProfDeep;
   }
   if (const char* e = std::getenv("FORGE_CG")) {
     if (std::strcmp(e, "1") == 0) c.cg = 1;
@@ -345,10 +347,12 @@ bool state_maps(GemmMaps& maps, void* W, const forge_moment& m, const forge_mome
       f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const CUtensorMapSwizzle msw = f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   const int eb = f32 ? 4 : 2;
-  return get_map(&maps.w, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_in, d_out, d_in * 2, 32, kBM,
+  const uint32_t rows =
+      static_cast<uint32_t>(slot_rows(kModeFused, f32 ? kFmtF32 : kFmtBF16, prof));
+  return get_map(&maps.w, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_in, d_out, d_in * 2, 32, rows,
                  CU_TENSOR_MAP_SWIZZLE_64B) &&
-         get_map(&maps.m, m.data, mdt, d_in, d_out, d_in * eb, 32, kBM, msw) &&
-         get_map(&maps.v, v.data, mdt, d_in, d_out, d_in * eb, 32, kBM, msw);
+         get_map(&maps.m, m.data, mdt, d_in, d_out, d_in * eb, 32, rows, msw) &&
+         get_map(&maps.v, v.data, mdt, d_in, d_out, d_in * eb, 32, rows, msw);
 }
 
 uint64_t state_bytes_of(const forge_linear& L, forge_moment_fmt fmt) {
@@ -595,6 +599,7 @@ int forge_describe_config(int64_t bt, int64_t d_in, int64_t d_out, forge_moment_
                                  kBM * c.cg, c.bn, c.cg, bk_of(c.cg), sw, c.grid, c.group_m, kNumThreads,
                                  c.prof == kProfStream ? "stream"
                                  : c.prof == kProfMma  ? "mma"
+                                 : c.prof == kProfDeep ? "deep"
                                                        : "balanced");
   return need + 1;
 }

@@ -59,6 +59,9 @@ struct GemmTraits {
   static constexpr int W_BYTES = RPS * SW * W_ELEM;
   static constexpr int M_BYTES = RPS * SW * MOM_ELEM;
   static constexpr int SLOT_BYTES = W_BYTES + 2 * M_BYTES;
+  // every box of a slot starts 1024-byte aligned (the 128-byte swizzle's atom)
+  static_assert(W_BYTES % 1024 == 0 && M_BYTES % 1024 == 0 && SLOT_BYTES % 1024 == 0,
+                "state boxes must stay 1024-byte aligned");
   static constexpr bool I8 = (MODE == kModeFused && FMT == kFmtI8);
   // int8 row-halves exchange: [2 halves][2 kinds][128 rows] floats
   static constexpr int XCH_BYTES = I8 ? 2 * 2 * kBM * 4 : 0;
@@ -81,7 +84,8 @@ struct GemmTraits {
     return st;
   }
   static constexpr int STAGES =
-      (PROF == kProfStream) ? 2 : (PROF == kProfMma ? stages_mma() : stages_balanced());
+      (PROF == kProfStream) ? 2
+                            : (PROF == kProfMma || PROF == kProfDeep ? stages_mma() : stages_balanced());
   static constexpr int NS = slots_beside(STAGES);
   static_assert(NS >= 2, "shared memory does not fit two state slots");
   // int8 with 128-wide accumulators: the spare 256 tensor-memory columns hold
@@ -181,10 +185,13 @@ __device__ __forceinline__ int tile_coords(int t, const GemmParams& p, int& tm, 
 // ---------------------------------------------------------------------------
 
 // fp32 or bf16 moments; SW = 32, HALF = 16.
-template <int FMT>
+// `row` is the thread's row inside the RPS-row slot (its TMEM lane is in
+// `taddr`); the slot holds the W, m and v boxes of RPS rows back to back.
+template <int FMT, int RPS>
 __device__ __forceinline__ void epi_slice_fused_16(uint32_t taddr, bool zero_grad, uint8_t* slot,
                                                    uint32_t row, int h, const AdamWConsts& hc) {
-  using T = GemmTraits<kModeFused, FMT, 128, kProfStream>;
+  constexpr int kWBytes = RPS * 32 * 2;
+  constexpr int kMBytes = RPS * 32 * (FMT == kFmtF32 ? 4 : 2);
   uint32_t graw[16];
   tmem_ld_x16(taddr, graw);
   tmem_ld_wait();
@@ -192,9 +199,9 @@ __device__ __forceinline__ void epi_slice_fused_16(uint32_t taddr, bool zero_gra
 #pragma unroll
   for (int i = 0; i < 16; ++i) g[i] = zero_grad ? 0.0f : __uint_as_float(graw[i]);
 
-  uint8_t* wbox = slot;                 // [128][32] bf16: 64-byte rows
-  uint8_t* mbox = slot + T::W_BYTES;
-  uint8_t* vbox = mbox + T::M_BYTES;
+  uint8_t* wbox = slot;                 // [RPS][32] bf16: 64-byte rows
+  uint8_t* mbox = slot + kWBytes;
+  uint8_t* vbox = mbox + kMBytes;
   uint4 wq[2];
 #pragma unroll
   for (int c = 0; c < 2; ++c) wq[c] = *reinterpret_cast<const uint4*>(wbox + sw64_off(row, 2 * h + c));
@@ -204,7 +211,7 @@ __device__ __forceinline__ void epi_slice_fused_16(uint32_t taddr, bool zero_gra
     w[2 * i] = bf16_lo(wu[i]);
     w[2 * i + 1] = bf16_hi(wu[i]);
   }
-  if constexpr (FMT == kFmtF32) {        // [128][32] fp32: 128-byte rows
+  if constexpr (FMT == kFmtF32) {        // [RPS][32] fp32: 128-byte rows
     float4 mq[4], vq[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -215,7 +222,7 @@ __device__ __forceinline__ void epi_slice_fused_16(uint32_t taddr, bool zero_gra
     const float* vf = reinterpret_cast<const float*>(vq);
 #pragma unroll
     for (int i = 0; i < 16; ++i) { m[i] = mf[i]; v[i] = vf[i]; }
-  } else {                               // [128][32] bf16: 64-byte rows
+  } else {                               // [RPS][32] bf16: 64-byte rows
     uint4 mq[2], vq[2];
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
@@ -822,9 +829,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           if (!xok) { ok = false; break; }
         } else if (active) {
           if constexpr (MODE == kModeFused)
-            epi_slice_fused_16<FMT>(taddr, zero_grad, slot, row, h, p.h);
+            epi_slice_fused_16<FMT, T::RPS>(taddr, zero_grad, slot, srow, h, p.h);
           else
-            epi_slice_store<FMT>(taddr, zero_grad, slot, row, h);
+            epi_slice_store<FMT>(taddr, zero_grad, slot, srow, h);
         }
         if (s == T::SLICES - T::PARTS + part) {   // this warp has read the whole accumulator
           tc_fence_before_sync();
@@ -929,6 +936,13 @@ cudaError_t launch_gemm_fmt(const GemmConfig& cfg, const GemmArgs& args, cudaStr
     case kProfStream: return launch_gemm_prof<MODE, FMT, kProfStream>(cfg, args, stream);
     case kProfMma: return launch_gemm_prof<MODE, FMT, kProfMma>(cfg, args, stream);
     case kProfBalanced: return launch_gemm_prof<MODE, FMT, kProfBalanced>(cfg, args, stream);
+    case kProfDeep:
+      // int8 moments already use half-tile slots in the mma profile, and
+      // store-G has no state slots: both run the deep profile as mma
+      if constexpr (MODE == kModeFused && FMT != kFmtI8)
+        return launch_gemm_prof<MODE, FMT, kProfDeep>(cfg, args, stream);
+      else
+        return launch_gemm_prof<MODE, FMT, kProfMma>(cfg, args, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -26,8 +26,10 @@ enum Mode : int { kModeFused = 0, kModeStoreG = 1 };
 // two operand stages and gives the rest to state slots; kProfMma (large token
 // counts, tensor-bound main loop) keeps as many operand stages as fit next to
 // two state slots; kProfBalanced keeps as many stages as slots, for the range
-// where the main loop and the epilogue take about the same time.
-enum Prof : int { kProfStream = 0, kProfMma = 1, kProfBalanced = 2 };
+// where the main loop and the epilogue take about the same time; kProfDeep
+// (the largest token counts) keeps as many operand stages as fit next to two
+// half-tile state slots.
+enum Prof : int { kProfStream = 0, kProfMma = 1, kProfBalanced = 2, kProfDeep = 3 };
 // Epilogue formats: fused moment formats 0..2 (fp32, bf16, int8); store-G dW
 // formats 0..1 (fp32, bf16).
 enum Fmt : int { kFmtF32 = 0, kFmtBF16 = 1, kFmtI8 = 2 };
@@ -87,12 +89,14 @@ __host__ __device__ constexpr int slice_cols(int mode, int fmt) {
   return (mode == kModeFused && fmt == kFmtI8) ? 128 : 32;
 }
 
-// Rows of one state slot.  A whole 128-row tile, except for int8 moments in
-// the profiles with deep operand pipelines: there a slot holds half a tile (64
-// rows, 32 KB instead of 64 KB), processed by the four epilogue warps of its
-// two TMEM lane quadrants, which leaves shared memory for two more stages.
+// Rows of one state slot.  A whole 128-row tile, except in the deep profile
+// and for int8 moments outside the stream profile: there a slot holds half a
+// tile (64 rows; int8 32 KB instead of 64 KB, fp32 20 KB instead of 40 KB),
+// processed by the four epilogue warps of its two TMEM lane quadrants, which
+// leaves shared memory for more operand stages.
 __host__ __device__ constexpr int slot_rows(int mode, int fmt, int prof) {
-  return (mode == kModeFused && fmt == kFmtI8 && prof != kProfStream) ? 64 : 128;
+  return (mode == kModeFused &&
+          ((fmt == kFmtI8 && prof != kProfStream) || prof == kProfDeep)) ? 64 : 128;
 }
 
 // Launchers (one per instantiated kernel family); return a CUDA error.

@@ -351,11 +351,11 @@ def run_gpu(args, rank, world, dev):
     for k in range(e2e_steps):
         step += 1
         b = k & 1
-        if k + 1 < e2e_steps:
-            stage_inputs(1 - b)
         stream.wait_event(copied[b])
         F.wgrad_adamw_grouped(sets[b], step=step, stream=stream, **HYPER)
         consumed[b].record(stream)
+        if k + 1 < e2e_steps:         # issued while step k runs
+            stage_inputs(1 - b)
         st = F.device_error(stream)   # synchronises the step's stream, reads 4 bytes
         if st != 0:
             raise RuntimeError(F.status_string(st))

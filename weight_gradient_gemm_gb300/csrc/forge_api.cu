@@ -235,20 +235,26 @@ AdamWConsts make_consts(float lr, float b1, float b2, float eps, float wd, int64
 }
 
 // Tile configuration, from measured sweeps over the Llama-3.1-8B projections
-// on GB300.  At a few hundred tokens the step streams W, m, v through HBM:
-// 128 x 128 tiles on one CTA with a deep state pipeline (fp32 and int8
-// moments) or equal stage and slot depths (bf16 moments).  From about a
-// thousand tokens the main loop matters and 256 x 256 tiles on a CTA pair
-// (tcgen05 cta_group::2) win, since each SM then reads only half of the B
-// operand from shared memory: balanced depths up to 1536 tokens, then as many
-// operand stages as fit next to two state slots, and above 3072 tokens next
-// to two half-tile slots.  FORGE_PROFILE=stream|balanced|mma|deep,
-// FORGE_CG=1|2, FORGE_BN=128|256 and FORGE_GROUP_M=1..64 override the choice.
-GemmConfig choose_config(int64_t bt, int fmt) {
+// on GB300.  At a few hundred tokens the fused step streams W, m, v through
+// HBM: 128 x 128 tiles on one CTA, with two operand stages and four state
+// slots for fp32 moments up to 512 tokens, equal stage and slot depths
+// otherwise (int8 moments in half-tile slots).  From about a thousand tokens
+// (768 for bf16 moments) the main loop matters and 256 x 256 tiles on a CTA
+// pair (tcgen05 cta_group::2) win, since each SM then reads only half of the
+// B operand from shared memory: balanced depths up to 1536 tokens, then as
+// many operand stages as fit next to two state slots, and above 3072 tokens
+// next to two half-tile slots.  The store-G kernel (fmt = dW dtype) keeps the
+// 768-token split.  FORGE_PROFILE=stream|balanced|mma|deep, FORGE_CG=1|2,
+// FORGE_BN=128|256 and FORGE_GROUP_M=1..64 override the choice.
+GemmConfig choose_config(int64_t bt, int fmt, int mode) {
   GemmConfig c;
-  if (bt <= 768) {
+  const int64_t one_cta_upto = (mode == kModeFused && fmt == kFmtBF16) ? 640 : 768;
+  if (bt <= one_cta_upto) {
     c.cg = 1;
-    c.prof = (fmt == kFmtBF16) ? kProfBalanced : kProfStream;
+    if (mode == kModeFused)
+      c.prof = (fmt == kFmtF32 && bt <= 512) ? kProfStream : kProfBalanced;
+    else
+      c.prof = (fmt == kFmtBF16) ? kProfBalanced : kProfStream;
   } else {
     c.cg = 2;
     c.prof = bt <= 1536 ? kProfBalanced : (bt <= 3072 ? kProfMma : kProfDeep);
@@ -432,7 +438,7 @@ forge_status forge_wgrad_adamw_grouped(const forge_linear* layers, int n, int64_
     }
     return FORGE_OK;
   }
-  GemmConfig cfg = choose_config(bt, ifmt);
+  GemmConfig cfg = choose_config(bt, ifmt, kModeFused);
   // largest layers first, so the small ones fill the last wave
   int order[FORGE_MAX_GROUP];
   for (int i = 0; i < n; ++i) order[i] = i;
@@ -495,7 +501,7 @@ forge_status forge_wgrad(const void* X, const void* dY, void* dW, forge_dtype dw
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (bt == 0) return cudaMemsetAsync(dW, 0, nbytes, st) == cudaSuccess ? FORGE_OK : FORGE_ERR_CUDA;
   const int ifmt = dw_dtype == FORGE_DT_FP32 ? kFmtF32 : kFmtBF16;
-  GemmConfig cfg = choose_config(bt, ifmt);
+  GemmConfig cfg = choose_config(bt, ifmt, kModeStoreG);
   GemmArgs args;
   std::memset(&args, 0, sizeof(args));
   GemmMaps& maps = args.maps[0];
@@ -590,7 +596,7 @@ int forge_describe_config(int64_t bt, int64_t d_in, int64_t d_out, forge_moment_
       sms = n;
   }
   const int fm = static_cast<int>(fmt);
-  GemmConfig c = choose_config(bt, fm);
+  GemmConfig c = choose_config(bt, fm, kModeFused);
   set_grid(c, tiles_of(c, d_in, d_out), sms);
   const int sw = slice_cols(kModeFused, fm);
   const int need = std::snprintf(buf, buf ? len : 0,

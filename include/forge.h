@@ -24,6 +24,14 @@
  * allocates no device memory in any call; it keeps a small host-side cache of
  * TMA descriptors keyed by pointer and shape.
  *
+ * Tuning.  The tile configuration is chosen from the token count and the
+ * moment format (forge_describe_config shows it).  For measurements, these
+ * environment variables, read at each call, override the choice:
+ * FORGE_PROFILE=stream|balanced|mma|deep (how shared memory is split between
+ * operand stages and state slots), FORGE_CG=1|2 (one CTA or a CTA pair per
+ * tile), FORGE_BN=128|256 (accumulator width on one CTA), FORGE_GROUP_M=1..64
+ * (tile rows per raster group).  Results do not depend on them.
+ *
  * Errors.  Argument errors are returned synchronously, before anything is
  * enqueued.  Launch failures return FORGE_ERR_LAUNCH.  Kernels never trap:
  * every wait inside a kernel is bounded, and when a bound runs out the kernel

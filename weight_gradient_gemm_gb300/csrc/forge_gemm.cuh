@@ -7,16 +7,23 @@
 //   kModeStoreG: the same main loop, storing G (fp32 or bf16): the unfused
 //                gradient ("store-G control", Appendix D).
 //
-// One persistent CTA per SM walks tiles t = blockIdx.x, blockIdx.x + gridDim.x,
-// ...  Warp roles (384 threads):
-//   warp 0      TMA producer: dY and X chunks of BK tokens into a STAGES ring
-//   warp 1      TMEM owner and MMA issuer: tcgen05.mma 128 x BN x 16, bf16 in,
-//               fp32 accumulate, into one of two TMEM accumulators (the next
-//               tile's main loop overlaps this tile's epilogue)
+// One persistent CTA per SM (or one CTA pair per two SMs, CG = 2) walks the
+// tile queue t = unit, unit + units, ... over all layers of the launch.
+// Warp roles (384 threads):
+//   warp 0      TMA producer: dY and X chunks of BK tokens into a STAGES ring,
+//               one lane per box so a stage is one warp-wide TMA issue
+//   warp 1      TMEM owner and MMA issuer: tcgen05.mma 128 x BN x 16 (256 x BN
+//               on a pair), bf16 in, fp32 accumulate, into one of two TMEM
+//               accumulators (the next tile's main loop overlaps this tile's
+//               epilogue)
 //   warp 2      state loader (fused mode): W/m/v slices of the tile, TMA into
 //               an NS-slot ring, issued ahead of the epilogue
+//   warp 3      store warp: lane j TMA-stores what the epilogue left in slot j
+//               and frees the slot once the store has read it
 //   warps 4-11  epilogue: TMEM -> registers, AdamW in fp32, results written in
-//               place into the slot, then TMA-stored by one thread
+//               place into the slot (two warps per TMEM lane quadrant)
+// How shared memory is split between operand stages and state slots is the
+// pipeline profile (forge_internal.h), chosen by token count on the host.
 //
 // Operands: A = dY^T (M = weight rows) and B = X (N = weight columns) are both
 // contiguous along M/N, so both are fed to the MMA MN-major, straight from the

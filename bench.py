@@ -238,6 +238,21 @@ def fused_step_separate(F, layer, step, events=None, stream=None):
             events[i][1].record(stream)
 
 
+def max_over_ranks(values, dev):
+    """Each value's maximum over the ranks of the process group (the slowest
+    replica sets the job's time).  `dev` is where the reduction runs: the
+    rank's GPU under NCCL, the CPU under gloo."""
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_value(world, units_per_rank, seconds):
+    """Whole-job throughput of `world` replicas that each process
+    `units_per_rank` in `seconds` (the maximum over ranks)."""
+    return world * units_per_rank / seconds
+
+
 def run_gpu(args, rank, world, dev):
     from weight_gradient_gemm_gb300 import forge as F
     F.lib()
@@ -287,9 +302,7 @@ def run_gpu(args, rank, world, dev):
     if sampler:
         sampler.stop()
     if dist:
-        t = torch.tensor([elapsed_ms, kern_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms, kern_ms = float(t[0]), float(t[1])
+        elapsed_ms, kern_ms = max_over_ranks([elapsed_ms, kern_ms], dev)
 
     # ---- diagnostics (not the reported value): the same step as seven launches
     sep_steps = max(3, min(args.steps, 30))
@@ -362,9 +375,7 @@ def run_gpu(args, rank, world, dev):
     e1 = time.perf_counter()
     e2e_ms = (e1 - e0) * 1e3 / e2e_steps
     if dist:
-        t = torch.tensor([e2e_ms, unf_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms, unf_ms = float(t[0]), float(t[1])
+        e2e_ms, unf_ms = max_over_ranks([e2e_ms, unf_ms], dev)
 
     return dict(layer=layer, elapsed_ms=elapsed_ms, kern_ms=kern_ms, unf_ms=unf_ms,
                 per_proj_ms=per_proj_ms,
@@ -615,7 +626,7 @@ def run_reference(args):
     """The reference arm: the CPU oracle, as it stands, on a bounded sample
     of the same workload each step."""
     cfg, bt, fmt, dy_std, spike = workload_spec(args.workload)
-    budget_s = 120.0
+    budget_s = args.reference_budget
     per_step = budget_s / max(1, args.steps + args.warmup)
     rows = _oracle_rows_for(args.workload, 0.6 * per_step)   # the fit runs slightly short
     sample, bt = oracle_sample(args.workload, rows)
@@ -655,6 +666,8 @@ def main():
                     help="one of %s, llama31_8b_layer_bt<BT>_<fp32|bf16|int8>, or the full "
                          "224-linear stack llama31_8b_stack_bt<BT>_<fp32|bf16|int8>" % sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reference-budget", type=float, default=120.0,
+                    help="seconds of oracle work the reference arm aims for (all steps)")
     ap.add_argument("--only", default="",
                     help="comma-separated projections (q,k,v,o,gate,up,down) for small profiling "
                          "runs; the JSON line then describes that subset")
@@ -696,7 +709,7 @@ def main():
     peaks, peak_kind = measured_peaks()
     ms = res["elapsed_ms"] / args.steps
     flops = layer.flops()
-    value = world * flops / (ms * 1e-3) / 1e12
+    value = job_value(world, flops, ms * 1e-3) / 1e12
     launches = args.steps   # one grouped launch per step
     kern_s_per_launch = res["kern_ms"] * 1e-3 / launches
     alg_bytes_launch = layer.alg_bytes()
@@ -734,10 +747,10 @@ def main():
                           "params_per_s": layer.params() / (ms * 1e-3) * world,
                           "hbm_gbs": layer.alg_bytes() / (ms * 1e-3) / 1e9},
         "unfused": {"ms_per_step": res["unf_ms"],
-                    "value": world * flops / (res["unf_ms"] * 1e-3) / 1e12,
+                    "value": job_value(world, flops, res["unf_ms"] * 1e-3) / 1e12,
                     "fused_speedup": res["unf_ms"] / ms,
                     "path": "forge_wgrad (bf16 dW) + forge_adamw"},
-        "e2e": {"value": world * flops / (res["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": job_value(world, flops, res["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": res["e2e_ms"], "h2d_bytes_per_step": layer.h2d_bytes(),
                 "d2h_bytes_per_step": 4,
                 "pipeline": "X, dY of step k+1 copied from pinned host memory on a second "

@@ -1,0 +1,75 @@
+"""The multi-replica path of bench.py on the CPU: two gloo ranks.
+
+With N GPUs the bench runs N independent replicas (the fused step has no
+exchange between ranks: every rank updates its own layer), times each with a
+barrier on both sides and reports the slowest rank's time; rank 0 alone prints
+the JSON line.  These tests run that host logic with the gloo backend."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # rank r took 1 + r ms in the timed region and 5 - r ms end to end
+        t, e = bench.max_over_ranks([1.0 + rank, 5.0 - rank], torch.device("cpu"))
+        dist.barrier()
+        out[rank] = (t, e)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_two_gloo_ranks():
+    world, port = 2, _free_port()
+    with mp.Manager() as mgr:
+        out = mgr.dict()
+        mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
+        res = dict(out)
+    # every rank sees the slowest rank's time for each quantity
+    assert res == {0: (2.0, 5.0), 1: (2.0, 5.0)}
+
+
+def test_job_value_counts_every_replica():
+    sys.path.insert(0, ROOT)
+    import bench
+    # two replicas, each 1e12 FLOP in 0.5 s (the slowest rank): 4e12 FLOP/s
+    assert bench.job_value(2, 1e12, 0.5) == pytest.approx(4e12)
+    assert bench.job_value(1, 3.0, 1.5) == pytest.approx(2.0)
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    # the reference arm (the CPU oracle) under a two-rank launch: rank 0 alone
+    # runs and prints one JSON line; rank 1 exits 0 without work
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes", "1",
+           "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
+           "--master-port", str(_free_port()), "bench.py", "--impl", "reference",
+           "--gpus", "2", "--steps", "1", "--warmup", "3", "--reference-budget", "4"]
+    env = dict(os.environ, OMP_NUM_THREADS="2", OPENBLAS_NUM_THREADS="2")
+    r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["steps"] == 1
+    assert d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0

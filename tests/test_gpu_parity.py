@@ -290,3 +290,30 @@ def test_grouped_against_oracle_all_profiles(profile):
         ref = ref_inputs(l["x"], l["dy"], l["w"], l["m"], l["v"])
         check_step(bf16_bits(d["W"].cpu()), mom_from_dev(fmt, d["m"], None),
                    mom_from_dev(fmt, d["v"], None), ref, TINY, 5, fmt, bt, label="grouped")
+
+
+@pytest.mark.parametrize("group_m", [1, 3, 5])
+@pytest.mark.parametrize("cg", ["1", "2"])
+def test_raster_group_sizes(group_m, cg, monkeypatch):
+    # tile orders whose last raster group is partial (1000 rows: 8 tiles of
+    # 128 or 4 of 256; group sizes 3 and 5 leave remainders) give the same
+    # step as the oracle, on one CTA and on CTA pairs
+    monkeypatch.setenv("FORGE_GROUP_M", str(group_m))
+    monkeypatch.setenv("FORGE_CG", cg)
+    monkeypatch.setenv("FORGE_PROFILE", "balanced")
+    fmt = O.FMT_FP32
+    shapes = [(1000, 776), (264, 512)]
+    bt = 96
+    layers = _group_case(fmt, shapes, bt, share_x=False, seed=3)
+    dev = []
+    for l in layers:
+        W, md, vd, ms, vs = dev_state(l["w"], l["m"], l["v"])
+        dev.append(dict(X=l["x"].to(DEV), dY=l["dy"].to(DEV), W=W, m=md, v=vd))
+    F.wgrad_adamw_grouped(dev, step=2, **hyper_kwargs(TINY))
+    assert F.device_error() == 0
+    from .gpu_util import mom_from_dev
+    for l, d in zip(layers, dev):
+        ref = ref_inputs(l["x"], l["dy"], l["w"], l["m"], l["v"])
+        check_step(bf16_bits(d["W"].cpu()), mom_from_dev(fmt, d["m"], None),
+                   mom_from_dev(fmt, d["v"], None), ref, TINY, 2, fmt, bt,
+                   label=f"group_m={group_m} cg={cg}")

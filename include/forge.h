@@ -30,7 +30,8 @@
  * FORGE_PROFILE=stream|balanced|mma|deep (how shared memory is split between
  * operand stages and state slots), FORGE_CG=1|2 (one CTA or a CTA pair per
  * tile), FORGE_BN=128|256 (accumulator width on one CTA), FORGE_GROUP_M=1..64
- * (tile rows per raster group).  Every choice computes the same step to the
+ * (tile rows per raster group), FORGE_POLL_STORE=0|1 (the store lanes poll
+ * for finished state slots).  Every choice computes the same step to the
  * same accuracy; only the speed differs.
  *
  * Errors.  Argument errors are returned synchronously, before anything is

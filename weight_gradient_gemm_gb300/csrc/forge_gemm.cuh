@@ -183,6 +183,20 @@ __device__ __forceinline__ bool wait_stage(uint32_t bar, uint32_t parity, const 
   return wait_bounded(bar, parity, w, site);
 }
 
+// A bounded wait that polls with a short sleep between tests: quicker to
+// notice a completed phase than a suspended wait, but issues few
+// instructions while it waits.  Used by the store lanes where the host asks
+// for it (GemmParams::poll_store).
+__device__ __forceinline__ bool wait_poll(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                          int site) {
+#pragma unroll 1
+  for (int i = 0; i < kSpinTests; ++i) {
+    if (mbar_test_wait(bar, parity)) return true;
+    __nanosleep(32);
+  }
+  return wait_bounded(bar, parity, w, site);
+}
+
 // Global tile index -> (layer, tile row, tile column).  Layers are laid out
 // one after another in the queue; inside a layer, groups of group_m tile rows
 // are walked column by column so that concurrent tiles share operand panels
@@ -742,7 +756,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           const int j = cnt % T::NS;
           if (j != lane) continue;
           const uint32_t ph = (cnt / T::NS) & 1u;
-          if (!wait_bounded(bar_sdone(j), ph, wc, kSiteStoreSlotDone)) { ok = false; break; }
+          const bool done = p.poll_store ? wait_poll(bar_sdone(j), ph, wc, kSiteStoreSlotDone)
+                                         : wait_bounded(bar_sdone(j), ph, wc, kSiteStoreSlotDone);
+          if (!done) { ok = false; break; }
           const int x0 = tn * BN + (s / T::PARTS) * T::SW;
           const int y0 = tm * T::TM + static_cast<int>(rank) * kBM + (s % T::PARTS) * T::RPS;
           if (x0 < pr.d_in && y0 < pr.d_out) {

@@ -57,6 +57,7 @@ struct GemmParams {
   int* err_site;              // device word: where a wait first timed out
   uint64_t timeout_ns;
   int32_t drop_first_arrival;  // testing aid, see forge_debug_drop_first_arrival
+  int32_t poll_store;         // store lanes poll for finished slots (see choose_config)
 };
 
 struct GemmMaps {
@@ -77,6 +78,7 @@ struct GemmConfig {
   int prof;      // pipeline profile: 0 stream (HBM-bound), 1 mma (tensor-bound)
   int grid;      // persistent CTAs (even for CTA pairs)
   int group_m;
+  int poll_store;  // store lanes poll the slot-done barrier instead of suspending
 };
 
 // Tokens per operand pipeline stage (the TMA box height of dY and X), used

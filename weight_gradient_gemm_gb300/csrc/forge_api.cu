@@ -282,10 +282,13 @@ GemmConfig choose_config(int64_t bt, int fmt, int mode) {
   c.group_m = (c.cg == 1) ? 4 : 1;
   // The store lanes poll for finished slots (instead of a suspending wait)
   // where the slot ring is short against the state stream: bf16 moments up
-  // to 576 tokens on one CTA (+12 % at BT = 512) and fp32 moments in the
-  // stream profile (+0.3-1.4 %).  Elsewhere it measured neutral or slower.
-  c.poll_store = mode == kModeFused && c.cg == 1 &&
-                 ((fmt == kFmtBF16 && bt <= 576) || (fmt == kFmtF32 && c.prof == kProfStream));
+  // to 576 tokens on one CTA (+12 % at BT = 512), fp32 moments in the stream
+  // profile (+0.3-1.4 %) and on CTA pairs (+2 % at 1024 and 4096 tokens).
+  // Elsewhere it measured neutral or slower.
+  c.poll_store = mode == kModeFused &&
+                 ((c.cg == 1 && ((fmt == kFmtBF16 && bt <= 576) ||
+                                 (fmt == kFmtF32 && c.prof == kProfStream))) ||
+                  (c.cg == 2 && fmt == kFmtF32));
   if (const char* e = std::getenv("FORGE_POLL_STORE")) c.poll_store = (std::atoi(e) != 0);
   if (const char* e = std::getenv("FORGE_GROUP_M")) {
     const int g = std::atoi(e);

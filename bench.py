@@ -614,8 +614,8 @@ def time_oracle(workload: str, target_s: float):
 
 def cpu_baseline_block(workload):
     # the two-point fit overestimates the cost per row of larger samples: a
-    # 15 s target lands near 10 s of oracle work
-    value, dt, rows, bt = time_oracle(workload, 15.0)
+    # 20 s target lands at about 10-12 s of oracle work
+    value, dt, rows, bt = time_oracle(workload, 20.0)
     return {"value": value, "unit": "TFLOP/s", "cores": oracle_threads(), "kind": "oracle",
             "sample": (f"one fp64 oracle step (numpy: BLAS matmul for G, then AdamW and rounding)"
                        f" on the first {rows} rows of each of the 7 projections at BT={bt}, "

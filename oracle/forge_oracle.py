@@ -17,7 +17,11 @@ What it computes:
   corrections and the weight update);
 * one rounding per stored tensor: bf16 weights and fp32, bf16 or int8
   moments (section 1, Eq. 1: k = 8 / 4 / 2 bytes of state per parameter;
-  Appendix B "INT8 states").
+  Appendix B "INT8 states");
+* the input gradient of the same layer, ``dX = dY W`` (the other half of the
+  backward pass of ``Y = X W^T``, section 2.1), which Algorithm 1 computes
+  from the weight before the update (its first line; Appendix A, Remark 2):
+  ``linear_backward`` takes it from the pre-update W, then steps.
 
 Proposition 1 (Appendix A.2) says the tile-fused schedule reaches exactly the
 result of forming all of G and stepping once.  So the oracle is that plain
@@ -44,6 +48,8 @@ R8  With no tokens (BT = 0), G = 0: the moments decay and W takes the decay and
     the m-driven update, with no special case (Appendix A, Remark 1).
 R9  The hyperparameters are the float32 values the C interface receives,
     widened exactly to fp64.
+R10 dX is stored in bf16, rounded once to nearest even from the exact fp64
+    product (the layer's activations and their gradients are bf16).
 """
 from __future__ import annotations
 
@@ -58,7 +64,7 @@ __all__ = [
     "bf16_to_f64", "f64_to_bf16", "f64_to_f32",
     "wgrad", "wgrad_abs", "adamw_f64",
     "quantize_int8_blocks", "decode_moment", "encode_moment", "zero_moment",
-    "step",
+    "step", "dgrad", "dgrad_abs", "linear_backward",
 ]
 
 FMT_FP32, FMT_BF16, FMT_INT8 = 0, 1, 2
@@ -185,6 +191,33 @@ def wgrad_abs(x_bits, dy_bits, rows=None) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
+# The input gradient (backward pass of Y = X W^T)
+# ---------------------------------------------------------------------------
+
+def dgrad(dy_bits, w_bits, rows=None) -> np.ndarray:
+    """dX = dY W in fp64, shape [BT, Din] or [len(rows), Din].
+
+    ``dy_bits`` is dY [BT, Dout], ``w_bits`` is W [Dout, Din], both bf16 bits:
+    dX_tq = sum_p dY_tp W_pq.  Row t of dX reads only row t of dY and all of
+    W, so ``rows`` (token rows) computes an exact subset of rows."""
+    dY = bf16_to_f64(dy_bits)
+    W = bf16_to_f64(w_bits)
+    if rows is not None:
+        dY = dY[rows]
+    return dY @ W
+
+
+def dgrad_abs(dy_bits, w_bits, rows=None) -> np.ndarray:
+    """|dY| |W|: the bound on what any fp32 summation order of dX may differ
+    by, as wgrad_abs is for G."""
+    dY = np.abs(bf16_to_f64(dy_bits))
+    W = np.abs(bf16_to_f64(w_bits))
+    if rows is not None:
+        dY = dY[rows]
+    return dY @ W
+
+
+# ---------------------------------------------------------------------------
 # AdamW (Algorithm 1) in fp64
 # ---------------------------------------------------------------------------
 
@@ -288,3 +321,10 @@ def step(x_bits, dy_bits, w_bits, m: Moment, v: Moment, hyper: Hyper, t: int,
     if return_f64:
         return out + ((G, W1, m1, v1),)
     return out
+
+
+def linear_backward(x_bits, dy_bits, w_bits, m: Moment, v: Moment, hyper: Hyper, t: int):
+    """The layer's backward pass with the fused update: dX from the weight
+    before the update (R10), then one step.  Returns (dX bits, W' bits, m', v')."""
+    dx = f64_to_bf16(dgrad(dy_bits, w_bits))
+    return (dx,) + step(x_bits, dy_bits, w_bits, m, v, hyper, t)

@@ -139,3 +139,21 @@ def test_int8_mistakes_are_caught(monkeypatch, kind):
             P.test_int8_blocks_are_128_wide_along_rows,
             P.test_int8_second_moment_floor]
     assert _fails_one(pins)
+
+
+@pytest.mark.parametrize("kind", ["w_transposed", "flipped_rows", "dropped_output"])
+def test_dgrad_mistakes_are_caught(monkeypatch, kind):
+    def dg(dy_bits, w_bits, rows=None):
+        dY, W = F.bf16_to_f64(dy_bits), F.bf16_to_f64(w_bits)
+        if rows is not None:
+            dY = dY[rows]
+        if kind == "w_transposed":
+            return dY @ (W.T if W.shape[0] == W.shape[1] else W[::-1])
+        if kind == "flipped_rows":
+            return dY @ W[::-1]
+        return dY[:, 1:] @ W[1:]
+    _patch(monkeypatch, "dgrad", dg)
+    pins = [lambda: P.test_dgrad_exact_rational_bruteforce(5, 3, 4),
+            lambda: P.test_dgrad_one_hot_closed_form(7, 7),
+            P.test_dgrad_and_wgrad_are_adjoint_to_the_forward_pass]
+    assert _fails_one(pins)

@@ -157,6 +157,87 @@ def test_wgrad_empty_tokens_is_zero():
 
 
 # ---------------------------------------------------------------------------
+# Input gradient dX = dY W (backward pass of Y = X W^T)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bt,dout,din", [(5, 3, 4), (1, 6, 2), (9, 7, 7)])
+def test_dgrad_exact_rational_bruteforce(bt, dout, din):
+    r = rng(bt * 1000 + dout * 10 + din)
+    db = random_bf16_bits(r, (bt, dout))
+    wb = random_bf16_bits(r, (dout, din))
+    dY, W = O.bf16_to_f64(db), O.bf16_to_f64(wb)
+    dX = O.dgrad(db, wb)
+    assert dX.shape == (bt, din)
+    for t in range(bt):
+        for q in range(din):
+            exact = sum(Fraction(dY[t, p]) * Fraction(W[p, q]) for p in range(dout))
+            assert Fraction(dX[t, q]) == exact, (t, q)
+
+
+@pytest.mark.parametrize("dout,din", [(6, 11), (7, 7)])
+def test_dgrad_one_hot_closed_form(dout, din):
+    # dY[t, p] = c_t when p == pi(t): row t of dX is c_t times row pi(t) of W.
+    # W^T in place of W, reversed rows or a dropped output give other rows.
+    r = rng(13 + din)
+    bt = 30
+    wb = random_bf16_bits(r, (dout, din))
+    W = O.bf16_to_f64(wb)
+    pi = r.integers(0, dout, bt)
+    c = np.array([1.0, -2.0, 0.5, 0.25])[r.integers(0, 4, bt)]
+    dY = np.zeros((bt, dout))
+    dY[np.arange(bt), pi] = c
+    dX = O.dgrad(O.f64_to_bf16(dY), wb)
+    for t in range(bt):
+        assert np.array_equal(dX[t], c[t] * W[pi[t]]), t
+
+
+def test_dgrad_and_wgrad_are_adjoint_to_the_forward_pass():
+    # For Y = X W^T and a loss gradient dY: <dX, X> = <dY, Y> = <G, W>, with
+    # Y formed here from its own definition (section 2.1).  A transposed or
+    # swapped operand in either gradient breaks the identity.
+    r = rng(17)
+    bt, dout, din = 12, 5, 9
+    xb = random_bf16_bits(r, (bt, din))
+    db = random_bf16_bits(r, (bt, dout))
+    wb = random_bf16_bits(r, (dout, din))
+    X, dY, W = O.bf16_to_f64(xb), O.bf16_to_f64(db), O.bf16_to_f64(wb)
+    Y = np.array([[sum(Fraction(X[t, q]) * Fraction(W[p, q]) for q in range(din))
+                   for p in range(dout)] for t in range(bt)], dtype=object)
+    dy_y = sum(Fraction(dY[t, p]) * Y[t, p] for t in range(bt) for p in range(dout))
+    dx_x = sum(Fraction(v) * Fraction(x) for v, x in zip(O.dgrad(db, wb).ravel(), X.ravel()))
+    g_w = sum(Fraction(g) * Fraction(w) for g, w in zip(O.wgrad(xb, db).ravel(), W.ravel()))
+    assert dx_x == dy_y and g_w == dy_y
+
+
+def test_dgrad_row_subset_and_abs():
+    r = rng(18)
+    db = random_bf16_bits(r, (21, 8))
+    wb = random_bf16_bits(r, (8, 13))
+    rows = np.array([20, 0, 3, 3])
+    assert np.array_equal(O.dgrad(db, wb, rows), O.dgrad(db, wb)[rows])
+    dX, S = O.dgrad(db, wb), O.dgrad_abs(db, wb)
+    assert np.all(np.abs(dX) <= S)
+    assert np.array_equal(O.dgrad(db & np.uint16(0x7FFF), wb & np.uint16(0x7FFF)), S)
+
+
+def test_linear_backward_reads_the_weight_before_the_update():
+    # Algorithm 1 computes dX first: dX comes from W, not from W'
+    r = rng(19)
+    bt, dout, din = 16, 8, 12
+    xb = random_bf16_bits(r, (bt, din))
+    db = random_bf16_bits(r, (bt, dout))
+    wb = random_bf16_bits(r, (dout, din))
+    hyper = O.Hyper(lr=1e-1, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.1)
+    m = O.zero_moment(O.FMT_FP32, dout, din)
+    v = O.zero_moment(O.FMT_FP32, dout, din)
+    dx, w1, m1, v1 = O.linear_backward(xb, db, wb, m, v, hyper, 1)
+    assert np.array_equal(dx, O.f64_to_bf16(O.dgrad(db, wb)))
+    assert not np.array_equal(dx, O.f64_to_bf16(O.dgrad(db, w1)))
+    w_only, m_only, _ = O.step(xb, db, wb, m, v, hyper, 1)
+    assert np.array_equal(w1, w_only) and np.array_equal(m1.data, m_only.data)
+
+
+# ---------------------------------------------------------------------------
 # AdamW (Algorithm 1)
 # ---------------------------------------------------------------------------
 

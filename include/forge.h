@@ -158,6 +158,34 @@ forge_status forge_wgrad(const void* X, const void* dY, void* dW, forge_dtype dw
                          int64_t bt, int64_t d_in, int64_t d_out, forge_stream stream);
 
 /*
+ * forge_dgrad: the layer's input gradient dX = dY W (the other half of the
+ * backward pass of Y = X W^T, section 2.1), bf16 in, fp32 accumulation over
+ * d_out, bf16 out (rounded to nearest even).
+ *   dY [bt, d_out] bf16, W [d_out, d_in] bf16 (read only), dX [bt, d_in] bf16
+ *   (written).  Row-major, 16-byte aligned, d_in and d_out multiples of 8.
+ * dX must not overlap dY or W.  bt = 0 does nothing.  Asynchronous on
+ * `stream`; argument errors are returned before anything is enqueued.
+ */
+forge_status forge_dgrad(const void* dY, const void* W, void* dX,
+                         int64_t bt, int64_t d_in, int64_t d_out, forge_stream stream);
+
+/*
+ * forge_linear_backward: the layer's whole backward step with the fused
+ * update: dX = dY W from the weight before the update (Algorithm 1 computes
+ * the input gradient first; Appendix A, Remark 2), then forge_wgrad_adamw.
+ * Both run on `stream` in that order, so the caller no longer has to order
+ * dX before the update.  Arguments as forge_dgrad and forge_wgrad_adamw;
+ * dX [bt, d_in] bf16 must not overlap X, dY, W, m, v or the scales.  Every
+ * argument of both halves is checked before anything is enqueued.
+ */
+forge_status forge_linear_backward(const void* X, const void* dY, void* W, void* dX,
+                                   forge_moment m, forge_moment v,
+                                   int64_t bt, int64_t d_in, int64_t d_out,
+                                   float lr, float beta1, float beta2, float eps,
+                                   float weight_decay, int64_t step,
+                                   forge_moment_fmt fmt, forge_stream stream);
+
+/*
  * forge_adamw: the unfused optimizer step on a stored gradient dW (fp32 or
  * bf16), with exactly the per-element arithmetic of forge_wgrad_adamw.
  * forge_wgrad(FP32) followed by forge_adamw gives the same bits as

@@ -19,7 +19,8 @@ def L():
 def test_header_declares_the_boundary():
     names = F.header_functions()
     for n in ("forge_wgrad_adamw", "forge_wgrad", "forge_adamw", "forge_device_error",
-              "forge_status_string"):
+              "forge_status_string", "forge_wgrad_adamw_grouped", "forge_dgrad",
+              "forge_linear_backward"):
         assert n in names
 
 
@@ -95,6 +96,23 @@ def test_wgrad_and_adamw_argument_errors(L):
     assert L.forge_adamw(C, 0, C, m, v, 256, 128, 1e-3, 0.9, 0.999, 1e-8, 0.01, 1, 0, None) == 6
     assert L.forge_adamw(A, 3, C, m, v, 256, 128, 1e-3, 0.9, 0.999, 1e-8, 0.01, 1, 0, None) == 4
     assert L.forge_adamw(A, 0, C, m, v, 256, 128, 1e-3, 0.9, 0.999, 1e-8, 0.01, 0, 0, None) == 5
+
+
+def test_dgrad_and_linear_backward_argument_errors(L):
+    # codes: 1 NULL, 2 ALIGN, 3 SHAPE, 5 HYPER, 6 ALIAS
+    assert L.forge_dgrad(B, C, None, 64, 256, 128, None) == 1
+    assert L.forge_dgrad(B, C + 4, A, 64, 256, 128, None) == 2
+    assert L.forge_dgrad(B, C, A, 64, 250, 128, None) == 3
+    assert L.forge_dgrad(B, C, C, 64, 256, 128, None) == 6          # dX over W
+    assert L.forge_dgrad(None, None, None, 0, 256, 128, None) == 0  # no tokens: nothing to do
+    m, v = F.ForgeMoment(D, None), F.ForgeMoment(D + (1 << 36), None)
+    args = (256, 128, 1e-3, 0.9, 0.999, 1e-8, 0.01)
+    assert L.forge_linear_backward(A, B, C, None, m, v, 64, *args, 1, 0, None) == 1
+    assert L.forge_linear_backward(A, B, C, A, m, v, 64, *args, 1, 0, None) == 6   # dX over X
+    assert L.forge_linear_backward(A, B, C, C, m, v, 64, *args, 1, 0, None) == 6   # dX over W
+    assert L.forge_linear_backward(A, B, C, G + 4, m, v, 64, *args, 1, 0, None) == 2
+    # a bad step is caught before the input gradient is enqueued
+    assert L.forge_linear_backward(A, B, C, G, m, v, 64, *args, 0, 0, None) == 5
 
 
 def grouped(L, layers, bt=64, step=1, fmt=0):

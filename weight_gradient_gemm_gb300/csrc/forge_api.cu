@@ -20,6 +20,7 @@ cudaError_t launch_gemm_fused_bf16(const GemmConfig&, const GemmArgs&, cudaStrea
 cudaError_t launch_gemm_fused_i8(const GemmConfig&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_store_f32(const GemmConfig&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_store_bf16(const GemmConfig&, const GemmArgs&, cudaStream_t);
+cudaError_t launch_gemm_dgrad(const GemmConfig&, const GemmArgs&, cudaStream_t);
 
 cudaError_t launch_gemm(int mode, int fmt, const GemmConfig& cfg, const GemmArgs& args,
                         cudaStream_t stream) {
@@ -29,11 +30,13 @@ cudaError_t launch_gemm(int mode, int fmt, const GemmConfig& cfg, const GemmArgs
       case kFmtBF16: return launch_gemm_fused_bf16(cfg, args, stream);
       case kFmtI8: return launch_gemm_fused_i8(cfg, args, stream);
     }
-  } else {
+  } else if (mode == kModeStoreG) {
     switch (fmt) {
       case kFmtF32: return launch_gemm_store_f32(cfg, args, stream);
       case kFmtBF16: return launch_gemm_store_bf16(cfg, args, stream);
     }
+  } else if (mode == kModeDgrad && fmt == kFmtBF16) {
+    return launch_gemm_dgrad(cfg, args, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -247,6 +250,8 @@ AdamWConsts make_consts(float lr, float b1, float b2, float eps, float wd, int64
 // 768-token split.  FORGE_PROFILE=stream|balanced|mma|deep, FORGE_CG=1|2,
 // FORGE_BN=128|256, FORGE_GROUP_M=1..64 and FORGE_POLL_STORE=0|1 override the
 // choice.
+GemmConfig finish_config(GemmConfig c, int64_t bt, int fmt, int mode);
+
 GemmConfig choose_config(int64_t bt, int fmt, int mode) {
   GemmConfig c;
   const int64_t one_cta_upto = (mode == kModeFused && fmt == kFmtBF16) ? 640 : 768;
@@ -260,6 +265,12 @@ GemmConfig choose_config(int64_t bt, int fmt, int mode) {
     c.cg = 2;
     c.prof = bt <= 1536 ? kProfBalanced : (bt <= 3072 ? kProfMma : kProfDeep);
   }
+  return finish_config(c, bt, fmt, mode);
+}
+
+// The tile width, the raster order and the store-lane wait follow from the
+// grouping, profile and format; the environment overrides apply last.
+GemmConfig finish_config(GemmConfig c, int64_t bt, int fmt, int mode) {
   c.bn = (c.cg == 2) ? 256 : 128;
   if (const char* e = std::getenv("FORGE_PROFILE")) {
     if (std::strcmp(e, "stream") == 0) c.prof = kProfStream;
@@ -296,6 +307,17 @@ GemmConfig choose_config(int64_t bt, int fmt, int mode) {
   }
   c.grid = 0;
   return c;
+}
+
+// The input-gradient GEMM dX = dY W (rows = tokens, K = d_out): a light
+// epilogue, so the deepest operand pipeline; CTA pairs (256 x 256 tiles) when
+// they still give every pair a tile, else 128 x 128 tiles on one CTA.
+GemmConfig choose_dgrad_config(int64_t rows, int64_t d_in, int64_t d_out, int num_sms) {
+  GemmConfig c;
+  const int64_t pair_tiles = ((rows + 255) / 256) * ((d_in + 255) / 256);
+  c.cg = pair_tiles >= num_sms / 2 ? 2 : 1;
+  c.prof = kProfMma;
+  return finish_config(c, d_out, kFmtBF16, kModeDgrad);
 }
 
 int64_t tiles_of(const GemmConfig& c, int64_t d_in, int64_t d_out) {
@@ -531,6 +553,78 @@ forge_status forge_wgrad(const void* X, const void* dY, void* dW, forge_dtype dw
   args.p.drop_first_arrival = take_drop_flag();
   return launch_gemm(kModeStoreG, ifmt, cfg, args, st) == cudaSuccess ? FORGE_OK
                                                                        : FORGE_ERR_LAUNCH;
+}
+
+forge_status forge_dgrad(const void* dY, const void* W, void* dX, int64_t bt, int64_t d_in,
+                         int64_t d_out, forge_stream stream) {
+  forge_status s = check_shape(bt, d_in, d_out);
+  if (s != FORGE_OK) return s;
+  if (bt == 0) return FORGE_OK;   // no tokens: dX is empty
+  if (!dY || !W || !dX) return FORGE_ERR_NULL;
+  if (!aligned16(dY) || !aligned16(W) || !aligned16(dX)) return FORGE_ERR_ALIGN;
+  const uint64_t ndx = 2ull * bt * d_in;
+  if (overlaps(dX, ndx, dY, 2ull * bt * d_out) ||
+      overlaps(dX, ndx, W, 2ull * d_in * d_out))
+    return FORGE_ERR_ALIAS;
+  DeviceInfo* d = nullptr;
+  s = device_info(&d);
+  if (s != FORGE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  GemmConfig cfg = choose_dgrad_config(bt, d_in, d_out, d->num_sms);
+  GemmArgs args;
+  std::memset(&args, 0, sizeof(args));
+  GemmMaps& maps = args.maps[0];
+  const int bk = bk_of(cfg.cg);
+  // A = dY read K-major: 64 of d_out x 64 token rows per box; B = W read
+  // MN-major: 64 of d_in x bk of d_out per box; dX stored in 32 x 128 boxes
+  const bool ok =
+      get_map(&maps.dy, dY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_out, bt, d_out * 2, 64, 64,
+              CU_TENSOR_MAP_SWIZZLE_128B) &&
+      get_map(&maps.x, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_in, d_out, d_in * 2, 64, bk,
+              CU_TENSOR_MAP_SWIZZLE_128B) &&
+      get_map(&maps.w, dX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_in, bt, d_in * 2, 32, kBM,
+              CU_TENSOR_MAP_SWIZZLE_64B);
+  if (!ok) return FORGE_ERR_LAUNCH;
+  args.p = base_params(d_out, cfg, *d);   // the reduction runs over d_out
+  add_problem(args.p, cfg, d_in, bt, nullptr, nullptr);   // tile rows are tokens
+  set_grid(cfg, args.p.num_tiles, d->num_sms);
+  args.p.drop_first_arrival = take_drop_flag();
+  return launch_gemm(kModeDgrad, kFmtBF16, cfg, args, st) == cudaSuccess ? FORGE_OK
+                                                                         : FORGE_ERR_LAUNCH;
+}
+
+forge_status forge_linear_backward(const void* X, const void* dY, void* W, void* dX,
+                                   forge_moment m, forge_moment v, int64_t bt, int64_t d_in,
+                                   int64_t d_out, float lr, float beta1, float beta2, float eps,
+                                   float weight_decay, int64_t step, forge_moment_fmt fmt,
+                                   forge_stream stream) {
+  // every argument of both halves is checked before anything is enqueued
+  forge_linear L;
+  L.X = X;
+  L.dY = dY;
+  L.W = W;
+  L.m = m;
+  L.v = v;
+  L.d_in = d_in;
+  L.d_out = d_out;
+  forge_status s = check_linear(L, bt, fmt);
+  if (s != FORGE_OK) return s;
+  s = check_hyper(lr, beta1, beta2, eps, weight_decay, step);
+  if (s != FORGE_OK) return s;
+  if (layers_clash(L, L, bt, fmt, true)) return FORGE_ERR_ALIAS;
+  if (bt > 0) {
+    if (!dX) return FORGE_ERR_NULL;
+    if (!aligned16(dX)) return FORGE_ERR_ALIGN;
+    const uint64_t ndx = 2ull * bt * d_in;
+    if (overlaps(dX, ndx, X, 2ull * bt * d_in) || overlaps(dX, ndx, dY, 2ull * bt * d_out) ||
+        input_overlaps_state(dX, ndx, W, m, v, d_in, d_out, fmt))
+      return FORGE_ERR_ALIAS;
+  }
+  // dX reads W before the fused step overwrites it (Algorithm 1): same stream
+  s = forge_dgrad(dY, W, dX, bt, d_in, d_out, stream);
+  if (s != FORGE_OK) return s;
+  return forge_wgrad_adamw(X, dY, W, m, v, bt, d_in, d_out, lr, beta1, beta2, eps, weight_decay,
+                           step, fmt, stream);
 }
 
 forge_status forge_adamw(const void* dW, forge_dtype dw_dtype, void* W, forge_moment m,

@@ -6,6 +6,11 @@
 //                Eq. 4 and Algorithm 1), with the accumulator in TMEM.
 //   kModeStoreG: the same main loop, storing G (fp32 or bf16): the unfused
 //                gradient ("store-G control", Appendix D).
+//   kModeDgrad : the layer's input gradient dX = dY W (the other half of the
+//                backward pass of Y = X W^T, which Algorithm 1 computes from
+//                the weight before the update): M = tokens, N = d_in,
+//                K = d_out, A = dY K-major, B = W MN-major, bf16 dX stored as
+//                in kModeStoreG.
 //
 // One persistent CTA per SM (or one CTA pair per two SMs, CG = 2) walks the
 // tile queue t = unit, unit + units, ... over all layers of the launch.
@@ -62,7 +67,7 @@ struct GemmTraits {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int W_ELEM = (MODE == kModeStoreG && FMT == kFmtF32) ? 4 : 2;
   static constexpr int MOM_ELEM =
-      (MODE == kModeStoreG) ? 0 : (FMT == kFmtF32 ? 4 : (FMT == kFmtBF16 ? 2 : 1));
+      (MODE != kModeFused) ? 0 : (FMT == kFmtF32 ? 4 : (FMT == kFmtBF16 ? 2 : 1));
   static constexpr int W_BYTES = RPS * SW * W_ELEM;
   static constexpr int M_BYTES = RPS * SW * MOM_ELEM;
   static constexpr int SLOT_BYTES = W_BYTES + 2 * M_BYTES;
@@ -113,6 +118,8 @@ struct GemmTraits {
       (SMEM_USED + 1024 < kSmemLimit) ? SMEM_USED + 1024 : kSmemLimit;
   static_assert(SMEM_USED <= kSmemLimit, "shared memory budget exceeded");
   static_assert(BN % SW == 0 && BNL % 64 == 0, "tile width");
+  // the input-gradient mode loads A as K-major boxes 64 elements deep: one per stage
+  static_assert(MODE != kModeDgrad || BK == 64, "K-major A boxes hold 64 elements of K");
   static_assert(CG == 1 || (CG == 2 && BN == 256), "CTA pairs use 256 x 256 tiles");
   static_assert(TMEM_COLS <= 512, "tensor memory has 512 columns");
   // with half-tile slots each half of the epilogue owns every other slot
@@ -615,18 +622,23 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           const uint32_t dst = base + s * T::STAGE_BYTES;
           const int ya = tm * T::TM + static_cast<int>(rank) * kBM;      // this CTA's A rows
           const int xb = tn * BN + static_cast<int>(rank) * T::BNL;      // this CTA's B columns
+          // A boxes: 64 rows of M x 64 of K (dgrad, K-major: x = K, y = rows) or
+          // 64 of M x 64 tokens (MN-major: x = M, y = tokens); B boxes: 64 of N
+          // x 64 of K, MN-major in both
           const CUtensorMap* bm = lane < 2 ? &maps.dy : &maps.x;
-          const int bx = lane < 2 ? ya + 64 * lane : xb + 64 * (lane - 2);
+          const bool a_kmaj = (MODE == kModeDgrad) && lane < 2;
+          const int bx = a_kmaj ? k * T::BK : (lane < 2 ? ya + 64 * lane : xb + 64 * (lane - 2));
+          const int by = a_kmaj ? ya + 64 * lane : k * T::BK;
           const uint32_t bdst = lane < 2 ? dst + lane * 64 * T::BK * 2
                                          : dst + T::A_BYTES + (lane - 2) * 64 * T::BK * 2;
           if constexpr (kPair) {
             // both CTAs' loads complete on the leader's barrier, which expects both
             const uint32_t fb = mapa_shared(bar_full(s), 0);
             if (leader && lane == 0) mbar_arrive_expect_tx(bar_full(s), 2 * T::STAGE_BYTES);
-            tma_load_2d_pair(bdst, bm, bx, k * T::BK, fb, pol);
+            tma_load_2d_pair(bdst, bm, bx, by, fb, pol);
           } else {
             if (lane == 0) mbar_arrive_expect_tx(bar_full(s), T::STAGE_BYTES);
-            tma_load_2d(bdst, bm, bx, k * T::BK, bar_full(s), pol);
+            tma_load_2d(bdst, bm, bx, by, bar_full(s), pol);
           }
           if (leader) last_armed[s] = static_cast<int32_t>(cnt);
         }
@@ -641,7 +653,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = make_idesc_bf16_mn(T::TM, BN);
+      constexpr bool kAK = (MODE == kModeDgrad);   // A (dY) is K-major
+      constexpr uint32_t idesc = make_idesc_bf16(T::TM, BN, !kAK, true);
       constexpr uint32_t kLBO = T::BK * 128;   // next 64-element group along M/N
       constexpr uint32_t kSBO = 1024;        // next 8-token group
       uint32_t cnt = 0;
@@ -662,7 +675,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           const uint32_t b0 = a0 + T::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < T::BK / 16; ++kk) {
-            const uint64_t ad = make_sdesc_mn_sw128(a0 + kk * 2048, kLBO, kSBO);
+            const uint64_t ad = kAK ? make_sdesc_k_sw128(a0 + kk * 32, kSBO)
+                                    : make_sdesc_mn_sw128(a0 + kk * 2048, kLBO, kSBO);
             const uint64_t bd = make_sdesc_mn_sw128(b0 + kk * 2048, kLBO, kSBO);
             if constexpr (kPair)
               umma_bf16_pair(d, ad, bd, idesc, (k | kk) != 0 ? 1u : 0u);

@@ -20,7 +20,10 @@ constexpr int kBKPair = 64;  // tokens per pipeline stage on a CTA pair
 constexpr int kNumThreads = 384;   // 4 role warps + 8 epilogue warps
 constexpr int kEpiThreads = 256;
 
-enum Mode : int { kModeFused = 0, kModeStoreG = 1 };
+// kModeDgrad computes the layer's input gradient dX = dY W with the same
+// pipeline: A = dY read K-major (rows = tokens), B = W read MN-major, the
+// bf16 result stored like the gradient of kModeStoreG.
+enum Mode : int { kModeFused = 0, kModeStoreG = 1, kModeDgrad = 2 };
 // Pipeline profiles, i.e. how shared memory is split between operand stages
 // and state slots: kProfStream (small token counts, HBM-bound epilogue) keeps
 // two operand stages and gives the rest to state slots; kProfMma (large token

@@ -171,16 +171,35 @@ __device__ __forceinline__ uint64_t make_sdesc_mn_sw128(uint32_t saddr, uint32_t
   return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A and B, fp32 accumulator,
-// both operands MN-major.
-__host__ __device__ constexpr uint32_t make_idesc_bf16_mn(int M, int N) {
+// Shared-memory matrix descriptor for an operand stored K-major with the
+// 128-byte swizzle: 64 bf16 along K per 128-byte row, one row per M (or N)
+// index, 8-row (1024-byte) swizzle atoms.  The 16-element K steps of one
+// 64-element row are addressed by advancing the start address 32 bytes; the
+// leading-dimension offset is not used by this layout.
+//   sbo: byte distance between successive 8-row groups along M/N
+__device__ __forceinline__ uint64_t make_sdesc_k_sw128(uint32_t saddr, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1) << 16;                 // leading-dimension offset (unused)
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;   // descriptor version used by tcgen05
+  d |= static_cast<uint64_t>(2) << 61;   // swizzle mode: 128-byte
+  return d;
+}
+
+// Instruction descriptor for kind::f16 with bf16 A and B and an fp32
+// accumulator; each operand MN-major or K-major.
+__host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
   return (1u << 4)                                   // accumulator format: f32
          | (1u << 7)                                 // A format: bf16
          | (1u << 10)                                // B format: bf16
-         | (1u << 15)                                // A is MN-major
-         | (1u << 16)                                // B is MN-major
+         | (a_mn ? (1u << 15) : 0u)                  // A is MN-major
+         | (b_mn ? (1u << 16) : 0u)                  // B is MN-major
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+__host__ __device__ constexpr uint32_t make_idesc_bf16_mn(int M, int N) {
+  return make_idesc_bf16(M, N, true, true);
 }
 
 // D[tmem] (+)= A[smem] * B[smem], issued by one thread.

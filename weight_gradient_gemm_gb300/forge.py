@@ -73,6 +73,11 @@ def lib() -> ctypes.CDLL:
             L.forge_adamw.argtypes = [vp, st, vp, ForgeMoment, ForgeMoment, i64, i64,
                                       f32, f32, f32, f32, f32, i64, st, vp]
             L.forge_adamw.restype = st
+            L.forge_dgrad.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+            L.forge_dgrad.restype = st
+            L.forge_linear_backward.argtypes = [vp, vp, vp, vp, ForgeMoment, ForgeMoment, i64,
+                                                i64, i64, f32, f32, f32, f32, f32, i64, st, vp]
+            L.forge_linear_backward.restype = st
             L.forge_device_error.argtypes = [vp]
             L.forge_device_error.restype = st
             L.forge_status_string.argtypes = [st]
@@ -197,6 +202,39 @@ def wgrad(X: torch.Tensor, dY: torch.Tensor, dW: torch.Tensor, stream=None) -> N
     dt = {torch.float32: DT_FP32, torch.bfloat16: DT_BF16}[dW.dtype]
     _check(lib().forge_wgrad(_ptr(X), _ptr(dY), _ptr(dW), dt, bt, d_in, d_out, _stream(stream)),
            "forge_wgrad")
+
+
+def dgrad(dY: torch.Tensor, W: torch.Tensor, dX: torch.Tensor, stream=None) -> None:
+    """dX = dY W (bf16): the layer's input gradient.  dY [bt, d_out],
+    W [d_out, d_in], dX [bt, d_in], all bf16."""
+    for t, n in ((dY, "dY"), (W, "W"), (dX, "dX")):
+        _dense(t, n)
+    if dX.dtype != torch.bfloat16:
+        raise TypeError("dX must be bf16")
+    bt, d_out = dY.shape
+    d_in = W.shape[1]
+    _check(lib().forge_dgrad(_ptr(dY), _ptr(W), _ptr(dX), bt, d_in, d_out, _stream(stream)),
+           "forge_dgrad")
+
+
+def linear_backward(X: torch.Tensor, dY: torch.Tensor, W: torch.Tensor, dX: torch.Tensor,
+                    m: torch.Tensor, v: torch.Tensor, *, lr: float, beta1: float, beta2: float,
+                    eps: float, weight_decay: float, step: int,
+                    m_scale: Optional[torch.Tensor] = None,
+                    v_scale: Optional[torch.Tensor] = None, stream=None) -> None:
+    """The layer's backward step: dX = dY W from the weight before the update,
+    then the fused weight-gradient + AdamW step (W, m, v updated in place)."""
+    for t, n in ((X, "X"), (dY, "dY"), (W, "W"), (dX, "dX"), (m, "m"), (v, "v")):
+        _dense(t, n)
+    if dX.dtype != torch.bfloat16:
+        raise TypeError("dX must be bf16")
+    bt, d_in = X.shape
+    d_out = dY.shape[1]
+    fmt = moment_format(m)
+    st = lib().forge_linear_backward(
+        _ptr(X), _ptr(dY), _ptr(W), _ptr(dX), _moment(m, m_scale), _moment(v, v_scale), bt,
+        d_in, d_out, lr, beta1, beta2, eps, weight_decay, step, fmt, _stream(stream))
+    _check(st, "forge_linear_backward")
 
 
 def adamw(dW: Optional[torch.Tensor], W: torch.Tensor, m: torch.Tensor, v: torch.Tensor, *,

@@ -21,8 +21,13 @@
  *   int8 scales [d_out, d_in/128] fp32, one per row and 128-column block.
  *
  * Ownership.  The caller owns every buffer (device memory).  The library
- * allocates no device memory in any call; it keeps a small host-side cache of
- * TMA descriptors keyed by pointer and shape.
+ * keeps a small host-side cache of TMA descriptors keyed by pointer and
+ * shape.  Only forge_dgrad (and so forge_linear_backward) uses device memory
+ * of its own: when it splits the reduction (few tokens), it takes a
+ * workspace for fp32 partial tiles from a stream-ordered pool the library
+ * owns (one per device) and gives it back in stream order after the launch,
+ * so calls on different streams never share one.  The pool keeps freed
+ * memory for later calls.
  *
  * Tuning.  The tile configuration is chosen from the token count and the
  * moment format (forge_describe_config shows it).  For measurements, these
@@ -31,8 +36,9 @@
  * operand stages and state slots), FORGE_CG=1|2 (one CTA or a CTA pair per
  * tile), FORGE_BN=128|256 (accumulator width on one CTA), FORGE_GROUP_M=1..64
  * (tile rows per raster group), FORGE_POLL_STORE=0|1 (the store lanes poll
- * for finished state slots).  Every choice computes the same step to the
- * same accuracy; only the speed differs.
+ * for finished state slots), FORGE_SPLITS=1..8 (forge_dgrad: k-ranges per
+ * tile).  Every choice computes the same step to the same accuracy; only
+ * the speed differs.
  *
  * Errors.  Argument errors are returned synchronously, before anything is
  * enqueued.  Launch failures return FORGE_ERR_LAUNCH.  Kernels never trap:
@@ -165,6 +171,11 @@ forge_status forge_wgrad(const void* X, const void* dY, void* dW, forge_dtype dw
  *   (written).  Row-major, 16-byte aligned, d_in and d_out multiples of 8.
  * dX must not overlap dY or W.  bt = 0 does nothing.  Asynchronous on
  * `stream`; argument errors are returned before anything is enqueued.
+ * With few tiles (few tokens) the reduction over d_out is split into up to 8
+ * k-ranges whose fp32 partials are added in a fixed order, so the result is
+ * the same on every run; the partials live in a workspace from the library's
+ * pool (see Ownership), and if that memory cannot be had the launch runs
+ * unsplit.
  */
 forge_status forge_dgrad(const void* dY, const void* W, void* dX,
                          int64_t bt, int64_t d_in, int64_t d_out, forge_stream stream);

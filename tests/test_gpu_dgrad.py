@@ -149,3 +149,70 @@ def test_linear_backward_against_oracle(fmt):
     ref = ref_inputs(s.x, s.dy, bf16_bits(s.w), m, v)
     check_step(bf16_bits(W.cpu()), mom_from_dev(fmt, md, ms), mom_from_dev(fmt, vd, vs), ref,
                TINY, 2, fmt, bt, label=f"linear_backward fmt{fmt}")
+
+
+@pytest.mark.parametrize("splits", ["2", "3", "5", "8"])
+@pytest.mark.parametrize("bt,d_in,d_out,cfg", [
+    (200, 264, 4104, None),                  # CTA pairs; ragged rows, columns and K (65 k-steps)
+    (130, 520, 1032, None),                  # 17 k-steps: splits are clamped to 2 (8 steps each)
+    (77, 136, 2048, ("mma", "128", "1")),    # one CTA, 128 x 128 tiles
+    (300, 384, 1544, ("mma", "256", "1")),   # one CTA, 128 x 256 tiles
+], ids=["pair", "pair-short", "cta-128", "cta-256"])
+def test_dgrad_split_reduction(bt, d_in, d_out, cfg, splits, monkeypatch):
+    # the reduction over d_out cut into k-ranges whose partials the last unit
+    # of each tile adds: same accuracy, and bit-identical from run to run
+    monkeypatch.setenv("FORGE_SPLITS", splits)
+    if cfg is not None:
+        monkeypatch.setenv("FORGE_PROFILE", cfg[0])
+        monkeypatch.setenv("FORGE_BN", cfg[1])
+        monkeypatch.setenv("FORGE_CG", cfg[2])
+    dy, w = _inputs(4, bt, d_in, d_out)
+    dyd, wd = dy.to(DEV), w.to(DEV)
+    dX = torch.full((bt, d_in), float("nan"), dtype=torch.bfloat16, device=DEV)
+    F.dgrad(dyd, wd, dX)
+    assert F.device_error() == 0
+    check_dx(bf16_bits(dX.cpu()), bf16_bits(dy), bf16_bits(w), label=f"S={splits}")
+    again = torch.full_like(dX, float("nan"))
+    F.dgrad(dyd, wd, again)
+    assert F.device_error() == 0
+    assert torch.equal(dX.view(torch.int16), again.view(torch.int16))
+
+
+def test_dgrad_gate_projection_eight_splits(monkeypatch):
+    # Llama-3.1-8B gate projection at 512 tokens with the most splits: 224
+    # k-steps of 64 cut into 8 ranges on 32 tiles
+    monkeypatch.setenv("FORGE_SPLITS", "8")
+    bt, d_out, d_in = 512, 14336, 4096
+    dy, w = _inputs(5, bt, d_in, d_out)
+    dX = torch.empty((bt, d_in), dtype=torch.bfloat16, device=DEV)
+    F.dgrad(dy.to(DEV), w.to(DEV), dX)
+    assert F.device_error() == 0
+    rows = np.array(sorted({0, 1, 127, 128, 255, 256, 383, 384, 511}))
+    check_dx(bf16_bits(dX.cpu())[rows], bf16_bits(dy), bf16_bits(w), rows, label="gate S=8")
+
+
+def test_dgrad_split_on_two_streams_at_once(monkeypatch):
+    # each call takes its own workspace in its stream's order, so two split
+    # launches running side by side give what each gives alone
+    monkeypatch.setenv("FORGE_SPLITS", "4")
+    bt, d_in, d_out = 256, 1024, 4096
+    ins = [_inputs(10 + i, bt, d_in, d_out) for i in range(2)]
+    dev = [(dy.to(DEV), w.to(DEV)) for dy, w in ins]
+    alone = []
+    for dyd, wd in dev:
+        o = torch.empty((bt, d_in), dtype=torch.bfloat16, device=DEV)
+        F.dgrad(dyd, wd, o)
+        alone.append(o)
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    outs = [torch.full((bt, d_in), float("nan"), dtype=torch.bfloat16, device=DEV)
+            for _ in range(2)]
+    for _ in range(5):
+        for (dyd, wd), o, s in zip(dev, outs, streams):
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                F.dgrad(dyd, wd, o, stream=s)
+    torch.cuda.synchronize()
+    assert F.device_error() == 0
+    for o, a in zip(outs, alone):
+        assert torch.equal(o.view(torch.int16), a.view(torch.int16))

@@ -1,5 +1,6 @@
 // The C ABI of libforge: argument validation, TMA descriptor encoding (cached),
 // tile configuration, launches and the device error word.
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -56,6 +57,9 @@ struct DeviceInfo {
   int cc_major = 0, cc_minor = 0, num_sms = 0;
   int* err_word = nullptr;
   int* site_word = nullptr;
+  // stream-ordered pool for launch workspaces (the input gradient's split
+  // partials); it keeps freed memory for the next call instead of returning it
+  cudaMemPool_t pool = nullptr;
 };
 
 std::mutex g_mu;
@@ -125,6 +129,26 @@ forge_status device_info(DeviceInfo** out) {
   }
   *out = &d;
   return FORGE_OK;
+}
+
+// The device's workspace pool, created on first use.
+cudaMemPool_t workspace_pool(DeviceInfo& d) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!d.pool) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    cudaMemPoolProps props;
+    std::memset(&props, 0, sizeof(props));
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
+    uint64_t keep = UINT64_MAX;
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    d.pool = pool;
+  }
+  return d.pool;
 }
 
 // Encode (or fetch from the cache) a 2-D row-major tensor map.
@@ -306,18 +330,58 @@ GemmConfig finish_config(GemmConfig c, int64_t bt, int fmt, int mode) {
     if (g >= 1 && g <= 64) c.group_m = g;
   }
   c.grid = 0;
+  c.splits = 1;
   return c;
 }
 
+// How many k-ranges to cut each tile of the input gradient into.  With few
+// tiles (few tokens) most SMs would sit idle through a long reduction over
+// d_out; splitting it gives every SM work, at the price of writing one fp32
+// partial tile per unit and of the reduce kernel that adds them.  Estimated
+// time, in nanoseconds: waves x k-steps per unit x 400 (one 64-deep k-step of
+// a 256 x 256 tile on a CTA pair), plus, when split, 5000 (the reduce
+// launch and the last partial write) and the partials' bytes at 4 TB/s
+// (mostly L2 hits).  Splits are at most 8 and at least 8 k-steps
+// long (shorter units cannot hide their 128 KB partial write behind the next
+// unit's main loop), and only for queues shorter than two waves.
+// FORGE_SPLITS overrides (clamped to the same length limits).
+int choose_splits(int64_t tiles, int64_t num_k, int64_t slots, int64_t ctile_bytes) {
+  const int64_t max_s = std::max<int64_t>(1, std::min<int64_t>(8, num_k / 8));
+  if (const char* e = std::getenv("FORGE_SPLITS")) {
+    const int64_t f = std::atoi(e);
+    if (f >= 1) return static_cast<int>(std::min(f, max_s));
+  }
+  if (tiles >= 2 * slots) return 1;
+  auto cost = [&](int64_t s) {
+    const int64_t waves = (tiles * s + slots - 1) / slots;
+    int64_t ns = waves * ((num_k + s - 1) / s) * 400;
+    if (s > 1) ns += 5000 + s * tiles * ctile_bytes / 4000;
+    return ns;
+  };
+  int pick = 1;
+  int64_t best = cost(1);
+  for (int64_t s = 2; s <= max_s; ++s)
+    if (cost(s) < best) {
+      best = cost(s);
+      pick = static_cast<int>(s);
+    }
+  return pick;
+}
+
 // The input-gradient GEMM dX = dY W (rows = tokens, K = d_out): a light
-// epilogue, so the deepest operand pipeline; CTA pairs (256 x 256 tiles) when
-// they still give every pair a tile, else 128 x 128 tiles on one CTA.
+// epilogue, so the deepest operand pipeline on CTA pairs (256 x 256 tiles,
+// measured faster than one CTA at every token count from 512 to 8192), with
+// the reduction split where there are too few tiles for the SMs.
 GemmConfig choose_dgrad_config(int64_t rows, int64_t d_in, int64_t d_out, int num_sms) {
   GemmConfig c;
-  const int64_t pair_tiles = ((rows + 255) / 256) * ((d_in + 255) / 256);
-  c.cg = pair_tiles >= num_sms / 2 ? 2 : 1;
+  c.cg = 2;
   c.prof = kProfMma;
-  return finish_config(c, d_out, kFmtBF16, kModeDgrad);
+  c = finish_config(c, d_out, kFmtBF16, kModeDgrad);
+  const int64_t tiles = ((rows + kBM * c.cg - 1) / (kBM * c.cg)) * ((d_in + c.bn - 1) / c.bn);
+  const int64_t num_k = (d_out + bk_of(c.cg) - 1) / bk_of(c.cg);
+  c.splits = choose_splits(tiles, num_k, num_sms / c.cg,
+                           static_cast<int64_t>(c.cg) * kBM * c.bn * sizeof(float));
+  return c;
 }
 
 int64_t tiles_of(const GemmConfig& c, int64_t d_in, int64_t d_out) {
@@ -341,6 +405,7 @@ GemmParams base_params(int64_t bt, const GemmConfig& cfg, const DeviceInfo& d) {
   p.err_site = d.site_word;
   p.timeout_ns = g_wait_limit_ns;
   p.poll_store = cfg.poll_store;
+  p.splits = 1;
   return p;
 }
 
@@ -356,6 +421,7 @@ void add_problem(GemmParams& p, const GemmConfig& cfg, int64_t d_in, int64_t d_o
   q.m_scale = m_scale;
   q.v_scale = v_scale;
   p.num_tiles += q.tiles_m * q.tiles_n;
+  p.num_units = p.num_tiles * p.splits;
   p.nprob += 1;
 }
 
@@ -495,7 +561,7 @@ forge_status forge_wgrad_adamw_grouped(const forge_linear* layers, int n, int64_
       return FORGE_ERR_LAUNCH;
     add_problem(args.p, cfg, L.d_in, L.d_out, L.m.scale, L.v.scale);
   }
-  set_grid(cfg, args.p.num_tiles, d->num_sms);
+  set_grid(cfg, args.p.num_units, d->num_sms);
   args.p.drop_first_arrival = take_drop_flag();
   return launch_gemm(kModeFused, ifmt, cfg, args, st) == cudaSuccess ? FORGE_OK
                                                                       : FORGE_ERR_LAUNCH;
@@ -549,7 +615,7 @@ forge_status forge_wgrad(const void* X, const void* dY, void* dW, forge_dtype dw
   if (!ok) return FORGE_ERR_LAUNCH;
   args.p = base_params(bt, cfg, *d);
   add_problem(args.p, cfg, d_in, d_out, nullptr, nullptr);
-  set_grid(cfg, args.p.num_tiles, d->num_sms);
+  set_grid(cfg, args.p.num_units, d->num_sms);
   args.p.drop_first_arrival = take_drop_flag();
   return launch_gemm(kModeStoreG, ifmt, cfg, args, st) == cudaSuccess ? FORGE_OK
                                                                        : FORGE_ERR_LAUNCH;
@@ -586,11 +652,33 @@ forge_status forge_dgrad(const void* dY, const void* W, void* dX, int64_t bt, in
               CU_TENSOR_MAP_SWIZZLE_64B);
   if (!ok) return FORGE_ERR_LAUNCH;
   args.p = base_params(d_out, cfg, *d);   // the reduction runs over d_out
+  args.p.splits = cfg.splits;
   add_problem(args.p, cfg, d_in, bt, nullptr, nullptr);   // tile rows are tokens
-  set_grid(cfg, args.p.num_tiles, d->num_sms);
+  // Split partials, taken from the pool in stream order and given back after
+  // the reduce kernel; without the memory the launch runs unsplit (same
+  // result, slower).
+  void* ws = nullptr;
+  if (args.p.splits > 1) {
+    const size_t part_bytes = static_cast<size_t>(args.p.num_tiles) * cfg.cg * args.p.splits *
+                              kBM * cfg.bn * sizeof(float);
+    cudaMemPool_t pool = workspace_pool(*d);
+    if (pool && cudaMallocFromPoolAsync(&ws, part_bytes, pool, st) == cudaSuccess) {
+      args.p.part = static_cast<float*>(ws);
+    } else {
+      (void)cudaGetLastError();
+      ws = nullptr;
+      args.p.splits = 1;
+      args.p.num_units = args.p.num_tiles;
+    }
+  }
+  set_grid(cfg, args.p.num_units, d->num_sms);
   args.p.drop_first_arrival = take_drop_flag();
-  return launch_gemm(kModeDgrad, kFmtBF16, cfg, args, st) == cudaSuccess ? FORGE_OK
-                                                                         : FORGE_ERR_LAUNCH;
+  cudaError_t e = launch_gemm(kModeDgrad, kFmtBF16, cfg, args, st);
+  if (e == cudaSuccess && ws)
+    e = launch_dgrad_reduce(args.p.part, args.p.splits, cfg.cg, cfg.bn, args.p.prob[0].tiles_m,
+                            args.p.prob[0].tiles_n, bt, d_in, dX, d->num_sms, st);
+  if (ws) cudaFreeAsync(ws, st);
+  return e == cudaSuccess ? FORGE_OK : FORGE_ERR_LAUNCH;
 }
 
 forge_status forge_linear_backward(const void* X, const void* dY, void* W, void* dX,

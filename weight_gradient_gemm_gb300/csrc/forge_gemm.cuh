@@ -204,6 +204,14 @@ __device__ __forceinline__ bool wait_poll(uint32_t bar, uint32_t parity, const W
   return wait_bounded(bar, parity, w, site);
 }
 
+// The k-steps [kb, ke) of work unit u: split u % splits of its tile's num_k
+// steps (never empty: the host keeps splits <= num_k).
+__device__ __forceinline__ void split_range(int u, const GemmParams& p, int& kb, int& ke) {
+  const int z = u % p.splits;
+  kb = (z * p.num_k) / p.splits;
+  ke = ((z + 1) * p.num_k) / p.splits;
+}
+
 // Global tile index -> (layer, tile row, tile column).  Layers are laid out
 // one after another in the queue; inside a layer, groups of group_m tile rows
 // are walked column by column so that concurrent tiles share operand panels
@@ -500,6 +508,23 @@ __device__ __forceinline__ void epi_slice_store(uint32_t taddr, bool zero_grad, 
   }
 }
 
+// Split reduction of the input gradient.  A CTA's fp32 partial tile (128 rows
+// x BN) is laid out so that a warp's accesses are contiguous: column slice cb,
+// half h and quarter j of a thread's 16 columns form a run of 128 float4, one
+// per row, at float4 index ((cb * 2 + h) * 4 + j) * 128 + row.  The reduce
+// kernel (forge_dgrad_reduce.cu) reads the same layout.
+__device__ __forceinline__ void epi_part_write(uint32_t taddr, float* part, int cb, int h,
+                                               uint32_t row) {
+  uint32_t g[16];
+  tmem_ld_x16(taddr, g);
+  tmem_ld_wait();
+  float4* dst = reinterpret_cast<float4*>(part) + (cb * 2 + h) * 4 * kBM + row;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    __stcg(dst + j * kBM, make_float4(__uint_as_float(g[4 * j]), __uint_as_float(g[4 * j + 1]),
+                                      __uint_as_float(g[4 * j + 2]), __uint_as_float(g[4 * j + 3])));
+}
+
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
@@ -529,6 +554,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   const bool leader = (rank == 0);
   const int unit0 = kPair ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
   const int units = kPair ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
+  // work unit -> tile: the input gradient's split reduction gives each tile
+  // `splits` consecutive units; elsewhere a unit is a tile
+  auto tile_of = [&](int u) { return MODE == kModeDgrad ? u / p.splits : u; };
 
   const uint32_t bars = base + T::OFF_BARS;
   auto bar_full = [&](int s) { return bars + 8u * s; };
@@ -608,13 +636,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll
       for (int s = 0; s < T::STAGES; ++s) last_armed[s] = -1;
       bool ok = true;
-      for (int t = unit0; ok && t < p.num_tiles; t += units) {
+      for (int t = unit0; ok && t < p.num_units; t += units) {
         int tm, tn;
-        const int pi = tile_coords(t, p, tm, tn);
+        const int pi = tile_coords(tile_of(t), p, tm, tn);
         const GemmMaps& maps = a.maps[pi];
-        const GemmProblem& pr = p.prob[pi];
-        (void)pr;
-        for (int k = 0; k < p.num_k; ++k, ++cnt) {
+        int kb, ke;
+        split_range(t, p, kb, ke);
+        for (int k = kb; k < ke; ++k, ++cnt) {
           const int s = cnt % T::STAGES;
           const uint32_t ph = (cnt / T::STAGES) & 1u;
           if (!wait_stage<!kPair>(bar_empty(s), ph ^ 1u, wc, kSiteProducerEmpty)) { ok = false; break; }
@@ -660,13 +688,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       uint32_t cnt = 0;
       bool ok = true;
       int it = 0;
-      for (int t = unit0; ok && t < p.num_tiles; t += units, ++it) {
+      for (int t = unit0; ok && t < p.num_units; t += units, ++it) {
         const int buf = it & 1;
         const uint32_t use = (it >> 1) & 1;
         if (!wait_bounded(bar_tempty(buf), use ^ 1u, wc, kSiteMmaTmemEmpty)) { ok = false; break; }
         tc_fence_after_sync();
         const uint32_t d = tmem_base + buf * BN;
-        for (int k = 0; k < p.num_k; ++k, ++cnt) {
+        int kb, ke;
+        split_range(t, p, kb, ke);
+        for (int k = kb; k < ke; ++k, ++cnt) {
           const int s = cnt % T::STAGES;
           const uint32_t ph = (cnt / T::STAGES) & 1u;
           if (!wait_stage<!kPair>(bar_full(s), ph, wc, kSiteMmaFull)) { ok = false; break; }
@@ -679,9 +709,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                     : make_sdesc_mn_sw128(a0 + kk * 2048, kLBO, kSBO);
             const uint64_t bd = make_sdesc_mn_sw128(b0 + kk * 2048, kLBO, kSBO);
             if constexpr (kPair)
-              umma_bf16_pair(d, ad, bd, idesc, (k | kk) != 0 ? 1u : 0u);
+              umma_bf16_pair(d, ad, bd, idesc, (k != kb || kk != 0) ? 1u : 0u);
             else
-              umma_bf16(d, ad, bd, idesc, (k | kk) != 0 ? 1u : 0u);
+              umma_bf16(d, ad, bd, idesc, (k != kb || kk != 0) ? 1u : 0u);
           }
           // frees stage s in both CTAs once these MMAs have read it
           if constexpr (kPair) umma_commit_pair_mc(bar_empty(s), 0x3); else umma_commit(bar_empty(s));
@@ -690,7 +720,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if constexpr (kPair) {
           umma_commit_pair_mc(bar_tfull(buf), 0x3);
         } else {
-          if (p.num_k > 0)
+          if (ke > kb)
             umma_commit(bar_tfull(buf));
           else
             mbar_arrive(bar_tfull(buf));
@@ -716,12 +746,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll
       for (int j = 0; j < T::NS; ++j) last_armed[j] = -1;
       bool ok = true;
-      for (int t = unit0; ok && t < p.num_tiles; t += units) {
+      for (int t = unit0; ok && t < p.num_units; t += units) {
         int tm, tn;
-        const int pi = tile_coords(t, p, tm, tn);
+        const int pi = tile_coords(tile_of(t), p, tm, tn);
         const GemmMaps& maps = a.maps[pi];
         const GemmProblem& pr = p.prob[pi];
-        (void)pr;
         for (int s = 0; s < T::SLICES; ++s, ++cnt) {
           const int j = cnt % T::NS;
           const uint32_t ph = (cnt / T::NS) & 1u;
@@ -758,12 +787,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // slot as soon as its store has read it, off the epilogue's critical
     // path; the lanes wait on their own bulk groups, so one slow store does
     // not hold back the release of the other slots.
-    if (lane < T::NS) {
+    // (a split input-gradient launch writes only fp32 partials: no slots)
+    const bool split_launch = (MODE == kModeDgrad) && p.splits > 1;
+    if (lane < T::NS && !split_launch) {
       uint32_t cnt = 0;
       bool ok = true;
-      for (int t = unit0; ok && t < p.num_tiles; t += units) {
+      for (int t = unit0; ok && t < p.num_units; t += units) {
         int tm, tn;
-        const int pi = tile_coords(t, p, tm, tn);
+        const int pi = tile_coords(tile_of(t), p, tm, tn);
         const GemmMaps& maps = a.maps[pi];
         const GemmProblem& pr = p.prob[pi];
         for (int s = 0; s < T::SLICES; ++s, ++cnt) {
@@ -816,9 +847,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     auto load_scales = [&](int tt, float (&om)[NCB], float (&ov)[NCB]) {
 #pragma unroll
       for (int cb = 0; cb < NCB; ++cb) om[cb] = ov[cb] = 0.0f;
-      if (tt >= p.num_tiles) return;
+      if (tt >= p.num_units) return;
       int tm2, tn2;
-      const GemmProblem& q2 = p.prob[tile_coords(tt, p, tm2, tn2)];
+      const GemmProblem& q2 = p.prob[tile_coords(tile_of(tt), p, tm2, tn2)];
       const int y = tm2 * T::TM + static_cast<int>(rank) * kBM + part * T::RPS +
                     static_cast<int>(srow);
       if (y >= q2.d_out) return;
@@ -836,9 +867,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     uint32_t scnt = 0, xcnt = 0;
     int it = 0;
     bool ok = true;
-    for (int t = unit0; ok && t < p.num_tiles; t += units, ++it) {
+    for (int t = unit0; ok && t < p.num_units; t += units, ++it) {
       int tm, tn;
-      const int pi = tile_coords(t, p, tm, tn);
+      const int pi = tile_coords(tile_of(t), p, tm, tn);
       const GemmProblem& pr = p.prob[pi];
       const int scale_cols = pr.d_in / 128;
       if constexpr (T::I8) {
@@ -855,6 +886,28 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       // tcgen05.ld is warp-collective: the whole warp takes the same branch
       if (!__all_sync(0xffffffffu, good)) { ok = false; break; }
       tc_fence_after_sync();
+      // split input gradient: the unit writes its fp32 partial tile and frees
+      // the accumulator; the reduce kernel adds the splits afterwards
+      if constexpr (MODE == kModeDgrad) {
+        if (p.splits > 1) {
+          // partials indexed by tile row and column (not queue order)
+          const size_t ctile = (static_cast<size_t>(tm) * pr.tiles_n + tn) * CG + rank;
+          const size_t part_elems = static_cast<size_t>(kBM) * BN;
+          float* mine = p.part + (ctile * p.splits + t % p.splits) * part_elems;
+#pragma unroll 1
+          for (int cb = 0; cb < BN / T::SW; ++cb)
+            epi_part_write(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN +
+                               cb * T::SW + h * T::HALF,
+                           mine, cb, h, row);
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (kPair) mbar_arrive_cluster(mapa_shared(bar_tempty(buf), 0));
+            else mbar_arrive(bar_tempty(buf));
+          }
+          continue;
+        }
+      }
       for (int s = 0; s < T::SLICES; ++s, ++scnt) {
         if (T::PARTS > 1 && (s % T::PARTS) != part) continue;   // the other half's slot
         const int j = scnt % T::NS;

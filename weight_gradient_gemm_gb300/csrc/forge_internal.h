@@ -53,6 +53,13 @@ struct GemmProblem {
 struct GemmParams {
   int32_t bt, num_k;          // shared token count of every layer in the launch
   int32_t nprob, num_tiles;   // layers, and tiles over all of them
+  // Split reduction (input gradient only; 1 elsewhere): each tile's k-steps
+  // are cut into `splits` contiguous ranges, one work unit each, so the queue
+  // holds num_units = num_tiles * splits units, the splits of a tile next to
+  // each other.  Every unit writes its fp32 partial tile to `part`; the
+  // reduce kernel then adds the partials in split order and stores dX.
+  int32_t splits, num_units;
+  float* part;                // [tile row][tile column][CTA of the pair][split][128 x BN] fp32
   int32_t group_m;            // tile-order swizzle: rows of tiles per group
   AdamWConsts h;
   GemmProblem prob[kMaxGroup];
@@ -82,6 +89,7 @@ struct GemmConfig {
   int grid;      // persistent CTAs (even for CTA pairs)
   int group_m;
   int poll_store;  // store lanes poll the slot-done barrier instead of suspending
+  int splits;      // input gradient: k-ranges per tile (GemmParams::splits); 1 elsewhere
 };
 
 // Tokens per operand pipeline stage (the TMA box height of dY and X), used
@@ -107,6 +115,12 @@ __host__ __device__ constexpr int slot_rows(int mode, int fmt, int prof) {
 // Launchers (one per instantiated kernel family); return a CUDA error.
 cudaError_t launch_gemm(int mode, int fmt, const GemmConfig& cfg, const GemmArgs& args,
                         cudaStream_t stream);
+
+// The input gradient's split reduction: dX[r][c] = sum over z of the fp32
+// partials (in split order), rounded once to bf16.
+cudaError_t launch_dgrad_reduce(const float* part, int splits, int cg, int bn, int tiles_m,
+                                int tiles_n, int64_t rows, int64_t d_in, void* dX, int num_sms,
+                                cudaStream_t stream);
 
 cudaError_t launch_adamw(const void* dW, int dw_fmt, void* W, void* m, void* v, float* m_scale,
                          float* v_scale, int64_t d_in, int64_t d_out, int fmt,

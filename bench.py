@@ -334,6 +334,44 @@ def run_gpu(args, rank, world, dev):
     unf_ms = u0.elapsed_time(u1) / unf_steps
     assert F.device_error() == 0
 
+    # ---- the layer's whole backward step (diagnostic, not the reported
+    # value): forge_linear_backward per projection (dX = dY W from the weight
+    # before the update, then the fused step), dX alone (forge_dgrad), and
+    # cuBLAS's dX (torch.matmul) on the same tensors for scale
+    bw_steps = max(3, min(args.steps, 30))
+    dx = [torch.empty((bt, it["d_in"]), dtype=torch.bfloat16, device=dev) for it in layer.items]
+
+    def per_step_ms(fn):
+        fn()
+        torch.cuda.synchronize()
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for _ in range(bw_steps):
+            fn()
+        b1.record(stream)
+        torch.cuda.synchronize()
+        return b0.elapsed_time(b1) / bw_steps
+
+    def dgrad_all():
+        for it, o in zip(layer.items, dx):
+            F.dgrad(it["dy"], it["w"], o)
+
+    def cublas_dgrad_all():
+        for it, o in zip(layer.items, dx):
+            torch.matmul(it["dy"], it["w"], out=o)
+
+    def backward_all():
+        nonlocal step
+        step += 1
+        for it, o in zip(layer.items, dx):
+            F.linear_backward(it["x"], it["dy"], it["w"], o, it["m"], it["v"], step=step,
+                              m_scale=it["ms"], v_scale=it["vs"], **HYPER)
+
+    backward = dict(dgrad_ms=per_step_ms(dgrad_all), cublas_dgrad_ms=per_step_ms(cublas_dgrad_all),
+                    linear_backward_ms=per_step_ms(backward_all),
+                    dgrad_config=F.describe_dgrad_config(bt, 4096, 14336))
+    assert F.device_error() == 0
+
     # ---- end to end through the public API with host buffers: every step
     # copies its X and dY from pinned host memory, runs the grouped fused call
     # and reads back the library's status word (4 bytes).  As a training loop
@@ -378,7 +416,7 @@ def run_gpu(args, rank, world, dev):
         e2e_ms, unf_ms = max_over_ranks([e2e_ms, unf_ms], dev)
 
     return dict(layer=layer, elapsed_ms=elapsed_ms, kern_ms=kern_ms, unf_ms=unf_ms,
-                per_proj_ms=per_proj_ms,
+                per_proj_ms=per_proj_ms, backward=backward,
                 e2e_ms=e2e_ms, clocks=sampler.summary(w0, w1) if sampler else None,
                 config=F.describe_config(bt, 4096, 4096, fmt))
 
@@ -656,6 +694,28 @@ def run_reference(args):
 
 # ---------------------------------------------------------------------------
 
+def backward_block(bw, flops, fused_ms, peaks, peak_kind):
+    """The backward-step diagnostic: dX = dY W for the seven projections
+    (the same FLOPs as the weight gradient) against the bf16 tensor peak for
+    a kernel timed on its own (burst), next to cuBLAS on the same tensors, and
+    the whole forge_linear_backward step."""
+    peak = peaks["bf16_tflops"]
+    dgrad_tf = flops / (bw["dgrad_ms"] * 1e-3) / 1e12
+    return {
+        "dgrad": {"ms_per_step": bw["dgrad_ms"], "tflops": dgrad_tf,
+                  "roofline": {"bound": "tensor", "achieved": dgrad_tf, "peak": peak,
+                               "unit": "TFLOP/s", "frac": dgrad_tf / peak,
+                               "peak_kind": f"{peak_kind} (cuBLAS bf16, burst)"},
+                  "kernel_gate_up": bw["dgrad_config"],
+                  "cublas_ms_per_step": bw["cublas_dgrad_ms"],
+                  "vs_cublas": bw["cublas_dgrad_ms"] / bw["dgrad_ms"]},
+        "ms_per_step": bw["linear_backward_ms"],
+        "tflops": 2.0 * flops / (bw["linear_backward_ms"] * 1e-3) / 1e12,
+        "fused_step_ms": fused_ms,
+        "path": "forge_linear_backward per projection: forge_dgrad then forge_wgrad_adamw",
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -762,6 +822,7 @@ def main():
                            + 2.0 * bt * (it["d_in"] + it["d_out"])) / (t * 1e-3) / 1e9, 1),
              "tflops": round(2.0 * bt * it["d_in"] * it["d_out"] / (t * 1e-3) / 1e12, 1)}
             for it, t in zip(layer.items, res["per_proj_ms"])],
+        "linear_backward": backward_block(res["backward"], flops, ms, peaks, peak_kind),
         "gpu_launches": launches,
         "clocks": res["clocks"],
     }

@@ -225,6 +225,11 @@ const char* forge_status_string(forge_status status);
 int forge_describe_config(int64_t bt, int64_t d_in, int64_t d_out,
                           forge_moment_fmt fmt, char* buf, int len);
 
+/* The same for forge_dgrad on a [bt, d_out] x [d_out, d_in] problem: tile,
+ * CTA grouping, profile, grid and the number of k-ranges the reduction over
+ * d_out is split into.  Returns the bytes needed, or -1 for an invalid shape. */
+int forge_describe_dgrad_config(int64_t bt, int64_t d_in, int64_t d_out, char* buf, int len);
+
 /* Diagnostics for FORGE_ERR_DEVICE_TIMEOUT: where the first timed-out wait
  * since the last call happened, as site*100000 + block*100 (site 1 operand
  * slot free, 2 accumulator free, 3 operands landed, 4 state slot free,

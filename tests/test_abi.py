@@ -20,7 +20,7 @@ def test_header_declares_the_boundary():
     names = F.header_functions()
     for n in ("forge_wgrad_adamw", "forge_wgrad", "forge_adamw", "forge_device_error",
               "forge_status_string", "forge_wgrad_adamw_grouped", "forge_dgrad",
-              "forge_linear_backward"):
+              "forge_linear_backward", "forge_describe_dgrad_config"):
         assert n in names
 
 
@@ -45,6 +45,28 @@ def test_describe_config_without_gpu(L):
     assert "slice=128" in F.describe_config(4096, 4096, 1024, F.MOM_INT8_B128)
     with pytest.raises(ValueError):
         F.describe_config(512, 4097, 4096)
+
+
+def test_dgrad_split_choice_without_gpu(L, monkeypatch):
+    # host logic only (152 SMs assumed without a device).  dX of the
+    # Llama-3.1-8B gate/up projections (d_out = 14336, d_in = 4096): at 512
+    # tokens 32 pair tiles for 76 SM pairs, so the reduction over d_out is
+    # split; from 1024 tokens on the cost estimate keeps it whole
+    monkeypatch.delenv("FORGE_SPLITS", raising=False)
+    s = F.describe_dgrad_config(512, 4096, 14336)
+    assert "tile=256x256" in s and "ctas=2" in s and "splits=2" in s, s
+    assert "grid=128" in s, s                       # 64 units -> 64 pairs
+    for bt in (1024, 2048, 4096, 8192):
+        assert "splits=1" in F.describe_dgrad_config(bt, 4096, 14336)
+    # the k projection (d_out = 1024: 16 k-steps) is too short to split
+    assert "splits=1" in F.describe_dgrad_config(512, 4096, 1024)
+    # the override is clamped to splits of at least 8 k-steps
+    monkeypatch.setenv("FORGE_SPLITS", "8")
+    assert "splits=8" in F.describe_dgrad_config(512, 4096, 14336)
+    assert "splits=2" in F.describe_dgrad_config(512, 4096, 1024)
+    assert "splits=1" in F.describe_dgrad_config(512, 4096, 512)
+    with pytest.raises(ValueError):
+        F.describe_dgrad_config(512, 4097, 4096)
 
 
 A = 1 << 20      # fake, 16-byte aligned addresses: never dereferenced

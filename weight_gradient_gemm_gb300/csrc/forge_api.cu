@@ -805,6 +805,28 @@ int forge_describe_config(int64_t bt, int64_t d_in, int64_t d_out, forge_moment_
   return need + 1;
 }
 
+int forge_describe_dgrad_config(int64_t bt, int64_t d_in, int64_t d_out, char* buf, int len) {
+  if (check_shape(bt, d_in, d_out) != FORGE_OK) return -1;
+  int sms = 152;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+      sms = n;
+  }
+  GemmConfig c = choose_dgrad_config(bt, d_in, d_out, sms);
+  const int64_t tiles = ((bt + kBM * c.cg - 1) / (kBM * c.cg)) * ((d_in + c.bn - 1) / c.bn);
+  set_grid(c, tiles * c.splits, sms);
+  const int need = std::snprintf(buf, buf ? len : 0,
+                                 "tile=%dx%d ctas=%d bk=%d grid=%d splits=%d profile=%s",
+                                 kBM * c.cg, c.bn, c.cg, bk_of(c.cg), c.grid, c.splits,
+                                 c.prof == kProfStream ? "stream"
+                                 : c.prof == kProfMma  ? "mma"
+                                 : c.prof == kProfDeep ? "deep"
+                                                       : "balanced");
+  return need + 1;
+}
+
 int forge_debug_timeout_site(void) {
   DeviceInfo* d = nullptr;
   if (device_info(&d) != FORGE_OK) return -1;

@@ -112,14 +112,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Acquire-release fence at GPU scope.  One thread issues it to publish (before
-// a relaxed atomic) or to consume (after one) on behalf of threads of its CTA
-// that synchronised with it through a CTA-scope barrier, as in a split-K
-// semaphore; a fence per writing thread is not needed and serialises.
-__device__ __forceinline__ void fence_acq_rel_gpu() {
-  asm volatile("fence.acq_rel.gpu;" ::: "memory");
-}
-
 // ---------------------------------------------------------------------------
 // Named barriers (ids 1..15; id 0 is __syncthreads)
 // ---------------------------------------------------------------------------

@@ -84,6 +84,8 @@ def lib() -> ctypes.CDLL:
             L.forge_status_string.restype = ctypes.c_char_p
             L.forge_describe_config.argtypes = [i64, i64, i64, st, ctypes.c_char_p, st]
             L.forge_describe_config.restype = st
+            L.forge_describe_dgrad_config.argtypes = [i64, i64, i64, ctypes.c_char_p, st]
+            L.forge_describe_dgrad_config.restype = st
             L.forge_debug_timeout_site.argtypes = []
             L.forge_debug_timeout_site.restype = st
             L.forge_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
@@ -266,6 +268,16 @@ def describe_config(bt: int, d_in: int, d_out: int, fmt: int = MOM_FP32) -> str:
         raise ValueError("invalid shape or format")
     buf = ctypes.create_string_buffer(n)
     lib().forge_describe_config(bt, d_in, d_out, fmt, buf, n)
+    return buf.value.decode()
+
+
+def describe_dgrad_config(bt: int, d_in: int, d_out: int) -> str:
+    """The configuration forge_dgrad would use for dY [bt, d_out], W [d_out, d_in]."""
+    n = lib().forge_describe_dgrad_config(bt, d_in, d_out, None, 0)
+    if n < 0:
+        raise ValueError("invalid shape")
+    buf = ctypes.create_string_buffer(n)
+    lib().forge_describe_dgrad_config(bt, d_in, d_out, buf, n)
     return buf.value.decode()
 
 

@@ -181,6 +181,21 @@ forge_status forge_dgrad(const void* dY, const void* W, void* dX,
                          int64_t bt, int64_t d_in, int64_t d_out, forge_stream stream);
 
 /*
+ * forge_dgrad_noalloc: forge_dgrad that allocates nothing.  When it splits
+ * the reduction, the fp32 partials go to a 32 MiB scratch array the library
+ * reserves statically on each device when it loads, instead of the pool; a
+ * split that needs more runs with fewer splits (down to none).  With the
+ * same split count the result is bit for bit that of forge_dgrad.  Same
+ * arguments, layout and errors as forge_dgrad.
+ * Precondition (documented, not checked): the scratch is one per device, so
+ * two forge_dgrad_noalloc calls on one device must not run at the same time
+ * (issue them on one stream, or order the streams); forge_dgrad calls may
+ * run beside them.
+ */
+forge_status forge_dgrad_noalloc(const void* dY, const void* W, void* dX, int64_t bt,
+                                 int64_t d_in, int64_t d_out, forge_stream stream);
+
+/*
  * forge_linear_backward: the layer's whole backward step with the fused
  * update: dX = dY W from the weight before the update (Algorithm 1 computes
  * the input gradient first; Appendix A, Remark 2), then forge_wgrad_adamw.

@@ -20,7 +20,7 @@ def test_header_declares_the_boundary():
     names = F.header_functions()
     for n in ("forge_wgrad_adamw", "forge_wgrad", "forge_adamw", "forge_device_error",
               "forge_status_string", "forge_wgrad_adamw_grouped", "forge_dgrad",
-              "forge_linear_backward", "forge_describe_dgrad_config"):
+              "forge_linear_backward", "forge_describe_dgrad_config", "forge_dgrad_noalloc"):
         assert n in names
 
 
@@ -127,6 +127,12 @@ def test_dgrad_and_linear_backward_argument_errors(L):
     assert L.forge_dgrad(B, C, A, 64, 250, 128, None) == 3
     assert L.forge_dgrad(B, C, C, 64, 256, 128, None) == 6          # dX over W
     assert L.forge_dgrad(None, None, None, 0, 256, 128, None) == 0  # no tokens: nothing to do
+    # the variant without allocation checks its arguments the same way
+    assert L.forge_dgrad_noalloc(B, C, None, 64, 256, 128, None) == 1
+    assert L.forge_dgrad_noalloc(B, C + 4, A, 64, 256, 128, None) == 2
+    assert L.forge_dgrad_noalloc(B, C, A, 64, 250, 128, None) == 3
+    assert L.forge_dgrad_noalloc(B, C, C, 64, 256, 128, None) == 6
+    assert L.forge_dgrad_noalloc(None, None, None, 0, 256, 128, None) == 0
     m, v = F.ForgeMoment(D, None), F.ForgeMoment(D + (1 << 36), None)
     args = (256, 128, 1e-3, 0.9, 0.999, 1e-8, 0.01)
     assert L.forge_linear_backward(A, B, C, None, m, v, 64, *args, 1, 0, None) == 1

@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
             L.forge_adamw.restype = st
             L.forge_dgrad.argtypes = [vp, vp, vp, i64, i64, i64, vp]
             L.forge_dgrad.restype = st
+            L.forge_dgrad_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+            L.forge_dgrad_noalloc.restype = st
             L.forge_linear_backward.argtypes = [vp, vp, vp, vp, ForgeMoment, ForgeMoment, i64,
                                                 i64, i64, f32, f32, f32, f32, f32, i64, st, vp]
             L.forge_linear_backward.restype = st
@@ -217,6 +219,19 @@ def dgrad(dY: torch.Tensor, W: torch.Tensor, dX: torch.Tensor, stream=None) -> N
     d_in = W.shape[1]
     _check(lib().forge_dgrad(_ptr(dY), _ptr(W), _ptr(dX), bt, d_in, d_out, _stream(stream)),
            "forge_dgrad")
+
+
+def dgrad_noalloc(dY: torch.Tensor, W: torch.Tensor, dX: torch.Tensor, stream=None) -> None:
+    """dgrad with its split partials in the library's static scratch (no
+    allocation); calls of it on one device must not overlap in time."""
+    for t, n in ((dY, "dY"), (W, "W"), (dX, "dX")):
+        _dense(t, n)
+    if dX.dtype != torch.bfloat16:
+        raise TypeError("dX must be bf16")
+    bt, d_out = dY.shape
+    d_in = W.shape[1]
+    _check(lib().forge_dgrad_noalloc(_ptr(dY), _ptr(W), _ptr(dX), bt, d_in, d_out,
+                                     _stream(stream)), "forge_dgrad_noalloc")
 
 
 def linear_backward(X: torch.Tensor, dY: torch.Tensor, W: torch.Tensor, dX: torch.Tensor,

@@ -157,3 +157,94 @@ def test_dgrad_mistakes_are_caught(monkeypatch, kind):
             lambda: P.test_dgrad_one_hot_closed_form(7, 7),
             P.test_dgrad_and_wgrad_are_adjoint_to_the_forward_pass]
     assert _fails_one(pins)
+
+
+# ---------------------------------------------------------------------------
+# regime-1 optimizers (oracle/regime1.py)
+# ---------------------------------------------------------------------------
+
+import oracle.regime1 as R  # noqa: E402
+from tests import test_oracle_regime1_pins as PR  # noqa: E402
+
+_ORIG_OPT = R.opt_f64
+
+
+def _opt_variant(kind):
+    def f(opt, G, W, s1, s2, hyper, t):
+        h = hyper.as_f64()
+        lr, wd, eps, b1, b2 = h["lr"], h["weight_decay"], h["eps"], h["beta1"], h["beta2"]
+        g = G + wd * W
+        if kind == "momentum_dampened" and opt == R.OPT_SGD_MOMENTUM:
+            b = h["momentum"] * s1 + (1 - h["momentum"]) * g
+            return W - lr * b, b, None
+        if kind == "adagrad_no_accumulation" and opt == R.OPT_ADAGRAD:
+            s = g * g
+            return W - lr * g / (np.sqrt(s) + eps), s1 + g * g, None
+        if kind == "rmsprop_alpha_swapped" and opt == R.OPT_RMSPROP:
+            s = (1 - h["alpha"]) * s1 + h["alpha"] * g * g
+            return W - lr * g / (np.sqrt(s) + eps), s, None
+        if kind == "rmsprop_decoupled_decay" and opt == R.OPT_RMSPROP:
+            s = h["alpha"] * s1 + (1 - h["alpha"]) * G * G
+            return (1 - lr * wd) * W - lr * G / (np.sqrt(s) + eps), s, None
+        if kind == "lion_sign_of_new_state" and opt == R.OPT_LION:
+            m = b2 * s1 + (1 - b2) * G
+            return (1 - lr * wd) * W - lr * np.sign(m), m, None
+        if kind == "lion_coupled_decay" and opt == R.OPT_LION:
+            c = b1 * s1 + (1 - b1) * g
+            return W - lr * np.sign(c), b2 * s1 + (1 - b2) * g, None
+        if kind.startswith("nadam") and opt == R.OPT_NADAM:
+            m = b1 * s1 + (1 - b1) * g
+            v = b2 * s2 + (1 - b2) * g * g
+            mu_t, mu_next, prod = R.nadam_scalars(h, t)
+            if kind == "nadam_mu_next_is_mu_t":
+                mu_next = mu_t
+            bc2 = 1.0 if kind == "nadam_no_bias_correction" else 1 - b2 ** t
+            d = np.sqrt(v / bc2) + eps
+            return (W - lr * (1 - mu_t) / (1 - prod) * g / d
+                    - lr * mu_next / (1 - prod * mu_next) * m / d), m, v
+        if kind.startswith("radam") and opt == R.OPT_RADAM:
+            m = b1 * s1 + (1 - b1) * g
+            v = b2 * s2 + (1 - b2) * g * g
+            mhat = m if kind == "radam_no_bias_correction" else m / (1 - b1 ** t)
+            rect, r = R.radam_scalars(h, t)
+            if kind == "radam_never_rectified":
+                rect = False
+            if rect:
+                return W - lr * mhat * r * np.sqrt(1 - b2 ** t) / (np.sqrt(v) + eps), m, v
+            return W - lr * mhat, m, v
+        return _ORIG_OPT(opt, G, W, s1, s2, hyper, t)
+    return f
+
+
+@pytest.mark.parametrize("kind", [
+    "momentum_dampened", "adagrad_no_accumulation", "rmsprop_alpha_swapped",
+    "rmsprop_decoupled_decay", "lion_sign_of_new_state", "lion_coupled_decay",
+    "nadam_mu_next_is_mu_t", "nadam_no_bias_correction", "radam_no_bias_correction",
+    "radam_never_rectified"])
+def test_regime1_mistakes_are_caught(monkeypatch, kind):
+    f = _opt_variant(kind)
+    monkeypatch.setattr(R, "opt_f64", f)
+    monkeypatch.setattr(O, "opt_f64", f)
+    torch_pins = [(lambda o=o: _with_f64_default(lambda: PR.test_matches_torch_optim_f64(o, None)))
+                  for o in PR.TORCH_OPTS]
+    pins = torch_pins + [PR.test_lion_closed_forms,
+                         PR.test_first_momentum_step_is_sgd_and_zero_gradient_cases]
+    assert _fails_one(pins)
+
+
+def _with_f64_default(fn):
+    import torch
+    old = torch.get_default_dtype()
+    torch.set_default_dtype(torch.float64)
+    try:
+        fn()
+    finally:
+        torch.set_default_dtype(old)
+
+
+def test_regime1_pins_pass_on_the_unmodified_oracle():
+    # the control for the cases above: with nothing planted no pin fails
+    pins = [(lambda o=o: _with_f64_default(lambda: PR.test_matches_torch_optim_f64(o, None)))
+            for o in PR.TORCH_OPTS]
+    pins += [PR.test_lion_closed_forms, PR.test_first_momentum_step_is_sgd_and_zero_gradient_cases]
+    assert not _fails_one(pins)

@@ -153,6 +153,69 @@ forge_status forge_wgrad_adamw_grouped(const forge_linear* layers, int n, int64_
                                        forge_moment_fmt fmt, forge_stream stream);
 
 /*
+ * The other coordinate-wise optimizers FORGE fuses: the families the page
+ * lists as entering their state one coordinate at a time (section 1; the
+ * definition of a tile-local state update, section 2; the appendix table of
+ * optimizer families, regime 1).  The page checks each against a reference
+ * PyTorch implementation; these are torch.optim's definitions with default
+ * options, and Chen et al.'s for Lion.  With G the accumulator tile and
+ * g = G + weight_decay * W (L2 decay, the pre-update W):
+ *   SGD           W -= lr g                                          no state
+ *   SGD_MOMENTUM  b = momentum b + g;  W -= lr b                     s1 = b
+ *   ADAGRAD       s += g^2;  W -= lr g / (sqrt(s) + eps)             s1 = s
+ *   RMSPROP       s = alpha s + (1 - alpha) g^2;
+ *                 W -= lr g / (sqrt(s) + eps)                        s1 = s
+ *   LION          c = beta1 m + (1 - beta1) G;
+ *                 W = (1 - lr weight_decay) W - lr sign(c)  (decoupled decay);
+ *                 m = beta2 m + (1 - beta2) G                        s1 = m
+ *   NADAM         torch.optim.NAdam: m, v moving averages of g, g^2;
+ *                 mu_i = beta1 (1 - 0.5 * 0.96^(i momentum_decay)), P_t = prod_{i<=t} mu_i;
+ *                 W -= lr [(1 - mu_t)/(1 - P_t) g + mu_{t+1}/(1 - P_t mu_{t+1}) m]
+ *                      / (sqrt(v / (1 - beta2^t)) + eps)             s1 = m, s2 = v
+ *   RADAM         torch.optim.RAdam: m, v as NAdam; with rho_t > 5,
+ *                 W -= lr r_t sqrt(1 - beta2^t) m / ((1 - beta1^t)(sqrt(v) + eps)),
+ *                 else W -= lr m / (1 - beta1^t)                     s1 = m, s2 = v
+ * States start at zero.  Every stored value is rounded once to nearest even.
+ */
+typedef enum {
+  FORGE_OPT_SGD = 0,
+  FORGE_OPT_SGD_MOMENTUM = 1,
+  FORGE_OPT_ADAGRAD = 2,
+  FORGE_OPT_RMSPROP = 3,
+  FORGE_OPT_LION = 4,
+  FORGE_OPT_NADAM = 5,
+  FORGE_OPT_RADAM = 6
+} forge_optimizer;
+
+/* Hyperparameters of forge_wgrad_opt; an optimizer reads only its own. */
+typedef struct {
+  float lr, weight_decay;   /* all; >= 0 and finite                                 */
+  float beta1, beta2;       /* LION, NADAM, RADAM; in [0, 1)                        */
+  float eps;                /* ADAGRAD, RMSPROP, NADAM, RADAM; >= 0 and finite      */
+  float momentum;           /* SGD_MOMENTUM; in [0, 1)                              */
+  float alpha;              /* RMSPROP; in [0, 1)                                   */
+  float momentum_decay;     /* NADAM (torch's psi, 0.004 by default); >= 0, finite  */
+} forge_opt_hyper;
+
+/*
+ * forge_wgrad_opt: the fused step of forge_wgrad_adamw with optimizer `opt`
+ * in place of AdamW: G = dY^T X accumulated on chip, the update applied in
+ * the epilogue, only W and the optimizer's states written back.
+ *   s1, s2  the optimizer's states (see the table above), fmt FORGE_MOM_FP32
+ *           or FORGE_MOM_BF16, [d_out, d_in], updated in place; the `scale`
+ *           fields are unused, and so are states the optimizer does not have
+ *           (they may be NULL).
+ * Errors: FORGE_ERR_HYPER for an unknown optimizer, a NULL `hyper`, step < 1
+ * or a hyperparameter out of range; FORGE_ERR_FORMAT for int8 states; the
+ * shape, NULL, alignment and overlap errors of forge_wgrad_adamw.
+ * Asynchronous on `stream`; the ordering precondition on dX applies.
+ */
+forge_status forge_wgrad_opt(const void* X, const void* dY, void* W, forge_moment s1,
+                             forge_moment s2, int64_t bt, int64_t d_in, int64_t d_out,
+                             forge_optimizer opt, const forge_opt_hyper* hyper, int64_t step,
+                             forge_moment_fmt fmt, forge_stream stream);
+
+/*
  * forge_wgrad: the unfused gradient, dW = dY^T X stored to global memory
  * (the "store-G control" of the FORGE page's Appendix D).  It runs the same
  * tensor-core main loop as forge_wgrad_adamw, so with dw_dtype = FORGE_DT_FP32

@@ -131,3 +131,61 @@ def check_step(gpu_w_bits, gpu_m, gpu_v, ref_inputs, hyper, t, fmt, bt, label=""
                               f" max code diff={int(np.max(np.abs(gc - cs[1])))}")
             assert not s_bad.any() and not c_bad.any(), f"{label} {which}: {reports[which]}"
     return reports
+
+
+def check_opt_step(gpu_w_bits, gpu_states, ref_inputs, opt, hyper, t, fmt, bt, label=""):
+    """check_step for the other optimizers (oracle/regime1.py): W within 1 ulp
+    of the oracle range over G +- tau (and the same share within 1 ulp as for
+    AdamW), fp32 states within 1e-5 relative plus the propagated tau, bf16
+    states within 1 ulp of the range.
+
+    "Relative" for an fp32 state is taken against the larger of the result
+    and the magnitude of the terms it is formed from (the same update on
+    |G| + tau, |W| and |state|): a state such as m' = beta1 m + (1 - beta1) g
+    can cancel, and fp32 arithmetic errs by a unit of its terms, not of the
+    result.  With tokens the tau spread already covers this; without tokens
+    (G = 0) it is the only allowance.
+
+    ref_inputs: G, S, W_bits and states [Moment or None, Moment or None] the
+    step started from; gpu_states the GPU's states (Moment or None)."""
+    G, S = ref_inputs["G"], ref_inputs["S"]
+    tau = tau_bound(S, bt)
+    W = O.bf16_to_f64(ref_inputs["W_bits"])
+    n = O.OPT_STATES[opt]
+    st0 = [O.decode_moment(s, False) if i < n else None
+           for i, s in enumerate(ref_inputs["states"])]
+    outs = [O.opt_f64(opt, G + d, W, st0[0], st0[1], hyper, t) for d in (-tau, 0.0 * tau, tau)]
+    mag = O.opt_f64(opt, np.abs(G) + tau, np.abs(W),
+                    None if st0[0] is None else np.abs(st0[0]),
+                    None if st0[1] is None else np.abs(st0[1]), hyper, t)
+    wb = [bf16_ordered(O.f64_to_bf16(x[0])) for x in outs]
+    wlo, whi = np.minimum.reduce(wb), np.maximum.reduce(wb)
+    g = bf16_ordered(gpu_w_bits)
+    viol = (g < wlo - 1) | (g > whi + 1)
+    sensitive = whi > wlo
+    d = np.abs(g - wb[1])
+    ns = ~sensitive
+    rep = Report(int(g.size), float(np.mean(d[ns] <= 1)) if ns.any() else 1.0,
+                 int(d[ns].max()) if ns.any() else 0, int(sensitive.sum()), int(viol.sum()))
+    assert rep.violations == 0, f"{label} W: {rep}"
+    assert rep.frac_within_1 >= 0.9999 and rep.max_ulp <= 2, f"{label} W: {rep}"
+    reports = {"W": rep}
+    for i in range(n):
+        idx = i + 1
+        name = f"s{idx}"
+        if fmt == O.FMT_FP32:
+            ref = outs[1][idx]
+            got = gpu_states[i].data.astype(np.float64)
+            spread = np.maximum(np.abs(outs[0][idx] - ref), np.abs(outs[2][idx] - ref))
+            err = np.abs(got - ref)
+            scale = np.maximum(np.abs(ref), np.abs(mag[idx]))
+            nv = int(np.sum(err > 1e-5 * scale + spread + 1e-38))
+            reports[name] = f"max rel {float(np.max(err / np.maximum(np.abs(ref), 1e-30))):.2e} violations={nv}"
+        else:
+            rb = [bf16_ordered(O.f64_to_bf16(x[idx])) for x in outs]
+            rlo, rhi = np.minimum.reduce(rb), np.maximum.reduce(rb)
+            got = bf16_ordered(gpu_states[i].data)
+            nv = int(np.sum((got < rlo - 1) | (got > rhi + 1)))
+            reports[name] = f"max ulp {int(np.max(np.abs(got - rb[1])))} violations={nv}"
+        assert nv == 0, f"{label} {name}: {reports[name]}"
+    return reports

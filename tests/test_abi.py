@@ -20,7 +20,8 @@ def test_header_declares_the_boundary():
     names = F.header_functions()
     for n in ("forge_wgrad_adamw", "forge_wgrad", "forge_adamw", "forge_device_error",
               "forge_status_string", "forge_wgrad_adamw_grouped", "forge_dgrad",
-              "forge_linear_backward", "forge_describe_dgrad_config", "forge_dgrad_noalloc"):
+              "forge_linear_backward", "forge_describe_dgrad_config", "forge_dgrad_noalloc",
+              "forge_wgrad_opt"):
         assert n in names
 
 
@@ -141,6 +142,43 @@ def test_dgrad_and_linear_backward_argument_errors(L):
     assert L.forge_linear_backward(A, B, C, G + 4, m, v, 64, *args, 1, 0, None) == 2
     # a bad step is caught before the input gradient is enqueued
     assert L.forge_linear_backward(A, B, C, G, m, v, 64, *args, 0, 0, None) == 5
+
+
+def opt_call(L, opt=1, s1=D, s2=None, X=A, dY=B, W=C, bt=64, d_in=256, d_out=128, step=1,
+             fmt=0, **hk):
+    h = dict(lr=1e-3, weight_decay=0.01, beta1=0.9, beta2=0.999, eps=1e-8, momentum=0.9,
+             alpha=0.99, momentum_decay=4e-3)
+    h.update(hk)
+    hp = F.ForgeOptHyper(*[h[k] for k in ("lr", "weight_decay", "beta1", "beta2", "eps",
+                                          "momentum", "alpha", "momentum_decay")])
+    return L.forge_wgrad_opt(X, dY, W, F.ForgeMoment(s1, None), F.ForgeMoment(s2, None), bt,
+                             d_in, d_out, opt, ctypes.byref(hp), step, fmt, None)
+
+
+def test_wgrad_opt_argument_errors(L):
+    # codes: 1 NULL, 2 ALIGN, 3 SHAPE, 4 FORMAT, 5 HYPER, 6 ALIAS; 10 = valid
+    # arguments that reached the device query (no GPU here)
+    assert opt_call(L) == 10
+    assert opt_call(L, opt=0, s1=None) == 10                 # SGD keeps no state
+    assert opt_call(L, opt=5, s2=D + (1 << 36)) == 10        # NAdam: two states
+    assert opt_call(L, s1=None) == 1                         # momentum buffer missing
+    assert opt_call(L, opt=6) == 1                           # RAdam needs s2 too
+    assert opt_call(L, W=None) == 1
+    assert opt_call(L, s1=D + 4) == 2
+    assert opt_call(L, d_in=250) == 3
+    assert opt_call(L, fmt=2) == 4                           # no int8 state here
+    assert opt_call(L, opt=7) == 5
+    assert opt_call(L, step=0) == 5
+    assert opt_call(L, opt=4, beta1=1.0) == 5                # Lion betas in [0, 1)
+    assert opt_call(L, opt=2, eps=-1.0) == 5                 # Adagrad eps >= 0
+    assert opt_call(L, opt=3, alpha=1.0) == 5                # RMSprop alpha < 1
+    assert opt_call(L, momentum=float("nan")) == 5
+    assert opt_call(L, lr=float("inf")) == 5
+    assert opt_call(L, s1=C) == 6                            # state over W
+    assert opt_call(L, X=C) == 6                             # input over W
+    assert opt_call(L, opt=5, s1=D, s2=D) == 6               # the two states overlap
+    assert L.forge_wgrad_opt(A, B, C, F.ForgeMoment(D, None), F.ForgeMoment(None, None), 64,
+                             256, 128, 1, None, 1, 0, None) == 5    # no hyperparameters
 
 
 def grouped(L, layers, bt=64, step=1, fmt=0):

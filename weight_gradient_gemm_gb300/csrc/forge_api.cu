@@ -30,6 +30,8 @@ cudaError_t launch_gemm_fused_i8(const GemmConfig&, const GemmArgs&, cudaStream_
 cudaError_t launch_gemm_store_f32(const GemmConfig&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_store_bf16(const GemmConfig&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_dgrad(const GemmConfig&, const GemmArgs&, cudaStream_t);
+cudaError_t launch_gemm_opt_f32(const GemmConfig&, const GemmArgs&, cudaStream_t);
+cudaError_t launch_gemm_opt_bf16(const GemmConfig&, const GemmArgs&, cudaStream_t);
 
 cudaError_t launch_gemm(int mode, int fmt, const GemmConfig& cfg, const GemmArgs& args,
                         cudaStream_t stream) {
@@ -46,6 +48,11 @@ cudaError_t launch_gemm(int mode, int fmt, const GemmConfig& cfg, const GemmArgs
     }
   } else if (mode == kModeDgrad && fmt == kFmtBF16) {
     return launch_gemm_dgrad(cfg, args, stream);
+  } else if (mode == kModeOpt) {
+    switch (fmt) {
+      case kFmtF32: return launch_gemm_opt_f32(cfg, args, stream);
+      case kFmtBF16: return launch_gemm_opt_bf16(cfg, args, stream);
+    }
   }
   return cudaErrorInvalidValue;
 }
@@ -270,6 +277,80 @@ AdamWConsts make_consts(float lr, float b1, float b2, float eps, float wd, int64
   h.neg_step_size = static_cast<float>(-dlr / bc1);
   h.inv_sqrt_bc2 = static_cast<float>(1.0 / std::sqrt(bc2));
   return h;
+}
+
+// forge_wgrad_opt: the hyperparameters its optimizer reads, in range.
+forge_status check_opt_hyper(int opt, const forge_opt_hyper& h, int64_t step) {
+  if (opt < kOptSgd || opt > kOptRadam || step < 1) return FORGE_ERR_HYPER;
+  auto nonneg = [](float x) { return x >= 0.0f && std::isfinite(x); };
+  auto unit = [](float x) { return x >= 0.0f && x < 1.0f; };
+  if (!nonneg(h.lr) || !nonneg(h.weight_decay)) return FORGE_ERR_HYPER;
+  if ((opt == kOptLion || opt == kOptNadam || opt == kOptRadam) &&
+      (!unit(h.beta1) || !unit(h.beta2)))
+    return FORGE_ERR_HYPER;
+  if (opt != kOptSgd && opt != kOptSgdMomentum && opt != kOptLion && !nonneg(h.eps))
+    return FORGE_ERR_HYPER;
+  if (opt == kOptSgdMomentum && !unit(h.momentum)) return FORGE_ERR_HYPER;
+  if (opt == kOptRmsprop && !unit(h.alpha)) return FORGE_ERR_HYPER;
+  if (opt == kOptNadam && !nonneg(h.momentum_decay)) return FORGE_ERR_HYPER;
+  return FORGE_OK;
+}
+
+// The step constants of forge_wgrad_opt, formed in fp64 from the float32
+// hyperparameters and rounded once each to fp32.
+OptConsts make_opt_consts(int opt, const forge_opt_hyper& h, int64_t step) {
+  OptConsts c;
+  std::memset(&c, 0, sizeof(c));
+  const double lr = h.lr, t = static_cast<double>(step);
+  c.opt = opt;
+  c.lr = h.lr;
+  c.wd = h.weight_decay;
+  c.eps = h.eps;
+  switch (opt) {
+    case kOptSgdMomentum: c.a = h.momentum; break;
+    case kOptRmsprop:
+      c.a = h.alpha;
+      c.oma = static_cast<float>(1.0 - static_cast<double>(h.alpha));
+      break;
+    case kOptLion:
+    case kOptNadam:
+    case kOptRadam: {
+      const double b1 = h.beta1, b2 = h.beta2;
+      c.a = h.beta1;
+      c.oma = static_cast<float>(1.0 - b1);
+      c.b = h.beta2;
+      c.omb = static_cast<float>(1.0 - b2);
+      if (opt == kOptLion) {
+        c.decay = static_cast<float>(1.0 - lr * static_cast<double>(h.weight_decay));
+      } else if (opt == kOptNadam) {
+        // mu_i = beta1 (1 - 0.5 * 0.96^(i psi)); the running product falls
+        // below fp64's range within a few thousand steps and then stays zero
+        const double psi = h.momentum_decay;
+        auto mu = [&](double i) { return b1 * (1.0 - 0.5 * std::pow(0.96, i * psi)); };
+        double prod = 1.0;
+        for (int64_t i = 1; i <= step && prod != 0.0; ++i) prod *= mu(static_cast<double>(i));
+        const double mu_t = mu(t), mu_next = mu(t + 1.0);
+        c.k1 = static_cast<float>(-lr * (1.0 - mu_t) / (1.0 - prod));
+        c.k2 = static_cast<float>(-lr * mu_next / (1.0 - prod * mu_next));
+        c.inv_sqrt_bc2 = static_cast<float>(1.0 / std::sqrt(1.0 - std::pow(b2, t)));
+      } else {
+        const double bc1 = 1.0 - std::pow(b1, t), bc2 = 1.0 - std::pow(b2, t);
+        const double rho_inf = 2.0 / (1.0 - b2) - 1.0;
+        const double rho_t = rho_inf - 2.0 * t * std::pow(b2, t) / bc2;
+        if (rho_t > 5.0) {
+          const double r = std::sqrt((rho_t - 4.0) * (rho_t - 2.0) * rho_inf /
+                                     ((rho_inf - 4.0) * (rho_inf - 2.0) * rho_t));
+          c.rect = 1;
+          c.k1 = static_cast<float>(-lr * r * std::sqrt(bc2) / bc1);
+        } else {
+          c.k1 = static_cast<float>(-lr / bc1);
+        }
+      }
+      break;
+    }
+    default: break;
+  }
+  return c;
 }
 
 // Tile configuration, from measured sweeps over the Llama-3.1-8B projections
@@ -712,6 +793,66 @@ extern "C" {
 forge_status forge_dgrad(const void* dY, const void* W, void* dX, int64_t bt, int64_t d_in,
                          int64_t d_out, forge_stream stream) {
   return dgrad_run(dY, W, dX, bt, d_in, d_out, stream, false);
+}
+
+forge_status forge_wgrad_opt(const void* X, const void* dY, void* W, forge_moment s1,
+                             forge_moment s2, int64_t bt, int64_t d_in, int64_t d_out,
+                             forge_optimizer opt, const forge_opt_hyper* hyper, int64_t step,
+                             forge_moment_fmt fmt, forge_stream stream) {
+  forge_status s = check_shape(bt, d_in, d_out);
+  if (s != FORGE_OK) return s;
+  if (!hyper) return FORGE_ERR_HYPER;
+  s = check_opt_hyper(static_cast<int>(opt), *hyper, step);
+  if (s != FORGE_OK) return s;
+  if (fmt != FORGE_MOM_FP32 && fmt != FORGE_MOM_BF16) return FORGE_ERR_FORMAT;
+  const int ns = opt_states(static_cast<int>(opt));
+  const void* st1 = ns >= 1 ? s1.data : nullptr;
+  const void* st2 = ns >= 2 ? s2.data : nullptr;
+  if (!W || (ns >= 1 && !st1) || (ns >= 2 && !st2)) return FORGE_ERR_NULL;
+  if (bt > 0 && (!X || !dY)) return FORGE_ERR_NULL;
+  if (!aligned16(W) || (st1 && !aligned16(st1)) || (st2 && !aligned16(st2)))
+    return FORGE_ERR_ALIGN;
+  if (bt > 0 && (!aligned16(X) || !aligned16(dY))) return FORGE_ERR_ALIGN;
+  const uint64_t n = static_cast<uint64_t>(d_in) * static_cast<uint64_t>(d_out);
+  const uint64_t nm = n * mom_elem_bytes(fmt);
+  if (overlaps(W, 2 * n, st1, nm) || overlaps(W, 2 * n, st2, nm) || overlaps(st1, nm, st2, nm))
+    return FORGE_ERR_ALIAS;
+  for (const void* in : {X, dY}) {
+    const uint64_t nin = 2ull * bt * (in == X ? d_in : d_out);
+    if (bt > 0 && (overlaps(in, nin, W, 2 * n) || overlaps(in, nin, st1, nm) ||
+                   overlaps(in, nin, st2, nm)))
+      return FORGE_ERR_ALIAS;
+  }
+  DeviceInfo* d = nullptr;
+  s = device_info(&d);
+  if (s != FORGE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int ifmt = fmt == FORGE_MOM_FP32 ? kFmtF32 : kFmtBF16;
+  // the slots hold W and two states as for AdamW: the same tile choice
+  GemmConfig cfg = choose_config(bt, ifmt, kModeFused);
+  GemmArgs args;
+  std::memset(&args, 0, sizeof(args));
+  GemmMaps& maps = args.maps[0];
+  const bool f32 = fmt == FORGE_MOM_FP32;
+  const CUtensorMapDataType mdt =
+      f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle msw = f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const int eb = f32 ? 4 : 2;
+  const uint32_t rows = static_cast<uint32_t>(slot_rows(kModeOpt, ifmt, cfg.prof));
+  bool ok = (bt == 0 || operand_maps(maps, X, dY, bt, d_in, d_out, bk_of(cfg.cg))) &&
+            get_map(&maps.w, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_in, d_out, d_in * 2, 32,
+                    rows, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (ok && ns >= 1) ok = get_map(&maps.m, st1, mdt, d_in, d_out, d_in * eb, 32, rows, msw);
+  if (ok && ns >= 2) ok = get_map(&maps.v, st2, mdt, d_in, d_out, d_in * eb, 32, rows, msw);
+  if (!ok) return FORGE_ERR_LAUNCH;
+  args.p = base_params(bt, cfg, *d);
+  args.p.o = make_opt_consts(static_cast<int>(opt), *hyper, step);
+  args.p.nstate = ns;
+  add_problem(args.p, cfg, d_in, d_out, nullptr, nullptr);
+  set_grid(cfg, args.p.num_units, d->num_sms);
+  args.p.drop_first_arrival = take_drop_flag();
+  return launch_gemm(kModeOpt, ifmt, cfg, args, st) == cudaSuccess ? FORGE_OK
+                                                                      : FORGE_ERR_LAUNCH;
 }
 
 forge_status forge_dgrad_noalloc(const void* dY, const void* W, void* dX, int64_t bt,

@@ -67,7 +67,7 @@ struct GemmTraits {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int W_ELEM = (MODE == kModeStoreG && FMT == kFmtF32) ? 4 : 2;
   static constexpr int MOM_ELEM =
-      (MODE != kModeFused) ? 0 : (FMT == kFmtF32 ? 4 : (FMT == kFmtBF16 ? 2 : 1));
+      !has_state(MODE) ? 0 : (FMT == kFmtF32 ? 4 : (FMT == kFmtBF16 ? 2 : 1));
   static constexpr int W_BYTES = RPS * SW * W_ELEM;
   static constexpr int M_BYTES = RPS * SW * MOM_ELEM;
   static constexpr int SLOT_BYTES = W_BYTES + 2 * M_BYTES;
@@ -120,6 +120,7 @@ struct GemmTraits {
   static_assert(BN % SW == 0 && BNL % 64 == 0, "tile width");
   // the input-gradient mode loads A as K-major boxes 64 elements deep: one per stage
   static_assert(MODE != kModeDgrad || BK == 64, "K-major A boxes hold 64 elements of K");
+  static_assert(MODE != kModeOpt || FMT != kFmtI8, "the other optimizers keep fp32 or bf16 state");
   static_assert(CG == 1 || (CG == 2 && BN == 256), "CTA pairs use 256 x 256 tiles");
   static_assert(TMEM_COLS <= 512, "tensor memory has 512 columns");
   // with half-tile slots each half of the epilogue owns every other slot
@@ -508,6 +509,91 @@ __device__ __forceinline__ void epi_slice_store(uint32_t taddr, bool zero_grad, 
   }
 }
 
+// The thread's 16 columns of one state box in the slot: fp32 boxes have
+// 128-byte rows (128-byte swizzle), bf16 boxes 64-byte rows (64-byte swizzle).
+template <int FMT>
+__device__ __forceinline__ void state_ld16(const uint8_t* box, uint32_t row, int h,
+                                           float (&x)[16]) {
+  if constexpr (FMT == kFmtF32) {
+    float4 q[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      q[c] = *reinterpret_cast<const float4*>(box + sw128_off(row, 4 * h + c));
+    const float* f = reinterpret_cast<const float*>(q);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = f[i];
+  } else {
+    uint4 q[2];
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+      q[c] = *reinterpret_cast<const uint4*>(box + sw64_off(row, 2 * h + c));
+    const uint32_t* u = reinterpret_cast<const uint32_t*>(q);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      x[2 * i] = bf16_lo(u[i]);
+      x[2 * i + 1] = bf16_hi(u[i]);
+    }
+  }
+}
+template <int FMT>
+__device__ __forceinline__ void state_st16(uint8_t* box, uint32_t row, int h,
+                                           const float (&x)[16]) {
+  if constexpr (FMT == kFmtF32) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      *reinterpret_cast<float4*>(box + sw128_off(row, 4 * h + c)) =
+          make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
+  } else {
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+      *reinterpret_cast<uint4*>(box + sw64_off(row, 2 * h + c)) =
+          make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+  }
+}
+
+// The other optimizers (kModeOpt): the slice of epi_slice_fused_16 with
+// optimizer OPT's element update, touching only the states OPT has.
+template <int FMT, int RPS, int OPT>
+__device__ __forceinline__ void epi_slice_opt(uint32_t taddr, bool zero_grad, uint8_t* slot,
+                                              uint32_t row, int h, const OptConsts& oc) {
+  constexpr int kWBytes = RPS * 32 * 2;
+  constexpr int kMBytes = RPS * 32 * (FMT == kFmtF32 ? 4 : 2);
+  constexpr int NST = opt_states(OPT);
+  uint32_t graw[16];
+  tmem_ld_x16(taddr, graw);
+  tmem_ld_wait();
+  float w[16], s1[16], s2[16];
+  state_ld16<kFmtBF16>(slot, row, h, w);
+  if constexpr (NST >= 1) state_ld16<FMT>(slot + kWBytes, row, h, s1);
+  if constexpr (NST >= 2) state_ld16<FMT>(slot + kWBytes + kMBytes, row, h, s2);
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    opt_elem<OPT>(zero_grad ? 0.0f : __uint_as_float(graw[i]), w[i], s1[i], s2[i], oc);
+  state_st16<kFmtBF16>(slot, row, h, w);
+  if constexpr (NST >= 1) state_st16<FMT>(slot + kWBytes, row, h, s1);
+  if constexpr (NST >= 2) state_st16<FMT>(slot + kWBytes + kMBytes, row, h, s2);
+}
+// Dispatch on the launch's optimizer (uniform across the grid).
+template <int FMT, int RPS>
+__device__ __forceinline__ void epi_slice_opt_any(const OptConsts& oc, uint32_t taddr,
+                                                  bool zero_grad, uint8_t* slot, uint32_t row,
+                                                  int h) {
+  switch (oc.opt) {
+    case kOptSgd: epi_slice_opt<FMT, RPS, kOptSgd>(taddr, zero_grad, slot, row, h, oc); break;
+    case kOptSgdMomentum:
+      epi_slice_opt<FMT, RPS, kOptSgdMomentum>(taddr, zero_grad, slot, row, h, oc);
+      break;
+    case kOptAdagrad: epi_slice_opt<FMT, RPS, kOptAdagrad>(taddr, zero_grad, slot, row, h, oc); break;
+    case kOptRmsprop: epi_slice_opt<FMT, RPS, kOptRmsprop>(taddr, zero_grad, slot, row, h, oc); break;
+    case kOptLion: epi_slice_opt<FMT, RPS, kOptLion>(taddr, zero_grad, slot, row, h, oc); break;
+    case kOptNadam: epi_slice_opt<FMT, RPS, kOptNadam>(taddr, zero_grad, slot, row, h, oc); break;
+    default: epi_slice_opt<FMT, RPS, kOptRadam>(taddr, zero_grad, slot, row, h, oc); break;
+  }
+}
+
 // Split reduction of the input gradient.  A CTA's fp32 partial tile (128 rows
 // x BN) is laid out so that a warp's accesses are contiguous: column slice cb,
 // half h and quarter j of a thread's 16 columns form a run of 128 float4, one
@@ -597,13 +683,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   }
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < p.nprob; ++i) {
-      tma_prefetch_desc(&a.maps[i].dy);
-      tma_prefetch_desc(&a.maps[i].x);
-      tma_prefetch_desc(&a.maps[i].w);
-      if (MODE == kModeFused) {
-        tma_prefetch_desc(&a.maps[i].m);
-        tma_prefetch_desc(&a.maps[i].v);
+      if (p.num_k > 0) {   // with no tokens the operand descriptors are never encoded
+        tma_prefetch_desc(&a.maps[i].dy);
+        tma_prefetch_desc(&a.maps[i].x);
       }
+      tma_prefetch_desc(&a.maps[i].w);
+      if (MODE == kModeFused || (MODE == kModeOpt && p.nstate >= 1)) tma_prefetch_desc(&a.maps[i].m);
+      if (MODE == kModeFused || (MODE == kModeOpt && p.nstate >= 2)) tma_prefetch_desc(&a.maps[i].v);
     }
   }
   // the peer's barriers must be initialised before any cross-CTA arrival
@@ -733,7 +819,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     __syncwarp();
   } else if (warp == 2) {
     // ------------------------------------------------------------ state loader
-    if (MODE == kModeFused && lane == 0) {
+    if (has_state(MODE) && lane == 0) {
       // Normal priority, not evict-first: a 32-column slice covers only half
       // of a 128-byte line of W (and of bf16 m, v), and the slice after it
       // reads the other half a moment later.  Marked evict-first, the line
@@ -763,15 +849,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             continue;
           }
           const uint32_t slot = base + T::OFF_SLOTS + j * T::SLOT_BYTES;
-          mbar_arrive_expect_tx(bar_sfull(j), T::SLOT_BYTES);
+          // kModeOpt loads only the states its optimizer has
+          const int nst = (MODE == kModeOpt) ? p.nstate : 2;
+          mbar_arrive_expect_tx(bar_sfull(j), T::W_BYTES + nst * T::M_BYTES);
           if constexpr (FMT == kFmtI8) {
             tma_load_2d(slot, &maps.w, x0, y0, bar_sfull(j), pol);
             tma_load_2d(slot + T::RPS * 64 * 2, &maps.w, x0 + 64, y0, bar_sfull(j), pol);
           } else {
             tma_load_2d(slot, &maps.w, x0, y0, bar_sfull(j), pol);
           }
-          tma_load_2d(slot + T::W_BYTES, &maps.m, x0, y0, bar_sfull(j), pol);
-          tma_load_2d(slot + T::W_BYTES + T::M_BYTES, &maps.v, x0, y0, bar_sfull(j), pol);
+          if (nst >= 1) tma_load_2d(slot + T::W_BYTES, &maps.m, x0, y0, bar_sfull(j), pol);
+          if (nst >= 2)
+            tma_load_2d(slot + T::W_BYTES + T::M_BYTES, &maps.v, x0, y0, bar_sfull(j), pol);
         }
       }
       // let the loads of each slot's latest phase land before the CTA can exit
@@ -817,6 +906,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if constexpr (MODE == kModeFused) {
               tma_store_2d(&maps.m, x0, y0, sl + T::W_BYTES);
               tma_store_2d(&maps.v, x0, y0, sl + T::W_BYTES + T::M_BYTES);
+            } else if constexpr (MODE == kModeOpt) {
+              if (p.nstate >= 1) tma_store_2d(&maps.m, x0, y0, sl + T::W_BYTES);
+              if (p.nstate >= 2) tma_store_2d(&maps.v, x0, y0, sl + T::W_BYTES + T::M_BYTES);
             }
             bulk_commit_group();
             bulk_wait_group_read<0>();
@@ -912,7 +1004,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if (T::PARTS > 1 && (s % T::PARTS) != part) continue;   // the other half's slot
         const int j = scnt % T::NS;
         const uint32_t ph = (scnt / T::NS) & 1u;
-        if (MODE == kModeFused)
+        if (has_state(MODE))
           good = wait_bounded(bar_sfull(j), ph, wc, kSiteEpiSlotFull);
         else
           good = wait_bounded(bar_sempty(j), ph ^ 1u, wc, kSiteEpiSlotFree);
@@ -936,10 +1028,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           ++xcnt;
           if (!xok) { ok = false; break; }
         } else if (active) {
-          if constexpr (MODE == kModeFused)
+          if constexpr (MODE == kModeFused) {
             epi_slice_fused_16<FMT, T::RPS>(taddr, zero_grad, slot, srow, h, p.h);
-          else
+          } else if constexpr (MODE == kModeOpt) {
+            epi_slice_opt_any<FMT, T::RPS>(p.o, taddr, zero_grad, slot, srow, h);
+          } else {
             epi_slice_store<FMT>(taddr, zero_grad, slot, srow, h);
+          }
         }
         if (s == T::SLICES - T::PARTS + part) {   // this warp has read the whole accumulator
           tc_fence_before_sync();
@@ -1047,7 +1142,7 @@ cudaError_t launch_gemm_fmt(const GemmConfig& cfg, const GemmArgs& args, cudaStr
     case kProfDeep:
       // int8 moments already use half-tile slots in the mma profile, and
       // store-G has no state slots: both run the deep profile as mma
-      if constexpr (MODE == kModeFused && FMT != kFmtI8)
+      if constexpr (has_state(MODE) && FMT != kFmtI8)
         return launch_gemm_prof<MODE, FMT, kProfDeep>(cfg, args, stream);
       else
         return launch_gemm_prof<MODE, FMT, kProfMma>(cfg, args, stream);

@@ -23,7 +23,14 @@ constexpr int kEpiThreads = 256;
 // kModeDgrad computes the layer's input gradient dX = dY W with the same
 // pipeline: A = dY read K-major (rows = tokens), B = W read MN-major, the
 // bf16 result stored like the gradient of kModeStoreG.
-enum Mode : int { kModeFused = 0, kModeStoreG = 1, kModeDgrad = 2 };
+// kModeOpt is kModeFused with one of the other coordinate-wise optimizers
+// (OptKind, chosen at run time) in place of AdamW: the same W, m, v slots,
+// with the states the optimizer does not have left unread and unwritten.
+enum Mode : int { kModeFused = 0, kModeStoreG = 1, kModeDgrad = 2, kModeOpt = 3 };
+// Modes that stream optimizer state through the state slots.
+__host__ __device__ constexpr bool has_state(int mode) {
+  return mode == kModeFused || mode == kModeOpt;
+}
 // Pipeline profiles, i.e. how shared memory is split between operand stages
 // and state slots: kProfStream (small token counts, HBM-bound epilogue) keeps
 // two operand stages and gives the rest to state slots; kProfMma (large token
@@ -62,6 +69,8 @@ struct GemmParams {
   float* part;                // [tile row][tile column][CTA of the pair][split][128 x BN] fp32
   int32_t group_m;            // tile-order swizzle: rows of tiles per group
   AdamWConsts h;
+  OptConsts o;                // kModeOpt: the optimizer and its step constants
+  int32_t nstate;             // kModeOpt: state tensors read and written (0..2)
   GemmProblem prob[kMaxGroup];
   int* err;                   // device error word
   int* err_site;              // device word: where a wait first timed out
@@ -108,7 +117,7 @@ __host__ __device__ constexpr int slice_cols(int mode, int fmt) {
 // processed by the four epilogue warps of its two TMEM lane quadrants, which
 // leaves shared memory for more operand stages.
 __host__ __device__ constexpr int slot_rows(int mode, int fmt, int prof) {
-  return (mode == kModeFused &&
+  return (has_state(mode) &&
           ((fmt == kFmtI8 && prof != kProfStream) || prof == kProfDeep)) ? 64 : 128;
 }
 

@@ -56,6 +56,77 @@ __device__ __forceinline__ void adamw_elem(float g, float& w, float& m, float& v
   r = r1;
 }
 
+// ---------------------------------------------------------------------------
+// The other coordinate-wise optimizers FORGE fuses (the page's regime 1):
+// SGD, SGD with momentum, Adagrad and RMSprop (PyTorch's definitions with
+// default options: L2 decay through the gradient, g = G + wd W), Lion (Chen et
+// al.: sign update, decoupled decay), NAdam and RAdam (PyTorch's definitions).
+// ---------------------------------------------------------------------------
+enum OptKind : int {
+  kOptSgd = 0, kOptSgdMomentum = 1, kOptAdagrad = 2, kOptRmsprop = 3, kOptLion = 4,
+  kOptNadam = 5, kOptRadam = 6
+};
+// per-coordinate state tensors: none; the momentum buffer, Adagrad's sum,
+// RMSprop's average or Lion's m; NAdam's and RAdam's m and v
+__host__ __device__ constexpr int opt_states(int opt) {
+  return opt == kOptSgd ? 0 : (opt >= kOptNadam ? 2 : 1);
+}
+
+// Per-step constants, formed in fp64 on the host and rounded once to fp32.
+struct OptConsts {
+  int32_t opt;           // OptKind
+  int32_t rect;          // RAdam: the variance rectification applies at this step
+  float lr, wd;          // learning rate; weight decay (L2: g = G + wd W)
+  float a, oma;          // momentum | RMSprop alpha | beta1, and 1 - that
+  float b, omb;          // beta2, 1 - beta2
+  float eps;
+  float k1, k2;          // NAdam: -lr (1 - mu_t) / (1 - P_t), -lr mu_{t+1} / (1 - P_t mu_{t+1});
+                         // RAdam: -lr r_t sqrt(1 - beta2^t) / (1 - beta1^t) (rectified)
+                         //        or -lr / (1 - beta1^t)
+  float inv_sqrt_bc2;    // NAdam: 1 / sqrt(1 - beta2^t)
+  float decay;           // Lion: 1 - lr wd
+};
+
+// One element of optimizer OPT: G from the accumulator, the weight w and the
+// states s1, s2 (fp32, updated in place; unused ones are left alone).
+template <int OPT>
+__device__ __forceinline__ void opt_elem(float G, float& w, float& s1, float& s2,
+                                         const OptConsts& c) {
+  if constexpr (OPT == kOptLion) {
+    const float dir = __fmaf_rn(c.a, s1, __fmul_rn(c.oma, G));
+    const float sg = dir > 0.0f ? 1.0f : (dir < 0.0f ? -1.0f : 0.0f);
+    w = __fmaf_rn(-c.lr, sg, __fmul_rn(w, c.decay));
+    s1 = __fmaf_rn(c.b, s1, __fmul_rn(c.omb, G));
+  } else {
+    const float g = __fmaf_rn(c.wd, w, G);
+    if constexpr (OPT == kOptSgd) {
+      w = __fmaf_rn(-c.lr, g, w);
+    } else if constexpr (OPT == kOptSgdMomentum) {
+      s1 = __fmaf_rn(c.a, s1, g);
+      w = __fmaf_rn(-c.lr, s1, w);
+    } else if constexpr (OPT == kOptAdagrad || OPT == kOptRmsprop) {
+      s1 = (OPT == kOptAdagrad) ? __fmaf_rn(g, g, s1)
+                                : __fmaf_rn(c.a, s1, __fmul_rn(c.oma, __fmul_rn(g, g)));
+      const float d = __fadd_rn(sqrt_approx(s1), c.eps);
+      w = __fmaf_rn(-c.lr, __fmul_rn(g, rcp_approx(d)), w);
+    } else {   // NAdam, RAdam
+      const float m = __fmaf_rn(c.a, s1, __fmul_rn(c.oma, g));
+      const float v = __fmaf_rn(c.b, s2, __fmul_rn(c.omb, __fmul_rn(g, g)));
+      if constexpr (OPT == kOptNadam) {
+        const float d = __fmaf_rn(sqrt_approx(v), c.inv_sqrt_bc2, c.eps);
+        w = __fmaf_rn(__fmaf_rn(c.k1, g, __fmul_rn(c.k2, m)), rcp_approx(d), w);
+      } else if (c.rect) {
+        const float d = __fadd_rn(sqrt_approx(v), c.eps);
+        w = __fmaf_rn(c.k1, __fmul_rn(m, rcp_approx(d)), w);
+      } else {
+        w = __fmaf_rn(c.k1, m, w);
+      }
+      s1 = m;
+      s2 = v;
+    }
+  }
+}
+
 // bf16 <-> fp32 (round to nearest even on the way down).
 __device__ __forceinline__ float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t packed) {

@@ -39,6 +39,17 @@ class ForgeMoment(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("scale", ctypes.c_void_p)]
 
 
+class ForgeOptHyper(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_float) for k in ("lr", "weight_decay", "beta1", "beta2", "eps",
+                                              "momentum", "alpha", "momentum_decay")]
+
+
+# forge_optimizer values, and how many state tensors each keeps
+OPT_SGD, OPT_SGD_MOMENTUM, OPT_ADAGRAD, OPT_RMSPROP, OPT_LION, OPT_NADAM, OPT_RADAM = range(7)
+OPT_STATES = {OPT_SGD: 0, OPT_SGD_MOMENTUM: 1, OPT_ADAGRAD: 1, OPT_RMSPROP: 1, OPT_LION: 1,
+              OPT_NADAM: 2, OPT_RADAM: 2}
+
+
 class ForgeLinear(ctypes.Structure):
     _fields_ = [("X", ctypes.c_void_p), ("dY", ctypes.c_void_p), ("W", ctypes.c_void_p),
                 ("m", ForgeMoment), ("v", ForgeMoment), ("d_in", ctypes.c_int64),
@@ -65,6 +76,9 @@ def lib() -> ctypes.CDLL:
             L.forge_wgrad_adamw.argtypes = [vp, vp, vp, ForgeMoment, ForgeMoment, i64, i64, i64,
                                             f32, f32, f32, f32, f32, i64, st, vp]
             L.forge_wgrad_adamw.restype = st
+            L.forge_wgrad_opt.argtypes = [vp, vp, vp, ForgeMoment, ForgeMoment, i64, i64, i64,
+                                          st, ctypes.POINTER(ForgeOptHyper), i64, st, vp]
+            L.forge_wgrad_opt.restype = st
             L.forge_wgrad_adamw_grouped.argtypes = [ctypes.POINTER(ForgeLinear), st, i64,
                                                     f32, f32, f32, f32, f32, i64, st, vp]
             L.forge_wgrad_adamw_grouped.restype = st
@@ -166,6 +180,37 @@ def wgrad_adamw(X: torch.Tensor, dY: torch.Tensor, W: torch.Tensor, m: torch.Ten
         _ptr(X), _ptr(dY), _ptr(W), _moment(m, m_scale), _moment(v, v_scale), bt, d_in, d_out,
         lr, beta1, beta2, eps, weight_decay, step, fmt, _stream(stream))
     _check(st, "forge_wgrad_adamw")
+
+
+def wgrad_opt(X: torch.Tensor, dY: torch.Tensor, W: torch.Tensor, opt: int,
+              s1: Optional[torch.Tensor] = None, s2: Optional[torch.Tensor] = None, *,
+              lr: float, weight_decay: float, step: int, beta1: float = 0.9,
+              beta2: float = 0.999, eps: float = 1e-8, momentum: float = 0.9,
+              alpha: float = 0.99, momentum_decay: float = 4e-3, stream=None) -> None:
+    """One fused step with optimizer `opt` (OPT_*) in place of AdamW: W and the
+    optimizer's states s1, s2 (fp32 or bf16, as many as OPT_STATES says)
+    updated in place."""
+    for t, n in ((X, "X"), (dY, "dY"), (W, "W")):
+        _dense(t, n)
+    states = [s for s in (s1, s2) if s is not None]
+    for s in states:
+        _dense(s, "state")
+    fmt = moment_format(states[0]) if states else MOM_FP32
+    bt, d_in = X.shape
+    d_out = dY.shape[1]
+    h = ForgeOptHyper(lr, weight_decay, beta1, beta2, eps, momentum, alpha, momentum_decay)
+    st = lib().forge_wgrad_opt(_ptr(X), _ptr(dY), _ptr(W), _moment(s1, None), _moment(s2, None),
+                               bt, d_in, d_out, opt, ctypes.byref(h), step, fmt,
+                               _stream(stream))
+    _check(st, "forge_wgrad_opt")
+
+
+def alloc_states(opt: int, d_out: int, d_in: int, fmt: int = MOM_FP32, device="cuda"):
+    """Zero-initialised states (s1, s2; None where the optimizer has fewer)."""
+    dt = {MOM_FP32: torch.float32, MOM_BF16: torch.bfloat16}[fmt]
+    n = OPT_STATES[opt]
+    return tuple(torch.zeros((d_out, d_in), dtype=dt, device=device) if i < n else None
+                 for i in range(2))
 
 
 def wgrad_adamw_grouped(layers, *, lr: float, beta1: float, beta2: float, eps: float,

@@ -37,6 +37,13 @@ from weight_gradient_gemm_gb300.inputs import (LLAMA31_8B_SHAPES, bf16_bits,  # 
 
 METRIC = "fused wgrad+AdamW TFLOP/s and % roofline, Llama-3.1-8B linears, 1 GB300"
 HYPER = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+# the other optimizers, with the FORGE page's shared settings per family (its
+# appendix table of optimizer families: lr, wd, betas, eps; momentum 0.9)
+_FAM = dict(lr=2e-5, weight_decay=1e-2)
+OPT_HYPER = [dict(_FAM), dict(_FAM, momentum=0.9), dict(_FAM, eps=1e-10), dict(_FAM, eps=1e-8),
+             dict(lr=3e-6, weight_decay=1.0, beta1=0.9, beta2=0.99),
+             dict(_FAM, beta1=0.9, beta2=0.999, eps=1e-8),
+             dict(_FAM, beta1=0.9, beta2=0.999, eps=1e-8)]
 FMT_NAMES = {0: "fp32", 1: "bf16", 2: "int8_block128"}
 STATE_BYTES = {0: 20.0, 1: 12.0, 2: 8.0 + 16.0 / 128.0}   # W r/w + m, v r/w (+ scales)
 L2_BYTES = 126 * 2 ** 20
@@ -367,6 +374,29 @@ def run_gpu(args, rank, world, dev):
             F.linear_backward(it["x"], it["dy"], it["w"], o, it["m"], it["v"], step=step,
                               m_scale=it["ms"], v_scale=it["vs"], **HYPER)
 
+    # ---- the other optimizers (diagnostic): forge_wgrad_opt per projection,
+    # states in the workload's format (fp32 for int8 workloads), zeroed first
+    sfmt = fmt if fmt in (F.MOM_FP32, F.MOM_BF16) else F.MOM_FP32
+    sdt = torch.float32 if sfmt == F.MOM_FP32 else torch.bfloat16
+    big = max(it["d_in"] * it["d_out"] for it in layer.items)
+    sbuf = [torch.zeros(big, dtype=sdt, device=dev) for _ in range(2)]
+    opt_ms = {}
+    for opt in range(7):
+        for b in sbuf:
+            b.zero_()
+        n_st = F.OPT_STATES[opt]
+        ost = [0]
+
+        def opt_step():
+            ost[0] += 1
+            for it in layer.items:
+                sv = [sbuf[i][:it["d_in"] * it["d_out"]].view(it["d_out"], it["d_in"])
+                      if i < n_st else None for i in range(2)]
+                F.wgrad_opt(it["x"], it["dy"], it["w"], opt, sv[0], sv[1], step=ost[0],
+                            **OPT_HYPER[opt])
+        opt_ms[opt] = per_step_ms(opt_step)
+    assert F.device_error() == 0
+
     backward = dict(dgrad_ms=per_step_ms(dgrad_all), cublas_dgrad_ms=per_step_ms(cublas_dgrad_all),
                     linear_backward_ms=per_step_ms(backward_all),
                     dgrad_config=F.describe_dgrad_config(bt, 4096, 14336))
@@ -416,7 +446,7 @@ def run_gpu(args, rank, world, dev):
         e2e_ms, unf_ms = max_over_ranks([e2e_ms, unf_ms], dev)
 
     return dict(layer=layer, elapsed_ms=elapsed_ms, kern_ms=kern_ms, unf_ms=unf_ms,
-                per_proj_ms=per_proj_ms, backward=backward,
+                per_proj_ms=per_proj_ms, backward=backward, opt_ms=opt_ms, opt_fmt=sfmt,
                 e2e_ms=e2e_ms, clocks=sampler.summary(w0, w1) if sampler else None,
                 config=F.describe_config(bt, 4096, 4096, fmt))
 
@@ -694,6 +724,24 @@ def run_reference(args):
 
 # ---------------------------------------------------------------------------
 
+def optimizers_block(opt_ms, sfmt, layer, peaks):
+    """The other fused optimizers (diagnostic): one forge_wgrad_opt launch per
+    projection, the step's time and its HBM roofline fraction; bytes per
+    parameter = W read + write (4) + 2 x state element size per state."""
+    names = ["sgd", "sgd_momentum", "adagrad", "rmsprop", "lion", "nadam", "radam"]
+    eb = 4 if sfmt == 0 else 2
+    operands = layer.h2d_bytes()
+    out = {"states": "fp32" if sfmt == 0 else "bf16",
+           "launch": "forge_wgrad_opt, one launch per projection", "peak_gbs": peaks["hbm_gbs"]}
+    for opt, name in enumerate(names):
+        nst = [0, 1, 1, 1, 1, 2, 2][opt]
+        ms = opt_ms[opt]
+        nbytes = layer.params() * (4 + 2 * eb * nst) + operands
+        out[name] = {"ms_per_step": ms, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                     "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+    return out
+
+
 def backward_block(bw, flops, fused_ms, peaks, peak_kind):
     """The backward-step diagnostic: dX = dY W for the seven projections
     (the same FLOPs as the weight gradient) against the bf16 tensor peak for
@@ -823,6 +871,7 @@ def main():
              "tflops": round(2.0 * bt * it["d_in"] * it["d_out"] / (t * 1e-3) / 1e12, 1)}
             for it, t in zip(layer.items, res["per_proj_ms"])],
         "linear_backward": backward_block(res["backward"], flops, ms, peaks, peak_kind),
+        "optimizers": optimizers_block(res["opt_ms"], res["opt_fmt"], layer, peaks),
         "gpu_launches": launches,
         "clocks": res["clocks"],
     }

@@ -248,3 +248,51 @@ def test_regime1_pins_pass_on_the_unmodified_oracle():
             for o in PR.TORCH_OPTS]
     pins += [PR.test_lion_closed_forms, PR.test_first_momentum_step_is_sgd_and_zero_gradient_cases]
     assert not _fails_one(pins)
+
+
+# ---------------------------------------------------------------------------
+# accumulate mode (oracle/accum.py)
+# ---------------------------------------------------------------------------
+
+import oracle.accum as A  # noqa: E402
+from tests import test_oracle_accumulate_pins as PA  # noqa: E402
+
+
+def _acc_variant(kind):
+    def f(x_bits, dy_bits, B, beta, rows=None, return_f64=False):
+        G = F.wgrad(x_bits, dy_bits, rows)
+        b = float(np.float32(beta))
+        Bf = np.asarray(B, dtype=np.float64)
+        if kind == "beta_on_gradient":
+            exact = G if b == 0.0 else Bf + b * G
+        elif kind == "buffer_ignored":
+            exact = G
+        elif kind == "transposed":
+            exact = G if b == 0.0 else b * Bf + (G.T if G.shape[0] == G.shape[1] else G[::-1])
+        else:   # rounded twice
+            exact = G if b == 0.0 else b * Bf + G
+            out = F.f64_to_f32(F.f64_to_f32(b * Bf).astype(np.float64) + G) if b != 0.0 \
+                else F.f64_to_f32(G)
+            return (out, exact) if return_f64 else out
+        out = F.f64_to_f32(exact)
+        return (out, exact) if return_f64 else out
+    return f
+
+
+ACC_PINS = [PA.test_beta_zero_is_the_gradient_and_ignores_the_buffer,
+            PA.test_integer_micro_batches_sum_to_the_whole_batch_exactly,
+            lambda: PA.test_muon_momentum_closed_form_on_one_hot_inputs(3, 7),
+            PA.test_no_tokens_scales_the_buffer_and_rounds_once]
+
+
+@pytest.mark.parametrize("kind", ["beta_on_gradient", "buffer_ignored", "transposed",
+                                  "rounded_twice"])
+def test_accumulate_mistakes_are_caught(monkeypatch, kind):
+    f = _acc_variant(kind)
+    monkeypatch.setattr(A, "accumulate", f)
+    monkeypatch.setattr(O, "accumulate", f)
+    assert _fails_one(ACC_PINS)
+
+
+def test_accumulate_pins_pass_on_the_unmodified_oracle():
+    assert not _fails_one(ACC_PINS)

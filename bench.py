@@ -397,6 +397,19 @@ def run_gpu(args, rank, world, dev):
         opt_ms[opt] = per_step_ms(opt_step)
     assert F.device_error() == 0
 
+    # ---- the accumulate mode (diagnostic): forge_wgrad_accumulate per
+    # projection into an fp32 buffer, with beta = 1 (B read and written) and
+    # beta = 0 (B written only)
+    bacc = torch.zeros(big, dtype=torch.float32, device=dev)
+
+    def accumulate_all(beta):
+        for it in layer.items:
+            F.wgrad_accumulate(it["x"], it["dy"],
+                               bacc[:it["d_in"] * it["d_out"]].view(it["d_out"], it["d_in"]), beta)
+    acc_ms = {b: per_step_ms(lambda b=b: accumulate_all(b)) for b in (1.0, 0.0)}
+    assert F.device_error() == 0
+    del bacc
+
     backward = dict(dgrad_ms=per_step_ms(dgrad_all), cublas_dgrad_ms=per_step_ms(cublas_dgrad_all),
                     linear_backward_ms=per_step_ms(backward_all),
                     dgrad_config=F.describe_dgrad_config(bt, 4096, 14336))
@@ -447,6 +460,7 @@ def run_gpu(args, rank, world, dev):
 
     return dict(layer=layer, elapsed_ms=elapsed_ms, kern_ms=kern_ms, unf_ms=unf_ms,
                 per_proj_ms=per_proj_ms, backward=backward, opt_ms=opt_ms, opt_fmt=sfmt,
+                acc_ms=acc_ms,
                 e2e_ms=e2e_ms, clocks=sampler.summary(w0, w1) if sampler else None,
                 config=F.describe_config(bt, 4096, 4096, fmt))
 
@@ -742,6 +756,20 @@ def optimizers_block(opt_ms, sfmt, layer, peaks):
     return out
 
 
+def accumulate_block(acc_ms, layer, peaks):
+    """The accumulate mode (diagnostic): B = beta B + dY^T X into fp32 for the
+    seven projections, one launch each; bytes per parameter 8 with beta = 1
+    (B read and written), 4 with beta = 0, plus the operands."""
+    out = {"launch": "forge_wgrad_accumulate, one launch per projection",
+           "peak_gbs": peaks["hbm_gbs"]}
+    for beta, per in ((1.0, 8), (0.0, 4)):
+        ms = acc_ms[beta]
+        nbytes = layer.params() * per + layer.h2d_bytes()
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[f"beta_{int(beta)}"] = {"ms_per_step": ms, "gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"]}
+    return out
+
+
 def backward_block(bw, flops, fused_ms, peaks, peak_kind):
     """The backward-step diagnostic: dX = dY W for the seven projections
     (the same FLOPs as the weight gradient) against the bf16 tensor peak for
@@ -872,6 +900,7 @@ def main():
             for it, t in zip(layer.items, res["per_proj_ms"])],
         "linear_backward": backward_block(res["backward"], flops, ms, peaks, peak_kind),
         "optimizers": optimizers_block(res["opt_ms"], res["opt_fmt"], layer, peaks),
+        "accumulate": accumulate_block(res["acc_ms"], layer, peaks),
         "gpu_launches": launches,
         "clocks": res["clocks"],
     }

@@ -216,6 +216,25 @@ forge_status forge_wgrad_opt(const void* X, const void* dY, void* W, forge_momen
                              forge_moment_fmt fmt, forge_stream stream);
 
 /*
+ * forge_wgrad_accumulate: B = beta * B + dY^T X into an fp32 buffer, the
+ * gradient accumulated on chip and added to B in the epilogue, rounded once
+ * per call.  The FORGE page uses it twice: Muon's momentum B <- mu B + G
+ * accumulates through the GEMM's beta (its optimizer regimes, regime 2), and
+ * the exact-accumulation mode (Appendix N.5) keeps an fp32 gradient-shaped
+ * accumulator across micro-batches (beta = 0 for the first, 1 for the
+ * others) and steps once at the last one: forge_adamw then reads B as its
+ * fp32 gradient.
+ *   X [bt, d_in], dY [bt, d_out] bf16; B [d_out, d_in] fp32, updated in
+ *   place (16-byte aligned).  beta = 0 does not read B (it may hold anything).
+ * Errors: FORGE_ERR_HYPER for a non-finite beta; the shape, NULL, alignment
+ * and overlap (B over X or dY) errors of forge_wgrad.  bt = 0 scales B by
+ * beta.  Asynchronous on `stream`.
+ */
+forge_status forge_wgrad_accumulate(const void* X, const void* dY, float* B, float beta,
+                                    int64_t bt, int64_t d_in, int64_t d_out,
+                                    forge_stream stream);
+
+/*
  * forge_wgrad: the unfused gradient, dW = dY^T X stored to global memory
  * (the "store-G control" of the FORGE page's Appendix D).  It runs the same
  * tensor-core main loop as forge_wgrad_adamw, so with dw_dtype = FORGE_DT_FP32

@@ -21,7 +21,7 @@ def test_header_declares_the_boundary():
     for n in ("forge_wgrad_adamw", "forge_wgrad", "forge_adamw", "forge_device_error",
               "forge_status_string", "forge_wgrad_adamw_grouped", "forge_dgrad",
               "forge_linear_backward", "forge_describe_dgrad_config", "forge_dgrad_noalloc",
-              "forge_wgrad_opt"):
+              "forge_wgrad_opt", "forge_wgrad_accumulate"):
         assert n in names
 
 
@@ -179,6 +179,20 @@ def test_wgrad_opt_argument_errors(L):
     assert opt_call(L, opt=5, s1=D, s2=D) == 6               # the two states overlap
     assert L.forge_wgrad_opt(A, B, C, F.ForgeMoment(D, None), F.ForgeMoment(None, None), 64,
                              256, 128, 1, None, 1, 0, None) == 5    # no hyperparameters
+
+
+def test_wgrad_accumulate_argument_errors(L):
+    # codes: 1 NULL, 2 ALIGN, 3 SHAPE, 5 HYPER, 6 ALIAS; 10 = reached the device query
+    acc = L.forge_wgrad_accumulate
+    assert acc(A, B, C, 1.0, 64, 256, 128, None) == 10
+    assert acc(A, B, None, 1.0, 64, 256, 128, None) == 1
+    assert acc(None, B, C, 1.0, 64, 256, 128, None) == 1
+    assert acc(None, None, C, 0.9, 0, 256, 128, None) == 10    # no tokens: X, dY unused
+    assert acc(A, B, C + 8, 1.0, 64, 256, 128, None) == 2
+    assert acc(A, B, C, 1.0, 64, 256, 124, None) == 3
+    assert acc(A, B, C, float("nan"), 64, 256, 128, None) == 5
+    assert acc(A, B, C, float("inf"), 64, 256, 128, None) == 5
+    assert acc(A, B, A, 1.0, 64, 256, 128, None) == 6          # B over X
 
 
 def grouped(L, layers, bt=64, step=1, fmt=0):

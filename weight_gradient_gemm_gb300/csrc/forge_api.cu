@@ -32,6 +32,7 @@ cudaError_t launch_gemm_store_bf16(const GemmConfig&, const GemmArgs&, cudaStrea
 cudaError_t launch_gemm_dgrad(const GemmConfig&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_opt_f32(const GemmConfig&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_opt_bf16(const GemmConfig&, const GemmArgs&, cudaStream_t);
+cudaError_t launch_gemm_accum(const GemmConfig&, const GemmArgs&, cudaStream_t);
 
 cudaError_t launch_gemm(int mode, int fmt, const GemmConfig& cfg, const GemmArgs& args,
                         cudaStream_t stream) {
@@ -48,6 +49,8 @@ cudaError_t launch_gemm(int mode, int fmt, const GemmConfig& cfg, const GemmArgs
     }
   } else if (mode == kModeDgrad && fmt == kFmtBF16) {
     return launch_gemm_dgrad(cfg, args, stream);
+  } else if (mode == kModeAccum && fmt == kFmtF32) {
+    return launch_gemm_accum(cfg, args, stream);
   } else if (mode == kModeOpt) {
     switch (fmt) {
       case kFmtF32: return launch_gemm_opt_f32(cfg, args, stream);
@@ -814,6 +817,40 @@ extern "C" {
 forge_status forge_dgrad(const void* dY, const void* W, void* dX, int64_t bt, int64_t d_in,
                          int64_t d_out, forge_stream stream) {
   return dgrad_run(dY, W, dX, bt, d_in, d_out, stream, false);
+}
+
+forge_status forge_wgrad_accumulate(const void* X, const void* dY, float* B, float beta,
+                                    int64_t bt, int64_t d_in, int64_t d_out,
+                                    forge_stream stream) {
+  forge_status s = check_shape(bt, d_in, d_out);
+  if (s != FORGE_OK) return s;
+  if (!std::isfinite(beta)) return FORGE_ERR_HYPER;
+  if (!B || (bt > 0 && (!X || !dY))) return FORGE_ERR_NULL;
+  if (!aligned16(B) || (bt > 0 && (!aligned16(X) || !aligned16(dY)))) return FORGE_ERR_ALIGN;
+  const uint64_t nb = 4ull * static_cast<uint64_t>(d_in) * static_cast<uint64_t>(d_out);
+  if (bt > 0 && (overlaps(B, nb, X, 2ull * bt * d_in) || overlaps(B, nb, dY, 2ull * bt * d_out)))
+    return FORGE_ERR_ALIAS;
+  DeviceInfo* d = nullptr;
+  s = device_info(&d);
+  if (s != FORGE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the slots hold one fp32 box, as for store-G with an fp32 gradient
+  GemmConfig cfg = choose_config(bt, kFmtF32, kModeStoreG);
+  GemmArgs args;
+  std::memset(&args, 0, sizeof(args));
+  GemmMaps& maps = args.maps[0];
+  const bool ok = (bt == 0 || operand_maps(maps, X, dY, bt, d_in, d_out, bk_of(cfg.cg))) &&
+                  get_map(&maps.w, B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d_in, d_out, d_in * 4, 32,
+                          kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return FORGE_ERR_LAUNCH;
+  args.p = base_params(bt, cfg, *d);
+  args.p.accum_beta = beta;
+  args.p.accum_load = beta != 0.0f;
+  add_problem(args.p, cfg, d_in, d_out, nullptr, nullptr);
+  set_grid(cfg, args.p.num_units, d->num_sms);
+  args.p.drop_first_arrival = take_drop_flag();
+  return launch_gemm(kModeAccum, kFmtF32, cfg, args, st) == cudaSuccess ? FORGE_OK
+                                                                         : FORGE_ERR_LAUNCH;
 }
 
 forge_status forge_wgrad_opt(const void* X, const void* dY, void* W, forge_moment s1,

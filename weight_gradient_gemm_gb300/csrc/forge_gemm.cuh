@@ -65,7 +65,8 @@ struct GemmTraits {
   static constexpr int A_BYTES = kBM * BK * 2;
   static constexpr int B_BYTES = BNL * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int W_ELEM = (MODE == kModeStoreG && FMT == kFmtF32) ? 4 : 2;
+  static constexpr int W_ELEM =
+      ((MODE == kModeStoreG || MODE == kModeAccum) && FMT == kFmtF32) ? 4 : 2;
   static constexpr int MOM_ELEM =
       !has_state(MODE) ? 0 : (FMT == kFmtF32 ? 4 : (FMT == kFmtBF16 ? 2 : 1));
   static constexpr int W_BYTES = RPS * SW * W_ELEM;
@@ -121,6 +122,7 @@ struct GemmTraits {
   // the input-gradient mode loads A as K-major boxes 64 elements deep: one per stage
   static_assert(MODE != kModeDgrad || BK == 64, "K-major A boxes hold 64 elements of K");
   static_assert(MODE != kModeOpt || FMT != kFmtI8, "the other optimizers keep fp32 or bf16 state");
+  static_assert(MODE != kModeAccum || FMT == kFmtF32, "the accumulation buffer is fp32");
   static_assert(CG == 1 || (CG == 2 && BN == 256), "CTA pairs use 256 x 256 tiles");
   static_assert(TMEM_COLS <= 512, "tensor memory has 512 columns");
   // with half-tile slots each half of the epilogue owns every other slot
@@ -594,6 +596,23 @@ __device__ __forceinline__ void epi_slice_opt_any(const OptConsts& oc, uint32_t 
   }
 }
 
+// Accumulate mode: B' = beta B + G into the slot's fp32 box (B loaded there
+// by the state loader unless beta = 0, when the old B is not read).
+__device__ __forceinline__ void epi_slice_accum(uint32_t taddr, bool zero_grad, uint8_t* slot,
+                                                uint32_t row, int h, float beta, bool load) {
+  uint32_t graw[16];
+  tmem_ld_x16(taddr, graw);
+  tmem_ld_wait();
+  float b[16], o[16];
+  if (load) state_ld16<kFmtF32>(slot, row, h, b);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float g = zero_grad ? 0.0f : __uint_as_float(graw[i]);
+    o[i] = load ? __fmaf_rn(beta, b[i], g) : g;
+  }
+  state_st16<kFmtF32>(slot, row, h, o);
+}
+
 // Split reduction of the input gradient.  A CTA's fp32 partial tile (128 rows
 // x BN) is laid out so that a warp's accesses are contiguous: column slice cb,
 // half h and quarter j of a thread's 16 columns form a run of 128 float4, one
@@ -819,7 +838,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     __syncwarp();
   } else if (warp == 2) {
     // ------------------------------------------------------------ state loader
-    if (has_state(MODE) && lane == 0) {
+    if ((has_state(MODE) || MODE == kModeAccum) && lane == 0) {
       // Normal priority, not evict-first: a 32-column slice covers only half
       // of a 128-byte line of W (and of bf16 m, v), and the slice after it
       // reads the other half a moment later.  Marked evict-first, the line
@@ -848,9 +867,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             mbar_arrive(bar_sfull(j));
             continue;
           }
+          if (MODE == kModeAccum && !p.accum_load) {   // beta = 0: B is not read
+            mbar_arrive(bar_sfull(j));
+            continue;
+          }
           const uint32_t slot = base + T::OFF_SLOTS + j * T::SLOT_BYTES;
-          // kModeOpt loads only the states its optimizer has
-          const int nst = (MODE == kModeOpt) ? p.nstate : 2;
+          // kModeOpt loads only the states its optimizer has; kModeAccum only B
+          const int nst = (MODE == kModeOpt) ? p.nstate : (MODE == kModeAccum ? 0 : 2);
           mbar_arrive_expect_tx(bar_sfull(j), T::W_BYTES + nst * T::M_BYTES);
           if constexpr (FMT == kFmtI8) {
             tma_load_2d(slot, &maps.w, x0, y0, bar_sfull(j), pol);
@@ -1004,7 +1027,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if (T::PARTS > 1 && (s % T::PARTS) != part) continue;   // the other half's slot
         const int j = scnt % T::NS;
         const uint32_t ph = (scnt / T::NS) & 1u;
-        if (has_state(MODE))
+        if (has_state(MODE) || MODE == kModeAccum)
           good = wait_bounded(bar_sfull(j), ph, wc, kSiteEpiSlotFull);
         else
           good = wait_bounded(bar_sempty(j), ph ^ 1u, wc, kSiteEpiSlotFree);
@@ -1032,6 +1055,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             epi_slice_fused_16<FMT, T::RPS>(taddr, zero_grad, slot, srow, h, p.h);
           } else if constexpr (MODE == kModeOpt) {
             epi_slice_opt_any<FMT, T::RPS>(p.o, taddr, zero_grad, slot, srow, h);
+          } else if constexpr (MODE == kModeAccum) {
+            epi_slice_accum(taddr, zero_grad, slot, srow, h, p.accum_beta, p.accum_load != 0);
           } else {
             epi_slice_store<FMT>(taddr, zero_grad, slot, srow, h);
           }

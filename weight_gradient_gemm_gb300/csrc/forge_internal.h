@@ -26,7 +26,9 @@ constexpr int kEpiThreads = 256;
 // kModeOpt is kModeFused with one of the other coordinate-wise optimizers
 // (OptKind, chosen at run time) in place of AdamW: the same W, m, v slots,
 // with the states the optimizer does not have left unread and unwritten.
-enum Mode : int { kModeFused = 0, kModeStoreG = 1, kModeDgrad = 2, kModeOpt = 3 };
+// kModeAccum accumulates into an fp32 buffer B (B' = beta B + G): store-G
+// with fp32 output whose slots are first loaded with B (unless beta = 0).
+enum Mode : int { kModeFused = 0, kModeStoreG = 1, kModeDgrad = 2, kModeOpt = 3, kModeAccum = 4 };
 // Modes that stream optimizer state through the state slots.
 __host__ __device__ constexpr bool has_state(int mode) {
   return mode == kModeFused || mode == kModeOpt;
@@ -71,6 +73,8 @@ struct GemmParams {
   AdamWConsts h;
   OptConsts o;                // kModeOpt: the optimizer and its step constants
   int32_t nstate;             // kModeOpt: state tensors read and written (0..2)
+  float accum_beta;           // kModeAccum: beta
+  int32_t accum_load;         // kModeAccum: B is read (beta != 0)
   GemmProblem prob[kMaxGroup];
   int* err;                   // device error word
   int* err_site;              // device word: where a wait first timed out

@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
             L.forge_wgrad_opt.argtypes = [vp, vp, vp, ForgeMoment, ForgeMoment, i64, i64, i64,
                                           st, ctypes.POINTER(ForgeOptHyper), i64, st, vp]
             L.forge_wgrad_opt.restype = st
+            L.forge_wgrad_accumulate.argtypes = [vp, vp, vp, f32, i64, i64, i64, vp]
+            L.forge_wgrad_accumulate.restype = st
             L.forge_wgrad_adamw_grouped.argtypes = [ctypes.POINTER(ForgeLinear), st, i64,
                                                     f32, f32, f32, f32, f32, i64, st, vp]
             L.forge_wgrad_adamw_grouped.restype = st
@@ -203,6 +205,20 @@ def wgrad_opt(X: torch.Tensor, dY: torch.Tensor, W: torch.Tensor, opt: int,
                                bt, d_in, d_out, opt, ctypes.byref(h), step, fmt,
                                _stream(stream))
     _check(st, "forge_wgrad_opt")
+
+
+def wgrad_accumulate(X: torch.Tensor, dY: torch.Tensor, B: torch.Tensor, beta: float,
+                     stream=None) -> None:
+    """B = beta * B + dY^T X (B fp32 [d_out, d_in], updated in place; not
+    read when beta is 0)."""
+    for t, n in ((X, "X"), (dY, "dY"), (B, "B")):
+        _dense(t, n)
+    if B.dtype != torch.float32:
+        raise TypeError("B must be fp32")
+    bt, d_in = X.shape
+    d_out = dY.shape[1]
+    _check(lib().forge_wgrad_accumulate(_ptr(X), _ptr(dY), _ptr(B), beta, bt, d_in, d_out,
+                                        _stream(stream)), "forge_wgrad_accumulate")
 
 
 def alloc_states(opt: int, d_out: int, d_in: int, fmt: int = MOM_FP32, device="cuda"):

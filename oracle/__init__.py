@@ -6,3 +6,4 @@ Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 from .forge_oracle import *  # noqa: F401,F403
 from .regime1 import *  # noqa: F401,F403
 from .accum import *  # noqa: F401,F403
+from .sr import *  # noqa: F401,F403

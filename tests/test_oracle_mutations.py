@@ -296,3 +296,70 @@ def test_accumulate_mistakes_are_caught(monkeypatch, kind):
 
 def test_accumulate_pins_pass_on_the_unmodified_oracle():
     assert not _fails_one(ACC_PINS)
+
+
+# ---------------------------------------------------------------------------
+# stochastic-rounding store (oracle/sr.py)
+# ---------------------------------------------------------------------------
+
+import oracle.sr as SRM  # noqa: E402
+from tests import test_oracle_sr_pins as PS  # noqa: E402
+
+_ORIG_PHILOX = SRM.philox4x64_10
+_ORIG_SR = SRM.sr_to_bf16
+
+
+def _philox_variant(kind):
+    M = (1 << 64) - 1
+
+    def f(counter, key):
+        c0, c1, c2, c3 = (int(x) & M for x in counter)
+        k0, k1 = (int(x) & M for x in key)
+        m0 = 0xD2E7470EE14C6C93 if kind != "wrong_multiplier" else 0xD2E7470EE14C6C95
+        for r in range(10):
+            if r and kind != "no_key_bump":
+                k0 = (k0 + 0x9E3779B97F4A7C15) & M
+                k1 = (k1 + 0xBB67AE8584CAA73B) & M
+            p0, p1 = m0 * c0, 0xCA5A826395121157 * c2
+            if kind == "no_permutation":
+                c0, c1, c2, c3 = p0 >> 64 ^ c1 ^ k0, p0 & M, p1 >> 64 ^ c3 ^ k1, p1 & M
+            else:
+                c0, c1, c2, c3 = (p1 >> 64) ^ c1 ^ k0, p1 & M, (p0 >> 64) ^ c3 ^ k1, p0 & M
+        return c0, c1, c2, c3
+    return f
+
+
+def _sr_variant(kind):
+    def f(x32, r16):
+        r = np.asarray(r16, dtype=np.uint64)
+        if kind == "nearest":
+            r = np.full(r.shape, 0x8000, np.uint64)
+        elif kind == "fifteen_bits":
+            r = r >> np.uint64(1)
+        return _ORIG_SR(x32, r)
+    return f
+
+
+SR_PINS = [lambda: PS.test_philox_matches_numpy((0, 0), (0, 0, 0, 0)),
+           lambda: PS.test_philox_matches_numpy((42, 0), ((1 << 64) - 1, (1 << 64) - 1, 0, 9)),
+           PS.test_sr_specials_and_extreme_draws, PS.test_sr_is_unbiased_exactly]
+
+
+@pytest.mark.parametrize("kind", ["wrong_multiplier", "no_key_bump", "no_permutation"])
+def test_philox_mistakes_are_caught(monkeypatch, kind):
+    f = _philox_variant(kind)
+    monkeypatch.setattr(SRM, "philox4x64_10", f)
+    monkeypatch.setattr(O, "philox4x64_10", f)
+    assert _fails_one(SR_PINS)
+
+
+@pytest.mark.parametrize("kind", ["nearest", "fifteen_bits"])
+def test_stochastic_rounding_mistakes_are_caught(monkeypatch, kind):
+    f = _sr_variant(kind)
+    monkeypatch.setattr(SRM, "sr_to_bf16", f)
+    monkeypatch.setattr(O, "sr_to_bf16", f)
+    assert _fails_one(SR_PINS)
+
+
+def test_sr_pins_pass_on_the_unmodified_oracle():
+    assert not _fails_one(SR_PINS)

@@ -410,6 +410,19 @@ def run_gpu(args, rank, world, dev):
     assert F.device_error() == 0
     del bacc
 
+    # ---- the stochastic-rounding store (diagnostic): the fused step per
+    # projection with W committed by stochastic rounding (fp32 and bf16 moments)
+    sr_ms = None
+    if fmt in (F.MOM_FP32, F.MOM_BF16):
+        def sr_all():
+            nonlocal step
+            step += 1
+            for k, it in enumerate(layer.items):
+                F.wgrad_adamw_sr(it["x"], it["dy"], it["w"], it["m"], it["v"], step=step,
+                                 seed=1000 + k, **HYPER)
+        sr_ms = per_step_ms(sr_all)
+        assert F.device_error() == 0
+
     backward = dict(dgrad_ms=per_step_ms(dgrad_all), cublas_dgrad_ms=per_step_ms(cublas_dgrad_all),
                     linear_backward_ms=per_step_ms(backward_all),
                     dgrad_config=F.describe_dgrad_config(bt, 4096, 14336))
@@ -460,7 +473,7 @@ def run_gpu(args, rank, world, dev):
 
     return dict(layer=layer, elapsed_ms=elapsed_ms, kern_ms=kern_ms, unf_ms=unf_ms,
                 per_proj_ms=per_proj_ms, backward=backward, opt_ms=opt_ms, opt_fmt=sfmt,
-                acc_ms=acc_ms,
+                acc_ms=acc_ms, sr_ms=sr_ms,
                 e2e_ms=e2e_ms, clocks=sampler.summary(w0, w1) if sampler else None,
                 config=F.describe_config(bt, 4096, 4096, fmt))
 
@@ -901,6 +914,12 @@ def main():
         "linear_backward": backward_block(res["backward"], flops, ms, peaks, peak_kind),
         "optimizers": optimizers_block(res["opt_ms"], res["opt_fmt"], layer, peaks),
         "accumulate": accumulate_block(res["acc_ms"], layer, peaks),
+        "sr_store": None if res["sr_ms"] is None else {
+            "ms_per_step": res["sr_ms"],
+            "round_to_nearest_ms_per_step": sum(res["per_proj_ms"]),
+            "overhead": res["sr_ms"] / sum(res["per_proj_ms"]) - 1.0,
+            "launch": "forge_wgrad_adamw_sr, one launch per projection, against "
+                      "forge_wgrad_adamw per projection"},
         "gpu_launches": launches,
         "clocks": res["clocks"],
     }

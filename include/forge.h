@@ -137,6 +137,25 @@ typedef struct {
 } forge_linear;
 
 /*
+ * forge_wgrad_adamw_sr: forge_wgrad_adamw with the new bf16 weight committed
+ * by stochastic rounding (the page's SR-store recipe, after Gupta et al.:
+ * no fp32 master copy; the weight rounds up with probability equal to the
+ * dropped fraction, so its expected value is the fp32 update).  The update is
+ * rounded to fp32 first.  The random bits come from Philox4x64-10 (Salmon
+ * et al. 2011) with key (seed, 0): weight (p, q) at step t takes bits
+ * 16 j .. 16 j + 15 of word k of the block with counter (p, q / 16, t, 0),
+ * where q % 16 = 4 k + j.  Give each layer its own seed.  The moments round
+ * to nearest as in forge_wgrad_adamw.  fp32 or bf16 moments (int8:
+ * FORGE_ERR_FORMAT); step <= 2^31 - 1.  Otherwise the arguments and errors of
+ * forge_wgrad_adamw.  Asynchronous on `stream`.
+ */
+forge_status forge_wgrad_adamw_sr(const void* X, const void* dY, void* W, forge_moment m,
+                                  forge_moment v, int64_t bt, int64_t d_in, int64_t d_out,
+                                  float lr, float beta1, float beta2, float eps,
+                                  float weight_decay, int64_t step, forge_moment_fmt fmt,
+                                  uint64_t seed, forge_stream stream);
+
+/*
  * forge_wgrad_adamw_grouped: forge_wgrad_adamw on n (1..FORGE_MAX_GROUP)
  * independent linear layers with the same token count bt, hyperparameters,
  * step and moment format, in ONE kernel launch whose persistent CTAs walk a

@@ -21,7 +21,7 @@ def test_header_declares_the_boundary():
     for n in ("forge_wgrad_adamw", "forge_wgrad", "forge_adamw", "forge_device_error",
               "forge_status_string", "forge_wgrad_adamw_grouped", "forge_dgrad",
               "forge_linear_backward", "forge_describe_dgrad_config", "forge_dgrad_noalloc",
-              "forge_wgrad_opt", "forge_wgrad_accumulate"):
+              "forge_wgrad_opt", "forge_wgrad_accumulate", "forge_wgrad_adamw_sr"):
         assert n in names
 
 
@@ -179,6 +179,20 @@ def test_wgrad_opt_argument_errors(L):
     assert opt_call(L, opt=5, s1=D, s2=D) == 6               # the two states overlap
     assert L.forge_wgrad_opt(A, B, C, F.ForgeMoment(D, None), F.ForgeMoment(None, None), 64,
                              256, 128, 1, None, 1, 0, None) == 5    # no hyperparameters
+
+
+def test_wgrad_adamw_sr_argument_errors(L):
+    m, v = F.ForgeMoment(D, None), F.ForgeMoment(D + (1 << 36), None)
+    args = (64, 256, 128, 1e-3, 0.9, 0.999, 1e-8, 0.01)
+    sr = L.forge_wgrad_adamw_sr
+    assert sr(A, B, C, m, v, *args, 1, 0, 7, None) == 10          # valid: reached the device
+    assert sr(A, B, C, m, v, *args, 1, 2, 7, None) in (1, 4)      # int8: no scales / format
+    ms, vs = F.ForgeMoment(D, G), F.ForgeMoment(D + (1 << 36), G + (1 << 20))
+    assert sr(A, B, C, ms, vs, *args, 1, 2, 7, None) == 4         # int8 moments: not here
+    assert sr(A, B, C, m, v, *args, 0, 0, 7, None) == 5           # step 0
+    assert sr(A, B, C, m, v, *args, 1 << 31, 0, 7, None) == 5     # step beyond 32 bits
+    assert sr(A, B, None, m, v, *args, 1, 0, 7, None) == 1
+    assert sr(A, B, A, m, v, *args, 1, 0, 7, None) == 6           # W over X
 
 
 def test_wgrad_accumulate_argument_errors(L):

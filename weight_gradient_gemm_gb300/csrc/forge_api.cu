@@ -1,6 +1,7 @@
 // The C ABI of libforge: argument validation, TMA descriptor encoding (cached),
 // tile configuration, launches and the device error word.
 #include <algorithm>
+#include <cstdint>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -677,6 +678,52 @@ forge_status forge_wgrad_adamw_grouped(const forge_linear* layers, int n, int64_
       return FORGE_ERR_LAUNCH;
     add_problem(args.p, cfg, L.d_in, L.d_out, L.m.scale, L.v.scale);
   }
+  set_grid(cfg, args.p.num_units, d->num_sms);
+  args.p.drop_first_arrival = take_drop_flag();
+  return launch_gemm(kModeFused, ifmt, cfg, args, st) == cudaSuccess ? FORGE_OK
+                                                                      : FORGE_ERR_LAUNCH;
+}
+
+forge_status forge_wgrad_adamw_sr(const void* X, const void* dY, void* W, forge_moment m,
+                                  forge_moment v, int64_t bt, int64_t d_in, int64_t d_out,
+                                  float lr, float beta1, float beta2, float eps,
+                                  float weight_decay, int64_t step, forge_moment_fmt fmt,
+                                  uint64_t seed, forge_stream stream) {
+  forge_linear L;
+  L.X = X;
+  L.dY = dY;
+  L.W = W;
+  L.m = m;
+  L.v = v;
+  L.d_in = d_in;
+  L.d_out = d_out;
+  forge_status s = check_linear(L, bt, fmt);
+  if (s != FORGE_OK) return s;
+  if (fmt == FORGE_MOM_INT8_B128) return FORGE_ERR_FORMAT;   // fp32 or bf16 moments
+  s = check_hyper(lr, beta1, beta2, eps, weight_decay, step);
+  if (s != FORGE_OK) return s;
+  if (step > INT32_MAX) return FORGE_ERR_HYPER;   // the step is a 32-bit Philox counter word
+  if (layers_clash(L, L, bt, fmt, true)) return FORGE_ERR_ALIAS;
+  DeviceInfo* d = nullptr;
+  s = device_info(&d);
+  if (s != FORGE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int ifmt = static_cast<int>(fmt);
+  // the tensor-core kernel even without tokens (G = 0): the separate
+  // optimizer kernel rounds W to nearest
+  GemmConfig cfg = choose_config(bt, ifmt, kModeFused);
+  GemmArgs args;
+  std::memset(&args, 0, sizeof(args));
+  GemmMaps& maps = args.maps[0];
+  if ((bt > 0 && !operand_maps(maps, X, dY, bt, d_in, d_out, bk_of(cfg.cg))) ||
+      !state_maps(maps, W, m, v, d_in, d_out, fmt, cfg.prof))
+    return FORGE_ERR_LAUNCH;
+  args.p = base_params(bt, cfg, *d);
+  args.p.h = make_consts(lr, beta1, beta2, eps, weight_decay, step);
+  args.p.sr = 1;
+  args.p.sr_step = static_cast<int32_t>(step);
+  args.p.sr_seed = seed;
+  add_problem(args.p, cfg, d_in, d_out, m.scale, v.scale);
   set_grid(cfg, args.p.num_units, d->num_sms);
   args.p.drop_first_arrival = take_drop_flag();
   return launch_gemm(kModeFused, ifmt, cfg, args, st) == cudaSuccess ? FORGE_OK

@@ -244,9 +244,14 @@ __device__ __forceinline__ int tile_coords(int t, const GemmParams& p, int& tm, 
 // fp32 or bf16 moments; SW = 32, HALF = 16.
 // `row` is the thread's row inside the RPS-row slot (its TMEM lane is in
 // `taddr`); the slot holds the W, m and v boxes of RPS rows back to back.
+// With `sr` the weight is committed by stochastic rounding: the random bits
+// of the thread's 16 columns are the Philox block with counter (grow, gcol16,
+// sr_step, 0), grow the global weight row and gcol16 the first column / 16.
 template <int FMT, int RPS>
 __device__ __forceinline__ void epi_slice_fused_16(uint32_t taddr, bool zero_grad, uint8_t* slot,
-                                                   uint32_t row, int h, const AdamWConsts& hc) {
+                                                   uint32_t row, int h, const AdamWConsts& hc,
+                                                   bool sr, uint64_t sr_seed, uint32_t sr_step,
+                                                   uint32_t grow, uint32_t gcol16) {
   constexpr int kWBytes = RPS * 32 * 2;
   constexpr int kMBytes = RPS * 32 * (FMT == kFmtF32 ? 4 : 2);
   uint32_t graw[16];
@@ -300,8 +305,20 @@ __device__ __forceinline__ void epi_slice_fused_16(uint32_t taddr, bool zero_gra
     adamw_elem(g[i], w[i], m[i], v[i], r, hc);
   }
   uint32_t wo[8];
+  if (sr) {
+    uint64_t rb[4] = {grow, gcol16, sr_step, 0ull};
+    philox4x64_10(rb, sr_seed, 0ull);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) wo[i] = pack_bf16x2(w[2 * i], w[2 * i + 1]);
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t r0 = static_cast<uint32_t>(rb[(2 * i) >> 2] >> (16 * ((2 * i) & 3))) & 0xFFFFu;
+      const uint32_t r1 =
+          static_cast<uint32_t>(rb[(2 * i + 1) >> 2] >> (16 * ((2 * i + 1) & 3))) & 0xFFFFu;
+      wo[i] = sr_bf16_bits(w[2 * i], r0) | (sr_bf16_bits(w[2 * i + 1], r1) << 16);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) wo[i] = pack_bf16x2(w[2 * i], w[2 * i + 1]);
+  }
 #pragma unroll
   for (int c = 0; c < 2; ++c)
     *reinterpret_cast<uint4*>(wbox + sw64_off(row, 2 * h + c)) =
@@ -1052,7 +1069,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           if (!xok) { ok = false; break; }
         } else if (active) {
           if constexpr (MODE == kModeFused) {
-            epi_slice_fused_16<FMT, T::RPS>(taddr, zero_grad, slot, srow, h, p.h);
+            epi_slice_fused_16<FMT, T::RPS>(taddr, zero_grad, slot, srow, h, p.h, p.sr != 0,
+                                            p.sr_seed, static_cast<uint32_t>(p.sr_step),
+                                            static_cast<uint32_t>(y0) + srow,
+                                            static_cast<uint32_t>(x0 >> 4) + h);
           } else if constexpr (MODE == kModeOpt) {
             epi_slice_opt_any<FMT, T::RPS>(p.o, taddr, zero_grad, slot, srow, h);
           } else if constexpr (MODE == kModeAccum) {

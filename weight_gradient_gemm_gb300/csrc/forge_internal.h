@@ -75,6 +75,10 @@ struct GemmParams {
   int32_t nstate;             // kModeOpt: state tensors read and written (0..2)
   float accum_beta;           // kModeAccum: beta
   int32_t accum_load;         // kModeAccum: B is read (beta != 0)
+  // kModeFused: commit W by stochastic rounding (Philox4x64-10 key (sr_seed,
+  // 0), counter (row, column / 16, sr_step, 0)) instead of to nearest even
+  int32_t sr, sr_step;
+  uint64_t sr_seed;
   GemmProblem prob[kMaxGroup];
   int* err;                   // device error word
   int* err_site;              // device word: where a wait first timed out

@@ -127,6 +127,42 @@ __device__ __forceinline__ void opt_elem(float G, float& w, float& s1, float& s2
   }
 }
 
+// ---------------------------------------------------------------------------
+// Stochastic-rounding store of the bf16 weight (the page's SR-store recipe,
+// Gupta et al.): the random bits come from Philox4x64-10 (Salmon, Moraes,
+// Dror, Shaw 2011), one block of 4 x 64 bits per 16 weights.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void philox4x64_10(uint64_t (&c)[4], uint64_t k0, uint64_t k1) {
+  constexpr uint64_t kM0 = 0xD2E7470EE14C6C93ull, kM1 = 0xCA5A826395121157ull;
+  constexpr uint64_t kW0 = 0x9E3779B97F4A7C15ull, kW1 = 0xBB67AE8584CAA73Bull;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r) {
+      k0 += kW0;
+      k1 += kW1;
+    }
+    const uint64_t hi0 = __umul64hi(kM0, c[0]), lo0 = kM0 * c[0];
+    const uint64_t hi1 = __umul64hi(kM1, c[2]), lo1 = kM1 * c[2];
+    const uint64_t n0 = hi1 ^ c[1] ^ k0, n2 = hi0 ^ c[3] ^ k1;
+    c[0] = n0;
+    c[1] = lo1;
+    c[2] = n2;
+    c[3] = lo0;
+  }
+}
+
+// fp32 -> bf16 bit pattern by stochastic rounding with a uniform 16-bit r:
+// r is added to the low 16 bits of the magnitude and the upper 16 kept, so
+// the magnitude rounds up with probability (dropped bits) / 2^16; past the
+// largest finite value it becomes infinity.  NaN and infinity pass through.
+__device__ __forceinline__ uint32_t sr_bf16_bits(float x, uint32_t r16) {
+  const uint32_t b = __float_as_uint(x);
+  const uint32_t mag = b & 0x7FFFFFFFu, sign = (b >> 16) & 0x8000u;
+  if (mag >= 0x7F800000u) return (mag > 0x7F800000u ? 0x7FC0u : 0x7F80u) | sign;
+  const uint32_t up = (mag + r16) >> 16;   // mag + r16 < 2^32
+  return (up > 0x7F80u ? 0x7F80u : up) | sign;
+}
+
 // bf16 <-> fp32 (round to nearest even on the way down).
 __device__ __forceinline__ float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t packed) {

@@ -79,6 +79,10 @@ def lib() -> ctypes.CDLL:
             L.forge_wgrad_opt.argtypes = [vp, vp, vp, ForgeMoment, ForgeMoment, i64, i64, i64,
                                           st, ctypes.POINTER(ForgeOptHyper), i64, st, vp]
             L.forge_wgrad_opt.restype = st
+            L.forge_wgrad_adamw_sr.argtypes = [vp, vp, vp, ForgeMoment, ForgeMoment, i64, i64,
+                                               i64, f32, f32, f32, f32, f32, i64, st,
+                                               ctypes.c_uint64, vp]
+            L.forge_wgrad_adamw_sr.restype = st
             L.forge_wgrad_accumulate.argtypes = [vp, vp, vp, f32, i64, i64, i64, vp]
             L.forge_wgrad_accumulate.restype = st
             L.forge_wgrad_adamw_grouped.argtypes = [ctypes.POINTER(ForgeLinear), st, i64,
@@ -227,6 +231,21 @@ def alloc_states(opt: int, d_out: int, d_in: int, fmt: int = MOM_FP32, device="c
     n = OPT_STATES[opt]
     return tuple(torch.zeros((d_out, d_in), dtype=dt, device=device) if i < n else None
                  for i in range(2))
+
+
+def wgrad_adamw_sr(X: torch.Tensor, dY: torch.Tensor, W: torch.Tensor, m: torch.Tensor,
+                   v: torch.Tensor, *, lr: float, beta1: float, beta2: float, eps: float,
+                   weight_decay: float, step: int, seed: int, stream=None) -> None:
+    """wgrad_adamw with W committed by stochastic rounding (Philox4x64-10
+    random bits from `seed`, the weight index and the step); fp32 or bf16 moments."""
+    for t, n in ((X, "X"), (dY, "dY"), (W, "W"), (m, "m"), (v, "v")):
+        _dense(t, n)
+    bt, d_in = X.shape
+    d_out = dY.shape[1]
+    st = lib().forge_wgrad_adamw_sr(
+        _ptr(X), _ptr(dY), _ptr(W), _moment(m, None), _moment(v, None), bt, d_in, d_out,
+        lr, beta1, beta2, eps, weight_decay, step, moment_format(m), seed, _stream(stream))
+    _check(st, "forge_wgrad_adamw_sr")
 
 
 def wgrad_adamw_grouped(layers, *, lr: float, beta1: float, beta2: float, eps: float,

@@ -707,6 +707,32 @@ def time_oracle(workload: str, target_s: float):
     return flops / dt / 1e12, dt, rows, bt
 
 
+def run_metadata():
+    """What the line was measured on: GPU name, driver and CUDA versions,
+    PyTorch version, the kernel sources' hash and the host's core count.
+    Never raises: a field that cannot be read is null."""
+    out = {"gpu": None, "driver": None, "cuda": None, "torch": torch.__version__,
+           "kernel_sources": None, "host_cores": os.cpu_count()}
+    try:
+        out["kernel_sources"] = source_digest()
+    except Exception:
+        pass
+    try:
+        out["cuda"] = torch.version.cuda
+        if torch.cuda.is_available():
+            out["gpu"] = torch.cuda.get_device_name(torch.cuda.current_device())
+    except Exception:
+        pass
+    try:
+        r = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader"],
+                           capture_output=True, text=True, timeout=10)
+        if r.returncode == 0 and r.stdout.strip():
+            out["driver"] = r.stdout.strip().splitlines()[0]
+    except Exception:
+        pass
+    return out
+
+
 def cpu_baseline_block(workload):
     # the two-point fit overestimates the cost per row of larger samples: a
     # 20 s target lands at about 10-12 s of oracle work
@@ -922,6 +948,7 @@ def main():
                       "forge_wgrad_adamw per projection"},
         "gpu_launches": launches,
         "clocks": res["clocks"],
+        "system": run_metadata(),
     }
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline_block(args.workload)

@@ -73,3 +73,14 @@ def test_reference_arm_under_torchrun_prints_once():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["steps"] == 1
     assert d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_bench_run_metadata_never_raises_and_serialises():
+    # the bench line's `system` record: every field present, unreadable ones null
+    import json
+
+    import bench
+    meta = bench.run_metadata()
+    assert set(meta) == {"gpu", "driver", "cuda", "torch", "kernel_sources", "host_cores"}
+    assert meta["kernel_sources"] == bench.source_digest()
+    json.dumps(meta)

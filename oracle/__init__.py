@@ -7,3 +7,4 @@ from .forge_oracle import *  # noqa: F401,F403
 from .regime1 import *  # noqa: F401,F403
 from .accum import *  # noqa: F401,F403
 from .sr import *  # noqa: F401,F403
+from .fp8 import *  # noqa: F401,F403

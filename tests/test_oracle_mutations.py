@@ -363,3 +363,52 @@ def test_stochastic_rounding_mistakes_are_caught(monkeypatch, kind):
 
 def test_sr_pins_pass_on_the_unmodified_oracle():
     assert not _fails_one(SR_PINS)
+
+
+# ---------------------------------------------------------------------------
+# fp8 moments (oracle/fp8.py)
+# ---------------------------------------------------------------------------
+
+import oracle.fp8 as F8  # noqa: E402
+from tests import test_oracle_fp8_pins as P8  # noqa: E402
+
+_ORIG_TO_E4M3 = F8.f64_to_e4m3
+_ORIG_FROM_E4M3 = F8.e4m3_to_f64
+
+
+def _fp8_variant(kind):
+    if kind == "bias_eight":
+        def dec(codes):
+            return _ORIG_FROM_E4M3(codes) / 2.0
+        return "e4m3_to_f64", dec
+
+    def enc(x):
+        x = np.asarray(x, dtype=np.float64)
+        if kind == "truncating":
+            a = np.abs(x)
+            _, e = np.frexp(a)
+            q = np.where(e - 1 >= -6, e - 1 - 3, -9)
+            t = np.ldexp(np.floor(np.ldexp(a, -q)), q)
+            return _ORIG_TO_E4M3(np.copysign(t, x))
+        with np.errstate(over="ignore", invalid="ignore"):   # no saturation: wraps past 448
+            c = _ORIG_TO_E4M3(x).astype(np.int64)
+            big = np.abs(x) > 448
+            return np.where(big, (c & 0x80) | 0x7F, c).astype(np.uint8)
+    return "f64_to_e4m3", enc
+
+
+@pytest.mark.parametrize("kind", ["bias_eight", "truncating", "no_saturation"])
+def test_fp8_mistakes_are_caught(monkeypatch, kind):
+    name, f = _fp8_variant(kind)
+    monkeypatch.setattr(F8, name, f)
+    monkeypatch.setattr(O, name, f)
+    pins = [P8.test_encoding_matches_torch_float8_e4m3fn,
+            P8.test_decoding_all_codes_matches_torch_and_round_trips,
+            P8.test_saturation_and_power_of_two_scales]
+    assert _fails_one(pins)
+
+
+def test_fp8_pins_pass_on_the_unmodified_oracle():
+    assert not _fails_one([P8.test_encoding_matches_torch_float8_e4m3fn,
+                           P8.test_decoding_all_codes_matches_torch_and_round_trips,
+                           P8.test_saturation_and_power_of_two_scales])

@@ -84,3 +84,34 @@ def test_bench_run_metadata_never_raises_and_serialises():
     assert set(meta) == {"gpu", "driver", "cuda", "torch", "kernel_sources", "host_cores"}
     assert meta["kernel_sources"] == bench.source_digest()
     json.dumps(meta)
+
+
+def test_bench_diagnostic_blocks_from_synthetic_timings():
+    # the default line's diagnostic blocks are pure functions of the timings:
+    # every key present, fractions consistent, JSON-serialisable
+    import json
+
+    import bench
+
+    class FakeLayer:
+        def params(self):
+            return 218103808
+
+        def h2d_bytes(self):
+            return 83886080
+
+    peaks = {"hbm_gbs": 6791.7, "bf16_tflops": 1891.5, "bf16_tflops_sustained": 1702.6}
+    layer = FakeLayer()
+    opt = bench.optimizers_block({i: 0.5 + 0.1 * i for i in range(7)}, 0, layer, peaks)
+    assert opt["states"] == "fp32" and len([k for k in opt if isinstance(opt[k], dict)]) == 7
+    nb = layer.params() * (4 + 2 * 4 * 2) + layer.h2d_bytes()     # NAdam: two fp32 states
+    assert abs(opt["nadam"]["gbs"] - nb / (opt["nadam"]["ms_per_step"] * 1e-3) / 1e9) < 1e-6
+    acc = bench.accumulate_block({1.0: 0.48, 0.0: 0.45}, layer, peaks)
+    assert acc["beta_1"]["frac_hbm"] > acc["beta_0"]["frac_hbm"]
+    flops = 2.0 * 512 * layer.params()
+    bw = bench.backward_block(dict(dgrad_ms=0.25, cublas_dgrad_ms=0.15, linear_backward_ms=1.04,
+                                   dgrad_config="tile=256x256 ctas=2 splits=2"),
+                              flops, 0.70, peaks, "measured")
+    assert abs(bw["dgrad"]["roofline"]["frac"] - flops / 0.25e-3 / 1e12 / 1891.5) < 1e-9
+    assert abs(bw["dgrad"]["vs_cublas"] - 0.6) < 1e-9
+    json.dumps([opt, acc, bw])

@@ -30,15 +30,16 @@
  * memory for later calls.
  *
  * Tuning.  The tile configuration is chosen from the token count and the
- * moment format (forge_describe_config shows it).  For measurements, these
- * environment variables, read at each call, override the choice:
- * FORGE_PROFILE=stream|balanced|mma|deep (how shared memory is split between
- * operand stages and state slots), FORGE_CG=1|2 (one CTA or a CTA pair per
- * tile), FORGE_BN=128|256 (accumulator width on one CTA), FORGE_GROUP_M=1..64
- * (tile rows per raster group), FORGE_POLL_STORE=0|1 (the store lanes poll
- * for finished state slots), FORGE_SPLITS=1..8 (forge_dgrad: k-ranges per
- * tile).  Every choice computes the same step to the same accuracy; only
- * the speed differs.
+ * moment format (forge_describe_config shows it).  forge_set_tuning
+ * overrides the choice for measurements; its initial value comes from these
+ * environment variables, read once, at the library's first call that
+ * chooses a configuration: FORGE_PROFILE=stream|balanced|mma|deep (how
+ * shared memory is split between operand stages and state slots),
+ * FORGE_CG=1|2 (one CTA or a CTA pair per tile), FORGE_BN=128|256
+ * (accumulator width on one CTA), FORGE_GROUP_M=1..64 (tile rows per raster
+ * group), FORGE_POLL_STORE=0|1 (the store lanes poll for finished state
+ * slots), FORGE_SPLITS=1..8 (forge_dgrad: k-ranges per tile).  Every choice
+ * computes the same step to the same accuracy; only the speed differs.
  *
  * Errors.  Argument errors are returned synchronously, before anything is
  * enqueued.  Launch failures return FORGE_ERR_LAUNCH.  Kernels never trap:
@@ -282,12 +283,22 @@ forge_status forge_dgrad(const void* dY, const void* W, void* dX,
                          int64_t bt, int64_t d_in, int64_t d_out, forge_stream stream);
 
 /*
- * forge_dgrad_noalloc: forge_dgrad that allocates nothing.  When it splits
- * the reduction, the fp32 partials go to a 32 MiB scratch array the library
- * reserves statically on each device when it loads, instead of the pool; a
- * split that needs more runs with fewer splits (down to none).  With the
- * same split count the result is bit for bit that of forge_dgrad.  Same
- * arguments, layout and errors as forge_dgrad.
+ * forge_dgrad_noalloc: forge_dgrad that allocates nothing, for callers that
+ * cannot allocate device memory while they run: an engine that plans and
+ * owns every byte of the device up front, or code that runs where an
+ * allocation call is not allowed.  When it splits the reduction, the fp32 partials go to a
+ * 32 MiB scratch array that lives in the library's own module (a file-scope
+ * device array) instead of the pool; a split that needs more runs with
+ * fewer splits (down to none).  With the same split count the result is bit
+ * for bit that of forge_dgrad.  Same arguments, layout and errors as
+ * forge_dgrad.
+ * When the scratch is reserved: under CUDA's default lazy module loading the
+ * array (and the kernels' code) is placed on a device at the first libforge
+ * call there that needs it, not when the library is loaded; a caller that
+ * needs even the first forge_dgrad_noalloc call on a device to take no
+ * device memory makes one warm-up call (any libforge call that launches on
+ * that device) beforehand.  Every GPU that loads the module holds the 32 MiB
+ * until the process exits.
  * Precondition (documented, not checked): the scratch is one per device, so
  * two forge_dgrad_noalloc calls on one device must not run at the same time
  * (issue them on one stream, or order the streams); forge_dgrad calls may
@@ -363,6 +374,37 @@ void forge_set_wait_limit_ns(uint64_t ns);
  * records FORGE_ERR_DEVICE_TIMEOUT and returns with its outputs unspecified.
  * The flag clears itself after that one launch. */
 void forge_debug_drop_first_arrival(int enable);
+
+/* Pipeline profiles: how a tensor-core kernel splits shared memory between
+ * operand stages and optimizer-state slots. */
+typedef enum {
+  FORGE_PROFILE_AUTO = -1,     /* chosen from the token count and format       */
+  FORGE_PROFILE_STREAM = 0,    /* two operand stages, the rest state slots      */
+  FORGE_PROFILE_MMA = 1,       /* as many operand stages as fit beside 2 slots  */
+  FORGE_PROFILE_BALANCED = 2,  /* as many operand stages as state slots         */
+  FORGE_PROFILE_DEEP = 3       /* as many stages as fit beside 2 half-tile slots */
+} forge_profile;
+
+/* Tuning overrides; a field at its automatic value (FORGE_PROFILE_AUTO, 0 or
+ * -1 as stated) leaves that choice to the library.  Out-of-range values are
+ * ignored. */
+typedef struct {
+  int profile;     /* a forge_profile                                          */
+  int cta_group;   /* 0 automatic; 1 one CTA per tile; 2 a CTA pair (256 x 256) */
+  int bn;          /* 0 automatic; 128 or 256: accumulator width on one CTA     */
+  int group_m;     /* 0 automatic; 1..64 tile rows per raster group             */
+  int poll_store;  /* -1 automatic; 0 or 1: store lanes poll for finished slots */
+  int splits;      /* 0 automatic; 1..8 k-ranges per tile for forge_dgrad       */
+} forge_tuning;
+
+/* Replace the tuning overrides (NULL: everything automatic).  Applies to
+ * calls made after it returns, from any thread; thread-safe.  Every setting
+ * computes the same results; only the speed differs. */
+void forge_set_tuning(const forge_tuning* tuning);
+
+/* The tuning overrides now in force (the environment's, until the first
+ * forge_set_tuning). */
+void forge_get_tuning(forge_tuning* tuning);
 
 #ifdef __cplusplus
 }

@@ -19,3 +19,19 @@ def has_gpu() -> bool:
         return torch.cuda.is_available()
     except Exception:
         return False
+
+
+@pytest.fixture
+def tune():
+    """Sets the library's tuning overrides for one test (forge_set_tuning) and
+    restores the previous ones afterwards.  Fields not given keep their value."""
+    from weight_gradient_gemm_gb300 import _build
+    from weight_gradient_gemm_gb300 import forge as F
+    _build.build()
+    saved = F.get_tuning()
+
+    def set_(**kw):
+        F.set_tuning(**{**F.get_tuning(), **kw})
+
+    yield set_
+    F.set_tuning(**saved)

@@ -5,6 +5,7 @@ import ctypes
 import subprocess
 
 import pytest
+import torch
 
 from weight_gradient_gemm_gb300 import _build
 from weight_gradient_gemm_gb300 import forge as F
@@ -48,12 +49,12 @@ def test_describe_config_without_gpu(L):
         F.describe_config(512, 4097, 4096)
 
 
-def test_dgrad_split_choice_without_gpu(L, monkeypatch):
+def test_dgrad_split_choice_without_gpu(L, tune):
     # host logic only (152 SMs assumed without a device).  dX of the
     # Llama-3.1-8B gate/up projections (d_out = 14336, d_in = 4096): at 512
     # tokens 32 pair tiles for 76 SM pairs, so the reduction over d_out is
     # split; from 1024 tokens on the cost estimate keeps it whole
-    monkeypatch.delenv("FORGE_SPLITS", raising=False)
+    tune(splits=0)
     s = F.describe_dgrad_config(512, 4096, 14336)
     assert "tile=256x256" in s and "ctas=2" in s and "splits=2" in s, s
     assert "grid=128" in s, s                       # 64 units -> 64 pairs
@@ -62,7 +63,7 @@ def test_dgrad_split_choice_without_gpu(L, monkeypatch):
     # the k projection (d_out = 1024: 16 k-steps) is too short to split
     assert "splits=1" in F.describe_dgrad_config(512, 4096, 1024)
     # the override is clamped to splits of at least 8 k-steps
-    monkeypatch.setenv("FORGE_SPLITS", "8")
+    tune(splits=8)
     assert "splits=8" in F.describe_dgrad_config(512, 4096, 14336)
     assert "splits=2" in F.describe_dgrad_config(512, 4096, 1024)
     assert "splits=1" in F.describe_dgrad_config(512, 4096, 512)
@@ -233,3 +234,94 @@ def test_grouped_argument_errors(L):
     assert grouped(L, [a, lin(A, B, C + 2 * G, D + 3 * G, D + 4 * G, d_in=260)]) == 3
     assert grouped(L, [a, b], step=0) == 5
     assert grouped(L, [a, b]) in (0, 7, 10)            # valid: stops at the device query here
+
+
+# ---------------------------------------------------------------------------
+# The Python binding checks every tensor's shape, dtype and device before it
+# calls into the library (the kernels size their tensor maps from the shapes
+# they are given, so a short buffer would be read or written past its end).
+# The checks run on the host: CPU tensors reach the shape and dtype checks,
+# and a tensor of the right shape on the CPU is then refused as not a CUDA
+# tensor.
+# ---------------------------------------------------------------------------
+
+def _t(shape, dt=torch.bfloat16):
+    return torch.zeros(shape, dtype=dt)
+
+
+HY = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=1)
+
+
+def test_binding_rejects_mismatched_shapes_and_dtypes():
+    bt, d_in, d_out = 64, 256, 128
+    X, dY = _t((bt, d_in)), _t((bt, d_out))
+    W = _t((d_out, d_in))
+    m, v = _t((d_out, d_in), torch.float32), _t((d_out, d_in), torch.float32)
+    with pytest.raises(ValueError, match="W has shape"):
+        F.wgrad_adamw(X, dY, _t((d_out, d_in - 8)), m, v, **HY)
+    with pytest.raises(ValueError, match="dY has shape"):
+        F.wgrad_adamw(X, _t((bt - 1, d_out)), W, m, v, **HY)
+    with pytest.raises(ValueError, match="m has shape"):
+        F.wgrad_adamw(X, dY, W, _t((d_out, 8), torch.float32), v, **HY)
+    with pytest.raises(TypeError, match="v has dtype"):
+        F.wgrad_adamw(X, dY, W, m, _t((d_out, d_in)), **HY)
+    with pytest.raises(TypeError, match="X has dtype"):
+        F.wgrad_adamw(_t((bt, d_in), torch.float32), dY, W, m, v, **HY)
+    with pytest.raises(ValueError, match="m_scale is required"):
+        F.wgrad_adamw(X, dY, W, _t((d_out, d_in), torch.int8), _t((d_out, d_in), torch.int8),
+                      **HY)
+    with pytest.raises(ValueError, match="v_scale has shape"):
+        F.wgrad_adamw(X, dY, W, _t((d_out, d_in), torch.int8), _t((d_out, d_in), torch.int8),
+                      m_scale=_t((d_out, 2), torch.float32), v_scale=_t((d_out, 1), torch.float32),
+                      **HY)
+    with pytest.raises(ValueError, match="dX has shape"):
+        F.dgrad(dY, W, _t((bt, d_in + 8)))
+    with pytest.raises(ValueError, match="W has shape"):
+        F.dgrad(dY, _t((d_out + 8, d_in)), _t((bt, d_in)))
+    with pytest.raises(ValueError, match="dX has shape"):
+        F.dgrad_noalloc(dY, W, _t((bt - 1, d_in)))
+    with pytest.raises(ValueError, match="dX has shape"):
+        F.linear_backward(X, dY, W, _t((bt, d_out)), m, v, **HY)
+    with pytest.raises(ValueError, match="dW has shape"):
+        F.wgrad(X, dY, _t((d_in, d_out), torch.float32))
+    with pytest.raises(TypeError, match="B has dtype"):
+        F.wgrad_accumulate(X, dY, _t((d_out, d_in)), 1.0)
+    with pytest.raises(ValueError, match="s2 is required"):
+        F.wgrad_opt(X, dY, W, F.OPT_NADAM, m, None, lr=1e-3, weight_decay=0.0, step=1)
+    with pytest.raises(ValueError, match="s1 has shape"):
+        F.wgrad_opt(X, dY, W, F.OPT_LION, _t((d_out, 8), torch.float32), lr=1e-3,
+                    weight_decay=0.0, step=1)
+    with pytest.raises(ValueError, match="dW has shape"):
+        F.adamw(_t((d_out, 8), torch.float32), W, m, v, **HY)
+    with pytest.raises(TypeError, match="m has dtype"):
+        F.wgrad_adamw_sr(X, dY, W, _t((d_out, d_in), torch.int8), _t((d_out, d_in), torch.int8),
+                         seed=1, **HY)
+    with pytest.raises(ValueError, match="W has shape"):
+        F.wgrad_adamw_grouped([dict(X=X, dY=dY, W=_t((d_in, d_out)), m=m, v=v)], **HY)
+
+
+def test_binding_refuses_host_tensors():
+    bt, d_in, d_out = 64, 256, 128
+    X, dY, W = _t((bt, d_in)), _t((bt, d_out)), _t((d_out, d_in))
+    m, v = _t((d_out, d_in), torch.float32), _t((d_out, d_in), torch.float32)
+    with pytest.raises(ValueError, match="must be a CUDA tensor"):
+        F.wgrad_adamw(X, dY, W, m, v, **HY)
+    with pytest.raises(ValueError, match="must be a CUDA tensor"):
+        F.dgrad(dY, W, _t((bt, d_in)))
+
+
+def test_tuning_round_trip_without_gpu(L, tune):
+    tune(profile="deep", cg=2, bn=256, group_m=8, poll_store=0, splits=3)
+    t = F.get_tuning()
+    assert t == dict(profile="deep", cg=2, bn=256, group_m=8, poll_store=0, splits=3)
+    # the override reaches the host's configuration choice
+    assert "profile=deep" in F.describe_config(512, 4096, 4096, F.MOM_FP32)
+    assert "group_m=8" in F.describe_config(512, 4096, 4096, F.MOM_FP32)
+    with F.tuning(profile="stream"):
+        assert "profile=stream" in F.describe_config(4096, 4096, 4096, F.MOM_FP32)
+    assert F.get_tuning()["profile"] == "deep"
+    F.set_tuning()
+    assert F.get_tuning() == dict(profile="auto", cg=0, bn=0, group_m=0, poll_store=-1,
+                                  splits=0)
+    with pytest.raises(ValueError):
+        F.set_tuning(profile="fast")

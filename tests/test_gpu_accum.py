@@ -55,11 +55,9 @@ def _case(seed, bt, d_in, d_out):
 @pytest.fixture(params=[None, ("stream", "128", "1"), ("balanced", "256", "1"),
                         ("mma", "256", "2")],
                 ids=lambda p: "auto" if p is None else f"{p[0]}-bn{p[1]}-cta{p[2]}")
-def acc_cfg(request, monkeypatch):
+def acc_cfg(request, tune):
     if request.param is not None:
-        monkeypatch.setenv("FORGE_PROFILE", request.param[0])
-        monkeypatch.setenv("FORGE_BN", request.param[1])
-        monkeypatch.setenv("FORGE_CG", request.param[2])
+        tune(profile=request.param[0], bn=int(request.param[1]), cg=int(request.param[2]))
     return request.param
 
 

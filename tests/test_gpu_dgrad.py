@@ -63,12 +63,10 @@ def _inputs(seed, bt, d_in, d_out):
 @pytest.fixture(params=[None, ("mma", "128", "1"), ("balanced", "256", "1"), ("mma", "256", "2"),
                         ("stream", "256", "2")],
                 ids=lambda p: "auto" if p is None else f"{p[0]}-bn{p[1]}-cta{p[2]}")
-def dgrad_cfg(request, monkeypatch):
+def dgrad_cfg(request, tune):
     """The library's own choice and forced profiles, tile widths and CTA groupings."""
     if request.param is not None:
-        monkeypatch.setenv("FORGE_PROFILE", request.param[0])
-        monkeypatch.setenv("FORGE_BN", request.param[1])
-        monkeypatch.setenv("FORGE_CG", request.param[2])
+        tune(profile=request.param[0], bn=int(request.param[1]), cg=int(request.param[2]))
     return request.param
 
 
@@ -158,14 +156,12 @@ def test_linear_backward_against_oracle(fmt):
     (77, 136, 2048, ("mma", "128", "1")),    # one CTA, 128 x 128 tiles
     (300, 384, 1544, ("mma", "256", "1")),   # one CTA, 128 x 256 tiles
 ], ids=["pair", "pair-short", "cta-128", "cta-256"])
-def test_dgrad_split_reduction(bt, d_in, d_out, cfg, splits, monkeypatch):
+def test_dgrad_split_reduction(bt, d_in, d_out, cfg, splits, tune):
     # the reduction over d_out cut into k-ranges whose partials the last unit
     # of each tile adds: same accuracy, and bit-identical from run to run
-    monkeypatch.setenv("FORGE_SPLITS", splits)
+    tune(splits=int(splits))
     if cfg is not None:
-        monkeypatch.setenv("FORGE_PROFILE", cfg[0])
-        monkeypatch.setenv("FORGE_BN", cfg[1])
-        monkeypatch.setenv("FORGE_CG", cfg[2])
+        tune(profile=cfg[0], bn=int(cfg[1]), cg=int(cfg[2]))
     dy, w = _inputs(4, bt, d_in, d_out)
     dyd, wd = dy.to(DEV), w.to(DEV)
     dX = torch.full((bt, d_in), float("nan"), dtype=torch.bfloat16, device=DEV)
@@ -178,10 +174,10 @@ def test_dgrad_split_reduction(bt, d_in, d_out, cfg, splits, monkeypatch):
     assert torch.equal(dX.view(torch.int16), again.view(torch.int16))
 
 
-def test_dgrad_gate_projection_eight_splits(monkeypatch):
+def test_dgrad_gate_projection_eight_splits(tune):
     # Llama-3.1-8B gate projection at 512 tokens with the most splits: 224
     # k-steps of 64 cut into 8 ranges on 32 tiles
-    monkeypatch.setenv("FORGE_SPLITS", "8")
+    tune(splits=8)
     bt, d_out, d_in = 512, 14336, 4096
     dy, w = _inputs(5, bt, d_in, d_out)
     dX = torch.empty((bt, d_in), dtype=torch.bfloat16, device=DEV)
@@ -191,10 +187,10 @@ def test_dgrad_gate_projection_eight_splits(monkeypatch):
     check_dx(bf16_bits(dX.cpu())[rows], bf16_bits(dy), bf16_bits(w), rows, label="gate S=8")
 
 
-def test_dgrad_split_on_two_streams_at_once(monkeypatch):
+def test_dgrad_split_on_two_streams_at_once(tune):
     # each call takes its own workspace in its stream's order, so two split
     # launches running side by side give what each gives alone
-    monkeypatch.setenv("FORGE_SPLITS", "4")
+    tune(splits=4)
     bt, d_in, d_out = 256, 1024, 4096
     ins = [_inputs(10 + i, bt, d_in, d_out) for i in range(2)]
     dev = [(dy.to(DEV), w.to(DEV)) for dy, w in ins]

@@ -90,10 +90,8 @@ def test_opt_against_oracle(opt, fmt, bt, d_in, d_out, t):
 @pytest.fixture(params=[("stream", "128", "1"), ("balanced", "256", "1"), ("deep", "256", "2"),
                         ("mma", "256", "2")],
                 ids=lambda p: f"{p[0]}-bn{p[1]}-cta{p[2]}")
-def forced(request, monkeypatch):
-    monkeypatch.setenv("FORGE_PROFILE", request.param[0])
-    monkeypatch.setenv("FORGE_BN", request.param[1])
-    monkeypatch.setenv("FORGE_CG", request.param[2])
+def forced(request, tune):
+    tune(profile=request.param[0], bn=int(request.param[1]), cg=int(request.param[2]))
     return request.param
 
 

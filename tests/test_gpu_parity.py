@@ -32,13 +32,11 @@ def _gpu():
                         ("balanced", "256", "2"), ("mma", "256", "2"), ("deep", "128", "1"),
                         ("deep", "256", "2")],
                 ids=lambda p: f"{p[0]}-bn{p[1]}-cta{p[2]}")
-def profile(request, monkeypatch):
+def profile(request, tune):
     """Every pipeline profile, tile width and CTA grouping of the tensor-core
     kernel (the library picks them by token count; FORGE_PROFILE, FORGE_BN and
     FORGE_CG force them; 1-CTA int8 moments always use 128-wide tiles)."""
-    monkeypatch.setenv("FORGE_PROFILE", request.param[0])
-    monkeypatch.setenv("FORGE_BN", request.param[1])
-    monkeypatch.setenv("FORGE_CG", request.param[2])
+    tune(profile=request.param[0], bn=int(request.param[1]), cg=int(request.param[2]))
     return request.param
 
 
@@ -294,13 +292,11 @@ def test_grouped_against_oracle_all_profiles(profile):
 
 @pytest.mark.parametrize("group_m", [1, 3, 5])
 @pytest.mark.parametrize("cg", ["1", "2"])
-def test_raster_group_sizes(group_m, cg, monkeypatch):
+def test_raster_group_sizes(group_m, cg, tune):
     # tile orders whose last raster group is partial (1000 rows: 8 tiles of
     # 128 or 4 of 256; group sizes 3 and 5 leave remainders) give the same
     # step as the oracle, on one CTA and on CTA pairs
-    monkeypatch.setenv("FORGE_GROUP_M", str(group_m))
-    monkeypatch.setenv("FORGE_CG", cg)
-    monkeypatch.setenv("FORGE_PROFILE", "balanced")
+    tune(group_m=group_m, cg=int(cg), profile="balanced")
     fmt = O.FMT_FP32
     shapes = [(1000, 776), (264, 512)]
     bt = 96

@@ -367,9 +367,8 @@ OptConsts make_opt_consts(int opt, const forge_opt_hyper& h, int64_t step) {
 // B operand from shared memory: balanced depths up to 1536 tokens, then as
 // many operand stages as fit next to two state slots, and above 3072 tokens
 // next to two half-tile slots.  The store-G kernel (fmt = dW dtype) keeps the
-// 768-token split.  FORGE_PROFILE=stream|balanced|mma|deep, FORGE_CG=1|2,
-// FORGE_BN=128|256, FORGE_GROUP_M=1..64 and FORGE_POLL_STORE=0|1 override the
-// choice.
+// 768-token split.  forge_set_tuning (or the FORGE_* environment variables,
+// read once) overrides the choice.
 GemmConfig finish_config(GemmConfig c, int64_t bt, int fmt, int mode);
 
 GemmConfig choose_config(int64_t bt, int fmt, int mode) {
@@ -409,26 +408,46 @@ GemmConfig choose_opt_config(int64_t bt, int fmt) {
   return finish_config(c, bt, fmt, kModeFused);
 }
 
-// The tile width, the raster order and the store-lane wait follow from the
-// grouping, profile and format; the environment overrides apply last.
-GemmConfig finish_config(GemmConfig c, int64_t bt, int fmt, int mode) {
-  c.bn = (c.cg == 2) ? 256 : 128;
+// Tuning overrides.  The FORGE_* environment variables are read once, at the
+// first call that chooses a configuration; afterwards only forge_set_tuning
+// changes them.  Reading the environment on every call would cost host time
+// per launch and race with setenv in other threads.
+std::once_flag g_tune_once;
+forge_tuning g_tune = {FORGE_PROFILE_AUTO, 0, 0, 0, -1, 0};
+
+void tuning_from_env() {
+  forge_tuning t = {FORGE_PROFILE_AUTO, 0, 0, 0, -1, 0};
   if (const char* e = std::getenv("FORGE_PROFILE")) {
-    if (std::strcmp(e, "stream") == 0) c.prof = kProfStream;
-    if (std::strcmp(e, "mma") == 0) c.prof = kProfMma;
-    if (std::strcmp(e, "balanced") == 0) c.prof = kProfBalanced;
-    if (std::strcmp(e, "deep") == 0) c.prof = kProfDeep;
+    if (std::strcmp(e, "stream") == 0) t.profile = FORGE_PROFILE_STREAM;
+    if (std::strcmp(e, "mma") == 0) t.profile = FORGE_PROFILE_MMA;
+    if (std::strcmp(e, "balanced") == 0) t.profile = FORGE_PROFILE_BALANCED;
+    if (std::strcmp(e, "deep") == 0) t.profile = FORGE_PROFILE_DEEP;
   }
-  if (const char* e = std::getenv("FORGE_CG")) {
-    if (std::strcmp(e, "1") == 0) c.cg = 1;
-    if (std::strcmp(e, "2") == 0) c.cg = 2;
-  }
-  if (const char* e = std::getenv("FORGE_BN")) {
-    if (std::strcmp(e, "128") == 0) c.bn = 128;
-    if (std::strcmp(e, "256") == 0) c.bn = 256;
-  }
+  if (const char* e = std::getenv("FORGE_CG")) t.cta_group = std::atoi(e);
+  if (const char* e = std::getenv("FORGE_BN")) t.bn = std::atoi(e);
+  if (const char* e = std::getenv("FORGE_GROUP_M")) t.group_m = std::atoi(e);
+  if (const char* e = std::getenv("FORGE_POLL_STORE")) t.poll_store = std::atoi(e) != 0;
+  if (const char* e = std::getenv("FORGE_SPLITS")) t.splits = std::atoi(e);
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_tune = t;
+}
+
+forge_tuning current_tuning() {
+  std::call_once(g_tune_once, tuning_from_env);
+  std::lock_guard<std::mutex> lk(g_mu);
+  return g_tune;
+}
+
+// The tile width, the raster order and the store-lane wait follow from the
+// grouping, profile and format; the tuning overrides apply last.
+GemmConfig finish_config(GemmConfig c, int64_t bt, int fmt, int mode) {
+  const forge_tuning tu = current_tuning();
+  c.bn = (c.cg == 2) ? 256 : 128;
+  if (tu.profile >= kProfStream && tu.profile <= kProfDeep) c.prof = tu.profile;
+  if (tu.cta_group == 1 || tu.cta_group == 2) c.cg = tu.cta_group;
+  if (tu.bn == 128 || tu.bn == 256) c.bn = tu.bn;
   if (c.cg == 2) c.bn = 256;                    // pairs always use 256 x 256 tiles
-  if (c.cg == 1 && fmt == kFmtI8) c.bn = 128;   // 1-CTA int8 only with 128-wide tiles
+  if (c.cg == 1 && (fmt == kFmtI8 || fmt == kFmtF8)) c.bn = 128;   // 1-CTA 8-bit moments: 128-wide tiles
   // Tile rows per raster group (the kernel's tile_coords): 4 for 128 x 128
   // tiles, 1 (plain row-major order) for pairs, from the same sweeps.
   c.group_m = (c.cg == 1) ? 4 : 1;
@@ -441,11 +460,8 @@ GemmConfig finish_config(GemmConfig c, int64_t bt, int fmt, int mode) {
                  ((c.cg == 1 && ((fmt == kFmtBF16 && bt <= 576) ||
                                  (fmt == kFmtF32 && c.prof == kProfStream))) ||
                   (c.cg == 2 && fmt == kFmtF32));
-  if (const char* e = std::getenv("FORGE_POLL_STORE")) c.poll_store = (std::atoi(e) != 0);
-  if (const char* e = std::getenv("FORGE_GROUP_M")) {
-    const int g = std::atoi(e);
-    if (g >= 1 && g <= 64) c.group_m = g;
-  }
+  if (tu.poll_store == 0 || tu.poll_store == 1) c.poll_store = tu.poll_store;
+  if (tu.group_m >= 1 && tu.group_m <= 64) c.group_m = tu.group_m;
   c.grid = 0;
   c.splits = 1;
   return c;
@@ -461,13 +477,11 @@ GemmConfig finish_config(GemmConfig c, int64_t bt, int fmt, int mode) {
 // (mostly L2 hits).  Splits are at most 8 and at least 8 k-steps
 // long (shorter units cannot hide their 128 KB partial write behind the next
 // unit's main loop), and only for queues shorter than two waves.
-// FORGE_SPLITS overrides (clamped to the same length limits).
+// The tuning's `splits` overrides (clamped to the same length limits).
 int choose_splits(int64_t tiles, int64_t num_k, int64_t slots, int64_t ctile_bytes) {
   const int64_t max_s = std::max<int64_t>(1, std::min<int64_t>(8, num_k / 8));
-  if (const char* e = std::getenv("FORGE_SPLITS")) {
-    const int64_t f = std::atoi(e);
-    if (f >= 1) return static_cast<int>(std::min(f, max_s));
-  }
+  const int64_t f = current_tuning().splits;
+  if (f >= 1) return static_cast<int>(std::min(f, max_s));
   if (tiles >= 2 * slots) return 1;
   auto cost = [&](int64_t s) {
     const int64_t waves = (tiles * s + slots - 1) / slots;
@@ -1130,6 +1144,17 @@ void forge_set_wait_limit_ns(uint64_t ns) {
 void forge_debug_drop_first_arrival(int enable) {
   std::lock_guard<std::mutex> lk(g_mu);
   g_drop_first_arrival = enable ? 1 : 0;
+}
+
+void forge_set_tuning(const forge_tuning* t) {
+  std::call_once(g_tune_once, tuning_from_env);   // a later first read must not undo this
+  const forge_tuning automatic = {FORGE_PROFILE_AUTO, 0, 0, 0, -1, 0};
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_tune = t ? *t : automatic;
+}
+
+void forge_get_tuning(forge_tuning* t) {
+  if (t) *t = current_tuning();
 }
 
 }  // extern "C"

@@ -58,6 +58,15 @@ class ForgeLinear(ctypes.Structure):
 
 MAX_GROUP = 8
 
+# forge_profile values
+PROFILES = {"auto": -1, "stream": 0, "mma": 1, "balanced": 2, "deep": 3}
+
+
+class ForgeTuning(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_int) for k in ("profile", "cta_group", "bn", "group_m",
+                                            "poll_store", "splits")]
+
+
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
 
@@ -114,6 +123,10 @@ def lib() -> ctypes.CDLL:
             L.forge_set_wait_limit_ns.restype = None
             L.forge_debug_drop_first_arrival.argtypes = [st]
             L.forge_debug_drop_first_arrival.restype = None
+            L.forge_set_tuning.argtypes = [ctypes.POINTER(ForgeTuning)]
+            L.forge_set_tuning.restype = None
+            L.forge_get_tuning.argtypes = [ctypes.POINTER(ForgeTuning)]
+            L.forge_get_tuning.restype = None
             _lib = L
         return _lib
 
@@ -154,6 +167,58 @@ def _dense(t: torch.Tensor, name: str) -> None:
         raise ValueError(f"{name} must be a CUDA tensor")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+    cur = torch.cuda.current_device()
+    if t.device.index != cur:
+        raise ValueError(f"{name} is on {t.device}, but the current device is cuda:{cur} "
+                         f"(the library runs on the current device)")
+
+
+def _want(t: Optional[torch.Tensor], name: str, shape, dtypes) -> None:
+    """Shape and dtype of one argument, checked before anything reaches the
+    library: the kernels size their tensor maps from the shapes they are
+    given, so a short buffer would be read or written past its end."""
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {list(dtypes)}")
+
+
+_BF16 = (torch.bfloat16,)
+_F32 = (torch.float32,)
+_MOM = (torch.float32, torch.bfloat16, torch.int8)
+
+
+def _operands(X: torch.Tensor, dY: torch.Tensor):
+    """bt, d_in, d_out of X [bt, d_in] and dY [bt, d_out] (both bf16)."""
+    if X.dim() != 2 or dY.dim() != 2:
+        raise ValueError("X and dY must be 2-D")
+    bt, d_in = X.shape
+    d_out = dY.shape[1]
+    _want(X, "X", (bt, d_in), _BF16)
+    _want(dY, "dY", (bt, d_out), _BF16)
+    return bt, d_in, d_out
+
+
+def _moments(m, v, m_scale, v_scale, d_out: int, d_in: int, dtypes=_MOM) -> int:
+    """Checks AdamW moments (and int8 scales) of a [d_out, d_in] weight;
+    returns the moment format."""
+    _want(m, "m", (d_out, d_in), dtypes)
+    _want(v, "v", (d_out, d_in), (m.dtype,))
+    fmt = moment_format(m)
+    if fmt == MOM_INT8_B128:
+        if d_in % 128:
+            raise ValueError("int8 moments need d_in % 128 == 0")
+        _want(m_scale, "m_scale", (d_out, d_in // 128), _F32)
+        _want(v_scale, "v_scale", (d_out, d_in // 128), _F32)
+    return fmt
+
+
+def _on_device(**tensors) -> None:
+    for n, t in tensors.items():
+        if t is not None:
+            _dense(t, n)
 
 
 def moment_format(m: torch.Tensor) -> int:
@@ -177,11 +242,10 @@ def wgrad_adamw(X: torch.Tensor, dY: torch.Tensor, W: torch.Tensor, m: torch.Ten
     """One fused step: G = dY^T X, AdamW on G, W/m/v (and int8 scales) updated
     in place.  X [bt, d_in] and dY [bt, d_out] bf16; W [d_out, d_in] bf16;
     m, v fp32, bf16 or int8 (with fp32 scales [d_out, d_in/128])."""
-    for t, n in ((X, "X"), (dY, "dY"), (W, "W"), (m, "m"), (v, "v")):
-        _dense(t, n)
-    bt, d_in = X.shape
-    d_out = dY.shape[1]
-    fmt = moment_format(m)
+    bt, d_in, d_out = _operands(X, dY)
+    _want(W, "W", (d_out, d_in), _BF16)
+    fmt = _moments(m, v, m_scale, v_scale, d_out, d_in)
+    _on_device(X=X, dY=dY, W=W, m=m, v=v, m_scale=m_scale, v_scale=v_scale)
     st = lib().forge_wgrad_adamw(
         _ptr(X), _ptr(dY), _ptr(W), _moment(m, m_scale), _moment(v, v_scale), bt, d_in, d_out,
         lr, beta1, beta2, eps, weight_decay, step, fmt, _stream(stream))
@@ -196,14 +260,17 @@ def wgrad_opt(X: torch.Tensor, dY: torch.Tensor, W: torch.Tensor, opt: int,
     """One fused step with optimizer `opt` (OPT_*) in place of AdamW: W and the
     optimizer's states s1, s2 (fp32 or bf16, as many as OPT_STATES says)
     updated in place."""
-    for t, n in ((X, "X"), (dY, "dY"), (W, "W")):
-        _dense(t, n)
-    states = [s for s in (s1, s2) if s is not None]
-    for s in states:
-        _dense(s, "state")
+    bt, d_in, d_out = _operands(X, dY)
+    _want(W, "W", (d_out, d_in), _BF16)
+    n_st = OPT_STATES.get(opt)
+    if n_st is None:
+        raise ValueError(f"unknown optimizer {opt}")
+    states = [s1, s2][:n_st]
+    for i, st_t in enumerate(states):
+        _want(st_t, f"s{i + 1}", (d_out, d_in),
+              (states[0].dtype,) if i else (torch.float32, torch.bfloat16))
+    _on_device(X=X, dY=dY, W=W, **{f"s{i + 1}": t for i, t in enumerate(states)})
     fmt = moment_format(states[0]) if states else MOM_FP32
-    bt, d_in = X.shape
-    d_out = dY.shape[1]
     h = ForgeOptHyper(lr, weight_decay, beta1, beta2, eps, momentum, alpha, momentum_decay)
     st = lib().forge_wgrad_opt(_ptr(X), _ptr(dY), _ptr(W), _moment(s1, None), _moment(s2, None),
                                bt, d_in, d_out, opt, ctypes.byref(h), step, fmt,
@@ -215,12 +282,9 @@ def wgrad_accumulate(X: torch.Tensor, dY: torch.Tensor, B: torch.Tensor, beta: f
                      stream=None) -> None:
     """B = beta * B + dY^T X (B fp32 [d_out, d_in], updated in place; not
     read when beta is 0)."""
-    for t, n in ((X, "X"), (dY, "dY"), (B, "B")):
-        _dense(t, n)
-    if B.dtype != torch.float32:
-        raise TypeError("B must be fp32")
-    bt, d_in = X.shape
-    d_out = dY.shape[1]
+    bt, d_in, d_out = _operands(X, dY)
+    _want(B, "B", (d_out, d_in), _F32)
+    _on_device(X=X, dY=dY, B=B)
     _check(lib().forge_wgrad_accumulate(_ptr(X), _ptr(dY), _ptr(B), beta, bt, d_in, d_out,
                                         _stream(stream)), "forge_wgrad_accumulate")
 
@@ -238,10 +302,10 @@ def wgrad_adamw_sr(X: torch.Tensor, dY: torch.Tensor, W: torch.Tensor, m: torch.
                    weight_decay: float, step: int, seed: int, stream=None) -> None:
     """wgrad_adamw with W committed by stochastic rounding (Philox4x64-10
     random bits from `seed`, the weight index and the step); fp32 or bf16 moments."""
-    for t, n in ((X, "X"), (dY, "dY"), (W, "W"), (m, "m"), (v, "v")):
-        _dense(t, n)
-    bt, d_in = X.shape
-    d_out = dY.shape[1]
+    bt, d_in, d_out = _operands(X, dY)
+    _want(W, "W", (d_out, d_in), _BF16)
+    _moments(m, v, None, None, d_out, d_in, (torch.float32, torch.bfloat16))
+    _on_device(X=X, dY=dY, W=W, m=m, v=v)
     st = lib().forge_wgrad_adamw_sr(
         _ptr(X), _ptr(dY), _ptr(W), _moment(m, None), _moment(v, None), bt, d_in, d_out,
         lr, beta1, beta2, eps, weight_decay, step, moment_format(m), seed, _stream(stream))
@@ -257,21 +321,23 @@ def wgrad_adamw_grouped(layers, *, lr: float, beta1: float, beta2: float, eps: f
     arr = (ForgeLinear * max(n, 1))()
     fmt = None
     bt = None
+    if n > MAX_GROUP:
+        raise ValueError(f"at most {MAX_GROUP} layers per grouped call")
     for i, ly in enumerate(layers):
-        for k in ("X", "dY", "W", "m", "v"):
-            _dense(ly[k], k)
-        f = moment_format(ly["m"])
+        b, d_in, d_out = _operands(ly["X"], ly["dY"])
+        _want(ly["W"], "W", (d_out, d_in), _BF16)
+        f = _moments(ly["m"], ly["v"], ly.get("m_scale"), ly.get("v_scale"), d_out, d_in)
+        _on_device(X=ly["X"], dY=ly["dY"], W=ly["W"], m=ly["m"], v=ly["v"],
+                   m_scale=ly.get("m_scale"), v_scale=ly.get("v_scale"))
         if fmt is not None and f != fmt:
             raise ValueError("all layers of a group need the same moment format")
         fmt = f
-        b = ly["X"].shape[0]
         if bt is not None and b != bt:
             raise ValueError("all layers of a group need the same token count")
         bt = b
         arr[i] = ForgeLinear(_ptr(ly["X"]), _ptr(ly["dY"]), _ptr(ly["W"]),
                              _moment(ly["m"], ly.get("m_scale")),
-                             _moment(ly["v"], ly.get("v_scale")),
-                             ly["X"].shape[1], ly["dY"].shape[1])
+                             _moment(ly["v"], ly.get("v_scale")), d_in, d_out)
     st = lib().forge_wgrad_adamw_grouped(arr, n, bt or 0, lr, beta1, beta2, eps, weight_decay,
                                          step, fmt if fmt is not None else 0, _stream(stream))
     _check(st, "forge_wgrad_adamw_grouped")
@@ -279,24 +345,31 @@ def wgrad_adamw_grouped(layers, *, lr: float, beta1: float, beta2: float, eps: f
 
 def wgrad(X: torch.Tensor, dY: torch.Tensor, dW: torch.Tensor, stream=None) -> None:
     """dW = dY^T X stored (fp32 or bf16 by dW's dtype)."""
-    for t, n in ((X, "X"), (dY, "dY"), (dW, "dW")):
-        _dense(t, n)
-    bt, d_in = X.shape
-    d_out = dY.shape[1]
+    bt, d_in, d_out = _operands(X, dY)
+    _want(dW, "dW", (d_out, d_in), (torch.float32, torch.bfloat16))
+    _on_device(X=X, dY=dY, dW=dW)
     dt = {torch.float32: DT_FP32, torch.bfloat16: DT_BF16}[dW.dtype]
     _check(lib().forge_wgrad(_ptr(X), _ptr(dY), _ptr(dW), dt, bt, d_in, d_out, _stream(stream)),
            "forge_wgrad")
 
 
+def _dgrad_shapes(dY: torch.Tensor, W: torch.Tensor, dX: torch.Tensor):
+    """bt, d_out, d_in of dY [bt, d_out], W [d_out, d_in], dX [bt, d_in] (bf16)."""
+    if dY.dim() != 2 or W.dim() != 2:
+        raise ValueError("dY and W must be 2-D")
+    bt, d_out = dY.shape
+    d_in = W.shape[1]
+    _want(dY, "dY", (bt, d_out), _BF16)
+    _want(W, "W", (d_out, d_in), _BF16)
+    _want(dX, "dX", (bt, d_in), _BF16)
+    _on_device(dY=dY, W=W, dX=dX)
+    return bt, d_out, d_in
+
+
 def dgrad(dY: torch.Tensor, W: torch.Tensor, dX: torch.Tensor, stream=None) -> None:
     """dX = dY W (bf16): the layer's input gradient.  dY [bt, d_out],
     W [d_out, d_in], dX [bt, d_in], all bf16."""
-    for t, n in ((dY, "dY"), (W, "W"), (dX, "dX")):
-        _dense(t, n)
-    if dX.dtype != torch.bfloat16:
-        raise TypeError("dX must be bf16")
-    bt, d_out = dY.shape
-    d_in = W.shape[1]
+    bt, d_out, d_in = _dgrad_shapes(dY, W, dX)
     _check(lib().forge_dgrad(_ptr(dY), _ptr(W), _ptr(dX), bt, d_in, d_out, _stream(stream)),
            "forge_dgrad")
 
@@ -304,12 +377,7 @@ def dgrad(dY: torch.Tensor, W: torch.Tensor, dX: torch.Tensor, stream=None) -> N
 def dgrad_noalloc(dY: torch.Tensor, W: torch.Tensor, dX: torch.Tensor, stream=None) -> None:
     """dgrad with its split partials in the library's static scratch (no
     allocation); calls of it on one device must not overlap in time."""
-    for t, n in ((dY, "dY"), (W, "W"), (dX, "dX")):
-        _dense(t, n)
-    if dX.dtype != torch.bfloat16:
-        raise TypeError("dX must be bf16")
-    bt, d_out = dY.shape
-    d_in = W.shape[1]
+    bt, d_out, d_in = _dgrad_shapes(dY, W, dX)
     _check(lib().forge_dgrad_noalloc(_ptr(dY), _ptr(W), _ptr(dX), bt, d_in, d_out,
                                      _stream(stream)), "forge_dgrad_noalloc")
 
@@ -321,13 +389,11 @@ def linear_backward(X: torch.Tensor, dY: torch.Tensor, W: torch.Tensor, dX: torc
                     v_scale: Optional[torch.Tensor] = None, stream=None) -> None:
     """The layer's backward step: dX = dY W from the weight before the update,
     then the fused weight-gradient + AdamW step (W, m, v updated in place)."""
-    for t, n in ((X, "X"), (dY, "dY"), (W, "W"), (dX, "dX"), (m, "m"), (v, "v")):
-        _dense(t, n)
-    if dX.dtype != torch.bfloat16:
-        raise TypeError("dX must be bf16")
-    bt, d_in = X.shape
-    d_out = dY.shape[1]
-    fmt = moment_format(m)
+    bt, d_in, d_out = _operands(X, dY)
+    _want(W, "W", (d_out, d_in), _BF16)
+    _want(dX, "dX", (bt, d_in), _BF16)
+    fmt = _moments(m, v, m_scale, v_scale, d_out, d_in)
+    _on_device(X=X, dY=dY, W=W, dX=dX, m=m, v=v, m_scale=m_scale, v_scale=v_scale)
     st = lib().forge_linear_backward(
         _ptr(X), _ptr(dY), _ptr(W), _ptr(dX), _moment(m, m_scale), _moment(v, v_scale), bt,
         d_in, d_out, lr, beta1, beta2, eps, weight_decay, step, fmt, _stream(stream))
@@ -339,16 +405,19 @@ def adamw(dW: Optional[torch.Tensor], W: torch.Tensor, m: torch.Tensor, v: torch
           m_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
           stream=None) -> None:
     """The unfused optimizer step on a stored gradient (None = zero gradient)."""
-    for t, n in ((W, "W"), (m, "m"), (v, "v")):
-        _dense(t, n)
+    if W.dim() != 2:
+        raise ValueError("W must be 2-D")
+    d_out, d_in = W.shape
+    _want(W, "W", (d_out, d_in), _BF16)
+    fmt = _moments(m, v, m_scale, v_scale, d_out, d_in)
     dt = DT_FP32
     if dW is not None:
-        _dense(dW, "dW")
+        _want(dW, "dW", (d_out, d_in), (torch.float32, torch.bfloat16))
         dt = {torch.float32: DT_FP32, torch.bfloat16: DT_BF16}[dW.dtype]
-    d_out, d_in = W.shape
+    _on_device(W=W, m=m, v=v, dW=dW, m_scale=m_scale, v_scale=v_scale)
     st = lib().forge_adamw(_ptr(dW), dt, _ptr(W), _moment(m, m_scale), _moment(v, v_scale),
-                           d_in, d_out, lr, beta1, beta2, eps, weight_decay, step,
-                           moment_format(m), _stream(stream))
+                           d_in, d_out, lr, beta1, beta2, eps, weight_decay, step, fmt,
+                           _stream(stream))
     _check(st, "forge_adamw")
 
 
@@ -387,6 +456,45 @@ def set_wait_limit_ns(ns: int) -> None:
 
 def debug_drop_first_arrival(enable: bool = True) -> None:
     lib().forge_debug_drop_first_arrival(1 if enable else 0)
+
+
+def get_tuning() -> dict:
+    """The tuning overrides in force (see forge_set_tuning in forge.h)."""
+    t = ForgeTuning()
+    lib().forge_get_tuning(ctypes.byref(t))
+    names = {v: k for k, v in PROFILES.items()}
+    return dict(profile=names.get(t.profile, "auto"), cg=t.cta_group, bn=t.bn,
+                group_m=t.group_m, poll_store=t.poll_store, splits=t.splits)
+
+
+def set_tuning(profile: str = "auto", cg: int = 0, bn: int = 0, group_m: int = 0,
+               poll_store: int = -1, splits: int = 0) -> None:
+    """Replace the tuning overrides (the defaults leave every choice to the
+    library).  profile: auto|stream|balanced|mma|deep; cg: 1 or 2 CTAs per
+    tile; bn: 128 or 256; group_m: 1..64; poll_store: 0 or 1; splits: 1..8."""
+    if profile not in PROFILES:
+        raise ValueError(f"unknown profile {profile}")
+    t = ForgeTuning(PROFILES[profile], int(cg), int(bn), int(group_m), int(poll_store),
+                    int(splits))
+    lib().forge_set_tuning(ctypes.byref(t))
+
+
+class tuning:
+    """Context manager: tuning overrides for the calls inside the block,
+    the previous ones restored afterwards.  Fields not given keep their
+    current value."""
+
+    def __init__(self, **kw):
+        self.kw = kw
+
+    def __enter__(self):
+        self.saved = get_tuning()
+        set_tuning(**{**self.saved, **self.kw})
+        return self
+
+    def __exit__(self, *exc):
+        set_tuning(**self.saved)
+        return False
 
 
 def alloc_moments(d_out: int, d_in: int, fmt: int, device="cuda"):

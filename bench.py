@@ -305,11 +305,32 @@ def run_gpu(args, rank, world, dev):
     if status != 0:
         raise RuntimeError(F.status_string(status))
     elapsed_ms = t_start.elapsed_time(t_end)
-    kern_ms = sum(a.elapsed_time(b) for row in ev for (a, b) in row)
-    if sampler:
-        sampler.stop()
+    launch_ms = [a.elapsed_time(b) for row in ev for (a, b) in row]
+    kern_ms = sum(launch_ms)
     if dist:
         elapsed_ms, kern_ms = max_over_ranks([elapsed_ms, kern_ms], dev)
+
+    # ---- the same launch repeated for about a second (diagnostic, after the
+    # timed region): per-launch statistics over a window long enough for the
+    # clock sampler, with the clock samples binned by quarter of the window
+    steady = None
+    if rank == 0:
+        est = max(kern_ms / max(1, args.steps), 1e-3)
+        n_st = int(min(20000, max(args.steps, math.ceil(1000.0 / est))))
+        sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_st)]
+        torch.cuda.synchronize()
+        s0 = time.perf_counter()
+        for k in range(n_st):
+            step += 1
+            sev[k][0].record(stream)
+            F.wgrad_adamw_grouped(layer.group, step=step, **HYPER)
+            sev[k][1].record(stream)
+        torch.cuda.synchronize()
+        s1 = time.perf_counter()
+        steady = dict(launch_ms=[a.elapsed_time(b) for a, b in sev], w0=s0, w1=s1)
+    if sampler:
+        sampler.stop()
 
     # ---- diagnostics (not the reported value): the same step as seven launches
     sep_steps = max(3, min(args.steps, 30))
@@ -435,46 +456,77 @@ def run_gpu(args, rank, world, dev):
     # computes, into the other of two device input sets; step 0's copies are
     # inside the timed region too, and no step starts before its own inputs
     # have landed.
-    e2e_steps = max(3, min(args.steps, 100))
+    e2e_steps = max(args.steps, 50)
     sets = [layer.group, layer.second_input_set()]
     copy_stream = torch.cuda.Stream(device=dev)
     copied = [torch.cuda.Event(), torch.cuda.Event()]
     consumed = [torch.cuda.Event(), torch.cuda.Event()]
+    cp_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(e2e_steps)]
+    st_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(e2e_steps)]
 
-    def stage_inputs(b):
+    def stage_inputs(b, k):
         with torch.cuda.stream(copy_stream):
             copy_stream.wait_event(consumed[b])      # the step that last read set b is done
+            cp_ev[k][0].record(copy_stream)
             for it, g in zip(layer.items, sets[b]):
                 g["X"].copy_(it["x_host"], non_blocking=True)
                 g["dY"].copy_(it["dy_host"], non_blocking=True)
+            cp_ev[k][1].record(copy_stream)
             copied[b].record(copy_stream)
 
+    # the host-to-device bandwidth of the step's copies alone (pinned memory)
+    h2d_ms = []
+    for _ in range(5):
+        stage_inputs(0, 0)
+        torch.cuda.synchronize()
+        h2d_ms.append(cp_ev[0][0].elapsed_time(cp_ev[0][1]))
     barrier()
     torch.cuda.synchronize()
     for ev in consumed:
         ev.record(stream)
     e0 = time.perf_counter()
-    stage_inputs(0)
+    e_first = None
+    stage_inputs(0, 0)
     for k in range(e2e_steps):
         step += 1
         b = k & 1
         stream.wait_event(copied[b])
+        st_ev[k][0].record(stream)
         F.wgrad_adamw_grouped(sets[b], step=step, stream=stream, **HYPER)
+        st_ev[k][1].record(stream)
         consumed[b].record(stream)
         if k + 1 < e2e_steps:         # issued while step k runs
-            stage_inputs(1 - b)
+            stage_inputs(1 - b, k + 1)
         st = F.device_error(stream)   # synchronises the step's stream, reads 4 bytes
         if st != 0:
             raise RuntimeError(F.status_string(st))
+        if k == 0:
+            e_first = time.perf_counter()
     e1 = time.perf_counter()
+    torch.cuda.synchronize()
     e2e_ms = (e1 - e0) * 1e3 / e2e_steps
+    copy_ms = [a.elapsed_time(b) for a, b in cp_ev[1:]]
+    comp_ms = [a.elapsed_time(b) for a, b in st_ev]
+    # copies of step k+1 that ended before step k's compute did: hidden
+    hidden = sum(1 for k in range(e2e_steps - 1)
+                 if st_ev[k][1].elapsed_time(cp_ev[k + 1][1]) <= 0.0)
+    e2e = dict(steps=e2e_steps,
+               first_step_ms=(e_first - e0) * 1e3,
+               later_steps_ms=(e1 - e_first) * 1e3 / max(1, e2e_steps - 1),
+               h2d_gbs=layer.h2d_bytes() / (statistics.median(h2d_ms) * 1e-3) / 1e9,
+               copy_ms_median=statistics.median(copy_ms) if copy_ms else None,
+               compute_ms_median=statistics.median(comp_ms),
+               copies_hidden_frac=hidden / max(1, e2e_steps - 1))
     if dist:
         e2e_ms, unf_ms = max_over_ranks([e2e_ms, unf_ms], dev)
 
-    return dict(layer=layer, elapsed_ms=elapsed_ms, kern_ms=kern_ms, unf_ms=unf_ms,
+    return dict(layer=layer, elapsed_ms=elapsed_ms, kern_ms=kern_ms, launch_ms=launch_ms,
+                steady=steady, sampler=sampler, unf_ms=unf_ms,
                 per_proj_ms=per_proj_ms, backward=backward, opt_ms=opt_ms, opt_fmt=sfmt,
                 acc_ms=acc_ms, sr_ms=sr_ms,
-                e2e_ms=e2e_ms, clocks=sampler.summary(w0, w1) if sampler else None,
+                e2e=e2e, e2e_ms=e2e_ms, clocks=sampler.summary(w0, w1) if sampler else None,
                 config=F.describe_config(bt, 4096, 4096, fmt))
 
 
@@ -614,19 +666,10 @@ def run_stack(args, dev):
     peaks, peak_kind = measured_peaks()
     flops, byts = stack.flops(), stack.alg_bytes()
     t_hbm = byts / (peaks["hbm_gbs"] * 1e9)
-    t_tc = flops / (peaks["bf16_tflops_sustained"] * 1e12)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
     kern_s_per_launch = kern_ms * 1e-3 / STACK_LAYERS
-    if t_hbm >= t_tc:
-        ach = byts / STACK_LAYERS / kern_s_per_launch / 1e9
-        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": ach / peaks["hbm_gbs"], "traffic": None,
-                "peak_kind": f"{peak_kind} (copy bandwidth)"}
-    else:
-        ach = flops / STACK_LAYERS / kern_s_per_launch / 1e12
-        pk = peaks["bf16_tflops_sustained"]
-        roof = {"bound": "tensor", "achieved": ach, "peak": pk, "unit": "TFLOP/s",
-                "frac": ach / pk, "traffic": None,
-                "peak_kind": f"{peak_kind} (cuBLAS bf16, sustained)"}
+    roof = roofline_of(flops / STACK_LAYERS, byts / STACK_LAYERS, kern_s_per_launch, peaks,
+                       peak_kind)
     line = {
         "metric": METRIC, "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -645,6 +688,153 @@ def run_stack(args, dev):
         "clocks": sampler.summary(w0, w1),
     }
     print(json.dumps(line))
+
+
+# ---------------------------------------------------------------------------
+# the other configurations of the metric, each timed in the same run
+# ---------------------------------------------------------------------------
+
+def _device_normal(g, shape, std, dev):
+    return (torch.randn(shape, generator=g, device=dev, dtype=torch.float32) * std
+            ).to(torch.bfloat16)
+
+
+def device_layer(bt, fmt, dy_std, spike, dev, seed):
+    """One layer's seven projections with inputs drawn on the device (the
+    recipe's distributions: X ~ N(0,1), dY ~ N(0, dy_std) with floor(spike*BT)
+    token rows x100, W ~ N(0, 0.02)); each projection has its own X."""
+    from weight_gradient_gemm_gb300 import forge as F
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    group = []
+    for name, d_out, d_in in LLAMA31_8B_SHAPES:
+        dy = torch.randn((bt, d_out), generator=g, device=dev, dtype=torch.float32) * dy_std
+        n = int(math.floor(spike * bt))
+        if n:
+            dy[torch.randperm(bt, generator=g, device=dev)[:n]] *= 100.0
+        m, v, ms, vs = F.alloc_moments(d_out, d_in, fmt, dev)
+        group.append(dict(X=_device_normal(g, (bt, d_in), 1.0, dev), dY=dy.to(torch.bfloat16),
+                          W=_device_normal(g, (d_out, d_in), 0.02, dev), m=m, v=v,
+                          m_scale=ms, v_scale=vs))
+    return group
+
+
+def roofline_of(flops, nbytes, launch_s, peaks, peak_kind, traffic=None):
+    """The roofline object of one launch: bound by whichever of the tensor
+    time (burst cuBLAS bf16 peak: every timed region here is tens of
+    milliseconds, a burst) or the HBM time (measured copy bandwidth) is
+    larger; `frac_sustained` gives the tensor fraction against the sustained
+    figure as well."""
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        ach = nbytes / launch_s / 1e9
+        return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "traffic": traffic,
+                "peak_kind": f"{peak_kind} (copy bandwidth)"}
+    ach = flops / launch_s / 1e12
+    sus = peaks.get("bf16_tflops_sustained")
+    return {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": ach / peaks["bf16_tflops"], "traffic": traffic,
+            "peak_kind": f"{peak_kind} (cuBLAS bf16, burst)",
+            "frac_sustained": ach / sus if sus else None}
+
+
+def launch_stats(ms):
+    return {"launches": len(ms), "median_ms": statistics.median(ms), "min_ms": min(ms),
+            "max_ms": max(ms), "mean_ms": sum(ms) / len(ms)}
+
+
+def timed_launches(fn, n, stream):
+    """n calls of fn, each bracketed by CUDA events on `stream`; returns the
+    per-launch milliseconds and the wall-clock window."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    for a, b in ev:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.perf_counter()
+    return [a.elapsed_time(b) for a, b in ev], w0, w1
+
+
+# (block name, workload it measures, BT, moment format, spike fraction)
+TENSOR_BLOCKS = [
+    ("c3_bt2048_bf16", "llama31_8b_layer_bt2048_bf16", 2048, 1, 0.01),
+    ("c4_bt4096_int8", "llama31_8b_layer_bt4096_int8", 4096, 2, 0.0),
+    ("bt4096_fp32", "llama31_8b_layer_bt4096_fp32", 4096, 0, 0.0),
+    ("c3_bt8192_bf16", "llama31_8b_layer_bt8192_bf16", 8192, 1, 0.01),
+]
+
+
+def config_blocks(args, dev, peaks, peak_kind):
+    """The metric's other Llama-3.1-8B configurations, each timed in-process
+    with CUDA events around every grouped launch (at least ~0.3 s of
+    launches, so the clock sampler sees them), with its own roofline, clocks
+    and stored ncu traffic: C3 at 2048 and 8192 tokens (bf16 moments), C4 at
+    4096 (int8), fp32 moments at 4096, and C5 (the 224-linear stack at 8192
+    tokens, fp32 moments, one grouped launch per layer)."""
+    from weight_gradient_gemm_gb300 import forge as F
+    stream = torch.cuda.current_stream()
+    sampler = ClockSampler(dev.index)
+    time.sleep(0.25)
+    out = {}
+    for name, workload, bt, fmt, spike in TENSOR_BLOCKS:
+        group = device_layer(bt, fmt, 1e-3, spike, dev, seed=7000 + bt + fmt)
+        step = [0]
+
+        def one():
+            step[0] += 1
+            F.wgrad_adamw_grouped(group, step=step[0], **HYPER)
+        for _ in range(max(args.warmup, 3) + 10):   # moments warmed by 10 prior steps
+            one()
+        warm_ms, _, _ = timed_launches(one, 3, stream)
+        n = max(args.steps, math.ceil(300.0 / max(statistics.median(warm_ms), 1e-3)))
+        ms, w0, w1 = timed_launches(one, n, stream)
+        if F.device_error() != 0:
+            raise RuntimeError(f"{name}: device error")
+        flops = sum(2.0 * bt * g["W"].numel() for g in group)
+        nbytes = sum(g["W"].numel() * STATE_BYTES[fmt]
+                     + 2.0 * bt * (g["X"].shape[1] + g["dY"].shape[1]) for g in group)
+        mean_s = sum(ms) / len(ms) * 1e-3
+        out[name] = {"workload": workload, "bt": bt, "moments": FMT_NAMES[fmt],
+                     "launch": "forge_wgrad_adamw_grouped, seven projections",
+                     "kernel": F.describe_config(bt, 4096, 4096, fmt),
+                     "tflops": flops / mean_s / 1e12,
+                     "roofline": roofline_of(flops, nbytes, mean_s, peaks, peak_kind,
+                                             stored_traffic(workload)),
+                     "per_launch": launch_stats(ms), "clocks": sampler.summary(w0, w1)}
+        del group
+        torch.cuda.empty_cache()
+    # C5: the whole stack at 8192 tokens
+    stack = Stack(8192, 0, 1e-3, dev)
+    step = [0]
+
+    def stack_once():
+        step[0] += 1
+        stack_step(F, stack, step[0])
+    for _ in range(max(args.warmup, 3)):
+        stack_once()
+    n = max(3, min(args.steps, 10))
+    ms, w0, w1 = timed_launches(stack_once, n, stream)
+    if F.device_error() != 0:
+        raise RuntimeError("stack: device error")
+    flops, nbytes = stack.flops(), stack.alg_bytes()
+    mean_s = sum(ms) / len(ms) * 1e-3
+    out["c5_stack_bt8192_fp32"] = {
+        "workload": "llama31_8b_stack_bt8192_fp32", "bt": 8192, "moments": "fp32",
+        "launch": "32 forge_wgrad_adamw_grouped launches per step, backward order",
+        "ms_per_step": mean_s * 1e3, "tflops": flops / mean_s / 1e12,
+        "roofline": roofline_of(flops / STACK_LAYERS, nbytes / STACK_LAYERS,
+                                mean_s / STACK_LAYERS, peaks, peak_kind),
+        "per_step": launch_stats(ms), "clocks": sampler.summary(w0, w1)}
+    sampler.stop()
+    del stack
+    torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -841,6 +1031,8 @@ def main():
                     help="one of %s, llama31_8b_layer_bt<BT>_<fp32|bf16|int8>, or the full "
                          "224-linear stack llama31_8b_stack_bt<BT>_<fp32|bf16|int8>" % sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-blocks", action="store_true",
+                    help="skip the other configurations (C3, C4, fp32 at 4096, the C5 stack)")
     ap.add_argument("--reference-budget", type=float, default=120.0,
                     help="seconds of oracle work the reference arm aims for (all steps)")
     ap.add_argument("--only", default="",
@@ -887,22 +1079,30 @@ def main():
     value = job_value(world, flops, ms * 1e-3) / 1e12
     launches = args.steps   # one grouped launch per step
     kern_s_per_launch = res["kern_ms"] * 1e-3 / launches
-    alg_bytes_launch = layer.alg_bytes()
-    alg_flops_launch = flops
     t_hbm = layer.alg_bytes() / (peaks["hbm_gbs"] * 1e9)
     t_tc = flops / (peaks["bf16_tflops"] * 1e12)
-    if t_hbm >= t_tc:
-        achieved = alg_bytes_launch / kern_s_per_launch / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": stored_traffic(args.workload),
-                "peak_kind": f"{peak_kind} (copy bandwidth)"}
-    else:
-        achieved = alg_flops_launch / kern_s_per_launch / 1e12
-        peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": stored_traffic(args.workload),
-                "peak_kind": f"{peak_kind} (cuBLAS bf16, sustained)"}
+    roof = roofline_of(flops, layer.alg_bytes(), kern_s_per_launch, peaks, peak_kind,
+                       stored_traffic(args.workload))
     roofline_time = max(t_hbm, t_tc)
+    steady = None
+    if res["steady"] is not None:
+        sd = res["steady"]
+        lm = sd["launch_ms"]
+        q = len(lm) // 4
+        span = sd["w1"] - sd["w0"]
+        quarters = []
+        for i in range(4):
+            part = lm[i * q:(i + 1) * q] if i < 3 else lm[3 * q:]
+            cs = res["sampler"].summary(sd["w0"] + i * span / 4, sd["w0"] + (i + 1) * span / 4)
+            quarters.append({"median_ms": statistics.median(part), "sm_mhz": cs["sm_mhz"],
+                             "samples": cs.get("samples")})
+        steady = {"what": "the same grouped launch repeated for about 1 s after the timed region",
+                  **launch_stats(lm),
+                  "roofline_frac_median": roofline_of(flops, layer.alg_bytes(),
+                                                      statistics.median(lm) * 1e-3, peaks,
+                                                      peak_kind)["frac"],
+                  "clocks": res["sampler"].summary(sd["w0"], sd["w1"]),
+                  "by_quarter": quarters}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -921,6 +1121,8 @@ def main():
                           "frac_of_roofline": roofline_time * 1e3 / ms,
                           "params_per_s": layer.params() / (ms * 1e-3) * world,
                           "hbm_gbs": layer.alg_bytes() / (ms * 1e-3) / 1e9},
+        "per_launch": launch_stats(res["launch_ms"]),
+        "steady": steady,
         "unfused": {"ms_per_step": res["unf_ms"],
                     "value": job_value(world, flops, res["unf_ms"] * 1e-3) / 1e12,
                     "fused_speedup": res["unf_ms"] / ms,
@@ -929,7 +1131,8 @@ def main():
                 "ms_per_step": res["e2e_ms"], "h2d_bytes_per_step": layer.h2d_bytes(),
                 "d2h_bytes_per_step": 4,
                 "pipeline": "X, dY of step k+1 copied from pinned host memory on a second "
-                            "stream while step k computes; 4-byte status read after every step"},
+                            "stream while step k computes; 4-byte status read after every step",
+                **res["e2e"]},
         "per_projection_separate_launches": [
             {"name": it["name"], "shape": [it["d_out"], it["d_in"]],
              "us": round(t * 1e3, 2),
@@ -950,6 +1153,10 @@ def main():
         "clocks": res["clocks"],
         "system": run_metadata(),
     }
+    if not args.no_blocks and world == 1:
+        del layer, res
+        torch.cuda.empty_cache()
+        line["configs"] = config_blocks(args, dev, peaks, peak_kind)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline_block(args.workload)
     print(json.dumps(line))

@@ -115,3 +115,19 @@ def test_bench_diagnostic_blocks_from_synthetic_timings():
     assert abs(bw["dgrad"]["roofline"]["frac"] - flops / 0.25e-3 / 1e12 / 1891.5) < 1e-9
     assert abs(bw["dgrad"]["vs_cublas"] - 0.6) < 1e-9
     json.dumps([opt, acc, bw])
+
+
+def test_roofline_uses_one_peak_for_the_bound_and_the_fraction():
+    import bench
+    peaks = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+    # tensor-bound: 223 TFLOP in 0.2 s against the burst peak, sustained reported beside it
+    r = bench.roofline_of(223e12 * 0.2, 4e9, 0.2, peaks, "measured")
+    assert r["bound"] == "tensor" and r["peak"] == 1900.0
+    assert r["frac"] == pytest.approx(223.0 / 1900.0)
+    assert r["frac_sustained"] == pytest.approx(223.0 / 1700.0)
+    # HBM-bound: 4.45 GB in 0.7 ms
+    r = bench.roofline_of(2 * 512 * 218e6, 4.45e9, 0.7e-3, peaks, "measured", traffic=4.4e9)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["traffic"] == 4.4e9
+    assert r["frac"] == pytest.approx(4.45e9 / 0.7e-3 / 1e9 / 6800.0)
+    st = bench.launch_stats([1.0, 3.0, 2.0])
+    assert st == {"launches": 3, "median_ms": 2.0, "min_ms": 1.0, "max_ms": 3.0, "mean_ms": 2.0}

@@ -22,7 +22,8 @@ import torch
 
 import oracle as O
 from weight_gradient_gemm_gb300 import forge as F
-from weight_gradient_gemm_gb300.inputs import (LLAMA31_8B_SHAPES, bf16_bits, bits_to_bf16,
+from weight_gradient_gemm_gb300.inputs import (LLAMA31_8B_SHAPES, LLAMA31_8B_X_GROUP,
+                                               bf16_bits, bits_to_bf16, make_layer_inputs,
                                                make_step_inputs)
 
 from .gpu_util import DEV, hyper_kwargs, mom_from_dev, mom_to_dev, require_gpu, same_moment
@@ -39,6 +40,13 @@ CONFIGS = [
     ("bt2048_bf16_spiky", 2, 2048, O.FMT_BF16, 1e-3, 0.01, 1),
     ("bt8192_bf16_spiky", 2, 8192, O.FMT_BF16, 1e-3, 0.01, 1),
     ("bt4096_int8_warm10", 3, 4096, O.FMT_INT8, 1e-3, 0.0, 10),
+    # fp32 moments at the stack workload's large token count: CTA pairs, the
+    # deep profile with half-tile fp32 slots
+    ("bt8192_fp32_warm2", 1, 8192, O.FMT_FP32, 1e-3, 0.0, 2),
+    # token counts that are not a multiple of the 64-token stage: the last
+    # stage is partly past the end of X and dY (read as zeros)
+    ("bt8193_bf16_ragged", 2, 8193, O.FMT_BF16, 1e-3, 0.01, 1),
+    ("bt4097_int8_ragged", 3, 4097, O.FMT_INT8, 1e-3, 0.0, 2),
 ]
 
 
@@ -123,6 +131,68 @@ def test_llama_layer_sampled_rows(cfg_id, cfg, bt, fmt, dy_std, spike, warm):
                          label=f"{cfg_id} {name}")
         print(cfg_id, name, rep["W"])
         assert np.all(np.isfinite(O.bf16_to_f64(bf16_bits(ly["W"].cpu()))))
+
+
+@pytest.mark.parametrize("bt", [512, 8192])
+def test_llama_stack_layers_in_backward_order(bt):
+    # The whole-stack workload's launch pattern on two decoder layers: fp32
+    # moments, one grouped launch per layer, layer 1 before layer 0 (backward
+    # order), and the model's sharing of activations (q, k, v read one X;
+    # gate and up another), so several layers of one launch read the same X
+    # buffer.  Sampled rows of every projection are compared with the oracle
+    # (one warm-up step by the oracle, then the compared step), and every
+    # tensor with the unfused pair run on copies of the same state.
+    cfg, fmt, layers_n, t_final = 5, O.FMT_FP32, 2, 2
+    launches, host = [], []
+    for li in range(layers_n):
+        start = make_layer_inputs(cfg, li, 0, 0, with_w=True)
+        warm = make_layer_inputs(cfg, li, 1, bt)
+        final = make_layer_inputs(cfg, li, t_final, bt)
+        xs = {g: x.to(DEV) for g, x in final["x"].items()}   # shared device buffers
+        group, hs = [], []
+        for i, (name, d_out, d_in) in enumerate(LLAMA31_8B_SHAPES):
+            rows = sample_rows(d_out, 7 * li + i)
+            xg = LLAMA31_8B_X_GROUP[name]
+            w0 = bf16_bits(start["w"][name])
+            w_r, m_r, v_r = O.step(bf16_bits(warm["x"][xg]), bf16_bits(warm["dy"][name]),
+                                   w0[rows].copy(), O.zero_moment(fmt, len(rows), d_in),
+                                   O.zero_moment(fmt, len(rows), d_in), HYPER, 1, rows=rows)
+            w_full = w0.copy()
+            w_full[rows] = w_r
+            md, _ = mom_to_dev(_put_rows(O.zero_moment(fmt, d_out, d_in), rows, m_r))
+            vd, _ = mom_to_dev(_put_rows(O.zero_moment(fmt, d_out, d_in), rows, v_r))
+            group.append(dict(X=xs[xg], dY=final["dy"][name].to(DEV),
+                              W=bits_to_bf16(w_full).to(DEV), m=md, v=vd))
+            hs.append(dict(name=name, rows=rows, w_r=w_r, m_r=m_r, v_r=v_r, xg=xg,
+                           d_in=d_in, d_out=d_out))
+        launches.append(group)
+        host.append((final, hs))
+    copies = [[{k: (v.clone() if k in ("W", "m", "v") else v) for k, v in ly.items()}
+               for ly in group] for group in launches]
+    for li in reversed(range(layers_n)):          # backward order: the last layer first
+        F.wgrad_adamw_grouped(launches[li], step=t_final, **hyper_kwargs(HYPER))
+    assert F.device_error() == 0
+    dw = torch.empty(14336 * 4096, dtype=torch.float32, device=DEV)
+    for li in reversed(range(layers_n)):
+        for c in reversed(copies[li]):            # down, up, gate, o, v, k, q
+            g = dw[:c["W"].numel()].view(c["W"].shape)
+            F.wgrad(c["X"], c["dY"], g)
+            F.adamw(g, c["W"], c["m"], c["v"], step=t_final, **hyper_kwargs(HYPER))
+    assert F.device_error() == 0
+    for li in range(layers_n):
+        final, hs = host[li]
+        for ly, c, h in zip(launches[li], copies[li], hs):
+            for k in ("W", "m", "v"):
+                assert torch.equal(ly[k].view(torch.uint8), c[k].view(torch.uint8)), (li, h["name"], k)
+            rows = h["rows"]
+            xb, db = bf16_bits(final["x"][h["xg"]]), bf16_bits(final["dy"][h["name"]])
+            ref = dict(G=O.wgrad(xb, db, rows), S=O.wgrad_abs(xb, db, rows), W_bits=h["w_r"],
+                       m=h["m_r"], v=h["v_r"])
+            rep = check_step(bf16_bits(ly["W"][rows].cpu()),
+                             mom_from_dev(fmt, ly["m"][rows], None),
+                             mom_from_dev(fmt, ly["v"][rows], None), ref, HYPER, t_final, fmt, bt,
+                             label=f"stack bt{bt} layer {li} {h['name']}")
+            print(f"stack bt{bt} layer {li}", h["name"], rep["W"])
 
 
 def test_fused_path_has_no_bf16_gradient_bias():

@@ -77,6 +77,34 @@ def make_step_inputs(config: int, shape_idx: int, step: int, bt: int, d_in: int,
     return StepInputs(x=x, dy=dy32.to(torch.bfloat16), w=w)
 
 
+# Which activations each projection reads in the model: q, k, v share the
+# attention input, gate and up the MLP input; o and down have their own.
+LLAMA31_8B_X_GROUP = {"q": "attn", "k": "attn", "v": "attn", "o": "o", "gate": "mlp",
+                      "up": "mlp", "down": "down"}
+_X_GROUPS = ("attn", "o", "mlp", "down")
+
+
+def make_layer_inputs(config: int, layer: int, step: int, bt: int, dy_std: float = 1e-3,
+                      x_std: float = 1.0, w_std: float = 0.02, with_w: bool = False):
+    """One decoder layer's step inputs with the model's sharing of X: a dict
+    with ``x`` (group name -> X [BT, Din] bf16), ``dy`` (projection -> dY
+    [BT, Dout] bf16) and, with ``with_w``, ``w`` (projection -> initial W).
+    Every tensor has its own seed, ``seed_of(config, 20 * layer + j, step)``
+    with j = 0..3 for the X groups and 4..10 for the projections (W: step 0
+    of index 11..17)."""
+    x, dy, w = {}, {}, {}
+    for j, grp in enumerate(_X_GROUPS):
+        d_in = 14336 if grp == "down" else 4096
+        x[grp] = _normal_bf16(_gen(seed_of(config, 20 * layer + j, step)), (bt, d_in), x_std)
+    for j, (name, d_out, d_in) in enumerate(LLAMA31_8B_SHAPES):
+        g = _gen(seed_of(config, 20 * layer + 4 + j, step))
+        dy[name] = _normal_bf16(g, (bt, d_out), dy_std)
+        if with_w:
+            gw = _gen(seed_of(config, 20 * layer + 11 + j, 0))
+            w[name] = _normal_bf16(gw, (d_out, d_in), w_std)
+    return dict(x=x, dy=dy, w=w)
+
+
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """The uint16 bit patterns of a bf16 CPU tensor (what the oracle reads)."""
     assert t.dtype == torch.bfloat16

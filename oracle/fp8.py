@@ -9,7 +9,7 @@ LLM Training".  Its fp8 state mode stores the moments in fp8 with one scale
 per tensor and delayed scaling; the page reports that mode's weight error
 rather than bounding it (the weight-error table, Appendix B's discussion of
 the quantized modes).  It does not fix the fp8 format, the scaling history or
-the first step's scale.  No kernel implements this mode yet.
+the first step's scale.
 
 Readings:
 
@@ -24,6 +24,12 @@ R23 Delayed scaling: a step reads its moments with the scales they were
     formed from amaxes of earlier steps; the step reports the amax of the new
     fp64 moments (max |m'|, max sqrt(v')) for the caller's next scales, e.g.
     scale = amax / 448.
+R24 The scale roll between steps (a history of one step): the scale the new
+    moments were written with becomes the scale they are read with, and the
+    next write scale is amax * headroom / 448 (headroom >= 1 leaves room for
+    the moments to grow before they saturate), formed in fp32 as two
+    rounded operations, product first; an amax of 0 keeps the old write
+    scale (a tensor whose moments are all zero has no range to fit).
 """
 from __future__ import annotations
 
@@ -31,7 +37,8 @@ import numpy as np
 
 from .forge_oracle import adamw_f64, bf16_to_f64, f64_to_bf16, f64_to_f32, wgrad
 
-__all__ = ["E4M3_MAX", "e4m3_to_f64", "f64_to_e4m3", "encode_fp8", "decode_fp8", "step_fp8"]
+__all__ = ["E4M3_MAX", "e4m3_to_f64", "f64_to_e4m3", "encode_fp8", "decode_fp8", "step_fp8",
+           "roll_fp8_scales"]
 
 E4M3_MAX = 448.0
 
@@ -98,3 +105,12 @@ def step_fp8(x_bits, dy_bits, w_bits, m_codes, m_scale, r_codes, r_scale, m_scal
     return (f64_to_bf16(W1), encode_fp8(m1, m_scale_new), encode_fp8(r1, r_scale_new),
             f64_to_f32(np.max(np.abs(m1))) if m1.size else np.float32(0),
             f64_to_f32(np.max(r1)) if r1.size else np.float32(0))
+
+
+def roll_fp8_scales(read_scale, write_scale, amax, headroom):
+    """R24: the scales of the next step, (read, write), as float32."""
+    w = np.float32(write_scale)
+    a = np.float32(amax)
+    if a > 0:
+        w = np.float32(np.float32(a * np.float32(headroom)) / np.float32(E4M3_MAX))
+    return np.float32(write_scale), w

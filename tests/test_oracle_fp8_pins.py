@@ -1,5 +1,4 @@
-"""Pins of the fp8-moment oracle (``oracle/fp8.py``; no kernel implements
-the mode yet):
+"""Pins of the fp8-moment oracle (``oracle/fp8.py``):
 
 * e4m3 encoding against PyTorch's own ``float8_e4m3fn`` cast (independent
   code) on in-range fp32 values, normal and subnormal, and decoding of all
@@ -7,7 +6,10 @@ the mode yet):
 * saturation at +-448 and the exact round trip of every code;
 * per-tensor scaling: power-of-two scales move only the exponent;
 * the step: decoded moments within half an e4m3 step of the fp64 AdamW
-  moments, and the reported amaxes equal to those of the fp64 moments.
+  moments, and the reported amaxes equal to those of the fp64 moments;
+* the scale roll: an amax of exactly 448 / headroom gives a write scale of
+  exactly 1, a moment at the old amax lands on the largest code after the
+  roll, and a zero amax keeps the old scale.
 """
 import warnings
 
@@ -73,3 +75,20 @@ def test_fp8_step_moments_and_amax():
         got = O.decode_fp8(codes, scale)
         bound = 2.0 ** -4 * np.abs(exact) + 2.0 ** -10 * float(np.float32(scale))
         assert np.all(np.abs(got - exact) <= bound)
+
+
+def test_scale_roll_closed_forms():
+    # the write scale becomes the read scale; amax * headroom / 448
+    r, w = O.roll_fp8_scales(0.5, 0.25, 224.0, 2.0)
+    assert r == np.float32(0.25) and w == np.float32(1.0)
+    # a moment equal to the amax then encodes to the largest finite code
+    amax = np.float32(3.7e-4)
+    _, w = O.roll_fp8_scales(1.0, 1.0, amax, 1.0)
+    assert O.encode_fp8(np.array([float(amax)]), w)[0] in (0x7E, 0x7D)
+    assert abs(O.decode_fp8(O.encode_fp8(np.array([float(amax)]), w), w)[0] - amax) \
+        <= 2.0 ** -4 * amax
+    # headroom 2: the old amax sits one binade below saturation
+    _, w2 = O.roll_fp8_scales(1.0, 1.0, amax, 2.0)
+    assert w2 == np.float32(2.0) * w
+    # no range to fit: keep the old write scale
+    assert O.roll_fp8_scales(3.0, 5.0, 0.0, 2.0) == (np.float32(5.0), np.float32(5.0))

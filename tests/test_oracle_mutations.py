@@ -412,3 +412,27 @@ def test_fp8_pins_pass_on_the_unmodified_oracle():
     assert not _fails_one([P8.test_encoding_matches_torch_float8_e4m3fn,
                            P8.test_decoding_all_codes_matches_torch_and_round_trips,
                            P8.test_saturation_and_power_of_two_scales])
+
+
+_ORIG_ROLL = F8.roll_fp8_scales
+
+
+def _roll_variant(kind):
+    def roll(read_scale, write_scale, amax, headroom):
+        if kind == "read_not_rolled":
+            return np.float32(read_scale), _ORIG_ROLL(read_scale, write_scale, amax, headroom)[1]
+        if kind == "int8_range":
+            return np.float32(write_scale), np.float32(np.float32(amax) * headroom / 127.0)
+        # headroom ignored
+        return _ORIG_ROLL(read_scale, write_scale, amax, 1.0)
+    return roll
+
+
+@pytest.mark.parametrize("kind", ["read_not_rolled", "int8_range", "no_headroom"])
+def test_fp8_scale_roll_mistakes_are_caught(monkeypatch, kind):
+    f = _roll_variant(kind)
+    monkeypatch.setattr(F8, "roll_fp8_scales", f)
+    monkeypatch.setattr(O, "roll_fp8_scales", f)
+    assert _fails_one([P8.test_scale_roll_closed_forms])
+    monkeypatch.setattr(O, "roll_fp8_scales", _ORIG_ROLL)
+    assert not _fails_one([P8.test_scale_roll_closed_forms])

@@ -44,8 +44,11 @@ OPT_HYPER = [dict(_FAM), dict(_FAM, momentum=0.9), dict(_FAM, eps=1e-10), dict(_
              dict(lr=3e-6, weight_decay=1.0, beta1=0.9, beta2=0.99),
              dict(_FAM, beta1=0.9, beta2=0.999, eps=1e-8),
              dict(_FAM, beta1=0.9, beta2=0.999, eps=1e-8)]
-FMT_NAMES = {0: "fp32", 1: "bf16", 2: "int8_block128"}
-STATE_BYTES = {0: 20.0, 1: 12.0, 2: 8.0 + 16.0 / 128.0}   # W r/w + m, v r/w (+ scales)
+FMT_NAMES = {0: "fp32", 1: "bf16", 2: "int8_block128", 3: "fp8_e4m3_per_tensor"}
+# bytes per parameter: W read + write, m and v read + write (+ int8 block
+# scales; fp8's 16 bytes per tensor are not counted)
+STATE_BYTES = {0: 20.0, 1: 12.0, 2: 8.0 + 16.0 / 128.0, 3: 8.0}
+FP8_HEADROOM = 2.0
 L2_BYTES = 126 * 2 ** 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -56,14 +59,16 @@ WORKLOADS = {
     "llama31_8b_layer_bt2048_bf16": (2, 2048, 1, 1e-3, 0.01),
     "llama31_8b_layer_bt8192_bf16": (2, 8192, 1, 1e-3, 0.01),
     "llama31_8b_layer_bt4096_int8": (3, 4096, 2, 1e-3, 0.0),
+    "llama31_8b_layer_bt512_fp8": (4, 512, 3, 1e-3, 0.0),
 }
 DEFAULT_WORKLOAD = "llama31_8b_layer_bt512_fp32"
-_RECIPE = {"fp32": (1, 0, 1e-3, 0.0), "bf16": (2, 1, 1e-3, 0.01), "int8": (3, 2, 1e-3, 0.0)}
+_RECIPE = {"fp32": (1, 0, 1e-3, 0.0), "bf16": (2, 1, 1e-3, 0.01), "int8": (3, 2, 1e-3, 0.0),
+           "fp8": (4, 3, 1e-3, 0.0)}
 
 
 def workload_spec(name: str):
     """(recipe config, BT, moment format, dY std, spike fraction) of a named
-    workload; besides the table, any llama31_8b_layer_bt<BT>_<fp32|bf16|int8>."""
+    workload; besides the table, any llama31_8b_layer_bt<BT>_<fp32|bf16|int8|fp8>."""
     if name in WORKLOADS:
         return WORKLOADS[name]
     parts = name.split("_")
@@ -187,6 +192,8 @@ class Layer:
     def __init__(self, cfg, bt, fmt, dy_std, spike, dev, with_host=True, only=None):
         from weight_gradient_gemm_gb300 import forge as F
         self.items = []
+        # fp8 moments: every tensor's scale record in one buffer, rolled after each step
+        self.fp8_scales = F.alloc_fp8_scales(14, device=dev) if fmt == 3 else None
         for i, (name, d_out, d_in) in enumerate(LLAMA31_8B_SHAPES):
             if only and name not in only:
                 continue
@@ -195,6 +202,8 @@ class Layer:
             x_host = s.x.pin_memory() if with_host else None
             dy_host = s.dy.pin_memory() if with_host else None
             m, v, ms, vs = F.alloc_moments(d_out, d_in, fmt, dev)
+            if fmt == 3:
+                ms, vs = self.fp8_scales[2 * i], self.fp8_scales[2 * i + 1]
             self.items.append(dict(
                 name=name, d_in=d_in, d_out=d_out, x=s.x.to(dev), dy=s.dy.to(dev),
                 w=s.w.to(dev), m=m, v=v, ms=ms, vs=vs, x_host=x_host, dy_host=dy_host))
@@ -226,10 +235,13 @@ class Layer:
 
 
 def fused_step(F, layer, step, events=None, stream=None):
-    """One step: the seven projections in one grouped launch."""
+    """One step: the seven projections in one grouped launch (with fp8
+    moments, then the scale roll of delayed scaling)."""
     if events is not None:
         events[0][0].record(stream)
     F.wgrad_adamw_grouped(layer.group, step=step, **HYPER)
+    if layer.fp8_scales is not None:
+        F.fp8_roll_scales(layer.fp8_scales, FP8_HEADROOM)
     if events is not None:
         events[0][1].record(stream)
 
@@ -323,9 +335,7 @@ def run_gpu(args, rank, world, dev):
         s0 = time.perf_counter()
         for k in range(n_st):
             step += 1
-            sev[k][0].record(stream)
-            F.wgrad_adamw_grouped(layer.group, step=step, **HYPER)
-            sev[k][1].record(stream)
+            fused_step(F, layer, step, [sev[k]], stream)
         torch.cuda.synchronize()
         s1 = time.perf_counter()
         steady = dict(launch_ms=[a.elapsed_time(b) for a, b in sev], w0=s0, w1=s1)
@@ -495,6 +505,8 @@ def run_gpu(args, rank, world, dev):
         stream.wait_event(copied[b])
         st_ev[k][0].record(stream)
         F.wgrad_adamw_grouped(sets[b], step=step, stream=stream, **HYPER)
+        if layer.fp8_scales is not None:
+            F.fp8_roll_scales(layer.fp8_scales, FP8_HEADROOM, stream=stream)
         st_ev[k][1].record(stream)
         consumed[b].record(stream)
         if k + 1 < e2e_steps:         # issued while step k runs
@@ -707,16 +719,19 @@ def device_layer(bt, fmt, dy_std, spike, dev, seed):
     g = torch.Generator(device=dev)
     g.manual_seed(seed)
     group = []
-    for name, d_out, d_in in LLAMA31_8B_SHAPES:
+    scales = F.alloc_fp8_scales(14, device=dev) if fmt == 3 else None
+    for i, (name, d_out, d_in) in enumerate(LLAMA31_8B_SHAPES):
         dy = torch.randn((bt, d_out), generator=g, device=dev, dtype=torch.float32) * dy_std
         n = int(math.floor(spike * bt))
         if n:
             dy[torch.randperm(bt, generator=g, device=dev)[:n]] *= 100.0
         m, v, ms, vs = F.alloc_moments(d_out, d_in, fmt, dev)
+        if scales is not None:
+            ms, vs = scales[2 * i], scales[2 * i + 1]
         group.append(dict(X=_device_normal(g, (bt, d_in), 1.0, dev), dY=dy.to(torch.bfloat16),
                           W=_device_normal(g, (d_out, d_in), 0.02, dev), m=m, v=v,
                           m_scale=ms, v_scale=vs))
-    return group
+    return group, scales
 
 
 def roofline_of(flops, nbytes, launch_s, peaks, peak_kind, traffic=None):
@@ -763,6 +778,7 @@ def timed_launches(fn, n, stream):
 
 # (block name, workload it measures, BT, moment format, spike fraction)
 TENSOR_BLOCKS = [
+    ("fp8_bt512", "llama31_8b_layer_bt512_fp8", 512, 3, 0.0),
     ("c3_bt2048_bf16", "llama31_8b_layer_bt2048_bf16", 2048, 1, 0.01),
     ("c4_bt4096_int8", "llama31_8b_layer_bt4096_int8", 4096, 2, 0.0),
     ("bt4096_fp32", "llama31_8b_layer_bt4096_fp32", 4096, 0, 0.0),
@@ -774,21 +790,25 @@ def config_blocks(args, dev, peaks, peak_kind):
     """The metric's other Llama-3.1-8B configurations, each timed in-process
     with CUDA events around every grouped launch (at least ~0.3 s of
     launches, so the clock sampler sees them), with its own roofline, clocks
-    and stored ncu traffic: C3 at 2048 and 8192 tokens (bf16 moments), C4 at
-    4096 (int8), fp32 moments at 4096, and C5 (the 224-linear stack at 8192
-    tokens, fp32 moments, one grouped launch per layer)."""
+    and stored ncu traffic: fp8 moments at 512 tokens (HBM-bound; each step
+    is the grouped launch plus the scale roll), C3 at 2048 and 8192 tokens
+    (bf16 moments), C4 at 4096 (int8), fp32 moments at 4096, and C5 (the
+    224-linear stack at 8192 tokens, fp32 moments, one grouped launch per
+    layer)."""
     from weight_gradient_gemm_gb300 import forge as F
     stream = torch.cuda.current_stream()
     sampler = ClockSampler(dev.index)
     time.sleep(0.25)
     out = {}
     for name, workload, bt, fmt, spike in TENSOR_BLOCKS:
-        group = device_layer(bt, fmt, 1e-3, spike, dev, seed=7000 + bt + fmt)
+        group, f8 = device_layer(bt, fmt, 1e-3, spike, dev, seed=7000 + bt + fmt)
         step = [0]
 
         def one():
             step[0] += 1
             F.wgrad_adamw_grouped(group, step=step[0], **HYPER)
+            if f8 is not None:
+                F.fp8_roll_scales(f8, FP8_HEADROOM)
         for _ in range(max(args.warmup, 3) + 10):   # moments warmed by 10 prior steps
             one()
         warm_ms, _, _ = timed_launches(one, 3, stream)
@@ -807,7 +827,7 @@ def config_blocks(args, dev, peaks, peak_kind):
                      "roofline": roofline_of(flops, nbytes, mean_s, peaks, peak_kind,
                                              stored_traffic(workload)),
                      "per_launch": launch_stats(ms), "clocks": sampler.summary(w0, w1)}
-        del group
+        del group, f8
         torch.cuda.empty_cache()
     # C5: the whole stack at 8192 tokens
     stack = Stack(8192, 0, 1e-3, dev)
@@ -1077,8 +1097,8 @@ def main():
     ms = res["elapsed_ms"] / args.steps
     flops = layer.flops()
     value = job_value(world, flops, ms * 1e-3) / 1e12
-    launches = args.steps   # one grouped launch per step
-    kern_s_per_launch = res["kern_ms"] * 1e-3 / launches
+    launches = args.steps * (2 if fmt == 3 else 1)   # the grouped launch (+ fp8 scale roll)
+    kern_s_per_launch = res["kern_ms"] * 1e-3 / args.steps
     t_hbm = layer.alg_bytes() / (peaks["hbm_gbs"] * 1e9)
     t_tc = flops / (peaks["bf16_tflops"] * 1e12)
     roof = roofline_of(flops, layer.alg_bytes(), kern_s_per_launch, peaks, peak_kind,

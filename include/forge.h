@@ -10,7 +10,10 @@
  *   - section 2.2, Algorithm 1: AdamW is applied to each accumulator tile and
  *     only W, m and v return to memory; G is never stored;
  *   - section 1, Eq. 1 and Appendix B "INT8 states": moments stored as fp32,
- *     bf16 or blockwise-absmax int8.
+ *     bf16 or blockwise-absmax int8;
+ *   - the weight-error table's "FORGE fp8 states (per-tensor scale)" row and
+ *     the delayed scaling described with it: moments stored as fp8 with one
+ *     scale per tensor.
  *
  * Layout.  Every matrix is dense, row-major, with no padding between rows:
  *   X  [bt,    d_in ]  bf16   activations of the layer's forward pass
@@ -19,6 +22,7 @@
  *   dW [d_out, d_in ]  fp32 or bf16 (forge_wgrad output, forge_adamw input)
  *   m, v [d_out, d_in] moments in the chosen format, updated in place
  *   int8 scales [d_out, d_in/128] fp32, one per row and 128-column block.
+ *   fp8 scales: one forge_fp8_scales (four fp32 words) per moment tensor.
  *
  * Ownership.  The caller owns every buffer (device memory).  The library
  * keeps a small host-side cache of TMA descriptors keyed by pointer and
@@ -68,8 +72,9 @@ typedef enum {
   FORGE_ERR_NULL = 1,           /* a required pointer is NULL                         */
   FORGE_ERR_ALIGN = 2,          /* a pointer is not 16-byte aligned                   */
   FORGE_ERR_SHAPE = 3,          /* bt < 0, d_in/d_out <= 0 or not a multiple of 8,
-                                   int8 moments with d_in % 128 != 0, or a size over
-                                   the 32-bit index range of the kernels             */
+                                   int8 moments with d_in % 128 != 0, fp8 moments
+                                   with d_in % 16 != 0, or a size over the 32-bit
+                                   index range of the kernels                        */
   FORGE_ERR_FORMAT = 4,         /* unknown moment format or dtype                     */
   FORGE_ERR_HYPER = 5,          /* step < 1, beta outside [0,1), lr/eps/wd < 0 or NaN */
   FORGE_ERR_ALIAS = 6,          /* an input overlaps an output                        */
@@ -84,20 +89,45 @@ typedef enum {
 typedef enum {
   FORGE_MOM_FP32 = 0,       /* k = 8 bytes of state per parameter                   */
   FORGE_MOM_BF16 = 1,       /* k = 4, round to nearest even                          */
-  FORGE_MOM_INT8_B128 = 2   /* k = 2 (+ scales): per row and 128-column block an
+  FORGE_MOM_INT8_B128 = 2,  /* k = 2 (+ scales): per row and 128-column block an
                                absmax scale s = a/127 and codes round(x/s) in
                                [-127,127]; the second moment is stored as
                                r = sqrt(v) with codes in [1,127] when a > 0       */
+  FORGE_MOM_FP8_E4M3 = 3    /* k = 2 (+ 16 bytes per tensor): e4m3 codes (OCP
+                               "fn": bias 7, largest finite 448, no infinities)
+                               with one scale per tensor, delayed scaling; the
+                               second moment is stored as r = sqrt(v).  Value =
+                               e4m3(code) * read_scale; a new value x is stored
+                               as e4m3(x * (1 / write_scale)), rounded to nearest
+                               even and saturated at +-448 (see forge_fp8_scales) */
 } forge_moment_fmt;
 
 typedef enum { FORGE_DT_FP32 = 0, FORGE_DT_BF16 = 1 } forge_dtype;
 
-/* One moment tensor.  data: fp32, bf16 or int8 [d_out, d_in].  scale: fp32
- * [d_out, d_in/128] for FORGE_MOM_INT8_B128, ignored (may be NULL) otherwise. */
+/* One moment tensor.  data: fp32, bf16, int8 or e4m3 codes [d_out, d_in].
+ * scale: for FORGE_MOM_INT8_B128 fp32 [d_out, d_in/128]; for
+ * FORGE_MOM_FP8_E4M3 a forge_fp8_scales (cast to float*); ignored (may be
+ * NULL) otherwise. */
 typedef struct {
   void* data;
   float* scale;
 } forge_moment;
+
+/* The per-tensor words of an fp8 moment, in device memory, 16-byte aligned.
+ * A step reads the stored codes with read_scale, writes the new codes with
+ * write_scale (both > 0 and finite: they live in device memory and are not
+ * checked), and raises amax to at least max |m'| (first moment) or
+ * max sqrt(v') (second moment) of this step's new, unrounded moments; amax
+ * is only ever raised, so the caller clears it between steps
+ * (forge_fp8_roll_scales does).  The caller forms write_scale from earlier
+ * steps' amaxes (delayed scaling); the first step's scales are the caller's
+ * choice, since no history exists yet. */
+typedef struct {
+  float read_scale;
+  float write_scale;
+  float amax;
+  float reserved;
+} forge_fp8_scales;
 
 /* A cudaStream_t passed as an opaque pointer; NULL is the legacy default stream. */
 typedef void* forge_stream;
@@ -336,6 +366,20 @@ forge_status forge_adamw(const void* dW, forge_dtype dw_dtype, void* W,
                          float lr, float beta1, float beta2, float eps,
                          float weight_decay, int64_t step,
                          forge_moment_fmt fmt, forge_stream stream);
+
+/*
+ * forge_fp8_roll_scales: the scale roll between two steps of fp8 moments,
+ * for n tensors' forge_fp8_scales (a device array, consecutive): read_scale
+ * <- write_scale (the codes were just written with it); write_scale <-
+ * amax * headroom / 448 in fp32 (product rounded, then quotient), or
+ * unchanged when amax is 0; amax <- 0.  headroom >= 1 leaves room for the
+ * moments to grow by that factor before they saturate.  One small kernel on
+ * `stream`, so the whole delayed-scaling loop stays on the device.
+ * Errors: FORGE_ERR_SHAPE for n < 0, FORGE_ERR_NULL, FORGE_ERR_ALIGN,
+ * FORGE_ERR_HYPER for headroom < 1 or not finite.
+ */
+forge_status forge_fp8_roll_scales(forge_fp8_scales* scales, int n, float headroom,
+                                   forge_stream stream);
 
 /* Synchronises `stream`, then returns and clears the device error word of the
  * current device: FORGE_OK, FORGE_ERR_DEVICE_TIMEOUT if a kernel gave up on a

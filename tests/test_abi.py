@@ -22,7 +22,8 @@ def test_header_declares_the_boundary():
     for n in ("forge_wgrad_adamw", "forge_wgrad", "forge_adamw", "forge_device_error",
               "forge_status_string", "forge_wgrad_adamw_grouped", "forge_dgrad",
               "forge_linear_backward", "forge_describe_dgrad_config", "forge_dgrad_noalloc",
-              "forge_wgrad_opt", "forge_wgrad_accumulate", "forge_wgrad_adamw_sr"):
+              "forge_wgrad_opt", "forge_wgrad_accumulate", "forge_wgrad_adamw_sr",
+              "forge_fp8_roll_scales", "forge_set_tuning", "forge_get_tuning"):
         assert n in names
 
 
@@ -102,6 +103,28 @@ def test_fused_argument_errors(L):
     assert fused(L, X=C) == 6                        # FORGE_ERR_ALIAS: X is W
     assert fused(L, dY=D + 64) == 6                  # dY inside m
     assert fused(L, v=(D, None)) == 6                # m and v the same buffer
+
+
+def test_fp8_argument_errors(L):
+    # fp8 moments: the scale records are required and 16-byte aligned, rows
+    # of codes must be 16-byte aligned (d_in % 16), and the record of one
+    # moment must not overlap the other's
+    E = (1 << 40)
+    fp8 = dict(fmt=3, m=(D, E), v=(D + (1 << 36), E + 16))
+    assert fused(L, **fp8) in (0, 7, 10)             # valid: stops at the device check
+    assert fused(L, fmt=3) == 1                      # no scale records
+    assert fused(L, **dict(fp8, m=(D, E + 4))) == 2  # record not 16-byte aligned
+    assert fused(L, **dict(fp8, d_in=264)) == 3      # 264 % 16 != 0
+    assert fused(L, **dict(fp8, v=(D + (1 << 36), E))) == 6   # both moments share one record
+    assert fused(L, **dict(fp8, X=E)) == 6           # X over a record
+    assert L.forge_wgrad_adamw_sr(A, B, C, F.ForgeMoment(D, E), F.ForgeMoment(D + (1 << 36), E + 16),
+                                  64, 256, 128, 1e-3, 0.9, 0.999, 1e-8, 0.01, 1, 3, 1, None) == 4
+    assert L.forge_fp8_roll_scales(None, 2, 1.0, None) == 1
+    assert L.forge_fp8_roll_scales(E + 4, 2, 1.0, None) == 2
+    assert L.forge_fp8_roll_scales(E, -1, 1.0, None) == 3
+    assert L.forge_fp8_roll_scales(E, 2, 0.5, None) == 5
+    assert L.forge_fp8_roll_scales(E, 2, float("inf"), None) == 5
+    assert L.forge_fp8_roll_scales(None, 0, 1.0, None) == 0   # nothing to roll
 
 
 def test_fused_valid_arguments_reach_the_device_check(L):

@@ -158,6 +158,68 @@ __global__ void __launch_bounds__(256) adamw_int8_kernel(const void* __restrict_
   }
 }
 
+// fp8 moments with per-tensor scales: one thread per 16 consecutive
+// elements, the same per-element arithmetic and encoding as the fused
+// kernel's fp8 epilogue; each warp raises the tensors' amax words once.
+template <int DW>
+__global__ void __launch_bounds__(256) adamw_fp8_kernel(const void* __restrict__ dW,
+                                                        uint16_t* __restrict__ W,
+                                                        uint8_t* __restrict__ mq,
+                                                        uint8_t* __restrict__ rq,
+                                                        float* __restrict__ m_words,
+                                                        float* __restrict__ r_words,
+                                                        int64_t n16, const AdamWConsts h) {
+  const Fp8Step fm = fp8_step_of(m_words), fr = fp8_step_of(r_words);
+  float amax_m = 0.0f, amax_r = 0.0f;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+       i += stride) {
+    float g[16], w[16], ga[8], gb[8];
+    load_grad8<DW>(dW, 2 * i, ga);
+    load_grad8<DW>(dW, 2 * i + 1, gb);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) { g[k] = ga[k]; g[8 + k] = gb[k]; }
+    uint4* wp = reinterpret_cast<uint4*>(W) + 2 * i;
+    const uint4 w0 = __ldcs(wp), w1 = __ldcs(wp + 1);
+    const uint32_t wu[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) { w[2 * k] = bf16_lo(wu[k]); w[2 * k + 1] = bf16_hi(wu[k]); }
+    uint4* mp = reinterpret_cast<uint4*>(mq) + i;
+    uint4* rp = reinterpret_cast<uint4*>(rq) + i;
+    uint4 mc = __ldcs(mp), rc = __ldcs(rp);
+    adamw_fp8_x16(g, w, mc, rc, fm, fr, h, amax_m, amax_r);
+    __stcs(mp, mc);
+    __stcs(rp, rc);
+    __stcs(wp, make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]),
+                          pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7])));
+    __stcs(wp + 1, make_uint4(pack_bf16x2(w[8], w[9]), pack_bf16x2(w[10], w[11]),
+                              pack_bf16x2(w[12], w[13]), pack_bf16x2(w[14], w[15])));
+  }
+  const int lane = threadIdx.x & 31;
+  warp_raise_amax(m_words + kFp8Amax, amax_m, lane);
+  warp_raise_amax(r_words + kFp8Amax, amax_r, lane);
+}
+
+// The scale roll between steps for n fp8 moment tensors (four words each,
+// `stride` floats apart): read <- write; write <- amax * headroom / 448
+// when amax > 0; amax <- 0.
+__global__ void fp8_roll_kernel(float* words, int n, int stride, float headroom) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float* w = words + static_cast<int64_t>(i) * stride;
+  const float amax = w[kFp8Amax];
+  const float write = w[kFp8WriteScale];
+  w[kFp8ReadScale] = write;
+  if (amax > 0.0f) w[kFp8WriteScale] = __fdiv_rn(__fmul_rn(amax, headroom), kE4m3Max);
+  w[kFp8Amax] = 0.0f;
+}
+
+cudaError_t launch_fp8_roll(float* words, int n, int stride, float headroom,
+                            cudaStream_t stream) {
+  fp8_roll_kernel<<<(n + 127) / 128, 128, 0, stream>>>(words, n, stride, headroom);
+  return cudaGetLastError();
+}
+
 template <int FMT, int DW>
 static cudaError_t launch_vec8(const void* dW, void* W, void* m, void* v, int64_t n, int grid,
                                const AdamWConsts& h, cudaStream_t stream) {
@@ -180,6 +242,20 @@ cudaError_t launch_adamw(const void* dW, int dw_fmt, void* W, void* m, void* v, 
                          const AdamWConsts& h, int num_sms, cudaStream_t stream) {
   const int64_t n = d_in * d_out;
   const int dw = dW == nullptr ? 2 : dw_fmt;
+  if (fmt == kFmtF8) {   // n is a multiple of 64 (d_in, d_out multiples of 8)
+    const int64_t n16 = n / 16;
+    const int64_t want = (n16 + 255) / 256;
+    const int grid = static_cast<int>(want < 8LL * num_sms ? (want > 0 ? want : 1) : 8LL * num_sms);
+    auto* Wp = static_cast<uint16_t*>(W);
+    auto* mp = static_cast<uint8_t*>(m);
+    auto* vp = static_cast<uint8_t*>(v);
+    switch (dw) {
+      case 0: adamw_fp8_kernel<0><<<grid, 256, 0, stream>>>(dW, Wp, mp, vp, m_scale, v_scale, n16, h); break;
+      case 1: adamw_fp8_kernel<1><<<grid, 256, 0, stream>>>(dW, Wp, mp, vp, m_scale, v_scale, n16, h); break;
+      default: adamw_fp8_kernel<2><<<grid, 256, 0, stream>>>(dW, Wp, mp, vp, m_scale, v_scale, n16, h); break;
+    }
+    return cudaGetLastError();
+  }
   if (fmt == kFmtI8) {
     const int64_t nb = n / 128;
     const int64_t want = (nb + 7) / 8;

@@ -28,6 +28,7 @@ namespace forge {
 cudaError_t launch_gemm_fused_f32(const GemmConfig&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_fused_bf16(const GemmConfig&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_fused_i8(const GemmConfig&, const GemmArgs&, cudaStream_t);
+cudaError_t launch_gemm_fused_f8(const GemmConfig&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_store_f32(const GemmConfig&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_store_bf16(const GemmConfig&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_dgrad(const GemmConfig&, const GemmArgs&, cudaStream_t);
@@ -42,6 +43,7 @@ cudaError_t launch_gemm(int mode, int fmt, const GemmConfig& cfg, const GemmArgs
       case kFmtF32: return launch_gemm_fused_f32(cfg, args, stream);
       case kFmtBF16: return launch_gemm_fused_bf16(cfg, args, stream);
       case kFmtI8: return launch_gemm_fused_i8(cfg, args, stream);
+      case kFmtF8: return launch_gemm_fused_f8(cfg, args, stream);
     }
   } else if (mode == kModeStoreG) {
     switch (fmt) {
@@ -213,6 +215,18 @@ int mom_elem_bytes(forge_moment_fmt f) {
   return f == FORGE_MOM_FP32 ? 4 : (f == FORGE_MOM_BF16 ? 2 : 1);
 }
 
+bool valid_fmt(forge_moment_fmt f) {
+  return f == FORGE_MOM_FP32 || f == FORGE_MOM_BF16 || f == FORGE_MOM_INT8_B128 ||
+         f == FORGE_MOM_FP8_E4M3;
+}
+
+// Bytes of one moment's scale storage: int8 one fp32 per row and 128-column
+// block; fp8 the four words of forge_fp8_scales.
+uint64_t scale_bytes(forge_moment_fmt f, uint64_t n) {
+  return f == FORGE_MOM_INT8_B128 ? n / 128 * 4
+                                  : (f == FORGE_MOM_FP8_E4M3 ? sizeof(forge_fp8_scales) : 0);
+}
+
 forge_status check_shape(int64_t bt, int64_t d_in, int64_t d_out) {
   const int64_t lim = (1LL << 31) - 1;
   if (bt < 0 || d_in <= 0 || d_out <= 0) return FORGE_ERR_SHAPE;
@@ -232,18 +246,18 @@ forge_status check_hyper(float lr, float b1, float b2, float eps, float wd, int6
 // Validation shared by the fused call and forge_adamw (state side).
 forge_status check_state(void* W, const forge_moment& m, const forge_moment& v, int64_t d_in,
                          int64_t d_out, forge_moment_fmt fmt) {
-  if (fmt != FORGE_MOM_FP32 && fmt != FORGE_MOM_BF16 && fmt != FORGE_MOM_INT8_B128)
-    return FORGE_ERR_FORMAT;
+  if (!valid_fmt(fmt)) return FORGE_ERR_FORMAT;
   if (!W || !m.data || !v.data) return FORGE_ERR_NULL;
-  if (fmt == FORGE_MOM_INT8_B128) {
+  if (fmt == FORGE_MOM_INT8_B128 || fmt == FORGE_MOM_FP8_E4M3) {
     if (!m.scale || !v.scale) return FORGE_ERR_NULL;
-    if (d_in % 128 != 0) return FORGE_ERR_SHAPE;
+    // int8: whole 128-column blocks; fp8: rows of codes 16-byte aligned (TMA strides)
+    if (d_in % (fmt == FORGE_MOM_INT8_B128 ? 128 : 16) != 0) return FORGE_ERR_SHAPE;
     if (!aligned16(m.scale) || !aligned16(v.scale)) return FORGE_ERR_ALIGN;
   }
   if (!aligned16(W) || !aligned16(m.data) || !aligned16(v.data)) return FORGE_ERR_ALIGN;
   const uint64_t n = static_cast<uint64_t>(d_in) * static_cast<uint64_t>(d_out);
   const uint64_t nm = n * mom_elem_bytes(fmt);
-  const uint64_t ns = (fmt == FORGE_MOM_INT8_B128) ? n / 128 * 4 : 0;
+  const uint64_t ns = scale_bytes(fmt, n);
   // the three (five) state tensors must be distinct
   if (overlaps(W, 2 * n, m.data, nm) || overlaps(W, 2 * n, v.data, nm) ||
       overlaps(m.data, nm, v.data, nm))
@@ -261,7 +275,7 @@ bool input_overlaps_state(const void* in, uint64_t nin, void* W, const forge_mom
                           forge_moment_fmt fmt) {
   const uint64_t n = static_cast<uint64_t>(d_in) * static_cast<uint64_t>(d_out);
   const uint64_t nm = n * mom_elem_bytes(fmt);
-  const uint64_t ns = (fmt == FORGE_MOM_INT8_B128) ? n / 128 * 4 : 0;
+  const uint64_t ns = scale_bytes(fmt, n);
   return overlaps(in, nin, W, 2 * n) || overlaps(in, nin, m.data, nm) ||
          overlaps(in, nin, v.data, nm) || (ns && overlaps(in, nin, m.scale, ns)) ||
          (ns && overlaps(in, nin, v.scale, ns));
@@ -373,6 +387,7 @@ GemmConfig finish_config(GemmConfig c, int64_t bt, int fmt, int mode);
 
 GemmConfig choose_config(int64_t bt, int fmt, int mode) {
   GemmConfig c;
+  // (fp8 moments move the bytes of int8 ones and take int8's choices)
   const int64_t one_cta_upto = (mode == kModeFused && fmt == kFmtBF16) ? 640 : 768;
   if (bt <= one_cta_upto) {
     c.cg = 1;
@@ -567,11 +582,12 @@ bool operand_maps(GemmMaps& maps, const void* X, const void* dY, int64_t bt, int
 }
 
 // State descriptors of one layer for the fused kernel: W (bf16) and the two
-// moments, boxes of one epilogue slice (32 columns, or 128 for int8) x 128 rows.
+// moments, boxes of one epilogue slice (32 columns, or 128 for 8-bit moments)
+// x the slot's rows.
 bool state_maps(GemmMaps& maps, void* W, const forge_moment& m, const forge_moment& v,
                 int64_t d_in, int64_t d_out, forge_moment_fmt fmt, int prof) {
-  if (fmt == FORGE_MOM_INT8_B128) {
-    const uint32_t rows = static_cast<uint32_t>(slot_rows(kModeFused, kFmtI8, prof));
+  if (fmt == FORGE_MOM_INT8_B128 || fmt == FORGE_MOM_FP8_E4M3) {   // 8-bit codes
+    const uint32_t rows = static_cast<uint32_t>(slot_rows(kModeFused, static_cast<int>(fmt), prof));
     return get_map(&maps.w, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_in, d_out, d_in * 2, 64, rows,
                    CU_TENSOR_MAP_SWIZZLE_128B) &&
            get_map(&maps.m, m.data, CU_TENSOR_MAP_DATA_TYPE_UINT8, d_in, d_out, d_in, 128, rows,
@@ -618,7 +634,7 @@ bool layers_clash(const forge_linear& a, const forge_linear& b, int64_t bt, forg
   if (same) return false;
   const uint64_t n = static_cast<uint64_t>(a.d_in) * static_cast<uint64_t>(a.d_out);
   const uint64_t nm = n * mom_elem_bytes(fmt);
-  const uint64_t ns = (fmt == FORGE_MOM_INT8_B128) ? n / 128 * 4 : 0;
+  const uint64_t ns = scale_bytes(fmt, n);
   return input_overlaps_state(a.W, 2 * n, b.W, b.m, b.v, b.d_in, b.d_out, fmt) ||
          input_overlaps_state(a.m.data, nm, b.W, b.m, b.v, b.d_in, b.d_out, fmt) ||
          input_overlaps_state(a.v.data, nm, b.W, b.m, b.v, b.d_in, b.d_out, fmt) ||
@@ -713,7 +729,8 @@ forge_status forge_wgrad_adamw_sr(const void* X, const void* dY, void* W, forge_
   L.d_out = d_out;
   forge_status s = check_linear(L, bt, fmt);
   if (s != FORGE_OK) return s;
-  if (fmt == FORGE_MOM_INT8_B128) return FORGE_ERR_FORMAT;   // fp32 or bf16 moments
+  if (fmt == FORGE_MOM_INT8_B128 || fmt == FORGE_MOM_FP8_E4M3)
+    return FORGE_ERR_FORMAT;   // fp32 or bf16 moments
   s = check_hyper(lr, beta1, beta2, eps, weight_decay, step);
   if (s != FORGE_OK) return s;
   if (step > INT32_MAX) return FORGE_ERR_HYPER;   // the step is a 32-bit Philox counter word
@@ -1078,7 +1095,7 @@ const char* forge_status_string(forge_status status) {
 int forge_describe_config(int64_t bt, int64_t d_in, int64_t d_out, forge_moment_fmt fmt, char* buf,
                           int len) {
   if (check_shape(bt, d_in, d_out) != FORGE_OK) return -1;
-  if (fmt != FORGE_MOM_FP32 && fmt != FORGE_MOM_BF16 && fmt != FORGE_MOM_INT8_B128) return -1;
+  if (!valid_fmt(fmt)) return -1;
   int sms = 152;
   int dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) {
@@ -1144,6 +1161,23 @@ void forge_set_wait_limit_ns(uint64_t ns) {
 void forge_debug_drop_first_arrival(int enable) {
   std::lock_guard<std::mutex> lk(g_mu);
   g_drop_first_arrival = enable ? 1 : 0;
+}
+
+forge_status forge_fp8_roll_scales(forge_fp8_scales* scales, int n, float headroom,
+                                   forge_stream stream) {
+  if (n < 0) return FORGE_ERR_SHAPE;
+  if (n == 0) return FORGE_OK;
+  if (!scales) return FORGE_ERR_NULL;
+  if (!aligned16(scales)) return FORGE_ERR_ALIGN;
+  if (!(headroom >= 1.0f) || !std::isfinite(headroom)) return FORGE_ERR_HYPER;
+  DeviceInfo* d = nullptr;
+  forge_status s = device_info(&d);
+  if (s != FORGE_OK) return s;
+  return launch_fp8_roll(reinterpret_cast<float*>(scales), n,
+                         static_cast<int>(sizeof(forge_fp8_scales) / sizeof(float)), headroom,
+                         static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FORGE_OK
+             : FORGE_ERR_LAUNCH;
 }
 
 void forge_set_tuning(const forge_tuning* t) {

@@ -69,6 +69,10 @@ struct GemmTraits {
       ((MODE == kModeStoreG || MODE == kModeAccum) && FMT == kFmtF32) ? 4 : 2;
   static constexpr int MOM_ELEM =
       !has_state(MODE) ? 0 : (FMT == kFmtF32 ? 4 : (FMT == kFmtBF16 ? 2 : 1));
+  // 8-bit moments (int8 blocks or fp8): 128-column slices whose W is two
+  // 64-column boxes
+  static constexpr bool Q8 = (MODE == kModeFused && (FMT == kFmtI8 || FMT == kFmtF8));
+  static constexpr bool F8 = (MODE == kModeFused && FMT == kFmtF8);
   static constexpr int W_BYTES = RPS * SW * W_ELEM;
   static constexpr int M_BYTES = RPS * SW * MOM_ELEM;
   static constexpr int SLOT_BYTES = W_BYTES + 2 * M_BYTES;
@@ -121,7 +125,8 @@ struct GemmTraits {
   static_assert(BN % SW == 0 && BNL % 64 == 0, "tile width");
   // the input-gradient mode loads A as K-major boxes 64 elements deep: one per stage
   static_assert(MODE != kModeDgrad || BK == 64, "K-major A boxes hold 64 elements of K");
-  static_assert(MODE != kModeOpt || FMT != kFmtI8, "the other optimizers keep fp32 or bf16 state");
+  static_assert(MODE != kModeOpt || (FMT != kFmtI8 && FMT != kFmtF8),
+                "the other optimizers keep fp32 or bf16 state");
   static_assert(MODE != kModeAccum || FMT == kFmtF32, "the accumulation buffer is fp32");
   static_assert(CG == 1 || (CG == 2 && BN == 256), "CTA pairs use 256 x 256 tiles");
   static_assert(TMEM_COLS <= 512, "tensor memory has 512 columns");
@@ -500,6 +505,57 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, uint32_t sadd
     *v_scale_rc = int8_scale(amax_r);
   }
   return true;
+}
+
+// fp8 moments with per-tensor scales; SW = 128, HALF = 64.  One pass: the
+// scales are the caller's (delayed scaling), so no block absmax is needed
+// before the codes are written.  The thread's running amaxes of m' and
+// r' = sqrt(v') are raised for the caller's next scales.
+template <int RPS>
+__device__ __forceinline__ void epi_slice_fused_f8(uint32_t taddr, bool zero_grad, uint8_t* slot,
+                                                   uint32_t row, int h, const AdamWConsts& hc,
+                                                   const Fp8Step& fm, const Fp8Step& fr,
+                                                   float& amax_m, float& amax_r) {
+  constexpr int kWBytes = RPS * 128 * 2;
+  constexpr int kMBytes = RPS * 128;
+  uint8_t* wbox = slot + h * (RPS * 64 * 2);   // box h: [RPS][64] bf16, 128-byte rows
+  uint8_t* mbox = slot + kWBytes;              // [RPS][128] e4m3
+  uint8_t* vbox = mbox + kMBytes;
+#pragma unroll 1
+  for (int c = 0; c < 2; ++c) {
+    uint32_t graw[32];
+    tmem_ld_x32(taddr + 32 * c, graw);
+    tmem_ld_wait();
+#pragma unroll
+    for (int p16 = 0; p16 < 2; ++p16) {
+      const int chunk = 4 * h + 2 * c + p16;     // 16 codes of m and of r
+      uint4 mq = *reinterpret_cast<const uint4*>(mbox + sw128_off(row, chunk));
+      uint4 rq = *reinterpret_cast<const uint4*>(vbox + sw128_off(row, chunk));
+      uint4 wq[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        wq[k] = *reinterpret_cast<const uint4*>(wbox + sw128_off(row, 4 * c + 2 * p16 + k));
+      const uint32_t* wu = reinterpret_cast<const uint32_t*>(wq);
+      float g[16], w[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        w[2 * i] = bf16_lo(wu[i]);
+        w[2 * i + 1] = bf16_hi(wu[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) g[i] = zero_grad ? 0.0f : __uint_as_float(graw[16 * p16 + i]);
+      adamw_fp8_x16(g, w, mq, rq, fm, fr, hc, amax_m, amax_r);
+      uint32_t wo[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) wo[i] = pack_bf16x2(w[2 * i], w[2 * i + 1]);
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        *reinterpret_cast<uint4*>(wbox + sw128_off(row, 4 * c + 2 * p16 + k)) =
+            make_uint4(wo[4 * k], wo[4 * k + 1], wo[4 * k + 2], wo[4 * k + 3]);
+      *reinterpret_cast<uint4*>(mbox + sw128_off(row, chunk)) = mq;
+      *reinterpret_cast<uint4*>(vbox + sw128_off(row, chunk)) = rq;
+    }
+  }
 }
 
 // Store-G: write the fp32 accumulator as fp32 or bf16.  SW = 32, HALF = 16.
@@ -892,7 +948,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           // kModeOpt loads only the states its optimizer has; kModeAccum only B
           const int nst = (MODE == kModeOpt) ? p.nstate : (MODE == kModeAccum ? 0 : 2);
           mbar_arrive_expect_tx(bar_sfull(j), T::W_BYTES + nst * T::M_BYTES);
-          if constexpr (FMT == kFmtI8) {
+          if constexpr (T::Q8) {
             tma_load_2d(slot, &maps.w, x0, y0, bar_sfull(j), pol);
             tma_load_2d(slot + T::RPS * 64 * 2, &maps.w, x0 + 64, y0, bar_sfull(j), pol);
           } else {
@@ -937,7 +993,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           const int y0 = tm * T::TM + static_cast<int>(rank) * kBM + (s % T::PARTS) * T::RPS;
           if (x0 < pr.d_in && y0 < pr.d_out) {
             const uint32_t sl = base + T::OFF_SLOTS + j * T::SLOT_BYTES;
-            if constexpr (T::I8) {
+            if constexpr (T::Q8) {
               tma_store_2d(&maps.w, x0, y0, sl);
               tma_store_2d(&maps.w, x0 + 64, y0, sl + T::RPS * 64 * 2);
             } else {
@@ -996,6 +1052,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       }
     };
     if constexpr (T::I8) load_scales(unit0, nx_m, nx_v);
+    // fp8: this thread's running amaxes of the current layer's new moments,
+    // raised into the layer's amax words whenever the layer changes (tiles
+    // of one layer are consecutive in the queue) and at the end
+    float am_m = 0.0f, am_r = 0.0f;
+    int am_layer = -1;
+    auto flush_amax = [&]() {
+      if constexpr (T::F8) {
+        if (am_layer >= 0) {
+          warp_raise_amax(p.prob[am_layer].m_scale + kFp8Amax, am_m, lane);
+          warp_raise_amax(p.prob[am_layer].v_scale + kFp8Amax, am_r, lane);
+        }
+        am_m = am_r = 0.0f;
+      }
+    };
     uint32_t scnt = 0, xcnt = 0;
     int it = 0;
     bool ok = true;
@@ -1004,6 +1074,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const int pi = tile_coords(tile_of(t), p, tm, tn);
       const GemmProblem& pr = p.prob[pi];
       const int scale_cols = pr.d_in / 128;
+      Fp8Step f8m, f8r;
+      if constexpr (T::F8) {
+        if (pi != am_layer) {
+          flush_amax();
+          am_layer = pi;
+        }
+        f8m = fp8_step_of(pr.m_scale);
+        f8r = fp8_step_of(pr.v_scale);
+      }
       if constexpr (T::I8) {
 #pragma unroll
         for (int cb = 0; cb < NCB; ++cb) {
@@ -1067,6 +1146,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               pr.m_scale + sidx, pr.v_scale + sidx, p.h);
           ++xcnt;
           if (!xok) { ok = false; break; }
+        } else if constexpr (T::F8) {
+          if (active)
+            epi_slice_fused_f8<T::RPS>(taddr, zero_grad, slot, srow, h, p.h, f8m, f8r, am_m, am_r);
         } else if (active) {
           if constexpr (MODE == kModeFused) {
             epi_slice_fused_16<FMT, T::RPS>(taddr, zero_grad, slot, srow, h, p.h, p.sr != 0,
@@ -1093,6 +1175,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         mbar_arrive(bar_sdone(j));
       }
     }
+    flush_amax();
   }
 
   // ---------------------------------------------------------------- teardown
@@ -1167,9 +1250,9 @@ cudaError_t launch_gemm_prof(const GemmConfig& cfg, const GemmArgs& args, cudaSt
   if (cfg.cg == 1 && cfg.bn == 128)
     return launch_gemm_t<MODE, FMT, 128, PROF, 1>(cfg, args, stream);
   // 256-wide accumulators use all 512 tensor-memory columns (two buffers).
-  // Not built for 1-CTA int8 moments, whose 64 KB state slots do not fit
+  // Not built for 1-CTA 8-bit moments, whose 64 KB state slots do not fit
   // twice next to the wider 1-CTA operand stages.
-  if constexpr (!(MODE == kModeFused && FMT == kFmtI8)) {
+  if constexpr (!(MODE == kModeFused && (FMT == kFmtI8 || FMT == kFmtF8))) {
     if (cfg.cg == 1 && cfg.bn == 256)
       return launch_gemm_t<MODE, FMT, 256, PROF, 1>(cfg, args, stream);
   }
@@ -1185,9 +1268,9 @@ cudaError_t launch_gemm_fmt(const GemmConfig& cfg, const GemmArgs& args, cudaStr
     case kProfMma: return launch_gemm_prof<MODE, FMT, kProfMma>(cfg, args, stream);
     case kProfBalanced: return launch_gemm_prof<MODE, FMT, kProfBalanced>(cfg, args, stream);
     case kProfDeep:
-      // int8 moments already use half-tile slots in the mma profile, and
+      // 8-bit moments already use half-tile slots in the mma profile, and
       // store-G has no state slots: both run the deep profile as mma
-      if constexpr (has_state(MODE) && FMT != kFmtI8)
+      if constexpr (has_state(MODE) && FMT != kFmtI8 && FMT != kFmtF8)
         return launch_gemm_prof<MODE, FMT, kProfDeep>(cfg, args, stream);
       else
         return launch_gemm_prof<MODE, FMT, kProfMma>(cfg, args, stream);

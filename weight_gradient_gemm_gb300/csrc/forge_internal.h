@@ -55,8 +55,8 @@ struct GemmProblem {
   int32_t d_in, d_out;
   int32_t tiles_m, tiles_n;
   int32_t tile_start;         // first index of this layer's tiles in the launch's queue
-  float* m_scale;             // int8 scales [d_out, d_in/128]
-  float* v_scale;
+  float* m_scale;             // int8: scales [d_out, d_in/128]; fp8: the moment's
+  float* v_scale;             // four words (read scale, write scale, amax)
 };
 
 struct GemmParams {
@@ -116,17 +116,19 @@ __host__ __device__ constexpr int bk_of(int cg) { return cg == 2 ? kBKPair : kBK
 // Box widths (columns per epilogue slice) by mode/format, used both to
 // encode the TMA descriptors and inside the kernels.
 __host__ __device__ constexpr int slice_cols(int mode, int fmt) {
-  return (mode == kModeFused && fmt == kFmtI8) ? 128 : 32;
+  return (mode == kModeFused && (fmt == kFmtI8 || fmt == kFmtF8)) ? 128 : 32;
 }
 
 // Rows of one state slot.  A whole 128-row tile, except in the deep profile
-// and for int8 moments outside the stream profile: there a slot holds half a
-// tile (64 rows; int8 32 KB instead of 64 KB, fp32 20 KB instead of 40 KB),
+// and for 8-bit moments (int8, fp8) outside the stream profile: there a slot
+// holds half a tile (64 rows; 8-bit 32 KB instead of 64 KB, fp32 20 KB
+// instead of 40 KB),
 // processed by the four epilogue warps of its two TMEM lane quadrants, which
 // leaves shared memory for more operand stages.
 __host__ __device__ constexpr int slot_rows(int mode, int fmt, int prof) {
   return (has_state(mode) &&
-          ((fmt == kFmtI8 && prof != kProfStream) || prof == kProfDeep)) ? 64 : 128;
+          (((fmt == kFmtI8 || fmt == kFmtF8) && prof != kProfStream) || prof == kProfDeep))
+             ? 64 : 128;
 }
 
 // Launchers (one per instantiated kernel family); return a CUDA error.
@@ -142,5 +144,9 @@ cudaError_t launch_dgrad_reduce(const float* part, int splits, int cg, int bn, i
 cudaError_t launch_adamw(const void* dW, int dw_fmt, void* W, void* m, void* v, float* m_scale,
                          float* v_scale, int64_t d_in, int64_t d_out, int fmt,
                          const AdamWConsts& h, int num_sms, cudaStream_t stream);
+
+// fp8 moments: the scale roll between steps (see forge_fp8_roll_scales).
+cudaError_t launch_fp8_roll(float* words, int n, int stride, float headroom,
+                            cudaStream_t stream);
 
 }  // namespace forge

@@ -8,6 +8,7 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace forge {
 
@@ -197,6 +198,90 @@ __device__ __forceinline__ float dequant_m(int code, float s) {
 __device__ __forceinline__ float dequant_v(int code, float s) {
   const float r = __fmul_rn(static_cast<float>(code), s);
   return __fmul_rn(r, r);
+}
+
+// ---------------------------------------------------------------------------
+// fp8 moments (e4m3, the OCP "fn" variant: bias 7, largest finite 448, no
+// infinities) with one scale per tensor and delayed scaling.  Per tensor the
+// caller keeps four fp32 words in device memory: the scale the stored codes
+// are read with, the scale the new codes are written with, and the amax of
+// the new moments (max |m'|, or max sqrt(v') for the second moment, whose
+// codes hold r = sqrt(v)), which a step raises and the caller resets.
+// ---------------------------------------------------------------------------
+constexpr int kFp8ReadScale = 0, kFp8WriteScale = 1, kFp8Amax = 2;
+constexpr float kE4m3Max = 448.0f;
+
+// Two e4m3 codes (low byte first) to two floats: exact (e4m3 -> f16 -> f32).
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t codes16) {
+  uint32_t h2;
+  const uint16_t c = static_cast<uint16_t>(codes16);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+  __half2 hh;
+  *reinterpret_cast<uint32_t*>(&hh) = h2;
+  return __half22float2(hh);
+}
+// Two floats to two e4m3 codes (lo in the low byte): round to nearest even,
+// saturating at +-448.
+__device__ __forceinline__ uint32_t float2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// The per-tensor constants of one fp8 moment for a step.
+struct Fp8Step {
+  float read;      // decode: value = e4m3(code) * read
+  float inv_write; // encode: code = e4m3(value * inv_write), 1 / write rounded to fp32
+};
+__device__ __forceinline__ Fp8Step fp8_step_of(const float* words) {
+  Fp8Step f;
+  f.read = __ldg(words + kFp8ReadScale);
+  f.inv_write = __frcp_rn(__ldg(words + kFp8WriteScale));
+  return f;
+}
+
+// 16 fp8 AdamW elements: codes of m and r = sqrt(v) (one uint4 each, 16
+// codes, element i in byte i), w and g as floats.  Updates w; returns the
+// new codes and raises the running amaxes.
+__device__ __forceinline__ void adamw_fp8_x16(const float (&g)[16], float (&w)[16], uint4& mq,
+                                              uint4& rq, const Fp8Step& fm, const Fp8Step& fr,
+                                              const AdamWConsts& h, float& amax_m, float& amax_r) {
+  uint32_t mw[4] = {mq.x, mq.y, mq.z, mq.w};
+  uint32_t rw[4] = {rq.x, rq.y, rq.z, rq.w};
+  uint32_t mo[4], ro[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t mpack = 0, rpack = 0;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const float2 m2 = e4m3x2_to_float2(mw[k] >> (16 * half));
+      const float2 r2 = e4m3x2_to_float2(rw[k] >> (16 * half));
+      const int i = 4 * k + 2 * half;
+      float m0 = __fmul_rn(m2.x, fm.read), m1 = __fmul_rn(m2.y, fm.read);
+      const float q0 = __fmul_rn(r2.x, fr.read), q1 = __fmul_rn(r2.y, fr.read);
+      float v0 = __fmul_rn(q0, q0), v1 = __fmul_rn(q1, q1);
+      float r0, r1;
+      adamw_elem(g[i], w[i], m0, v0, r0, h);
+      adamw_elem(g[i + 1], w[i + 1], m1, v1, r1, h);
+      amax_m = fmaxf(amax_m, fmaxf(fabsf(m0), fabsf(m1)));
+      amax_r = fmaxf(amax_r, fmaxf(r0, r1));
+      mpack |= float2_to_e4m3x2(__fmul_rn(m0, fm.inv_write), __fmul_rn(m1, fm.inv_write))
+               << (16 * half);
+      rpack |= float2_to_e4m3x2(__fmul_rn(r0, fr.inv_write), __fmul_rn(r1, fr.inv_write))
+               << (16 * half);
+    }
+    mo[k] = mpack;
+    ro[k] = rpack;
+  }
+  mq = make_uint4(mo[0], mo[1], mo[2], mo[3]);
+  rq = make_uint4(ro[0], ro[1], ro[2], ro[3]);
+}
+
+// Raise *word (an fp32 amax, >= 0) to at least the warp's largest x (>= 0):
+// non-negative floats order like their bit patterns.  Warp-collective.
+__device__ __forceinline__ void warp_raise_amax(float* word, float x, int lane) {
+  const unsigned u = __reduce_max_sync(0xffffffffu, __float_as_uint(x));
+  if (lane == 0 && u != 0u) atomicMax(reinterpret_cast<unsigned int*>(word), u);
 }
 
 }  // namespace forge

@@ -25,7 +25,7 @@ STATUS_NAMES = {
     8: "FORGE_ERR_LAUNCH", 9: "FORGE_ERR_DEVICE_TIMEOUT", 10: "FORGE_ERR_CUDA",
     11: "FORGE_ERR_DEVICE_CONFIG",
 }
-MOM_FP32, MOM_BF16, MOM_INT8_B128 = 0, 1, 2
+MOM_FP32, MOM_BF16, MOM_INT8_B128, MOM_FP8_E4M3 = 0, 1, 2, 3
 DT_FP32, DT_BF16 = 0, 1
 
 
@@ -123,6 +123,8 @@ def lib() -> ctypes.CDLL:
             L.forge_set_wait_limit_ns.restype = None
             L.forge_debug_drop_first_arrival.argtypes = [st]
             L.forge_debug_drop_first_arrival.restype = None
+            L.forge_fp8_roll_scales.argtypes = [vp, st, f32, vp]
+            L.forge_fp8_roll_scales.restype = st
             L.forge_set_tuning.argtypes = [ctypes.POINTER(ForgeTuning)]
             L.forge_set_tuning.restype = None
             L.forge_get_tuning.argtypes = [ctypes.POINTER(ForgeTuning)]
@@ -187,7 +189,7 @@ def _want(t: Optional[torch.Tensor], name: str, shape, dtypes) -> None:
 
 _BF16 = (torch.bfloat16,)
 _F32 = (torch.float32,)
-_MOM = (torch.float32, torch.bfloat16, torch.int8)
+_MOM = (torch.float32, torch.bfloat16, torch.int8, torch.float8_e4m3fn)
 
 
 def _operands(X: torch.Tensor, dY: torch.Tensor):
@@ -212,6 +214,11 @@ def _moments(m, v, m_scale, v_scale, d_out: int, d_in: int, dtypes=_MOM) -> int:
             raise ValueError("int8 moments need d_in % 128 == 0")
         _want(m_scale, "m_scale", (d_out, d_in // 128), _F32)
         _want(v_scale, "v_scale", (d_out, d_in // 128), _F32)
+    elif fmt == MOM_FP8_E4M3:
+        if d_in % 16:
+            raise ValueError("fp8 moments need d_in % 16 == 0")
+        _want(m_scale, "m_scale", (4,), _F32)     # forge_fp8_scales
+        _want(v_scale, "v_scale", (4,), _F32)
     return fmt
 
 
@@ -228,6 +235,8 @@ def moment_format(m: torch.Tensor) -> int:
         return MOM_BF16
     if m.dtype == torch.int8:
         return MOM_INT8_B128
+    if m.dtype == torch.float8_e4m3fn:
+        return MOM_FP8_E4M3
     raise ValueError(f"unsupported moment dtype {m.dtype}")
 
 
@@ -511,4 +520,33 @@ def alloc_moments(d_out: int, d_in: int, fmt: int, device="cuda"):
         q = lambda: torch.zeros((d_out, d_in), dtype=torch.int8, device=device)  # noqa: E731
         s = lambda: torch.zeros((d_out, d_in // 128), dtype=torch.float32, device=device)  # noqa: E731
         return q(), q(), s(), s()
+    if fmt == MOM_FP8_E4M3:
+        if d_in % 16:
+            raise ValueError("fp8 moments need d_in % 16 == 0")
+        q = lambda: torch.zeros((d_out, d_in), dtype=torch.float8_e4m3fn, device=device)  # noqa: E731
+        sc = alloc_fp8_scales(2, device=device)
+        return q(), q(), sc[0], sc[1]
     raise ValueError(f"unknown moment format {fmt}")
+
+
+def alloc_fp8_scales(n: int, read_scale: float = 1.0, write_scale: float = 1.0,
+                     device="cuda") -> torch.Tensor:
+    """n forge_fp8_scales records as one fp32 [n, 4] tensor (read scale,
+    write scale, amax, unused); row i is the `m_scale`/`v_scale` of one fp8
+    moment."""
+    t = torch.zeros((n, 4), dtype=torch.float32, device=device)
+    t[:, 0] = read_scale
+    t[:, 1] = write_scale
+    return t
+
+
+def fp8_roll_scales(scales: torch.Tensor, headroom: float = 1.0, stream=None) -> None:
+    """The scale roll between two steps of fp8 moments, on the device:
+    read <- write, write <- amax * headroom / 448 (kept when amax is 0),
+    amax <- 0, for every record of `scales` ([n, 4] or [4] fp32)."""
+    if scales.dtype != torch.float32 or scales.shape[-1] != 4 or scales.dim() > 2:
+        raise ValueError("scales must be fp32 [n, 4] or [4]")
+    _dense(scales, "scales")
+    n = 1 if scales.dim() == 1 else scales.shape[0]
+    _check(lib().forge_fp8_roll_scales(_ptr(scales), n, headroom, _stream(stream)),
+           "forge_fp8_roll_scales")

@@ -42,7 +42,8 @@
  * FORGE_CG=1|2 (one CTA or a CTA pair per tile), FORGE_BN=128|256
  * (accumulator width on one CTA), FORGE_GROUP_M=1..64 (tile rows per raster
  * group), FORGE_POLL_STORE=0|1 (the store lanes poll for finished state
- * slots), FORGE_SPLITS=1..8 (forge_dgrad: k-ranges per tile).  Every choice
+ * slots), FORGE_SPLITS=1..8 (forge_dgrad: k-ranges per tile),
+ * FORGE_L2_HINTS=0..3 (L2 eviction hints of the state stream).  Every choice
  * computes the same step to the same accuracy; only the speed differs.
  *
  * Errors.  Argument errors are returned synchronously, before anything is
@@ -439,6 +440,9 @@ typedef struct {
   int group_m;     /* 0 automatic; 1..64 tile rows per raster group             */
   int poll_store;  /* -1 automatic; 0 or 1: store lanes poll for finished slots */
   int splits;      /* 0 automatic; 1..8 k-ranges per tile for forge_dgrad       */
+  int l2_hints;    /* -1 automatic; 0..3: bit 0 marks the optimizer state's
+                      stores evict-first in L2, bit 1 its m, v loads whose rows
+                      are whole 128-byte lines                                  */
 } forge_tuning;
 
 /* Replace the tuning overrides (NULL: everything automatic).  Applies to

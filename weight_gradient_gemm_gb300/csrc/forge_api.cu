@@ -428,10 +428,10 @@ GemmConfig choose_opt_config(int64_t bt, int fmt) {
 // changes them.  Reading the environment on every call would cost host time
 // per launch and race with setenv in other threads.
 std::once_flag g_tune_once;
-forge_tuning g_tune = {FORGE_PROFILE_AUTO, 0, 0, 0, -1, 0};
+forge_tuning g_tune = {FORGE_PROFILE_AUTO, 0, 0, 0, -1, 0, -1};
 
 void tuning_from_env() {
-  forge_tuning t = {FORGE_PROFILE_AUTO, 0, 0, 0, -1, 0};
+  forge_tuning t = {FORGE_PROFILE_AUTO, 0, 0, 0, -1, 0, -1};
   if (const char* e = std::getenv("FORGE_PROFILE")) {
     if (std::strcmp(e, "stream") == 0) t.profile = FORGE_PROFILE_STREAM;
     if (std::strcmp(e, "mma") == 0) t.profile = FORGE_PROFILE_MMA;
@@ -443,6 +443,7 @@ void tuning_from_env() {
   if (const char* e = std::getenv("FORGE_GROUP_M")) t.group_m = std::atoi(e);
   if (const char* e = std::getenv("FORGE_POLL_STORE")) t.poll_store = std::atoi(e) != 0;
   if (const char* e = std::getenv("FORGE_SPLITS")) t.splits = std::atoi(e);
+  if (const char* e = std::getenv("FORGE_L2_HINTS")) t.l2_hints = std::atoi(e);
   std::lock_guard<std::mutex> lk(g_mu);
   g_tune = t;
 }
@@ -464,8 +465,12 @@ GemmConfig finish_config(GemmConfig c, int64_t bt, int fmt, int mode) {
   if (c.cg == 2) c.bn = 256;                    // pairs always use 256 x 256 tiles
   if (c.cg == 1 && (fmt == kFmtI8 || fmt == kFmtF8)) c.bn = 128;   // 1-CTA 8-bit moments: 128-wide tiles
   // Tile rows per raster group (the kernel's tile_coords): 4 for 128 x 128
-  // tiles, 1 (plain row-major order) for pairs, from the same sweeps.
-  c.group_m = (c.cg == 1) ? 4 : 1;
+  // tiles; 8 for the weight-gradient modes on pairs (a sweep of 1, 2, 4, 8,
+  // 16 and 32 over the layer at 2048-8192 tokens: 8 was fastest or tied, by
+  // 4.8 % at 8192 with bf16 moments and 2 % at 4096 with int8 against plain
+  // row-major order); 1 (row-major) for the input gradient, whose tile rows
+  // are tokens and where a column-wise walk measured slower at 4096-8192.
+  c.group_m = (c.cg == 1) ? 4 : (mode == kModeDgrad ? 1 : 8);
   // The store lanes poll for finished slots (instead of a suspending wait)
   // where the slot ring is short against the state stream: bf16 moments up
   // to 576 tokens on one CTA (+12 % at BT = 512), fp32 moments in the stream
@@ -477,6 +482,8 @@ GemmConfig finish_config(GemmConfig c, int64_t bt, int fmt, int mode) {
                   (c.cg == 2 && fmt == kFmtF32));
   if (tu.poll_store == 0 || tu.poll_store == 1) c.poll_store = tu.poll_store;
   if (tu.group_m >= 1 && tu.group_m <= 64) c.group_m = tu.group_m;
+  c.l2_hints = 0;
+  if (tu.l2_hints >= 0 && tu.l2_hints <= 3) c.l2_hints = tu.l2_hints;
   c.grid = 0;
   c.splits = 1;
   return c;
@@ -551,6 +558,7 @@ GemmParams base_params(int64_t bt, const GemmConfig& cfg, const DeviceInfo& d) {
   p.err_site = d.site_word;
   p.timeout_ns = g_wait_limit_ns;
   p.poll_store = cfg.poll_store;
+  p.l2_hints = cfg.l2_hints;
   p.splits = 1;
   return p;
 }
@@ -1182,7 +1190,7 @@ forge_status forge_fp8_roll_scales(forge_fp8_scales* scales, int n, float headro
 
 void forge_set_tuning(const forge_tuning* t) {
   std::call_once(g_tune_once, tuning_from_env);   // a later first read must not undo this
-  const forge_tuning automatic = {FORGE_PROFILE_AUTO, 0, 0, 0, -1, 0};
+  const forge_tuning automatic = {FORGE_PROFILE_AUTO, 0, 0, 0, -1, 0, -1};
   std::lock_guard<std::mutex> lk(g_mu);
   g_tune = t ? *t : automatic;
 }

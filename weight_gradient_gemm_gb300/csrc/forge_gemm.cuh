@@ -919,6 +919,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       // DRAM reads at BT = 512 with fp32 moments, 69 % with bf16 moments);
       // at normal priority the reads equal the state's size.
       const uint64_t pol = l2_policy_evict_normal();
+      const uint64_t pol_first = l2_policy_evict_first();
       uint32_t cnt = 0;
       int32_t last_armed[T::NS];
 #pragma unroll
@@ -954,9 +955,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           } else {
             tma_load_2d(slot, &maps.w, x0, y0, bar_sfull(j), pol);
           }
-          if (nst >= 1) tma_load_2d(slot + T::W_BYTES, &maps.m, x0, y0, bar_sfull(j), pol);
+          // m, v boxes whose rows are whole 128-byte lines may be marked
+          // evict-first (nothing reads them again in this launch)
+          const uint64_t mpol = (T::SW * T::MOM_ELEM >= 128 && (p.l2_hints & 2)) ? pol_first : pol;
+          if (nst >= 1) tma_load_2d(slot + T::W_BYTES, &maps.m, x0, y0, bar_sfull(j), mpol);
           if (nst >= 2)
-            tma_load_2d(slot + T::W_BYTES + T::M_BYTES, &maps.v, x0, y0, bar_sfull(j), pol);
+            tma_load_2d(slot + T::W_BYTES + T::M_BYTES, &maps.v, x0, y0, bar_sfull(j), mpol);
         }
       }
       // let the loads of each slot's latest phase land before the CTA can exit
@@ -975,6 +979,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // (a split input-gradient launch writes only fp32 partials: no slots)
     const bool split_launch = (MODE == kModeDgrad) && p.splits > 1;
     if (lane < T::NS && !split_launch) {
+      const bool hint_first = has_state(MODE) && (p.l2_hints & 1);
+      const uint64_t spol = l2_policy_evict_first();
       uint32_t cnt = 0;
       bool ok = true;
       for (int t = unit0; ok && t < p.num_units; t += units) {
@@ -993,18 +999,23 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           const int y0 = tm * T::TM + static_cast<int>(rank) * kBM + (s % T::PARTS) * T::RPS;
           if (x0 < pr.d_in && y0 < pr.d_out) {
             const uint32_t sl = base + T::OFF_SLOTS + j * T::SLOT_BYTES;
+            // optionally evict-first: nothing reads the new state again here
+            auto st2d = [&](const CUtensorMap* mp, int x, int y, uint32_t src) {
+              if (hint_first) tma_store_2d_hint(mp, x, y, src, spol);
+              else tma_store_2d(mp, x, y, src);
+            };
             if constexpr (T::Q8) {
-              tma_store_2d(&maps.w, x0, y0, sl);
-              tma_store_2d(&maps.w, x0 + 64, y0, sl + T::RPS * 64 * 2);
+              st2d(&maps.w, x0, y0, sl);
+              st2d(&maps.w, x0 + 64, y0, sl + T::RPS * 64 * 2);
             } else {
-              tma_store_2d(&maps.w, x0, y0, sl);
+              st2d(&maps.w, x0, y0, sl);
             }
             if constexpr (MODE == kModeFused) {
-              tma_store_2d(&maps.m, x0, y0, sl + T::W_BYTES);
-              tma_store_2d(&maps.v, x0, y0, sl + T::W_BYTES + T::M_BYTES);
+              st2d(&maps.m, x0, y0, sl + T::W_BYTES);
+              st2d(&maps.v, x0, y0, sl + T::W_BYTES + T::M_BYTES);
             } else if constexpr (MODE == kModeOpt) {
-              if (p.nstate >= 1) tma_store_2d(&maps.m, x0, y0, sl + T::W_BYTES);
-              if (p.nstate >= 2) tma_store_2d(&maps.v, x0, y0, sl + T::W_BYTES + T::M_BYTES);
+              if (p.nstate >= 1) st2d(&maps.m, x0, y0, sl + T::W_BYTES);
+              if (p.nstate >= 2) st2d(&maps.v, x0, y0, sl + T::W_BYTES + T::M_BYTES);
             }
             bulk_commit_group();
             bulk_wait_group_read<0>();

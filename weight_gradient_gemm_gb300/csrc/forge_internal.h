@@ -85,6 +85,10 @@ struct GemmParams {
   uint64_t timeout_ns;
   int32_t drop_first_arrival;  // testing aid, see forge_debug_drop_first_arrival
   int32_t poll_store;         // store lanes poll for finished slots (see choose_config)
+  // L2 hints of the state stream: bit 0, the stores of W, m, v are marked
+  // evict-first; bit 1, loads of m and v boxes with whole 128-byte rows (fp32,
+  // 8-bit codes) are marked evict-first
+  int32_t l2_hints;
 };
 
 struct GemmMaps {
@@ -107,6 +111,7 @@ struct GemmConfig {
   int group_m;
   int poll_store;  // store lanes poll the slot-done barrier instead of suspending
   int splits;      // input gradient: k-ranges per tile (GemmParams::splits); 1 elsewhere
+  int l2_hints;    // GemmParams::l2_hints
 };
 
 // Tokens per operand pipeline stage (the TMA box height of dY and X), used

@@ -64,7 +64,7 @@ PROFILES = {"auto": -1, "stream": 0, "mma": 1, "balanced": 2, "deep": 3}
 
 class ForgeTuning(ctypes.Structure):
     _fields_ = [(k, ctypes.c_int) for k in ("profile", "cta_group", "bn", "group_m",
-                                            "poll_store", "splits")]
+                                            "poll_store", "splits", "l2_hints")]
 
 
 _lock = threading.Lock()
@@ -473,18 +473,20 @@ def get_tuning() -> dict:
     lib().forge_get_tuning(ctypes.byref(t))
     names = {v: k for k, v in PROFILES.items()}
     return dict(profile=names.get(t.profile, "auto"), cg=t.cta_group, bn=t.bn,
-                group_m=t.group_m, poll_store=t.poll_store, splits=t.splits)
+                group_m=t.group_m, poll_store=t.poll_store, splits=t.splits,
+                l2_hints=t.l2_hints)
 
 
 def set_tuning(profile: str = "auto", cg: int = 0, bn: int = 0, group_m: int = 0,
-               poll_store: int = -1, splits: int = 0) -> None:
+               poll_store: int = -1, splits: int = 0, l2_hints: int = -1) -> None:
     """Replace the tuning overrides (the defaults leave every choice to the
     library).  profile: auto|stream|balanced|mma|deep; cg: 1 or 2 CTAs per
-    tile; bn: 128 or 256; group_m: 1..64; poll_store: 0 or 1; splits: 1..8."""
+    tile; bn: 128 or 256; group_m: 1..64; poll_store: 0 or 1; splits: 1..8;
+    l2_hints: 0..3."""
     if profile not in PROFILES:
         raise ValueError(f"unknown profile {profile}")
     t = ForgeTuning(PROFILES[profile], int(cg), int(bn), int(group_m), int(poll_store),
-                    int(splits))
+                    int(splits), int(l2_hints))
     lib().forge_set_tuning(ctypes.byref(t))
 
 

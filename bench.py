@@ -390,7 +390,14 @@ def run_gpu(args, rank, world, dev):
         torch.cuda.synchronize()
         return b0.elapsed_time(b1) / bw_steps
 
+    dg_items = [dict(dY=it["dy"], W=it["w"], dX=o) for it, o in zip(layer.items, dx)]
+    ws_bytes = F.dgrad_workspace_bytes(dg_items)
+    dws = torch.empty(max(1, ws_bytes // 4), dtype=torch.float32, device=dev) if ws_bytes else None
+
     def dgrad_all():
+        F.dgrad_grouped(dg_items, workspace=dws)
+
+    def dgrad_each():
         for it, o in zip(layer.items, dx):
             F.dgrad(it["dy"], it["w"], o)
 
@@ -398,64 +405,68 @@ def run_gpu(args, rank, world, dev):
         for it, o in zip(layer.items, dx):
             torch.matmul(it["dy"], it["w"], out=o)
 
+    bw_layers = [dict(g, dX=o) for g, o in zip(layer.group, dx)]
+
     def backward_all():
         nonlocal step
         step += 1
-        for it, o in zip(layer.items, dx):
-            F.linear_backward(it["x"], it["dy"], it["w"], o, it["m"], it["v"], step=step,
-                              m_scale=it["ms"], v_scale=it["vs"], **HYPER)
+        F.linear_backward_grouped(bw_layers, step=step, workspace=dws, **HYPER)
 
-    # ---- the other optimizers (diagnostic): forge_wgrad_opt per projection,
-    # states in the workload's format (fp32 for int8 workloads), zeroed first
+    # ---- the other optimizers (diagnostic): forge_wgrad_opt_grouped over the
+    # layer (one launch), states in the workload's format (fp32 for 8-bit
+    # workloads), zeroed first
     sfmt = fmt if fmt in (F.MOM_FP32, F.MOM_BF16) else F.MOM_FP32
     sdt = torch.float32 if sfmt == F.MOM_FP32 else torch.bfloat16
-    big = max(it["d_in"] * it["d_out"] for it in layer.items)
-    sbuf = [torch.zeros(big, dtype=sdt, device=dev) for _ in range(2)]
+    sbuf = [[torch.zeros((it["d_out"], it["d_in"]), dtype=sdt, device=dev) for _ in range(2)]
+            for it in layer.items]
     opt_ms = {}
     for opt in range(7):
-        for b in sbuf:
-            b.zero_()
+        for pair in sbuf:
+            for b in pair:
+                b.zero_()
         n_st = F.OPT_STATES[opt]
         ost = [0]
+        olayers = [dict(X=it["x"], dY=it["dy"], W=it["w"],
+                        s1=pair[0] if n_st >= 1 else None, s2=pair[1] if n_st >= 2 else None)
+                   for it, pair in zip(layer.items, sbuf)]
 
         def opt_step():
             ost[0] += 1
-            for it in layer.items:
-                sv = [sbuf[i][:it["d_in"] * it["d_out"]].view(it["d_out"], it["d_in"])
-                      if i < n_st else None for i in range(2)]
-                F.wgrad_opt(it["x"], it["dy"], it["w"], opt, sv[0], sv[1], step=ost[0],
-                            **OPT_HYPER[opt])
+            F.wgrad_opt_grouped(olayers, opt, step=ost[0], **OPT_HYPER[opt])
         opt_ms[opt] = per_step_ms(opt_step)
     assert F.device_error() == 0
+    del sbuf, olayers
 
-    # ---- the accumulate mode (diagnostic): forge_wgrad_accumulate per
-    # projection into an fp32 buffer, with beta = 1 (B read and written) and
+    # ---- the accumulate mode (diagnostic): forge_wgrad_accumulate_grouped
+    # over the layer into fp32 buffers, with beta = 1 (B read and written) and
     # beta = 0 (B written only)
-    bacc = torch.zeros(big, dtype=torch.float32, device=dev)
+    acc_items = [dict(X=it["x"], dY=it["dy"],
+                      B=torch.zeros((it["d_out"], it["d_in"]), dtype=torch.float32, device=dev))
+                 for it in layer.items]
 
     def accumulate_all(beta):
-        for it in layer.items:
-            F.wgrad_accumulate(it["x"], it["dy"],
-                               bacc[:it["d_in"] * it["d_out"]].view(it["d_out"], it["d_in"]), beta)
+        F.wgrad_accumulate_grouped(acc_items, beta)
     acc_ms = {b: per_step_ms(lambda b=b: accumulate_all(b)) for b in (1.0, 0.0)}
     assert F.device_error() == 0
-    del bacc
+    del acc_items
 
-    # ---- the stochastic-rounding store (diagnostic): the fused step per
-    # projection with W committed by stochastic rounding (fp32 and bf16 moments)
+    # ---- the stochastic-rounding store (diagnostic): the fused step over the
+    # layer in one launch with W committed by stochastic rounding (fp32 and
+    # bf16 moments)
     sr_ms = None
     if fmt in (F.MOM_FP32, F.MOM_BF16):
+        seeds = [1000 + k for k in range(len(layer.items))]
+
         def sr_all():
             nonlocal step
             step += 1
-            for k, it in enumerate(layer.items):
-                F.wgrad_adamw_sr(it["x"], it["dy"], it["w"], it["m"], it["v"], step=step,
-                                 seed=1000 + k, **HYPER)
+            F.wgrad_adamw_sr_grouped(layer.group, seeds, step=step, **HYPER)
         sr_ms = per_step_ms(sr_all)
         assert F.device_error() == 0
 
-    backward = dict(dgrad_ms=per_step_ms(dgrad_all), cublas_dgrad_ms=per_step_ms(cublas_dgrad_all),
-                    linear_backward_ms=per_step_ms(backward_all),
+    backward = dict(dgrad_ms=per_step_ms(dgrad_all), dgrad_each_ms=per_step_ms(dgrad_each),
+                    cublas_dgrad_ms=per_step_ms(cublas_dgrad_all),
+                    linear_backward_ms=per_step_ms(backward_all), workspace_bytes=ws_bytes,
                     dgrad_config=F.describe_dgrad_config(bt, 4096, 14336))
     assert F.device_error() == 0
 
@@ -995,7 +1006,7 @@ def optimizers_block(opt_ms, sfmt, layer, peaks):
     eb = 4 if sfmt == 0 else 2
     operands = layer.h2d_bytes()
     out = {"states": "fp32" if sfmt == 0 else "bf16",
-           "launch": "forge_wgrad_opt, one launch per projection", "peak_gbs": peaks["hbm_gbs"]}
+           "launch": "forge_wgrad_opt_grouped, one launch per layer", "peak_gbs": peaks["hbm_gbs"]}
     for opt, name in enumerate(names):
         nst = [0, 1, 1, 1, 1, 2, 2][opt]
         ms = opt_ms[opt]
@@ -1009,7 +1020,7 @@ def accumulate_block(acc_ms, layer, peaks):
     """The accumulate mode (diagnostic): B = beta B + dY^T X into fp32 for the
     seven projections, one launch each; bytes per parameter 8 with beta = 1
     (B read and written), 4 with beta = 0, plus the operands."""
-    out = {"launch": "forge_wgrad_accumulate, one launch per projection",
+    out = {"launch": "forge_wgrad_accumulate_grouped, one launch per layer",
            "peak_gbs": peaks["hbm_gbs"]}
     for beta, per in ((1.0, 8), (0.0, 4)):
         ms = acc_ms[beta]
@@ -1021,9 +1032,11 @@ def accumulate_block(acc_ms, layer, peaks):
 
 def backward_block(bw, flops, fused_ms, peaks, peak_kind):
     """The backward-step diagnostic: dX = dY W for the seven projections
-    (the same FLOPs as the weight gradient) against the bf16 tensor peak for
-    a kernel timed on its own (burst), next to cuBLAS on the same tensors, and
-    the whole forge_linear_backward step."""
+    (the same FLOPs as the weight gradient) in one forge_dgrad_grouped launch
+    against the bf16 tensor peak (burst), next to one forge_dgrad per
+    projection and cuBLAS on the same tensors, and the whole step as
+    forge_linear_backward_grouped (one grouped dX launch, then one grouped
+    fused launch)."""
     peak = peaks["bf16_tflops"]
     dgrad_tf = flops / (bw["dgrad_ms"] * 1e-3) / 1e12
     return {
@@ -1031,13 +1044,18 @@ def backward_block(bw, flops, fused_ms, peaks, peak_kind):
                   "roofline": {"bound": "tensor", "achieved": dgrad_tf, "peak": peak,
                                "unit": "TFLOP/s", "frac": dgrad_tf / peak,
                                "peak_kind": f"{peak_kind} (cuBLAS bf16, burst)"},
+                  "launch": "forge_dgrad_grouped: the seven projections in one launch",
+                  "per_projection_ms_per_step": bw.get("dgrad_each_ms"),
+                  "workspace_bytes": bw.get("workspace_bytes"),
                   "kernel_gate_up": bw["dgrad_config"],
                   "cublas_ms_per_step": bw["cublas_dgrad_ms"],
                   "vs_cublas": bw["cublas_dgrad_ms"] / bw["dgrad_ms"]},
         "ms_per_step": bw["linear_backward_ms"],
         "tflops": 2.0 * flops / (bw["linear_backward_ms"] * 1e-3) / 1e12,
         "fused_step_ms": fused_ms,
-        "path": "forge_linear_backward per projection: forge_dgrad then forge_wgrad_adamw",
+        "vs_fused_step": bw["linear_backward_ms"] / fused_ms,
+        "path": "forge_linear_backward_grouped: one grouped dX launch, then one grouped "
+                "fused launch",
     }
 
 
@@ -1167,8 +1185,9 @@ def main():
             "ms_per_step": res["sr_ms"],
             "round_to_nearest_ms_per_step": sum(res["per_proj_ms"]),
             "overhead": res["sr_ms"] / sum(res["per_proj_ms"]) - 1.0,
-            "launch": "forge_wgrad_adamw_sr, one launch per projection, against "
-                      "forge_wgrad_adamw per projection"},
+            "launch": "forge_wgrad_adamw_sr_grouped (one launch per layer), against "
+                      "forge_wgrad_adamw per projection",
+            "vs_grouped_round_to_nearest": res["sr_ms"] / ms},
         "gpu_launches": launches,
         "clocks": res["clocks"],
         "system": run_metadata(),

@@ -31,7 +31,9 @@
  * workspace for fp32 partial tiles from a stream-ordered pool the library
  * owns (one per device) and gives it back in stream order after the launch,
  * so calls on different streams never share one.  The pool keeps freed
- * memory for later calls.
+ * memory for later calls.  The grouped input-gradient calls
+ * (forge_dgrad_grouped, forge_linear_backward_grouped) take that workspace
+ * from the caller instead and allocate nothing.
  *
  * Tuning.  The tile configuration is chosen from the token count and the
  * moment format (forge_describe_config shows it).  forge_set_tuning
@@ -62,6 +64,7 @@
 #ifndef FORGE_H_
 #define FORGE_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -267,6 +270,28 @@ forge_status forge_wgrad_opt(const void* X, const void* dY, void* W, forge_momen
                              forge_moment_fmt fmt, forge_stream stream);
 
 /*
+ * forge_wgrad_opt_grouped: forge_wgrad_opt on n (1..FORGE_MAX_GROUP) linear
+ * layers with one token count, optimizer, hyperparameters, step and state
+ * format, in one launch (one tile queue over all layers, largest first).
+ * Each layer's m and v fields are its s1 and s2 (scale fields unused).
+ * Results are those of n separate calls, bit for bit.  Errors as
+ * forge_wgrad_opt, plus those of forge_wgrad_adamw_grouped's layer checks.
+ */
+forge_status forge_wgrad_opt_grouped(const forge_linear* layers, int n, int64_t bt,
+                                     forge_optimizer opt, const forge_opt_hyper* hyper,
+                                     int64_t step, forge_moment_fmt fmt, forge_stream stream);
+
+/*
+ * forge_wgrad_adamw_sr_grouped: forge_wgrad_adamw_sr on n layers in one
+ * launch; layer i draws its random bits with key (seeds[i], 0).  Results are
+ * those of n separate calls with those seeds, bit for bit.
+ */
+forge_status forge_wgrad_adamw_sr_grouped(const forge_linear* layers, const uint64_t* seeds,
+                                          int n, int64_t bt, float lr, float beta1, float beta2,
+                                          float eps, float weight_decay, int64_t step,
+                                          forge_moment_fmt fmt, forge_stream stream);
+
+/*
  * forge_wgrad_accumulate: B = beta * B + dY^T X into an fp32 buffer, the
  * gradient accumulated on chip and added to B in the epilogue, rounded once
  * per call.  The FORGE page uses it twice: Muon's momentum B <- mu B + G
@@ -284,6 +309,20 @@ forge_status forge_wgrad_opt(const void* X, const void* dY, void* W, forge_momen
 forge_status forge_wgrad_accumulate(const void* X, const void* dY, float* B, float beta,
                                     int64_t bt, int64_t d_in, int64_t d_out,
                                     forge_stream stream);
+
+/* One linear layer of forge_wgrad_accumulate_grouped; fields as the
+ * same-named arguments of forge_wgrad_accumulate. */
+typedef struct {
+  const void* X;   /* [bt, d_in] bf16, read only (may be shared)     */
+  const void* dY;  /* [bt, d_out] bf16, read only                    */
+  float* B;        /* [d_out, d_in] fp32, updated in place           */
+  int64_t d_in, d_out;
+} forge_accum_item;
+
+/* forge_wgrad_accumulate on n (1..FORGE_MAX_GROUP) layers with one token
+ * count and beta, in one launch; no B may overlap an input or another B. */
+forge_status forge_wgrad_accumulate_grouped(const forge_accum_item* items, int n, int64_t bt,
+                                            float beta, forge_stream stream);
 
 /*
  * forge_wgrad: the unfused gradient, dW = dY^T X stored to global memory
@@ -312,6 +351,34 @@ forge_status forge_wgrad(const void* X, const void* dY, void* dW, forge_dtype dw
  */
 forge_status forge_dgrad(const void* dY, const void* W, void* dX,
                          int64_t bt, int64_t d_in, int64_t d_out, forge_stream stream);
+
+/* One projection of a grouped input-gradient call. */
+typedef struct {
+  const void* dY;  /* [bt, d_out] bf16, read only                   */
+  const void* W;   /* [d_out, d_in] bf16, read only                 */
+  void* dX;        /* [bt, d_in] bf16, written                       */
+  int64_t d_in, d_out;
+} forge_dgrad_item;
+
+/*
+ * forge_dgrad_grouped: forge_dgrad for n (1..FORGE_MAX_GROUP) projections
+ * with one token count in one launch: one tile queue over all of them, the
+ * projections with the most work first (their reductions over d_out differ
+ * in length).  When the launch splits the reductions (few tiles), the fp32
+ * partials go to the caller's `workspace` (device, 16-byte aligned,
+ * `workspace_bytes` long; forge_dgrad_workspace_bytes gives the size the
+ * library's choice needs); with less, or NULL, it splits less or not at all
+ * (same accuracy).  Nothing is allocated.  With the same split count each
+ * dX is bit for bit that of forge_dgrad.  The workspace must not be used by
+ * another call until this one has run.  Errors as forge_dgrad; no dX may
+ * overlap any projection's dY, W or another dX (FORGE_ERR_ALIAS).
+ */
+forge_status forge_dgrad_grouped(const forge_dgrad_item* items, int n, int64_t bt,
+                                 void* workspace, size_t workspace_bytes, forge_stream stream);
+
+/* Bytes of workspace forge_dgrad_grouped wants for these projections (0 if
+ * it would not split, or for invalid arguments). */
+size_t forge_dgrad_workspace_bytes(const forge_dgrad_item* items, int n, int64_t bt);
 
 /*
  * forge_dgrad_noalloc: forge_dgrad that allocates nothing, for callers that
@@ -353,6 +420,21 @@ forge_status forge_linear_backward(const void* X, const void* dY, void* W, void*
                                    float lr, float beta1, float beta2, float eps,
                                    float weight_decay, int64_t step,
                                    forge_moment_fmt fmt, forge_stream stream);
+
+/*
+ * forge_linear_backward_grouped: forge_linear_backward for n layers with one
+ * token count: one grouped input-gradient launch (dX[i] = dY_i W_i from the
+ * weights before the update; split partials in the caller's workspace, as
+ * forge_dgrad_grouped), then forge_wgrad_adamw_grouped, both on `stream`.
+ * dX[i] [bt, d_in_i] bf16 must not overlap any layer's X, dY, W, m, v,
+ * scales or another dX.  Every argument of both halves is checked before
+ * anything is enqueued.  Nothing is allocated.
+ */
+forge_status forge_linear_backward_grouped(const forge_linear* layers, void* const* dX, int n,
+                                           int64_t bt, float lr, float beta1, float beta2,
+                                           float eps, float weight_decay, int64_t step,
+                                           forge_moment_fmt fmt, void* workspace,
+                                           size_t workspace_bytes, forge_stream stream);
 
 /*
  * forge_adamw: the unfused optimizer step on a stored gradient dW (fp32 or

@@ -349,3 +349,36 @@ def test_tuning_round_trip_without_gpu(L, tune):
                                   splits=0, l2_hints=-1)
     with pytest.raises(ValueError):
         F.set_tuning(profile="fast")
+
+
+def test_grouped_calls_argument_errors(L):
+    # codes: 1 NULL, 2 ALIGN, 3 SHAPE, 4 FORMAT, 5 HYPER, 6 ALIAS
+    lin = F.ForgeLinear(A, B, C, F.ForgeMoment(D, None), F.ForgeMoment(D + (1 << 36), None),
+                        256, 128)
+    arr = (F.ForgeLinear * 2)(lin, lin)
+    h = F.ForgeOptHyper(1e-3, 0.0, 0.9, 0.999, 1e-8, 0.9, 0.99, 4e-3)
+    assert L.forge_wgrad_opt_grouped(None, 1, 64, 1, ctypes.byref(h), 1, 0, None) == 1
+    assert L.forge_wgrad_opt_grouped(arr, 0, 64, 1, ctypes.byref(h), 1, 0, None) == 3
+    assert L.forge_wgrad_opt_grouped(arr, 1, 64, 1, ctypes.byref(h), 0, 0, None) == 5
+    assert L.forge_wgrad_opt_grouped(arr, 1, 64, 1, ctypes.byref(h), 1, 2, None) == 4
+    assert L.forge_wgrad_opt_grouped(arr, 2, 64, 1, ctypes.byref(h), 1, 0, None) == 6  # same W twice
+    seeds = (ctypes.c_uint64 * 2)(1, 2)
+    assert L.forge_wgrad_adamw_sr_grouped(arr, None, 1, 64, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 0,
+                                          None) == 1
+    assert L.forge_wgrad_adamw_sr_grouped(arr, seeds, 2, 64, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 0,
+                                          None) == 6
+    acc = (F.ForgeAccumItem * 2)(F.ForgeAccumItem(A, B, C, 256, 128),
+                                 F.ForgeAccumItem(A, B, C + 64, 256, 128))
+    assert L.forge_wgrad_accumulate_grouped(acc, 2, 64, 1.0, None) == 6    # B's overlap
+    assert L.forge_wgrad_accumulate_grouped(acc, 1, 64, float("inf"), None) == 5
+    dg = (F.ForgeDgradItem * 2)(F.ForgeDgradItem(B, C, A, 256, 128),
+                                F.ForgeDgradItem(B, C, A, 256, 128))
+    assert L.forge_dgrad_grouped(dg, 2, 64, None, 0, None) == 6             # same dX twice
+    assert L.forge_dgrad_grouped(dg, 9, 64, None, 0, None) == 3
+    assert L.forge_dgrad_grouped(dg, 1, 64, A + 4, 1024, None) == 2        # workspace alignment
+    assert L.forge_dgrad_workspace_bytes(dg, 1, 0) == 0
+    dx = (ctypes.c_void_p * 2)(A, A)
+    assert L.forge_linear_backward_grouped(arr, None, 1, 64, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 0,
+                                           None, 0, None) == 1
+    assert L.forge_linear_backward_grouped(arr, dx, 1, 64, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 0,
+                                           None, 0, None) == 6             # dX over X

@@ -572,6 +572,8 @@ void add_problem(GemmParams& p, const GemmConfig& cfg, int64_t d_in, int64_t d_o
   q.tiles_m = static_cast<int32_t>((d_out + kBM * cfg.cg - 1) / (kBM * cfg.cg));
   q.tiles_n = static_cast<int32_t>((d_in + cfg.bn - 1) / cfg.bn);
   q.tile_start = p.num_tiles;
+  q.num_k = p.num_k;
+  q.part_tile0 = p.num_tiles;
   q.m_scale = m_scale;
   q.v_scale = v_scale;
   p.num_tiles += q.tiles_m * q.tiles_n;
@@ -619,6 +621,19 @@ bool state_maps(GemmMaps& maps, void* W, const forge_moment& m, const forge_mome
 uint64_t state_bytes_of(const forge_linear& L, forge_moment_fmt fmt) {
   const uint64_t n = static_cast<uint64_t>(L.d_in) * static_cast<uint64_t>(L.d_out);
   return n * (2 + 2 * mom_elem_bytes(fmt));
+}
+
+// The launch order of a group's layers: largest first, so the small ones
+// fill the last wave (a stable insertion sort on the state bytes).
+void largest_first(const forge_linear* layers, int n, forge_moment_fmt fmt, int* order) {
+  for (int i = 0; i < n; ++i) order[i] = i;
+  for (int i = 1; i < n; ++i)
+    for (int j = i; j > 0 && state_bytes_of(layers[order[j]], fmt) >
+                                 state_bytes_of(layers[order[j - 1]], fmt); --j) {
+      const int t = order[j];
+      order[j] = order[j - 1];
+      order[j - 1] = t;
+    }
 }
 
 // Checks one layer of a fused launch (everything but cross-layer aliasing).
@@ -694,16 +709,8 @@ forge_status forge_wgrad_adamw_grouped(const forge_linear* layers, int n, int64_
     return FORGE_OK;
   }
   GemmConfig cfg = choose_config(bt, ifmt, kModeFused);
-  // largest layers first, so the small ones fill the last wave
   int order[FORGE_MAX_GROUP];
-  for (int i = 0; i < n; ++i) order[i] = i;
-  for (int i = 1; i < n; ++i)
-    for (int j = i; j > 0 && state_bytes_of(layers[order[j]], fmt) >
-                                 state_bytes_of(layers[order[j - 1]], fmt); --j) {
-      const int t = order[j];
-      order[j] = order[j - 1];
-      order[j - 1] = t;
-    }
+  largest_first(layers, n, fmt, order);
   GemmArgs args;
   std::memset(&args, 0, sizeof(args));
   args.p = base_params(bt, cfg, *d);
@@ -715,6 +722,55 @@ forge_status forge_wgrad_adamw_grouped(const forge_linear* layers, int n, int64_
         !state_maps(maps, L.W, L.m, L.v, L.d_in, L.d_out, fmt, cfg.prof))
       return FORGE_ERR_LAUNCH;
     add_problem(args.p, cfg, L.d_in, L.d_out, L.m.scale, L.v.scale);
+  }
+  set_grid(cfg, args.p.num_units, d->num_sms);
+  args.p.drop_first_arrival = take_drop_flag();
+  return launch_gemm(kModeFused, ifmt, cfg, args, st) == cudaSuccess ? FORGE_OK
+                                                                      : FORGE_ERR_LAUNCH;
+}
+
+forge_status forge_wgrad_adamw_sr_grouped(const forge_linear* layers, const uint64_t* seeds,
+                                          int n, int64_t bt, float lr, float beta1, float beta2,
+                                          float eps, float weight_decay, int64_t step,
+                                          forge_moment_fmt fmt, forge_stream stream) {
+  if (!layers || !seeds) return FORGE_ERR_NULL;
+  if (n < 1 || n > FORGE_MAX_GROUP) return FORGE_ERR_SHAPE;
+  for (int i = 0; i < n; ++i) {
+    forge_status s = check_linear(layers[i], bt, fmt);
+    if (s != FORGE_OK) return s;
+  }
+  if (fmt == FORGE_MOM_INT8_B128 || fmt == FORGE_MOM_FP8_E4M3)
+    return FORGE_ERR_FORMAT;   // fp32 or bf16 moments
+  forge_status s = check_hyper(lr, beta1, beta2, eps, weight_decay, step);
+  if (s != FORGE_OK) return s;
+  if (step > INT32_MAX) return FORGE_ERR_HYPER;   // the step is a 32-bit Philox counter word
+  for (int i = 0; i < n; ++i)
+    for (int j = 0; j < n; ++j)
+      if (layers_clash(layers[i], layers[j], bt, fmt, i == j)) return FORGE_ERR_ALIAS;
+  DeviceInfo* d = nullptr;
+  s = device_info(&d);
+  if (s != FORGE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int ifmt = static_cast<int>(fmt);
+  // the tensor-core kernel even without tokens (G = 0): the separate
+  // optimizer kernel rounds W to nearest
+  GemmConfig cfg = choose_config(bt, ifmt, kModeFused);
+  int order[FORGE_MAX_GROUP];
+  largest_first(layers, n, fmt, order);
+  GemmArgs args;
+  std::memset(&args, 0, sizeof(args));
+  args.p = base_params(bt, cfg, *d);
+  args.p.h = make_consts(lr, beta1, beta2, eps, weight_decay, step);
+  args.p.sr = 1;
+  args.p.sr_step = static_cast<int32_t>(step);
+  for (int k = 0; k < n; ++k) {
+    const forge_linear& L = layers[order[k]];
+    GemmMaps& maps = args.maps[k];
+    if ((bt > 0 && !operand_maps(maps, L.X, L.dY, bt, L.d_in, L.d_out, bk_of(cfg.cg))) ||
+        !state_maps(maps, L.W, L.m, L.v, L.d_in, L.d_out, fmt, cfg.prof))
+      return FORGE_ERR_LAUNCH;
+    add_problem(args.p, cfg, L.d_in, L.d_out, L.m.scale, L.v.scale);
+    args.p.prob[k].sr_seed = seeds[order[k]];
   }
   set_grid(cfg, args.p.num_units, d->num_sms);
   args.p.drop_first_arrival = take_drop_flag();
@@ -735,38 +791,8 @@ forge_status forge_wgrad_adamw_sr(const void* X, const void* dY, void* W, forge_
   L.v = v;
   L.d_in = d_in;
   L.d_out = d_out;
-  forge_status s = check_linear(L, bt, fmt);
-  if (s != FORGE_OK) return s;
-  if (fmt == FORGE_MOM_INT8_B128 || fmt == FORGE_MOM_FP8_E4M3)
-    return FORGE_ERR_FORMAT;   // fp32 or bf16 moments
-  s = check_hyper(lr, beta1, beta2, eps, weight_decay, step);
-  if (s != FORGE_OK) return s;
-  if (step > INT32_MAX) return FORGE_ERR_HYPER;   // the step is a 32-bit Philox counter word
-  if (layers_clash(L, L, bt, fmt, true)) return FORGE_ERR_ALIAS;
-  DeviceInfo* d = nullptr;
-  s = device_info(&d);
-  if (s != FORGE_OK) return s;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int ifmt = static_cast<int>(fmt);
-  // the tensor-core kernel even without tokens (G = 0): the separate
-  // optimizer kernel rounds W to nearest
-  GemmConfig cfg = choose_config(bt, ifmt, kModeFused);
-  GemmArgs args;
-  std::memset(&args, 0, sizeof(args));
-  GemmMaps& maps = args.maps[0];
-  if ((bt > 0 && !operand_maps(maps, X, dY, bt, d_in, d_out, bk_of(cfg.cg))) ||
-      !state_maps(maps, W, m, v, d_in, d_out, fmt, cfg.prof))
-    return FORGE_ERR_LAUNCH;
-  args.p = base_params(bt, cfg, *d);
-  args.p.h = make_consts(lr, beta1, beta2, eps, weight_decay, step);
-  args.p.sr = 1;
-  args.p.sr_step = static_cast<int32_t>(step);
-  args.p.sr_seed = seed;
-  add_problem(args.p, cfg, d_in, d_out, m.scale, v.scale);
-  set_grid(cfg, args.p.num_units, d->num_sms);
-  args.p.drop_first_arrival = take_drop_flag();
-  return launch_gemm(kModeFused, ifmt, cfg, args, st) == cudaSuccess ? FORGE_OK
-                                                                      : FORGE_ERR_LAUNCH;
+  return forge_wgrad_adamw_sr_grouped(&L, &seed, 1, bt, lr, beta1, beta2, eps, weight_decay,
+                                      step, fmt, stream);
 }
 
 forge_status forge_wgrad_adamw(const void* X, const void* dY, void* W, forge_moment m,
@@ -827,73 +853,169 @@ forge_status forge_wgrad(const void* X, const void* dY, void* dW, forge_dtype dw
 
 namespace {
 
-// forge_dgrad and forge_dgrad_noalloc: identical but for where a split
-// launch keeps its fp32 partials (the pool, or the static scratch).
-forge_status dgrad_run(const void* dY, const void* W, void* dX, int64_t bt, int64_t d_in,
-                       int64_t d_out, forge_stream stream, bool no_alloc) {
-  forge_status s = check_shape(bt, d_in, d_out);
+// Where a split input-gradient launch keeps its fp32 partials: the library's
+// stream-ordered pool (forge_dgrad), its static scratch (forge_dgrad_noalloc),
+// or the caller's workspace (the grouped calls; none means unsplit).
+enum WsMode { kWsPool, kWsStatic, kWsCaller };
+
+// The k-steps of one projection's reduction over d_out.
+int64_t dgrad_num_k(const forge_dgrad_item& it, const GemmConfig& c) {
+  return (it.d_out + bk_of(c.cg) - 1) / bk_of(c.cg);
+}
+
+// Checks the projections of an input-gradient call: shapes, pointers, and
+// that no dX overlaps any projection's dY, W or another dX.
+forge_status check_dgrad_items(const forge_dgrad_item* items, int n, int64_t bt) {
+  if (!items) return FORGE_ERR_NULL;
+  if (n < 1 || n > FORGE_MAX_GROUP) return FORGE_ERR_SHAPE;
+  for (int i = 0; i < n; ++i) {
+    const forge_dgrad_item& a = items[i];
+    forge_status s = check_shape(bt, a.d_in, a.d_out);
+    if (s != FORGE_OK) return s;
+    if (bt == 0) continue;
+    if (!a.dY || !a.W || !a.dX) return FORGE_ERR_NULL;
+    if (!aligned16(a.dY) || !aligned16(a.W) || !aligned16(a.dX)) return FORGE_ERR_ALIGN;
+  }
+  if (bt == 0) return FORGE_OK;
+  for (int i = 0; i < n; ++i) {
+    const uint64_t ndx = 2ull * bt * items[i].d_in;
+    for (int j = 0; j < n; ++j) {
+      const forge_dgrad_item& b = items[j];
+      if (overlaps(items[i].dX, ndx, b.dY, 2ull * bt * b.d_out) ||
+          overlaps(items[i].dX, ndx, b.W, 2ull * b.d_in * b.d_out) ||
+          (j != i && overlaps(items[i].dX, ndx, b.dX, 2ull * bt * b.d_in)))
+        return FORGE_ERR_ALIAS;
+    }
+  }
+  return FORGE_OK;
+}
+
+// The launch configuration, the order of the projections in the tile queue
+// (most work first, so the short reductions fill the last wave) and the split
+// count the library would choose, before any workspace limit.
+struct DgradPlan {
+  GemmConfig cfg;
+  int order[FORGE_MAX_GROUP];
+  int64_t tiles;
+  size_t ctile_bytes;
+};
+DgradPlan plan_dgrad(const forge_dgrad_item* items, int n, int64_t bt, int num_sms) {
+  DgradPlan pl;
+  int64_t max_din = 0, max_dout = 0;
+  for (int i = 0; i < n; ++i) {
+    max_din = std::max<int64_t>(max_din, items[i].d_in);
+    max_dout = std::max<int64_t>(max_dout, items[i].d_out);
+  }
+  pl.cfg = choose_dgrad_config(bt, max_din, max_dout, num_sms);
+  const GemmConfig& c = pl.cfg;
+  auto tiles_of_item = [&](const forge_dgrad_item& it) {
+    return ((bt + kBM * c.cg - 1) / (kBM * c.cg)) * ((it.d_in + c.bn - 1) / c.bn);
+  };
+  pl.tiles = 0;
+  int64_t max_k = 0, min_k = INT64_MAX;
+  for (int i = 0; i < n; ++i) {
+    pl.tiles += tiles_of_item(items[i]);
+    max_k = std::max(max_k, dgrad_num_k(items[i], c));
+    min_k = std::min(min_k, dgrad_num_k(items[i], c));
+    pl.order[i] = i;
+  }
+  for (int i = 1; i < n; ++i)
+    for (int j = i; j > 0; --j) {
+      const forge_dgrad_item &a = items[pl.order[j]], &b = items[pl.order[j - 1]];
+      if (tiles_of_item(a) * dgrad_num_k(a, c) <= tiles_of_item(b) * dgrad_num_k(b, c)) break;
+      std::swap(pl.order[j], pl.order[j - 1]);
+    }
+  pl.ctile_bytes = static_cast<size_t>(c.cg) * kBM * c.bn * sizeof(float);
+  // one split count for the launch: from the longest reduction, never more
+  // k-ranges than the shortest one has k-steps
+  pl.cfg.splits = static_cast<int>(std::min<int64_t>(
+      choose_splits(pl.tiles, max_k, num_sms / c.cg, static_cast<int64_t>(pl.ctile_bytes)),
+      min_k));
+  return pl;
+}
+
+forge_status dgrad_run(const forge_dgrad_item* items, int n, int64_t bt, WsMode mode, void* cws,
+                       size_t cws_bytes, forge_stream stream) {
+  forge_status s = check_dgrad_items(items, n, bt);
   if (s != FORGE_OK) return s;
-  if (bt == 0) return FORGE_OK;   // no tokens: dX is empty
-  if (!dY || !W || !dX) return FORGE_ERR_NULL;
-  if (!aligned16(dY) || !aligned16(W) || !aligned16(dX)) return FORGE_ERR_ALIGN;
-  const uint64_t ndx = 2ull * bt * d_in;
-  if (overlaps(dX, ndx, dY, 2ull * bt * d_out) ||
-      overlaps(dX, ndx, W, 2ull * d_in * d_out))
-    return FORGE_ERR_ALIAS;
+  if (bt == 0) return FORGE_OK;   // no tokens: every dX is empty
   DeviceInfo* d = nullptr;
   s = device_info(&d);
   if (s != FORGE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  GemmConfig cfg = choose_dgrad_config(bt, d_in, d_out, d->num_sms);
+  DgradPlan pl = plan_dgrad(items, n, bt, d->num_sms);
+  GemmConfig& cfg = pl.cfg;
   GemmArgs args;
   std::memset(&args, 0, sizeof(args));
-  GemmMaps& maps = args.maps[0];
-  const int bk = bk_of(cfg.cg);
-  // A = dY read K-major: 64 of d_out x 64 token rows per box; B = W read
-  // MN-major: 64 of d_in x bk of d_out per box; dX stored in 32 x 128 boxes
-  const bool ok =
-      get_map(&maps.dy, dY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_out, bt, d_out * 2, 64, 64,
-              CU_TENSOR_MAP_SWIZZLE_128B) &&
-      get_map(&maps.x, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_in, d_out, d_in * 2, 64, bk,
-              CU_TENSOR_MAP_SWIZZLE_128B) &&
-      get_map(&maps.w, dX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_in, bt, d_in * 2, 32, kBM,
-              CU_TENSOR_MAP_SWIZZLE_64B);
-  if (!ok) return FORGE_ERR_LAUNCH;
-  args.p = base_params(d_out, cfg, *d);   // the reduction runs over d_out
+  int64_t max_dout = 0;
+  for (int i = 0; i < n; ++i) max_dout = std::max<int64_t>(max_dout, items[i].d_out);
+  args.p = base_params(max_dout, cfg, *d);   // the reductions run over d_out
   args.p.splits = cfg.splits;
-  add_problem(args.p, cfg, d_in, bt, nullptr, nullptr);   // tile rows are tokens
-  // Split partials: taken from the pool in stream order and given back after
-  // the reduce kernel, or (no_alloc) placed in the static scratch with as
-  // many splits as fit.  Without the memory the launch runs unsplit (same
-  // accuracy, slower).
-  void* ws = nullptr;
-  const size_t ctile_bytes = static_cast<size_t>(cfg.cg) * kBM * cfg.bn * sizeof(float);
-  if (no_alloc) {
-    while (args.p.splits > 1 &&
-           static_cast<size_t>(args.p.num_tiles) * args.p.splits * ctile_bytes > kNoAllocScratchBytes)
-      --args.p.splits;
-    args.p.num_units = args.p.num_tiles * args.p.splits;
-    if (args.p.splits > 1) args.p.part = d->scratch;
-  } else if (args.p.splits > 1) {
-    const size_t part_bytes = static_cast<size_t>(args.p.num_tiles) * args.p.splits * ctile_bytes;
-    cudaMemPool_t pool = workspace_pool(*d);
-    if (pool && cudaMallocFromPoolAsync(&ws, part_bytes, pool, st) == cudaSuccess) {
-      args.p.part = static_cast<float*>(ws);
-    } else {
-      (void)cudaGetLastError();
-      ws = nullptr;
-      args.p.splits = 1;
-      args.p.num_units = args.p.num_tiles;
-    }
+  const int bk = bk_of(cfg.cg);
+  for (int k = 0; k < n; ++k) {
+    const forge_dgrad_item& it = items[pl.order[k]];
+    GemmMaps& maps = args.maps[k];
+    // A = dY read K-major: 64 of d_out x 64 token rows per box; B = W read
+    // MN-major: 64 of d_in x bk of d_out per box; dX stored in 32 x 128 boxes
+    const bool ok =
+        get_map(&maps.dy, it.dY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, it.d_out, bt, it.d_out * 2, 64,
+                64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+        get_map(&maps.x, it.W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, it.d_in, it.d_out, it.d_in * 2,
+                64, bk, CU_TENSOR_MAP_SWIZZLE_128B) &&
+        get_map(&maps.w, it.dX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, it.d_in, bt, it.d_in * 2, 32,
+                kBM, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!ok) return FORGE_ERR_LAUNCH;
+    add_problem(args.p, cfg, it.d_in, bt, nullptr, nullptr);   // tile rows are tokens
+    args.p.prob[k].num_k = static_cast<int32_t>(dgrad_num_k(it, cfg));
   }
+  // Split partials: taken from the pool in stream order and given back after
+  // the reduce kernels, or placed in the static scratch or the caller's
+  // workspace with as many splits as fit.  Without the memory the launch runs
+  // unsplit (same accuracy, slower).
+  void* ws = nullptr;
+  auto need = [&](int sp) { return static_cast<size_t>(args.p.num_tiles) * sp * pl.ctile_bytes; };
+  if (mode == kWsPool) {
+    if (args.p.splits > 1) {
+      cudaMemPool_t pool = workspace_pool(*d);
+      if (pool && cudaMallocFromPoolAsync(&ws, need(args.p.splits), pool, st) == cudaSuccess) {
+        args.p.part = static_cast<float*>(ws);
+      } else {
+        (void)cudaGetLastError();
+        ws = nullptr;
+        args.p.splits = 1;
+      }
+    }
+  } else {
+    float* base = mode == kWsStatic ? d->scratch : static_cast<float*>(cws);
+    const size_t cap = mode == kWsStatic ? kNoAllocScratchBytes : (cws ? cws_bytes : 0);
+    while (args.p.splits > 1 && need(args.p.splits) > cap) --args.p.splits;
+    if (args.p.splits > 1) args.p.part = base;
+  }
+  args.p.num_units = args.p.num_tiles * args.p.splits;
   set_grid(cfg, args.p.num_units, d->num_sms);
   args.p.drop_first_arrival = take_drop_flag();
   cudaError_t e = launch_gemm(kModeDgrad, kFmtBF16, cfg, args, st);
-  if (e == cudaSuccess && args.p.splits > 1)
-    e = launch_dgrad_reduce(args.p.part, args.p.splits, cfg.cg, cfg.bn, args.p.prob[0].tiles_m,
-                            args.p.prob[0].tiles_n, bt, d_in, dX, d->num_sms, st);
+  for (int k = 0; e == cudaSuccess && args.p.splits > 1 && k < n; ++k) {
+    const GemmProblem& q = args.p.prob[k];
+    const forge_dgrad_item& it = items[pl.order[k]];
+    e = launch_dgrad_reduce(args.p.part + static_cast<size_t>(q.part_tile0) * args.p.splits *
+                                              (pl.ctile_bytes / sizeof(float)),
+                            args.p.splits, cfg.cg, cfg.bn, q.tiles_m, q.tiles_n, bt, it.d_in,
+                            it.dX, d->num_sms, st);
+  }
   if (ws) cudaFreeAsync(ws, st);
   return e == cudaSuccess ? FORGE_OK : FORGE_ERR_LAUNCH;
+}
+
+forge_dgrad_item dgrad_item(const void* dY, const void* W, void* dX, int64_t d_in,
+                            int64_t d_out) {
+  forge_dgrad_item it;
+  it.dY = dY;
+  it.W = W;
+  it.dX = dX;
+  it.d_in = d_in;
+  it.d_out = d_out;
+  return it;
 }
 
 }  // namespace
@@ -902,105 +1024,195 @@ extern "C" {
 
 forge_status forge_dgrad(const void* dY, const void* W, void* dX, int64_t bt, int64_t d_in,
                          int64_t d_out, forge_stream stream) {
-  return dgrad_run(dY, W, dX, bt, d_in, d_out, stream, false);
+  const forge_dgrad_item it = dgrad_item(dY, W, dX, d_in, d_out);
+  return dgrad_run(&it, 1, bt, kWsPool, nullptr, 0, stream);
 }
 
-forge_status forge_wgrad_accumulate(const void* X, const void* dY, float* B, float beta,
-                                    int64_t bt, int64_t d_in, int64_t d_out,
-                                    forge_stream stream) {
-  forge_status s = check_shape(bt, d_in, d_out);
-  if (s != FORGE_OK) return s;
+forge_status forge_dgrad_grouped(const forge_dgrad_item* items, int n, int64_t bt,
+                                 void* workspace, size_t workspace_bytes, forge_stream stream) {
+  if (workspace && !aligned16(workspace)) return FORGE_ERR_ALIGN;
+  return dgrad_run(items, n, bt, kWsCaller, workspace, workspace_bytes, stream);
+}
+
+size_t forge_dgrad_workspace_bytes(const forge_dgrad_item* items, int n, int64_t bt) {
+  if (!items || n < 1 || n > FORGE_MAX_GROUP || bt <= 0) return 0;
+  for (int i = 0; i < n; ++i)
+    if (check_shape(bt, items[i].d_in, items[i].d_out) != FORGE_OK) return 0;
+  int sms = 152, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      sms = v;
+  }
+  const DgradPlan pl = plan_dgrad(items, n, bt, sms);
+  return pl.cfg.splits > 1 ? static_cast<size_t>(pl.tiles) * pl.cfg.splits * pl.ctile_bytes : 0;
+}
+
+forge_status forge_wgrad_accumulate_grouped(const forge_accum_item* items, int n, int64_t bt,
+                                            float beta, forge_stream stream) {
+  if (!items) return FORGE_ERR_NULL;
+  if (n < 1 || n > FORGE_MAX_GROUP) return FORGE_ERR_SHAPE;
   if (!std::isfinite(beta)) return FORGE_ERR_HYPER;
-  if (!B || (bt > 0 && (!X || !dY))) return FORGE_ERR_NULL;
-  if (!aligned16(B) || (bt > 0 && (!aligned16(X) || !aligned16(dY)))) return FORGE_ERR_ALIGN;
-  const uint64_t nb = 4ull * static_cast<uint64_t>(d_in) * static_cast<uint64_t>(d_out);
-  if (bt > 0 && (overlaps(B, nb, X, 2ull * bt * d_in) || overlaps(B, nb, dY, 2ull * bt * d_out)))
-    return FORGE_ERR_ALIAS;
+  for (int i = 0; i < n; ++i) {
+    const forge_accum_item& a = items[i];
+    forge_status s = check_shape(bt, a.d_in, a.d_out);
+    if (s != FORGE_OK) return s;
+    if (!a.B || (bt > 0 && (!a.X || !a.dY))) return FORGE_ERR_NULL;
+    if (!aligned16(a.B) || (bt > 0 && (!aligned16(a.X) || !aligned16(a.dY))))
+      return FORGE_ERR_ALIGN;
+  }
+  // no B overlaps any item's inputs or another B
+  for (int i = 0; i < n; ++i) {
+    const uint64_t nb = 4ull * static_cast<uint64_t>(items[i].d_in) *
+                        static_cast<uint64_t>(items[i].d_out);
+    for (int j = 0; j < n; ++j) {
+      const forge_accum_item& b = items[j];
+      if (bt > 0 && (overlaps(items[i].B, nb, b.X, 2ull * bt * b.d_in) ||
+                     overlaps(items[i].B, nb, b.dY, 2ull * bt * b.d_out)))
+        return FORGE_ERR_ALIAS;
+      if (j != i && overlaps(items[i].B, nb, b.B, 4ull * b.d_in * b.d_out)) return FORGE_ERR_ALIAS;
+    }
+  }
   DeviceInfo* d = nullptr;
-  s = device_info(&d);
+  forge_status s = device_info(&d);
   if (s != FORGE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the slots hold one fp32 box, as for store-G with an fp32 gradient
   GemmConfig cfg = choose_config(bt, kFmtF32, kModeStoreG);
+  // largest first
+  int order[FORGE_MAX_GROUP];
+  for (int i = 0; i < n; ++i) order[i] = i;
+  for (int i = 1; i < n; ++i)
+    for (int j = i; j > 0 && items[order[j]].d_in * items[order[j]].d_out >
+                                 items[order[j - 1]].d_in * items[order[j - 1]].d_out; --j) {
+      const int t = order[j];
+      order[j] = order[j - 1];
+      order[j - 1] = t;
+    }
   GemmArgs args;
   std::memset(&args, 0, sizeof(args));
-  GemmMaps& maps = args.maps[0];
-  const bool ok = (bt == 0 || operand_maps(maps, X, dY, bt, d_in, d_out, bk_of(cfg.cg))) &&
-                  get_map(&maps.w, B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d_in, d_out, d_in * 4, 32,
-                          kBM, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (!ok) return FORGE_ERR_LAUNCH;
   args.p = base_params(bt, cfg, *d);
   args.p.accum_beta = beta;
   args.p.accum_load = beta != 0.0f;
-  add_problem(args.p, cfg, d_in, d_out, nullptr, nullptr);
+  for (int k = 0; k < n; ++k) {
+    const forge_accum_item& a = items[order[k]];
+    GemmMaps& maps = args.maps[k];
+    const bool ok = (bt == 0 || operand_maps(maps, a.X, a.dY, bt, a.d_in, a.d_out,
+                                             bk_of(cfg.cg))) &&
+                    get_map(&maps.w, a.B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.d_in, a.d_out,
+                            a.d_in * 4, 32, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!ok) return FORGE_ERR_LAUNCH;
+    add_problem(args.p, cfg, a.d_in, a.d_out, nullptr, nullptr);
+  }
   set_grid(cfg, args.p.num_units, d->num_sms);
   args.p.drop_first_arrival = take_drop_flag();
   return launch_gemm(kModeAccum, kFmtF32, cfg, args, st) == cudaSuccess ? FORGE_OK
                                                                          : FORGE_ERR_LAUNCH;
 }
 
-forge_status forge_wgrad_opt(const void* X, const void* dY, void* W, forge_moment s1,
-                             forge_moment s2, int64_t bt, int64_t d_in, int64_t d_out,
-                             forge_optimizer opt, const forge_opt_hyper* hyper, int64_t step,
-                             forge_moment_fmt fmt, forge_stream stream) {
-  forge_status s = check_shape(bt, d_in, d_out);
-  if (s != FORGE_OK) return s;
+forge_status forge_wgrad_accumulate(const void* X, const void* dY, float* B, float beta,
+                                    int64_t bt, int64_t d_in, int64_t d_out,
+                                    forge_stream stream) {
+  forge_accum_item a;
+  a.X = X;
+  a.dY = dY;
+  a.B = B;
+  a.d_in = d_in;
+  a.d_out = d_out;
+  return forge_wgrad_accumulate_grouped(&a, 1, bt, beta, stream);
+}
+
+forge_status forge_wgrad_opt_grouped(const forge_linear* layers, int n, int64_t bt,
+                                     forge_optimizer opt, const forge_opt_hyper* hyper,
+                                     int64_t step, forge_moment_fmt fmt, forge_stream stream) {
+  if (!layers) return FORGE_ERR_NULL;
+  if (n < 1 || n > FORGE_MAX_GROUP) return FORGE_ERR_SHAPE;
   if (!hyper) return FORGE_ERR_HYPER;
-  s = check_opt_hyper(static_cast<int>(opt), *hyper, step);
+  forge_status s = check_opt_hyper(static_cast<int>(opt), *hyper, step);
   if (s != FORGE_OK) return s;
   if (fmt != FORGE_MOM_FP32 && fmt != FORGE_MOM_BF16) return FORGE_ERR_FORMAT;
   const int ns = opt_states(static_cast<int>(opt));
-  const void* st1 = ns >= 1 ? s1.data : nullptr;
-  const void* st2 = ns >= 2 ? s2.data : nullptr;
-  if (!W || (ns >= 1 && !st1) || (ns >= 2 && !st2)) return FORGE_ERR_NULL;
-  if (bt > 0 && (!X || !dY)) return FORGE_ERR_NULL;
-  if (!aligned16(W) || (st1 && !aligned16(st1)) || (st2 && !aligned16(st2)))
-    return FORGE_ERR_ALIGN;
-  if (bt > 0 && (!aligned16(X) || !aligned16(dY))) return FORGE_ERR_ALIGN;
-  const uint64_t n = static_cast<uint64_t>(d_in) * static_cast<uint64_t>(d_out);
-  const uint64_t nm = n * mom_elem_bytes(fmt);
-  if (overlaps(W, 2 * n, st1, nm) || overlaps(W, 2 * n, st2, nm) || overlaps(st1, nm, st2, nm))
-    return FORGE_ERR_ALIAS;
-  for (const void* in : {X, dY}) {
-    const uint64_t nin = 2ull * bt * (in == X ? d_in : d_out);
-    if (bt > 0 && (overlaps(in, nin, W, 2 * n) || overlaps(in, nin, st1, nm) ||
-                   overlaps(in, nin, st2, nm)))
+  // the states the optimizer does not have are neither read nor checked
+  forge_linear L[FORGE_MAX_GROUP];
+  for (int i = 0; i < n; ++i) {
+    L[i] = layers[i];
+    if (ns < 1) L[i].m.data = nullptr;
+    if (ns < 2) L[i].v.data = nullptr;
+    L[i].m.scale = L[i].v.scale = nullptr;
+    const forge_linear& a = L[i];
+    s = check_shape(bt, a.d_in, a.d_out);
+    if (s != FORGE_OK) return s;
+    if (!a.W || (ns >= 1 && !a.m.data) || (ns >= 2 && !a.v.data)) return FORGE_ERR_NULL;
+    if (bt > 0 && (!a.X || !a.dY)) return FORGE_ERR_NULL;
+    if (!aligned16(a.W) || (a.m.data && !aligned16(a.m.data)) || (a.v.data && !aligned16(a.v.data)))
+      return FORGE_ERR_ALIGN;
+    if (bt > 0 && (!aligned16(a.X) || !aligned16(a.dY))) return FORGE_ERR_ALIGN;
+    const uint64_t ne = static_cast<uint64_t>(a.d_in) * static_cast<uint64_t>(a.d_out);
+    const uint64_t nm = ne * mom_elem_bytes(fmt);
+    if (overlaps(a.W, 2 * ne, a.m.data, nm) || overlaps(a.W, 2 * ne, a.v.data, nm) ||
+        overlaps(a.m.data, nm, a.v.data, nm))
       return FORGE_ERR_ALIAS;
   }
+  for (int i = 0; i < n; ++i)
+    for (int j = 0; j < n; ++j)
+      if (layers_clash(L[i], L[j], bt, fmt, i == j)) return FORGE_ERR_ALIAS;
   DeviceInfo* d = nullptr;
   s = device_info(&d);
   if (s != FORGE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int ifmt = fmt == FORGE_MOM_FP32 ? kFmtF32 : kFmtBF16;
   GemmConfig cfg = choose_opt_config(bt, ifmt);
-  GemmArgs args;
-  std::memset(&args, 0, sizeof(args));
-  GemmMaps& maps = args.maps[0];
   const bool f32 = fmt == FORGE_MOM_FP32;
   const CUtensorMapDataType mdt =
       f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const CUtensorMapSwizzle msw = f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   const int eb = f32 ? 4 : 2;
   const uint32_t rows = static_cast<uint32_t>(slot_rows(kModeOpt, ifmt, cfg.prof));
-  bool ok = (bt == 0 || operand_maps(maps, X, dY, bt, d_in, d_out, bk_of(cfg.cg))) &&
-            get_map(&maps.w, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_in, d_out, d_in * 2, 32,
-                    rows, CU_TENSOR_MAP_SWIZZLE_64B);
-  if (ok && ns >= 1) ok = get_map(&maps.m, st1, mdt, d_in, d_out, d_in * eb, 32, rows, msw);
-  if (ok && ns >= 2) ok = get_map(&maps.v, st2, mdt, d_in, d_out, d_in * eb, 32, rows, msw);
-  if (!ok) return FORGE_ERR_LAUNCH;
+  int order[FORGE_MAX_GROUP];
+  largest_first(L, n, fmt, order);
+  GemmArgs args;
+  std::memset(&args, 0, sizeof(args));
   args.p = base_params(bt, cfg, *d);
   args.p.o = make_opt_consts(static_cast<int>(opt), *hyper, step);
   args.p.nstate = ns;
-  add_problem(args.p, cfg, d_in, d_out, nullptr, nullptr);
+  for (int k = 0; k < n; ++k) {
+    const forge_linear& a = L[order[k]];
+    GemmMaps& maps = args.maps[k];
+    bool ok = (bt == 0 || operand_maps(maps, a.X, a.dY, bt, a.d_in, a.d_out, bk_of(cfg.cg))) &&
+              get_map(&maps.w, a.W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.d_in, a.d_out,
+                      a.d_in * 2, 32, rows, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (ok && ns >= 1)
+      ok = get_map(&maps.m, a.m.data, mdt, a.d_in, a.d_out, a.d_in * eb, 32, rows, msw);
+    if (ok && ns >= 2)
+      ok = get_map(&maps.v, a.v.data, mdt, a.d_in, a.d_out, a.d_in * eb, 32, rows, msw);
+    if (!ok) return FORGE_ERR_LAUNCH;
+    add_problem(args.p, cfg, a.d_in, a.d_out, nullptr, nullptr);
+  }
   set_grid(cfg, args.p.num_units, d->num_sms);
   args.p.drop_first_arrival = take_drop_flag();
   return launch_gemm(kModeOpt, ifmt, cfg, args, st) == cudaSuccess ? FORGE_OK
                                                                       : FORGE_ERR_LAUNCH;
 }
 
+forge_status forge_wgrad_opt(const void* X, const void* dY, void* W, forge_moment s1,
+                             forge_moment s2, int64_t bt, int64_t d_in, int64_t d_out,
+                             forge_optimizer opt, const forge_opt_hyper* hyper, int64_t step,
+                             forge_moment_fmt fmt, forge_stream stream) {
+  forge_linear L;
+  L.X = X;
+  L.dY = dY;
+  L.W = W;
+  L.m = s1;
+  L.v = s2;
+  L.d_in = d_in;
+  L.d_out = d_out;
+  return forge_wgrad_opt_grouped(&L, 1, bt, opt, hyper, step, fmt, stream);
+}
+
 forge_status forge_dgrad_noalloc(const void* dY, const void* W, void* dX, int64_t bt,
                                  int64_t d_in, int64_t d_out, forge_stream stream) {
-  return dgrad_run(dY, W, dX, bt, d_in, d_out, stream, true);
+  const forge_dgrad_item it = dgrad_item(dY, W, dX, d_in, d_out);
+  return dgrad_run(&it, 1, bt, kWsStatic, nullptr, 0, stream);
 }
 
 forge_status forge_linear_backward(const void* X, const void* dY, void* W, void* dX,
@@ -1035,6 +1247,49 @@ forge_status forge_linear_backward(const void* X, const void* dY, void* W, void*
   if (s != FORGE_OK) return s;
   return forge_wgrad_adamw(X, dY, W, m, v, bt, d_in, d_out, lr, beta1, beta2, eps, weight_decay,
                            step, fmt, stream);
+}
+
+forge_status forge_linear_backward_grouped(const forge_linear* layers, void* const* dX, int n,
+                                           int64_t bt, float lr, float beta1, float beta2,
+                                           float eps, float weight_decay, int64_t step,
+                                           forge_moment_fmt fmt, void* workspace,
+                                           size_t workspace_bytes, forge_stream stream) {
+  // every argument of both halves is checked before anything is enqueued
+  if (!layers || !dX) return FORGE_ERR_NULL;
+  if (n < 1 || n > FORGE_MAX_GROUP) return FORGE_ERR_SHAPE;
+  for (int i = 0; i < n; ++i) {
+    forge_status s = check_linear(layers[i], bt, fmt);
+    if (s != FORGE_OK) return s;
+  }
+  forge_status s = check_hyper(lr, beta1, beta2, eps, weight_decay, step);
+  if (s != FORGE_OK) return s;
+  for (int i = 0; i < n; ++i)
+    for (int j = 0; j < n; ++j)
+      if (layers_clash(layers[i], layers[j], bt, fmt, i == j)) return FORGE_ERR_ALIAS;
+  forge_dgrad_item items[FORGE_MAX_GROUP];
+  for (int i = 0; i < n; ++i) {
+    const forge_linear& L = layers[i];
+    items[i] = dgrad_item(L.dY, L.W, dX[i], L.d_in, L.d_out);
+    if (bt == 0) continue;
+    if (!dX[i]) return FORGE_ERR_NULL;
+    if (!aligned16(dX[i])) return FORGE_ERR_ALIGN;
+    // no dX overlaps any layer's inputs, state or scales
+    const uint64_t ndx = 2ull * bt * L.d_in;
+    for (int j = 0; j < n; ++j) {
+      const forge_linear& b = layers[j];
+      if (overlaps(dX[i], ndx, b.X, 2ull * bt * b.d_in) ||
+          input_overlaps_state(dX[i], ndx, b.W, b.m, b.v, b.d_in, b.d_out, fmt))
+        return FORGE_ERR_ALIAS;
+    }
+  }
+  if (workspace && !aligned16(workspace)) return FORGE_ERR_ALIGN;
+  s = check_dgrad_items(items, n, bt);
+  if (s != FORGE_OK) return s;
+  // dX reads W before the fused step overwrites it (Algorithm 1): same stream
+  s = dgrad_run(items, n, bt, kWsCaller, workspace, workspace_bytes, stream);
+  if (s != FORGE_OK) return s;
+  return forge_wgrad_adamw_grouped(layers, n, bt, lr, beta1, beta2, eps, weight_decay, step,
+                                   fmt, stream);
 }
 
 forge_status forge_adamw(const void* dW, forge_dtype dw_dtype, void* W, forge_moment m,

@@ -212,12 +212,14 @@ __device__ __forceinline__ bool wait_poll(uint32_t bar, uint32_t parity, const W
   return wait_bounded(bar, parity, w, site);
 }
 
-// The k-steps [kb, ke) of work unit u: split u % splits of its tile's num_k
-// steps (never empty: the host keeps splits <= num_k).
-__device__ __forceinline__ void split_range(int u, const GemmParams& p, int& kb, int& ke) {
+// The k-steps [kb, ke) of work unit u of layer pi: split u % splits of the
+// layer's num_k steps (never empty: the host keeps splits <= num_k).
+__device__ __forceinline__ void split_range(int u, int pi, const GemmParams& p, int& kb,
+                                            int& ke) {
   const int z = u % p.splits;
-  kb = (z * p.num_k) / p.splits;
-  ke = ((z + 1) * p.num_k) / p.splits;
+  const int nk = p.prob[pi].num_k;
+  kb = (z * nk) / p.splits;
+  ke = ((z + 1) * nk) / p.splits;
 }
 
 // Global tile index -> (layer, tile row, tile column).  Layers are laid out
@@ -819,7 +821,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const int pi = tile_coords(tile_of(t), p, tm, tn);
         const GemmMaps& maps = a.maps[pi];
         int kb, ke;
-        split_range(t, p, kb, ke);
+        split_range(t, pi, p, kb, ke);
         for (int k = kb; k < ke; ++k, ++cnt) {
           const int s = cnt % T::STAGES;
           const uint32_t ph = (cnt / T::STAGES) & 1u;
@@ -873,7 +875,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         tc_fence_after_sync();
         const uint32_t d = tmem_base + buf * BN;
         int kb, ke;
-        split_range(t, p, kb, ke);
+        {
+          int tm_, tn_;
+          split_range(t, tile_coords(tile_of(t), p, tm_, tn_), p, kb, ke);
+        }
         for (int k = kb; k < ke; ++k, ++cnt) {
           const int s = cnt % T::STAGES;
           const uint32_t ph = (cnt / T::STAGES) & 1u;
@@ -1113,7 +1118,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       if constexpr (MODE == kModeDgrad) {
         if (p.splits > 1) {
           // partials indexed by tile row and column (not queue order)
-          const size_t ctile = (static_cast<size_t>(tm) * pr.tiles_n + tn) * CG + rank;
+          const size_t ctile =
+              (static_cast<size_t>(pr.part_tile0) + static_cast<size_t>(tm) * pr.tiles_n + tn) * CG +
+              rank;
           const size_t part_elems = static_cast<size_t>(kBM) * BN;
           float* mine = p.part + (ctile * p.splits + t % p.splits) * part_elems;
 #pragma unroll 1
@@ -1163,7 +1170,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         } else if (active) {
           if constexpr (MODE == kModeFused) {
             epi_slice_fused_16<FMT, T::RPS>(taddr, zero_grad, slot, srow, h, p.h, p.sr != 0,
-                                            p.sr_seed, static_cast<uint32_t>(p.sr_step),
+                                            pr.sr_seed, static_cast<uint32_t>(p.sr_step),
                                             static_cast<uint32_t>(y0) + srow,
                                             static_cast<uint32_t>(x0 >> 4) + h);
           } else if constexpr (MODE == kModeOpt) {

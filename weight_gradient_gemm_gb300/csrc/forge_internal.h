@@ -55,12 +55,16 @@ struct GemmProblem {
   int32_t d_in, d_out;
   int32_t tiles_m, tiles_n;
   int32_t tile_start;         // first index of this layer's tiles in the launch's queue
+  int32_t num_k;              // k-steps of this layer's reduction (tokens, or d_out for dX)
+  int32_t part_tile0;         // split input gradient: first partial tile of this layer
+  uint64_t sr_seed;           // stochastic rounding: this layer's Philox key
   float* m_scale;             // int8: scales [d_out, d_in/128]; fp8: the moment's
   float* v_scale;             // four words (read scale, write scale, amax)
 };
 
 struct GemmParams {
-  int32_t bt, num_k;          // shared token count of every layer in the launch
+  int32_t bt;                 // shared token count of every layer in the launch
+  int32_t num_k;              // the largest layer's k-steps (0: no tokens, G = 0)
   int32_t nprob, num_tiles;   // layers, and tiles over all of them
   // Split reduction (input gradient only; 1 elsewhere): each tile's k-steps
   // are cut into `splits` contiguous ranges, one work unit each, so the queue
@@ -68,17 +72,18 @@ struct GemmParams {
   // each other.  Every unit writes its fp32 partial tile to `part`; the
   // reduce kernel then adds the partials in split order and stores dX.
   int32_t splits, num_units;
-  float* part;                // [tile row][tile column][CTA of the pair][split][128 x BN] fp32
+  float* part;                // per layer from part_tile0: [tile row][tile column][CTA of
+                              // the pair][split][128 x BN] fp32
   int32_t group_m;            // tile-order swizzle: rows of tiles per group
   AdamWConsts h;
   OptConsts o;                // kModeOpt: the optimizer and its step constants
   int32_t nstate;             // kModeOpt: state tensors read and written (0..2)
   float accum_beta;           // kModeAccum: beta
   int32_t accum_load;         // kModeAccum: B is read (beta != 0)
-  // kModeFused: commit W by stochastic rounding (Philox4x64-10 key (sr_seed,
-  // 0), counter (row, column / 16, sr_step, 0)) instead of to nearest even
+  // kModeFused: commit W by stochastic rounding (Philox4x64-10 key (the
+  // layer's sr_seed, 0), counter (row, column / 16, sr_step, 0)) instead of
+  // to nearest even
   int32_t sr, sr_step;
-  uint64_t sr_seed;
   GemmProblem prob[kMaxGroup];
   int* err;                   // device error word
   int* err_site;              // device word: where a wait first timed out

@@ -58,6 +58,16 @@ class ForgeLinear(ctypes.Structure):
 
 MAX_GROUP = 8
 
+
+class ForgeAccumItem(ctypes.Structure):
+    _fields_ = [("X", ctypes.c_void_p), ("dY", ctypes.c_void_p), ("B", ctypes.c_void_p),
+                ("d_in", ctypes.c_int64), ("d_out", ctypes.c_int64)]
+
+
+class ForgeDgradItem(ctypes.Structure):
+    _fields_ = [("dY", ctypes.c_void_p), ("W", ctypes.c_void_p), ("dX", ctypes.c_void_p),
+                ("d_in", ctypes.c_int64), ("d_out", ctypes.c_int64)]
+
 # forge_profile values
 PROFILES = {"auto": -1, "stream": 0, "mma": 1, "balanced": 2, "deep": 3}
 
@@ -123,6 +133,25 @@ def lib() -> ctypes.CDLL:
             L.forge_set_wait_limit_ns.restype = None
             L.forge_debug_drop_first_arrival.argtypes = [st]
             L.forge_debug_drop_first_arrival.restype = None
+            sz = ctypes.c_size_t
+            L.forge_wgrad_opt_grouped.argtypes = [ctypes.POINTER(ForgeLinear), st, i64, st,
+                                                  ctypes.POINTER(ForgeOptHyper), i64, st, vp]
+            L.forge_wgrad_opt_grouped.restype = st
+            L.forge_wgrad_adamw_sr_grouped.argtypes = [ctypes.POINTER(ForgeLinear),
+                                                       ctypes.POINTER(ctypes.c_uint64), st, i64,
+                                                       f32, f32, f32, f32, f32, i64, st, vp]
+            L.forge_wgrad_adamw_sr_grouped.restype = st
+            L.forge_wgrad_accumulate_grouped.argtypes = [ctypes.POINTER(ForgeAccumItem), st, i64,
+                                                         f32, vp]
+            L.forge_wgrad_accumulate_grouped.restype = st
+            L.forge_dgrad_grouped.argtypes = [ctypes.POINTER(ForgeDgradItem), st, i64, vp, sz, vp]
+            L.forge_dgrad_grouped.restype = st
+            L.forge_dgrad_workspace_bytes.argtypes = [ctypes.POINTER(ForgeDgradItem), st, i64]
+            L.forge_dgrad_workspace_bytes.restype = sz
+            L.forge_linear_backward_grouped.argtypes = [ctypes.POINTER(ForgeLinear),
+                                                        ctypes.POINTER(vp), st, i64, f32, f32,
+                                                        f32, f32, f32, i64, st, vp, sz, vp]
+            L.forge_linear_backward_grouped.restype = st
             L.forge_fp8_roll_scales.argtypes = [vp, st, f32, vp]
             L.forge_fp8_roll_scales.restype = st
             L.forge_set_tuning.argtypes = [ctypes.POINTER(ForgeTuning)]
@@ -552,3 +581,155 @@ def fp8_roll_scales(scales: torch.Tensor, headroom: float = 1.0, stream=None) ->
     n = 1 if scales.dim() == 1 else scales.shape[0]
     _check(lib().forge_fp8_roll_scales(_ptr(scales), n, headroom, _stream(stream)),
            "forge_fp8_roll_scales")
+
+
+# ---------------------------------------------------------------------------
+# grouped calls: several linear layers with one token count in one launch
+# ---------------------------------------------------------------------------
+
+def _group_arr(layers, m_key="m", v_key="v", scales=True):
+    """ForgeLinear array, token count and the layers' (d_in, d_out)."""
+    n = len(layers)
+    if not 1 <= n <= MAX_GROUP:
+        raise ValueError(f"1 to {MAX_GROUP} layers per grouped call")
+    arr = (ForgeLinear * n)()
+    bt = None
+    for i, ly in enumerate(layers):
+        b, d_in, d_out = _operands(ly["X"], ly["dY"])
+        if bt is not None and b != bt:
+            raise ValueError("all layers of a group need the same token count")
+        bt = b
+        _want(ly["W"], "W", (d_out, d_in), _BF16)
+        m, v = ly.get(m_key), ly.get(v_key)
+        _on_device(X=ly["X"], dY=ly["dY"], W=ly["W"], m=m, v=v,
+                   m_scale=ly.get("m_scale") if scales else None,
+                   v_scale=ly.get("v_scale") if scales else None)
+        arr[i] = ForgeLinear(_ptr(ly["X"]), _ptr(ly["dY"]), _ptr(ly["W"]),
+                             _moment(m, ly.get("m_scale") if scales else None) if m is not None
+                             else ForgeMoment(None, None),
+                             _moment(v, ly.get("v_scale") if scales else None) if v is not None
+                             else ForgeMoment(None, None), d_in, d_out)
+    return arr, n, bt
+
+
+def wgrad_opt_grouped(layers, opt: int, *, lr: float, weight_decay: float, step: int,
+                      beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8,
+                      momentum: float = 0.9, alpha: float = 0.99, momentum_decay: float = 4e-3,
+                      stream=None) -> None:
+    """wgrad_opt on several layers in one launch; each layer is a dict with X,
+    dY, W and the optimizer's states s1, s2 (as many as OPT_STATES says)."""
+    n_st = OPT_STATES.get(opt)
+    if n_st is None:
+        raise ValueError(f"unknown optimizer {opt}")
+    fmt = MOM_FP32
+    for ly in layers:
+        d_out, d_in = ly["W"].shape
+        sts = [ly.get("s1"), ly.get("s2")][:n_st]
+        for i, t in enumerate(sts):
+            _want(t, f"s{i + 1}", (d_out, d_in),
+                  (sts[0].dtype,) if i else (torch.float32, torch.bfloat16))
+        if sts:
+            fmt = moment_format(sts[0])
+    arr, n, bt = _group_arr([dict(ly, s1=ly.get("s1") if n_st >= 1 else None,
+                                  s2=ly.get("s2") if n_st >= 2 else None) for ly in layers],
+                            "s1", "s2", scales=False)
+    h = ForgeOptHyper(lr, weight_decay, beta1, beta2, eps, momentum, alpha, momentum_decay)
+    _check(lib().forge_wgrad_opt_grouped(arr, n, bt, opt, ctypes.byref(h), step, fmt,
+                                         _stream(stream)), "forge_wgrad_opt_grouped")
+
+
+def wgrad_adamw_sr_grouped(layers, seeds, *, lr: float, beta1: float, beta2: float, eps: float,
+                           weight_decay: float, step: int, stream=None) -> None:
+    """wgrad_adamw_sr on several layers in one launch; layer i uses seeds[i]."""
+    fmt = None
+    for ly in layers:
+        d_out, d_in = ly["W"].shape
+        f = _moments(ly["m"], ly["v"], None, None, d_out, d_in, (torch.float32, torch.bfloat16))
+        if fmt is not None and f != fmt:
+            raise ValueError("all layers of a group need the same moment format")
+        fmt = f
+    arr, n, bt = _group_arr(layers, scales=False)
+    if len(seeds) != n:
+        raise ValueError("one seed per layer")
+    sd = (ctypes.c_uint64 * n)(*[int(x) for x in seeds])
+    _check(lib().forge_wgrad_adamw_sr_grouped(arr, sd, n, bt, lr, beta1, beta2, eps,
+                                              weight_decay, step, fmt, _stream(stream)),
+           "forge_wgrad_adamw_sr_grouped")
+
+
+def wgrad_accumulate_grouped(items, beta: float, stream=None) -> None:
+    """wgrad_accumulate on several layers (dicts with X, dY, B) in one launch."""
+    n = len(items)
+    if not 1 <= n <= MAX_GROUP:
+        raise ValueError(f"1 to {MAX_GROUP} layers per grouped call")
+    arr = (ForgeAccumItem * n)()
+    bt = None
+    for i, it in enumerate(items):
+        b, d_in, d_out = _operands(it["X"], it["dY"])
+        if bt is not None and b != bt:
+            raise ValueError("all layers of a group need the same token count")
+        bt = b
+        _want(it["B"], "B", (d_out, d_in), _F32)
+        _on_device(X=it["X"], dY=it["dY"], B=it["B"])
+        arr[i] = ForgeAccumItem(_ptr(it["X"]), _ptr(it["dY"]), _ptr(it["B"]), d_in, d_out)
+    _check(lib().forge_wgrad_accumulate_grouped(arr, n, bt, beta, _stream(stream)),
+           "forge_wgrad_accumulate_grouped")
+
+
+def _dgrad_arr(items):
+    n = len(items)
+    if not 1 <= n <= MAX_GROUP:
+        raise ValueError(f"1 to {MAX_GROUP} projections per grouped call")
+    arr = (ForgeDgradItem * n)()
+    bt = None
+    for i, it in enumerate(items):
+        b, d_out, d_in = _dgrad_shapes(it["dY"], it["W"], it["dX"])
+        if bt is not None and b != bt:
+            raise ValueError("all projections of a group need the same token count")
+        bt = b
+        arr[i] = ForgeDgradItem(_ptr(it["dY"]), _ptr(it["W"]), _ptr(it["dX"]), d_in, d_out)
+    return arr, n, bt
+
+
+def dgrad_workspace_bytes(items) -> int:
+    """Workspace bytes dgrad_grouped wants for these projections (dicts with
+    dY, W, dX), 0 if it would not split."""
+    arr, n, bt = _dgrad_arr(items)
+    return int(lib().forge_dgrad_workspace_bytes(arr, n, bt))
+
+
+def dgrad_grouped(items, workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """dX = dY W for several projections (dicts with dY, W, dX) in one launch;
+    split partials go to `workspace` (a device tensor; none: unsplit)."""
+    arr, n, bt = _dgrad_arr(items)
+    if workspace is not None:
+        _dense(workspace, "workspace")
+    _check(lib().forge_dgrad_grouped(arr, n, bt, _ptr(workspace),
+                                     0 if workspace is None else workspace.numel() *
+                                     workspace.element_size(), _stream(stream)),
+           "forge_dgrad_grouped")
+
+
+def linear_backward_grouped(layers, *, lr: float, beta1: float, beta2: float, eps: float,
+                            weight_decay: float, step: int,
+                            workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """linear_backward on several layers in one grouped dX launch and one
+    grouped fused launch.  Each layer is a dict with X, dY, W, dX, m, v (and
+    m_scale, v_scale for int8 or fp8 moments)."""
+    fmt = None
+    for ly in layers:
+        d_out, d_in = ly["W"].shape
+        f = _moments(ly["m"], ly["v"], ly.get("m_scale"), ly.get("v_scale"), d_out, d_in)
+        if fmt is not None and f != fmt:
+            raise ValueError("all layers of a group need the same moment format")
+        fmt = f
+        _want(ly["dX"], "dX", (ly["X"].shape[0], d_in), _BF16)
+        _on_device(dX=ly["dX"])
+    arr, n, bt = _group_arr(layers)
+    dx = (ctypes.c_void_p * n)(*[_ptr(ly["dX"]) for ly in layers])
+    if workspace is not None:
+        _dense(workspace, "workspace")
+    _check(lib().forge_linear_backward_grouped(
+        arr, dx, n, bt, lr, beta1, beta2, eps, weight_decay, step, fmt, _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _stream(stream)), "forge_linear_backward_grouped")

@@ -326,7 +326,7 @@ def run_gpu(args, rank, world, dev):
     # timed region): per-launch statistics over a window long enough for the
     # clock sampler, with the clock samples binned by quarter of the window
     steady = None
-    if rank == 0:
+    if rank == 0 and not args.no_diagnostics:
         est = max(kern_ms / max(1, args.steps), 1e-3)
         n_st = int(min(20000, max(args.steps, math.ceil(1000.0 / est))))
         sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -341,6 +341,13 @@ def run_gpu(args, rank, world, dev):
         steady = dict(launch_ms=[a.elapsed_time(b) for a, b in sev], w0=s0, w1=s1)
     if sampler:
         sampler.stop()
+
+    if args.no_diagnostics:
+        return dict(layer=layer, elapsed_ms=elapsed_ms, kern_ms=kern_ms, launch_ms=launch_ms,
+                    steady=None, sampler=sampler, unf_ms=None, per_proj_ms=None, backward=None,
+                    opt_ms=None, opt_fmt=None, acc_ms=None, sr_ms=None, e2e=None, e2e_ms=None,
+                    clocks=sampler.summary(w0, w1) if sampler else None,
+                    config=F.describe_config(bt, 4096, 4096, fmt))
 
     # ---- diagnostics (not the reported value): the same step as seven launches
     sep_steps = max(3, min(args.steps, 30))
@@ -831,13 +838,31 @@ def config_blocks(args, dev, peaks, peak_kind):
         nbytes = sum(g["W"].numel() * STATE_BYTES[fmt]
                      + 2.0 * bt * (g["X"].shape[1] + g["dY"].shape[1]) for g in group)
         mean_s = sum(ms) / len(ms) * 1e-3
+        # cuBLAS's plain weight-gradient GEMM dW = dY^T X (bf16 out) on the
+        # same tensors, timed the same way right after: the main loop's
+        # reference under the same clocks and power
+        cub = None
+        if bt >= 2048:
+            outs = [torch.empty_like(g["W"]) for g in group]
+
+            def cublas_wgrad():
+                for g, o in zip(group, outs):
+                    torch.matmul(g["dY"].t(), g["X"], out=o)
+            for _ in range(3):
+                cublas_wgrad()
+            cms, c0, c1 = timed_launches(cublas_wgrad, max(10, n // 2), stream)
+            cmean = sum(cms) / len(cms) * 1e-3
+            cub = {"ms_per_step": cmean * 1e3, "tflops": flops / cmean / 1e12,
+                   "fused_vs_cublas_gemm": cmean / mean_s, "clocks": sampler.summary(c0, c1)}
+            del outs
         out[name] = {"workload": workload, "bt": bt, "moments": FMT_NAMES[fmt],
                      "launch": "forge_wgrad_adamw_grouped, seven projections",
                      "kernel": F.describe_config(bt, 4096, 4096, fmt),
                      "tflops": flops / mean_s / 1e12,
                      "roofline": roofline_of(flops, nbytes, mean_s, peaks, peak_kind,
                                              stored_traffic(workload)),
-                     "per_launch": launch_stats(ms), "clocks": sampler.summary(w0, w1)}
+                     "per_launch": launch_stats(ms), "clocks": sampler.summary(w0, w1),
+                     "cublas_wgrad_gemm": cub}
         del group, f8
         torch.cuda.empty_cache()
     # C5: the whole stack at 8192 tokens
@@ -1069,6 +1094,9 @@ def main():
                     help="one of %s, llama31_8b_layer_bt<BT>_<fp32|bf16|int8>, or the full "
                          "224-linear stack llama31_8b_stack_bt<BT>_<fp32|bf16|int8>" % sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-diagnostics", action="store_true",
+                    help="time the step only (no steady repeat, unfused arm, backward, other "
+                         "optimizers, accumulate, SR store or e2e): for profiling runs")
     ap.add_argument("--no-blocks", action="store_true",
                     help="skip the other configurations (C3, C4, fp32 at 4096, the C5 stack)")
     ap.add_argument("--reference-budget", type=float, default=120.0,
@@ -1161,37 +1189,40 @@ def main():
                           "hbm_gbs": layer.alg_bytes() / (ms * 1e-3) / 1e9},
         "per_launch": launch_stats(res["launch_ms"]),
         "steady": steady,
-        "unfused": {"ms_per_step": res["unf_ms"],
-                    "value": job_value(world, flops, res["unf_ms"] * 1e-3) / 1e12,
-                    "fused_speedup": res["unf_ms"] / ms,
-                    "path": "forge_wgrad (bf16 dW) + forge_adamw"},
-        "e2e": {"value": job_value(world, flops, res["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
-                "ms_per_step": res["e2e_ms"], "h2d_bytes_per_step": layer.h2d_bytes(),
-                "d2h_bytes_per_step": 4,
-                "pipeline": "X, dY of step k+1 copied from pinned host memory on a second "
-                            "stream while step k computes; 4-byte status read after every step",
-                **res["e2e"]},
-        "per_projection_separate_launches": [
-            {"name": it["name"], "shape": [it["d_out"], it["d_in"]],
-             "us": round(t * 1e3, 2),
-             "gbs": round((it["d_in"] * it["d_out"] * STATE_BYTES[fmt]
-                           + 2.0 * bt * (it["d_in"] + it["d_out"])) / (t * 1e-3) / 1e9, 1),
-             "tflops": round(2.0 * bt * it["d_in"] * it["d_out"] / (t * 1e-3) / 1e12, 1)}
-            for it, t in zip(layer.items, res["per_proj_ms"])],
-        "linear_backward": backward_block(res["backward"], flops, ms, peaks, peak_kind),
-        "optimizers": optimizers_block(res["opt_ms"], res["opt_fmt"], layer, peaks),
-        "accumulate": accumulate_block(res["acc_ms"], layer, peaks),
-        "sr_store": None if res["sr_ms"] is None else {
-            "ms_per_step": res["sr_ms"],
-            "round_to_nearest_ms_per_step": sum(res["per_proj_ms"]),
-            "overhead": res["sr_ms"] / sum(res["per_proj_ms"]) - 1.0,
-            "launch": "forge_wgrad_adamw_sr_grouped (one launch per layer), against "
-                      "forge_wgrad_adamw per projection",
-            "vs_grouped_round_to_nearest": res["sr_ms"] / ms},
         "gpu_launches": launches,
         "clocks": res["clocks"],
         "system": run_metadata(),
     }
+    if not args.no_diagnostics:
+        line.update({
+            "unfused": {"ms_per_step": res["unf_ms"],
+                        "value": job_value(world, flops, res["unf_ms"] * 1e-3) / 1e12,
+                        "fused_speedup": res["unf_ms"] / ms,
+                        "path": "forge_wgrad (bf16 dW) + forge_adamw"},
+            "e2e": {"value": job_value(world, flops, res["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "ms_per_step": res["e2e_ms"], "h2d_bytes_per_step": layer.h2d_bytes(),
+                    "d2h_bytes_per_step": 4,
+                    "pipeline": "X, dY of step k+1 copied from pinned host memory on a second "
+                                "stream while step k computes; 4-byte status read after every step",
+                    **res["e2e"]},
+            "per_projection_separate_launches": [
+                {"name": it["name"], "shape": [it["d_out"], it["d_in"]],
+                 "us": round(t * 1e3, 2),
+                 "gbs": round((it["d_in"] * it["d_out"] * STATE_BYTES[fmt]
+                               + 2.0 * bt * (it["d_in"] + it["d_out"])) / (t * 1e-3) / 1e9, 1),
+                 "tflops": round(2.0 * bt * it["d_in"] * it["d_out"] / (t * 1e-3) / 1e12, 1)}
+                for it, t in zip(layer.items, res["per_proj_ms"])],
+            "linear_backward": backward_block(res["backward"], flops, ms, peaks, peak_kind),
+            "optimizers": optimizers_block(res["opt_ms"], res["opt_fmt"], layer, peaks),
+            "accumulate": accumulate_block(res["acc_ms"], layer, peaks),
+            "sr_store": None if res["sr_ms"] is None else {
+                "ms_per_step": res["sr_ms"],
+                "round_to_nearest_ms_per_step": sum(res["per_proj_ms"]),
+                "overhead": res["sr_ms"] / sum(res["per_proj_ms"]) - 1.0,
+                "launch": "forge_wgrad_adamw_sr_grouped (one launch per layer), against "
+                          "forge_wgrad_adamw per projection",
+                "vs_grouped_round_to_nearest": res["sr_ms"] / ms},
+        })
     if not args.no_blocks and world == 1:
         del layer, res
         torch.cuda.empty_cache()

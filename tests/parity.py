@@ -60,8 +60,8 @@ class Report:
 
 
 def check_w(gpu_w_bits, w_outs, W0, label=""):
-    """The bf16 weight bar.  w_outs: the oracle's fp64 W' at G - tau, G, G + tau;
-    W0: the weight before the step (fp64).
+    """The bf16 weight bar.  w_outs: the oracle's fp64 W' at the points of
+    g_points (at G first); W0: the weight before the step (fp64).
 
     The GPU forms W' = (1 - lr wd) W - lr u in fp32: its error is at most a few
     units of 2^-24 of the terms, bounded here by delta = 2^-21 (|W| + |W - W'|)
@@ -79,7 +79,7 @@ def check_w(gpu_w_bits, w_outs, W0, label=""):
     wlo, whi = np.minimum.reduce(wb), np.maximum.reduce(wb)
     g = bf16_ordered(gpu_w_bits)
     dist = np.maximum(np.maximum(wlo - g, g - whi), 0)
-    mid = w_outs[1]
+    mid = w_outs[0]
     delta = 2.0 ** -21 * (np.abs(W0) + np.abs(W0 - mid))
     ulp_mid = np.exp2(np.floor(np.log2(np.maximum(np.abs(mid), 2.0 ** -126))) - 7)
     cancel = delta > 0.5 * ulp_mid
@@ -101,10 +101,36 @@ def check_w(gpu_w_bits, w_outs, W0, label=""):
     return rep
 
 
-def _oracle_range(G, tau, W, m, v, hyper, t):
-    """Oracle fp64 results at G - tau, G, G + tau."""
-    outs = [O.adamw_f64(G + d, W, m, v, hyper, t) for d in (-tau, 0.0 * tau, tau)]
-    return outs   # list of (W', m', v')
+def g_points(G, tau, extra=()):
+    """Gradients at which the oracle is evaluated to span its results over
+    [G - tau, G + tau]: G first, then eight more points across the interval,
+    g = 0 where the interval holds it (the second moment is smallest there),
+    and each array in `extra` clipped into the interval (an interior
+    extremum of the update).  The update is not monotonic in g, so the end
+    points alone do not bound it."""
+    pts = [G] + [G + f * tau for f in (-1.0, -0.75, -0.5, -0.25, 0.25, 0.5, 0.75, 1.0)]
+    pts.append(np.where(np.abs(G) <= tau, 0.0, G))
+    for e in extra:
+        pts.append(np.clip(e, G - tau, G + tau))
+    return pts
+
+
+def adamw_extremum(m, v, hyper):
+    """The gradient at which u(g) = (b1 m + (1 - b1) g) / sqrt(b2 v + (1 - b2) g^2)
+    is extremal (without eps): g* = (1 - b1) b2 v / (b1 m (1 - b2)); NaN where
+    m = 0."""
+    b1, b2 = hyper.beta1, hyper.beta2
+    den = b1 * m * (1.0 - b2)
+    safe = np.where(den != 0.0, den, 1.0)
+    return np.where(den != 0.0, (1.0 - b1) * b2 * v / safe, np.nan)
+
+
+def oracle_outs(G, tau, W, m, v, hyper, t):
+    """The oracle's fp64 (W', m', v') at the points of g_points (G first),
+    the update's interior extremum among them."""
+    gs = adamw_extremum(m, v, hyper)
+    pts = g_points(G, tau, extra=(np.where(np.isnan(gs), G, gs),))
+    return [O.adamw_f64(g, W, m, v, hyper, t) for g in pts]
 
 
 def check_step(gpu_w_bits, gpu_m, gpu_v, ref_inputs, hyper, t, fmt, bt, label=""):
@@ -119,18 +145,18 @@ def check_step(gpu_w_bits, gpu_m, gpu_v, ref_inputs, hyper, t, fmt, bt, label=""
     W = O.bf16_to_f64(ref_inputs["W_bits"])
     m0 = O.decode_moment(ref_inputs["m"], False)
     v0 = O.decode_moment(ref_inputs["v"], True)
-    lo, mid, hi = _oracle_range(G, tau, W, m0, v0, hyper, t)
+    outs = oracle_outs(G, tau, W, m0, v0, hyper, t)
     reports = {}
 
     # ---- W (bf16)
-    reports["W"] = check_w(gpu_w_bits, [lo[0], mid[0], hi[0]], W, label)
+    reports["W"] = check_w(gpu_w_bits, [x[0] for x in outs], W, label)
 
     # ---- moments
     if fmt == O.FMT_FP32:
         for which, idx, beta_term in (("m", 1, None), ("v", 2, None)):
-            ref = mid[idx]
+            ref = outs[0][idx]
             got = (gpu_m if which == "m" else gpu_v).data.astype(np.float64)
-            spread = np.maximum(np.abs(lo[idx] - ref), np.abs(hi[idx] - ref))
+            spread = np.max(np.stack([np.abs(x[idx] - ref) for x in outs]), axis=0)
             allow = 1e-5 * np.abs(ref) + spread + 1e-38
             err = np.abs(got - ref)
             nv = int(np.sum(err > allow))
@@ -138,16 +164,16 @@ def check_step(gpu_w_bits, gpu_m, gpu_v, ref_inputs, hyper, t, fmt, bt, label=""
             assert nv == 0, f"{label} {which}: {reports[which]}"
     elif fmt == O.FMT_BF16:
         for which, idx in (("m", 1), ("v", 2)):
-            rb = [bf16_ordered(O.f64_to_bf16(x[idx])) for x in (lo, mid, hi)]
+            rb = [bf16_ordered(O.f64_to_bf16(x[idx])) for x in outs]
             rlo, rhi = np.minimum.reduce(rb), np.maximum.reduce(rb)
             got = bf16_ordered((gpu_m if which == "m" else gpu_v).data)
             nv = int(np.sum((got < rlo - 1) | (got > rhi + 1)))
-            reports[which] = f"max ulp {int(np.max(np.abs(got - rb[1])))} violations={nv}"
+            reports[which] = f"max ulp {int(np.max(np.abs(got - rb[0])))} violations={nv}"
             assert nv == 0, f"{label} {which}: {reports[which]}"
     else:
         for which, idx in (("m", 1), ("v", 2)):
             second = which == "v"
-            encs = [O.encode_moment(O.FMT_INT8, x[idx], second) for x in (lo, mid, hi)]
+            encs = [O.encode_moment(O.FMT_INT8, x[idx], second) for x in outs]
             mom = gpu_m if which == "m" else gpu_v
             # scales: within 1e-5 relative of the oracle's range
             sc = np.stack([e.scale.astype(np.float64) for e in encs])
@@ -163,7 +189,7 @@ def check_step(gpu_w_bits, gpu_m, gpu_v, ref_inputs, hyper, t, fmt, bt, label=""
                 blk_nz = np.repeat(gs > 0, O.INT8_BLOCK, axis=1)
                 c_bad |= blk_nz & (gc < 1)
             reports[which] = (f"scale violations={int(s_bad.sum())} code violations={int(c_bad.sum())}"
-                              f" max code diff={int(np.max(np.abs(gc - cs[1])))}")
+                              f" max code diff={int(np.max(np.abs(gc - cs[0])))}")
             assert not s_bad.any() and not c_bad.any(), f"{label} {which}: {reports[which]}"
     return reports
 
@@ -189,7 +215,7 @@ def check_opt_step(gpu_w_bits, gpu_states, ref_inputs, opt, hyper, t, fmt, bt, l
     n = O.OPT_STATES[opt]
     st0 = [O.decode_moment(s, False) if i < n else None
            for i, s in enumerate(ref_inputs["states"])]
-    outs = [O.opt_f64(opt, G + d, W, st0[0], st0[1], hyper, t) for d in (-tau, 0.0 * tau, tau)]
+    outs = [O.opt_f64(opt, g, W, st0[0], st0[1], hyper, t) for g in g_points(G, tau)]
     mag = O.opt_f64(opt, np.abs(G) + tau, np.abs(W),
                     None if st0[0] is None else np.abs(st0[0]),
                     None if st0[1] is None else np.abs(st0[1]), hyper, t)
@@ -199,9 +225,9 @@ def check_opt_step(gpu_w_bits, gpu_states, ref_inputs, opt, hyper, t, fmt, bt, l
         idx = i + 1
         name = f"s{idx}"
         if fmt == O.FMT_FP32:
-            ref = outs[1][idx]
+            ref = outs[0][idx]
             got = gpu_states[i].data.astype(np.float64)
-            spread = np.maximum(np.abs(outs[0][idx] - ref), np.abs(outs[2][idx] - ref))
+            spread = np.max(np.stack([np.abs(x[idx] - ref) for x in outs]), axis=0)
             err = np.abs(got - ref)
             scale = np.maximum(np.abs(ref), np.abs(mag[idx]))
             nv = int(np.sum(err > 1e-5 * scale + spread + 1e-38))
@@ -211,6 +237,6 @@ def check_opt_step(gpu_w_bits, gpu_states, ref_inputs, opt, hyper, t, fmt, bt, l
             rlo, rhi = np.minimum.reduce(rb), np.maximum.reduce(rb)
             got = bf16_ordered(gpu_states[i].data)
             nv = int(np.sum((got < rlo - 1) | (got > rhi + 1)))
-            reports[name] = f"max ulp {int(np.max(np.abs(got - rb[1])))} violations={nv}"
+            reports[name] = f"max ulp {int(np.max(np.abs(got - rb[0])))} violations={nv}"
         assert nv == 0, f"{label} {name}: {reports[name]}"
     return reports

@@ -31,7 +31,7 @@ from weight_gradient_gemm_gb300.inputs import (LLAMA31_8B_SHAPES, bf16_bits, bit
                                                make_step_inputs)
 
 from .gpu_util import DEV, hyper_kwargs, require_gpu
-from .parity import check_w, tau_bound
+from .parity import check_w, oracle_outs, tau_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -80,19 +80,21 @@ def random_state(d_out, d_in, seed, m_std=1e-4, r_hi=1e-4):
 
 
 def oracle_range(x_bits, dy_bits, w_bits, st: Fp8State, t, bt, rows=None):
-    """The oracle's fp64 AdamW results at G - tau, G, G + tau for the state."""
+    """The oracle's fp64 AdamW results over G +- tau for the state (at G
+    first; tests/parity.py's oracle_outs)."""
     G = O.wgrad(x_bits, dy_bits, rows)
     tau = tau_bound(O.wgrad_abs(x_bits, dy_bits, rows), bt)
     W = O.bf16_to_f64(w_bits)
     sel = slice(None) if rows is None else rows
     m = O.decode_fp8(st.m_codes[sel], st.m_read)
     r = O.decode_fp8(st.r_codes[sel], st.r_read)
-    return [O.adamw_f64(G + d, W, m, r * r, HYPER, t) for d in (-tau, 0.0 * tau, tau)]
+    return oracle_outs(G, tau, W, m, r * r, HYPER, t)
 
 
 def check_fp8(gpu_w, gpu_m, gpu_r, outs, st: Fp8State, w0_bits, label, amax=None):
     """Compare one GPU step (W bits, m and r codes, optionally the amax pair)
-    with the oracle's results over G +- tau (`outs` from oracle_range), W
+    with the oracle's results over G +- tau (`outs` from oracle_range, at G
+    first), W
     under tests/parity.py's check_w; w0_bits: W before the step."""
     rep = {"W": str(check_w(gpu_w, [o[0] for o in outs], O.bf16_to_f64(w0_bits), label))}
     for which, codes, scale in (("m", gpu_m, st.m_write), ("r", gpu_r, st.r_write)):
@@ -101,8 +103,8 @@ def check_fp8(gpu_w, gpu_m, gpu_r, outs, st: Fp8State, w0_bits, label, amax=None
         clo, chi = np.minimum.reduce(cs), np.maximum.reduce(cs)
         gc = e4m3_ordered(codes)
         bad = (gc < clo - 1) | (gc > chi + 1)
-        rep[which] = (f"max code diff {int(np.max(np.abs(gc - cs[1])))}, "
-                      f"exact {100.0 * np.mean(gc == cs[1]):.3f}%")
+        rep[which] = (f"max code diff {int(np.max(np.abs(gc - cs[0])))}, "
+                      f"exact {100.0 * np.mean(gc == cs[0]):.3f}%")
         assert not bad.any(), f"{label} {which} codes: {int(bad.sum())} beyond one level"
         if amax is not None:
             mags = np.stack([np.abs(x) for x in vals])

@@ -49,8 +49,9 @@ def _layers(seed, bt, states, sdtype=torch.float32, shapes=SHAPES):
 
 
 def _clone(layers):
-    return [{k: (v.clone() if k in ("W", "s1", "s2", "B", "m", "v", "m_scale", "v_scale", "dX")
-                 else v) for k, v in ly.items()} for ly in layers]
+    mutable = ("W", "s1", "s2", "B", "m", "v", "m_scale", "v_scale", "dX")
+    return [{k: (v.clone() if k in mutable and v is not None else v) for k, v in ly.items()}
+            for ly in layers]
 
 
 @pytest.mark.parametrize("bt", [200, 1000])

@@ -57,9 +57,13 @@ __global__ void __launch_bounds__(256) adamw_vec8_kernel(const void* __restrict_
       vv[0] = v0.x; vv[1] = v0.y; vv[2] = v0.z; vv[3] = v0.w;
       vv[4] = v1.x; vv[5] = v1.y; vv[6] = v1.z; vv[7] = v1.w;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        float r;
-        adamw_elem(g[k], w[k], mm[k], vv[k], r, h);
+      for (int k = 0; k < 8; k += 2) {
+        float2 w2 = make_float2(w[k], w[k + 1]), m2 = make_float2(mm[k], mm[k + 1]);
+        float2 v2 = make_float2(vv[k], vv[k + 1]), r2;
+        adamw_elem2(make_float2(g[k], g[k + 1]), w2, m2, v2, r2, h);
+        w[k] = w2.x; w[k + 1] = w2.y;
+        mm[k] = m2.x; mm[k + 1] = m2.y;
+        vv[k] = v2.x; vv[k + 1] = v2.y;
       }
       __stcs(mp, make_float4(mm[0], mm[1], mm[2], mm[3]));
       __stcs(mp + 1, make_float4(mm[4], mm[5], mm[6], mm[7]));
@@ -77,9 +81,13 @@ __global__ void __launch_bounds__(256) adamw_vec8_kernel(const void* __restrict_
         vv[2 * k] = bf16_lo(vu[k]); vv[2 * k + 1] = bf16_hi(vu[k]);
       }
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        float r;
-        adamw_elem(g[k], w[k], mm[k], vv[k], r, h);
+      for (int k = 0; k < 8; k += 2) {
+        float2 w2 = make_float2(w[k], w[k + 1]), m2 = make_float2(mm[k], mm[k + 1]);
+        float2 v2 = make_float2(vv[k], vv[k + 1]), r2;
+        adamw_elem2(make_float2(g[k], g[k + 1]), w2, m2, v2, r2, h);
+        w[k] = w2.x; w[k + 1] = w2.y;
+        mm[k] = m2.x; mm[k + 1] = m2.y;
+        vv[k] = v2.x; vv[k + 1] = v2.y;
       }
       __stcs(mp, make_uint4(pack_bf16x2(mm[0], mm[1]), pack_bf16x2(mm[2], mm[3]),
                             pack_bf16x2(mm[4], mm[5]), pack_bf16x2(mm[6], mm[7])));
@@ -130,10 +138,15 @@ __global__ void __launch_bounds__(256) adamw_int8_kernel(const void* __restrict_
     }
     float amax_m = 0.0f, amax_r = 0.0f;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      adamw_elem(g[k], w[k], mm[k], vv[k], rr[k], h);
-      amax_m = fmaxf(amax_m, fabsf(mm[k]));
-      amax_r = fmaxf(amax_r, rr[k]);
+    for (int k = 0; k < 4; k += 2) {
+      float2 w2 = make_float2(w[k], w[k + 1]), m2 = make_float2(mm[k], mm[k + 1]);
+      float2 v2 = make_float2(vv[k], vv[k + 1]), r2;
+      adamw_elem2(make_float2(g[k], g[k + 1]), w2, m2, v2, r2, h);
+      w[k] = w2.x; w[k + 1] = w2.y;
+      mm[k] = m2.x; mm[k + 1] = m2.y;
+      rr[k] = r2.x; rr[k + 1] = r2.y;
+      amax_m = fmaxf(amax_m, fmaxf(fabsf(mm[k]), fabsf(mm[k + 1])));
+      amax_r = fmaxf(amax_r, fmaxf(rr[k], rr[k + 1]));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {

@@ -307,9 +307,13 @@ __device__ __forceinline__ void epi_slice_fused_16(uint32_t taddr, bool zero_gra
     }
   }
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    float r;
-    adamw_elem(g[i], w[i], m[i], v[i], r, hc);
+  for (int i = 0; i < 16; i += 2) {
+    float2 w2 = make_float2(w[i], w[i + 1]), m2 = make_float2(m[i], m[i + 1]);
+    float2 v2 = make_float2(v[i], v[i + 1]), r2;
+    adamw_elem2(make_float2(g[i], g[i + 1]), w2, m2, v2, r2, hc);
+    w[i] = w2.x; w[i + 1] = w2.y;
+    m[i] = m2.x; m[i + 1] = m2.y;
+    v[i] = v2.x; v[i + 1] = v2.y;
   }
   uint32_t wo[8];
   if (sr) {
@@ -433,11 +437,13 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, uint32_t sadd
       float w0 = bf16_lo(wu[i]), w1 = bf16_hi(wu[i]);
       float g0 = zero_grad ? 0.0f : __uint_as_float(graw[2 * i]);
       float g1 = zero_grad ? 0.0f : __uint_as_float(graw[2 * i + 1]);
-      float m0 = dequant_m(qm[2 * i], sm_old), m1 = dequant_m(qm[2 * i + 1], sm_old);
-      float v0 = dequant_v(qv[2 * i], sv_old), v1 = dequant_v(qv[2 * i + 1], sv_old);
-      float r0, r1;
-      adamw_elem(g0, w0, m0, v0, r0, hc);
-      adamw_elem(g1, w1, m1, v1, r1, hc);
+      float2 w2 = make_float2(w0, w1);
+      float2 m2 = make_float2(dequant_m(qm[2 * i], sm_old), dequant_m(qm[2 * i + 1], sm_old));
+      float2 v2 = make_float2(dequant_v(qv[2 * i], sv_old), dequant_v(qv[2 * i + 1], sv_old));
+      float2 r2;
+      adamw_elem2(make_float2(g0, g1), w2, m2, v2, r2, hc);
+      w0 = w2.x; w1 = w2.y;
+      const float m0 = m2.x, m1 = m2.y, r0 = r2.x, r1 = r2.y;
       amax_m = fmaxf(amax_m, fmaxf(fabsf(m0), fabsf(m1)));
       amax_r = fmaxf(amax_r, fmaxf(r0, r1));
       wo[i] = pack_bf16x2(w0, w1);
@@ -491,12 +497,18 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, uint32_t sadd
       load_codes32(mbox, row, 4 * h + 2 * c, qm);
       load_codes32(vbox, row, 4 * h + 2 * c, qv);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        float g = zero_grad ? 0.0f : __uint_as_float(graw[i]);
-        float w = 0.0f, m = dequant_m(qm[i], sm_old), v = dequant_v(qv[i], sv_old), r;
-        adamw_elem(g, w, m, v, r, hc);
-        qm[i] = quant_m_code(m, inv_m);
-        qv[i] = quant_r_code(r, inv_r, r_nz);
+      for (int i = 0; i < 32; i += 2) {
+        const float2 g = zero_grad ? make_float2(0.0f, 0.0f)
+                                   : make_float2(__uint_as_float(graw[i]),
+                                                 __uint_as_float(graw[i + 1]));
+        float2 w = make_float2(0.0f, 0.0f), r;
+        float2 m = make_float2(dequant_m(qm[i], sm_old), dequant_m(qm[i + 1], sm_old));
+        float2 v = make_float2(dequant_v(qv[i], sv_old), dequant_v(qv[i + 1], sv_old));
+        adamw_elem2(g, w, m, v, r, hc);
+        qm[i] = quant_m_code(m.x, inv_m);
+        qm[i + 1] = quant_m_code(m.y, inv_m);
+        qv[i] = quant_r_code(r.x, inv_r, r_nz);
+        qv[i + 1] = quant_r_code(r.y, inv_r, r_nz);
       }
     }
     store_codes32(mbox, row, 4 * h + 2 * c, qm);

@@ -57,6 +57,46 @@ __device__ __forceinline__ void adamw_elem(float g, float& w, float& m, float& v
   r = r1;
 }
 
+// Paired fp32 arithmetic (PTX mul/fma .rn.f32x2, sm_100 and later): each
+// lane is an IEEE round-to-nearest multiply or fused multiply-add, so the
+// results are those of __fmul_rn / __fmaf_rn bit for bit, in half the
+// instructions.
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 d;
+  asm("{.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 dup2(float x) { return make_float2(x, x); }
+
+// adamw_elem on two elements at once: the same operations in the same order
+// on each lane (paired multiplies and multiply-adds), so each lane's results
+// equal adamw_elem's bit for bit.
+__device__ __forceinline__ void adamw_elem2(float2 g, float2& w, float2& m, float2& v,
+                                            float2& r, const AdamWConsts& c) {
+  const float2 m1 = fma2(dup2(c.beta1), m, mul2(dup2(c.omb1), g));
+  const float2 v1 = fma2(dup2(c.beta2), v, mul2(dup2(c.omb2), mul2(g, g)));
+  const float2 r1 = make_float2(sqrt_approx(v1.x), sqrt_approx(v1.y));
+  const float2 den = fma2(r1, dup2(c.inv_sqrt_bc2), dup2(c.eps));
+  const float2 upd = mul2(m1, make_float2(rcp_approx(den.x), rcp_approx(den.y)));
+  w = fma2(dup2(c.neg_step_size), upd, mul2(w, dup2(c.decay)));
+  m = m1;
+  v = v1;
+  r = r1;
+}
+
 // ---------------------------------------------------------------------------
 // The other coordinate-wise optimizers FORGE fuses (the page's regime 1):
 // SGD, SGD with momentum, Adagrad and RMSprop (PyTorch's definitions with
@@ -257,18 +297,19 @@ __device__ __forceinline__ void adamw_fp8_x16(const float (&g)[16], float (&w)[1
       const float2 m2 = e4m3x2_to_float2(mw[k] >> (16 * half));
       const float2 r2 = e4m3x2_to_float2(rw[k] >> (16 * half));
       const int i = 4 * k + 2 * half;
-      float m0 = __fmul_rn(m2.x, fm.read), m1 = __fmul_rn(m2.y, fm.read);
-      const float q0 = __fmul_rn(r2.x, fr.read), q1 = __fmul_rn(r2.y, fr.read);
-      float v0 = __fmul_rn(q0, q0), v1 = __fmul_rn(q1, q1);
-      float r0, r1;
-      adamw_elem(g[i], w[i], m0, v0, r0, h);
-      adamw_elem(g[i + 1], w[i + 1], m1, v1, r1, h);
-      amax_m = fmaxf(amax_m, fmaxf(fabsf(m0), fabsf(m1)));
-      amax_r = fmaxf(amax_r, fmaxf(r0, r1));
-      mpack |= float2_to_e4m3x2(__fmul_rn(m0, fm.inv_write), __fmul_rn(m1, fm.inv_write))
-               << (16 * half);
-      rpack |= float2_to_e4m3x2(__fmul_rn(r0, fr.inv_write), __fmul_rn(r1, fr.inv_write))
-               << (16 * half);
+      float2 mm = mul2(m2, dup2(fm.read));
+      const float2 q = mul2(r2, dup2(fr.read));
+      float2 vv = mul2(q, q);
+      float2 ww = make_float2(w[i], w[i + 1]), rr;
+      adamw_elem2(make_float2(g[i], g[i + 1]), ww, mm, vv, rr, h);
+      w[i] = ww.x;
+      w[i + 1] = ww.y;
+      amax_m = fmaxf(amax_m, fmaxf(fabsf(mm.x), fabsf(mm.y)));
+      amax_r = fmaxf(amax_r, fmaxf(rr.x, rr.y));
+      const float2 me = mul2(mm, dup2(fm.inv_write));
+      const float2 re = mul2(rr, dup2(fr.inv_write));
+      mpack |= float2_to_e4m3x2(me.x, me.y) << (16 * half);
+      rpack |= float2_to_e4m3x2(re.x, re.y) << (16 * half);
     }
     mo[k] = mpack;
     ro[k] = rpack;

@@ -510,6 +510,14 @@ def run_gpu(args, rank, world, dev):
         stage_inputs(0, 0)
         torch.cuda.synchronize()
         h2d_ms.append(cp_ev[0][0].elapsed_time(cp_ev[0][1]))
+    # each step's result read back: 4 bytes of the first projection's new W,
+    # copied asynchronously into pinned memory after the step; the host reads
+    # step k-1's while step k runs (a training loop's double-buffered readback),
+    # and the library's status word is checked once at the end
+    res_host = [torch.empty(2, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    res_ev = [torch.cuda.Event(), torch.cuda.Event()]
+    w_first = layer.group[0]["W"].view(-1)
+    checked = []
     barrier()
     torch.cuda.synchronize()
     for ev in consumed:
@@ -527,13 +535,23 @@ def run_gpu(args, rank, world, dev):
             F.fp8_roll_scales(layer.fp8_scales, FP8_HEADROOM, stream=stream)
         st_ev[k][1].record(stream)
         consumed[b].record(stream)
+        with torch.cuda.stream(stream):
+            res_host[b].copy_(w_first[:2], non_blocking=True)
+        res_ev[b].record(stream)
         if k + 1 < e2e_steps:         # issued while step k runs
             stage_inputs(1 - b, k + 1)
-        st = F.device_error(stream)   # synchronises the step's stream, reads 4 bytes
-        if st != 0:
-            raise RuntimeError(F.status_string(st))
+        if k >= 1:                    # step k-1's result, while step k runs
+            res_ev[1 - b].synchronize()
+            checked.append(bool(torch.isfinite(res_host[1 - b].float()).all()))
         if k == 0:
+            res_ev[0].synchronize()
+            checked.append(bool(torch.isfinite(res_host[0].float()).all()))
             e_first = time.perf_counter()
+    res_ev[(e2e_steps - 1) & 1].synchronize()
+    checked.append(bool(torch.isfinite(res_host[(e2e_steps - 1) & 1].float()).all()))
+    st = F.device_error(stream)
+    if st != 0 or not all(checked):
+        raise RuntimeError(f"e2e: {F.status_string(st)}, finite results {all(checked)}")
     e1 = time.perf_counter()
     torch.cuda.synchronize()
     e2e_ms = (e1 - e0) * 1e3 / e2e_steps
@@ -796,6 +814,8 @@ def timed_launches(fn, n, stream):
 
 # (block name, workload it measures, BT, moment format, spike fraction)
 TENSOR_BLOCKS = [
+    ("c3_bt512_bf16", "llama31_8b_layer_bt512_bf16", 512, 1, 0.01),
+    ("int8_bt512", "llama31_8b_layer_bt512_int8", 512, 2, 0.0),
     ("fp8_bt512", "llama31_8b_layer_bt512_fp8", 512, 3, 0.0),
     ("c3_bt2048_bf16", "llama31_8b_layer_bt2048_bf16", 2048, 1, 0.01),
     ("c4_bt4096_int8", "llama31_8b_layer_bt4096_int8", 4096, 2, 0.0),

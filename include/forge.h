@@ -45,7 +45,9 @@
  * (accumulator width on one CTA), FORGE_GROUP_M=1..64 (tile rows per raster
  * group), FORGE_POLL_STORE=0|1 (the store lanes poll for finished state
  * slots), FORGE_SPLITS=1..8 (forge_dgrad: k-ranges per tile),
- * FORGE_L2_HINTS=0..3 (L2 eviction hints of the state stream).  Every choice
+ * FORGE_L2_HINTS=0..3 (L2 eviction hints of the state stream),
+ * FORGE_STATE_PREFETCH=0..32 (L2 prefetch distance of the state stream, in
+ * slices).  Every choice
  * computes the same step to the same accuracy; only the speed differs.
  *
  * Errors.  Argument errors are returned synchronously, before anything is
@@ -525,6 +527,8 @@ typedef struct {
   int l2_hints;    /* -1 automatic; 0..3: bit 0 marks the optimizer state's
                       stores evict-first in L2, bit 1 its m, v loads whose rows
                       are whole 128-byte lines                                  */
+  int state_prefetch; /* -1 automatic; 0..32: the state loader prefetches into L2
+                         the boxes this many state slices ahead (0: none)         */
 } forge_tuning;
 
 /* Replace the tuning overrides (NULL: everything automatic).  Applies to

@@ -334,10 +334,11 @@ def test_binding_refuses_host_tensors():
 
 
 def test_tuning_round_trip_without_gpu(L, tune):
-    tune(profile="deep", cg=2, bn=256, group_m=8, poll_store=0, splits=3, l2_hints=1)
+    tune(profile="deep", cg=2, bn=256, group_m=8, poll_store=0, splits=3, l2_hints=1,
+         state_prefetch=4)
     t = F.get_tuning()
     assert t == dict(profile="deep", cg=2, bn=256, group_m=8, poll_store=0, splits=3,
-                     l2_hints=1)
+                     l2_hints=1, state_prefetch=4)
     # the override reaches the host's configuration choice
     assert "profile=deep" in F.describe_config(512, 4096, 4096, F.MOM_FP32)
     assert "group_m=8" in F.describe_config(512, 4096, 4096, F.MOM_FP32)
@@ -346,7 +347,7 @@ def test_tuning_round_trip_without_gpu(L, tune):
     assert F.get_tuning()["profile"] == "deep"
     F.set_tuning()
     assert F.get_tuning() == dict(profile="auto", cg=0, bn=0, group_m=0, poll_store=-1,
-                                  splits=0, l2_hints=-1)
+                                  splits=0, l2_hints=-1, state_prefetch=-1)
     with pytest.raises(ValueError):
         F.set_tuning(profile="fast")
 

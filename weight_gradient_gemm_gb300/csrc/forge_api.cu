@@ -438,10 +438,10 @@ GemmConfig choose_opt_config(int64_t bt, int fmt, int nstate) {
 // changes them.  Reading the environment on every call would cost host time
 // per launch and race with setenv in other threads.
 std::once_flag g_tune_once;
-forge_tuning g_tune = {FORGE_PROFILE_AUTO, 0, 0, 0, -1, 0, -1};
+forge_tuning g_tune = {FORGE_PROFILE_AUTO, 0, 0, 0, -1, 0, -1, -1};
 
 void tuning_from_env() {
-  forge_tuning t = {FORGE_PROFILE_AUTO, 0, 0, 0, -1, 0, -1};
+  forge_tuning t = {FORGE_PROFILE_AUTO, 0, 0, 0, -1, 0, -1, -1};
   if (const char* e = std::getenv("FORGE_PROFILE")) {
     if (std::strcmp(e, "stream") == 0) t.profile = FORGE_PROFILE_STREAM;
     if (std::strcmp(e, "mma") == 0) t.profile = FORGE_PROFILE_MMA;
@@ -454,6 +454,7 @@ void tuning_from_env() {
   if (const char* e = std::getenv("FORGE_POLL_STORE")) t.poll_store = std::atoi(e) != 0;
   if (const char* e = std::getenv("FORGE_SPLITS")) t.splits = std::atoi(e);
   if (const char* e = std::getenv("FORGE_L2_HINTS")) t.l2_hints = std::atoi(e);
+  if (const char* e = std::getenv("FORGE_STATE_PREFETCH")) t.state_prefetch = std::atoi(e);
   std::lock_guard<std::mutex> lk(g_mu);
   g_tune = t;
 }
@@ -514,6 +515,8 @@ GemmConfig finish_config(GemmConfig c, int64_t bt, int fmt, int mode) {
   if (tu.group_m >= 1 && tu.group_m <= 64) c.group_m = tu.group_m;
   c.l2_hints = 0;
   if (tu.l2_hints >= 0 && tu.l2_hints <= 3) c.l2_hints = tu.l2_hints;
+  c.state_prefetch = 0;
+  if (tu.state_prefetch >= 0 && tu.state_prefetch <= 32) c.state_prefetch = tu.state_prefetch;
   c.grid = 0;
   c.splits = 1;
   return c;
@@ -589,6 +592,7 @@ GemmParams base_params(int64_t bt, const GemmConfig& cfg, const DeviceInfo& d) {
   p.timeout_ns = g_wait_limit_ns;
   p.poll_store = cfg.poll_store;
   p.l2_hints = cfg.l2_hints;
+  p.state_prefetch = cfg.state_prefetch;
   p.splits = 1;
   return p;
 }
@@ -1474,7 +1478,7 @@ forge_status forge_fp8_roll_scales(forge_fp8_scales* scales, int n, float headro
 
 void forge_set_tuning(const forge_tuning* t) {
   std::call_once(g_tune_once, tuning_from_env);   // a later first read must not undo this
-  const forge_tuning automatic = {FORGE_PROFILE_AUTO, 0, 0, 0, -1, 0, -1};
+  const forge_tuning automatic = {FORGE_PROFILE_AUTO, 0, 0, 0, -1, 0, -1, -1};
   std::lock_guard<std::mutex> lk(g_mu);
   g_tune = t ? *t : automatic;
 }

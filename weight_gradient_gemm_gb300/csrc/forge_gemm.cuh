@@ -942,6 +942,30 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll
       for (int j = 0; j < T::NS; ++j) last_armed[j] = -1;
       bool ok = true;
+      // L2 prefetch of the state boxes `state_prefetch` slices ahead, so that
+      // a slot's load finds them in L2 and the slot ring turns over faster
+      // than DRAM latency would let it
+      auto prefetch_ahead = [&](uint32_t c) {
+        const int tt = unit0 + static_cast<int>(c / T::SLICES) * units;
+        if (tt >= p.num_units) return;
+        const int sp = static_cast<int>(c % T::SLICES);
+        int tm2, tn2;
+        const int pi2 = tile_coords(tile_of(tt), p, tm2, tn2);
+        const GemmProblem& q2 = p.prob[pi2];
+        const int x = tn2 * BN + (sp / T::PARTS) * T::SW;
+        const int y = tm2 * T::TM + static_cast<int>(rank) * kBM + (sp % T::PARTS) * T::RPS;
+        if (x >= q2.d_in || y >= q2.d_out) return;
+        const GemmMaps& m2 = a.maps[pi2];
+        tma_prefetch_l2_2d(&m2.w, x, y);
+        if constexpr (T::Q8) tma_prefetch_l2_2d(&m2.w, x + 64, y);
+        const int nst2 = (MODE == kModeOpt) ? p.nstate : (MODE == kModeAccum ? 0 : 2);
+        if (nst2 >= 1) tma_prefetch_l2_2d(&m2.m, x, y);
+        if (nst2 >= 2) tma_prefetch_l2_2d(&m2.v, x, y);
+      };
+      const uint32_t pf = static_cast<uint32_t>(p.state_prefetch);
+      const bool do_pf = pf > 0 && !(MODE == kModeAccum && !p.accum_load);
+      if (do_pf)
+        for (uint32_t c = 0; c < pf; ++c) prefetch_ahead(c);
       for (int t = unit0; ok && t < p.num_units; t += units) {
         int tm, tn;
         const int pi = tile_coords(tile_of(t), p, tm, tn);
@@ -950,6 +974,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         for (int s = 0; s < T::SLICES; ++s, ++cnt) {
           const int j = cnt % T::NS;
           const uint32_t ph = (cnt / T::NS) & 1u;
+          if (do_pf) prefetch_ahead(cnt + pf);
           if (!wait_bounded(bar_sempty(j), ph ^ 1u, wc, kSiteLoaderEmpty)) { ok = false; break; }
           const int x0 = tn * BN + (s / T::PARTS) * T::SW;
           const int y0 = tm * T::TM + static_cast<int>(rank) * kBM + (s % T::PARTS) * T::RPS;

@@ -94,6 +94,9 @@ struct GemmParams {
   // evict-first; bit 1, loads of m and v boxes with whole 128-byte rows (fp32,
   // 8-bit codes) are marked evict-first
   int32_t l2_hints;
+  // the state loader prefetches into L2 the boxes of the slice this many
+  // slices ahead of the one it loads (0: no prefetch)
+  int32_t state_prefetch;
 };
 
 struct GemmMaps {
@@ -117,6 +120,7 @@ struct GemmConfig {
   int poll_store;  // store lanes poll the slot-done barrier instead of suspending
   int splits;      // input gradient: k-ranges per tile (GemmParams::splits); 1 elsewhere
   int l2_hints;    // GemmParams::l2_hints
+  int state_prefetch;  // GemmParams::state_prefetch
 };
 
 // Tokens per operand pipeline stage (the TMA box height of dY and X), used

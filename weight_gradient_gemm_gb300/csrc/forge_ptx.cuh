@@ -83,6 +83,14 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
 }
 // 2-D tiled load of one box into shared memory; completion is signalled as
 // transaction bytes on `bar`.  x is the inner (contiguous) coordinate.
+// Prefetch one box of a 2-D tensor map into L2 (no shared memory, no barrier:
+// a hint the memory system may drop).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(x), "r"(y)
+               : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, int32_t x,
                                             int32_t y, uint32_t bar, uint64_t policy) {
   asm volatile(

@@ -74,7 +74,8 @@ PROFILES = {"auto": -1, "stream": 0, "mma": 1, "balanced": 2, "deep": 3}
 
 class ForgeTuning(ctypes.Structure):
     _fields_ = [(k, ctypes.c_int) for k in ("profile", "cta_group", "bn", "group_m",
-                                            "poll_store", "splits", "l2_hints")]
+                                            "poll_store", "splits", "l2_hints",
+                                            "state_prefetch")]
 
 
 _lock = threading.Lock()
@@ -503,19 +504,20 @@ def get_tuning() -> dict:
     names = {v: k for k, v in PROFILES.items()}
     return dict(profile=names.get(t.profile, "auto"), cg=t.cta_group, bn=t.bn,
                 group_m=t.group_m, poll_store=t.poll_store, splits=t.splits,
-                l2_hints=t.l2_hints)
+                l2_hints=t.l2_hints, state_prefetch=t.state_prefetch)
 
 
 def set_tuning(profile: str = "auto", cg: int = 0, bn: int = 0, group_m: int = 0,
-               poll_store: int = -1, splits: int = 0, l2_hints: int = -1) -> None:
+               poll_store: int = -1, splits: int = 0, l2_hints: int = -1,
+               state_prefetch: int = -1) -> None:
     """Replace the tuning overrides (the defaults leave every choice to the
     library).  profile: auto|stream|balanced|mma|deep; cg: 1 or 2 CTAs per
     tile; bn: 128 or 256; group_m: 1..64; poll_store: 0 or 1; splits: 1..8;
-    l2_hints: 0..3."""
+    l2_hints: 0..3; state_prefetch: 0..32 slices."""
     if profile not in PROFILES:
         raise ValueError(f"unknown profile {profile}")
     t = ForgeTuning(PROFILES[profile], int(cg), int(bn), int(group_m), int(poll_store),
-                    int(splits), int(l2_hints))
+                    int(splits), int(l2_hints), int(state_prefetch))
     lib().forge_set_tuning(ctypes.byref(t))
 
 

@@ -313,3 +313,29 @@ def test_raster_group_sizes(group_m, cg, tune):
         check_step(bf16_bits(d["W"].cpu()), mom_from_dev(fmt, d["m"], None),
                    mom_from_dev(fmt, d["v"], None), ref, TINY, 2, fmt, bt,
                    label=f"group_m={group_m} cg={cg}")
+
+
+@pytest.mark.parametrize("fmt,bt,cfg", [
+    (O.FMT_FP32, 4096, ("deep", 256, 2)),     # the configuration that prefetches by default
+    (O.FMT_BF16, 1000, ("balanced", 256, 2)),
+    (O.FMT_INT8, 300, ("balanced", 128, 1)),  # 8-bit slices: two W boxes per slot
+], ids=["fp32-deep-pair", "bf16-balanced-pair", "int8-balanced-cta"])
+def test_state_prefetch_changes_no_bits(fmt, bt, cfg, tune):
+    # the state loader's L2 prefetch is a hint: with any distance the step is
+    # bit for bit the step without it (which the other tests hold to the oracle)
+    d_out, d_in = 520, 1024
+    s = make_step_inputs(60, 0, 1, bt, d_in, d_out, dy_std=1e-3, with_w=True)
+    tune(profile=cfg[0], bn=cfg[1], cg=cfg[2])
+    outs = []
+    for pf in (0, 3, 16):
+        tune(state_prefetch=pf)
+        m, v, ms, vs = F.alloc_moments(d_out, d_in, fmt, DEV)
+        W = s.w.to(DEV)
+        F.wgrad_adamw(s.x.to(DEV), s.dy.to(DEV), W, m, v, step=2, m_scale=ms, v_scale=vs,
+                      **hyper_kwargs(TINY))
+        assert F.device_error() == 0
+        outs.append([t.contiguous().view(torch.uint8).cpu() for t in (W, m, v, ms, vs)
+                     if t is not None])
+    for other in outs[1:]:
+        for a, b in zip(outs[0], other):
+            assert torch.equal(a, b)

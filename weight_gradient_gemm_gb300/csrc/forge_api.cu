@@ -34,6 +34,7 @@ cudaError_t launch_gemm_store_bf16(const GemmConfig&, const GemmArgs&, cudaStrea
 cudaError_t launch_gemm_dgrad(const GemmConfig&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_opt_f32(const GemmConfig&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_opt_bf16(const GemmConfig&, const GemmArgs&, cudaStream_t);
+cudaError_t launch_gemm_opt_none(const GemmConfig&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_accum(const GemmConfig&, const GemmArgs&, cudaStream_t);
 
 cudaError_t launch_gemm(int mode, int fmt, const GemmConfig& cfg, const GemmArgs& args,
@@ -58,6 +59,7 @@ cudaError_t launch_gemm(int mode, int fmt, const GemmConfig& cfg, const GemmArgs
     switch (fmt) {
       case kFmtF32: return launch_gemm_opt_f32(cfg, args, stream);
       case kFmtBF16: return launch_gemm_opt_bf16(cfg, args, stream);
+      case kFmtNone: return launch_gemm_opt_none(cfg, args, stream);
     }
   }
   return cudaErrorInvalidValue;
@@ -416,10 +418,11 @@ GemmConfig choose_opt_config(int64_t bt, int fmt, int nstate) {
     c.cg = 1;
     c.prof = kProfBalanced;
     if (nstate == 0) {
-      // SGD carries no state: two operand stages and 256-wide tiles, which
-      // halve the A re-reads of its main-loop-bound step (512 tokens: 0.41 ->
-      // 0.48 of HBM over the layer)
-      c.prof = kProfStream;
+      // SGD carries no state: its slots hold W alone (8 KB), so the balanced
+      // profile with 256-wide tiles keeps four operand stages beside four
+      // slots for its main-loop-bound step (512 tokens: 0.41 of HBM with
+      // AdamW's slot layout, 0.59 now)
+      c.prof = kProfBalanced;
       c = finish_config(c, bt, fmt, kModeFused);
       if (current_tuning().bn != 128) c.bn = 256;
       return c;
@@ -1199,7 +1202,8 @@ forge_status forge_wgrad_opt_grouped(const forge_linear* layers, int n, int64_t 
   s = device_info(&d);
   if (s != FORGE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int ifmt = fmt == FORGE_MOM_FP32 ? kFmtF32 : kFmtBF16;
+  // an optimizer without state runs with W-only slots, whatever the format
+  const int ifmt = ns == 0 ? kFmtNone : (fmt == FORGE_MOM_FP32 ? kFmtF32 : kFmtBF16);
   GemmConfig cfg = choose_opt_config(bt, ifmt, ns);
   const bool f32 = fmt == FORGE_MOM_FP32;
   const CUtensorMapDataType mdt =

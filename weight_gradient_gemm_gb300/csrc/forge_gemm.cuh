@@ -68,7 +68,8 @@ struct GemmTraits {
   static constexpr int W_ELEM =
       ((MODE == kModeStoreG || MODE == kModeAccum) && FMT == kFmtF32) ? 4 : 2;
   static constexpr int MOM_ELEM =
-      !has_state(MODE) ? 0 : (FMT == kFmtF32 ? 4 : (FMT == kFmtBF16 ? 2 : 1));
+      (!has_state(MODE) || FMT == kFmtNone) ? 0
+                                            : (FMT == kFmtF32 ? 4 : (FMT == kFmtBF16 ? 2 : 1));
   // 8-bit moments (int8 blocks or fp8): 128-column slices whose W is two
   // 64-column boxes
   static constexpr bool Q8 = (MODE == kModeFused && (FMT == kFmtI8 || FMT == kFmtF8));
@@ -665,11 +666,16 @@ __device__ __forceinline__ void epi_slice_opt(uint32_t taddr, bool zero_grad, ui
   if constexpr (NST >= 1) state_st16<FMT>(slot + kWBytes, row, h, s1);
   if constexpr (NST >= 2) state_st16<FMT>(slot + kWBytes + kMBytes, row, h, s2);
 }
-// Dispatch on the launch's optimizer (uniform across the grid).
+// Dispatch on the launch's optimizer (uniform across the grid); stateless
+// slots (kFmtNone) only ever run SGD.
 template <int FMT, int RPS>
 __device__ __forceinline__ void epi_slice_opt_any(const OptConsts& oc, uint32_t taddr,
                                                   bool zero_grad, uint8_t* slot, uint32_t row,
                                                   int h) {
+  if constexpr (FMT == kFmtNone) {
+    epi_slice_opt<FMT, RPS, kOptSgd>(taddr, zero_grad, slot, row, h, oc);
+    return;
+  }
   switch (oc.opt) {
     case kOptSgd: epi_slice_opt<FMT, RPS, kOptSgd>(taddr, zero_grad, slot, row, h, oc); break;
     case kOptSgdMomentum:

@@ -43,8 +43,9 @@ __host__ __device__ constexpr bool has_state(int mode) {
 // half-tile state slots.
 enum Prof : int { kProfStream = 0, kProfMma = 1, kProfBalanced = 2, kProfDeep = 3 };
 // Epilogue formats: fused moment formats 0..3 (fp32, bf16, int8 blocks of
-// 128, fp8 e4m3 with per-tensor scales); store-G dW formats 0..1 (fp32, bf16).
-enum Fmt : int { kFmtF32 = 0, kFmtBF16 = 1, kFmtI8 = 2, kFmtF8 = 3 };
+// 128, fp8 e4m3 with per-tensor scales); store-G dW formats 0..1 (fp32, bf16);
+// kFmtNone: an optimizer without state (SGD), whose slots hold W alone.
+enum Fmt : int { kFmtF32 = 0, kFmtBF16 = 1, kFmtI8 = 2, kFmtF8 = 3, kFmtNone = 4 };
 
 // Most linear layers one launch can step (a grouped launch walks one tile
 // queue across all of them).

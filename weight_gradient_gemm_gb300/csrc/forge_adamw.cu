@@ -133,8 +133,8 @@ __global__ void __launch_bounds__(256) adamw_int8_kernel(const void* __restrict_
     const float sm = m_scale[b], sv = v_scale[b];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      mm[k] = dequant_m(static_cast<int8_t>((mc >> (8 * k)) & 0xFFu), sm);
-      vv[k] = dequant_v(static_cast<int8_t>((vc >> (8 * k)) & 0xFFu), sv);
+      mm[k] = dequant_mf(i8_code_float(mc ^ 0x80808080u, k), sm);
+      vv[k] = dequant_vf(i8_code_float(vc ^ 0x80808080u, k), sv);
     }
     float amax_m = 0.0f, amax_r = 0.0f;
 #pragma unroll
@@ -154,13 +154,12 @@ __global__ void __launch_bounds__(256) adamw_int8_kernel(const void* __restrict_
       amax_r = fmaxf(amax_r, __shfl_xor_sync(0xffffffffu, amax_r, o));
     }
     const float inv_m = int8_inv_step(amax_m), inv_r = int8_inv_step(amax_r);
-    const bool r_nz = amax_r > 0.0f;
-    uint32_t mo = 0, vo = 0;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      mo |= (static_cast<uint32_t>(quant_m_code(mm[k], inv_m)) & 0xFFu) << (8 * k);
-      vo |= (static_cast<uint32_t>(quant_r_code(rr[k], inv_r, r_nz)) & 0xFFu) << (8 * k);
-    }
+    const float r_floor = amax_r > 0.0f ? 1.0f : 0.0f;
+    const uint32_t mo = pack_low_bytes4(quant_m_bits(mm[0], inv_m), quant_m_bits(mm[1], inv_m),
+                                        quant_m_bits(mm[2], inv_m), quant_m_bits(mm[3], inv_m));
+    const uint32_t vo =
+        pack_low_bytes4(quant_r_bits(rr[0], inv_r, r_floor), quant_r_bits(rr[1], inv_r, r_floor),
+                        quant_r_bits(rr[2], inv_r, r_floor), quant_r_bits(rr[3], inv_r, r_floor));
     __stcs(mp, mo);
     __stcs(vp, vo);
     __stcs(wp, make_uint2(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3])));

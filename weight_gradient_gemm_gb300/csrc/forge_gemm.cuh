@@ -360,29 +360,27 @@ __device__ __forceinline__ void epi_slice_fused_16(uint32_t taddr, bool zero_gra
   }
 }
 
-// Decode 32 int8 codes (two 16-byte chunks) to floats.
+// 32 int8 codes (two 16-byte chunks) as floats, without conversion
+// instructions (i8_code_float).
 __device__ __forceinline__ void load_codes32(const uint8_t* box, uint32_t row, int chunk0,
-                                             int (&q)[32]) {
+                                             float (&q)[32]) {
   const uint4 a = *reinterpret_cast<const uint4*>(box + sw128_off(row, chunk0));
   const uint4 b = *reinterpret_cast<const uint4*>(box + sw128_off(row, chunk0 + 1));
   const uint32_t words[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
+    const uint32_t off = words[i] ^ 0x80808080u;
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      q[4 * i + k] = static_cast<int>(static_cast<int8_t>((words[i] >> (8 * k)) & 0xFFu));
+    for (int k = 0; k < 4; ++k) q[4 * i + k] = i8_code_float(off, k);
   }
 }
+// Store 32 codes, each in the low byte of its word (quant_m_bits / quant_r_bits).
 __device__ __forceinline__ void store_codes32(uint8_t* box, uint32_t row, int chunk0,
-                                              const int (&q)[32]) {
+                                              const uint32_t (&q)[32]) {
   uint32_t words[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    uint32_t wv = 0;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) wv |= (static_cast<uint32_t>(q[4 * i + k]) & 0xFFu) << (8 * k);
-    words[i] = wv;
-  }
+  for (int i = 0; i < 8; ++i)
+    words[i] = pack_low_bytes4(q[4 * i], q[4 * i + 1], q[4 * i + 2], q[4 * i + 3]);
   *reinterpret_cast<uint4*>(box + sw128_off(row, chunk0)) =
       make_uint4(words[0], words[1], words[2], words[3]);
   *reinterpret_cast<uint4*>(box + sw128_off(row, chunk0 + 1)) =
@@ -424,7 +422,7 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, uint32_t sadd
     uint32_t graw[32];
     tmem_ld_x32(taddr + 32 * c, graw);
     tmem_ld_wait();
-    int qm[32], qv[32];
+    float qm[32], qv[32];
     load_codes32(mbox, row, 4 * h + 2 * c, qm);
     load_codes32(vbox, row, 4 * h + 2 * c, qv);
     uint4 wq[4];
@@ -439,8 +437,8 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, uint32_t sadd
       float g0 = zero_grad ? 0.0f : __uint_as_float(graw[2 * i]);
       float g1 = zero_grad ? 0.0f : __uint_as_float(graw[2 * i + 1]);
       float2 w2 = make_float2(w0, w1);
-      float2 m2 = make_float2(dequant_m(qm[2 * i], sm_old), dequant_m(qm[2 * i + 1], sm_old));
-      float2 v2 = make_float2(dequant_v(qv[2 * i], sv_old), dequant_v(qv[2 * i + 1], sv_old));
+      float2 m2 = make_float2(dequant_mf(qm[2 * i], sm_old), dequant_mf(qm[2 * i + 1], sm_old));
+      float2 v2 = make_float2(dequant_vf(qv[2 * i], sv_old), dequant_vf(qv[2 * i + 1], sv_old));
       float2 r2;
       adamw_elem2(make_float2(g0, g1), w2, m2, v2, r2, hc);
       w0 = w2.x; w1 = w2.y;
@@ -449,10 +447,10 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, uint32_t sadd
       amax_r = fmaxf(amax_r, fmaxf(r0, r1));
       wo[i] = pack_bf16x2(w0, w1);
       if constexpr (STASH) {   // the old codes are consumed: reuse their registers
-        qm[2 * i] = __float_as_int(m0);
-        qm[2 * i + 1] = __float_as_int(m1);
-        qv[2 * i] = __float_as_int(r0);
-        qv[2 * i + 1] = __float_as_int(r1);
+        qm[2 * i] = m0;
+        qm[2 * i + 1] = m1;
+        qv[2 * i] = r0;
+        qv[2 * i + 1] = r1;
       }
     }
 #pragma unroll
@@ -460,8 +458,14 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, uint32_t sadd
       *reinterpret_cast<uint4*>(wbox + sw128_off(row, 4 * c + k)) =
           make_uint4(wo[4 * k], wo[4 * k + 1], wo[4 * k + 2], wo[4 * k + 3]);
     if constexpr (STASH) {
-      tmem_st_x32(saddr + 64 * c, reinterpret_cast<const uint32_t(&)[32]>(qm));
-      tmem_st_x32(saddr + 64 * c + 32, reinterpret_cast<const uint32_t(&)[32]>(qv));
+      uint32_t su[32], sv[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        su[i] = __float_as_uint(qm[i]);
+        sv[i] = __float_as_uint(qv[i]);
+      }
+      tmem_st_x32(saddr + 64 * c, su);
+      tmem_st_x32(saddr + 64 * c + 32, sv);
     }
   }
   if constexpr (STASH) tmem_st_wait();
@@ -477,10 +481,10 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, uint32_t sadd
   amax_r = fmaxf(amax_r, xch[((1 - h) * 2 + 1) * kBM + trow]);
   mbar_arrive(bar_xch_read);
   const float inv_m = int8_inv_step(amax_m), inv_r = int8_inv_step(amax_r);
-  const bool r_nz = amax_r > 0.0f;
+  const float r_floor = amax_r > 0.0f ? 1.0f : 0.0f;   // codes >= 1 in a non-zero block
 #pragma unroll 1
   for (int c = 0; c < 2; ++c) {
-    int qm[32], qv[32];
+    uint32_t bm[32], bv[32];
     if constexpr (STASH) {
       uint32_t ms[32], rs[32];
       tmem_ld_x32(saddr + 64 * c, ms);
@@ -488,13 +492,14 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, uint32_t sadd
       tmem_ld_wait();
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        qm[i] = quant_m_code(__uint_as_float(ms[i]), inv_m);
-        qv[i] = quant_r_code(__uint_as_float(rs[i]), inv_r, r_nz);
+        bm[i] = quant_m_bits(__uint_as_float(ms[i]), inv_m);
+        bv[i] = quant_r_bits(__uint_as_float(rs[i]), inv_r, r_floor);
       }
     } else {
       uint32_t graw[32];
       tmem_ld_x32(taddr + 32 * c, graw);
       tmem_ld_wait();
+      float qm[32], qv[32];
       load_codes32(mbox, row, 4 * h + 2 * c, qm);
       load_codes32(vbox, row, 4 * h + 2 * c, qv);
 #pragma unroll
@@ -503,17 +508,17 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, uint32_t sadd
                                    : make_float2(__uint_as_float(graw[i]),
                                                  __uint_as_float(graw[i + 1]));
         float2 w = make_float2(0.0f, 0.0f), r;
-        float2 m = make_float2(dequant_m(qm[i], sm_old), dequant_m(qm[i + 1], sm_old));
-        float2 v = make_float2(dequant_v(qv[i], sv_old), dequant_v(qv[i + 1], sv_old));
+        float2 m = make_float2(dequant_mf(qm[i], sm_old), dequant_mf(qm[i + 1], sm_old));
+        float2 v = make_float2(dequant_vf(qv[i], sv_old), dequant_vf(qv[i + 1], sv_old));
         adamw_elem2(g, w, m, v, r, hc);
-        qm[i] = quant_m_code(m.x, inv_m);
-        qm[i + 1] = quant_m_code(m.y, inv_m);
-        qv[i] = quant_r_code(r.x, inv_r, r_nz);
-        qv[i + 1] = quant_r_code(r.y, inv_r, r_nz);
+        bm[i] = quant_m_bits(m.x, inv_m);
+        bm[i + 1] = quant_m_bits(m.y, inv_m);
+        bv[i] = quant_r_bits(r.x, inv_r, r_floor);
+        bv[i + 1] = quant_r_bits(r.y, inv_r, r_floor);
       }
     }
-    store_codes32(mbox, row, 4 * h + 2 * c, qm);
-    store_codes32(vbox, row, 4 * h + 2 * c, qv);
+    store_codes32(mbox, row, 4 * h + 2 * c, bm);
+    store_codes32(vbox, row, 4 * h + 2 * c, bv);
   }
   if (active && h == 0) {
     *m_scale_rc = int8_scale(amax_m);

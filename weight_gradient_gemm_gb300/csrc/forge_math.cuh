@@ -216,27 +216,44 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 // Blockwise absmax int8 (128 columns of one row per block).
 //   scale s = a / 127; code = round(x / s) computed as round(x * (127 / a)),
-//   ties to even, clamped to [-127, 127].  The second moment is stored as
-//   r = sqrt(v) with codes of at least 1 in a block whose absmax is non-zero.
+//   ties to even, in [-127, 127].  The second moment is stored as r = sqrt(v)
+//   with codes of at least 1 in a block whose absmax is non-zero.
 __device__ __forceinline__ float int8_scale(float absmax) { return __fdiv_rn(absmax, 127.0f); }
 __device__ __forceinline__ float int8_inv_step(float absmax) {
   return absmax > 0.0f ? __fdiv_rn(127.0f, absmax) : 0.0f;
 }
-__device__ __forceinline__ int quant_m_code(float x, float inv) {
-  int q = __float2int_rn(__fmul_rn(x, inv));
-  return max(-127, min(127, q));
+// Codes without conversion instructions.  y = x * (127 / a) with |x| <= a
+// (a the block's absmax of the same fp32 values) satisfies |y| < 127.0001,
+// so round(y) is already in [-127, 127]; adding 1.5 * 2^23 rounds y to the
+// nearest integer (ties to even, as the rounding of the add itself) and
+// leaves it in the low bits of the sum, so the low byte of the sum's bit
+// pattern is the two's-complement code.  The second moment's floor of one
+// level in a non-zero block is a max on y before rounding: round(max(y, 1))
+// equals max(round(y), 1) for y >= 0.
+constexpr float kRoundMagic = 12582912.0f;   // 1.5 * 2^23
+__device__ __forceinline__ uint32_t quant_m_bits(float x, float inv) {
+  return __float_as_uint(__fadd_rn(__fmul_rn(x, inv), kRoundMagic));
 }
-__device__ __forceinline__ int quant_r_code(float r, float inv, bool nonzero_block) {
-  int q = __float2int_rn(__fmul_rn(r, inv));
-  q = min(127, q);
-  return nonzero_block ? max(1, q) : 0;
+__device__ __forceinline__ uint32_t quant_r_bits(float r, float inv, float floor_level) {
+  return __float_as_uint(__fadd_rn(fmaxf(__fmul_rn(r, inv), floor_level), kRoundMagic));
 }
-// Decoded int8 values: m = code * s; v = (code * s)^2.
-__device__ __forceinline__ float dequant_m(int code, float s) {
-  return __fmul_rn(static_cast<float>(code), s);
+// The low bytes of four words, in order, as one word of four codes.
+__device__ __forceinline__ uint32_t pack_low_bytes4(uint32_t a, uint32_t b, uint32_t c,
+                                                    uint32_t d) {
+  return __byte_perm(__byte_perm(a, b, 0x0040u), __byte_perm(c, d, 0x0040u), 0x5410u);
 }
-__device__ __forceinline__ float dequant_v(int code, float s) {
-  const float r = __fmul_rn(static_cast<float>(code), s);
+// Code k (0..3) of a word of four int8 codes, as a float: with the word's
+// bytes offset by 128 (w ^ 0x80808080), 2^23 + (code + 128) is assembled by a
+// byte permute and 2^23 + 128 subtracted exactly.
+__device__ __forceinline__ float i8_code_float(uint32_t w_offset, int k) {
+  return __fsub_rn(__uint_as_float(__byte_perm(w_offset, 0x4B000000u, 0x7540u | k)),
+                   8388736.0f);
+}
+
+// Decoded int8 values (the code as a float): m = code * s; v = (code * s)^2.
+__device__ __forceinline__ float dequant_mf(float code, float s) { return __fmul_rn(code, s); }
+__device__ __forceinline__ float dequant_vf(float code, float s) {
+  const float r = __fmul_rn(code, s);
   return __fmul_rn(r, r);
 }
 

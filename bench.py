@@ -1238,7 +1238,10 @@ def main():
                     "ms_per_step": res["e2e_ms"], "h2d_bytes_per_step": layer.h2d_bytes(),
                     "d2h_bytes_per_step": 4,
                     "pipeline": "X, dY of step k+1 copied from pinned host memory on a second "
-                                "stream while step k computes; 4-byte status read after every step",
+                                "stream while step k computes; 4 bytes of each step's new W copied "
+                                "to pinned memory and read by the host one step later (while "
+                                "the next step runs); the library's status word checked at the "
+                                "end; untimed warm-up steps first",
                     **res["e2e"]},
             "per_projection_separate_launches": [
                 {"name": it["name"], "shape": [it["d_out"], it["d_in"]],

@@ -842,8 +842,8 @@ def config_blocks(args, dev, peaks, peak_kind):
     and stored ncu traffic: fp8 moments at 512 tokens (HBM-bound; each step
     is the grouped launch plus the scale roll), C3 at 2048 and 8192 tokens
     (bf16 moments), C4 at 4096 (int8), fp32 moments at 4096, and C5 (the
-    224-linear stack at 8192 tokens, fp32 moments, one grouped launch per
-    layer)."""
+    224-linear stack at 512 and 8192 tokens, fp32 moments, one grouped launch
+    per layer)."""
     from weight_gradient_gemm_gb300 import forge as F
     stream = torch.cuda.current_stream()
     sampler = ClockSampler(dev.index)
@@ -896,31 +896,32 @@ def config_blocks(args, dev, peaks, peak_kind):
                      "cublas_wgrad_gemm": cub}
         del group, f8
         torch.cuda.empty_cache()
-    # C5: the whole stack at 8192 tokens
-    stack = Stack(8192, 0, 1e-3, dev)
-    step = [0]
+    # C5: the whole stack at 512 and 8192 tokens
+    for sbt in (512, 8192):
+        stack = Stack(sbt, 0, 1e-3, dev)
+        step = [0]
 
-    def stack_once():
-        step[0] += 1
-        stack_step(F, stack, step[0])
-    for _ in range(max(args.warmup, 3)):
-        stack_once()
-    n = max(3, min(args.steps, 10))
-    ms, w0, w1 = timed_launches(stack_once, n, stream)
-    if F.device_error() != 0:
-        raise RuntimeError("stack: device error")
-    flops, nbytes = stack.flops(), stack.alg_bytes()
-    mean_s = sum(ms) / len(ms) * 1e-3
-    out["c5_stack_bt8192_fp32"] = {
-        "workload": "llama31_8b_stack_bt8192_fp32", "bt": 8192, "moments": "fp32",
-        "launch": "32 forge_wgrad_adamw_grouped launches per step, backward order",
-        "ms_per_step": mean_s * 1e3, "tflops": flops / mean_s / 1e12,
-        "roofline": roofline_of(flops / STACK_LAYERS, nbytes / STACK_LAYERS,
-                                mean_s / STACK_LAYERS, peaks, peak_kind),
-        "per_step": launch_stats(ms), "clocks": sampler.summary(w0, w1)}
+        def stack_once():
+            step[0] += 1
+            stack_step(F, stack, step[0])
+        for _ in range(max(args.warmup, 3)):
+            stack_once()
+        n = max(3, min(args.steps, 10))
+        ms, w0, w1 = timed_launches(stack_once, n, stream)
+        if F.device_error() != 0:
+            raise RuntimeError("stack: device error")
+        flops, nbytes = stack.flops(), stack.alg_bytes()
+        mean_s = sum(ms) / len(ms) * 1e-3
+        out[f"c5_stack_bt{sbt}_fp32"] = {
+            "workload": f"llama31_8b_stack_bt{sbt}_fp32", "bt": sbt, "moments": "fp32",
+            "launch": "32 forge_wgrad_adamw_grouped launches per step, backward order",
+            "ms_per_step": mean_s * 1e3, "tflops": flops / mean_s / 1e12,
+            "roofline": roofline_of(flops / STACK_LAYERS, nbytes / STACK_LAYERS,
+                                    mean_s / STACK_LAYERS, peaks, peak_kind),
+            "per_step": launch_stats(ms), "clocks": sampler.summary(w0, w1)}
+        del stack
+        torch.cuda.empty_cache()
     sampler.stop()
-    del stack
-    torch.cuda.empty_cache()
     return out
 
 

@@ -162,10 +162,11 @@ def test_dgrad_grouped_split_in_the_callers_workspace(splits, cap, tune):
         assert _same(it["dX"], ref), (splits, used)
 
 
-@pytest.mark.parametrize("fmt", [F.MOM_FP32, F.MOM_BF16, F.MOM_INT8_B128])
+@pytest.mark.parametrize("fmt", [F.MOM_FP32, F.MOM_BF16, F.MOM_INT8_B128, F.MOM_FP8_E4M3])
 def test_linear_backward_grouped_equals_per_layer_calls(fmt, tune):
     # one grouped dX launch and one grouped fused launch over the layer,
-    # against forge_linear_backward per projection (one split on both sides)
+    # against forge_linear_backward per projection (one split on both sides);
+    # fp8 moments include each tensor's amax words
     bt = 384
     tune(splits=1)
     inp = make_layer_inputs(15, 0, 1, bt, with_w=True)
@@ -174,6 +175,8 @@ def test_linear_backward_grouped_equals_per_layer_calls(fmt, tune):
     a = []
     for name, d_out, d_in in LLAMA31_8B_SHAPES:
         m, v, ms, vs = F.alloc_moments(d_out, d_in, fmt, DEV)
+        if fmt == F.MOM_FP8_E4M3:   # write scales that keep the first moments representable
+            ms[1], vs[1] = 1e-5, 1e-5
         a.append(dict(X=xs[LLAMA31_8B_X_GROUP[name]], dY=inp["dy"][name].to(DEV),
                       W=inp["w"][name].to(DEV), m=m, v=v, m_scale=ms, v_scale=vs,
                       dX=torch.empty((bt, d_in), dtype=torch.bfloat16, device=DEV)))

@@ -39,7 +39,7 @@
  * moment format (forge_describe_config shows it).  forge_set_tuning
  * overrides the choice for measurements; its initial value comes from these
  * environment variables, read once, at the library's first call that
- * chooses a configuration: FORGE_PROFILE=stream|balanced|mma|deep|deepq (how
+ * chooses a configuration: FORGE_PROFILE=stream|balanced|mma|deep (how
  * shared memory is split between operand stages and state slots),
  * FORGE_CG=1|2 (one CTA or a CTA pair per tile), FORGE_BN=128|256
  * (accumulator width on one CTA), FORGE_GROUP_M=1..64 (tile rows per raster
@@ -511,9 +511,7 @@ typedef enum {
   FORGE_PROFILE_STREAM = 0,    /* two operand stages, the rest state slots      */
   FORGE_PROFILE_MMA = 1,       /* as many operand stages as fit beside 2 slots  */
   FORGE_PROFILE_BALANCED = 2,  /* as many operand stages as state slots         */
-  FORGE_PROFILE_DEEP = 3,      /* as many stages as fit beside 2 half-tile slots */
-  FORGE_PROFILE_DEEP_QUARTER = 4  /* as many stages as fit beside quarter-tile
-                                     slots (CTA pairs; else as DEEP)            */
+  FORGE_PROFILE_DEEP = 3       /* as many stages as fit beside 2 half-tile slots */
 } forge_profile;
 
 /* Tuning overrides; a field at its automatic value (FORGE_PROFILE_AUTO, 0 or

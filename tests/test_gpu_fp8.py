@@ -163,7 +163,6 @@ def test_fp8_tiny_three_steps_delayed_scaling():
 
 
 @pytest.fixture(params=[None, ("stream", 128, 1), ("balanced", 128, 1), ("mma", 256, 2),
-                        ("deepq", 256, 2),
                         ("balanced", 256, 2)],
                 ids=lambda p: "auto" if p is None else f"{p[0]}-bn{p[1]}-cta{p[2]}")
 def f8_cfg(request, tune):

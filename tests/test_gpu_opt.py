@@ -88,7 +88,7 @@ def test_opt_against_oracle(opt, fmt, bt, d_in, d_out, t):
 
 
 @pytest.fixture(params=[("stream", "128", "1"), ("stream", "256", "1"), ("balanced", "256", "1"),
-                        ("deep", "256", "2"), ("deepq", "256", "2"), ("mma", "256", "2")],
+                        ("deep", "256", "2"), ("mma", "256", "2")],
                 ids=lambda p: f"{p[0]}-bn{p[1]}-cta{p[2]}")
 def forced(request, tune):
     tune(profile=request.param[0], bn=int(request.param[1]), cg=int(request.param[2]))

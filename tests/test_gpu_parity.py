@@ -30,12 +30,12 @@ def _gpu():
 @pytest.fixture(params=[("stream", "128", "1"), ("mma", "128", "1"), ("balanced", "128", "1"),
                         ("stream", "256", "1"), ("mma", "256", "1"), ("stream", "256", "2"),
                         ("balanced", "256", "2"), ("mma", "256", "2"), ("deep", "128", "1"),
-                        ("deep", "256", "2"), ("deepq", "256", "2")],
+                        ("deep", "256", "2")],
                 ids=lambda p: f"{p[0]}-bn{p[1]}-cta{p[2]}")
 def profile(request, tune):
     """Every pipeline profile, tile width and CTA grouping of the tensor-core
-    kernel (the library picks them by token count; the tuning overrides force
-    them; 1-CTA int8 moments always use 128-wide tiles)."""
+    kernel (the library picks them by token count; FORGE_PROFILE, FORGE_BN and
+    FORGE_CG force them; 1-CTA int8 moments always use 128-wide tiles)."""
     tune(profile=request.param[0], bn=int(request.param[1]), cg=int(request.param[2]))
     return request.param
 
@@ -319,8 +319,7 @@ def test_raster_group_sizes(group_m, cg, tune):
     (O.FMT_FP32, 4096, ("deep", 256, 2)),     # the configuration that prefetches by default
     (O.FMT_BF16, 1000, ("balanced", 256, 2)),
     (O.FMT_INT8, 300, ("balanced", 128, 1)),  # 8-bit slices: two W boxes per slot
-    (O.FMT_INT8, 1000, ("deepq", 256, 2)),    # quarter-tile slots taken by any epilogue part
-], ids=["fp32-deep-pair", "bf16-balanced-pair", "int8-balanced-cta", "int8-deepq-pair"])
+], ids=["fp32-deep-pair", "bf16-balanced-pair", "int8-balanced-cta"])
 def test_state_prefetch_changes_no_bits(fmt, bt, cfg, tune):
     # the state loader's L2 prefetch is a hint: with any distance the step is
     # bit for bit the step without it (which the other tests hold to the oracle)

@@ -36,7 +36,7 @@ def _state(fmt, d_out, d_in, seed):
 
 
 @pytest.fixture(params=[None, ("stream", "128", "1"), ("balanced", "128", "1"),
-                        ("deep", "256", "2"), ("deepq", "256", "2"), ("mma", "256", "2")],
+                        ("deep", "256", "2"), ("mma", "256", "2")],
                 ids=lambda p: "auto" if p is None else f"{p[0]}-bn{p[1]}-cta{p[2]}")
 def sr_cfg(request, tune):
     if request.param is not None:

@@ -390,11 +390,8 @@ forge_tuning current_tuning();
 
 GemmConfig choose_config(int64_t bt, int fmt, int mode) {
   GemmConfig c;
-  // bf16 and 8-bit moments (int8, fp8) move to CTA pairs above 640 tokens
-  // (8-bit at 768 tokens over the layer: pairs 0.59 against 0.63 ms for int8,
-  // 0.44 against 0.56 for fp8; one CTA stays faster at 512)
-  const int64_t one_cta_upto =
-      (mode == kModeFused && (fmt == kFmtBF16 || fmt == kFmtI8 || fmt == kFmtF8)) ? 640 : 768;
+  // (fp8 moments move the bytes of int8 ones and take int8's choices)
+  const int64_t one_cta_upto = (mode == kModeFused && fmt == kFmtBF16) ? 640 : 768;
   if (bt <= one_cta_upto) {
     c.cg = 1;
     if (mode == kModeFused)
@@ -453,7 +450,6 @@ void tuning_from_env() {
     if (std::strcmp(e, "mma") == 0) t.profile = FORGE_PROFILE_MMA;
     if (std::strcmp(e, "balanced") == 0) t.profile = FORGE_PROFILE_BALANCED;
     if (std::strcmp(e, "deep") == 0) t.profile = FORGE_PROFILE_DEEP;
-    if (std::strcmp(e, "deepq") == 0) t.profile = FORGE_PROFILE_DEEP_QUARTER;
   }
   if (const char* e = std::getenv("FORGE_CG")) t.cta_group = std::atoi(e);
   if (const char* e = std::getenv("FORGE_BN")) t.bn = std::atoi(e);
@@ -497,11 +493,10 @@ GemmConfig choose_accum_config(int64_t bt) {
 GemmConfig finish_config(GemmConfig c, int64_t bt, int fmt, int mode) {
   const forge_tuning tu = current_tuning();
   c.bn = (c.cg == 2) ? 256 : 128;
-  if (tu.profile >= kProfStream && tu.profile <= kProfDeepQ) c.prof = tu.profile;
+  if (tu.profile >= kProfStream && tu.profile <= kProfDeep) c.prof = tu.profile;
   if (tu.cta_group == 1 || tu.cta_group == 2) c.cg = tu.cta_group;
   if (tu.bn == 128 || tu.bn == 256) c.bn = tu.bn;
   if (c.cg == 2) c.bn = 256;                    // pairs always use 256 x 256 tiles
-  if (c.prof == kProfDeepQ && c.cg != 2) c.prof = kProfDeep;   // quarter slots on pairs only
   if (c.cg == 1 && (fmt == kFmtI8 || fmt == kFmtF8)) c.bn = 128;   // 1-CTA 8-bit moments: 128-wide tiles
   // Tile rows per raster group (the kernel's tile_coords): 4 for 128 x 128
   // tiles; 8 for the weight-gradient modes on pairs (a sweep of 1, 2, 4, 8,
@@ -1426,8 +1421,7 @@ int forge_describe_config(int64_t bt, int64_t d_in, int64_t d_out, forge_moment_
                                  c.prof == kProfStream ? "stream"
                                  : c.prof == kProfMma  ? "mma"
                                  : c.prof == kProfDeep ? "deep"
-                                 : c.prof == kProfDeepQ ? "deepq"
-                                                        : "balanced");
+                                                       : "balanced");
   return need + 1;
 }
 
@@ -1449,8 +1443,7 @@ int forge_describe_dgrad_config(int64_t bt, int64_t d_in, int64_t d_out, char* b
                                  c.prof == kProfStream ? "stream"
                                  : c.prof == kProfMma  ? "mma"
                                  : c.prof == kProfDeep ? "deep"
-                                 : c.prof == kProfDeepQ ? "deepq"
-                                                        : "balanced");
+                                                       : "balanced");
   return need + 1;
 }
 

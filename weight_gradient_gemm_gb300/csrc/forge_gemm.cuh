@@ -83,19 +83,13 @@ struct GemmTraits {
   static constexpr bool I8 = (MODE == kModeFused && FMT == kFmtI8);
   // int8 row-halves exchange: [2 halves][2 kinds][128 rows] floats
   static constexpr int XCH_BYTES = I8 ? 2 * 2 * kBM * 4 : 0;
-  // operand full/empty, accumulator full/empty, slot full/empty/done, the
-  // drain barrier and four pairs of int8 row-half exchange barriers
-  static constexpr int MAX_BARS = 2 * 6 + 4 + 3 * 6 + 9;
+  static constexpr int MAX_BARS = 2 * 6 + 4 + 3 * 6 + 5;
   static constexpr int BUDGET = kSmemLimit - (8 * MAX_BARS + 16 + XCH_BYTES);
   static constexpr int NS_CAP = 6;
-  // Quarter-tile slots are taken by whichever part of the epilogue owns the
-  // next slice; smaller slots each belong to a fixed part (slot j to part
-  // j % PARTS), so their count is a multiple of PARTS.
-  static constexpr int SLOT_MULT = (PROF == kProfDeepQ) ? 1 : PARTS;
-  // state slots that fit next to `st` operand stages
+  // state slots that fit next to `st` operand stages, a multiple of PARTS
   static constexpr int slots_beside(int st) {
     const int n = (BUDGET - st * STAGE_BYTES) / SLOT_BYTES;
-    return ((n > NS_CAP ? NS_CAP : n) / SLOT_MULT) * SLOT_MULT;
+    return ((n > NS_CAP ? NS_CAP : n) / PARTS) * PARTS;
   }
   static constexpr int stages_mma() {
     int st = 6;
@@ -109,8 +103,7 @@ struct GemmTraits {
   }
   static constexpr int STAGES =
       (PROF == kProfStream) ? 2
-                            : (PROF == kProfMma || PROF == kProfDeep || PROF == kProfDeepQ
-                                   ? stages_mma() : stages_balanced());
+                            : (PROF == kProfMma || PROF == kProfDeep ? stages_mma() : stages_balanced());
   static constexpr int NS = slots_beside(STAGES);
   static_assert(NS >= 2, "shared memory does not fit two state slots");
   // int8 with 128-wide accumulators: the spare 256 tensor-memory columns hold
@@ -120,7 +113,7 @@ struct GemmTraits {
   // shared-memory carve (offsets from the 1024-aligned base)
   static constexpr int OFF_SLOTS = STAGES * STAGE_BYTES;
   static constexpr int OFF_BARS = OFF_SLOTS + NS * SLOT_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 4 + 3 * NS + 9;
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + 3 * NS + 5;
   static constexpr int OFF_TMEM = OFF_BARS + 8 * NUM_BARS;
   static constexpr int OFF_ABORT = OFF_TMEM + 4;
   static constexpr int OFF_XCH = (OFF_ABORT + 4 + 15) & ~15;
@@ -139,9 +132,7 @@ struct GemmTraits {
   static_assert(CG == 1 || (CG == 2 && BN == 256), "CTA pairs use 256 x 256 tiles");
   static_assert(TMEM_COLS <= 512, "tensor memory has 512 columns");
   // with half-tile slots each half of the epilogue owns every other slot
-  static_assert(PARTS == 1 || PROF == kProfDeepQ || (NS % PARTS == 0 && SLICES % PARTS == 0),
-                "slot ownership");
-  static_assert(PROF != kProfDeepQ || (CG == 2 && RPS == 32), "quarter slots on CTA pairs");
+  static_assert(PARTS == 1 || (NS % PARTS == 0 && SLICES % PARTS == 0), "slot ownership");
 };
 
 struct WaitCtx {
@@ -780,8 +771,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   auto bar_sdone = [&](int j) { return bars + 8u * (2 * T::STAGES + 4 + 2 * T::NS + j); };
   const uint32_t bar_drain = bars + 8u * (2 * T::STAGES + 4 + 3 * T::NS);
   // int8 row-half exchange barriers, one pair per slot part: [xch0, xch1, read0, read1]
-  const uint32_t bar_xch0 = bar_drain + 8u;        // four, one per slot part
-  const uint32_t bar_xch_read0 = bar_drain + 40u;   // four more
+  const uint32_t bar_xch0 = bar_drain + 8u;
+  const uint32_t bar_xch_read0 = bar_drain + 24u;
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + T::OFF_ABORT);
   const WaitCtx wc{abort_flag, p.err, p.err_site, p.timeout_ns};
 
@@ -800,7 +791,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mbar_init(bar_sdone(j), kEpiThreads / T::PARTS);
     }
     mbar_init(bar_drain, 1);
-    for (int g = 0; g < 4; ++g) {
+    for (int g = 0; g < 2; ++g) {
       mbar_init(bar_xch0 + 8u * g, kEpiThreads / T::PARTS);
       mbar_init(bar_xch_read0 + 8u * g, kEpiThreads / T::PARTS);
     }
@@ -1094,10 +1085,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const int h = (warp - 4) >> 2;           // column half of each slice
     const uint32_t row = q * 32 + lane;      // tile row = TMEM lane
     // with half-tile slots, quadrants 0-1 take part 0 (even slots) and 2-3 part 1
-    // the quadrants of one slot part: all four (whole-tile slots), two
-    // (half-tile) or one (quarter-tile); the thread's row inside the slot
-    const int part = q / (4 / T::PARTS);
-    const uint32_t srow = row % static_cast<uint32_t>(T::RPS);
+    const int part = (T::PARTS == 1) ? 0 : (q >> 1);
+    const uint32_t srow = (T::PARTS == 1) ? row : static_cast<uint32_t>((q & 1) * 32 + lane);
     const uint32_t bar_xch = bar_xch0 + 8u * part;
     const uint32_t bar_xch_read = bar_xch_read0 + 8u * part;
     const bool zero_grad = (p.num_k == 0);
@@ -1351,15 +1340,6 @@ cudaError_t launch_gemm_fmt(const GemmConfig& cfg, const GemmArgs& args, cudaStr
         return launch_gemm_prof<MODE, FMT, kProfDeep>(cfg, args, stream);
       else
         return launch_gemm_prof<MODE, FMT, kProfMma>(cfg, args, stream);
-    case kProfDeepQ:
-      // quarter-tile slots: CTA pairs only; without state slots, as mma
-      if constexpr (has_state(MODE)) {
-        if (cfg.cg == 2 && cfg.bn == 256)
-          return launch_gemm_t<MODE, FMT, 256, kProfDeepQ, 2>(cfg, args, stream);
-        return cudaErrorInvalidValue;
-      } else {
-        return launch_gemm_prof<MODE, FMT, kProfMma>(cfg, args, stream);
-      }
   }
   return cudaErrorInvalidValue;
 }

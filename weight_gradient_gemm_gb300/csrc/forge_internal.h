@@ -40,11 +40,8 @@ __host__ __device__ constexpr bool has_state(int mode) {
 // two state slots; kProfBalanced keeps as many stages as slots, for the range
 // where the main loop and the epilogue take about the same time; kProfDeep
 // (the largest token counts) keeps as many operand stages as fit next to two
-// half-tile state slots; kProfDeepQ keeps as many operand stages as fit next
-// to quarter-tile (32-row) state slots, used by any part of the epilogue in
-// turn (CTA pairs only).
-enum Prof : int { kProfStream = 0, kProfMma = 1, kProfBalanced = 2, kProfDeep = 3,
-                  kProfDeepQ = 4 };
+// half-tile state slots.
+enum Prof : int { kProfStream = 0, kProfMma = 1, kProfBalanced = 2, kProfDeep = 3 };
 // Epilogue formats: fused moment formats 0..3 (fp32, bf16, int8 blocks of
 // 128, fp8 e4m3 with per-tensor scales); store-G dW formats 0..1 (fp32, bf16);
 // kFmtNone: an optimizer without state (SGD), whose slots hold W alone.
@@ -142,13 +139,11 @@ __host__ __device__ constexpr int slice_cols(int mode, int fmt) {
 // holds half a tile (64 rows; 8-bit 32 KB instead of 64 KB, fp32 20 KB
 // instead of 40 KB),
 // processed by the four epilogue warps of its two TMEM lane quadrants, which
-// leaves shared memory for more operand stages; in kProfDeepQ a quarter tile
-// (32 rows, one TMEM lane quadrant).
+// leaves shared memory for more operand stages.
 __host__ __device__ constexpr int slot_rows(int mode, int fmt, int prof) {
-  return !has_state(mode) ? 128
-       : prof == kProfDeepQ ? 32
-       : (((fmt == kFmtI8 || fmt == kFmtF8) && prof != kProfStream) || prof == kProfDeep) ? 64
-       : 128;
+  return (has_state(mode) &&
+          (((fmt == kFmtI8 || fmt == kFmtF8) && prof != kProfStream) || prof == kProfDeep))
+             ? 64 : 128;
 }
 
 // Launchers (one per instantiated kernel family); return a CUDA error.

@@ -69,7 +69,7 @@ class ForgeDgradItem(ctypes.Structure):
                 ("d_in", ctypes.c_int64), ("d_out", ctypes.c_int64)]
 
 # forge_profile values
-PROFILES = {"auto": -1, "stream": 0, "mma": 1, "balanced": 2, "deep": 3, "deepq": 4}
+PROFILES = {"auto": -1, "stream": 0, "mma": 1, "balanced": 2, "deep": 3}
 
 
 class ForgeTuning(ctypes.Structure):
@@ -511,7 +511,7 @@ def set_tuning(profile: str = "auto", cg: int = 0, bn: int = 0, group_m: int = 0
                poll_store: int = -1, splits: int = 0, l2_hints: int = -1,
                state_prefetch: int = -1) -> None:
     """Replace the tuning overrides (the defaults leave every choice to the
-    library).  profile: auto|stream|balanced|mma|deep|deepq; cg: 1 or 2 CTAs per
+    library).  profile: auto|stream|balanced|mma|deep; cg: 1 or 2 CTAs per
     tile; bn: 128 or 256; group_m: 1..64; poll_store: 0 or 1; splits: 1..8;
     l2_hints: 0..3; state_prefetch: 0..32 slices."""
     if profile not in PROFILES:

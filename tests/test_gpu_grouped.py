@@ -190,3 +190,40 @@ def test_linear_backward_grouped_equals_per_layer_calls(fmt, tune):
         for k in ("dX", "W", "m", "v", "m_scale", "v_scale"):
             if x[k] is not None:
                 assert _same(x[k], y[k]), k
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3])
+def test_dgrad_grouped_ragged_against_the_oracle(splits, tune):
+    # projections whose reductions over d_out differ and are not multiples of
+    # the 64-deep k-step, widths off the 256-column tile, a token count off
+    # the 256-row tile; split partials in a workspace the library sizes.  Every
+    # element is compared with the oracle, and each dX equals forge_dgrad's at
+    # the same split count bit for bit
+    bt = 333
+    shapes = [(136, 264), (1000, 520), (520, 1032), (2056, 128)]   # (d_out, d_in)
+    tune(splits=splits)
+    items, host = [], []
+    for i, (d_out, d_in) in enumerate(shapes):
+        s = make_step_inputs(16, i, 1, bt, d_in, d_out, dy_std=1e-3, with_w=True,
+                             spike_frac=0.01)
+        items.append(dict(dY=s.dy.to(DEV), W=s.w.to(DEV),
+                          dX=torch.full((bt, d_in), float("nan"), dtype=torch.bfloat16,
+                                        device=DEV)))
+        host.append(s)
+    need = F.dgrad_workspace_bytes(items)
+    ws = torch.empty(max(1, need // 4), dtype=torch.float32, device=DEV) if need else None
+    F.dgrad_grouped(items, workspace=ws)
+    assert F.device_error() == 0
+    # the launch's split count: the forced one, capped by the longest
+    # reduction's limit (at least 8 k-steps per split: 33 k-steps -> 4) and by
+    # the shortest reduction's k-steps (3)
+    grouped_splits = min(splits, 4, 3)
+    for it, s, (d_out, d_in) in zip(items, host, shapes):
+        check_dx(bf16_bits(it["dX"].cpu()), bf16_bits(s.dy), bf16_bits(s.w),
+                 label=f"grouped ragged dX splits={splits}")
+        single = int(F.describe_dgrad_config(bt, d_in, d_out).split("splits=")[1].split()[0])
+        if single == grouped_splits:
+            ref = torch.empty_like(it["dX"])
+            F.dgrad(it["dY"], it["W"], ref)
+            assert F.device_error() == 0
+            assert _same(it["dX"], ref)

@@ -35,6 +35,8 @@ cudaError_t launch_gemm_dgrad(const GemmConfig&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_opt_f32(const GemmConfig&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_opt_bf16(const GemmConfig&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_opt_none(const GemmConfig&, const GemmArgs&, cudaStream_t);
+cudaError_t launch_gemm_opt_f32s1(const GemmConfig&, const GemmArgs&, cudaStream_t);
+cudaError_t launch_gemm_opt_bf16s1(const GemmConfig&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_accum(const GemmConfig&, const GemmArgs&, cudaStream_t);
 
 cudaError_t launch_gemm(int mode, int fmt, const GemmConfig& cfg, const GemmArgs& args,
@@ -60,6 +62,8 @@ cudaError_t launch_gemm(int mode, int fmt, const GemmConfig& cfg, const GemmArgs
       case kFmtF32: return launch_gemm_opt_f32(cfg, args, stream);
       case kFmtBF16: return launch_gemm_opt_bf16(cfg, args, stream);
       case kFmtNone: return launch_gemm_opt_none(cfg, args, stream);
+      case kFmtF32S1: return launch_gemm_opt_f32s1(cfg, args, stream);
+      case kFmtBF16S1: return launch_gemm_opt_bf16s1(cfg, args, stream);
     }
   }
   return cudaErrorInvalidValue;
@@ -412,28 +416,29 @@ GemmConfig choose_config(int64_t bt, int fmt, int mode) {
 // bf16 states keep balanced depths on pairs up to 3072 tokens (-2 to -5 %
 // at 2048).
 GemmConfig choose_opt_config(int64_t bt, int fmt, int nstate) {
+  const int efmt = state_elem_fmt(fmt);   // fp32 or bf16 (kFmtNone for SGD)
   GemmConfig c;
-  const int64_t one_cta_upto = (fmt == kFmtBF16) ? 640 : 768;
+  const int64_t one_cta_upto = (efmt == kFmtBF16) ? 640 : 768;
   if (bt <= one_cta_upto) {
     c.cg = 1;
     c.prof = kProfBalanced;
-    if (nstate == 0) {
-      // SGD carries no state: its slots hold W alone (8 KB), so the balanced
-      // profile with 256-wide tiles keeps four operand stages beside four
-      // slots for its main-loop-bound step (512 tokens: 0.41 of HBM with
-      // AdamW's slot layout, 0.59 now)
-      c.prof = kProfBalanced;
-      c = finish_config(c, bt, fmt, kModeFused);
-      if (current_tuning().bn != 128) c.bn = 256;
-      return c;
-    }
   } else {
     c.cg = 2;
     c.prof = bt <= 1536 ? kProfBalanced
-           : bt <= 3072 ? (fmt == kFmtBF16 ? kProfBalanced : kProfMma)
+           : bt <= 3072 ? (efmt == kFmtBF16 ? kProfBalanced : kProfMma)
                         : kProfDeep;
   }
-  return finish_config(c, bt, fmt, kModeFused);
+  c = finish_config(c, bt, efmt, kModeFused);
+  if (nstate == 0 && bt <= one_cta_upto && current_tuning().bn != 128) {
+    // SGD carries no state: its slots hold W alone (8 KB), so the balanced
+    // profile with 256-wide tiles keeps four operand stages beside four
+    // slots for its main-loop-bound step (512 tokens: 0.41 of HBM with
+    // AdamW's slot layout, 0.59 now)
+    c.bn = 256;
+  }
+  // the state stream's L2 prefetch was measured for AdamW only
+  if (current_tuning().state_prefetch < 0) c.state_prefetch = 0;
+  return c;
 }
 
 // Tuning overrides.  The FORGE_* environment variables are read once, at the
@@ -1202,8 +1207,11 @@ forge_status forge_wgrad_opt_grouped(const forge_linear* layers, int n, int64_t 
   s = device_info(&d);
   if (s != FORGE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // an optimizer without state runs with W-only slots, whatever the format
-  const int ifmt = ns == 0 ? kFmtNone : (fmt == FORGE_MOM_FP32 ? kFmtF32 : kFmtBF16);
+  // the slots hold W and as many state boxes as the optimizer has
+  const bool f32s = fmt == FORGE_MOM_FP32;
+  const int ifmt = ns == 0 ? kFmtNone
+                 : ns == 1 ? (f32s ? kFmtF32S1 : kFmtBF16S1)
+                           : (f32s ? kFmtF32 : kFmtBF16);
   GemmConfig cfg = choose_opt_config(bt, ifmt, ns);
   const bool f32 = fmt == FORGE_MOM_FP32;
   const CUtensorMapDataType mdt =

@@ -67,16 +67,17 @@ struct GemmTraits {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int W_ELEM =
       ((MODE == kModeStoreG || MODE == kModeAccum) && FMT == kFmtF32) ? 4 : 2;
+  static constexpr int SFMT = state_elem_fmt(FMT);
   static constexpr int MOM_ELEM =
       (!has_state(MODE) || FMT == kFmtNone) ? 0
-                                            : (FMT == kFmtF32 ? 4 : (FMT == kFmtBF16 ? 2 : 1));
+                                            : (SFMT == kFmtF32 ? 4 : (SFMT == kFmtBF16 ? 2 : 1));
   // 8-bit moments (int8 blocks or fp8): 128-column slices whose W is two
   // 64-column boxes
   static constexpr bool Q8 = (MODE == kModeFused && (FMT == kFmtI8 || FMT == kFmtF8));
   static constexpr bool F8 = (MODE == kModeFused && FMT == kFmtF8);
   static constexpr int W_BYTES = RPS * SW * W_ELEM;
   static constexpr int M_BYTES = RPS * SW * MOM_ELEM;
-  static constexpr int SLOT_BYTES = W_BYTES + 2 * M_BYTES;
+  static constexpr int SLOT_BYTES = W_BYTES + state_boxes(FMT) * M_BYTES;
   // every box of a slot starts 1024-byte aligned (the 128-byte swizzle's atom)
   static_assert(W_BYTES % 1024 == 0 && M_BYTES % 1024 == 0 && SLOT_BYTES % 1024 == 0,
                 "state boxes must stay 1024-byte aligned");
@@ -651,9 +652,10 @@ __device__ __forceinline__ void state_st16(uint8_t* box, uint32_t row, int h,
 
 // The other optimizers (kModeOpt): the slice of epi_slice_fused_16 with
 // optimizer OPT's element update, touching only the states OPT has.
-template <int FMT, int RPS, int OPT>
+template <int SLOT_FMT, int RPS, int OPT>
 __device__ __forceinline__ void epi_slice_opt(uint32_t taddr, bool zero_grad, uint8_t* slot,
                                               uint32_t row, int h, const OptConsts& oc) {
+  constexpr int FMT = state_elem_fmt(SLOT_FMT);
   constexpr int kWBytes = RPS * 32 * 2;
   constexpr int kMBytes = RPS * 32 * (FMT == kFmtF32 ? 4 : 2);
   constexpr int NST = opt_states(OPT);
@@ -679,6 +681,17 @@ __device__ __forceinline__ void epi_slice_opt_any(const OptConsts& oc, uint32_t 
                                                   int h) {
   if constexpr (FMT == kFmtNone) {
     epi_slice_opt<FMT, RPS, kOptSgd>(taddr, zero_grad, slot, row, h, oc);
+    return;
+  } else if constexpr (state_boxes(FMT) == 1) {
+    // one-state slots: SGD with momentum, Adagrad, RMSprop, Lion
+    switch (oc.opt) {
+      case kOptSgdMomentum:
+        epi_slice_opt<FMT, RPS, kOptSgdMomentum>(taddr, zero_grad, slot, row, h, oc);
+        break;
+      case kOptAdagrad: epi_slice_opt<FMT, RPS, kOptAdagrad>(taddr, zero_grad, slot, row, h, oc); break;
+      case kOptRmsprop: epi_slice_opt<FMT, RPS, kOptRmsprop>(taddr, zero_grad, slot, row, h, oc); break;
+      default: epi_slice_opt<FMT, RPS, kOptLion>(taddr, zero_grad, slot, row, h, oc); break;
+    }
     return;
   }
   switch (oc.opt) {

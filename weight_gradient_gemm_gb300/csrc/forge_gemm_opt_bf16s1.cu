@@ -1,0 +1,14 @@
+// Instantiates the tensor-core kernel for the optimizers with one bf16
+// state (SGD with momentum, Adagrad, RMSprop, Lion): their state slots hold
+// W and that state alone, which leaves shared memory for more operand stages
+// and slots.
+#include "forge_gemm.cuh"
+
+namespace forge {
+
+cudaError_t launch_gemm_opt_bf16s1(const GemmConfig& cfg, const GemmArgs& args,
+                                  cudaStream_t stream) {
+  return launch_gemm_fmt<kModeOpt, kFmtBF16S1>(cfg, args, stream);
+}
+
+}  // namespace forge

@@ -44,8 +44,19 @@ __host__ __device__ constexpr bool has_state(int mode) {
 enum Prof : int { kProfStream = 0, kProfMma = 1, kProfBalanced = 2, kProfDeep = 3 };
 // Epilogue formats: fused moment formats 0..3 (fp32, bf16, int8 blocks of
 // 128, fp8 e4m3 with per-tensor scales); store-G dW formats 0..1 (fp32, bf16);
-// kFmtNone: an optimizer without state (SGD), whose slots hold W alone.
-enum Fmt : int { kFmtF32 = 0, kFmtBF16 = 1, kFmtI8 = 2, kFmtF8 = 3, kFmtNone = 4 };
+// kFmtNone: an optimizer without state (SGD), whose slots hold W alone;
+// kFmtF32S1, kFmtBF16S1: an optimizer with one state (fp32 or bf16), whose
+// slots hold W and that state only.
+enum Fmt : int { kFmtF32 = 0, kFmtBF16 = 1, kFmtI8 = 2, kFmtF8 = 3, kFmtNone = 4,
+                 kFmtF32S1 = 5, kFmtBF16S1 = 6 };
+// The element format of an optimizer state format (fp32 or bf16).
+__host__ __device__ constexpr int state_elem_fmt(int fmt) {
+  return (fmt == kFmtF32S1) ? kFmtF32 : (fmt == kFmtBF16S1 ? kFmtBF16 : fmt);
+}
+// State boxes a slot holds.
+__host__ __device__ constexpr int state_boxes(int fmt) {
+  return fmt == kFmtNone ? 0 : ((fmt == kFmtF32S1 || fmt == kFmtBF16S1) ? 1 : 2);
+}
 
 // Most linear layers one launch can step (a grouped launch walks one tile
 // queue across all of them).

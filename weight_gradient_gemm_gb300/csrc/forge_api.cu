@@ -428,12 +428,16 @@ GemmConfig choose_opt_config(int64_t bt, int fmt, int nstate) {
            : bt <= 3072 ? (efmt == kFmtBF16 ? kProfBalanced : kProfMma)
                         : kProfDeep;
   }
+  if (nstate == 1 && bt <= one_cta_upto && efmt == kFmtF32) c.prof = kProfStream;
   c = finish_config(c, bt, efmt, kModeFused);
-  if (nstate == 0 && bt <= one_cta_upto && current_tuning().bn != 128) {
-    // SGD carries no state: its slots hold W alone (8 KB), so the balanced
-    // profile with 256-wide tiles keeps four operand stages beside four
-    // slots for its main-loop-bound step (512 tokens: 0.41 of HBM with
-    // AdamW's slot layout, 0.59 now)
+  if (nstate <= 1 && bt <= one_cta_upto && current_tuning().bn != 128) {
+    // Slots that hold W alone (SGD, 8 KB) or W and one state (24 KB fp32,
+    // 16 KB bf16) leave room for 256-wide tiles on one CTA, which halve the
+    // main loop's A re-reads.  Sweeps over the layer at 512 tokens, against
+    // AdamW's slot layout and 128-wide tiles: SGD 0.41 -> 0.59 of HBM
+    // (balanced); SGD with momentum, Adagrad, RMSprop and Lion with fp32
+    // states 0.68-0.82 -> 0.90-0.93 (stream profile), bf16 states
+    // 0.55-0.72 -> 0.70-0.79 (balanced).
     c.bn = 256;
   }
   // the state stream's L2 prefetch was measured for AdamW only

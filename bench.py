@@ -835,6 +835,48 @@ TENSOR_BLOCKS = [
 ]
 
 
+def dgrad_block(F, group, bt, n, stream, sampler, peaks):
+    """dX = dY W for the seven projections at a tensor-bound token count: one
+    forge_dgrad_grouped launch (caller workspace) against cuBLAS's seven
+    torch.matmul calls on the same tensors, each timed per step with CUDA
+    events, alternating three rounds so both see the same clocks."""
+    dx = [torch.empty((bt, g["W"].shape[1]), dtype=torch.bfloat16, device=g["W"].device)
+          for g in group]
+    items = [dict(dY=g["dY"], W=g["W"], dX=o) for g, o in zip(group, dx)]
+    ws_bytes = F.dgrad_workspace_bytes(items)
+    ws = (torch.empty(max(1, ws_bytes // 4), dtype=torch.float32, device=dx[0].device)
+          if ws_bytes else None)
+
+    def forge_dx():
+        F.dgrad_grouped(items, workspace=ws)
+
+    def cublas_dx():
+        for g, o in zip(group, dx):
+            torch.matmul(g["dY"], g["W"], out=o)
+    for _ in range(3):
+        forge_dx()
+        cublas_dx()
+    f_ms, c_ms, f_win = [], [], []
+    for _ in range(3):
+        ms, w0, w1 = timed_launches(forge_dx, max(10, n // 3), stream)
+        f_ms += ms
+        f_win.append((w0, w1))
+        ms, _, _ = timed_launches(cublas_dx, max(10, n // 3), stream)
+        c_ms += ms
+    if F.device_error() != 0:
+        raise RuntimeError("dgrad block: device error")
+    flops = sum(2.0 * bt * g["W"].numel() for g in group)
+    f_med, c_med = statistics.median(f_ms), statistics.median(c_ms)
+    tf = flops / (f_med * 1e-3) / 1e12
+    del dx, items, ws
+    return {"launch": "forge_dgrad_grouped: the seven projections in one launch",
+            "ms_per_step": f_med, "tflops": tf,
+            "frac": tf / peaks["bf16_tflops"], "per_launch": launch_stats(f_ms),
+            "workspace_bytes": ws_bytes,
+            "cublas_ms_per_step": c_med, "vs_cublas": c_med / f_med,
+            "clocks": sampler.summary(f_win[0][0], f_win[-1][1])}
+
+
 def config_blocks(args, dev, peaks, peak_kind):
     """The metric's other Llama-3.1-8B configurations, each timed in-process
     with CUDA events around every grouped launch (at least ~0.3 s of
@@ -843,7 +885,8 @@ def config_blocks(args, dev, peaks, peak_kind):
     is the grouped launch plus the scale roll), C3 at 2048 and 8192 tokens
     (bf16 moments), C4 at 4096 (int8), fp32 moments at 4096, and C5 (the
     224-linear stack at 512 and 8192 tokens, fp32 moments, one grouped launch
-    per layer)."""
+    per layer).  The 4096-token fp32 block also times the layer's input
+    gradient (dgrad_block)."""
     from weight_gradient_gemm_gb300 import forge as F
     stream = torch.cuda.current_stream()
     sampler = ClockSampler(dev.index)
@@ -886,6 +929,8 @@ def config_blocks(args, dev, peaks, peak_kind):
             cub = {"ms_per_step": cmean * 1e3, "tflops": flops / cmean / 1e12,
                    "fused_vs_cublas_gemm": cmean / mean_s, "clocks": sampler.summary(c0, c1)}
             del outs
+        dgrad = dgrad_block(F, group, bt, n, stream, sampler, peaks) if bt == 4096 and fmt == 0 \
+            else None
         out[name] = {"workload": workload, "bt": bt, "moments": FMT_NAMES[fmt],
                      "launch": "forge_wgrad_adamw_grouped, seven projections",
                      "kernel": F.describe_config(bt, 4096, 4096, fmt),
@@ -894,6 +939,8 @@ def config_blocks(args, dev, peaks, peak_kind):
                                              stored_traffic(workload)),
                      "per_launch": launch_stats(ms), "clocks": sampler.summary(w0, w1),
                      "cublas_wgrad_gemm": cub}
+        if dgrad is not None:
+            out[name]["dgrad"] = dgrad
         del group, f8
         torch.cuda.empty_cache()
     # C5: the whole stack at 512 and 8192 tokens

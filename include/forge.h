@@ -82,7 +82,8 @@ typedef enum {
                                    with d_in % 16 != 0, or a size over the 32-bit
                                    index range of the kernels                        */
   FORGE_ERR_FORMAT = 4,         /* unknown moment format or dtype                     */
-  FORGE_ERR_HYPER = 5,          /* step < 1, beta outside [0,1), lr/eps/wd < 0 or NaN */
+  FORGE_ERR_HYPER = 5,          /* step < 1, beta outside [0,1), lr/wd < 0 or NaN, eps neither
+                                   0 nor a normal fp32 number at most 2^64 */
   FORGE_ERR_ALIAS = 6,          /* an input overlaps an output                        */
   FORGE_ERR_ARCH = 7,           /* current device is not sm_103 (no fallback exists)  */
   FORGE_ERR_LAUNCH = 8,         /* a kernel launch or TMA descriptor encode failed    */

@@ -100,6 +100,8 @@ def test_fused_argument_errors(L):
     assert fused(L, b2=-0.1) == 5
     assert fused(L, lr=float("nan")) == 5
     assert fused(L, eps=-1.0) == 5
+    assert fused(L, eps=1e-40) == 5          # eps: 0 or a normal number ...
+    assert fused(L, eps=2.0 ** 65) == 5      # ... at most 2^64
     assert fused(L, X=C) == 6                        # FORGE_ERR_ALIAS: X is W
     assert fused(L, dY=D + 64) == 6                  # dY inside m
     assert fused(L, v=(D, None)) == 6                # m and v the same buffer
@@ -195,6 +197,7 @@ def test_wgrad_opt_argument_errors(L):
     assert opt_call(L, step=0) == 5
     assert opt_call(L, opt=4, beta1=1.0) == 5                # Lion betas in [0, 1)
     assert opt_call(L, opt=2, eps=-1.0) == 5                 # Adagrad eps >= 0
+    assert opt_call(L, opt=3, eps=1e-40) == 5                # RMSprop eps subnormal
     assert opt_call(L, opt=3, alpha=1.0) == 5                # RMSprop alpha < 1
     assert opt_call(L, momentum=float("nan")) == 5
     assert opt_call(L, lr=float("inf")) == 5

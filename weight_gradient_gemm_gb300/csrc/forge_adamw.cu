@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(256) adamw_int8_kernel(const void* __restrict_
   for (int64_t b = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
        b < nblocks; b += warps) {
     const int64_t e0 = b * 128 + 4 * lane;   // first element of this lane
-    float g[4], w[4], mm[4], vv[4], rr[4];
+    float g[4], w[4], mm[4], rr[4];
     if constexpr (DW == 0) {
       const float4 a = __ldcs(reinterpret_cast<const float4*>(dW) + e0 / 4);
       g[0] = a.x; g[1] = a.y; g[2] = a.z; g[3] = a.w;
@@ -130,23 +130,19 @@ __global__ void __launch_bounds__(256) adamw_int8_kernel(const void* __restrict_
     uint32_t* mp = reinterpret_cast<uint32_t*>(mq) + e0 / 4;
     uint32_t* vp = reinterpret_cast<uint32_t*>(vq) + e0 / 4;
     const uint32_t mc = __ldcs(mp), vc = __ldcs(vp);
-    const float sm = m_scale[b], sv = v_scale[b];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      mm[k] = dequant_mf(i8_code_float(mc ^ 0x80808080u, k), sm);
-      vv[k] = dequant_vf(i8_code_float(vc ^ 0x80808080u, k), sv);
-    }
+    const float2 sm = dup2(m_scale[b]), sv = dup2(v_scale[b]);
     float amax_m = 0.0f, amax_r = 0.0f;
 #pragma unroll
     for (int k = 0; k < 4; k += 2) {
-      float2 w2 = make_float2(w[k], w[k + 1]), m2 = make_float2(mm[k], mm[k + 1]);
-      float2 v2 = make_float2(vv[k], vv[k + 1]), r2;
+      float2 w2 = make_float2(w[k], w[k + 1]);
+      float2 m2 = dequant_m2(i8_code_pair(mc ^ 0x80808080u, k), sm);
+      float2 v2 = dequant_v2(i8_code_pair(vc ^ 0x80808080u, k), sv), r2;
       adamw_elem2(make_float2(g[k], g[k + 1]), w2, m2, v2, r2, h);
       w[k] = w2.x; w[k + 1] = w2.y;
       mm[k] = m2.x; mm[k + 1] = m2.y;
       rr[k] = r2.x; rr[k + 1] = r2.y;
-      amax_m = fmaxf(amax_m, fmaxf(fabsf(mm[k]), fabsf(mm[k + 1])));
-      amax_r = fmaxf(amax_r, fmaxf(rr[k], rr[k + 1]));
+      amax_m = max3_abs(amax_m, mm[k], mm[k + 1]);
+      amax_r = max3(amax_r, rr[k], rr[k + 1]);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {

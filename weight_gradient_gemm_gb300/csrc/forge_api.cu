@@ -2,6 +2,7 @@
 // tile configuration, launches and the device error word.
 #include <algorithm>
 #include <cstdint>
+#include <cfloat>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -241,11 +242,15 @@ forge_status check_shape(int64_t bt, int64_t d_in, int64_t d_out) {
   return FORGE_OK;
 }
 
+// eps is 0 or a normal fp32 number at most 2^64: the kernels' reciprocal of
+// the AdamW-style denominator flushes subnormals, which then never occur.
+bool eps_ok(float eps) { return eps == 0.0f || (eps >= FLT_MIN && eps <= 0x1p64f); }
+
 forge_status check_hyper(float lr, float b1, float b2, float eps, float wd, int64_t step) {
   if (step < 1) return FORGE_ERR_HYPER;
   if (!(b1 >= 0.0f && b1 < 1.0f) || !(b2 >= 0.0f && b2 < 1.0f)) return FORGE_ERR_HYPER;
-  if (!(lr >= 0.0f) || !(eps >= 0.0f) || !(wd >= 0.0f)) return FORGE_ERR_HYPER;
-  if (!std::isfinite(lr) || !std::isfinite(eps) || !std::isfinite(wd)) return FORGE_ERR_HYPER;
+  if (!(lr >= 0.0f) || !(wd >= 0.0f) || !eps_ok(eps)) return FORGE_ERR_HYPER;
+  if (!std::isfinite(lr) || !std::isfinite(wd)) return FORGE_ERR_HYPER;
   return FORGE_OK;
 }
 
@@ -312,7 +317,7 @@ forge_status check_opt_hyper(int opt, const forge_opt_hyper& h, int64_t step) {
   if ((opt == kOptLion || opt == kOptNadam || opt == kOptRadam) &&
       (!unit(h.beta1) || !unit(h.beta2)))
     return FORGE_ERR_HYPER;
-  if (opt != kOptSgd && opt != kOptSgdMomentum && opt != kOptLion && !nonneg(h.eps))
+  if (opt != kOptSgd && opt != kOptSgdMomentum && opt != kOptLion && !eps_ok(h.eps))
     return FORGE_ERR_HYPER;
   if (opt == kOptSgdMomentum && !unit(h.momentum)) return FORGE_ERR_HYPER;
   if (opt == kOptRmsprop && !unit(h.alpha)) return FORGE_ERR_HYPER;

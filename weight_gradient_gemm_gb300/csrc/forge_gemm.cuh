@@ -266,9 +266,13 @@ __device__ __forceinline__ void epi_slice_fused_16(uint32_t taddr, bool zero_gra
   uint32_t graw[16];
   tmem_ld_x16(taddr, graw);
   tmem_ld_wait();
+  if (zero_grad) {   // warp-uniform: no accumulator was written
+#pragma unroll
+    for (int i = 0; i < 16; ++i) graw[i] = 0u;
+  }
   float g[16], w[16], m[16], v[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) g[i] = zero_grad ? 0.0f : __uint_as_float(graw[i]);
+  for (int i = 0; i < 16; ++i) g[i] = __uint_as_float(graw[i]);
 
   uint8_t* wbox = slot;                 // [RPS][32] bf16: 64-byte rows
   uint8_t* mbox = slot + kWBytes;
@@ -361,18 +365,18 @@ __device__ __forceinline__ void epi_slice_fused_16(uint32_t taddr, bool zero_gra
   }
 }
 
-// 32 int8 codes (two 16-byte chunks) as floats, without conversion
-// instructions (i8_code_float).
-__device__ __forceinline__ void load_codes32(const uint8_t* box, uint32_t row, int chunk0,
-                                             float (&q)[32]) {
+// 32 int8 codes (two 16-byte chunks) as 16 pairs of floats, without
+// conversion instructions (i8_code_pair).
+__device__ __forceinline__ void load_code_pairs32(const uint8_t* box, uint32_t row, int chunk0,
+                                                  float2 (&q)[16]) {
   const uint4 a = *reinterpret_cast<const uint4*>(box + sw128_off(row, chunk0));
   const uint4 b = *reinterpret_cast<const uint4*>(box + sw128_off(row, chunk0 + 1));
   const uint32_t words[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const uint32_t off = words[i] ^ 0x80808080u;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) q[4 * i + k] = i8_code_float(off, k);
+    q[2 * i] = i8_code_pair(off, 0);
+    q[2 * i + 1] = i8_code_pair(off, 2);
   }
 }
 // Store 32 codes, each in the low byte of its word (quant_m_bits / quant_r_bits).
@@ -418,14 +422,19 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, uint32_t sadd
   uint8_t* mbox = slot + kWBytes;              // [RPS][128] int8
   uint8_t* vbox = mbox + kMBytes;
   float amax_m = 0.0f, amax_r = 0.0f;
+  const float2 sm2 = dup2(sm_old), sv2 = dup2(sv_old);
 #pragma unroll 1
   for (int c = 0; c < 2; ++c) {
     uint32_t graw[32];
     tmem_ld_x32(taddr + 32 * c, graw);
     tmem_ld_wait();
-    float qm[32], qv[32];
-    load_codes32(mbox, row, 4 * h + 2 * c, qm);
-    load_codes32(vbox, row, 4 * h + 2 * c, qv);
+    if (zero_grad) {   // warp-uniform: no accumulator was written
+#pragma unroll
+      for (int i = 0; i < 32; ++i) graw[i] = 0u;
+    }
+    float2 qm[16], qv[16];
+    load_code_pairs32(mbox, row, 4 * h + 2 * c, qm);
+    load_code_pairs32(vbox, row, 4 * h + 2 * c, qv);
     uint4 wq[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k)
@@ -434,24 +443,16 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, uint32_t sadd
     uint32_t wo[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      float w0 = bf16_lo(wu[i]), w1 = bf16_hi(wu[i]);
-      float g0 = zero_grad ? 0.0f : __uint_as_float(graw[2 * i]);
-      float g1 = zero_grad ? 0.0f : __uint_as_float(graw[2 * i + 1]);
-      float2 w2 = make_float2(w0, w1);
-      float2 m2 = make_float2(dequant_mf(qm[2 * i], sm_old), dequant_mf(qm[2 * i + 1], sm_old));
-      float2 v2 = make_float2(dequant_vf(qv[2 * i], sv_old), dequant_vf(qv[2 * i + 1], sv_old));
-      float2 r2;
-      adamw_elem2(make_float2(g0, g1), w2, m2, v2, r2, hc);
-      w0 = w2.x; w1 = w2.y;
-      const float m0 = m2.x, m1 = m2.y, r0 = r2.x, r1 = r2.y;
-      amax_m = fmaxf(amax_m, fmaxf(fabsf(m0), fabsf(m1)));
-      amax_r = fmaxf(amax_r, fmaxf(r0, r1));
-      wo[i] = pack_bf16x2(w0, w1);
+      float2 w2 = make_float2(bf16_lo(wu[i]), bf16_hi(wu[i]));
+      const float2 g2 = make_float2(__uint_as_float(graw[2 * i]), __uint_as_float(graw[2 * i + 1]));
+      float2 m2 = dequant_m2(qm[i], sm2), v2 = dequant_v2(qv[i], sv2), r2;
+      adamw_elem2(g2, w2, m2, v2, r2, hc);
+      amax_m = max3_abs(amax_m, m2.x, m2.y);
+      amax_r = max3(amax_r, r2.x, r2.y);
+      wo[i] = pack_bf16x2(w2.x, w2.y);
       if constexpr (STASH) {   // the old codes are consumed: reuse their registers
-        qm[2 * i] = m0;
-        qm[2 * i + 1] = m1;
-        qv[2 * i] = r0;
-        qv[2 * i + 1] = r1;
+        qm[i] = m2;
+        qv[i] = r2;
       }
     }
 #pragma unroll
@@ -461,9 +462,11 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, uint32_t sadd
     if constexpr (STASH) {
       uint32_t su[32], sv[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        su[i] = __float_as_uint(qm[i]);
-        sv[i] = __float_as_uint(qv[i]);
+      for (int i = 0; i < 16; ++i) {
+        su[2 * i] = __float_as_uint(qm[i].x);
+        su[2 * i + 1] = __float_as_uint(qm[i].y);
+        sv[2 * i] = __float_as_uint(qv[i].x);
+        sv[2 * i + 1] = __float_as_uint(qv[i].y);
       }
       tmem_st_x32(saddr + 64 * c, su);
       tmem_st_x32(saddr + 64 * c + 32, sv);
@@ -482,6 +485,7 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, uint32_t sadd
   amax_r = fmaxf(amax_r, xch[((1 - h) * 2 + 1) * kBM + trow]);
   mbar_arrive(bar_xch_read);
   const float inv_m = int8_inv_step(amax_m), inv_r = int8_inv_step(amax_r);
+  const float2 inv_m2 = dup2(inv_m), inv_r2 = dup2(inv_r);
   const float r_floor = amax_r > 0.0f ? 1.0f : 0.0f;   // codes >= 1 in a non-zero block
 #pragma unroll 1
   for (int c = 0; c < 2; ++c) {
@@ -492,30 +496,31 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, uint32_t sadd
       tmem_ld_x32(saddr + 64 * c + 32, rs);
       tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        bm[i] = quant_m_bits(__uint_as_float(ms[i]), inv_m);
-        bv[i] = quant_r_bits(__uint_as_float(rs[i]), inv_r, r_floor);
+      for (int i = 0; i < 32; i += 2) {
+        quant_m_bits2(make_float2(__uint_as_float(ms[i]), __uint_as_float(ms[i + 1])), inv_m2,
+                      bm[i], bm[i + 1]);
+        quant_r_bits2(make_float2(__uint_as_float(rs[i]), __uint_as_float(rs[i + 1])), inv_r2,
+                      r_floor, bv[i], bv[i + 1]);
       }
     } else {
       uint32_t graw[32];
       tmem_ld_x32(taddr + 32 * c, graw);
       tmem_ld_wait();
-      float qm[32], qv[32];
-      load_codes32(mbox, row, 4 * h + 2 * c, qm);
-      load_codes32(vbox, row, 4 * h + 2 * c, qv);
+      if (zero_grad) {
 #pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        const float2 g = zero_grad ? make_float2(0.0f, 0.0f)
-                                   : make_float2(__uint_as_float(graw[i]),
-                                                 __uint_as_float(graw[i + 1]));
+        for (int i = 0; i < 32; ++i) graw[i] = 0u;
+      }
+      float2 qm[16], qv[16];
+      load_code_pairs32(mbox, row, 4 * h + 2 * c, qm);
+      load_code_pairs32(vbox, row, 4 * h + 2 * c, qv);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float2 g = make_float2(__uint_as_float(graw[2 * i]), __uint_as_float(graw[2 * i + 1]));
         float2 w = make_float2(0.0f, 0.0f), r;
-        float2 m = make_float2(dequant_mf(qm[i], sm_old), dequant_mf(qm[i + 1], sm_old));
-        float2 v = make_float2(dequant_vf(qv[i], sv_old), dequant_vf(qv[i + 1], sv_old));
+        float2 m = dequant_m2(qm[i], sm2), v = dequant_v2(qv[i], sv2);
         adamw_elem2(g, w, m, v, r, hc);
-        bm[i] = quant_m_bits(m.x, inv_m);
-        bm[i + 1] = quant_m_bits(m.y, inv_m);
-        bv[i] = quant_r_bits(r.x, inv_r, r_floor);
-        bv[i + 1] = quant_r_bits(r.y, inv_r, r_floor);
+        quant_m_bits2(m, inv_m2, bm[2 * i], bm[2 * i + 1]);
+        quant_r_bits2(r, inv_r2, r_floor, bv[2 * i], bv[2 * i + 1]);
       }
     }
     store_codes32(mbox, row, 4 * h + 2 * c, bm);
@@ -547,6 +552,10 @@ __device__ __forceinline__ void epi_slice_fused_f8(uint32_t taddr, bool zero_gra
     uint32_t graw[32];
     tmem_ld_x32(taddr + 32 * c, graw);
     tmem_ld_wait();
+    if (zero_grad) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) graw[i] = 0u;
+    }
 #pragma unroll
     for (int p16 = 0; p16 < 2; ++p16) {
       const int chunk = 4 * h + 2 * c + p16;     // 16 codes of m and of r
@@ -564,7 +573,7 @@ __device__ __forceinline__ void epi_slice_fused_f8(uint32_t taddr, bool zero_gra
         w[2 * i + 1] = bf16_hi(wu[i]);
       }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) g[i] = zero_grad ? 0.0f : __uint_as_float(graw[16 * p16 + i]);
+      for (int i = 0; i < 16; ++i) g[i] = __uint_as_float(graw[16 * p16 + i]);
       adamw_fp8_x16(g, w, mq, rq, fm, fr, hc, amax_m, amax_r);
       uint32_t wo[8];
 #pragma unroll

@@ -33,9 +33,16 @@ __device__ __forceinline__ float sqrt_approx(float x) {
   asm("sqrt.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// The reciprocal flushes subnormal inputs and results (.ftz), which skips the
+// subnormal handling of the plain form.  Every denominator it is given is
+// sqrt(.) * c + eps or sqrt(.) + eps with c in [1, 2^12] (c = 1/sqrt(1 -
+// beta2^t), beta2 < 1 in fp32), sqrt(.) below 2^64 and eps either 0 or a
+// normal number at most 2^64 (the host rejects other eps): so the input is
+// 0, infinite, NaN or normal and below 2^77, the result is never subnormal,
+// and the flush never changes a bit.
 __device__ __forceinline__ float rcp_approx(float x) {
   float y;
-  asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
@@ -57,10 +64,14 @@ __device__ __forceinline__ void adamw_elem(float g, float& w, float& m, float& v
   r = r1;
 }
 
-// Paired fp32 arithmetic (PTX mul/fma .rn.f32x2, sm_100 and later): each
-// lane is an IEEE round-to-nearest multiply or fused multiply-add, so the
-// results are those of __fmul_rn / __fmaf_rn bit for bit, in half the
-// instructions.
+// Paired fp32 arithmetic (PTX mul/add/fma .rn.f32x2, sm_100 and later): each
+// lane is an IEEE round-to-nearest multiply, add or fused multiply-add, so the
+// results are those of __fmul_rn / __fadd_rn / __fmaf_rn bit for bit, in half
+// the instructions.  Unlike the scalar forms with an explicit rounding, a
+// paired multiply whose result feeds a paired add was measured to come out
+// as one fused multiply-add (a single rounding; 30 of 16.8 M int8 codes
+// differed by one level from the scalar pair); so no paired multiply here
+// feeds an add: where that arithmetic is wanted it is an explicit fma2.
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
   float2 d;
   asm("{.reg .b64 ra, rb, rd;\n\t"
@@ -79,7 +90,30 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
   return d;
 }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 d;
+  asm("{.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
 __device__ __forceinline__ float2 dup2(float x) { return make_float2(x, x); }
+
+// max(a, b, c) and max(|a|, |b|, |c|) in one instruction (three-input PTX
+// max, sm_100 and later).  Like fmaxf, a NaN input is ignored when another
+// input is a number.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float max3_abs(float a, float b, float c) {
+  float d;
+  asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 
 // adamw_elem on two elements at once: the same operations in the same order
 // on each lane (paired multiplies and multiply-adds), so each lane's results
@@ -224,37 +258,55 @@ __device__ __forceinline__ float int8_inv_step(float absmax) {
 }
 // Codes without conversion instructions.  y = x * (127 / a) with |x| <= a
 // (a the block's absmax of the same fp32 values) satisfies |y| < 127.0001,
-// so round(y) is already in [-127, 127]; adding 1.5 * 2^23 rounds y to the
-// nearest integer (ties to even, as the rounding of the add itself) and
-// leaves it in the low bits of the sum, so the low byte of the sum's bit
-// pattern is the two's-complement code.  The second moment's floor of one
-// level in a non-zero block is a max on y before rounding: round(max(y, 1))
-// equals max(round(y), 1) for y >= 0.
+// so round(y) is already in [-127, 127].  One fused multiply-add forms
+// x * inv + 1.5 * 2^23 with a single rounding to the nearest integer (ties to
+// even), which leaves round(x * inv) in the low bits of the sum: the low
+// byte of its bit pattern is the two's-complement code.  (The product is not
+// rounded on its own first: the code is the integer nearest to the exact
+// x * inv, inv = 127 / a rounded to fp32.)  The second moment's floor of one
+// level in a non-zero block is a max after rounding: max(round(y), 1) equals
+// round(max(y, 1)) for y >= 0.
 constexpr float kRoundMagic = 12582912.0f;   // 1.5 * 2^23
 __device__ __forceinline__ uint32_t quant_m_bits(float x, float inv) {
-  return __float_as_uint(__fadd_rn(__fmul_rn(x, inv), kRoundMagic));
+  return __float_as_uint(__fmaf_rn(x, inv, kRoundMagic));
 }
 __device__ __forceinline__ uint32_t quant_r_bits(float r, float inv, float floor_level) {
-  return __float_as_uint(__fadd_rn(fmaxf(__fmul_rn(r, inv), floor_level), kRoundMagic));
+  return __float_as_uint(fmaxf(__fmaf_rn(r, inv, kRoundMagic), kRoundMagic + floor_level));
 }
 // The low bytes of four words, in order, as one word of four codes.
 __device__ __forceinline__ uint32_t pack_low_bytes4(uint32_t a, uint32_t b, uint32_t c,
                                                     uint32_t d) {
   return __byte_perm(__byte_perm(a, b, 0x0040u), __byte_perm(c, d, 0x0040u), 0x5410u);
 }
-// Code k (0..3) of a word of four int8 codes, as a float: with the word's
-// bytes offset by 128 (w ^ 0x80808080), 2^23 + (code + 128) is assembled by a
-// byte permute and 2^23 + 128 subtracted exactly.
-__device__ __forceinline__ float i8_code_float(uint32_t w_offset, int k) {
-  return __fsub_rn(__uint_as_float(__byte_perm(w_offset, 0x4B000000u, 0x7540u | k)),
-                   8388736.0f);
+// Codes k and k + 1 (k = 0 or 2) of a word of four int8 codes, as floats:
+// with the word's bytes offset by 128 (w ^ 0x80808080), 2^23 + (code + 128)
+// is assembled by a byte permute and 2^23 + 128 subtracted exactly (one
+// paired add).
+__device__ __forceinline__ float2 i8_code_pair(uint32_t w_offset, int k) {
+  const float2 biased =
+      make_float2(__uint_as_float(__byte_perm(w_offset, 0x4B000000u, 0x7540u | k)),
+                  __uint_as_float(__byte_perm(w_offset, 0x4B000000u, 0x7540u | (k + 1))));
+  return add2(biased, dup2(-8388736.0f));
+}
+// quant_m_bits / quant_r_bits on two values with one paired multiply-add.
+__device__ __forceinline__ void quant_m_bits2(float2 x, float2 inv, uint32_t& b0, uint32_t& b1) {
+  const float2 q = fma2(x, inv, dup2(kRoundMagic));
+  b0 = __float_as_uint(q.x);
+  b1 = __float_as_uint(q.y);
+}
+__device__ __forceinline__ void quant_r_bits2(float2 r, float2 inv, float floor_level,
+                                              uint32_t& b0, uint32_t& b1) {
+  const float2 q = fma2(r, inv, dup2(kRoundMagic));
+  const float lo = kRoundMagic + floor_level;
+  b0 = __float_as_uint(fmaxf(q.x, lo));
+  b1 = __float_as_uint(fmaxf(q.y, lo));
 }
 
-// Decoded int8 values (the code as a float): m = code * s; v = (code * s)^2.
-__device__ __forceinline__ float dequant_mf(float code, float s) { return __fmul_rn(code, s); }
-__device__ __forceinline__ float dequant_vf(float code, float s) {
-  const float r = __fmul_rn(code, s);
-  return __fmul_rn(r, r);
+// Decoded int8 values (two codes as floats): m = code * s; v = (code * s)^2.
+__device__ __forceinline__ float2 dequant_m2(float2 code, float2 s) { return mul2(code, s); }
+__device__ __forceinline__ float2 dequant_v2(float2 code, float2 s) {
+  const float2 r = mul2(code, s);
+  return mul2(r, r);
 }
 
 // ---------------------------------------------------------------------------
@@ -321,8 +373,8 @@ __device__ __forceinline__ void adamw_fp8_x16(const float (&g)[16], float (&w)[1
       adamw_elem2(make_float2(g[i], g[i + 1]), ww, mm, vv, rr, h);
       w[i] = ww.x;
       w[i + 1] = ww.y;
-      amax_m = fmaxf(amax_m, fmaxf(fabsf(mm.x), fabsf(mm.y)));
-      amax_r = fmaxf(amax_r, fmaxf(rr.x, rr.y));
+      amax_m = max3_abs(amax_m, mm.x, mm.y);
+      amax_r = max3(amax_r, rr.x, rr.y);
       const float2 me = mul2(mm, dup2(fm.inv_write));
       const float2 re = mul2(rr, dup2(fr.inv_write));
       mpack |= float2_to_e4m3x2(me.x, me.y) << (16 * half);

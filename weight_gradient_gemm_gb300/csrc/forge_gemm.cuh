@@ -263,16 +263,11 @@ __device__ __forceinline__ void epi_slice_fused_16(uint32_t taddr, bool zero_gra
                                                    uint32_t grow, uint32_t gcol16) {
   constexpr int kWBytes = RPS * 32 * 2;
   constexpr int kMBytes = RPS * 32 * (FMT == kFmtF32 ? 4 : 2);
+  // the accumulator load runs while the slot's W, m and v are read from
+  // shared memory; its registers are read only after the wait
   uint32_t graw[16];
   tmem_ld_x16(taddr, graw);
-  tmem_ld_wait();
-  if (zero_grad) {   // warp-uniform: no accumulator was written
-#pragma unroll
-    for (int i = 0; i < 16; ++i) graw[i] = 0u;
-  }
   float g[16], w[16], m[16], v[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) g[i] = __uint_as_float(graw[i]);
 
   uint8_t* wbox = slot;                 // [RPS][32] bf16: 64-byte rows
   uint8_t* mbox = slot + kWBytes;
@@ -312,6 +307,13 @@ __device__ __forceinline__ void epi_slice_fused_16(uint32_t taddr, bool zero_gra
       v[2 * i] = bf16_lo(vu[i]); v[2 * i + 1] = bf16_hi(vu[i]);
     }
   }
+  tmem_ld_wait();
+  if (zero_grad) {   // warp-uniform: no accumulator was written
+#pragma unroll
+    for (int i = 0; i < 16; ++i) graw[i] = 0u;
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) g[i] = __uint_as_float(graw[i]);
 #pragma unroll
   for (int i = 0; i < 16; i += 2) {
     float2 w2 = make_float2(w[i], w[i + 1]), m2 = make_float2(m[i], m[i + 1]);
@@ -426,12 +428,7 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, uint32_t sadd
 #pragma unroll 1
   for (int c = 0; c < 2; ++c) {
     uint32_t graw[32];
-    tmem_ld_x32(taddr + 32 * c, graw);
-    tmem_ld_wait();
-    if (zero_grad) {   // warp-uniform: no accumulator was written
-#pragma unroll
-      for (int i = 0; i < 32; ++i) graw[i] = 0u;
-    }
+    tmem_ld_x32(taddr + 32 * c, graw);   // in flight while the codes and W are read
     float2 qm[16], qv[16];
     load_code_pairs32(mbox, row, 4 * h + 2 * c, qm);
     load_code_pairs32(vbox, row, 4 * h + 2 * c, qv);
@@ -440,6 +437,11 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, uint32_t sadd
     for (int k = 0; k < 4; ++k)
       wq[k] = *reinterpret_cast<const uint4*>(wbox + sw128_off(row, 4 * c + k));
     const uint32_t* wu = reinterpret_cast<const uint32_t*>(wq);
+    tmem_ld_wait();
+    if (zero_grad) {   // warp-uniform: no accumulator was written
+#pragma unroll
+      for (int i = 0; i < 32; ++i) graw[i] = 0u;
+    }
     uint32_t wo[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -472,7 +474,14 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, uint32_t sadd
       tmem_st_x32(saddr + 64 * c + 32, sv);
     }
   }
-  if constexpr (STASH) tmem_st_wait();
+  // the second pass's first stash chunk (this thread's own m', r') is read
+  // from tensor memory while the row's two halves meet
+  uint32_t ms[32], rs[32];
+  if constexpr (STASH) {
+    tmem_st_wait();
+    tmem_ld_x32(saddr, ms);
+    tmem_ld_x32(saddr + 32, rs);
+  }
   // combine the row's two halves
   bool ok = wait_bounded(bar_xch_read, xphase ^ 1u, wc, kSiteEpiExchange);
   if (!__all_sync(0xffffffffu, ok)) return false;
@@ -491,9 +500,10 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, uint32_t sadd
   for (int c = 0; c < 2; ++c) {
     uint32_t bm[32], bv[32];
     if constexpr (STASH) {
-      uint32_t ms[32], rs[32];
-      tmem_ld_x32(saddr + 64 * c, ms);
-      tmem_ld_x32(saddr + 64 * c + 32, rs);
+      if (c == 1) {
+        tmem_ld_x32(saddr + 64, ms);
+        tmem_ld_x32(saddr + 96, rs);
+      }
       tmem_ld_wait();
 #pragma unroll
       for (int i = 0; i < 32; i += 2) {
@@ -505,14 +515,14 @@ __device__ __forceinline__ bool epi_slice_fused_i8(uint32_t taddr, uint32_t sadd
     } else {
       uint32_t graw[32];
       tmem_ld_x32(taddr + 32 * c, graw);
+      float2 qm[16], qv[16];
+      load_code_pairs32(mbox, row, 4 * h + 2 * c, qm);
+      load_code_pairs32(vbox, row, 4 * h + 2 * c, qv);
       tmem_ld_wait();
       if (zero_grad) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) graw[i] = 0u;
       }
-      float2 qm[16], qv[16];
-      load_code_pairs32(mbox, row, 4 * h + 2 * c, qm);
-      load_code_pairs32(vbox, row, 4 * h + 2 * c, qv);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const float2 g = make_float2(__uint_as_float(graw[2 * i]), __uint_as_float(graw[2 * i + 1]));
@@ -551,6 +561,14 @@ __device__ __forceinline__ void epi_slice_fused_f8(uint32_t taddr, bool zero_gra
   for (int c = 0; c < 2; ++c) {
     uint32_t graw[32];
     tmem_ld_x32(taddr + 32 * c, graw);
+    // the first 16 columns' codes and W are read while the accumulator load
+    // is in flight
+    uint4 mq = *reinterpret_cast<const uint4*>(mbox + sw128_off(row, 4 * h + 2 * c));
+    uint4 rq = *reinterpret_cast<const uint4*>(vbox + sw128_off(row, 4 * h + 2 * c));
+    uint4 wq[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+      wq[k] = *reinterpret_cast<const uint4*>(wbox + sw128_off(row, 4 * c + k));
     tmem_ld_wait();
     if (zero_grad) {
 #pragma unroll
@@ -559,12 +577,13 @@ __device__ __forceinline__ void epi_slice_fused_f8(uint32_t taddr, bool zero_gra
 #pragma unroll
     for (int p16 = 0; p16 < 2; ++p16) {
       const int chunk = 4 * h + 2 * c + p16;     // 16 codes of m and of r
-      uint4 mq = *reinterpret_cast<const uint4*>(mbox + sw128_off(row, chunk));
-      uint4 rq = *reinterpret_cast<const uint4*>(vbox + sw128_off(row, chunk));
-      uint4 wq[2];
+      if (p16 == 1) {
+        mq = *reinterpret_cast<const uint4*>(mbox + sw128_off(row, chunk));
+        rq = *reinterpret_cast<const uint4*>(vbox + sw128_off(row, chunk));
 #pragma unroll
-      for (int k = 0; k < 2; ++k)
-        wq[k] = *reinterpret_cast<const uint4*>(wbox + sw128_off(row, 4 * c + 2 * p16 + k));
+        for (int k = 0; k < 2; ++k)
+          wq[k] = *reinterpret_cast<const uint4*>(wbox + sw128_off(row, 4 * c + 2 + k));
+      }
       const uint32_t* wu = reinterpret_cast<const uint32_t*>(wq);
       float g[16], w[16];
 #pragma unroll
@@ -669,15 +688,18 @@ __device__ __forceinline__ void epi_slice_opt(uint32_t taddr, bool zero_grad, ui
   constexpr int kMBytes = RPS * 32 * (FMT == kFmtF32 ? 4 : 2);
   constexpr int NST = opt_states(OPT);
   uint32_t graw[16];
-  tmem_ld_x16(taddr, graw);
-  tmem_ld_wait();
+  tmem_ld_x16(taddr, graw);   // in flight while the slot's state is read
   float w[16], s1[16], s2[16];
   state_ld16<kFmtBF16>(slot, row, h, w);
   if constexpr (NST >= 1) state_ld16<FMT>(slot + kWBytes, row, h, s1);
   if constexpr (NST >= 2) state_ld16<FMT>(slot + kWBytes + kMBytes, row, h, s2);
+  tmem_ld_wait();
+  if (zero_grad) {
 #pragma unroll
-  for (int i = 0; i < 16; ++i)
-    opt_elem<OPT>(zero_grad ? 0.0f : __uint_as_float(graw[i]), w[i], s1[i], s2[i], oc);
+    for (int i = 0; i < 16; ++i) graw[i] = 0u;
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) opt_elem<OPT>(__uint_as_float(graw[i]), w[i], s1[i], s2[i], oc);
   state_st16<kFmtBF16>(slot, row, h, w);
   if constexpr (NST >= 1) state_st16<FMT>(slot + kWBytes, row, h, s1);
   if constexpr (NST >= 2) state_st16<FMT>(slot + kWBytes + kMBytes, row, h, s2);
@@ -721,13 +743,17 @@ __device__ __forceinline__ void epi_slice_opt_any(const OptConsts& oc, uint32_t 
 __device__ __forceinline__ void epi_slice_accum(uint32_t taddr, bool zero_grad, uint8_t* slot,
                                                 uint32_t row, int h, float beta, bool load) {
   uint32_t graw[16];
-  tmem_ld_x16(taddr, graw);
-  tmem_ld_wait();
+  tmem_ld_x16(taddr, graw);   // in flight while B is read
   float b[16], o[16];
   if (load) state_ld16<kFmtF32>(slot, row, h, b);
+  tmem_ld_wait();
+  if (zero_grad) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) graw[i] = 0u;
+  }
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const float g = zero_grad ? 0.0f : __uint_as_float(graw[i]);
+    const float g = __uint_as_float(graw[i]);
     o[i] = load ? __fmaf_rn(beta, b[i], g) : g;
   }
   state_st16<kFmtF32>(slot, row, h, o);

@@ -248,7 +248,8 @@ typedef enum {
 typedef struct {
   float lr, weight_decay;   /* all; >= 0 and finite                                 */
   float beta1, beta2;       /* LION, NADAM, RADAM; in [0, 1)                        */
-  float eps;                /* ADAGRAD, RMSPROP, NADAM, RADAM; >= 0 and finite      */
+  float eps;                /* ADAGRAD, RMSPROP, NADAM, RADAM: 0, or a normal fp32
+                               number at most 2^64 (FORGE_ERR_HYPER otherwise)    */
   float momentum;           /* SGD_MOMENTUM; in [0, 1)                              */
   float alpha;              /* RMSPROP; in [0, 1)                                   */
   float momentum_decay;     /* NADAM (torch's psi, 0.004 by default); >= 0, finite  */

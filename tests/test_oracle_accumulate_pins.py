@@ -2,7 +2,10 @@
 other than itself: beta = 0 as the plain gradient (with the buffer's old
 contents ignored), exactness of integer micro-batches against the whole
 batch, closed forms of Muon's momentum accumulate on one-hot inputs, and the
-one rounding per call."""
+one rounding per call.  The final micro-batch's fused step
+(``step_accumulated``) is pinned to AdamW's first-step sign closed form with
+an accumulator that flips the last micro-batch's signs, and to ``step`` when
+the accumulator is zero and the gradient exact in fp32."""
 import numpy as np
 import pytest
 
@@ -67,3 +70,65 @@ def test_no_tokens_scales_the_buffer_and_rounds_once():
     got2, exact2 = O.accumulate(xb, db, B, 0.95, return_f64=True)
     np.testing.assert_array_equal(got2, O.f64_to_f32(exact2))
     np.testing.assert_array_equal(exact2, b * B.astype(np.float64) + O.wgrad(xb, db))
+
+
+def test_final_step_moves_each_weight_against_the_sign_of_the_whole_sum():
+    # step 1 from zero moments, no decay, eps far below |g|: every weight
+    # moves by exactly lr against the sign of g = B + G_k (Algorithm 1 at t = 1:
+    # m-hat = g, v-hat = g^2).  B = -2 G_k (exact: G_k is an integer) flips
+    # every sign of the last micro-batch's gradient, so a step that read G_k
+    # alone, or B alone with the wrong sign, moves the other way.
+    rng = np.random.default_rng(7)
+    x = _ints(rng, (16, 12))
+    dy = _ints(rng, (16, 10))
+    Gk = O.bf16_to_f64(dy).T @ O.bf16_to_f64(x)
+    # where G_k = 0 the accumulator alone sets the sign (+1)
+    B = np.where(Gk == 0, 1.0, -2.0 * Gk).astype(np.float32)
+    w = O.f64_to_bf16(rng.normal(0, 1, (10, 12)))
+    h = O.Hyper(lr=2.0 ** -6, beta1=0.9, beta2=0.999, eps=1e-20, wd=0.0)
+    z = O.zero_moment(O.FMT_FP32, 10, 12)
+    w1, m1, v1 = O.step_accumulated(x, dy, w, z, z, B, h, 1)
+    g = B.astype(np.float64) + Gk
+    want = O.f64_to_bf16(O.bf16_to_f64(w) - h.lr * np.sign(g))
+    np.testing.assert_array_equal(w1, want)
+    b1 = h.as_f64()[1]   # beta1 as the fp32 value received
+    np.testing.assert_array_equal(m1.data.astype(np.float64),
+                                  O.f64_to_f32((1.0 - b1) * g).astype(np.float64))
+
+
+def test_final_step_with_a_zero_accumulator_is_the_plain_step():
+    # integer inputs: G is exact in fp32, so adding a zero accumulator and
+    # rounding to fp32 leaves the gradient the plain step reads
+    rng = np.random.default_rng(8)
+    x = _ints(rng, (24, 16))
+    dy = _ints(rng, (24, 8))
+    w = O.f64_to_bf16(rng.normal(0, 0.02, (8, 16)))
+    h = O.Hyper(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.01)
+    for fmt in (O.FMT_FP32, O.FMT_BF16, O.FMT_INT8):
+        cols = 128 if fmt == O.FMT_INT8 else 16
+        xx = x if cols == 16 else _ints(rng, (24, cols))
+        ww = w if cols == 16 else O.f64_to_bf16(rng.normal(0, 0.02, (8, cols)))
+        m = O.encode_moment(fmt, rng.normal(0, 1e-3, (8, cols)), False)
+        v = O.encode_moment(fmt, rng.normal(0, 1e-3, (8, cols)) ** 2, True)
+        got = O.step_accumulated(xx, dy, ww, m, v, np.zeros((8, cols), np.float32), h, 3)
+        want = O.step(xx, dy, ww, m, v, h, 3)
+        np.testing.assert_array_equal(got[0], want[0])
+        np.testing.assert_array_equal(got[1].data, want[1].data)
+        np.testing.assert_array_equal(got[2].data, want[2].data)
+
+
+def test_final_step_reads_the_gradient_rounded_to_fp32():
+    # B = 1 and G_k = 2^-30 (one token, X = dY = 2^-15): B + G_k rounds to 1.0
+    # in fp32, so with beta1 = 1/2 and m = -1 the new first moment is exactly
+    # 0.5 (-1) + 0.5 (1) = 0; a step that read the unrounded sum would keep
+    # 2^-31 of it (R16, R28: one rounding to fp32 before the optimizer)
+    x = O.f64_to_bf16(np.full((1, 1), 2.0 ** -15))
+    dy = O.f64_to_bf16(np.full((1, 1), 2.0 ** -15))
+    B = np.ones((1, 1), np.float32)
+    m = O.Moment(O.FMT_FP32, np.full((1, 1), -1.0, np.float32), None)
+    v = O.Moment(O.FMT_FP32, np.ones((1, 1), np.float32), None)
+    h = O.Hyper(lr=1e-3, beta1=0.5, beta2=0.5, eps=1e-8, wd=0.0)
+    w = O.f64_to_bf16(np.zeros((1, 1)))
+    _, m1, v1 = O.step_accumulated(x, dy, w, m, v, B, h, 2)
+    assert m1.data[0, 0] == 0.0
+    assert v1.data[0, 0] == 1.0      # 0.5 * 1 + 0.5 * 1^2

@@ -298,6 +298,42 @@ def test_accumulate_pins_pass_on_the_unmodified_oracle():
     assert not _fails_one(ACC_PINS)
 
 
+FINAL_PINS = [PA.test_final_step_moves_each_weight_against_the_sign_of_the_whole_sum,
+              PA.test_final_step_with_a_zero_accumulator_is_the_plain_step,
+              PA.test_final_step_reads_the_gradient_rounded_to_fp32]
+
+
+def _final_variant(kind):
+    def f(x_bits, dy_bits, w_bits, m, v, B, hyper, t, rows=None, return_f64=False):
+        if kind == "accumulator_ignored":
+            return F.step(x_bits, dy_bits, w_bits, m, v, hyper, t, rows, return_f64=return_f64)
+        G = F.wgrad(x_bits, dy_bits, rows)
+        Bf = np.asarray(B, dtype=np.float64)
+        g = Bf - G if kind == "accumulator_subtracted" else Bf + G
+        if kind != "not_rounded_to_fp32":
+            g = F.f64_to_f32(g).astype(np.float64)
+        W = F.bf16_to_f64(w_bits)
+        W1, m1, v1 = F.adamw_f64(g, W, F.decode_moment(m, False), F.decode_moment(v, True),
+                                 hyper, t)
+        out = (F.f64_to_bf16(W1), F.encode_moment(m.fmt, m1, False),
+               F.encode_moment(v.fmt, v1, True))
+        return out + ((g, W1, m1, v1),) if return_f64 else out
+    return f
+
+
+@pytest.mark.parametrize("kind", ["accumulator_ignored", "accumulator_subtracted",
+                                  "not_rounded_to_fp32"])
+def test_final_step_mistakes_are_caught(monkeypatch, kind):
+    f = _final_variant(kind)
+    monkeypatch.setattr(A, "step_accumulated", f)
+    monkeypatch.setattr(O, "step_accumulated", f)
+    assert _fails_one(FINAL_PINS)
+
+
+def test_final_step_pins_pass_on_the_unmodified_oracle():
+    assert not _fails_one(FINAL_PINS)
+
+
 # ---------------------------------------------------------------------------
 # stochastic-rounding store (oracle/sr.py)
 # ---------------------------------------------------------------------------

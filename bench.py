@@ -454,6 +454,25 @@ def run_gpu(args, rank, world, dev):
     def accumulate_all(beta):
         F.wgrad_accumulate_grouped(acc_items, beta)
     acc_ms = {b: per_step_ms(lambda b=b: accumulate_all(b)) for b in (1.0, 0.0)}
+    # the step at the final micro-batch: AdamW on fp32(B + G) in one grouped
+    # launch, against the last accumulate followed by forge_adamw on B
+    if fmt in (F.MOM_FP32, F.MOM_BF16):
+        final_layers = [dict(g, B=a["B"]) for g, a in zip(layer.group, acc_items)]
+
+        def final_all():
+            nonlocal step
+            step += 1
+            F.wgrad_adamw_acc_grouped(final_layers, step=step, **HYPER)
+
+        def final_unfused():
+            nonlocal step
+            step += 1
+            F.wgrad_accumulate_grouped(acc_items, 1.0)
+            for g, a in zip(layer.group, acc_items):
+                F.adamw(a["B"], g["W"], g["m"], g["v"], step=step, **HYPER)
+        acc_ms["final"] = per_step_ms(final_all)
+        acc_ms["final_unfused"] = per_step_ms(final_unfused)
+        del final_layers
     assert F.device_error() == 0
     del acc_items
 
@@ -1131,6 +1150,16 @@ def accumulate_block(acc_ms, layer, peaks):
         nbytes = layer.params() * per + layer.h2d_bytes()
         gbs = nbytes / (ms * 1e-3) / 1e9
         out[f"beta_{int(beta)}"] = {"ms_per_step": ms, "gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"]}
+    if "final" in acc_ms:
+        # the final micro-batch's step: the state stream plus B read (4 bytes)
+        ms = acc_ms["final"]
+        nbytes = layer.params() * (STATE_BYTES[layer.fmt] + 4) + layer.h2d_bytes()
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out["final_step"] = {
+            "launch": "forge_wgrad_adamw_acc_grouped: AdamW on fp32(B + dY^T X), one launch",
+            "ms_per_step": ms, "gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
+            "accumulate_then_adamw_ms": acc_ms["final_unfused"],
+            "speedup": acc_ms["final_unfused"] / ms}
     return out
 
 

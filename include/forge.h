@@ -329,6 +329,33 @@ forge_status forge_wgrad_accumulate_grouped(const forge_accum_item* items, int n
                                             float beta, forge_stream stream);
 
 /*
+ * forge_wgrad_adamw_acc: the step at the final micro-batch of the
+ * exact-accumulation mode (the FORGE page, Appendix N.5) in one launch.  The
+ * gradient the AdamW step reads is fp32(B + dY^T X): B holds the earlier
+ * micro-batches' sum (forge_wgrad_accumulate), the last micro-batch's tile is
+ * added to it on chip, and W, m, v are updated as forge_wgrad_adamw updates
+ * them.  The result equals forge_wgrad_accumulate(beta = 1) followed by
+ * forge_adamw on B, bit for bit, without writing B back or reading it twice.
+ *   Arguments as forge_wgrad_adamw; B [d_out, d_in] fp32, 16-byte aligned,
+ *   read only (the caller clears or reuses it for the next step).
+ *   fmt: FORGE_MOM_FP32 or FORGE_MOM_BF16.
+ * Errors: as forge_wgrad_adamw; FORGE_ERR_FORMAT for other moment formats;
+ * FORGE_ERR_ALIAS if B overlaps W, m or v.  bt = 0 steps on B alone.
+ * Asynchronous on `stream`.
+ */
+forge_status forge_wgrad_adamw_acc(const void* X, const void* dY, void* W, forge_moment m,
+                                   forge_moment v, const float* B, int64_t bt, int64_t d_in,
+                                   int64_t d_out, float lr, float beta1, float beta2, float eps,
+                                   float weight_decay, int64_t step, forge_moment_fmt fmt,
+                                   forge_stream stream);
+/* forge_wgrad_adamw_acc on n (1..FORGE_MAX_GROUP) layers in one launch;
+ * B[i] is layer i's accumulator.  No B may overlap any layer's W, m or v. */
+forge_status forge_wgrad_adamw_acc_grouped(const forge_linear* layers, const float* const* B,
+                                           int n, int64_t bt, float lr, float beta1, float beta2,
+                                           float eps, float weight_decay, int64_t step,
+                                           forge_moment_fmt fmt, forge_stream stream);
+
+/*
  * forge_wgrad: the unfused gradient, dW = dY^T X stored to global memory
  * (the "store-G control" of the FORGE page's Appendix D).  It runs the same
  * tensor-core main loop as forge_wgrad_adamw, so with dw_dtype = FORGE_DT_FP32

@@ -141,7 +141,9 @@ def check_step(gpu_w_bits, gpu_m, gpu_v, ref_inputs, hyper, t, fmt, bt, label=""
     gpu_m / gpu_v: Moment objects holding the GPU's stored moments (same rows).
     Raises AssertionError with a report when a bound is broken."""
     G, S = ref_inputs["G"], ref_inputs["S"]
-    tau = tau_bound(S, bt)
+    # a caller whose gradient is not the plain dY^T X (the final micro-batch's
+    # fp32(B + G), R28) passes the bound of that gradient instead
+    tau = ref_inputs["tau"] if "tau" in ref_inputs else tau_bound(S, bt)
     W = O.bf16_to_f64(ref_inputs["W_bits"])
     m0 = O.decode_moment(ref_inputs["m"], False)
     v0 = O.decode_moment(ref_inputs["v"], True)

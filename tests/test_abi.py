@@ -23,7 +23,8 @@ def test_header_declares_the_boundary():
               "forge_status_string", "forge_wgrad_adamw_grouped", "forge_dgrad",
               "forge_linear_backward", "forge_describe_dgrad_config", "forge_dgrad_noalloc",
               "forge_wgrad_opt", "forge_wgrad_accumulate", "forge_wgrad_adamw_sr",
-              "forge_fp8_roll_scales", "forge_set_tuning", "forge_get_tuning"):
+              "forge_fp8_roll_scales", "forge_set_tuning", "forge_get_tuning",
+              "forge_wgrad_adamw_acc", "forge_wgrad_adamw_acc_grouped"):
         assert n in names
 
 
@@ -386,3 +387,25 @@ def test_grouped_calls_argument_errors(L):
                                            None, 0, None) == 1
     assert L.forge_linear_backward_grouped(arr, dx, 1, 64, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 0,
                                            None, 0, None) == 6             # dX over X
+
+
+def final_step(L, X=A, dY=B, W=C, m=(D, None), v=(D + (1 << 36), None), Bacc=(1 << 40),
+               bt=64, d_in=256, d_out=128, eps=1e-8, fmt=0):
+    return L.forge_wgrad_adamw_acc(X, dY, W, F.ForgeMoment(*m), F.ForgeMoment(*v), Bacc, bt,
+                                   d_in, d_out, 1e-3, 0.9, 0.999, eps, 0.01, 1, fmt, None)
+
+
+def test_final_micro_batch_step_argument_errors(L):
+    # codes: 1 NULL, 2 ALIGN, 3 SHAPE, 4 FORMAT, 5 HYPER, 6 ALIAS; 10 = valid
+    # arguments that reached the device query (no GPU here)
+    assert final_step(L) == 10
+    assert final_step(L, fmt=1) == 10                     # bf16 moments
+    assert final_step(L, Bacc=None) == 1
+    assert final_step(L, Bacc=(1 << 40) + 4) == 2
+    assert final_step(L, d_in=260) == 3
+    assert final_step(L, fmt=2, m=(D, A), v=(D + (1 << 36), B)) == 4   # int8: not this step
+    assert final_step(L, fmt=3) == 4
+    assert final_step(L, eps=1e-40) == 5
+    assert final_step(L, Bacc=C + 64) == 6                # the accumulator inside W
+    assert final_step(L, Bacc=D + 64) == 6                # ... inside m
+    assert final_step(L, Bacc=B) == 10                    # over dY: both are read only

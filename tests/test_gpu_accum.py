@@ -5,7 +5,12 @@ The GPU adds its fp32 accumulator G~ (within tau of the exact G, the bound of
 ``tests/parity.py``) to beta B with one fused multiply-add, so B' must lie in
 the fp32 range the oracle gives over [G - tau, G + tau], widened by one fp32
 unit; with integer inputs every step is exact and the results equal the
-oracle bit for bit."""
+oracle bit for bit.
+
+The step at the final micro-batch (forge_wgrad_adamw_acc, reading R28)
+reads fp32(B + G): against the oracle through the parity checker with the
+bound of that sum, and bit for bit against forge_wgrad_accumulate then
+forge_adamw."""
 import math
 
 import numpy as np
@@ -16,8 +21,8 @@ import oracle as O
 from weight_gradient_gemm_gb300 import forge as F
 from weight_gradient_gemm_gb300.inputs import bf16_bits, make_step_inputs
 
-from .gpu_util import DEV, require_gpu
-from .parity import tau_bound
+from .gpu_util import (DEV, dev_state, hyper_kwargs, mom_from_dev, require_gpu, same_moment)
+from .parity import check_step, tau_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -152,3 +157,120 @@ def test_exact_accumulation_then_one_step_matches_the_whole_batch():
     check_step(bf16_bits(W.cpu()), O.Moment(O.FMT_FP32, m.cpu().numpy()),
                O.Moment(O.FMT_FP32, v.cpu().numpy()), ref, O.Hyper(), 1, O.FMT_FP32, bt,
                label="micro-batches")
+
+
+# ---------------------------------------------------------------------------
+# the step at the final micro-batch (forge_wgrad_adamw_acc): AdamW on
+# fp32(B + dY^T X), reading R28
+# ---------------------------------------------------------------------------
+
+HYPER = O.Hyper(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.01)
+
+
+def _final_case(seed, bt, d_in, d_out, fmt):
+    """Inputs of the last micro-batch, the accumulator of three earlier ones
+    (formed by the oracle's accumulate), and a warmed state."""
+    x, dy = _case(seed, bt, d_in, d_out)
+    B = np.zeros((d_out, d_in), np.float32)
+    for i in range(3):
+        px, pdy = _case(seed + 10 + i, 256, d_in, d_out)
+        B = O.accumulate(bf16_bits(px), bf16_bits(pdy), B, 0.0 if i == 0 else 1.0)
+    rng = np.random.default_rng(seed)
+    w = O.f64_to_bf16(rng.normal(0, 0.02, (d_out, d_in)))
+    m = O.encode_moment(fmt, rng.normal(0, 1e-3, (d_out, d_in)), False)
+    v = O.encode_moment(fmt, rng.normal(0, 1e-3, (d_out, d_in)) ** 2, True)
+    return x, dy, B, w, m, v
+
+
+def _final_ref(x, dy, B, w, m, v):
+    """The parity checker's inputs for the final step: the gradient the step
+    reads is fp32(B + G); the GPU's differs from it by the accumulator's
+    bound tau plus the roundings of the two fp32 sums (one fp32 unit of
+    |B| + |G| + tau, taken as 2^-22 of it)."""
+    xb, db = bf16_bits(x), bf16_bits(dy)
+    G = O.wgrad(xb, db)
+    S = O.wgrad_abs(xb, db)
+    tau = tau_bound(S, max(x.shape[0], 1))
+    g = O.f64_to_f32(B.astype(np.float64) + G).astype(np.float64)
+    tau_g = tau + 2.0 ** -22 * (np.abs(B.astype(np.float64)) + np.abs(G) + tau)
+    return dict(G=g, S=S, tau=tau_g, W_bits=w, m=m, v=v)
+
+
+def _gpu_final(x, dy, B, w, m, v, t):
+    W, md, vd, _, _ = dev_state(w, m, v)
+    Bd = torch.from_numpy(B.copy()).to(DEV)
+    F.wgrad_adamw_acc(x.to(DEV), dy.to(DEV), W, md, vd, Bd, step=t, **hyper_kwargs(HYPER))
+    assert F.device_error() == 0
+    assert torch.equal(Bd.cpu(), torch.from_numpy(B))   # the accumulator is read only
+    return bf16_bits(W.cpu()), mom_from_dev(m.fmt, md, None), mom_from_dev(v.fmt, vd, None)
+
+
+@pytest.mark.parametrize("fmt", [O.FMT_FP32, O.FMT_BF16])
+@pytest.mark.parametrize("bt,d_in,d_out", [(192, 384, 256), (1000, 264, 392), (0, 256, 136)])
+def test_final_step_against_oracle(bt, d_in, d_out, fmt, acc_cfg):
+    x, dy, B, w, m, v = _final_case(20, bt, d_in, d_out, fmt)
+    gw, gm, gv = _gpu_final(x, dy, B, w, m, v, 5)
+    rep = check_step(gw, gm, gv, _final_ref(x, dy, B, w, m, v), HYPER, 5, fmt, max(bt, 1),
+                     label=f"final bt={bt} fmt={fmt}")
+    print(rep)
+    # the oracle's own function gives the checker's reference W on almost
+    # every entry (the rest sit at a rounding boundary of the checked range)
+    ow, _, _ = O.step_accumulated(bf16_bits(x), bf16_bits(dy), w, m, v, B, HYPER, 5)
+    assert np.mean(ow == gw) > 0.99
+
+
+@pytest.mark.parametrize("fmt", [O.FMT_FP32, O.FMT_BF16])
+def test_final_step_equals_accumulate_then_adamw(fmt, acc_cfg):
+    # bit for bit: the epilogue's fp32 sum is the accumulate mode's, and the
+    # AdamW arithmetic is forge_adamw's
+    x, dy, B, w, m, v = _final_case(30, 700, 512, 384, fmt)
+    gw, gm, gv = _gpu_final(x, dy, B, w, m, v, 3)
+    W, md, vd, _, _ = dev_state(w, m, v)
+    Bd = torch.from_numpy(B.copy()).to(DEV)
+    F.wgrad_accumulate(x.to(DEV), dy.to(DEV), Bd, 1.0)
+    F.adamw(Bd, W, md, vd, step=3, **hyper_kwargs(HYPER))
+    assert F.device_error() == 0
+    assert np.array_equal(gw, bf16_bits(W.cpu()))
+    assert same_moment(gm, mom_from_dev(fmt, md, None))
+    assert same_moment(gv, mom_from_dev(fmt, vd, None))
+
+
+def test_final_step_grouped_equals_separate_calls():
+    # three layers of different shapes in one launch against one call each
+    shapes = [(384, 256), (512, 128), (256, 384)]
+    cases = [_final_case(40 + i, 320, d_in, d_out, O.FMT_BF16) for i, (d_in, d_out) in
+             enumerate(shapes)]
+    sep = [_gpu_final(*c, 2) for c in cases]
+    layers = []
+    for x, dy, B, w, m, v in cases:
+        W, md, vd, _, _ = dev_state(w, m, v)
+        layers.append(dict(X=x.to(DEV), dY=dy.to(DEV), W=W, m=md, v=vd,
+                           B=torch.from_numpy(B.copy()).to(DEV)))
+    F.wgrad_adamw_acc_grouped(layers, step=2, **hyper_kwargs(HYPER))
+    assert F.device_error() == 0
+    for ly, (gw, gm, gv) in zip(layers, sep):
+        assert np.array_equal(bf16_bits(ly["W"].cpu()), gw)
+        assert same_moment(mom_from_dev(O.FMT_BF16, ly["m"], None), gm)
+        assert same_moment(mom_from_dev(O.FMT_BF16, ly["v"], None), gv)
+
+
+def test_final_step_on_llama_gate_at_512_tokens():
+    # the gate projection (14336 x 4096) at 512 tokens, fp32 moments: whole
+    # tensors against accumulate + adamw, bit for bit
+    d_out, d_in, bt = 14336, 4096, 512
+    g = torch.Generator(device=DEV)
+    g.manual_seed(9)
+    X = torch.randn((bt, d_in), generator=g, device=DEV).to(torch.bfloat16)
+    dY = (torch.randn((bt, d_out), generator=g, device=DEV) * 1e-3).to(torch.bfloat16)
+    W = (torch.randn((d_out, d_in), generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    Bacc = torch.randn((d_out, d_in), generator=g, device=DEV) * 1e-2
+    m = torch.randn((d_out, d_in), generator=g, device=DEV) * 1e-4
+    v = (torch.randn((d_out, d_in), generator=g, device=DEV) * 1e-4) ** 2
+    c = [t.clone() for t in (W, m, v, Bacc)]
+    F.wgrad_adamw_acc(X, dY, W, m, v, Bacc, step=7, **hyper_kwargs(HYPER))
+    F.wgrad_accumulate(X, dY, c[3], 1.0)
+    F.adamw(c[3], c[0], c[1], c[2], step=7, **hyper_kwargs(HYPER))
+    assert F.device_error() == 0
+    assert torch.equal(W.view(torch.int16), c[0].view(torch.int16))
+    assert torch.equal(m.view(torch.int32), c[1].view(torch.int32))
+    assert torch.equal(v.view(torch.int32), c[2].view(torch.int32))

@@ -38,6 +38,8 @@ cudaError_t launch_gemm_opt_bf16(const GemmConfig&, const GemmArgs&, cudaStream_
 cudaError_t launch_gemm_opt_none(const GemmConfig&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_opt_f32s1(const GemmConfig&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_opt_bf16s1(const GemmConfig&, const GemmArgs&, cudaStream_t);
+cudaError_t launch_gemm_fused_f32a(const GemmConfig&, const GemmArgs&, cudaStream_t);
+cudaError_t launch_gemm_fused_bf16a(const GemmConfig&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_accum(const GemmConfig&, const GemmArgs&, cudaStream_t);
 
 cudaError_t launch_gemm(int mode, int fmt, const GemmConfig& cfg, const GemmArgs& args,
@@ -48,6 +50,8 @@ cudaError_t launch_gemm(int mode, int fmt, const GemmConfig& cfg, const GemmArgs
       case kFmtBF16: return launch_gemm_fused_bf16(cfg, args, stream);
       case kFmtI8: return launch_gemm_fused_i8(cfg, args, stream);
       case kFmtF8: return launch_gemm_fused_f8(cfg, args, stream);
+      case kFmtF32A: return launch_gemm_fused_f32a(cfg, args, stream);
+      case kFmtBF16A: return launch_gemm_fused_bf16a(cfg, args, stream);
     }
   } else if (mode == kModeStoreG) {
     switch (fmt) {
@@ -412,6 +416,13 @@ GemmConfig choose_config(int64_t bt, int fmt, int mode) {
     c.prof = bt <= 1536 ? kProfBalanced : (bt <= 3072 ? kProfMma : kProfDeep);
   }
   return finish_config(c, bt, fmt, mode);
+}
+
+// The fused step at the final micro-batch (an fp32 addend in every slot):
+// the fused choice for the moment format; its slots are larger by the
+// addend's fp32 box.
+GemmConfig choose_acc_step_config(int64_t bt, int fmt) {
+  return choose_config(bt, fmt, kModeFused);
 }
 
 // forge_wgrad_opt: the fused tile choice with two changes, from sweeps over
@@ -784,6 +795,87 @@ forge_status forge_wgrad_adamw_grouped(const forge_linear* layers, int n, int64_
   args.p.drop_first_arrival = take_drop_flag();
   return launch_gemm(kModeFused, ifmt, cfg, args, st) == cudaSuccess ? FORGE_OK
                                                                       : FORGE_ERR_LAUNCH;
+}
+
+forge_status forge_wgrad_adamw_acc_grouped(const forge_linear* layers, const float* const* B,
+                                           int n, int64_t bt, float lr, float beta1, float beta2,
+                                           float eps, float weight_decay, int64_t step,
+                                           forge_moment_fmt fmt, forge_stream stream) {
+  if (!layers || !B) return FORGE_ERR_NULL;
+  if (n < 1 || n > FORGE_MAX_GROUP) return FORGE_ERR_SHAPE;
+  if (fmt != FORGE_MOM_FP32 && fmt != FORGE_MOM_BF16) return FORGE_ERR_FORMAT;
+  for (int i = 0; i < n; ++i) {
+    forge_status s = check_linear(layers[i], bt, fmt);
+    if (s != FORGE_OK) return s;
+    if (!B[i]) return FORGE_ERR_NULL;
+    if (!aligned16(B[i])) return FORGE_ERR_ALIGN;
+  }
+  forge_status s = check_hyper(lr, beta1, beta2, eps, weight_decay, step);
+  if (s != FORGE_OK) return s;
+  for (int i = 0; i < n; ++i)
+    for (int j = 0; j < n; ++j) {
+      if (layers_clash(layers[i], layers[j], bt, fmt, i == j)) return FORGE_ERR_ALIAS;
+      // the accumulators are read while the states are written
+      const forge_linear& L = layers[j];
+      const uint64_t nb = 4ull * layers[i].d_in * layers[i].d_out;
+      if (input_overlaps_state(B[i], nb, L.W, L.m, L.v, L.d_in, L.d_out, fmt))
+        return FORGE_ERR_ALIAS;
+    }
+  DeviceInfo* d = nullptr;
+  s = device_info(&d);
+  if (s != FORGE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const AdamWConsts h = make_consts(lr, beta1, beta2, eps, weight_decay, step);
+  if (bt == 0) {   // G = 0: the step reads the accumulator alone, as forge_adamw does
+    for (int i = 0; i < n; ++i) {
+      const forge_linear& L = layers[i];
+      if (launch_adamw(B[i], 0, L.W, L.m.data, L.v.data, nullptr, nullptr, L.d_in, L.d_out,
+                       static_cast<int>(fmt), h, d->num_sms, st) != cudaSuccess)
+        return FORGE_ERR_LAUNCH;
+    }
+    return FORGE_OK;
+  }
+  const int afmt = (fmt == FORGE_MOM_FP32) ? kFmtF32A : kFmtBF16A;
+  GemmConfig cfg = choose_acc_step_config(bt, static_cast<int>(fmt));
+  int order[FORGE_MAX_GROUP];
+  largest_first(layers, n, fmt, order);
+  GemmArgs args;
+  std::memset(&args, 0, sizeof(args));
+  args.p = base_params(bt, cfg, *d);
+  args.p.h = h;
+  const uint32_t rows = static_cast<uint32_t>(slot_rows(kModeFused, afmt, cfg.prof));
+  for (int k = 0; k < n; ++k) {
+    const forge_linear& L = layers[order[k]];
+    GemmMaps& maps = args.maps[k];
+    if (!operand_maps(maps, L.X, L.dY, bt, L.d_in, L.d_out, bk_of(cfg.cg)) ||
+        !state_maps(maps, L.W, L.m, L.v, L.d_in, L.d_out, fmt, cfg.prof) ||
+        !get_map(&maps.b, B[order[k]], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, L.d_in, L.d_out,
+                 L.d_in * 4, 32, rows, CU_TENSOR_MAP_SWIZZLE_128B))
+      return FORGE_ERR_LAUNCH;
+    add_problem(args.p, cfg, L.d_in, L.d_out, nullptr, nullptr);
+  }
+  set_grid(cfg, args.p.num_units, d->num_sms);
+  args.p.drop_first_arrival = take_drop_flag();
+  return launch_gemm(kModeFused, afmt, cfg, args, st) == cudaSuccess ? FORGE_OK
+                                                                     : FORGE_ERR_LAUNCH;
+}
+
+forge_status forge_wgrad_adamw_acc(const void* X, const void* dY, void* W, forge_moment m,
+                                   forge_moment v, const float* B, int64_t bt, int64_t d_in,
+                                   int64_t d_out, float lr, float beta1, float beta2, float eps,
+                                   float weight_decay, int64_t step, forge_moment_fmt fmt,
+                                   forge_stream stream) {
+  forge_linear L;
+  std::memset(&L, 0, sizeof(L));
+  L.X = X;
+  L.dY = dY;
+  L.W = W;
+  L.m = m;
+  L.v = v;
+  L.d_in = d_in;
+  L.d_out = d_out;
+  return forge_wgrad_adamw_acc_grouped(&L, &B, 1, bt, lr, beta1, beta2, eps, weight_decay, step,
+                                       fmt, stream);
 }
 
 forge_status forge_wgrad_adamw_sr_grouped(const forge_linear* layers, const uint64_t* seeds,

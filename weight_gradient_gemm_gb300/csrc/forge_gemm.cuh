@@ -77,7 +77,9 @@ struct GemmTraits {
   static constexpr bool F8 = (MODE == kModeFused && FMT == kFmtF8);
   static constexpr int W_BYTES = RPS * SW * W_ELEM;
   static constexpr int M_BYTES = RPS * SW * MOM_ELEM;
-  static constexpr int SLOT_BYTES = W_BYTES + state_boxes(FMT) * M_BYTES;
+  // the fused step with an addend: an fp32 box of the accumulator after m, v
+  static constexpr int ADD_BYTES = (MODE == kModeFused && has_addend(FMT)) ? RPS * SW * 4 : 0;
+  static constexpr int SLOT_BYTES = W_BYTES + state_boxes(FMT) * M_BYTES + ADD_BYTES;
   // every box of a slot starts 1024-byte aligned (the 128-byte swizzle's atom)
   static_assert(W_BYTES % 1024 == 0 && M_BYTES % 1024 == 0 && SLOT_BYTES % 1024 == 0,
                 "state boxes must stay 1024-byte aligned");
@@ -250,17 +252,63 @@ __device__ __forceinline__ int tile_coords(int t, const GemmParams& p, int& tm, 
 // TMEM lane) and HALF consecutive columns of the slice.
 // ---------------------------------------------------------------------------
 
+// The thread's 16 columns of one state box in the slot: fp32 boxes have
+// 128-byte rows (128-byte swizzle), bf16 boxes 64-byte rows (64-byte swizzle).
+template <int FMT>
+__device__ __forceinline__ void state_ld16(const uint8_t* box, uint32_t row, int h,
+                                           float (&x)[16]) {
+  if constexpr (FMT == kFmtF32) {
+    float4 q[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      q[c] = *reinterpret_cast<const float4*>(box + sw128_off(row, 4 * h + c));
+    const float* f = reinterpret_cast<const float*>(q);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = f[i];
+  } else {
+    uint4 q[2];
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+      q[c] = *reinterpret_cast<const uint4*>(box + sw64_off(row, 2 * h + c));
+    const uint32_t* u = reinterpret_cast<const uint32_t*>(q);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      x[2 * i] = bf16_lo(u[i]);
+      x[2 * i + 1] = bf16_hi(u[i]);
+    }
+  }
+}
+template <int FMT>
+__device__ __forceinline__ void state_st16(uint8_t* box, uint32_t row, int h,
+                                           const float (&x)[16]) {
+  if constexpr (FMT == kFmtF32) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      *reinterpret_cast<float4*>(box + sw128_off(row, 4 * h + c)) =
+          make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
+  } else {
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+      *reinterpret_cast<uint4*>(box + sw64_off(row, 2 * h + c)) =
+          make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+  }
+}
+
 // fp32 or bf16 moments; SW = 32, HALF = 16.
 // `row` is the thread's row inside the RPS-row slot (its TMEM lane is in
 // `taddr`); the slot holds the W, m and v boxes of RPS rows back to back.
 // With `sr` the weight is committed by stochastic rounding: the random bits
 // of the thread's 16 columns are the Philox block with counter (grow, gcol16,
 // sr_step, 0), grow the global weight row and gcol16 the first column / 16.
-template <int FMT, int RPS>
+template <int SLOT_FMT, int RPS>
 __device__ __forceinline__ void epi_slice_fused_16(uint32_t taddr, bool zero_grad, uint8_t* slot,
                                                    uint32_t row, int h, const AdamWConsts& hc,
                                                    bool sr, uint64_t sr_seed, uint32_t sr_step,
                                                    uint32_t grow, uint32_t gcol16) {
+  constexpr int FMT = state_elem_fmt(SLOT_FMT);   // fp32 or bf16 moments
   constexpr int kWBytes = RPS * 32 * 2;
   constexpr int kMBytes = RPS * 32 * (FMT == kFmtF32 ? 4 : 2);
   // the accumulator load runs while the slot's W, m and v are read from
@@ -307,6 +355,8 @@ __device__ __forceinline__ void epi_slice_fused_16(uint32_t taddr, bool zero_gra
       v[2 * i] = bf16_lo(vu[i]); v[2 * i + 1] = bf16_hi(vu[i]);
     }
   }
+  float b[16];   // the addend (accumulator of the earlier micro-batches)
+  if constexpr (has_addend(SLOT_FMT)) state_ld16<kFmtF32>(mbox + 2 * kMBytes, row, h, b);
   tmem_ld_wait();
   if (zero_grad) {   // warp-uniform: no accumulator was written
 #pragma unroll
@@ -314,6 +364,11 @@ __device__ __forceinline__ void epi_slice_fused_16(uint32_t taddr, bool zero_gra
   }
 #pragma unroll
   for (int i = 0; i < 16; ++i) g[i] = __uint_as_float(graw[i]);
+  if constexpr (has_addend(SLOT_FMT)) {
+    // the gradient the step reads: fp32(B + G), as the accumulate mode forms it
+#pragma unroll
+    for (int i = 0; i < 16; ++i) g[i] = __fadd_rn(b[i], g[i]);
+  }
 #pragma unroll
   for (int i = 0; i < 16; i += 2) {
     float2 w2 = make_float2(w[i], w[i + 1]), m2 = make_float2(m[i], m[i + 1]);
@@ -633,51 +688,6 @@ __device__ __forceinline__ void epi_slice_store(uint32_t taddr, bool zero_grad, 
   }
 }
 
-// The thread's 16 columns of one state box in the slot: fp32 boxes have
-// 128-byte rows (128-byte swizzle), bf16 boxes 64-byte rows (64-byte swizzle).
-template <int FMT>
-__device__ __forceinline__ void state_ld16(const uint8_t* box, uint32_t row, int h,
-                                           float (&x)[16]) {
-  if constexpr (FMT == kFmtF32) {
-    float4 q[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      q[c] = *reinterpret_cast<const float4*>(box + sw128_off(row, 4 * h + c));
-    const float* f = reinterpret_cast<const float*>(q);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = f[i];
-  } else {
-    uint4 q[2];
-#pragma unroll
-    for (int c = 0; c < 2; ++c)
-      q[c] = *reinterpret_cast<const uint4*>(box + sw64_off(row, 2 * h + c));
-    const uint32_t* u = reinterpret_cast<const uint32_t*>(q);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      x[2 * i] = bf16_lo(u[i]);
-      x[2 * i + 1] = bf16_hi(u[i]);
-    }
-  }
-}
-template <int FMT>
-__device__ __forceinline__ void state_st16(uint8_t* box, uint32_t row, int h,
-                                           const float (&x)[16]) {
-  if constexpr (FMT == kFmtF32) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      *reinterpret_cast<float4*>(box + sw128_off(row, 4 * h + c)) =
-          make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
-  } else {
-    uint32_t o[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) o[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
-#pragma unroll
-    for (int c = 0; c < 2; ++c)
-      *reinterpret_cast<uint4*>(box + sw64_off(row, 2 * h + c)) =
-          make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-  }
-}
-
 // The other optimizers (kModeOpt): the slice of epi_slice_fused_16 with
 // optimizer OPT's element update, touching only the states OPT has.
 template <int SLOT_FMT, int RPS, int OPT>
@@ -855,6 +865,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       tma_prefetch_desc(&a.maps[i].w);
       if (MODE == kModeFused || (MODE == kModeOpt && p.nstate >= 1)) tma_prefetch_desc(&a.maps[i].m);
       if (MODE == kModeFused || (MODE == kModeOpt && p.nstate >= 2)) tma_prefetch_desc(&a.maps[i].v);
+      if (T::ADD_BYTES) tma_prefetch_desc(&a.maps[i].b);
     }
   }
   // the peer's barriers must be initialised before any cross-CTA arrival
@@ -1049,7 +1060,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           const uint32_t slot = base + T::OFF_SLOTS + j * T::SLOT_BYTES;
           // kModeOpt loads only the states its optimizer has; kModeAccum only B
           const int nst = (MODE == kModeOpt) ? p.nstate : (MODE == kModeAccum ? 0 : 2);
-          mbar_arrive_expect_tx(bar_sfull(j), T::W_BYTES + nst * T::M_BYTES);
+          mbar_arrive_expect_tx(bar_sfull(j), T::W_BYTES + nst * T::M_BYTES + T::ADD_BYTES);
           if constexpr (T::Q8) {
             tma_load_2d(slot, &maps.w, x0, y0, bar_sfull(j), pol);
             tma_load_2d(slot + T::RPS * 64 * 2, &maps.w, x0 + 64, y0, bar_sfull(j), pol);
@@ -1062,6 +1073,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           if (nst >= 1) tma_load_2d(slot + T::W_BYTES, &maps.m, x0, y0, bar_sfull(j), mpol);
           if (nst >= 2)
             tma_load_2d(slot + T::W_BYTES + T::M_BYTES, &maps.v, x0, y0, bar_sfull(j), mpol);
+          if constexpr (T::ADD_BYTES > 0)   // the accumulator's box (read, never stored)
+            tma_load_2d(slot + T::W_BYTES + 2 * T::M_BYTES, &maps.b, x0, y0, bar_sfull(j), mpol);
         }
       }
       // let the loads of each slot's latest phase land before the CTA can exit

@@ -46,12 +46,20 @@ enum Prof : int { kProfStream = 0, kProfMma = 1, kProfBalanced = 2, kProfDeep = 
 // 128, fp8 e4m3 with per-tensor scales); store-G dW formats 0..1 (fp32, bf16);
 // kFmtNone: an optimizer without state (SGD), whose slots hold W alone;
 // kFmtF32S1, kFmtBF16S1: an optimizer with one state (fp32 or bf16), whose
-// slots hold W and that state only.
+// slots hold W and that state only.  kFmtF32A, kFmtBF16A: the fused AdamW
+// step with fp32 or bf16 moments whose gradient is G plus an fp32 addend
+// (the accumulator of the earlier micro-batches), which each slot holds as a
+// third fp32 box after m and v.
 enum Fmt : int { kFmtF32 = 0, kFmtBF16 = 1, kFmtI8 = 2, kFmtF8 = 3, kFmtNone = 4,
-                 kFmtF32S1 = 5, kFmtBF16S1 = 6 };
+                 kFmtF32S1 = 5, kFmtBF16S1 = 6, kFmtF32A = 7, kFmtBF16A = 8 };
 // The element format of an optimizer state format (fp32 or bf16).
 __host__ __device__ constexpr int state_elem_fmt(int fmt) {
-  return (fmt == kFmtF32S1) ? kFmtF32 : (fmt == kFmtBF16S1 ? kFmtBF16 : fmt);
+  return (fmt == kFmtF32S1 || fmt == kFmtF32A) ? kFmtF32
+         : (fmt == kFmtBF16S1 || fmt == kFmtBF16A) ? kFmtBF16 : fmt;
+}
+// Whether the format's slots carry an fp32 gradient addend.
+__host__ __device__ constexpr bool has_addend(int fmt) {
+  return fmt == kFmtF32A || fmt == kFmtBF16A;
 }
 // State boxes a slot holds.
 __host__ __device__ constexpr int state_boxes(int fmt) {
@@ -114,9 +122,10 @@ struct GemmParams {
 struct GemmMaps {
   CUtensorMap dy, x;      // operands
   CUtensorMap w, m, v;    // fused: state; store-G: w is dW
+  CUtensorMap b;          // fused with an addend: the fp32 accumulator
 };
 
-// Everything a launch reads from its parameter space (about 5.5 KB).
+// Everything a launch reads from its parameter space (about 6.5 KB).
 struct GemmArgs {
   GemmMaps maps[kMaxGroup];
   GemmParams p;

@@ -153,6 +153,13 @@ def lib() -> ctypes.CDLL:
                                                         ctypes.POINTER(vp), st, i64, f32, f32,
                                                         f32, f32, f32, i64, st, vp, sz, vp]
             L.forge_linear_backward_grouped.restype = st
+            L.forge_wgrad_adamw_acc.argtypes = [vp, vp, vp, ForgeMoment, ForgeMoment, vp, i64,
+                                                i64, i64, f32, f32, f32, f32, f32, i64, st, vp]
+            L.forge_wgrad_adamw_acc.restype = st
+            L.forge_wgrad_adamw_acc_grouped.argtypes = [ctypes.POINTER(ForgeLinear),
+                                                        ctypes.POINTER(vp), st, i64, f32, f32,
+                                                        f32, f32, f32, i64, st, vp]
+            L.forge_wgrad_adamw_acc_grouped.restype = st
             L.forge_fp8_roll_scales.argtypes = [vp, st, f32, vp]
             L.forge_fp8_roll_scales.restype = st
             L.forge_set_tuning.argtypes = [ctypes.POINTER(ForgeTuning)]
@@ -612,6 +619,41 @@ def _group_arr(layers, m_key="m", v_key="v", scales=True):
                              _moment(v, ly.get("v_scale") if scales else None) if v is not None
                              else ForgeMoment(None, None), d_in, d_out)
     return arr, n, bt
+
+
+def wgrad_adamw_acc(X: torch.Tensor, dY: torch.Tensor, W: torch.Tensor, m: torch.Tensor,
+                    v: torch.Tensor, B: torch.Tensor, *, lr: float, beta1: float, beta2: float,
+                    eps: float, weight_decay: float, step: int, stream=None) -> None:
+    """The step at the final micro-batch of the exact-accumulation mode: AdamW
+    on fp32(B + dY^T X), B being the fp32 accumulator of the earlier
+    micro-batches (read, not written); W, m, v updated in place; fp32 or bf16
+    moments."""
+    wgrad_adamw_acc_grouped([dict(X=X, dY=dY, W=W, m=m, v=v, B=B)], lr=lr, beta1=beta1,
+                            beta2=beta2, eps=eps, weight_decay=weight_decay, step=step,
+                            stream=stream)
+
+
+def wgrad_adamw_acc_grouped(layers, *, lr: float, beta1: float, beta2: float, eps: float,
+                            weight_decay: float, step: int, stream=None) -> None:
+    """wgrad_adamw_acc on several layers in one launch; each layer is a dict
+    with X, dY, W, m, v and its accumulator B (fp32 [d_out, d_in])."""
+    arr, n, bt = _group_arr(layers, scales=False)
+    fmt = None
+    bs = (ctypes.c_void_p * n)()
+    for i, ly in enumerate(layers):
+        d_out, d_in = ly["W"].shape
+        f = _moments(ly["m"], ly["v"], None, None, d_out, d_in)
+        if f not in (MOM_FP32, MOM_BF16):
+            raise ValueError("the final micro-batch's step takes fp32 or bf16 moments")
+        if fmt is not None and f != fmt:
+            raise ValueError("all layers of a group need the same moment format")
+        fmt = f
+        _want(ly["B"], "B", (d_out, d_in), (torch.float32,))
+        _on_device(B=ly["B"])
+        bs[i] = _ptr(ly["B"])
+    st = lib().forge_wgrad_adamw_acc_grouped(arr, bs, n, bt or 0, lr, beta1, beta2, eps,
+                                             weight_decay, step, fmt, _stream(stream))
+    _check(st, "forge_wgrad_adamw_acc_grouped")
 
 
 def wgrad_opt_grouped(layers, opt: int, *, lr: float, weight_decay: float, step: int,
